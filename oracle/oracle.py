@@ -1,0 +1,380 @@
+"""Oracle: a plain fp64 CPU restatement of batched draft-token verification.
+
+TEST INFRASTRUCTURE, NOT PART OF THE PRODUCT. Only the tests, the package-level
+smoke check and the benchmark's CPU-baseline / reference legs may import this
+module. The CUDA library never calls it, and the two share no code, header,
+table or helper; they meet only on the arrays of the seeded input generator.
+
+Everything is computed in float64 from the exact widening of the stored logits
+(bf16 bit patterns or fp32), one sequence at a time, in the order the pages give
+the steps. Library primitives (max, sum, exp, log, cumsum, argmax) are the only
+building blocks; there is no blocking, fusion or reordering beyond them.
+
+Sources (page title, then section):
+  [SpS] speculative-sampling article "大模型推理的投机采样：Draft 小模型辅助与验证加速",
+        section "核心算法数学原理：无损拒绝采样" -- alpha = min(1, p(x)/q(x)); a draft
+        token is accepted when a uniform r <= alpha; on rejection a new token is drawn
+        from max(0, p - q)/norm and drafting stops there; section "核心实现" -- the target
+        is evaluated on the last gamma+1 positions (one row per draft plus one more).
+  [CoD] "Chain of Draft" article, section 3.2 (compute_nkl) -- both rows are softmaxed
+        at one temperature, KL(draft || target) is summed over the vocabulary and
+        divided by log(vocab size); drafts with NKL below delta = 0.15 are kept.
+  [MTP] Gemma 4 multi-token-prediction drafter article, section 2.3 -- greedy
+        verification: d_i is accepted while it equals the argmax of target row i; at
+        the first mismatch r the target's own token replaces d_r; section 4.1 gives
+        the same loop as pseudo-code.
+  [PD]  Parallel Drafting article, section 2.2 -- the P-EAGLE draft tree (three root
+        candidates, at most 12 nodes), verified by the longest accepted path.
+
+Readings taken where the pages are silent, garbled or disagree:
+  R1  bonus token: when all gamma drafts are accepted, one more token is drawn from
+      target row gamma (the (gamma+1)-th row the pages slice out), by the same
+      inverse-CDF rule as the correction.
+  R2  correction on rejection follows [SpS]'s stated residual math, not the argmax
+      shortcut in the same page's sample code.
+  R3  no 1e-8 floor on q(x) (the sample code's max(1e-8, q)); q(x) > 0 for finite
+      logits. Rows with q(x) < 1e-8 are flagged.
+  R4  comparison: accept iff u <= alpha (u == alpha is accepted).
+  R5  "norm" is Z = sum_v max(0, p_v - q_v).
+  R6  if a rejection meets Z == 0 (only rounding can cause it), the correction is
+      drawn from p at that position; the row is flagged.
+  R7  inverse CDF in ascending token order with a strict ">": y = min{v : C(v) > u*Z},
+      so a zero-mass token is never drawn; if rounding leaves u*Z >= C(V-1) the last
+      token with positive mass is taken.
+  R8  one u_sample per sequence serves either the correction or the bonus token.
+  R9  one temperature T for target and draft ([CoD] 3.2: temperatures must match).
+  R10 greedy argmax on the raw logits (T does not matter), ties to the lowest index.
+  R11 NKL = KL(q || p) / ln V with q the draft distribution; natural log.
+  R12 NKL is reported as the raw ratio, unclamped (KL(q||p) can exceed ln V).
+  R13 accept mask = NKL < delta (strict).
+  R14 the exact KL is the definition; the page's epsilon-guarded form
+      sum q (log(q + 1e-12) - log(p + 1e-12)) is reported beside it.
+  R15 tree: node j is accepted iff its token equals the argmax of its parent's row
+      and its parent is accepted (roots compare against the parent row, row 0); the
+      pick is the accepted node of greatest depth, ties to the lowest node index;
+      the correction is the argmax of the picked node's row (row 0 if none).
+  R16 errors: a non-finite logit in any row a sequence uses, or a draft / node token
+      outside [0, V), makes that sequence an error: its count is -1 and all its
+      outputs are -1 (integers) or NaN (reals). For the standalone NKL call the
+      error is per row pair.
+
+Parity pins for every function: tests/test_oracle_pins.py.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+FLAG_BAND = 1e-5          # decisions closer than this to a boundary are flagged
+NKL_EPS = 1e-12           # the guard in [CoD]'s compute_nkl code
+
+ERR_TOKEN_RANGE = 1
+ERR_NONFINITE = 2
+ERR_OFFSETS = 4
+
+
+# ---------------------------------------------------------------------------
+# input widening (bit patterns -> exact float64)
+
+def widen(raw: np.ndarray, dtype: str) -> np.ndarray:
+    """Stored logits -> float64. bf16 is the high half of an IEEE fp32, so the
+    widening is exact: shift the 16 stored bits into the top of a 32-bit word."""
+    if dtype == "bf16":
+        return (np.asarray(raw).astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    if dtype == "f32":
+        return np.asarray(raw, dtype=np.float32).astype(np.float64)
+    raise ValueError(dtype)
+
+
+# ---------------------------------------------------------------------------
+# [CoD] 3.2 step 1: temperature-scaled softmax, here in log form
+
+def log_softmax_T(z: np.ndarray, T: float) -> np.ndarray:
+    """log softmax(z / T) over the last axis, two-pass (max, then log-sum-exp)."""
+    s = z / T
+    m = np.max(s, axis=-1, keepdims=True)
+    lse = m + np.log(np.sum(np.exp(s - m), axis=-1, keepdims=True))
+    return s - lse
+
+
+def softmax_T(z: np.ndarray, T: float) -> np.ndarray:
+    return np.exp(log_softmax_T(z, T))
+
+
+# ---------------------------------------------------------------------------
+# [SpS] acceptance, first rejection, residual, inverse CDF
+
+def acceptance_prob(log_p_x: float, log_q_x: float) -> float:
+    """alpha = min(1, p(x)/q(x)), evaluated as exp(min(0, log p(x) - log q(x)))."""
+    return math.exp(min(0.0, log_p_x - log_q_x))
+
+
+def first_rejection(u: np.ndarray, alpha: np.ndarray) -> int:
+    """Number of leading accepted drafts: the first i with not (u_i <= alpha_i), else gamma (R4)."""
+    for i in range(len(alpha)):
+        if not (u[i] <= alpha[i]):
+            return i
+    return len(alpha)
+
+
+def residual(p: np.ndarray, q: np.ndarray) -> np.ndarray:
+    """max(0, p - q) over the vocabulary (unnormalised; R5)."""
+    return np.maximum(0.0, p - q)
+
+
+def inverse_cdf(w: np.ndarray, u: float):
+    """Draw from the (unnormalised) weights w with the uniform u (R7).
+
+    Returns (token, Z, C_before, C_at): Z = sum w, C = running sum in token order,
+    token = min{v : C(v) > u*Z}; C_before = C(token-1) (0 for token 0), C_at = C(token)."""
+    Z = float(np.sum(w))
+    C = np.cumsum(w)
+    target = u * Z
+    hit = np.nonzero(C > target)[0]
+    if hit.size:
+        y = int(hit[0])
+    else:
+        y = int(np.nonzero(w > 0)[0][-1])
+    c_before = float(C[y - 1]) if y > 0 else 0.0
+    return y, Z, c_before, float(C[y])
+
+
+# ---------------------------------------------------------------------------
+# [CoD] 3.2: NKL
+
+def nkl_pair(zt: np.ndarray, zd: np.ndarray, T: float):
+    """(NKL, NKL_eps) for one (target row, draft row) pair, NKL = KL(q || p) / ln V.
+
+    KL(q||p) = sum_v q_v (log q_v - log p_v) with q = softmax(zd/T), p = softmax(zt/T)."""
+    V = zt.shape[-1]
+    lp = log_softmax_T(zt, T)
+    lq = log_softmax_T(zd, T)
+    q = np.exp(lq)
+    p = np.exp(lp)
+    kl = float(np.sum(q * (lq - lp)))
+    kl_eps = float(np.sum(q * (np.log(q + NKL_EPS) - np.log(p + NKL_EPS))))
+    lnV = math.log(V)
+    return kl / lnV, kl_eps / lnV
+
+
+# ---------------------------------------------------------------------------
+# one sequence, stochastic
+
+def verify_stochastic_sequence(t_rows: np.ndarray, d_rows: np.ndarray, tokens: np.ndarray, T: float,
+                               u_accept: np.ndarray, u_sample: float, nkl_delta: float = 0.15) -> dict:
+    """Stochastic verification of one sequence ([SpS]; bonus token R1).
+
+    t_rows: float64 [gamma+1, V]; d_rows: float64 [gamma, V]; tokens int [gamma]."""
+    g = d_rows.shape[0]
+    V = t_rows.shape[1]
+    out = {"n": -1, "tokens": np.full(g + 1, -1, dtype=np.int64),
+           "p_x": np.full(g, np.nan), "q_x": np.full(g, np.nan), "alpha": np.full(g, np.nan),
+           "nkl": np.full(g, np.nan), "nkl_eps": np.full(g, np.nan), "mask": np.zeros(g, dtype=np.uint8),
+           "greedy_n": -1, "greedy_tokens": np.full(g + 1, -1, dtype=np.int64),
+           "err": 0, "flag": False, "flags": []}
+    if not (np.all(np.isfinite(t_rows)) and np.all(np.isfinite(d_rows))):
+        out["err"] |= ERR_NONFINITE
+    if np.any((tokens < 0) | (tokens >= V)):
+        out["err"] |= ERR_TOKEN_RANGE
+    if out["err"]:
+        return out
+
+    # temperature-scaled log-probabilities of every row (one T for both, R9)
+    lp = log_softmax_T(t_rows, T)          # [g+1, V]
+    lq = log_softmax_T(d_rows, T)          # [g, V]
+
+    # gather at the drafted tokens, acceptance probability
+    for i in range(g):
+        x = int(tokens[i])
+        out["p_x"][i] = math.exp(lp[i, x])
+        out["q_x"][i] = math.exp(lq[i, x])
+        out["alpha"][i] = acceptance_prob(lp[i, x], lq[i, x])
+        if out["q_x"][i] < 1e-8:
+            out["flags"].append(("q_below_1e-8", i))
+        out["nkl"][i], out["nkl_eps"][i] = nkl_pair(t_rows[i], d_rows[i], T)
+        out["mask"][i] = 1 if out["nkl"][i] < nkl_delta else 0
+
+    # first rejection
+    n = first_rejection(u_accept, out["alpha"])
+    for i in range(min(n + 1, g)):
+        if abs(float(u_accept[i]) - out["alpha"][i]) < FLAG_BAND:
+            out["flags"].append(("accept_band", i))
+
+    # correction (residual) or bonus token
+    if n < g:
+        p = np.exp(lp[n])
+        q = np.exp(lq[n])
+        w = residual(p, q)
+        if float(np.sum(w)) <= 1e-30:                     # R6
+            out["flags"].append(("zero_residual", n))
+            w = p
+    else:
+        w = np.exp(lp[g])
+    y, Z, c0, c1 = inverse_cdf(w, float(u_sample))
+    if abs(c0 / Z - u_sample) < FLAG_BAND or abs(c1 / Z - u_sample) < FLAG_BAND:
+        out["flags"].append(("cdf_band", n))
+
+    out["n"] = n
+    out["tokens"][:n] = tokens[:n]
+    out["tokens"][n] = y
+
+    # greedy mode on the same rows (R10)
+    gn, gtok = greedy_sequence_core(t_rows, tokens)
+    out["greedy_n"], out["greedy_tokens"] = gn, gtok
+    out["flag"] = bool(out["flags"])
+    return out
+
+
+# ---------------------------------------------------------------------------
+# greedy
+
+def greedy_sequence_core(t_rows: np.ndarray, tokens: np.ndarray):
+    """[MTP] 2.3: accept while d_i == argmax(target row i); at the first mismatch n the
+    target's argmax replaces d_n; if all match, the argmax of row gamma follows."""
+    g = len(tokens)
+    amax = np.argmax(t_rows, axis=1)            # first maximal index = lowest-index tie-break
+    n = g
+    for i in range(g):
+        if int(tokens[i]) != int(amax[i]):
+            n = i
+            break
+    toks = np.full(g + 1, -1, dtype=np.int64)
+    toks[:n] = tokens[:n]
+    toks[n] = amax[n]
+    return n, toks
+
+
+def verify_greedy_sequence(t_rows: np.ndarray, tokens: np.ndarray) -> dict:
+    g = len(tokens)
+    V = t_rows.shape[1]
+    err = 0
+    if not np.all(np.isfinite(t_rows)):
+        err |= ERR_NONFINITE
+    if np.any((tokens < 0) | (tokens >= V)):
+        err |= ERR_TOKEN_RANGE
+    if err:
+        return {"n": -1, "tokens": np.full(g + 1, -1, dtype=np.int64), "err": err}
+    n, toks = greedy_sequence_core(t_rows, tokens)
+    return {"n": n, "tokens": toks, "err": 0}
+
+
+# ---------------------------------------------------------------------------
+# tree
+
+def tree_depths(parent) -> list:
+    depth = []
+    for j, pj in enumerate(parent):
+        depth.append(1 if pj < 0 else depth[pj] + 1)
+    return depth
+
+
+def verify_tree_sequence(t_rows: np.ndarray, node_tokens: np.ndarray, parent) -> dict:
+    """[PD] 2.2 tree, read as R15. t_rows [N+1, V]: row 0 is the parent position,
+    row j+1 scores the token that follows node j."""
+    N = len(parent)
+    V = t_rows.shape[1]
+    depth = tree_depths(parent)
+    Dmax = max(depth) if N else 0
+    res = {"len": -1, "path": np.full(Dmax, -1, dtype=np.int64),
+           "tokens": np.full(Dmax + 1, -1, dtype=np.int64), "err": 0}
+    if not np.all(np.isfinite(t_rows)):
+        res["err"] |= ERR_NONFINITE
+    if np.any((node_tokens < 0) | (node_tokens >= V)):
+        res["err"] |= ERR_TOKEN_RANGE
+    if res["err"]:
+        return res
+    amax = np.argmax(t_rows, axis=1)
+    ok = [False] * N
+    for j in range(N):
+        prow = 0 if parent[j] < 0 else parent[j] + 1
+        ok[j] = int(node_tokens[j]) == int(amax[prow]) and (parent[j] < 0 or ok[parent[j]])
+    pick, best = -1, 0
+    for j in range(N):
+        if ok[j] and depth[j] > best:
+            pick, best = j, depth[j]
+    chain = []
+    k = pick
+    while k >= 0:
+        chain.append(k)
+        k = parent[k]
+    chain.reverse()
+    res["len"] = best
+    res["path"][:best] = chain
+    res["tokens"][:best] = [int(node_tokens[j]) for j in chain]
+    res["tokens"][best] = int(amax[pick + 1]) if pick >= 0 else int(amax[0])
+    return res
+
+
+# ---------------------------------------------------------------------------
+# batch drivers over the packed layout (target rows of sequence b start at
+# cu_draft[b] + b, draft rows at cu_draft[b])
+
+def verify_stochastic(target_raw, draft_raw, tokens, cu_draft, T, u_accept, u_sample, dtype,
+                      nkl_delta=0.15, seqs=None) -> dict:
+    """Run verify_stochastic_sequence over sequences `seqs` (default: all)."""
+    B = len(cu_draft) - 1
+    seqs = range(B) if seqs is None else seqs
+    res = {}
+    for b in seqs:
+        d0, d1 = int(cu_draft[b]), int(cu_draft[b + 1])
+        t0 = d0 + b
+        g = d1 - d0
+        t_rows = widen(target_raw[t0:t0 + g + 1], dtype)
+        d_rows = widen(draft_raw[d0:d1], dtype)
+        res[b] = verify_stochastic_sequence(t_rows, d_rows, np.asarray(tokens[d0:d1]), T,
+                                            np.asarray(u_accept[d0:d1], dtype=np.float64),
+                                            float(u_sample[b]), nkl_delta)
+    return res
+
+
+def verify_greedy(target_raw, tokens, cu_draft, dtype, seqs=None) -> dict:
+    B = len(cu_draft) - 1
+    seqs = range(B) if seqs is None else seqs
+    res = {}
+    for b in seqs:
+        d0, d1 = int(cu_draft[b]), int(cu_draft[b + 1])
+        t0 = d0 + b
+        res[b] = verify_greedy_sequence(widen(target_raw[t0:t0 + (d1 - d0) + 1], dtype),
+                                        np.asarray(tokens[d0:d1]))
+    return res
+
+
+def verify_tree(target_raw, node_tokens, parent, dtype, seqs=None) -> dict:
+    N = len(parent)
+    B = node_tokens.shape[0]
+    seqs = range(B) if seqs is None else seqs
+    res = {}
+    for b in seqs:
+        rows = widen(target_raw[b * (N + 1):(b + 1) * (N + 1)], dtype)
+        res[b] = verify_tree_sequence(rows, np.asarray(node_tokens[b]), list(parent))
+    return res
+
+
+def nkl_rows(target_raw, draft_raw, cu_draft, T, dtype, delta=0.15, seqs=None) -> dict:
+    """Standalone NKL over every (target row i, draft row i) pair of the chosen sequences,
+    per-row errors (R16)."""
+    B = len(cu_draft) - 1
+    seqs = range(B) if seqs is None else seqs
+    res = {}
+    for b in seqs:
+        d0, d1 = int(cu_draft[b]), int(cu_draft[b + 1])
+        t0 = d0 + b
+        vals, eps, mask = [], [], []
+        for i in range(d1 - d0):
+            zt = widen(target_raw[t0 + i], dtype)
+            zd = widen(draft_raw[d0 + i], dtype)
+            if not (np.all(np.isfinite(zt)) and np.all(np.isfinite(zd))):
+                vals.append(np.nan), eps.append(np.nan), mask.append(0)
+                continue
+            a, e = nkl_pair(zt, zd, T)
+            vals.append(a), eps.append(e), mask.append(1 if a < delta else 0)
+        res[b] = {"nkl": np.array(vals), "nkl_eps": np.array(eps), "mask": np.array(mask, dtype=np.uint8)}
+    return res
+
+
+def position_delta(pos: int, delta_base: float = 0.15, a: float = 0.08, delta_max: float = 0.3) -> float:
+    """[CoD] 4.3 position-adaptive threshold, read with log2(pos), pos 1-based, capped at
+    delta_max: the page's printed values at pos 1 (0.15) and 1024 (0.27) fit log2(pos),
+    not the log2(pos + 1) its formula shows; its 0.192 at pos 128 fits neither."""
+    return min(delta_max, delta_base * (1.0 + a * math.log2(pos)))

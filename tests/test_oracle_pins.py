@@ -1,0 +1,414 @@
+"""Pins for the fp64 oracle: closed forms, invariants, brute force and the values the
+pages print. No GPU. Each check is chosen so that a plausible slip in the oracle (a
+swapped p/q, T multiplied instead of divided, a wrong row index, '<' for '<=', a
+non-strict CDF comparison, log2 for ln) makes at least one of them fail."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special as sps
+import scipy.stats
+
+from oracle import oracle as O
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def gold(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------- widening
+
+def test_widen_bf16_is_exact_ieee():
+    bits = np.array([0x3F80, 0xC040, 0x7F7F, 0x0001, 0x8000, 0x4049], dtype=np.uint16)
+    want = [1.0, -3.0, 3.3895313892515355e38, 2.0 ** -133, -0.0, 3.140625]
+    got = O.widen(bits, "bf16")
+    assert list(got) == want
+    assert math.copysign(1.0, got[4]) == -1.0
+
+
+# ---------------------------------------------------------------- softmax at temperature T
+
+def test_two_point_softmax_is_sigmoid_of_scaled_gap():
+    a, T = 1.7, 0.6
+    lp = O.log_softmax_T(np.array([0.0, a]), T)
+    assert abs(math.exp(lp[1]) - 1.0 / (1.0 + math.exp(-a / T))) < 1e-15
+
+
+def test_uniform_row_and_shift_invariance():
+    V = 1000
+    lp = O.log_softmax_T(np.full(V, 2.5), 0.7)
+    assert np.allclose(lp, -math.log(V), atol=1e-14, rtol=0)
+    rng = np.random.default_rng(5)
+    z = rng.normal(0, 3, 4096)
+    assert np.allclose(O.log_softmax_T(z, 0.8), O.log_softmax_T(z + 11.0, 0.8), atol=1e-12, rtol=0)
+
+
+def test_softmax_matches_scipy_and_sums_to_one():
+    rng = np.random.default_rng(6)
+    z = rng.normal(0, 3, (3, 128256))
+    for T in (0.6, 1.0, 1.7):
+        p = O.softmax_T(z, T)
+        assert np.allclose(p.sum(axis=1), 1.0, atol=1e-12, rtol=0)
+        assert np.allclose(p, sps.softmax(z / T, axis=1), rtol=1e-12, atol=1e-300)
+
+
+# ---------------------------------------------------------------- acceptance
+
+def test_acceptance_prob_closed_form():
+    assert O.acceptance_prob(math.log(0.25), math.log(0.5)) == pytest.approx(0.5, abs=1e-15)
+    assert O.acceptance_prob(math.log(0.5), math.log(0.25)) == 1.0
+
+
+def test_first_rejection_uses_less_or_equal():
+    assert O.first_rejection(np.array([0.5, 0.5, 0.5]), np.array([0.5, 0.5, 0.5])) == 3
+    assert O.first_rejection(np.array([0.1, 0.2, 0.9]), np.array([0.5, 0.5, 0.5])) == 2
+    assert O.first_rejection(np.array([0.6]), np.array([0.5])) == 0
+    assert O.first_rejection(np.array([]), np.array([])) == 0
+
+
+def _rows(rng, g, V, scale=3.0):
+    return rng.normal(0, scale, (g + 1, V))
+
+
+def test_identical_rows_accept_everything():
+    """Invariant (a): q == p gives alpha == 1 at every position and n == gamma for any u < 1."""
+    rng = np.random.default_rng(7)
+    for V, g in ((2, 1), (8, 3), (1000, 5), (32000, 4)):
+        t = _rows(rng, g, V)
+        d = t[:g].copy()
+        tok = rng.integers(0, V, g)
+        u = np.full(g, np.float32(1.0) - np.float32(2.0 ** -24), dtype=np.float64)
+        r = O.verify_stochastic_sequence(t, d, tok, 0.9, u, 0.3)
+        assert np.all(r["alpha"] == 1.0)
+        assert r["n"] == g
+        assert np.all(r["nkl"] == 0.0) or np.all(np.abs(r["nkl"]) < 1e-15)
+        assert list(r["tokens"][:g]) == list(tok)
+
+
+def test_the_drafter_gets_no_acceptance():
+    """The 'Chain of Draft' article's degenerate drafter (always the same token):
+    q(x) ~ 1 so alpha = p(x), tiny at V = 32000; with seeded u every sequence stops at 0."""
+    want = gold("cod_the_drafter.json")["acceptance_rate"]
+    rng = np.random.default_rng(8)
+    V, g, the = 32000, 4, 17
+    accepted = 0
+    for _ in range(64):
+        t = _rows(rng, g, V)
+        d = rng.normal(0, 3, (g, V))
+        d[:, the] = 60.0
+        u = rng.random(g).astype(np.float32).astype(np.float64)
+        r = O.verify_stochastic_sequence(t, d, np.full(g, the), 1.0, u, float(rng.random()))
+        assert np.allclose(r["alpha"], r["p_x"], rtol=1e-9)
+        accepted += r["n"]
+    assert accepted / (64 * g) == want
+
+
+# ---------------------------------------------------------------- inverse CDF
+
+def test_inverse_cdf_hand_cases():
+    w = np.array([0.0, 1.0, 0.0, 3.0])
+    assert O.inverse_cdf(w, 0.0)[0] == 1          # a zero-mass token is never drawn
+    assert O.inverse_cdf(w, 0.2499)[0] == 1
+    assert O.inverse_cdf(w, 0.25)[0] == 3         # strict '>': C(1) = 1 is not > 1
+    assert O.inverse_cdf(w, 0.99999)[0] == 3
+    y, Z, c0, c1 = O.inverse_cdf(w, 0.5)
+    assert (y, Z, c0, c1) == (3, 4.0, 1.0, 4.0)
+
+
+def test_bonus_two_token_closed_form():
+    """V = 2, everything accepted: the bonus token is 1 iff u_sample >= p_gamma(0)."""
+    zt = np.array([[0.3, -0.4], [1.1, 0.2]])
+    p0 = sps.softmax(zt[1] / 0.8)[0]
+    for us, want in ((p0 - 1e-9, 0), (p0 + 1e-9, 1), (0.0, 0), (0.999, 1)):
+        r = O.verify_stochastic_sequence(zt, zt[:1].copy(), np.array([1]), 0.8, np.array([0.0]), us)
+        assert r["n"] == 1 and r["tokens"][1] == want
+
+
+# ---------------------------------------------------------------- losslessness by enumeration
+
+def _measure(fn, lo=0.0, hi=1.0, iters=60):
+    """Length of the set of u in [lo, hi) where fn(u) is True, for fn monotone (True then False)."""
+    if not fn(lo):
+        return 0.0
+    if fn(np.nextafter(hi, 0)):
+        return hi - lo
+    a, b = lo, hi
+    for _ in range(iters):
+        m = 0.5 * (a + b)
+        if fn(m):
+            a = m
+        else:
+            b = m
+    return a - lo
+
+
+def _sampler_masses(call, V):
+    """Masses of u_sample mapping to each token: the map is monotone non-decreasing in u,
+    so the breakpoints are found by bisection."""
+    masses = np.zeros(V)
+    for v in range(V):
+        masses[v] = _measure(lambda u: call(u) <= v) - (_measure(lambda u: call(u) <= v - 1) if v else 0.0)
+    return masses
+
+
+@pytest.mark.parametrize("V,T", [(2, 1.0), (3, 0.5), (5, 1.3), (8, 0.7), (8, 2.0)])
+def test_output_marginal_equals_target_distribution(V, T):
+    """Invariant (b): draw x ~ q, accept with the oracle's own rule, else draw from the
+    oracle's residual sampler; the emitted token's law must be p within 1e-12."""
+    rng = np.random.default_rng(100 + V)
+    zt = rng.normal(0, 2, (2, V))
+    zd = rng.normal(0, 2, (1, V))
+    p = sps.softmax(zt[0] / T)
+    q = sps.softmax(zd[0] / T)
+
+    def n_for(x, u):
+        return O.verify_stochastic_sequence(zt, zd, np.array([x]), T, np.array([u]), 0.5)["n"]
+
+    acc = np.array([_measure(lambda u, x=x: n_for(x, u) >= 1) for x in range(V)])
+    # the correction does not depend on which x was rejected; take the draft token
+    # with the lowest acceptance so that a rejection is reachable
+    xr = int(np.argmin(acc))
+    assert acc[xr] < 1.0
+    res = _sampler_masses(lambda us: O.verify_stochastic_sequence(
+        zt, zd, np.array([xr]), T, np.array([np.nextafter(1.0, 0)]), us)["tokens"][0], V)
+    emitted = q * acc + np.sum(q * (1.0 - acc)) * res
+    assert np.allclose(emitted, p, atol=1e-12, rtol=0)
+    assert np.allclose(acc, np.minimum(1.0, p / q), atol=1e-12, rtol=0)
+
+
+def test_second_position_and_bonus_use_their_own_rows():
+    """gamma = 2: given the first draft accepted, the second emitted token follows p_1,
+    and when both are accepted the third follows p_2 (the bonus row)."""
+    V, T = 6, 0.9
+    rng = np.random.default_rng(11)
+    zt = rng.normal(0, 2, (3, V))
+    zd = rng.normal(0, 2, (2, V))
+    p1 = sps.softmax(zt[1] / T)
+    p2 = sps.softmax(zt[2] / T)
+    q1 = sps.softmax(zd[1] / T)
+    x0 = 0
+
+    def run(x1, u1, us):
+        return O.verify_stochastic_sequence(zt, zd, np.array([x0, x1]), T, np.array([0.0, u1]), us)
+
+    acc1 = np.array([_measure(lambda u, x=x: run(x, u, 0.5)["n"] == 2) for x in range(V)])
+    xr = int(np.argmin(acc1))
+    res = _sampler_masses(lambda us: run(xr, np.nextafter(1.0, 0), us)["tokens"][1], V)
+    second = q1 * acc1 + np.sum(q1 * (1 - acc1)) * res
+    assert np.allclose(second, p1, atol=1e-12, rtol=0)
+    xa = int(np.argmax(acc1))
+    bonus = _sampler_masses(lambda us: run(xa, 0.0, us)["tokens"][2], V)
+    assert np.allclose(bonus, p2, atol=1e-12, rtol=0)
+
+
+def test_worked_example_three_accepted_one_corrected():
+    ex = gold("sps_worked_example.json")
+    g = ex["drafted"]
+    rng = np.random.default_rng(12)
+    V = 50
+    t = rng.normal(0, 2, (g + 1, V))
+    d = t[:g].copy()
+    d[3] = rng.normal(0, 2, V)                 # the 4th draft row disagrees with the target
+    q3 = sps.softmax(d[3])
+    p3 = sps.softmax(t[3])
+    x3 = int(np.argmax(q3 / p3))               # a token the target under-weights: alpha < 1
+    tok = np.array([5, 9, 7, x3])
+    u = np.array([0.3, 0.7, 0.99, 0.999999])
+    r = O.verify_stochastic_sequence(t, d, tok, 1.0, u, 0.42)
+    assert r["alpha"][3] < 0.999999
+    assert r["n"] == ex["accepted"]
+    valid = int(np.sum(r["tokens"] >= 0))
+    assert valid == ex["emitted"] == ex["accepted"] + ex["corrected"]
+    assert list(r["tokens"][:3]) == [5, 9, 7]
+    w = np.maximum(0, p3 - q3)
+    assert w[r["tokens"][3]] > 0                # the correction comes from the residual's support
+
+
+# ---------------------------------------------------------------- greedy
+
+def test_greedy_accepts_target_argmax_drafts():
+    """Invariant (c)."""
+    rng = np.random.default_rng(13)
+    t = rng.normal(0, 3, (6, 777))
+    am = [int(np.argmax(r)) for r in t]
+    r = O.verify_greedy_sequence(t, np.array(am[:5]))
+    assert r["n"] == 5 and list(r["tokens"]) == am
+
+
+def test_greedy_first_mismatch_and_ties():
+    t = np.array([[3.0, 5.0, 5.0, 1.0], [0.0, 0.0, 0.0, 0.0], [1.0, 2.0, 9.0, 9.0]])
+    r = O.verify_greedy_sequence(t, np.array([1, 0]))
+    assert r["n"] == 2 and list(r["tokens"]) == [1, 0, 2]
+    r = O.verify_greedy_sequence(t, np.array([2, 0]))
+    assert r["n"] == 0 and list(r["tokens"]) == [1, -1, -1]
+    r = O.verify_greedy_sequence(t, np.array([1, 3]))
+    assert r["n"] == 1 and list(r["tokens"]) == [1, 0, -1]
+
+
+# ---------------------------------------------------------------- tree
+
+def _tree_brute(t_rows, tok, parent):
+    """Walk every root-to-leaf chain, keep the longest prefix whose tokens each equal the
+    argmax of the row before them; best = deepest end node, lowest index on ties."""
+    N = len(parent)
+    children = {j: [k for k in range(N) if parent[k] == j] for j in range(-1, N)}
+    chains = []
+
+    def walk(j, acc):
+        acc = acc + [j]
+        if not children[j]:
+            chains.append(acc)
+        for c in children[j]:
+            walk(c, acc)
+
+    for r in children[-1]:
+        walk(r, [])
+    ends = []
+    for ch in chains:
+        row = 0
+        good = []
+        for j in ch:
+            if int(tok[j]) == int(np.argmax(t_rows[row])):
+                good.append(j)
+                row = j + 1
+            else:
+                break
+        if good:
+            ends.append((len(good), good[-1], good))
+    if not ends:
+        return 0, [], int(np.argmax(t_rows[0]))
+    best = min(ends, key=lambda e: (-e[0], e[1]))
+    return best[0], best[2], int(np.argmax(t_rows[best[1] + 1]))
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_tree_matches_brute_force(seed):
+    parent = [-1, -1, -1, 0, 1, 2, 3, 4, 5, 6, 7, 8]
+    assert len(parent) == gold("pd_tree_shape.json")["max_nodes"]
+    assert sum(1 for p in parent if p < 0) == gold("pd_tree_shape.json")["root_candidates"]
+    rng = np.random.default_rng(seed)
+    V = 9
+    t = rng.normal(0, 1, (13, V))
+    am = np.argmax(t, axis=1)
+    tok = rng.integers(0, V, 12)
+    for j in range(12):                          # force matches at random
+        if rng.random() < 0.6:
+            tok[j] = am[0 if parent[j] < 0 else parent[j] + 1]
+    r = O.verify_tree_sequence(t, tok, parent)
+    L, path, corr = _tree_brute(t, tok, parent)
+    assert r["len"] == L
+    assert list(r["path"][:L]) == path and np.all(r["path"][L:] == -1)
+    assert list(r["tokens"][:L]) == [int(tok[j]) for j in path]
+    assert r["tokens"][L] == corr and np.all(r["tokens"][L + 1:] == -1)
+
+
+def test_tree_branching_shapes_and_ties():
+    parent = [-1, 0, 0, 1, 2, -1]               # two branches of equal depth under root 0
+    t = np.zeros((7, 4))
+    t[0, 2] = 1; t[1, 1] = 1; t[2, 3] = 1; t[3, 0] = 1
+    tok = np.array([2, 1, 1, 3, 0, 0])          # nodes 3 and 4 both accepted at depth 3: lowest wins
+    r = O.verify_tree_sequence(t, tok, parent)
+    L, path, corr = _tree_brute(t, tok, parent)
+    assert (r["len"], list(r["path"][:L])) == (L, path) == (3, [0, 1, 3])
+    tok2 = np.array([2, 1, 1, 0, 1, 0])         # only depth-2 nodes 1 and 2 accepted: lowest wins
+    r = O.verify_tree_sequence(t, tok2, parent)
+    assert r["len"] == 2 and list(r["path"][:2]) == [0, 1] and r["tokens"][2] == int(np.argmax(t[2]))
+
+
+def test_chain_tree_reduces_to_greedy():
+    rng = np.random.default_rng(21)
+    for _ in range(20):
+        V, N = 11, 6
+        t = rng.normal(0, 1, (N + 1, V))
+        am = np.argmax(t, axis=1)
+        tok = np.where(rng.random(N) < 0.7, am[:N], rng.integers(0, V, N))
+        tr = O.verify_tree_sequence(t, tok, [-1, 0, 1, 2, 3, 4])
+        gr = O.verify_greedy_sequence(t, tok)
+        assert tr["len"] == gr["n"]
+        assert list(tr["tokens"]) == list(gr["tokens"])
+
+
+# ---------------------------------------------------------------- NKL
+
+def test_nkl_zero_on_identical_rows_and_nonnegative():
+    """Invariant (d)."""
+    rng = np.random.default_rng(31)
+    z = rng.normal(0, 3, 5000)
+    assert abs(O.nkl_pair(z, z.copy(), 0.6)[0]) < 1e-15
+    for _ in range(20):
+        a, b = rng.normal(0, 3, 300), rng.normal(0, 3, 300)
+        assert O.nkl_pair(a, b, 0.6)[0] >= 0.0
+
+
+def test_nkl_two_point_and_direction():
+    """KL(q || p) with q the DRAFT row, natural log, divided by ln V: against scipy's
+    relative entropy, which is not symmetric, so a swapped direction fails."""
+    zt = np.array([0.0, 1.2])
+    zd = np.array([0.0, -0.9])
+    T = 0.7
+    p = sps.softmax(zt / T)
+    q = sps.softmax(zd / T)
+    want = scipy.stats.entropy(q, p) / math.log(2)
+    assert O.nkl_pair(zt, zd, T)[0] == pytest.approx(want, rel=1e-12)
+    assert abs(scipy.stats.entropy(p, q) / math.log(2) - want) > 1e-3
+
+
+def test_nkl_scale_is_log_vocab():
+    """Against a uniform target a one-hot draft has KL = ln V, so NKL -> 1; at the page's
+    128k vocabulary ln V ~ 11.76, the 'about 12' the page quotes."""
+    c = gold("cod_nkl_constants.json")
+    V = c["vocab_size"]
+    assert abs(math.log(V) - c["page_kl_scale_about"]) < 0.5
+    assert math.log(V) == pytest.approx(11.7618, abs=1e-4)
+    zt = np.zeros(V)
+    zd = np.zeros(V)
+    zd[123] = 2000.0
+    nkl, nkl_eps = O.nkl_pair(zt, zd, 1.0)
+    assert nkl == pytest.approx(1.0, abs=1e-12)
+    assert abs(nkl_eps - nkl) < 1e-6
+
+
+def test_nkl_mask_threshold_and_eps_form():
+    c = gold("cod_nkl_constants.json")
+    rng = np.random.default_rng(33)
+    V, g = 4000, 3
+    t = rng.normal(0, 3, (g + 1, V))
+    d = 0.9 * t[:g] + rng.normal(0, 1, (g, V))
+    r = O.verify_stochastic_sequence(t, d, np.zeros(g, dtype=int), 0.6, np.zeros(g), 0.5, c["delta"])
+    assert np.all(r["mask"] == (r["nkl"] < c["delta"]))
+    assert np.all(np.abs(r["nkl_eps"] - r["nkl"]) <= 1e-4 * r["nkl"])
+
+
+# ---------------------------------------------------------------- position-adaptive delta
+
+def test_position_delta_printed_values():
+    c = gold("cod_position_delta.json")
+    for pos, val in c["printed"].items():
+        got = O.position_delta(int(pos), c["delta_base"], c["alpha"], c["delta_max"])
+        if pos in c["page_inconsistent"]:
+            assert abs(got - val) > 0.03          # the page's 0.192 fits neither log form
+        else:
+            assert got == pytest.approx(val, abs=1e-12)
+    assert O.position_delta(10 ** 9) == c["delta_max"]
+
+
+# ---------------------------------------------------------------- error semantics
+
+def test_errors_mark_the_whole_sequence():
+    rng = np.random.default_rng(41)
+    t = rng.normal(0, 1, (4, 10))
+    d = rng.normal(0, 1, (3, 10))
+    bad = t.copy()
+    bad[3, 4] = np.inf
+    r = O.verify_stochastic_sequence(bad, d, np.array([1, 2, 3]), 1.0, np.zeros(3), 0.5)
+    assert r["n"] == -1 and r["err"] == O.ERR_NONFINITE and np.all(r["tokens"] == -1)
+    assert np.all(np.isnan(r["alpha"]))
+    r = O.verify_stochastic_sequence(t, d, np.array([1, 10, 3]), 1.0, np.zeros(3), 0.5)
+    assert r["n"] == -1 and r["err"] == O.ERR_TOKEN_RANGE
+    r = O.verify_greedy_sequence(t, np.array([-1, 2, 3]))
+    assert r["n"] == -1 and r["err"] == O.ERR_TOKEN_RANGE
