@@ -1,0 +1,456 @@
+"""Throughput of batched draft-token verification on GB300.
+
+One step = one spec_verify_stochastic call on the headline workload (B=256 sequences,
+gamma=8 drafts, V=128256, bf16 logits, T=0.6): temperature softmax of every target and
+draft row, acceptance, first rejection, residual or bonus token, per-position NKL with
+its delta=0.15 mask and the greedy decision, all from one read of the logits. The
+metric is verified target rows per second (B*(gamma+1) rows per step).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank verifies its own batch (weak scaling, no collective on the
+data path); rank 0 prints one JSON line. `--impl reference` times the fp64 CPU oracle
+instead, on a bounded sample of the same workload."""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "verified rows/s & HBM GB/s vs GB300 peak (B=256, gamma=8, V=128256, bf16)"
+HEADLINE = 2
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def algorithmic_bytes(w) -> dict:
+    """Bytes the verification must read: every target and draft logit once, plus one
+    (target, draft) row pair per sequence for the residual / bonus sample."""
+    es = w.elem_bytes
+    t = w.total_target * w.V * es
+    d = w.total_draft * w.V * es
+    resid = w.B * 2 * w.V * es
+    small = w.total_draft * (4 + 4) + w.B * 4
+    return {"stochastic": t + d + resid + small, "greedy": t + w.total_draft * 4, "nkl": w.total_draft * w.V * es * 2}
+
+
+# ---------------------------------------------------------------- distributed plumbing
+
+def dist_setup(n_gpus):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+
+CLOCK_Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+           "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+           "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={CLOCK_Q}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(gpu_index)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- our arm
+
+def _to_dev(a, dev):
+    import torch
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+
+class StochasticCall:
+    """Preallocated inputs/outputs for repeated spec_verify_stochastic calls."""
+
+    def __init__(self, w, dev, host_inputs=False):
+        import ctypes
+
+        import torch
+
+        from speculative_decoding_token_temp_gb300 import _lib
+        self.w = w
+        self.dev = dev
+        self.lib = _lib.lib()
+        B, V = w.B, w.V
+        rows, tot = w.total_target, w.total_draft
+        self.t = _to_dev(w.target, dev)
+        self.d = _to_dev(w.draft, dev)
+        self.tok = _to_dev(w.tokens, dev)
+        self.ua = _to_dev(w.u_accept, dev)
+        self.us = _to_dev(w.u_sample, dev)
+        self.cu = None if w.dense else _to_dev(w.cu_draft, dev)
+        z = lambda n, dt: torch.empty(n, dtype=dt, device=dev)  # noqa: E731
+        self.n = z(B, torch.int32)
+        self.out = z(rows, torch.int32)
+        self.px, self.qx, self.al, self.nkl = (z(tot, torch.float32) for _ in range(4))
+        self.mask = z(tot, torch.uint8)
+        self.gn = z(B, torch.int32)
+        self.gt = z(rows, torch.int32)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.g = _lib.SpecBatch(B, w.gamma_max if not w.dense else int(w.gammas[0]), V, tot,
+                                ctypes.c_void_p(self.cu.data_ptr()) if self.cu is not None else None)
+        nbytes = self.lib.spec_workspace_bytes(self.g, _lib.SPEC_MODE_STOCHASTIC)
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        self.dt = _lib.SPEC_BF16 if w.dtype == "bf16" else _lib.SPEC_F32
+        self.host = None
+        if host_inputs:
+            pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+            self.host = {"t": pin(self.t), "d": pin(self.d), "tok": pin(self.tok), "ua": pin(self.ua),
+                         "us": pin(self.us)}
+            self.host_out = {"n": torch.empty(B, dtype=torch.int32).pin_memory(),
+                             "out": torch.empty(rows, dtype=torch.int32).pin_memory()}
+        self.P = ctypes.c_void_p
+
+    def h2d_bytes(self):
+        return sum(v.numel() * v.element_size() for v in self.host.values())
+
+    def d2h_bytes(self):
+        return sum(v.numel() * v.element_size() for v in self.host_out.values())
+
+    def __call__(self, stream_handle):
+        P = self.P
+        code = self.lib.spec_verify_stochastic(
+            self.g, self.dt, P(self.t.data_ptr()), P(self.d.data_ptr()), P(self.tok.data_ptr()), self.w.T,
+            P(self.ua.data_ptr()), P(self.us.data_ptr()), P(self.n.data_ptr()), P(self.out.data_ptr()),
+            P(self.px.data_ptr()), P(self.qx.data_ptr()), P(self.al.data_ptr()), P(self.nkl.data_ptr()),
+            P(self.mask.data_ptr()), 0.15, P(self.gn.data_ptr()), P(self.gt.data_ptr()), P(self.status.data_ptr()),
+            P(self.ws.data_ptr()), self.ws.numel(), P(stream_handle))
+        if code != 0:
+            raise RuntimeError(f"spec_verify_stochastic returned {code}")
+
+    def e2e_step(self, stream_handle):
+        self.t.copy_(self.host["t"], non_blocking=True)
+        self.d.copy_(self.host["d"], non_blocking=True)
+        self.tok.copy_(self.host["tok"], non_blocking=True)
+        self.ua.copy_(self.host["ua"], non_blocking=True)
+        self.us.copy_(self.host["us"], non_blocking=True)
+        self(stream_handle)
+        self.host_out["n"].copy_(self.n, non_blocking=True)
+        self.host_out["out"].copy_(self.out, non_blocking=True)
+
+
+def time_loop(fn, steps, warmup, stream, world, dev):
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    return a.elapsed_time(b) / 1e3
+
+
+def time_mode(fn, steps, warmup, dev):
+    """Per-call device time of a secondary mode (single GPU, no barrier)."""
+    import torch
+    s = torch.cuda.current_stream(dev)
+    return time_loop(fn, steps, warmup, s, 1, dev) / steps
+
+
+def cpu_baseline(w, budget_s=12.0):
+    """The fp64 oracle as it stands on this host: stochastic + NKL + greedy per sequence,
+    sequences taken in order until the time budget is spent."""
+    from oracle import oracle as O
+    t0 = time.perf_counter()
+    rows = 0
+    done = 0
+    for b in range(w.B):
+        O.verify_stochastic(w.target, w.draft, w.tokens, w.cu_draft, w.T, w.u_accept, w.u_sample, w.dtype,
+                            seqs=[b])
+        rows += int(w.gammas[b]) + 1
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    el = time.perf_counter() - t0
+    return {"value": rows / el, "unit": "rows/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} of {w.B} sequences ({rows} target rows) of the B=256/gamma=8/V=128256 bf16 "
+                      f"workload, stochastic+NKL+greedy in fp64 numpy, single thread, {el:.1f} s"}
+
+
+def run_ours(args):
+    import torch
+
+    import __graft_entry__
+    from speculative_decoding_token_temp_gb300 import api, synth
+
+    world, rank, local = dist_setup(args.gpus)
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    __graft_entry__.build()
+    cfg = synth.CONFIGS[HEADLINE]
+    w = cfg.make(seed=cfg.seed + 1000 * rank)
+    call = StochasticCall(w, dev, host_inputs=True)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    step = lambda: call(sh)  # noqa: E731
+
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    el = time_loop(step, args.steps, args.warmup, stream, world, dev)
+    ck = clocks.stop()
+    el = max_over_ranks(el, world, dev)
+    status = int(call.status.item())
+    rows_step = w.total_target
+    total_rows = sum_over_ranks(rows_step * args.steps, world, dev)
+    value = total_rows / el
+    ms = el / args.steps * 1e3
+
+    hbm, peak_kind = peaks()
+    ab = algorithmic_bytes(w)
+    achieved = ab["stochastic"] / (ms / 1e3) / 1e9
+
+    # end to end: host buffers, H2D of every input and D2H of the decisions inside the timed region
+    e2e_steps = max(3, min(20, args.steps))
+    e2e_el = time_loop(lambda: call.e2e_step(sh), e2e_steps, 2, stream, world, dev)
+    e2e_el = max_over_ranks(e2e_el, world, dev)
+    e2e_val = sum_over_ranks(rows_step * e2e_steps, world, dev) / e2e_el
+
+    modes = {}
+    if rank == 0 and not args.no_modes:
+        # the standalone calls, same inputs
+        res = {}
+        g_out = {}
+        gfn = lambda: api.spec_verify_greedy(call.t, call.tok, gamma=8, out=g_out)  # noqa: E731
+        t_g = time_mode(gfn, 200, 10, dev)
+        modes["greedy_B256_g8_V128256"] = {"us_per_call": t_g * 1e6,
+                                           "GBps": ab["greedy"] / t_g / 1e9, "rows_per_s": rows_step / t_g}
+        n_out = {}
+        nfn = lambda: api.spec_nkl(call.t, call.d, w.T, gamma=8, out=n_out)  # noqa: E731
+        t_n = time_mode(nfn, 200, 10, dev)
+        modes["nkl_B256_g8_V128256"] = {"us_per_call": t_n * 1e6, "GBps": ab["nkl"] / t_n / 1e9}
+        del res
+        tw = synth.CONFIGS[3].make()
+        tt = _to_dev(tw.target, dev)
+        tn = _to_dev(tw.node_tokens, dev)
+        t_out = {}
+        tfn = lambda: api.spec_verify_tree(tt, tn, list(tw.parent), out=t_out)  # noqa: E731
+        t_t = time_mode(tfn, 500, 10, dev)
+        tbytes = tw.target.nbytes
+        modes["tree_B32_N12_V128256"] = {"us_per_call": t_t * 1e6, "GBps": tbytes / t_t / 1e9,
+                                         "rows_per_s": tw.B * (tw.N + 1) / t_t}
+        del tt, tn
+        w1 = synth.CONFIGS[1].make(T=0.6)
+        c1 = StochasticCall(w1, dev)
+        t_1 = time_mode(lambda: c1(sh), 500, 10, dev)
+        b1 = algorithmic_bytes(w1)["stochastic"]
+        modes["stochastic_B64_g5_V32000_warm_L2"] = {"us_per_call": t_1 * 1e6, "GBps": b1 / t_1 / 1e9,
+                                                     "rows_per_s": w1.total_target / t_1,
+                                                     "note": "53 MB of inputs fit in L2: warm-cache figure"}
+        del c1
+        if not args.skip_ragged:
+            w4 = synth.CONFIGS[4].make()
+            c4 = StochasticCall(w4, dev)
+            t_4 = time_mode(lambda: c4(sh), 100, 5, dev)
+            b4 = algorithmic_bytes(w4)["stochastic"]
+            modes["stochastic_ragged_B512_V152064"] = {"us_per_call": t_4 * 1e6, "GBps": b4 / t_4 / 1e9,
+                                                       "rows_per_s": w4.total_target / t_4,
+                                                       "frac_of_peak": b4 / t_4 / 1e9 / hbm}
+            del c4
+
+    if rank != 0:
+        return
+    cpu = cpu_baseline(w) if world == 1 and not args.no_cpu else None
+    out = {
+        "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "B256_g8_V128256_bf16: stochastic verify + NKL(delta=0.15) + greedy, one call",
+                   "B": w.B, "gamma": 8, "V": w.V, "T": w.T, "seed": cfg.seed, "rows_per_step": rows_step,
+                   "l2": "inputs 1116 MB per step, larger than the 129 MB L2; no flush",
+                   "parallelism": f"{world} independent shard(s), no collective"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": None,
+                     "kernel": "spec_verify_stochastic call (prologue + rows_kernel + sample_kernel)",
+                     "algorithmic_bytes": ab["stochastic"], "peak_source": peak_kind},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_val, "unit": "rows/s", "h2d_bytes_per_step": call.h2d_bytes(),
+                "d2h_bytes_per_step": call.d2h_bytes()},
+        "gpu_launches": 3 * args.steps,
+        "clocks": ck,
+        "device_status": status,
+        "modes": modes,
+    }
+    print(json.dumps(out))
+
+
+# ---------------------------------------------------------------- reference arm (the oracle)
+
+def run_reference(args):
+    """The fp64 oracle on the host cores, on the same workload. Each step verifies a
+    bounded sample: m whole sequences, or, when K+W steps of one sequence each would
+    not finish in about two minutes, the first k positions of a sequence (a sub-sequence
+    whose last target row serves as its bonus row), k and m sized from one calibration
+    sequence."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from oracle import oracle as O
+    from speculative_decoding_token_temp_gb300 import synth
+    cfg = synth.CONFIGS[HEADLINE]
+    g = cfg.gamma
+    budget = 120.0
+    cal = synth.make_stochastic(1, cfg.V, cfg.dtype, cfg.T[0], cfg.seed + 77, gamma=g)
+    t0 = time.perf_counter()
+    O.verify_stochastic(cal.target, cal.draft, cal.tokens, cal.cu_draft, cal.T, cal.u_accept, cal.u_sample,
+                        cal.dtype)
+    t_seq = time.perf_counter() - t0
+    per_step = budget / (args.steps + args.warmup)
+    m = int(max(1, min(3, per_step // t_seq)))
+    k = g if per_step >= t_seq else int(max(1, min(g, (per_step / t_seq) * (g + 1) - 1)))
+    nseq = m * (args.steps + args.warmup) if k == g else (args.steps + args.warmup)
+    pool = min(nseq, 64)
+    w = synth.make_stochastic(pool, cfg.V, cfg.dtype, cfg.T[0], cfg.seed, gamma=g)
+    widen = lambda a: O.widen(a, w.dtype)  # noqa: E731
+    step_i = 0
+
+    def step():
+        nonlocal step_i
+        if k == g:
+            seqs = [(step_i * m + j) % pool for j in range(m)]
+            O.verify_stochastic(w.target, w.draft, w.tokens, w.cu_draft, w.T, w.u_accept, w.u_sample, w.dtype,
+                                seqs=seqs)
+        else:
+            b = step_i % pool
+            t_rows, d_rows, tok, ua, us = w.sequence(b)
+            O.verify_stochastic_sequence(widen(t_rows[:k + 1]), widen(d_rows[:k]), tok[:k], w.T,
+                                         ua[:k].astype(np.float64), us)
+        step_i += 1
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    rows_per_step = m * (g + 1) if k == g else k + 1
+    val = rows_per_step * args.steps / el
+    sample = (f"{m} whole sequence(s) per step" if k == g else f"the first {k} of {g} positions of one sequence "
+              f"per step (+ its next target row as bonus row)")
+    out = {"impl": "reference", "metric": METRIC, "value": val, "unit": "rows/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": "B256_g8_V128256_bf16: stochastic verify + NKL(delta=0.15) + greedy",
+                      "B": cfg.B, "gamma": g, "V": cfg.V, "T": cfg.T[0], "seed": cfg.seed,
+                      "sample_per_step": sample},
+           "cpu_baseline": {"value": val, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                            "sample": sample + f" ({rows_per_step} target rows), fp64 numpy, single thread"},
+           "e2e": {"value": val, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-modes", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--skip-ragged", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,183 @@
+/*
+ * spec_verify.h -- C ABI of the batched draft-token verification library (GB300, sm_103a).
+ *
+ * One speculative-decoding round ends with a target forward over the gamma drafted
+ * positions plus one; this library takes those target logits, the drafter's logits and
+ * tokens, and decides what is kept. Sources, by page title and section:
+ *
+ *   [SpS] speculative-sampling article ("大模型推理的投机采样：Draft 小模型辅助与验证加速"),
+ *         section "核心算法数学原理：无损拒绝采样": a draft token x is accepted when a uniform
+ *         r satisfies r <= min(1, p(x)/q(x)); at the first rejection a replacement is drawn
+ *         from max(0, p - q)/norm and the remaining drafts are dropped; section "核心实现":
+ *         the target scores the last gamma+1 positions.
+ *   [CoD] "Chain of Draft" article, section 3.2: NKL = KL(draft || target) / log(vocab),
+ *         both rows softmaxed at one temperature, drafts kept while NKL < delta (0.15).
+ *   [MTP] Gemma 4 multi-token-prediction drafter article, section 2.3: greedy verification
+ *         (accept while the draft equals the target argmax; the target's argmax replaces
+ *         the first mismatch).
+ *   [PD]  Parallel Drafting article, section 2.2: the P-EAGLE draft tree (three root
+ *         candidates, at most 12 nodes), verified along its longest accepted path.
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument is a DEVICE pointer unless its comment says "host".
+ *     The caller owns every buffer; the library keeps no pointer after the call returns
+ *     and allocates no memory.
+ *   - All work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *     stream) and is asynchronous. The return value reports only what can be checked
+ *     on the host before launch (null pointers, sizes, temperature, dtype, workspace
+ *     size) and launch failures; it never waits for the GPU.
+ *   - Data errors found on the GPU are OR-ed into *device_status (a 32-bit device word,
+ *     SPEC_DEV_* bits). The word is sticky: the library never clears it, the caller
+ *     zeroes it when it wants a fresh reading. A sequence with a data error reports
+ *     n = -1, -1 in its integer outputs and NaN in its real outputs. No kernel traps,
+ *     asserts or waits on another block.
+ *   - Logits are row-major [rows, V] with V contiguous, fp32 or bf16 (raw bf16 bit
+ *     patterns). Rows whose byte size is a multiple of 16 and whose base pointers are
+ *     16-byte aligned take the vectorised path; any other layout takes a slower scalar
+ *     path with the same results.
+ *   - Packed batches: sequence b has gamma_b drafts. Its draft rows, draft tokens and
+ *     u_accept entries start at cu_draft[b]; its target rows (gamma_b + 1 of them: one
+ *     per draft plus the bonus row) and its out_tokens entries start at cu_draft[b] + b.
+ *     cu_draft == NULL means a dense batch with gamma_b = gamma for every b.
+ *   - `workspace` is scratch memory of at least spec_workspace_bytes() bytes. Its
+ *     contents need no initialisation and are meaningless between calls. Two calls may
+ *     not use one workspace at the same time (e.g. on two streams).
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* spec_stream_t; /* the same handle as cudaStream_t */
+
+typedef enum {
+  SPEC_OK = 0,
+  SPEC_ERR_INVALID_ARG = 1, /* null pointer, bad size, non-finite or non-positive T, bad tree */
+  SPEC_ERR_DTYPE = 2,       /* unknown spec_dtype */
+  SPEC_ERR_WORKSPACE = 3,   /* workspace NULL or smaller than spec_workspace_bytes() */
+  SPEC_ERR_CUDA = 6         /* a kernel launch failed (cudaGetLastError after launch) */
+} spec_status;
+
+/* bits of *device_status */
+#define SPEC_DEV_TOKEN_RANGE 1u /* a draft or node token outside [0, V) ([PD] section 4.1: token ids must agree) */
+#define SPEC_DEV_NONFINITE 2u   /* a NaN or infinite logit in a row the sequence uses */
+#define SPEC_DEV_OFFSETS 4u     /* cu_draft not non-decreasing from 0 to total_draft, or a gamma_b > gamma */
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
+
+/* which call a workspace is sized for */
+typedef enum { SPEC_MODE_STOCHASTIC = 0, SPEC_MODE_GREEDY = 1, SPEC_MODE_NKL = 2 } spec_mode;
+
+#define SPEC_MAX_GAMMA 128    /* largest gamma_b */
+#define SPEC_MAX_TREE_NODES 64
+
+/* Batch geometry, passed by value. */
+typedef struct {
+  int32_t B;               /* sequences, >= 0 (0 = nothing to do) */
+  int32_t gamma;           /* dense: drafts per sequence; packed: an upper bound on every gamma_b; 0..SPEC_MAX_GAMMA */
+  int32_t V;               /* vocabulary size, >= 1 */
+  int32_t total_draft;     /* sum of gamma_b (dense: B * gamma); must equal cu_draft[B] */
+  const int32_t* cu_draft; /* device [B+1], non-decreasing prefix sums of gamma_b; NULL = dense */
+} spec_batch;
+
+/* Bytes of scratch memory a call of `mode` needs for geometry g (dtype-independent). */
+size_t spec_workspace_bytes(spec_batch g, spec_mode mode);
+
+/* Bytes of scratch memory spec_verify_tree needs. */
+size_t spec_tree_workspace_bytes(int32_t B, int32_t N, int32_t V);
+
+/*
+ * Stochastic verification with residual resampling and a bonus token ([SpS]), with the
+ * per-position NKL of [CoD] 3.2 and the greedy decision of [MTP] 2.3 from the same read.
+ *
+ * For each sequence b and position i < gamma_b, with p = softmax(target row i / T) and
+ * q = softmax(draft row i / T), x_i = draft_tokens[i]:
+ *   alpha_i = min(1, p(x_i) / q(x_i)); draft i is accepted iff u_accept[i] <= alpha_i;
+ *   n = the first i not accepted, else gamma_b;
+ *   if n < gamma_b the last token is the smallest y with C(y) > u_sample[b] * Z, C the
+ *   running sum in token order of max(0, p - q) over row pair n and Z its total;
+ *   if n == gamma_b the same rule over p of target row gamma_b (the bonus token).
+ *   (Z == 0 at a rejection, reachable only through rounding: the row p is used instead.)
+ *
+ *   target_logits [total_draft + B, V], draft_logits [total_draft, V], draft_tokens
+ *   [total_draft] int32, u_accept [total_draft] fp32 in [0,1), u_sample [B] fp32 in [0,1),
+ *   temperature: finite, > 0, applied to both rows.
+ * Outputs (caller-allocated):
+ *   n_accepted [B]                     required: n per sequence (-1 on a data error)
+ *   out_tokens [total_draft + B]       required: per sequence x_0..x_{n-1}, then the
+ *                                      correction or bonus token, then -1 up to gamma_b
+ *   p_x, q_x, alpha [total_draft]      optional (NULL skips): p(x_i), q(x_i), alpha_i
+ *   nkl [total_draft], nkl_mask [total_draft]  optional: KL(q||p)/ln V and (nkl < nkl_delta)
+ *   greedy_n [B], greedy_tokens [total_draft + B]  optional: the greedy decision on the
+ *                                      same target rows (argmax of the raw logits, ties to
+ *                                      the lowest id), laid out like n_accepted / out_tokens
+ *   device_status [1]                  required, sticky (see above)
+ */
+spec_status spec_verify_stochastic(spec_batch g, spec_dtype dtype, const void* target_logits,
+                                   const void* draft_logits, const int32_t* draft_tokens,
+                                   float temperature, const float* u_accept, const float* u_sample,
+                                   int32_t* n_accepted, int32_t* out_tokens, float* p_x, float* q_x,
+                                   float* alpha, float* nkl, uint8_t* nkl_mask, float nkl_delta,
+                                   int32_t* greedy_n, int32_t* greedy_tokens, uint32_t* device_status,
+                                   void* workspace, size_t workspace_bytes, spec_stream_t stream);
+
+/*
+ * Greedy argmax-match verification ([MTP] 2.3): g_i = argmax of target row i (raw logits,
+ * ties to the lowest id); n = the first i with draft_tokens[i] != g_i, else gamma_b;
+ * out = x_0..x_{n-1}, g_n, then -1 up to gamma_b. Reads the target rows only.
+ *   target_logits [total_draft + B, V], draft_tokens [total_draft];
+ *   n_accepted [B], out_tokens [total_draft + B], device_status [1].
+ */
+spec_status spec_verify_greedy(spec_batch g, spec_dtype dtype, const void* target_logits,
+                               const int32_t* draft_tokens, int32_t* n_accepted, int32_t* out_tokens,
+                               uint32_t* device_status, void* workspace, size_t workspace_bytes,
+                               spec_stream_t stream);
+
+/*
+ * Greedy tree verification ([PD] 2.2). Every sequence carries the same tree of N nodes.
+ *   parent: HOST [N], parent[j] in {-1, 0..j-1} (-1 = a root); 1 <= N <= SPEC_MAX_TREE_NODES.
+ *   target_logits [B * (N + 1), V]: row 0 of a sequence scores the position before the
+ *   tree, row j+1 scores the position after node j. node_tokens [B, N] int32.
+ * Node j is accepted iff node_tokens[j] equals the argmax of its parent's row (row 0 for a
+ * root) and its parent is accepted. The pick is the accepted node of greatest depth (ties
+ * to the lowest node index). With D = spec_tree_depth(parent, N):
+ *   accept_len [B]           depth of the pick (0 if no node is accepted)
+ *   path_nodes [B, D]        node indices from the root to the pick, then -1
+ *   out_tokens [B, D + 1]    the path's tokens, then the argmax of the pick's row (of row 0
+ *                            if none), then -1
+ * A data error gives accept_len = -1 and -1 everywhere in that sequence's outputs.
+ */
+spec_status spec_verify_tree(int32_t B, int32_t N, int32_t V, spec_dtype dtype, const void* target_logits,
+                             const int32_t* node_tokens, const int32_t* parent, int32_t* accept_len,
+                             int32_t* path_nodes, int32_t* out_tokens, uint32_t* device_status,
+                             void* workspace, size_t workspace_bytes, spec_stream_t stream);
+
+/* Depth of the tree described by the HOST array parent[N] (a root has depth 1); -1 if the
+ * array is not a valid topologically ordered forest or N is out of range. */
+int32_t spec_tree_depth(const int32_t* parent, int32_t N);
+
+/*
+ * NKL alone ([CoD] 3.2) for every (target row i, draft row i), i < gamma_b:
+ *   nkl[i] = KL(q || p) / ln V with q = softmax(draft/T), p = softmax(target/T), natural log,
+ *   unclamped; nkl_mask[i] = (nkl[i] < delta), optional (NULL skips).
+ * Layout as spec_verify_stochastic (target row i of sequence b at cu_draft[b] + b + i).
+ * A non-finite logit in a row pair gives NaN / 0 for that pair only.
+ */
+spec_status spec_nkl(spec_batch g, spec_dtype dtype, const void* target_logits, const void* draft_logits,
+                     float temperature, float delta, float* nkl, uint8_t* nkl_mask,
+                     uint32_t* device_status, void* workspace, size_t workspace_bytes,
+                     spec_stream_t stream);
+
+/* A static English description of a spec_status value. */
+const char* spec_status_str(spec_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

@@ -1,0 +1,94 @@
+"""ctypes view of the C ABI in include/spec_verify.h (libspecverify.so).
+
+Loading fails loudly when the shared library has not been built: there is no
+other implementation behind these calls."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+from .build import INCLUDE, LIB
+
+SPEC_OK = 0
+SPEC_ERR_INVALID_ARG = 1
+SPEC_ERR_DTYPE = 2
+SPEC_ERR_WORKSPACE = 3
+SPEC_ERR_CUDA = 6
+
+SPEC_DEV_TOKEN_RANGE = 1
+SPEC_DEV_NONFINITE = 2
+SPEC_DEV_OFFSETS = 4
+
+SPEC_F32 = 0
+SPEC_BF16 = 1
+
+SPEC_MODE_STOCHASTIC = 0
+SPEC_MODE_GREEDY = 1
+SPEC_MODE_NKL = 2
+
+SPEC_MAX_GAMMA = 128
+SPEC_MAX_TREE_NODES = 64
+
+
+class SpecBatch(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("gamma", ctypes.c_int32), ("V", ctypes.c_int32),
+                ("total_draft", ctypes.c_int32), ("cu_draft", ctypes.c_void_p)]
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int32
+_F = ctypes.c_float
+_S = ctypes.c_size_t
+
+SIGNATURES = {
+    "spec_workspace_bytes": (_S, [SpecBatch, ctypes.c_int]),
+    "spec_tree_workspace_bytes": (_S, [_I, _I, _I]),
+    "spec_tree_depth": (_I, [_P, _I]),
+    "spec_verify_stochastic": (ctypes.c_int, [SpecBatch, ctypes.c_int, _P, _P, _P, _F, _P, _P, _P, _P, _P, _P, _P,
+                                              _P, _P, _F, _P, _P, _P, _P, _S, _P]),
+    "spec_verify_greedy": (ctypes.c_int, [SpecBatch, ctypes.c_int, _P, _P, _P, _P, _P, _P, _S, _P]),
+    "spec_verify_tree": (ctypes.c_int, [_I, _I, _I, ctypes.c_int, _P, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
+    "spec_nkl": (ctypes.c_int, [SpecBatch, ctypes.c_int, _P, _P, _F, _F, _P, _P, _P, _P, _S, _P]),
+    "spec_status_str": (ctypes.c_char_p, [ctypes.c_int]),
+}
+
+_LIB = None
+
+
+def declared_functions() -> list:
+    """Names of the functions include/spec_verify.h declares."""
+    with open(os.path.join(INCLUDE, "spec_verify.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_[a-z_]+)\s*\(", text)))
+
+
+def lib() -> ctypes.CDLL:
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB):
+            raise RuntimeError(f"{LIB} is missing: build the CUDA library first "
+                               "(python -c 'import __graft_entry__ as g; g.build()')")
+        handle = ctypes.CDLL(LIB)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = handle
+    return _LIB
+
+
+def status_str(code: int) -> str:
+    return lib().spec_status_str(code).decode()
+
+
+class SpecError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} returned {code} ({status_str(code)})")
+        self.code = code
+
+
+def check(fn: str, code: int) -> None:
+    if code != SPEC_OK:
+        raise SpecError(fn, code)

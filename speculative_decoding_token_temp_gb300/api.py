@@ -1,0 +1,254 @@
+"""Torch-facing binding of the C ABI: the same four calls under the same names.
+
+Each function checks dtype, device, contiguity and shapes, allocates the outputs
+(unless `out=` passes them in) and the scratch workspace, and calls the C entry
+point on the current CUDA stream with the tensors' data pointers. Every step of
+the verification itself runs in the CUDA kernels of libspecverify.so.
+
+Logits are torch.bfloat16 or torch.float32 tensors on a CUDA device, shaped
+[rows, V] (packed layout, see include/spec_verify.h) or, for dense batches,
+[B, gamma+1, V] / [B, gamma, V]."""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import SpecBatch, check
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return _lib.SPEC_BF16
+    if t.dtype == torch.float32:
+        return _lib.SPEC_F32
+    raise TypeError(f"logits must be bfloat16 or float32, got {t.dtype}")
+
+
+def _need(t: torch.Tensor, name: str, dtype=None, numel=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name} must have {numel} elements, got {t.numel()}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+class Workspace:
+    """Device scratch buffer reused across calls (grown on demand)."""
+
+    def __init__(self):
+        self.buf = None
+
+    def get(self, nbytes: int, device) -> torch.Tensor:
+        nbytes = max(int(nbytes), 256)
+        if self.buf is None or self.buf.numel() < nbytes or self.buf.device != device:
+            self.buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        return self.buf
+
+
+_DEFAULT_WS = {}
+
+
+def _workspace(ws, nbytes, device):
+    if isinstance(ws, torch.Tensor):
+        if ws.numel() < nbytes:
+            raise ValueError(f"workspace has {ws.numel()} bytes, needs {nbytes}")
+        return ws
+    if ws is None:
+        ws = _DEFAULT_WS.setdefault((device.type, device.index), Workspace())
+    return ws.get(nbytes, device)
+
+
+def _geometry(target, draft_rows_or_tokens, cu_draft, gamma, has_bonus=True):
+    """(B, gamma_max, V, total_draft, cu pointer, 2-D target view)."""
+    V = target.shape[-1]
+    if cu_draft is None:
+        if target.dim() == 3:
+            B = target.shape[0]
+            g = target.shape[1] - (1 if has_bonus else 0)
+        else:
+            if gamma is None:
+                raise ValueError("a 2-D dense target needs gamma")
+            g = int(gamma)
+            rows = target.shape[0]
+            B = rows // (g + 1) if has_bonus else rows // max(g, 1)
+        total = B * g
+        return B, g, V, total, None
+    _need(cu_draft, "cu_draft", torch.int32, device=target.device)
+    B = cu_draft.numel() - 1
+    if gamma is None:
+        raise ValueError("packed batches need gamma (an upper bound on every gamma_b)")
+    total = int(draft_rows_or_tokens.numel()) if draft_rows_or_tokens is not None else None
+    return B, int(gamma), V, total, cu_draft
+
+
+def spec_workspace_bytes(B: int, gamma: int, V: int, total_draft: int, mode: int, packed: bool = False) -> int:
+    g = SpecBatch(B, gamma, V, total_draft, ctypes.c_void_p(1) if packed else None)
+    return int(_lib.lib().spec_workspace_bytes(g, mode))
+
+
+def spec_verify_stochastic(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torch.Tensor,
+                           temperature: float, u_accept: torch.Tensor, u_sample: torch.Tensor, *,
+                           cu_draft: torch.Tensor | None = None, gamma: int | None = None,
+                           nkl_delta: float = 0.15, want_probs: bool = True, want_nkl: bool = True,
+                           want_greedy: bool = True, out: dict | None = None, workspace=None,
+                           device_status: torch.Tensor | None = None) -> dict:
+    """Stochastic verification with residual / bonus resampling; see spec_verify.h.
+
+    Returns a dict of device tensors: n_accepted [B], out_tokens [total_draft+B] (dense:
+    [B, gamma+1]), and optionally p_x, q_x, alpha, nkl, nkl_mask, greedy_n,
+    greedy_tokens, plus device_status [1] (sticky error bits)."""
+    dt = _dtype_code(target)
+    dev = target.device
+    B, g, V, total, cu = _geometry(target, draft_tokens, cu_draft, gamma)
+    rows = total + B
+    _need(target, "target", target.dtype, rows * V, dev)
+    if total > 0:
+        _need(draft, "draft", target.dtype, total * V, dev)
+    _need(draft_tokens, "draft_tokens", torch.int32, total, dev)
+    _need(u_accept, "u_accept", torch.float32, total, dev)
+    _need(u_sample, "u_sample", torch.float32, B, dev)
+    o = {} if out is None else out
+
+    def get(name, n, dtype):
+        t = o.get(name)
+        if t is None:
+            t = torch.empty(n, dtype=dtype, device=dev)
+            o[name] = t
+        _need(t, name, dtype, n, dev)
+        return t
+
+    n_acc = get("n_accepted", B, torch.int32)
+    out_tok = get("out_tokens", rows, torch.int32)
+    p_x = get("p_x", total, torch.float32) if want_probs else None
+    q_x = get("q_x", total, torch.float32) if want_probs else None
+    alpha = get("alpha", total, torch.float32) if want_probs else None
+    nkl = get("nkl", total, torch.float32) if want_nkl else None
+    mask = get("nkl_mask", total, torch.uint8) if want_nkl else None
+    g_n = get("greedy_n", B, torch.int32) if want_greedy else None
+    g_tok = get("greedy_tokens", rows, torch.int32) if want_greedy else None
+    if device_status is None:
+        device_status = o.get("device_status")
+        if device_status is None:
+            device_status = torch.zeros(1, dtype=torch.int32, device=dev)
+    o["device_status"] = device_status
+    gb = SpecBatch(B, g, V, total, _ptr(cu))
+    nbytes = int(_lib.lib().spec_workspace_bytes(gb, _lib.SPEC_MODE_STOCHASTIC))
+    ws = _workspace(workspace, nbytes, dev)
+    code = _lib.lib().spec_verify_stochastic(
+        gb, dt, _ptr(target), _ptr(draft) if total > 0 else None, _ptr(draft_tokens), float(temperature),
+        _ptr(u_accept), _ptr(u_sample), _ptr(n_acc), _ptr(out_tok), _ptr(p_x), _ptr(q_x), _ptr(alpha),
+        _ptr(nkl), _ptr(mask), float(nkl_delta), _ptr(g_n), _ptr(g_tok), _ptr(device_status), _ptr(ws),
+        ws.numel(), _stream(dev))
+    check("spec_verify_stochastic", code)
+    return o
+
+
+def spec_verify_greedy(target: torch.Tensor, draft_tokens: torch.Tensor, *, cu_draft=None, gamma=None,
+                       out: dict | None = None, workspace=None, device_status=None) -> dict:
+    """Greedy argmax-match verification; returns n_accepted [B], out_tokens [total_draft+B]."""
+    dt = _dtype_code(target)
+    dev = target.device
+    B, g, V, total, cu = _geometry(target, draft_tokens, cu_draft, gamma)
+    rows = total + B
+    _need(target, "target", target.dtype, rows * V, dev)
+    _need(draft_tokens, "draft_tokens", torch.int32, total, dev)
+    o = {} if out is None else out
+    n_acc = o.setdefault("n_accepted", torch.empty(B, dtype=torch.int32, device=dev))
+    out_tok = o.setdefault("out_tokens", torch.empty(rows, dtype=torch.int32, device=dev))
+    _need(n_acc, "n_accepted", torch.int32, B, dev)
+    _need(out_tok, "out_tokens", torch.int32, rows, dev)
+    if device_status is None:
+        device_status = o.get("device_status")
+        if device_status is None:
+            device_status = torch.zeros(1, dtype=torch.int32, device=dev)
+    o["device_status"] = device_status
+    gb = SpecBatch(B, g, V, total, _ptr(cu))
+    nbytes = int(_lib.lib().spec_workspace_bytes(gb, _lib.SPEC_MODE_GREEDY))
+    ws = _workspace(workspace, nbytes, dev)
+    code = _lib.lib().spec_verify_greedy(gb, dt, _ptr(target), _ptr(draft_tokens), _ptr(n_acc), _ptr(out_tok),
+                                         _ptr(device_status), _ptr(ws), ws.numel(), _stream(dev))
+    check("spec_verify_greedy", code)
+    return o
+
+
+def spec_tree_depth(parent) -> int:
+    arr = (ctypes.c_int32 * len(parent))(*[int(x) for x in parent])
+    return int(_lib.lib().spec_tree_depth(ctypes.cast(arr, ctypes.c_void_p), len(parent)))
+
+
+def spec_verify_tree(target: torch.Tensor, node_tokens: torch.Tensor, parent, *, out: dict | None = None,
+                     workspace=None, device_status=None) -> dict:
+    """Greedy tree verification. target [B*(N+1), V] or [B, N+1, V]; node_tokens [B, N] int32;
+    parent: host sequence of N ints. Returns accept_len [B], path_nodes [B, D], out_tokens [B, D+1]."""
+    dt = _dtype_code(target)
+    dev = target.device
+    N = len(parent)
+    D = spec_tree_depth(parent)
+    if D < 1:
+        raise ValueError("parent must be a topologically ordered forest of 1..64 nodes")
+    B = node_tokens.shape[0] if node_tokens.dim() == 2 else node_tokens.numel() // max(N, 1)
+    V = target.shape[-1]
+    _need(target, "target", target.dtype, B * (N + 1) * V, dev)
+    _need(node_tokens, "node_tokens", torch.int32, B * N, dev)
+    o = {} if out is None else out
+    acc = o.setdefault("accept_len", torch.empty(B, dtype=torch.int32, device=dev))
+    path = o.setdefault("path_nodes", torch.empty(B, D, dtype=torch.int32, device=dev))
+    tok = o.setdefault("out_tokens", torch.empty(B, D + 1, dtype=torch.int32, device=dev))
+    if device_status is None:
+        device_status = o.get("device_status")
+        if device_status is None:
+            device_status = torch.zeros(1, dtype=torch.int32, device=dev)
+    o["device_status"] = device_status
+    nbytes = int(_lib.lib().spec_tree_workspace_bytes(B, N, V))
+    ws = _workspace(workspace, nbytes, dev)
+    par = (ctypes.c_int32 * N)(*[int(x) for x in parent])
+    code = _lib.lib().spec_verify_tree(B, N, V, dt, _ptr(target), _ptr(node_tokens),
+                                       ctypes.cast(par, ctypes.c_void_p), _ptr(acc), _ptr(path), _ptr(tok),
+                                       _ptr(device_status), _ptr(ws), ws.numel(), _stream(dev))
+    check("spec_verify_tree", code)
+    return o
+
+
+def spec_nkl(target: torch.Tensor, draft: torch.Tensor, temperature: float, *, cu_draft=None, gamma=None,
+             delta: float = 0.15, want_mask: bool = True, out: dict | None = None, workspace=None,
+             device_status=None) -> dict:
+    """NKL = KL(q||p)/ln V per (target row i, draft row i); returns nkl [total_draft], nkl_mask."""
+    dt = _dtype_code(target)
+    dev = target.device
+    B, g, V, total, cu = _geometry(target, draft, cu_draft, gamma)
+    if cu is not None:
+        total = draft.numel() // V
+    _need(target, "target", target.dtype, (total + B) * V, dev)
+    _need(draft, "draft", target.dtype, total * V, dev)
+    o = {} if out is None else out
+    nkl = o.setdefault("nkl", torch.empty(total, dtype=torch.float32, device=dev))
+    mask = o.setdefault("nkl_mask", torch.empty(total, dtype=torch.uint8, device=dev)) if want_mask else None
+    if device_status is None:
+        device_status = o.get("device_status")
+        if device_status is None:
+            device_status = torch.zeros(1, dtype=torch.int32, device=dev)
+    o["device_status"] = device_status
+    gb = SpecBatch(B, g, V, total, _ptr(cu))
+    nbytes = int(_lib.lib().spec_workspace_bytes(gb, _lib.SPEC_MODE_NKL))
+    ws = _workspace(workspace, nbytes, dev)
+    code = _lib.lib().spec_nkl(gb, dt, _ptr(target), _ptr(draft), float(temperature), float(delta), _ptr(nkl),
+                               _ptr(mask), _ptr(device_status), _ptr(ws), ws.numel(), _stream(dev))
+    check("spec_nkl", code)
+    return o

@@ -1,0 +1,470 @@
+// Device code of the draft-token verification library (sm_103a).
+//
+// Pipeline of one call (all on the caller's stream):
+//   prologue_kernel  zeroes the per-sequence tickets, marks every sequence "pending",
+//                    checks packed offsets.
+//   rows_kernel      one block per (row, vocabulary chunk) tile. Streams the target row
+//                    (and, for a pair, the draft row) once with 16-byte read-only loads
+//                    and keeps per-thread online statistics: the raw maximum and its
+//                    lowest index, sum_v exp((z_v - max)/T), and for the draft row also
+//                    sum_v exp((zd_v - max_d)/T) (zd_v - zt_v). Block-reduces them into a
+//                    32-byte partial. The last tile of a sequence to finish (an atomic
+//                    ticket, no waiting) merges the partials of all its rows and applies
+//                    the acceptance rule, NKL, greedy or tree decision.
+//   sample_kernel    (stochastic only) one block per (vocabulary segment, sequence):
+//                    masses of the residual max(0, p - q) (or of p for the bonus row) on
+//                    the one row pair the sequence needs; the last segment's block finds
+//                    the inverse-CDF crossing by re-reading one segment and one 256-token
+//                    step.
+// Launches after the first use programmatic dependent launch so that a kernel's
+// blocks are resident before its predecessor drains; griddepcontrol.wait guards every
+// read of the predecessor's results.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "spec_verify.h"
+
+namespace sv {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kMaxRows = SPEC_MAX_GAMMA + 1;
+constexpr int kMaxSteps = 64;        // 256-token steps per warp in one sampling segment
+constexpr int kSegElems = 16384;     // largest sampling segment (kWarps * kMaxSteps * 32 scalar loads)
+constexpr int kTargetTiles = 1216;   // 152 SMs x 8 resident blocks: enough tiles to fill the GPU
+
+enum Mode : int { M_STOCH = 0, M_GREEDY = 1, M_NKL = 2, M_TREE = 3 };
+enum Kind : int { K_PAIR = 0, K_TSUM = 1, K_ARGMAX = 2 };
+enum SampleMode : int { S_RESID = 0, S_P = 1 };
+enum RecState : int { REC_READY = 0, REC_SKIP = 1, REC_PENDING = 2 };
+
+// Per-tile partial statistics (32 bytes).
+struct __align__(16) Partial {
+  float tm, ts;   // target raw max, sum exp2((z - tm) * c)
+  int tidx, bad;  // lowest index of the target max, non-finite seen
+  float dm, ds;   // draft raw max, sum exp2((zd - dm) * c)
+  float dk;       // sum exp2((zd - dm) * c) * (zd - zt)
+  int pad;
+};
+
+// What the sampler needs for one sequence (32 bytes).
+struct __align__(16) SeqRec {
+  int state, n, t_row, d_row;
+  float lt2, ld2;  // log2 normalisers: p_v = exp2(zt_v * c - lt2), q_v = exp2(zd_v * c - ld2)
+  float us;
+  int mode;
+};
+
+struct RowsParams {
+  const void* target;
+  const void* draft;
+  const int32_t* tokens;
+  const float* u_accept;
+  const float* u_sample;
+  const int32_t* cu;
+  const int32_t* node_tokens;
+  int B, V, gamma, total_draft, total_rows, nchunks, chunk_elems, N;
+  float c, invT, delta, pad0;
+  double inv_lnV;
+  int32_t* n_acc;
+  int32_t* out_tok;
+  float* p_x;
+  float* q_x;
+  float* alpha;
+  float* nkl;
+  uint8_t* mask;
+  int32_t* g_n;
+  int32_t* g_tok;
+  int32_t* accept_len;
+  int32_t* path_nodes;
+  uint32_t* status;
+  Partial* part;
+  unsigned* cnt;
+  SeqRec* rec;
+  int depth;
+  int8_t parent[SPEC_MAX_TREE_NODES];
+};
+
+struct SampleParams {
+  const void* target;
+  const void* draft;
+  int V, total_rows, total_draft, B, nseg, seg_elems;
+  float c;
+  const SeqRec* rec;
+  double* segtot;
+  unsigned* cnt;
+  int32_t* out_tok;
+  uint32_t* status;
+};
+
+struct ProParams {
+  const int32_t* cu;
+  int B, gamma, total_draft;
+  unsigned* cntA;
+  unsigned* cntB;
+  SeqRec* rec;
+  uint32_t* status;
+};
+
+// ---------------------------------------------------------------------------
+// small helpers
+
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) x = fmaxf(x, __shfl_xor_sync(kFull, x, o));
+  return x;
+}
+__device__ __forceinline__ float warp_max_nan(float x) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) x = max_nan(x, __shfl_xor_sync(kFull, x, o));
+  return x;
+}
+__device__ __forceinline__ float warp_min(float x) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) x = fminf(x, __shfl_xor_sync(kFull, x, o));
+  return x;
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
+  return x;
+}
+__device__ __forceinline__ int warp_min_i(int x) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) x = min(x, __shfl_xor_sync(kFull, x, o));
+  return x;
+}
+
+// s was accumulated relative to max m; express it relative to M >= m.
+__device__ __forceinline__ float rescale(float s, float m, float M, float c) {
+  return (m == -INFINITY) ? s * 0.f : s * ex2((m - M) * c);
+}
+
+// ---------------------------------------------------------------------------
+// element access: E = uint16_t (bf16 bit patterns) or float; VEC elements per load
+
+template <typename E, int VEC>
+struct IO;
+
+template <>
+struct IO<uint16_t, 8> {
+  using raw_t = uint4;
+  __device__ static raw_t load(const uint16_t* row, int v) { return ld_stream16(row + (size_t)v * 8); }
+  __device__ static void unpack(const raw_t& r, float (&f)[8]) {
+    f[0] = __uint_as_float(r.x << 16);
+    f[1] = __uint_as_float(r.x & 0xffff0000u);
+    f[2] = __uint_as_float(r.y << 16);
+    f[3] = __uint_as_float(r.y & 0xffff0000u);
+    f[4] = __uint_as_float(r.z << 16);
+    f[5] = __uint_as_float(r.z & 0xffff0000u);
+    f[6] = __uint_as_float(r.w << 16);
+    f[7] = __uint_as_float(r.w & 0xffff0000u);
+  }
+};
+
+template <>
+struct IO<float, 4> {
+  using raw_t = uint4;
+  __device__ static raw_t load(const float* row, int v) { return ld_stream16(row + (size_t)v * 4); }
+  __device__ static void unpack(const raw_t& r, float (&f)[4]) {
+    f[0] = __uint_as_float(r.x);
+    f[1] = __uint_as_float(r.y);
+    f[2] = __uint_as_float(r.z);
+    f[3] = __uint_as_float(r.w);
+  }
+};
+
+template <>
+struct IO<uint16_t, 1> {
+  using raw_t = unsigned short;
+  __device__ static raw_t load(const uint16_t* row, int v) { return __ldg(reinterpret_cast<const unsigned short*>(row) + v); }
+  __device__ static void unpack(const raw_t& r, float (&f)[1]) { f[0] = __uint_as_float(((unsigned)r) << 16); }
+};
+
+template <>
+struct IO<float, 1> {
+  using raw_t = float;
+  __device__ static raw_t load(const float* row, int v) { return __ldg(row + v); }
+  __device__ static void unpack(const raw_t& r, float (&f)[1]) { f[0] = r; }
+};
+
+template <typename E>
+__device__ __forceinline__ float elem_at(const E* row, int x);
+template <>
+__device__ __forceinline__ float elem_at<uint16_t>(const uint16_t* row, int x) {
+  return __uint_as_float(((unsigned)__ldg(reinterpret_cast<const unsigned short*>(row) + x)) << 16);
+}
+template <>
+__device__ __forceinline__ float elem_at<float>(const float* row, int x) {
+  return __ldg(row + x);
+}
+
+// ---------------------------------------------------------------------------
+// per-thread online statistics
+
+struct TAcc {
+  float m, s, nmc, lo, hi;
+  int idx;
+};
+struct DAcc {
+  float m, s, k, nmc;
+};
+
+__device__ __forceinline__ void init(TAcc& a) {
+  a.m = -INFINITY; a.s = 0.f; a.nmc = 0.f; a.lo = INFINITY; a.hi = -INFINITY; a.idx = INT_MAX;
+}
+__device__ __forceinline__ void init(DAcc& a) { a.m = -INFINITY; a.s = 0.f; a.k = 0.f; a.nmc = 0.f; }
+
+template <int VEC>
+__device__ __forceinline__ float tree_sum(const float (&e)[VEC]) {
+  if constexpr (VEC == 1) {
+    return e[0];
+  } else if constexpr (VEC == 4) {
+    return (e[0] + e[1]) + (e[2] + e[3]);
+  } else {
+    return ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
+  }
+}
+
+template <int VEC>
+__device__ __forceinline__ int lowest_match(const float (&t)[VEC], float v) {
+  int k = VEC - 1;
+#pragma unroll
+  for (int j = VEC - 2; j >= 0; --j)
+    if (t[j] == v) k = j;
+  return k;
+}
+
+// target row with sum (bonus row of the stochastic call); LO tracks the minimum so a
+// -inf entry, which the sum alone cannot see, is still reported
+template <int VEC>
+__device__ __forceinline__ void tsum_update(TAcc& a, const float (&t)[VEC], int e0, float c) {
+  float vm = t[0], vl = t[0];
+#pragma unroll
+  for (int k = 1; k < VEC; ++k) {
+    vm = fmaxf(vm, t[k]);
+    vl = fminf(vl, t[k]);
+  }
+  a.lo = fminf(a.lo, vl);
+  if (vm > a.m) {
+    a.s *= ex2((a.m - vm) * c);
+    a.m = vm;
+    a.nmc = -vm * c;
+    a.idx = e0 + lowest_match<VEC>(t, vm);
+  }
+  float e[VEC];
+#pragma unroll
+  for (int k = 0; k < VEC; ++k) e[k] = ex2(fmaf(t[k], c, a.nmc));
+  a.s += tree_sum<VEC>(e);
+}
+
+// argmax only (greedy and tree rows): no exponentials; hi propagates NaN
+template <int VEC>
+__device__ __forceinline__ void argmax_update(TAcc& a, const float (&t)[VEC], int e0) {
+  float vh = t[0], vl = t[0];
+#pragma unroll
+  for (int k = 1; k < VEC; ++k) {
+    vh = max_nan(vh, t[k]);
+    vl = fminf(vl, t[k]);
+  }
+  a.hi = max_nan(a.hi, vh);
+  a.lo = fminf(a.lo, vl);
+  if (vh > a.m) {
+    a.m = vh;
+    a.idx = e0 + lowest_match<VEC>(t, vh);
+  }
+}
+
+// (target row, draft row) pair; a -inf or NaN in either makes the KL sum non-finite
+template <int VEC, bool IDX>
+__device__ __forceinline__ void pair_update(TAcc& a, DAcc& d, const float (&t)[VEC], const float (&z)[VEC], int e0,
+                                            float c) {
+  float tm = t[0], dm = z[0];
+#pragma unroll
+  for (int k = 1; k < VEC; ++k) {
+    tm = fmaxf(tm, t[k]);
+    dm = fmaxf(dm, z[k]);
+  }
+  if (tm > a.m) {
+    a.s *= ex2((a.m - tm) * c);
+    a.m = tm;
+    a.nmc = -tm * c;
+    if (IDX) a.idx = e0 + lowest_match<VEC>(t, tm);
+  }
+  if (dm > d.m) {
+    const float f = ex2((d.m - dm) * c);
+    d.s *= f;
+    d.k *= f;
+    d.m = dm;
+    d.nmc = -dm * c;
+  }
+  float et[VEC], ed[VEC];
+  float k0 = 0.f, k1 = 0.f;
+#pragma unroll
+  for (int k = 0; k < VEC; ++k) {
+    et[k] = ex2(fmaf(t[k], c, a.nmc));
+    ed[k] = ex2(fmaf(z[k], c, d.nmc));
+    if (k & 1)
+      k1 = fmaf(ed[k], z[k] - t[k], k1);
+    else
+      k0 = fmaf(ed[k], z[k] - t[k], k0);
+  }
+  a.s += tree_sum<VEC>(et);
+  d.s += tree_sum<VEC>(ed);
+  d.k += k0 + k1;
+}
+
+// ---------------------------------------------------------------------------
+// block reduction of a tile into a Partial (valid in thread 0)
+
+__device__ __forceinline__ Partial reduce_tile(int kind, const TAcc& ta, const DAcc& da, float c) {
+  __shared__ float s_m[2][kWarps];
+  __shared__ float s_v[5][kWarps];
+  __shared__ int s_i[kWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const float wtm = warp_max(ta.m);
+  const float wdm = (kind == K_PAIR) ? warp_max(da.m) : -INFINITY;
+  if (lane == 0) {
+    s_m[0][warp] = wtm;
+    s_m[1][warp] = wdm;
+  }
+  __syncthreads();
+  float TM = s_m[0][0], DM = s_m[1][0];
+#pragma unroll
+  for (int w = 1; w < kWarps; ++w) {
+    TM = fmaxf(TM, s_m[0][w]);
+    DM = fmaxf(DM, s_m[1][w]);
+  }
+  const int wi = warp_min_i(ta.m == TM ? ta.idx : INT_MAX);
+  float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f, v4 = 0.f;
+  if (kind == K_ARGMAX) {
+    v0 = warp_max_nan(ta.hi);
+    v1 = warp_min(ta.lo);
+  } else {
+    v0 = warp_sum(rescale(ta.s, ta.m, TM, c));
+    if (kind == K_TSUM) v1 = warp_min(ta.lo);
+    if (kind == K_PAIR) {
+      const float fd = (da.m == -INFINITY) ? 0.f : ex2((da.m - DM) * c);
+      v2 = warp_sum(da.s * fd);
+      v3 = warp_sum(da.k * fd);
+    }
+  }
+  if (lane == 0) {
+    s_v[0][warp] = v0;
+    s_v[1][warp] = v1;
+    s_v[2][warp] = v2;
+    s_v[3][warp] = v3;
+    s_v[4][warp] = v4;
+    s_i[warp] = wi;
+  }
+  __syncthreads();
+  Partial out;
+  out.tm = TM;
+  out.dm = DM;
+  out.pad = 0;
+  out.tidx = INT_MAX;
+  out.ts = out.ds = out.dk = 0.f;
+  out.bad = 0;
+  if (threadIdx.x == 0) {
+    int idx = INT_MAX;
+    float a0 = s_v[0][0], a1 = s_v[1][0], a2 = 0.f, a3 = 0.f;
+    for (int w = 0; w < kWarps; ++w) idx = min(idx, s_i[w]);
+    if (kind == K_ARGMAX) {
+      for (int w = 1; w < kWarps; ++w) {
+        a0 = max_nan(a0, s_v[0][w]);
+        a1 = fminf(a1, s_v[1][w]);
+      }
+      out.bad = (isnan(a0) || a0 == INFINITY || a1 == -INFINITY) ? 1 : 0;
+    } else {
+      a0 = 0.f;
+      for (int w = 0; w < kWarps; ++w) {
+        a0 += s_v[0][w];
+        a2 += s_v[2][w];
+        a3 += s_v[3][w];
+      }
+      out.ts = a0;
+      bool bad = !isfinite(a0) || !isfinite(TM);
+      if (kind == K_TSUM) {
+        for (int w = 1; w < kWarps; ++w) a1 = fminf(a1, s_v[1][w]);
+        bad = bad || a1 == -INFINITY;
+      } else {
+        out.ds = a2;
+        out.dk = a3;
+        bad = bad || !isfinite(a2) || !isfinite(a3) || !isfinite(DM);
+      }
+      out.bad = bad ? 1 : 0;
+    }
+    out.tidx = idx;
+  }
+  return out;
+}
+
+// ---------------------------------------------------------------------------
+// merging the partials of one row (one warp per row)
+
+struct RowStat {
+  float tm, ts, dm, ds, dk;
+  int tidx, bad;
+};
+
+__device__ __forceinline__ RowStat merge_row(const Partial* pp, int nchunks, float c) {
+  const int lane = threadIdx.x & 31;
+  float tm = -INFINITY, ts = 0.f, dm = -INFINITY, ds = 0.f, dk = 0.f;
+  int idx = INT_MAX, bad = 0;
+  for (int ch = lane; ch < nchunks; ch += 32) {
+    const float4 lo = __ldcg(reinterpret_cast<const float4*>(pp + ch));
+    const float4 hi = __ldcg(reinterpret_cast<const float4*>(pp + ch) + 1);
+    const float qtm = lo.x, qts = lo.y;
+    const int qidx = __float_as_int(lo.z), qbad = __float_as_int(lo.w);
+    const float qdm = hi.x, qds = hi.y, qdk = hi.z;
+    bad |= qbad;
+    if (qtm > tm || (qtm == tm && qidx < idx)) idx = qidx;
+    const float M = fmaxf(tm, qtm);
+    ts = rescale(ts, tm, M, c) + rescale(qts, qtm, M, c);
+    tm = M;
+    const float D = fmaxf(dm, qdm);
+    const float f0 = (dm == -INFINITY) ? 0.f : ex2((dm - D) * c);
+    const float f1 = (qdm == -INFINITY) ? 0.f : ex2((qdm - D) * c);
+    ds = ds * f0 + qds * f1;
+    dk = dk * f0 + qdk * f1;
+    dm = D;
+  }
+  RowStat r;
+  r.tm = warp_max(tm);
+  r.tidx = warp_min_i(tm == r.tm ? idx : INT_MAX);
+  r.ts = warp_sum(rescale(ts, tm, r.tm, c));
+  r.dm = warp_max(dm);
+  const float fd = (dm == -INFINITY) ? 0.f : ex2((dm - r.dm) * c);
+  r.ds = warp_sum(ds * fd);
+  r.dk = warp_sum(dk * fd);
+  r.bad = __any_sync(kFull, bad) ? 1 : 0;
+  return r;
+}
+
+}  // namespace sv

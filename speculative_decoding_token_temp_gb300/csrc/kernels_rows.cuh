@@ -1,0 +1,359 @@
+// Tile kernel and per-sequence finalisation (see kernels.cuh for the pipeline).
+#pragma once
+
+#include "kernels.cuh"
+
+namespace sv {
+
+__global__ void prologue_kernel(const __grid_constant__ ProParams p) {
+  griddep_launch();
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= p.B) return;
+  p.cntA[b] = 0u;
+  p.cntB[b] = 0u;
+  SeqRec q;
+  q.state = REC_PENDING;
+  q.n = -1;
+  q.t_row = -1;
+  q.d_row = -1;
+  q.lt2 = 0.f;
+  q.ld2 = 0.f;
+  q.us = 0.f;
+  q.mode = 0;
+  p.rec[b] = q;
+  if (p.cu != nullptr) {
+    const int c0 = __ldg(p.cu + b), c1 = __ldg(p.cu + b + 1);
+    const bool bad = c1 < c0 || c1 - c0 > p.gamma || c0 < 0 || c1 > p.total_draft || (b == 0 && c0 != 0) ||
+                     (b == p.B - 1 && c1 != p.total_draft);
+    if (bad) atomicOr(p.status, SPEC_DEV_OFFSETS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// finalisation, run by the last tile of a sequence
+
+template <typename E, int MODE>
+__device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int row0, int c0) {
+  constexpr int HB = (MODE == M_NKL) ? 0 : 1;
+  __shared__ RowStat rs[kMaxRows];
+  __shared__ int s_n, s_gn;
+  __shared__ unsigned s_err;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int R = gb + HB;
+  const float c = p.c;
+  const size_t V = (size_t)p.V;
+  if (tid == 0) {
+    s_n = gb;
+    s_gn = gb;
+    s_err = 0u;
+  }
+  for (int i = warp; i < R; i += kWarps) {
+    const RowStat r = merge_row(p.part + (size_t)(row0 + i) * p.nchunks, p.nchunks, c);
+    if (lane == 0) rs[i] = r;
+  }
+  __syncthreads();
+
+  const int tb = c0 + b * HB;  // first target row of the sequence (NKL: c0 + b, set below)
+  const int db = c0;           // first draft row / token / u_accept entry
+  const E* target = static_cast<const E*>(p.target);
+  const E* draft = static_cast<const E*>(p.draft);
+
+  if constexpr (MODE == M_TREE) {
+    // one thread walks the (at most 64-node) tree
+    if (tid == 0) {
+      const int N = p.N, D = p.depth;
+      const int32_t* tok = p.node_tokens + (size_t)b * N;
+      unsigned err = 0u;
+      for (int r = 0; r <= N; ++r)
+        if (rs[r].bad) err |= SPEC_DEV_NONFINITE;
+      for (int j = 0; j < N; ++j) {
+        const int x = tok[j];
+        if (x < 0 || x >= p.V) err |= SPEC_DEV_TOKEN_RANGE;
+      }
+      int32_t* path = p.path_nodes + (size_t)b * D;
+      int32_t* out = p.out_tok + (size_t)b * (D + 1);
+      if (err) {
+        atomicOr(p.status, err);
+        p.accept_len[b] = -1;
+        for (int k = 0; k < D; ++k) path[k] = -1;
+        for (int k = 0; k <= D; ++k) out[k] = -1;
+        return;
+      }
+      unsigned long long ok = 0ull;
+      int depth[SPEC_MAX_TREE_NODES];
+      int pick = -1, best = 0;
+      for (int j = 0; j < N; ++j) {
+        const int pj = p.parent[j];
+        depth[j] = (pj < 0) ? 1 : depth[pj] + 1;
+        const int prow = (pj < 0) ? 0 : pj + 1;
+        const bool acc = tok[j] == rs[prow].tidx && (pj < 0 || ((ok >> pj) & 1ull));
+        if (acc) {
+          ok |= 1ull << j;
+          if (depth[j] > best) {
+            best = depth[j];
+            pick = j;
+          }
+        }
+      }
+      p.accept_len[b] = best;
+      int k = pick;
+      for (int d = best - 1; d >= 0; --d) {
+        path[d] = k;
+        out[d] = tok[k];
+        k = p.parent[k];
+      }
+      for (int d = best; d < D; ++d) path[d] = -1;
+      out[best] = rs[pick + 1].tidx;  // pick == -1 gives row 0
+      for (int d = best + 1; d <= D; ++d) out[d] = -1;
+    }
+    return;
+  } else if constexpr (MODE == M_NKL) {
+    const int tbn = c0 + b;
+    for (int i = tid; i < gb; i += kThreads) {
+      const RowStat r = rs[i];
+      float v = __int_as_float(0x7fc00000);
+      uint8_t m = 0;
+      if (r.bad) {
+        atomicOr(p.status, SPEC_DEV_NONFINITE);
+      } else {
+        const double kl = ((double)r.dk / (double)r.ds - ((double)r.dm - (double)r.tm)) * (double)p.invT -
+                          (log((double)r.ds) - log((double)r.ts));
+        v = (float)(kl * p.inv_lnV);
+        m = v < p.delta ? 1 : 0;
+      }
+      p.nkl[db + i] = v;
+      if (p.mask) p.mask[db + i] = m;
+    }
+    (void)tbn;
+    return;
+  } else {
+  // stochastic and greedy: validate the sequence first
+  for (int i = tid; i < R; i += kThreads) {
+    unsigned e = rs[i].bad ? SPEC_DEV_NONFINITE : 0u;
+    if (i < gb) {
+      const int x = p.tokens[db + i];
+      if (x < 0 || x >= p.V) e |= SPEC_DEV_TOKEN_RANGE;
+    }
+    if (e) atomicOr(&s_err, e);
+  }
+  __syncthreads();
+  if (s_err) {
+    if (tid == 0) atomicOr(p.status, s_err);
+    for (int k = tid; k <= gb; k += kThreads) {
+      p.out_tok[tb + k] = -1;
+      if (MODE == M_STOCH && p.g_tok) p.g_tok[tb + k] = -1;
+      if (MODE == M_STOCH && k < gb) {
+        const float qnan = __int_as_float(0x7fc00000);
+        if (p.p_x) p.p_x[db + k] = qnan;
+        if (p.q_x) p.q_x[db + k] = qnan;
+        if (p.alpha) p.alpha[db + k] = qnan;
+        if (p.nkl) p.nkl[db + k] = qnan;
+        if (p.mask) p.mask[db + k] = 0;
+      }
+    }
+    if (tid == 0) {
+      p.n_acc[b] = -1;
+      if (MODE == M_STOCH) {
+        if (p.g_n) p.g_n[b] = -1;
+        SeqRec q;
+        q.state = REC_SKIP;
+        q.n = -1;
+        q.t_row = q.d_row = -1;
+        q.lt2 = q.ld2 = q.us = 0.f;
+        q.mode = 0;
+        p.rec[b] = q;
+      }
+    }
+    return;
+  }
+
+  if constexpr (MODE == M_GREEDY) {
+    for (int i = tid; i < gb; i += kThreads)
+      if (p.tokens[db + i] != rs[i].tidx) atomicMin(&s_gn, i);
+    __syncthreads();
+    const int n = s_gn;
+    for (int k = tid; k <= gb; k += kThreads)
+      p.out_tok[tb + k] = (k < n) ? p.tokens[db + k] : (k == n ? rs[n].tidx : -1);
+    if (tid == 0) p.n_acc[b] = n;
+    return;
+  } else {
+  // stochastic
+  for (int i = tid; i < gb; i += kThreads) {
+    const RowStat r = rs[i];
+    const int x = p.tokens[db + i];
+    const float zt = elem_at<E>(target + (size_t)(tb + i) * V, x);
+    const float zd = elem_at<E>(draft + (size_t)(db + i) * V, x);
+    const float lp2 = (zt - r.tm) * c - log2f(r.ts);  // log2 p(x)
+    const float lq2 = (zd - r.dm) * c - log2f(r.ds);  // log2 q(x)
+    const float a = exp2f(fminf(0.f, lp2 - lq2));
+    if (p.p_x) p.p_x[db + i] = exp2f(lp2);
+    if (p.q_x) p.q_x[db + i] = exp2f(lq2);
+    if (p.alpha) p.alpha[db + i] = a;
+    if (p.nkl || p.mask) {
+      const double kl = ((double)r.dk / (double)r.ds - ((double)r.dm - (double)r.tm)) * (double)p.invT -
+                        (log((double)r.ds) - log((double)r.ts));
+      const float v = (float)(kl * p.inv_lnV);
+      if (p.nkl) p.nkl[db + i] = v;
+      if (p.mask) p.mask[db + i] = v < p.delta ? 1 : 0;
+    }
+    if (!(p.u_accept[db + i] <= a)) atomicMin(&s_n, i);
+    if (x != r.tidx) atomicMin(&s_gn, i);
+  }
+  __syncthreads();
+  const int n = s_n, gn = s_gn;
+  for (int k = tid; k <= gb; k += kThreads) {
+    const int xk = (k < gb) ? p.tokens[db + k] : -1;
+    if (k != n) p.out_tok[tb + k] = (k < n) ? xk : -1;
+    if (p.g_tok) p.g_tok[tb + k] = (k < gn) ? xk : (k == gn ? rs[gn].tidx : -1);
+  }
+  if (tid == 0) {
+    p.n_acc[b] = n;
+    if (p.g_n) p.g_n[b] = gn;
+    SeqRec q;
+    q.state = REC_READY;
+    q.n = n;
+    q.t_row = tb + n;
+    q.d_row = (n < gb) ? db + n : -1;
+    q.lt2 = rs[n].tm * c + log2f(rs[n].ts);
+    q.ld2 = (n < gb) ? rs[n].dm * c + log2f(rs[n].ds) : 0.f;
+    q.us = p.u_sample[b];
+    q.mode = (n < gb) ? S_RESID : S_P;
+    p.rec[b] = q;
+  }
+  }  // stochastic
+  }  // stochastic and greedy
+}
+
+// ---------------------------------------------------------------------------
+// tile kernel
+
+template <typename E, int VEC, int MODE>
+__global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant__ RowsParams p) {
+  using io = IO<E, VEC>;
+  using raw_t = typename io::raw_t;
+  constexpr int HB = (MODE == M_NKL) ? 0 : 1;
+  griddep_launch();
+  __shared__ int s_b;
+  __shared__ int s_last;
+  const int tile = blockIdx.x;
+  const int r = tile / p.nchunks;
+  const int chunk = tile - r * p.nchunks;
+  int b, i, gb, c0;
+  if (p.cu == nullptr) {
+    const int R = p.gamma + HB;
+    b = r / R;
+    i = r - b * R;
+    gb = p.gamma;
+    c0 = b * p.gamma;
+  } else {
+    // locate the sequence owning row r: one coalesced pass over the offsets
+    if (threadIdx.x == 0) s_b = INT_MAX;
+    __syncthreads();
+    for (int k = threadIdx.x; k < p.B; k += kThreads) {
+      const int lo = __ldg(p.cu + k) + HB * k;
+      const int hi = __ldg(p.cu + k + 1) + HB * (k + 1);
+      if (lo <= r && r < hi) atomicMin(&s_b, k);
+    }
+    __syncthreads();
+    b = s_b;
+    if (b == INT_MAX) {
+      if (threadIdx.x == 0) atomicOr(p.status, SPEC_DEV_OFFSETS);
+      return;
+    }
+    c0 = __ldg(p.cu + b);
+    const int c1 = __ldg(p.cu + b + 1);
+    gb = c1 - c0;
+    i = r - (c0 + HB * b);
+    if (gb < 0 || gb > p.gamma || c0 < 0 || c1 > p.total_draft || i < 0 || i >= gb + HB) {
+      if (threadIdx.x == 0) atomicOr(p.status, SPEC_DEV_OFFSETS);
+      return;
+    }
+  }
+  const int kind = (MODE == M_NKL) ? K_PAIR : (MODE == M_STOCH ? (i < gb ? K_PAIR : K_TSUM) : K_ARGMAX);
+  const size_t V = (size_t)p.V;
+  const size_t trow_i = (MODE == M_NKL) ? (size_t)r + b : (size_t)r;
+  const size_t drow_i = (MODE == M_NKL) ? (size_t)r : (size_t)(r - b);
+  const E* trow = static_cast<const E*>(p.target) + trow_i * V;
+  const E* drow = static_cast<const E*>(p.draft) + ((kind == K_PAIR) ? drow_i * V : 0);
+  const int e_begin = chunk * p.chunk_elems;
+  const int e_end = min(e_begin + p.chunk_elems, p.V);
+  const int v1 = e_end / VEC;
+  const float c = p.c;
+
+  TAcc ta;
+  DAcc da;
+  init(ta);
+  init(da);
+  int v = e_begin / VEC + threadIdx.x;
+  if (kind == K_PAIR) {
+    for (; v + kThreads < v1; v += 2 * kThreads) {
+      const raw_t t0 = io::load(trow, v), t1 = io::load(trow, v + kThreads);
+      const raw_t d0 = io::load(drow, v), d1 = io::load(drow, v + kThreads);
+      float ft[VEC], fd[VEC];
+      io::unpack(t0, ft);
+      io::unpack(d0, fd);
+      pair_update<VEC, MODE == M_STOCH>(ta, da, ft, fd, v * VEC, c);
+      io::unpack(t1, ft);
+      io::unpack(d1, fd);
+      pair_update<VEC, MODE == M_STOCH>(ta, da, ft, fd, (v + kThreads) * VEC, c);
+    }
+    if (v < v1) {
+      float ft[VEC], fd[VEC];
+      io::unpack(io::load(trow, v), ft);
+      io::unpack(io::load(drow, v), fd);
+      pair_update<VEC, MODE == M_STOCH>(ta, da, ft, fd, v * VEC, c);
+    }
+  } else if (kind == K_TSUM) {
+    for (; v + 3 * kThreads < v1; v += 4 * kThreads) {
+      raw_t t[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) t[u] = io::load(trow, v + u * kThreads);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        float ft[VEC];
+        io::unpack(t[u], ft);
+        tsum_update<VEC>(ta, ft, (v + u * kThreads) * VEC, c);
+      }
+    }
+    for (; v < v1; v += kThreads) {
+      float ft[VEC];
+      io::unpack(io::load(trow, v), ft);
+      tsum_update<VEC>(ta, ft, v * VEC, c);
+    }
+  } else {
+    for (; v + 3 * kThreads < v1; v += 4 * kThreads) {
+      raw_t t[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) t[u] = io::load(trow, v + u * kThreads);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        float ft[VEC];
+        io::unpack(t[u], ft);
+        argmax_update<VEC>(ta, ft, (v + u * kThreads) * VEC);
+      }
+    }
+    for (; v < v1; v += kThreads) {
+      float ft[VEC];
+      io::unpack(io::load(trow, v), ft);
+      argmax_update<VEC>(ta, ft, v * VEC);
+    }
+  }
+
+  const Partial part = reduce_tile(kind, ta, da, c);
+  if (threadIdx.x == 0) {
+    float4* dst = reinterpret_cast<float4*>(p.part + tile);
+    __stcg(dst, make_float4(part.tm, part.ts, __int_as_float(part.tidx), __int_as_float(part.bad)));
+    __stcg(dst + 1, make_float4(part.dm, part.ds, part.dk, 0.f));
+    __threadfence();
+    griddep_wait();  // the prologue has zeroed the tickets
+    const unsigned total = (unsigned)((gb + HB) * p.nchunks);
+    const unsigned old = atomicAdd(p.cnt + b, 1u);
+    s_last = (old + 1u == total) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  finalize<E, MODE>(p, b, gb, r - i, c0);
+}
+
+}  // namespace sv

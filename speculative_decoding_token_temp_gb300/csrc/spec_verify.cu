@@ -1,0 +1,370 @@
+// Host entry points of the C ABI declared in include/spec_verify.h: argument checks,
+// workspace layout, path selection (16-byte vectors or scalar) and launches.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "kernels.cuh"
+#include "kernels_rows.cuh"
+#include "kernels_sample.cuh"
+#include "spec_verify.h"
+
+namespace sv {
+namespace {
+
+inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Vocabulary chunking of the tile kernel: chunks of at most 32768 tokens, split further
+// (down to 8192) while the grid has fewer tiles than the GPU has block slots. Chunk
+// sizes are multiples of 8 so every chunk starts on a 16-byte vector boundary.
+void chunking(int V, long long rows, int* nchunks, int* chunk_elems) {
+  long long nc = ceil_div(V, 32768);
+  while (rows * nc < kTargetTiles && V / (nc + 1) >= 8192) ++nc;
+  long long ce = ceil_div(ceil_div(V, nc), 8) * 8;
+  *chunk_elems = (int)ce;
+  *nchunks = (int)ceil_div(V, ce);
+}
+
+// Sampling segments: at most kSegElems tokens (so a warp's step table fits), more while
+// the sampling grid is small.
+void segmenting(int V, int B, int* nseg, int* seg_elems) {
+  long long ns = ceil_div(V, kSegElems);
+  const long long want = ceil_div(kTargetTiles, B > 0 ? B : 1);
+  while (ns < want && V / (ns + 1) >= 2048) ++ns;
+  long long se = ceil_div(ceil_div(V, ns), 8) * 8;
+  *seg_elems = (int)se;
+  *nseg = (int)ceil_div(V, se);
+}
+
+struct Layout {
+  size_t cntA, cntB, rec, part, segtot, total;
+  int nchunks, chunk_elems, nseg, seg_elems;
+  long long rows;
+};
+
+Layout layout(int B, int V, long long rows, bool sample) {
+  Layout L;
+  L.rows = rows;
+  chunking(V, rows > 0 ? rows : 1, &L.nchunks, &L.chunk_elems);
+  if (sample)
+    segmenting(V, B, &L.nseg, &L.seg_elems);
+  else
+    L.nseg = L.seg_elems = 0;
+  size_t off = 0;
+  L.cntA = off;
+  off = align256(off + sizeof(unsigned) * (size_t)B);
+  L.cntB = off;
+  off = align256(off + sizeof(unsigned) * (size_t)B);
+  L.rec = off;
+  off = align256(off + sizeof(SeqRec) * (size_t)B);
+  L.part = off;
+  off = align256(off + sizeof(Partial) * (size_t)(rows * L.nchunks));
+  L.segtot = off;
+  off = align256(off + sizeof(double) * (size_t)B * (size_t)L.nseg);
+  L.total = off;
+  return L;
+}
+
+long long rows_for(spec_mode mode, const spec_batch& g) {
+  if (mode == SPEC_MODE_NKL) return g.total_draft;
+  return (long long)g.total_draft + g.B;
+}
+
+bool aligned16(const void* p) { return p == nullptr || ((uintptr_t)p & 15u) == 0; }
+
+spec_status check_batch(const spec_batch& g) {
+  if (g.B < 0 || g.V < 1 || g.gamma < 0 || g.gamma > SPEC_MAX_GAMMA || g.total_draft < 0) return SPEC_ERR_INVALID_ARG;
+  if (g.cu_draft == nullptr && (long long)g.B * g.gamma != g.total_draft) return SPEC_ERR_INVALID_ARG;
+  if ((long long)g.total_draft > (long long)g.B * g.gamma) return SPEC_ERR_INVALID_ARG;
+  // row indices and element offsets stay inside int / size_t arithmetic
+  if ((long long)g.total_draft + g.B > (1LL << 30)) return SPEC_ERR_INVALID_ARG;
+  if (g.V > (1 << 26)) return SPEC_ERR_INVALID_ARG;
+  return SPEC_OK;
+}
+
+// Launch with programmatic stream serialisation (pdl = true): the kernel may start while
+// its predecessor in the stream drains; it reads the predecessor's results only after
+// griddepcontrol.wait. The prologue of a call is launched without it, so a call never
+// overlaps the previous call on the same stream.
+template <typename K, typename P>
+cudaError_t launch(K kernel, dim3 grid, dim3 block, cudaStream_t stream, const P& params, bool pdl) {
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, params);
+}
+
+template <typename K, typename P>
+cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, cudaStream_t stream, const P& params) {
+  return launch(kernel, grid, block, stream, params, true);
+}
+
+cudaError_t launch_prologue(const spec_batch& g, const Layout& L, char* ws, uint32_t* status, cudaStream_t stream) {
+  ProParams pp;
+  pp.cu = g.cu_draft;
+  pp.B = g.B;
+  pp.gamma = g.gamma;
+  pp.total_draft = g.total_draft;
+  pp.cntA = reinterpret_cast<unsigned*>(ws + L.cntA);
+  pp.cntB = reinterpret_cast<unsigned*>(ws + L.cntB);
+  pp.rec = reinterpret_cast<SeqRec*>(ws + L.rec);
+  pp.status = status;
+  return launch(prologue_kernel, dim3((unsigned)ceil_div(g.B, kThreads)), dim3(kThreads), stream, pp, false);
+}
+
+template <int MODE>
+cudaError_t launch_rows(bool bf16, bool vec, const RowsParams& rp, long long tiles, cudaStream_t stream) {
+  const dim3 grid((unsigned)tiles), block(kThreads);
+  if (bf16) {
+    if (vec) return launch_pdl(rows_kernel<uint16_t, 8, MODE>, grid, block, stream, rp);
+    return launch_pdl(rows_kernel<uint16_t, 1, MODE>, grid, block, stream, rp);
+  }
+  if (vec) return launch_pdl(rows_kernel<float, 4, MODE>, grid, block, stream, rp);
+  return launch_pdl(rows_kernel<float, 1, MODE>, grid, block, stream, rp);
+}
+
+cudaError_t launch_sample(bool bf16, bool vec, const SampleParams& sp, long long blocks, cudaStream_t stream) {
+  const dim3 grid((unsigned)blocks), block(kThreads);
+  if (bf16) {
+    if (vec) return launch_pdl(sample_kernel<uint16_t, 8>, grid, block, stream, sp);
+    return launch_pdl(sample_kernel<uint16_t, 1>, grid, block, stream, sp);
+  }
+  if (vec) return launch_pdl(sample_kernel<float, 4>, grid, block, stream, sp);
+  return launch_pdl(sample_kernel<float, 1>, grid, block, stream, sp);
+}
+
+RowsParams base_params(const spec_batch& g, const Layout& L, char* ws, uint32_t* status) {
+  RowsParams rp;
+  memset(&rp, 0, sizeof(rp));
+  rp.cu = g.cu_draft;
+  rp.B = g.B;
+  rp.V = g.V;
+  rp.gamma = g.gamma;
+  rp.total_draft = g.total_draft;
+  rp.total_rows = (int)L.rows;
+  rp.nchunks = L.nchunks;
+  rp.chunk_elems = L.chunk_elems;
+  rp.status = status;
+  rp.part = reinterpret_cast<Partial*>(ws + L.part);
+  rp.cnt = reinterpret_cast<unsigned*>(ws + L.cntA);
+  rp.rec = reinterpret_cast<SeqRec*>(ws + L.rec);
+  rp.inv_lnV = g.V > 1 ? 1.0 / log((double)g.V) : 0.0;
+  return rp;
+}
+
+bool vec_path(spec_dtype dt, int V, const void* a, const void* b) {
+  const int es = dt == SPEC_BF16 ? 2 : 4;
+  return ((long long)V * es) % 16 == 0 && aligned16(a) && aligned16(b);
+}
+
+bool temperature_ok(float T) { return isfinite(T) && T > 0.f; }
+
+}  // namespace
+}  // namespace sv
+
+using namespace sv;
+
+extern "C" {
+
+size_t spec_workspace_bytes(spec_batch g, spec_mode mode) {
+  if (check_batch(g) != SPEC_OK) return 0;
+  return layout(g.B, g.V, rows_for(mode, g), mode == SPEC_MODE_STOCHASTIC).total;
+}
+
+size_t spec_tree_workspace_bytes(int32_t B, int32_t N, int32_t V) {
+  if (B < 0 || N < 1 || N > SPEC_MAX_TREE_NODES || V < 1) return 0;
+  return layout(B, V, (long long)B * (N + 1), false).total;
+}
+
+int32_t spec_tree_depth(const int32_t* parent, int32_t N) {
+  if (parent == nullptr || N < 1 || N > SPEC_MAX_TREE_NODES) return -1;
+  int depth[SPEC_MAX_TREE_NODES];
+  int D = 0;
+  for (int j = 0; j < N; ++j) {
+    const int pj = parent[j];
+    if (pj < -1 || pj >= j) return -1;
+    depth[j] = pj < 0 ? 1 : depth[pj] + 1;
+    if (depth[j] > D) D = depth[j];
+  }
+  return D;
+}
+
+spec_status spec_verify_stochastic(spec_batch g, spec_dtype dtype, const void* target_logits,
+                                   const void* draft_logits, const int32_t* draft_tokens, float temperature,
+                                   const float* u_accept, const float* u_sample, int32_t* n_accepted,
+                                   int32_t* out_tokens, float* p_x, float* q_x, float* alpha, float* nkl,
+                                   uint8_t* nkl_mask, float nkl_delta, int32_t* greedy_n, int32_t* greedy_tokens,
+                                   uint32_t* device_status, void* workspace, size_t workspace_bytes,
+                                   spec_stream_t stream_) {
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
+  spec_status st = check_batch(g);
+  if (st != SPEC_OK) return st;
+  if (!temperature_ok(temperature)) return SPEC_ERR_INVALID_ARG;
+  if (g.B == 0) return SPEC_OK;
+  if (!target_logits || !n_accepted || !out_tokens || !u_sample || !device_status) return SPEC_ERR_INVALID_ARG;
+  if (g.total_draft > 0 && (!draft_logits || !draft_tokens || !u_accept)) return SPEC_ERR_INVALID_ARG;
+  if ((greedy_n == nullptr) != (greedy_tokens == nullptr)) return SPEC_ERR_INVALID_ARG;
+  const Layout L = layout(g.B, g.V, rows_for(SPEC_MODE_STOCHASTIC, g), true);
+  if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u)) return SPEC_ERR_WORKSPACE;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  char* ws = static_cast<char*>(workspace);
+  const bool bf16 = dtype == SPEC_BF16;
+  const bool vec = vec_path(dtype, g.V, target_logits, draft_logits);
+
+  if (launch_prologue(g, L, ws, device_status, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  RowsParams rp = base_params(g, L, ws, device_status);
+  rp.target = target_logits;
+  rp.draft = draft_logits;
+  rp.tokens = draft_tokens;
+  rp.u_accept = u_accept;
+  rp.u_sample = u_sample;
+  rp.c = (float)(1.4426950408889634 / (double)temperature);
+  rp.invT = (float)(1.0 / (double)temperature);
+  rp.delta = nkl_delta;
+  rp.n_acc = n_accepted;
+  rp.out_tok = out_tokens;
+  rp.p_x = p_x;
+  rp.q_x = q_x;
+  rp.alpha = alpha;
+  rp.nkl = nkl;
+  rp.mask = nkl_mask;
+  rp.g_n = greedy_n;
+  rp.g_tok = greedy_tokens;
+  if (launch_rows<M_STOCH>(bf16, vec, rp, L.rows * L.nchunks, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+
+  SampleParams sp;
+  memset(&sp, 0, sizeof(sp));
+  sp.target = target_logits;
+  sp.draft = draft_logits;
+  sp.V = g.V;
+  sp.total_rows = (int)L.rows;
+  sp.total_draft = g.total_draft;
+  sp.B = g.B;
+  sp.nseg = L.nseg;
+  sp.seg_elems = L.seg_elems;
+  sp.c = rp.c;
+  sp.rec = rp.rec;
+  sp.segtot = reinterpret_cast<double*>(ws + L.segtot);
+  sp.cnt = reinterpret_cast<unsigned*>(ws + L.cntB);
+  sp.out_tok = out_tokens;
+  sp.status = device_status;
+  if (launch_sample(bf16, vec, sp, (long long)g.B * L.nseg, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  return SPEC_OK;
+}
+
+spec_status spec_verify_greedy(spec_batch g, spec_dtype dtype, const void* target_logits,
+                               const int32_t* draft_tokens, int32_t* n_accepted, int32_t* out_tokens,
+                               uint32_t* device_status, void* workspace, size_t workspace_bytes,
+                               spec_stream_t stream_) {
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
+  spec_status st = check_batch(g);
+  if (st != SPEC_OK) return st;
+  if (g.B == 0) return SPEC_OK;
+  if (!target_logits || !n_accepted || !out_tokens || !device_status) return SPEC_ERR_INVALID_ARG;
+  if (g.total_draft > 0 && !draft_tokens) return SPEC_ERR_INVALID_ARG;
+  const Layout L = layout(g.B, g.V, rows_for(SPEC_MODE_GREEDY, g), false);
+  if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u)) return SPEC_ERR_WORKSPACE;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  char* ws = static_cast<char*>(workspace);
+  if (launch_prologue(g, L, ws, device_status, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  RowsParams rp = base_params(g, L, ws, device_status);
+  rp.target = target_logits;
+  rp.tokens = draft_tokens;
+  rp.n_acc = n_accepted;
+  rp.out_tok = out_tokens;
+  rp.c = 1.f;
+  if (launch_rows<M_GREEDY>(dtype == SPEC_BF16, vec_path(dtype, g.V, target_logits, nullptr), rp,
+                            L.rows * L.nchunks, stream) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  return SPEC_OK;
+}
+
+spec_status spec_verify_tree(int32_t B, int32_t N, int32_t V, spec_dtype dtype, const void* target_logits,
+                             const int32_t* node_tokens, const int32_t* parent, int32_t* accept_len,
+                             int32_t* path_nodes, int32_t* out_tokens, uint32_t* device_status, void* workspace,
+                             size_t workspace_bytes, spec_stream_t stream_) {
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
+  if (B < 0 || V < 1 || V > (1 << 26)) return SPEC_ERR_INVALID_ARG;
+  const int D = spec_tree_depth(parent, N);
+  if (D < 1) return SPEC_ERR_INVALID_ARG;
+  if ((long long)B * (N + 1) > (1LL << 30)) return SPEC_ERR_INVALID_ARG;
+  if (B == 0) return SPEC_OK;
+  if (!target_logits || !node_tokens || !accept_len || !path_nodes || !out_tokens || !device_status)
+    return SPEC_ERR_INVALID_ARG;
+  spec_batch g;
+  g.B = B;
+  g.gamma = N;
+  g.V = V;
+  g.total_draft = B * N;
+  g.cu_draft = nullptr;
+  const Layout L = layout(B, V, (long long)B * (N + 1), false);
+  if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u)) return SPEC_ERR_WORKSPACE;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  char* ws = static_cast<char*>(workspace);
+  if (launch_prologue(g, L, ws, device_status, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  RowsParams rp = base_params(g, L, ws, device_status);
+  rp.target = target_logits;
+  rp.node_tokens = node_tokens;
+  rp.N = N;
+  rp.depth = D;
+  for (int j = 0; j < N; ++j) rp.parent[j] = (int8_t)parent[j];
+  rp.accept_len = accept_len;
+  rp.path_nodes = path_nodes;
+  rp.out_tok = out_tokens;
+  rp.c = 1.f;
+  if (launch_rows<M_TREE>(dtype == SPEC_BF16, vec_path(dtype, V, target_logits, nullptr), rp, L.rows * L.nchunks,
+                          stream) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  return SPEC_OK;
+}
+
+spec_status spec_nkl(spec_batch g, spec_dtype dtype, const void* target_logits, const void* draft_logits,
+                     float temperature, float delta, float* nkl, uint8_t* nkl_mask, uint32_t* device_status,
+                     void* workspace, size_t workspace_bytes, spec_stream_t stream_) {
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
+  spec_status st = check_batch(g);
+  if (st != SPEC_OK) return st;
+  if (!temperature_ok(temperature)) return SPEC_ERR_INVALID_ARG;
+  if (g.B == 0 || g.total_draft == 0) return SPEC_OK;
+  if (!target_logits || !draft_logits || !nkl || !device_status) return SPEC_ERR_INVALID_ARG;
+  const Layout L = layout(g.B, g.V, rows_for(SPEC_MODE_NKL, g), false);
+  if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u)) return SPEC_ERR_WORKSPACE;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  char* ws = static_cast<char*>(workspace);
+  if (launch_prologue(g, L, ws, device_status, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  RowsParams rp = base_params(g, L, ws, device_status);
+  rp.target = target_logits;
+  rp.draft = draft_logits;
+  rp.c = (float)(1.4426950408889634 / (double)temperature);
+  rp.invT = (float)(1.0 / (double)temperature);
+  rp.delta = delta;
+  rp.nkl = nkl;
+  rp.mask = nkl_mask;
+  if (launch_rows<M_NKL>(dtype == SPEC_BF16, vec_path(dtype, g.V, target_logits, draft_logits), rp,
+                         L.rows * L.nchunks, stream) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  return SPEC_OK;
+}
+
+const char* spec_status_str(spec_status s) {
+  switch (s) {
+    case SPEC_OK: return "ok";
+    case SPEC_ERR_INVALID_ARG: return "invalid argument";
+    case SPEC_ERR_DTYPE: return "unknown dtype";
+    case SPEC_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case SPEC_ERR_CUDA: return "CUDA launch failed";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -31,6 +31,8 @@ so one sequence of a large workload can be regenerated alone.
 """
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -137,6 +139,18 @@ class TreeWorkload:
         return 2 if self.dtype == BF16 else 4
 
 
+def _for_each(fn, n: int) -> None:
+    """Run fn(0..n-1); sequences draw from independent streams, so the order and the
+    thread count do not change the result (numpy releases the GIL in the bulk draws)."""
+    workers = min(16, os.cpu_count() or 1, max(1, n))
+    if workers == 1 or n < 4:
+        for b in range(n):
+            fn(b)
+        return
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        list(ex.map(fn, range(n)))
+
+
 def _draw_sequence(rng, gamma: int, V: int, dtype: str, T: float, agreement: float):
     """Target rows [gamma+1, V], draft rows [gamma, V] (storage dtype), tokens, u_accept."""
     base = rng.standard_normal((gamma + 1, V), dtype=np.float32)
@@ -157,7 +171,7 @@ def _draw_sequence(rng, gamma: int, V: int, dtype: str, T: float, agreement: flo
     t_st = storage(target32, dtype)
     d_st = storage(draft32, dtype)
     d_seen = stored_as_f32(d_st, dtype)
-    gumbel = -np.log(expo)
+    gumbel = -np.log(np.maximum(expo, np.float32(np.finfo(np.float32).tiny)))
     tokens = np.argmax(d_seen / np.float32(T) + gumbel, axis=1).astype(np.int32)
     return t_st, d_st, tokens, u_acc
 
@@ -184,7 +198,7 @@ def make_stochastic(B: int, V: int, dtype: str, T: float, seed: int, gamma: int 
     tokens = np.empty(tot_d, dtype=np.int32)
     u_acc = np.empty(tot_d, dtype=np.float32)
     u_smp = np.empty(B, dtype=np.float32)
-    for b in range(B):
+    def one(b):
         rng = np.random.default_rng([seed, b])
         g = int(gammas[b])
         t_st, d_st, tok, ua = _draw_sequence(rng, g, V, dtype, T, agreement)
@@ -194,6 +208,8 @@ def make_stochastic(B: int, V: int, dtype: str, T: float, seed: int, gamma: int 
         tokens[d0:d0 + g] = tok
         u_acc[d0:d0 + g] = ua
         u_smp[b] = rng.random(dtype=np.float32)
+
+    _for_each(one, B)
     return StochasticWorkload(B=B, V=V, dtype=dtype, T=float(T), gammas=gammas, cu_draft=cu,
                               target=target, draft=draft, tokens=tokens, u_accept=u_acc,
                               u_sample=u_smp, dense=dense, name=name)
@@ -210,7 +226,7 @@ def make_tree(B: int, V: int, dtype: str, seed: int, parent=TREE_PARENT, agreeme
     sdt = np.uint16 if dtype == BF16 else np.float32
     target = np.empty((B * (N + 1), V), dtype=sdt)
     node_tokens = np.empty((B, N), dtype=np.int32)
-    for b in range(B):
+    def one(b):
         rng = np.random.default_rng([seed, b])
         base = rng.standard_normal((N + 1, V), dtype=np.float32)
         base *= np.float32(TARGET_SIGMA)
@@ -230,6 +246,8 @@ def make_tree(B: int, V: int, dtype: str, seed: int, parent=TREE_PARENT, agreeme
         for j in range(N):
             if parent[j] >= 0:
                 node_tokens[b, j] = int(np.argmax(d_seen[parent[j] + 1]))
+
+    _for_each(one, B)
     return TreeWorkload(B=B, N=N, V=V, dtype=dtype, parent=parent, target=target,
                         node_tokens=node_tokens, name=name)
 

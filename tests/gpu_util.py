@@ -1,0 +1,152 @@
+"""Helpers for the GPU parity tests: run the CUDA calls on workloads and compare with the oracle."""
+import numpy as np
+import torch
+
+from oracle import oracle as O
+from speculative_decoding_token_temp_gb300 import api, synth
+
+REL = 1e-4        # p(x), q(x), alpha, NKL: relative to fp64
+NKL_ABS = 2e-6    # NKL near zero: fp32 terms of size ~|E_q[a]| ~ 10 carry ~1e-6 absolute error, / ln V
+
+
+def to_dev(a, dev):
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+    return torch.from_numpy(a).to(dev)
+
+
+def run_stochastic(w, dev, T=None, delta=0.15, offset=0):
+    """Call spec_verify_stochastic on a workload; offset > 0 shifts the logit buffers by
+    that many elements (misaligned base pointers force the scalar path)."""
+    T = w.T if T is None else T
+
+    def put(a):
+        if offset == 0:
+            return to_dev(a, dev)
+        flat = to_dev(np.ascontiguousarray(a).reshape(-1), dev)
+        buf = torch.empty(flat.numel() + offset, dtype=flat.dtype, device=dev)
+        buf[offset:] = flat
+        return buf[offset:]
+
+    t = put(w.target)
+    d = put(w.draft)
+    cu = None if w.dense else torch.from_numpy(w.cu_draft).to(dev)
+    res = api.spec_verify_stochastic(t, d, to_dev(w.tokens, dev), T, to_dev(w.u_accept, dev),
+                                     to_dev(w.u_sample, dev), cu_draft=cu, gamma=w.gamma_max if not w.dense
+                                     else int(w.gammas[0]) if w.B else 0, nkl_delta=delta)
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in res.items()}
+
+
+def compare_stochastic(w, res, seqs, T=None, delta=0.15, check_greedy=True):
+    """Bit-exact n / tokens except oracle-flagged sequences; reals within REL. Returns
+    (number compared, number flagged)."""
+    T = w.T if T is None else T
+    ref = O.verify_stochastic(w.target, w.draft, w.tokens, w.cu_draft, T, w.u_accept, w.u_sample, w.dtype,
+                              nkl_delta=delta, seqs=seqs)
+    flagged = 0
+    for b in seqs:
+        r = ref[b]
+        g = int(w.gammas[b])
+        t0, d0 = w.target_base(b), w.draft_base(b)
+        n = int(res["n_accepted"][b])
+        toks = res["out_tokens"][t0:t0 + g + 1]
+        if r["flag"]:
+            flagged += 1
+        else:
+            assert n == r["n"], (b, n, r["n"], r["alpha"], w.u_accept[d0:d0 + g])
+            assert list(toks) == list(r["tokens"]), (b, toks, r["tokens"])
+        if g:
+            for k in ("p_x", "q_x", "alpha"):
+                got = res[k][d0:d0 + g].astype(np.float64)
+                assert np.allclose(got, r[k], rtol=REL, atol=1e-30), (b, k, got, r[k])
+            got = res["nkl"][d0:d0 + g].astype(np.float64)
+            assert np.allclose(got, r["nkl"], rtol=REL, atol=NKL_ABS), (b, got, r["nkl"])
+            m = res["nkl_mask"][d0:d0 + g]
+            near = np.abs(r["nkl"] - delta) <= REL * delta + NKL_ABS
+            assert np.all((m == r["mask"]) | near), (b, m, r["mask"])
+        if check_greedy:
+            assert int(res["greedy_n"][b]) == r["greedy_n"]
+            assert list(res["greedy_tokens"][t0:t0 + g + 1]) == list(r["greedy_tokens"])
+    return len(list(seqs)), flagged
+
+
+def run_greedy(w, dev):
+    cu = None if w.dense else torch.from_numpy(w.cu_draft).to(dev)
+    res = api.spec_verify_greedy(to_dev(w.target, dev), to_dev(w.tokens, dev), cu_draft=cu,
+                                 gamma=w.gamma_max if not w.dense else int(w.gammas[0]))
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in res.items()}
+
+
+def compare_greedy(w, res, seqs):
+    ref = O.verify_greedy(w.target, w.tokens, w.cu_draft, w.dtype, seqs=seqs)
+    for b in seqs:
+        g = int(w.gammas[b])
+        t0 = w.target_base(b)
+        assert int(res["n_accepted"][b]) == ref[b]["n"], b
+        assert list(res["out_tokens"][t0:t0 + g + 1]) == list(ref[b]["tokens"]), b
+
+
+def run_nkl(w, dev, delta=0.15):
+    cu = None if w.dense else torch.from_numpy(w.cu_draft).to(dev)
+    res = api.spec_nkl(to_dev(w.target, dev), to_dev(w.draft, dev), w.T, cu_draft=cu,
+                       gamma=w.gamma_max if not w.dense else int(w.gammas[0]), delta=delta)
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in res.items()}
+
+
+def compare_nkl(w, res, seqs, delta=0.15):
+    ref = O.nkl_rows(w.target, w.draft, w.cu_draft, w.T, w.dtype, delta=delta, seqs=seqs)
+    for b in seqs:
+        g = int(w.gammas[b])
+        d0 = w.draft_base(b)
+        got = res["nkl"][d0:d0 + g].astype(np.float64)
+        assert np.allclose(got, ref[b]["nkl"], rtol=REL, atol=NKL_ABS, equal_nan=True), (b, got, ref[b]["nkl"])
+        m = res["nkl_mask"][d0:d0 + g]
+        near = np.abs(ref[b]["nkl"] - delta) <= REL * delta + NKL_ABS
+        assert np.all((m == ref[b]["mask"]) | near)
+
+
+def run_tree(w, dev):
+    res = api.spec_verify_tree(to_dev(w.target, dev), to_dev(w.node_tokens, dev), list(w.parent))
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in res.items()}
+
+
+def compare_tree(w, res, seqs):
+    ref = O.verify_tree(w.target, w.node_tokens, list(w.parent), w.dtype, seqs=seqs)
+    for b in seqs:
+        assert int(res["accept_len"][b]) == ref[b]["len"], b
+        assert list(res["path_nodes"][b]) == list(ref[b]["path"]), b
+        assert list(res["out_tokens"][b]) == list(ref[b]["tokens"]), b
+
+
+def sample_seqs(B, k, seed=0):
+    if B <= k:
+        return list(range(B))
+    rng = np.random.default_rng(seed)
+    s = set(rng.choice(B, size=k - 2, replace=False).tolist()) | {0, B - 1}
+    return sorted(s)
+
+
+def handmade(B, gamma, V, dtype, T=1.0, seed=0, draft_equals_target=False, the_token=None):
+    """A small dense workload from plain random logits (edge-case tests)."""
+    rng = np.random.default_rng(seed)
+    t32 = rng.normal(0, 2, ((gamma + 1) * B, V)).astype(np.float32)
+    d32 = np.empty((gamma * B, V), dtype=np.float32)
+    for b in range(B):
+        if draft_equals_target:
+            d32[b * gamma:(b + 1) * gamma] = t32[b * (gamma + 1):b * (gamma + 1) + gamma]
+        else:
+            d32[b * gamma:(b + 1) * gamma] = rng.normal(0, 2, (gamma, V))
+    if the_token is not None:
+        d32[:, the_token] = 40.0
+    tokens = rng.integers(0, V, gamma * B).astype(np.int32)
+    if the_token is not None:
+        tokens[:] = the_token
+    cu = np.arange(B + 1, dtype=np.int32) * gamma
+    return synth.StochasticWorkload(B=B, V=V, dtype=dtype, T=T, gammas=np.full(B, gamma, dtype=np.int32),
+                                    cu_draft=cu, target=synth.storage(t32, dtype), draft=synth.storage(d32, dtype),
+                                    tokens=tokens, u_accept=rng.random(gamma * B, dtype=np.float32),
+                                    u_sample=rng.random(B, dtype=np.float32), dense=True, name="handmade")

@@ -1,0 +1,86 @@
+"""The C-ABI library loads and exports what include/spec_verify.h declares; host-side
+argument checks and workspace sizing. No GPU: nothing here launches a kernel."""
+import ctypes
+
+import pytest
+
+from speculative_decoding_token_temp_gb300 import _lib, build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.lib()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _lib.declared_functions()
+    assert {"spec_verify_stochastic", "spec_verify_greedy", "spec_verify_tree", "spec_nkl",
+            "spec_workspace_bytes", "spec_tree_workspace_bytes", "spec_tree_depth", "spec_status_str"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(_lib.SIGNATURES) >= set(names)
+
+
+def test_status_strings(lib):
+    assert lib.spec_status_str(0) == b"ok"
+    assert b"workspace" in lib.spec_status_str(3)
+
+
+def _g(B, gamma, V, total=None, cu=None):
+    return _lib.SpecBatch(B, gamma, V, B * gamma if total is None else total, cu)
+
+
+def test_workspace_sizes(lib):
+    h = lib.spec_workspace_bytes(_g(256, 8, 128256), _lib.SPEC_MODE_STOCHASTIC)
+    # 2304 rows x 4 chunks x 32 B partials, plus tickets, records and segment totals
+    assert 2304 * 4 * 32 <= h < 2304 * 4 * 32 + 256 * 200
+    assert lib.spec_workspace_bytes(_g(256, 8, 128256), _lib.SPEC_MODE_GREEDY) <= h
+    assert lib.spec_workspace_bytes(_g(0, 8, 100), _lib.SPEC_MODE_STOCHASTIC) >= 0
+    assert lib.spec_workspace_bytes(_g(2, 200, 100), 0) == 0        # gamma above the limit
+    assert lib.spec_tree_workspace_bytes(32, 12, 128256) > 0
+    assert lib.spec_tree_workspace_bytes(32, 65, 128256) == 0
+
+
+def _tree_depth(lib, parent):
+    arr = (ctypes.c_int32 * len(parent))(*parent)
+    return lib.spec_tree_depth(ctypes.cast(arr, ctypes.c_void_p), len(parent))
+
+
+def test_tree_depth(lib):
+    assert _tree_depth(lib, [-1, -1, -1, 0, 1, 2, 3, 4, 5, 6, 7, 8]) == 4
+    assert _tree_depth(lib, [-1, 0, 1, 2]) == 4
+    assert _tree_depth(lib, [-1, 1]) == -1        # not topologically ordered
+    assert _tree_depth(lib, [0]) == -1
+
+
+def test_host_validation_without_launch(lib):
+    """Every rejected argument returns before any CUDA call, so this runs without a GPU."""
+    P = ctypes.c_void_p
+    one = P(256)
+    args = dict(dt=_lib.SPEC_BF16, T=0.6)
+
+    def stoch(g, dt=_lib.SPEC_BF16, T=0.6, ws=one, wsb=1 << 30, target=one, status=one):
+        return lib.spec_verify_stochastic(g, dt, target, one, one, T, one, one, one, one, None, None, None, None,
+                                          None, 0.15, None, None, status, ws, wsb, None)
+
+    g = _g(4, 3, 1000)
+    assert stoch(g, dt=7) == _lib.SPEC_ERR_DTYPE
+    assert stoch(g, T=0.0) == _lib.SPEC_ERR_INVALID_ARG
+    assert stoch(g, T=float("nan")) == _lib.SPEC_ERR_INVALID_ARG
+    assert stoch(g, T=-1.0) == _lib.SPEC_ERR_INVALID_ARG
+    assert stoch(g, target=None) == _lib.SPEC_ERR_INVALID_ARG
+    assert stoch(g, status=None) == _lib.SPEC_ERR_INVALID_ARG
+    assert stoch(g, ws=None) == _lib.SPEC_ERR_WORKSPACE
+    assert stoch(g, wsb=16) == _lib.SPEC_ERR_WORKSPACE
+    assert stoch(g, ws=P(257)) == _lib.SPEC_ERR_WORKSPACE           # not 256-byte aligned
+    assert stoch(_g(4, 3, 1000, total=11)) == _lib.SPEC_ERR_INVALID_ARG   # dense total != B*gamma
+    assert stoch(_g(4, 3, 0)) == _lib.SPEC_ERR_INVALID_ARG
+    assert stoch(_g(4, 129, 10)) == _lib.SPEC_ERR_INVALID_ARG
+    assert stoch(_g(0, 3, 10)) == _lib.SPEC_OK                       # empty batch: nothing to do
+    assert lib.spec_verify_greedy(g, 5, one, one, one, one, one, one, 1 << 30, None) == _lib.SPEC_ERR_DTYPE
+    assert lib.spec_nkl(g, _lib.SPEC_F32, one, one, 0.0, 0.15, one, None, one, one, 1 << 30, None) == \
+        _lib.SPEC_ERR_INVALID_ARG
+    bad_parent = (ctypes.c_int32 * 2)(-1, 5)
+    assert lib.spec_verify_tree(2, 2, 100, _lib.SPEC_BF16, one, one, ctypes.cast(bad_parent, P), one, one, one,
+                                one, one, 1 << 30, None) == _lib.SPEC_ERR_INVALID_ARG

@@ -1,0 +1,266 @@
+"""GPU parity: the CUDA library, called through the C ABI, against the fp64 oracle.
+
+Tolerances: accepted counts and tokens bit-exact in greedy and tree modes, and in
+stochastic mode except the sequences the oracle flags (a decision within 1e-5 of its
+boundary); p(x), q(x), alpha and NKL within 1e-4 relative of fp64 (NKL also within an
+absolute 2e-6 near zero)."""
+import numpy as np
+import pytest
+import scipy.stats
+import torch
+
+from oracle import oracle as O
+from speculative_decoding_token_temp_gb300 import _lib, api, synth
+
+from gpu_util import (compare_greedy, compare_nkl, compare_stochastic, compare_tree, handmade, run_greedy,
+                      run_nkl, run_stochastic, run_tree, sample_seqs, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    return torch.device("cuda:0")
+
+
+_CACHE = {}
+
+
+def workload(i):
+    if i not in _CACHE:
+        _CACHE[i] = synth.CONFIGS[i].make()
+    return _CACHE[i]
+
+
+# ---------------------------------------------------------------- the five workloads
+
+def test_config0_tiny_f32(dev):
+    w = workload(0)
+    res = run_stochastic(w, dev)
+    compare_stochastic(w, res, range(w.B))
+    assert res["device_status"][0] == 0
+    compare_greedy(w, run_greedy(w, dev), range(w.B))
+    compare_nkl(w, run_nkl(w, dev), range(w.B))
+
+
+@pytest.mark.parametrize("T", [0.6, 1.0])
+def test_config1_bf16_all_sequences(dev, T):
+    w = synth.CONFIGS[1].make(T=T)
+    res = run_stochastic(w, dev)
+    n, flagged = compare_stochastic(w, res, range(w.B))
+    assert flagged <= 1
+    assert res["device_status"][0] == 0
+    compare_greedy(w, run_greedy(w, dev), range(w.B))
+    compare_nkl(w, run_nkl(w, dev), range(w.B))
+
+
+def test_config2_headline_sampled(dev):
+    w = workload(2)
+    res = run_stochastic(w, dev)
+    assert res["device_status"][0] == 0
+    seqs = sample_seqs(w.B, 12, seed=2)
+    compare_stochastic(w, res, seqs)
+    # greedy: every sequence
+    compare_greedy(w, run_greedy(w, dev), range(w.B))
+    # fused greedy outputs agree with the standalone call
+    g = run_greedy(w, dev)
+    assert np.array_equal(g["n_accepted"], res["greedy_n"])
+    assert np.array_equal(g["out_tokens"], res["greedy_tokens"])
+    # properties that hold at every size
+    n = res["n_accepted"]
+    assert np.all((n >= 0) & (n <= 8))
+    out = res["out_tokens"].reshape(w.B, 9)
+    for b in range(w.B):
+        assert np.all(out[b, :n[b]] == w.tokens[b * 8:b * 8 + n[b]])
+        assert 0 <= out[b, n[b]] < w.V and np.all(out[b, n[b] + 1:] == -1)
+    assert np.all(res["alpha"] <= 1.0) and np.all(res["alpha"] > 0)
+    assert np.all(res["nkl"] >= -NKL_FLOOR)
+
+
+NKL_FLOOR = 1e-6
+
+
+def test_config2_nkl_standalone_sampled(dev):
+    w = workload(2)
+    res = run_nkl(w, dev)
+    compare_nkl(w, res, sample_seqs(w.B, 6, seed=5))
+
+
+def test_config3_tree_all_sequences(dev):
+    w = synth.CONFIGS[3].make()
+    res = run_tree(w, dev)
+    assert res["device_status"][0] == 0
+    compare_tree(w, res, range(w.B))
+
+
+def test_config4_ragged_sampled(dev):
+    w = synth.CONFIGS[4].make()
+    assert not w.dense
+    res = run_stochastic(w, dev)
+    assert res["device_status"][0] == 0
+    compare_stochastic(w, res, sample_seqs(w.B, 10, seed=4))
+    compare_greedy(w, run_greedy(w, dev), sample_seqs(w.B, 64, seed=6))
+    n = res["n_accepted"]
+    assert np.all((n >= 0) & (n <= w.gammas))
+
+
+# ---------------------------------------------------------------- edge cases
+
+@pytest.mark.parametrize("V", [1, 2, 7, 8, 9, 4095, 4096, 4097, 40000])
+@pytest.mark.parametrize("dtype", [synth.F32, synth.BF16])
+def test_odd_vocab_sizes(dev, V, dtype):
+    w = handmade(3, 3, V, dtype, T=0.8, seed=V)
+    res = run_stochastic(w, dev)
+    compare_stochastic(w, res, range(w.B))
+    compare_greedy(w, run_greedy(w, dev), range(w.B))
+    compare_nkl(w, run_nkl(w, dev), range(w.B))
+
+
+@pytest.mark.parametrize("offset", [1, 3])
+def test_misaligned_buffers_take_scalar_path(dev, offset):
+    w = handmade(4, 5, 4096, synth.BF16, T=0.7, seed=11)
+    res = run_stochastic(w, dev, offset=offset)
+    compare_stochastic(w, res, range(w.B))
+
+
+def test_gamma_zero_and_one(dev):
+    for g in (0, 1):
+        w = handmade(5, g, 3000, synth.BF16, seed=20 + g)
+        res = run_stochastic(w, dev)
+        compare_stochastic(w, res, range(w.B))
+        if g == 0:
+            assert np.all(res["n_accepted"] == 0)
+
+
+def test_max_gamma(dev):
+    w = handmade(2, 128, 600, synth.F32, seed=21)
+    res = run_stochastic(w, dev)
+    compare_stochastic(w, res, range(w.B))
+
+
+def test_identical_rows_accept_all(dev):
+    """Invariant (a) on the GPU: q == p gives alpha == 1 and n == gamma; NKL == 0."""
+    w = handmade(6, 4, 5000, synth.BF16, seed=22, draft_equals_target=True)
+    w.u_accept[:] = np.float32(1.0) - np.float32(2.0 ** -24)
+    res = run_stochastic(w, dev)
+    assert np.all(res["n_accepted"] == 4)
+    assert np.all(res["alpha"] == 1.0)
+    assert np.all(np.abs(res["nkl"]) <= NKL_FLOOR)
+    compare_stochastic(w, res, range(w.B))
+
+
+def test_the_drafter_accepts_nothing(dev):
+    w = handmade(16, 4, 32000, synth.BF16, seed=23, the_token=17)
+    res = run_stochastic(w, dev)
+    compare_stochastic(w, res, range(w.B))
+    assert np.allclose(res["alpha"], res["p_x"], rtol=1e-3)
+    assert res["n_accepted"].sum() == 0
+
+
+def test_ties_and_flat_rows(dev):
+    V = 64
+    t = np.zeros((3, V), dtype=np.float32)
+    t[0, [5, 9, 40]] = 3.0          # tie: lowest index 5
+    t[2, [63, 62]] = 1.0            # tie at the end: 62
+    d = np.zeros((2, V), dtype=np.float32)
+    w = synth.StochasticWorkload(B=1, V=V, dtype=synth.F32, T=1.0, gammas=np.array([2], np.int32),
+                                 cu_draft=np.array([0, 2], np.int32), target=t, draft=d,
+                                 tokens=np.array([5, 0], np.int32), u_accept=np.array([0.1, 0.2], np.float32),
+                                 u_sample=np.array([0.3], np.float32))
+    res = run_greedy(w, dev)
+    assert res["n_accepted"][0] == 2 and list(res["out_tokens"]) == [5, 0, 62]
+    res = run_stochastic(w, dev)
+    compare_stochastic(w, res, [0])
+
+
+def test_nonfinite_and_token_range_are_reported(dev):
+    w = handmade(4, 3, 2048, synth.F32, seed=24)
+    w.target[1 * 4 + 2, 100] = np.inf          # sequence 1
+    w.draft[2 * 3 + 0, 7] = np.nan             # sequence 2
+    w.tokens[3 * 3 + 1] = 2048                 # sequence 3
+    res = run_stochastic(w, dev)
+    assert res["device_status"][0] == (_lib.SPEC_DEV_NONFINITE | _lib.SPEC_DEV_TOKEN_RANGE)
+    assert list(res["n_accepted"][1:]) == [-1, -1, -1]
+    assert np.all(res["out_tokens"][4:] == -1)
+    assert np.all(np.isnan(res["alpha"][3:]))
+    compare_stochastic(w, res, [0])            # the clean sequence is unaffected
+    g = run_greedy(w, dev)
+    assert g["device_status"][0] & _lib.SPEC_DEV_NONFINITE and g["n_accepted"][1] == -1
+    w2 = handmade(2, 2, 512, synth.F32, seed=25)
+    w2.target[2, 3] = -np.inf                  # the bonus row of sequence 0
+    r2 = run_stochastic(w2, dev)
+    assert r2["device_status"][0] == _lib.SPEC_DEV_NONFINITE and r2["n_accepted"][0] == -1
+    nk = run_nkl(w2, dev)
+    assert nk["device_status"][0] == 0         # the bonus row is not part of any NKL pair
+
+
+def test_ragged_with_empty_sequences_and_bad_offsets(dev):
+    w = synth.make_stochastic(9, 3000, synth.BF16, 0.8, seed=26, gamma_range=(0, 5), agreement=0.7)
+    res = run_stochastic(w, dev)
+    compare_stochastic(w, res, range(w.B))
+    compare_greedy(w, run_greedy(w, dev), range(w.B))
+    compare_nkl(w, run_nkl(w, dev), range(w.B))
+    # non-monotone offsets are reported, with every access kept in bounds
+    cu = torch.tensor([0, 5, 3, 8], dtype=torch.int32, device=dev)
+    t = torch.zeros(11, 64, dtype=torch.bfloat16, device=dev)
+    d = torch.zeros(8, 64, dtype=torch.bfloat16, device=dev)
+    r = api.spec_verify_stochastic(t, d, torch.zeros(8, dtype=torch.int32, device=dev), 1.0,
+                                   torch.zeros(8, device=dev), torch.zeros(3, device=dev), cu_draft=cu, gamma=5)
+    torch.cuda.synchronize()
+    assert int(r["device_status"][0]) & _lib.SPEC_DEV_OFFSETS
+
+
+def test_tree_shapes(dev):
+    rng = np.random.default_rng(30)
+    for parent in ([-1], [-1, 0, 1, 2, 3], [-1, 0, 0, 1, 2, -1], list(range(-1, 63))):
+        N = len(parent)
+        B, V = 7, 300
+        t32 = rng.normal(0, 1, (B * (N + 1), V)).astype(np.float32)
+        t32[:, 7] = 5.0                           # makes many nodes match
+        tok = np.where(rng.random((B, N)) < 0.85, 7, rng.integers(0, V, (B, N))).astype(np.int32)
+        w = synth.TreeWorkload(B=B, N=N, V=V, dtype=synth.BF16, parent=np.array(parent, np.int32),
+                               target=synth.storage(t32, synth.BF16), node_tokens=tok)
+        compare_tree(w, run_tree(w, dev), range(B))
+
+
+def test_output_distribution_is_the_target(dev):
+    """Losslessness on the GPU: many sequences share one row pair and differ only in
+    their uniforms; the emitted first token must follow p (chi-square)."""
+    V, B, T = 6, 200000, 0.9
+    rng = np.random.default_rng(31)
+    zt = rng.normal(0, 1.5, (2, V)).astype(np.float32)
+    zd = rng.normal(0, 1.5, (1, V)).astype(np.float32)
+    q = np.exp(zd[0] / T) / np.exp(zd[0] / T).sum()
+    x = rng.choice(V, size=B, p=q / q.sum()).astype(np.int32)    # drafts drawn from q
+    w = synth.StochasticWorkload(B=B, V=V, dtype=synth.F32, T=T, gammas=np.ones(B, np.int32),
+                                 cu_draft=np.arange(B + 1, dtype=np.int32), target=np.tile(zt, (B, 1)),
+                                 draft=np.tile(zd, (B, 1)), tokens=x,
+                                 u_accept=rng.random(B, dtype=np.float32), u_sample=rng.random(B, dtype=np.float32))
+    res = run_stochastic(w, dev)
+    first = res["out_tokens"].reshape(B, 2)[:, 0]
+    p = np.exp(zt[0].astype(np.float64) / T)
+    p /= p.sum()
+    counts = np.bincount(first, minlength=V)
+    stat, pval = scipy.stats.chisquare(counts, p * B)
+    assert pval > 1e-4, (counts, p * B)
+
+
+def test_large_vocab(dev):
+    w = handmade(2, 2, 1 << 20, synth.BF16, T=0.7, seed=32)
+    res = run_stochastic(w, dev)
+    compare_stochastic(w, res, range(w.B))
+
+
+def test_repeat_calls_reuse_workspace(dev):
+    """Tickets are re-armed by every call: two calls on one workspace give the same result,
+    also after a call with a different geometry."""
+    w = handmade(8, 3, 5000, synth.BF16, seed=33)
+    a = run_stochastic(w, dev)
+    run_stochastic(handmade(3, 5, 700, synth.F32, seed=34), dev)
+    b = run_stochastic(w, dev)
+    for k in ("n_accepted", "out_tokens", "alpha", "nkl", "greedy_tokens"):
+        assert np.array_equal(a[k], b[k]), k
