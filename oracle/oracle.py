@@ -53,6 +53,8 @@ Readings taken where the pages are silent, garbled or disagree:
       and its parent is accepted (roots compare against the parent row, row 0); the
       pick is the accepted node of greatest depth, ties to the lowest node index;
       the correction is the argmax of the picked node's row (row 0 if none).
+  R17 a one-token vocabulary (V = 1): both rows are the same point mass, KL = 0, and
+      the ratio 0 / ln 1 is taken as 0.
   R16 errors: a non-finite logit in any row a sequence uses, or a draft / node token
       outside [0, V), makes that sequence an error: its count is -1 and all its
       outputs are -1 (integers) or NaN (reals). For the standalone NKL call the
@@ -154,6 +156,8 @@ def nkl_pair(zt: np.ndarray, zd: np.ndarray, T: float):
     p = np.exp(lp)
     kl = float(np.sum(q * (lq - lp)))
     kl_eps = float(np.sum(q * (np.log(q + NKL_EPS) - np.log(p + NKL_EPS))))
+    if V == 1:                                   # R17
+        return 0.0, 0.0
     lnV = math.log(V)
     return kl / lnV, kl_eps / lnV
 

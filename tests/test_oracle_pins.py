@@ -345,6 +345,10 @@ def test_nkl_zero_on_identical_rows_and_nonnegative():
         assert O.nkl_pair(a, b, 0.6)[0] >= 0.0
 
 
+def test_nkl_one_token_vocabulary_is_zero():
+    assert O.nkl_pair(np.array([3.0]), np.array([-7.0]), 0.5) == (0.0, 0.0)
+
+
 def test_nkl_two_point_and_direction():
     """KL(q || p) with q the DRAFT row, natural log, divided by ln V: against scipy's
     relative entropy, which is not symmetric, so a swapped direction fails."""
