@@ -26,7 +26,7 @@ def run_stochastic(w, dev, T=None, delta=0.15, offset=0):
         flat = to_dev(np.ascontiguousarray(a).reshape(-1), dev)
         buf = torch.empty(flat.numel() + offset, dtype=flat.dtype, device=dev)
         buf[offset:] = flat
-        return buf[offset:]
+        return buf[offset:].view(a.shape)
 
     t = put(w.target)
     d = put(w.draft)
@@ -39,23 +39,25 @@ def run_stochastic(w, dev, T=None, delta=0.15, offset=0):
 
 
 def compare_stochastic(w, res, seqs, T=None, delta=0.15, check_greedy=True):
-    """Bit-exact n / tokens except oracle-flagged sequences; reals within REL. Returns
-    (number compared, number flagged)."""
+    """n / tokens bit-exact for every sequence the oracle does not flag; a flagged sequence
+    (a decision within 1e-5 of its boundary) may differ, but at most max(1, 1e-4 of the
+    sequences compared) may. Reals within REL. Returns (compared, flagged, mismatched)."""
     T = w.T if T is None else T
     ref = O.verify_stochastic(w.target, w.draft, w.tokens, w.cu_draft, T, w.u_accept, w.u_sample, w.dtype,
                               nkl_delta=delta, seqs=seqs)
-    flagged = 0
+    flagged = mismatched = 0
+    seqs = list(seqs)
     for b in seqs:
         r = ref[b]
         g = int(w.gammas[b])
         t0, d0 = w.target_base(b), w.draft_base(b)
         n = int(res["n_accepted"][b])
         toks = res["out_tokens"][t0:t0 + g + 1]
-        if r["flag"]:
-            flagged += 1
-        else:
-            assert n == r["n"], (b, n, r["n"], r["alpha"], w.u_accept[d0:d0 + g])
-            assert list(toks) == list(r["tokens"]), (b, toks, r["tokens"])
+        same = n == r["n"] and list(toks) == list(r["tokens"])
+        flagged += int(r["flag"])
+        if not same:
+            assert r["flag"], (b, n, r["n"], list(toks), list(r["tokens"]), r["alpha"], w.u_accept[d0:d0 + g])
+            mismatched += 1
         if g:
             for k in ("p_x", "q_x", "alpha"):
                 got = res[k][d0:d0 + g].astype(np.float64)
@@ -68,7 +70,8 @@ def compare_stochastic(w, res, seqs, T=None, delta=0.15, check_greedy=True):
         if check_greedy:
             assert int(res["greedy_n"][b]) == r["greedy_n"]
             assert list(res["greedy_tokens"][t0:t0 + g + 1]) == list(r["greedy_tokens"])
-    return len(list(seqs)), flagged
+    assert mismatched <= max(1, int(1e-4 * len(seqs))), (mismatched, len(seqs))
+    return len(seqs), flagged, mismatched
 
 
 def run_greedy(w, dev):
