@@ -60,7 +60,8 @@ typedef enum {
   SPEC_ERR_INVALID_ARG = 1, /* null pointer, bad size, non-finite or non-positive T, bad tree */
   SPEC_ERR_DTYPE = 2,       /* unknown spec_dtype */
   SPEC_ERR_WORKSPACE = 3,   /* workspace NULL or smaller than spec_workspace_bytes() */
-  SPEC_ERR_CUDA = 6         /* a kernel launch failed (cudaGetLastError after launch) */
+  SPEC_ERR_CUDA = 6,        /* a CUDA call or kernel launch failed */
+  SPEC_ERR_TOO_LARGE = 7    /* spec_verify_stochastic_static: the problem needs more scratch than it has */
 } spec_status;
 
 /* bits of *device_status */
@@ -172,6 +173,36 @@ spec_status spec_nkl(spec_batch g, spec_dtype dtype, const void* target_logits, 
                      float temperature, float delta, float* nkl, uint8_t* nkl_mask,
                      uint32_t* device_status, void* workspace, size_t workspace_bytes,
                      spec_stream_t stream);
+
+/*
+ * spec_verify_stochastic without a workspace argument: the same computation, inputs and
+ * outputs, with its scratch memory inside the library. The pages have no counterpart to
+ * this entry point; it exists for callers that cannot allocate device memory -- code that
+ * is handed its buffers by a host framework (for example a plugin whose memory pool is
+ * owned by an inference server) and must not call cudaMalloc/cudaFree, which may
+ * synchronise the device or fragment a pool it does not own.
+ *
+ *   - Nothing is allocated: the scratch is one static device array of
+ *     SPEC_STATIC_SCRATCH_BYTES bytes, present on every GPU that loads the library until
+ *     the process exits. A problem whose spec_workspace_bytes(g, SPEC_MODE_STOCHASTIC)
+ *     exceeds it returns SPEC_ERR_TOO_LARGE before anything runs.
+ *   - The first call on each device (with that device current) looks up the array's
+ *     device address with cudaGetSymbolAddress and caches it; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array. Calls on the same stream are ordered
+ *     and safe; calls that overlap on the GPU (other streams, other host threads) race
+ *     on it and give undefined results. Each call re-initialises what it needs, so no
+ *     state carries over from the previous call.
+ */
+#define SPEC_STATIC_SCRATCH_BYTES (1u << 20)
+
+spec_status spec_verify_stochastic_static(spec_batch g, spec_dtype dtype, const void* target_logits,
+                                          const void* draft_logits, const int32_t* draft_tokens,
+                                          float temperature, const float* u_accept, const float* u_sample,
+                                          int32_t* n_accepted, int32_t* out_tokens, float* p_x, float* q_x,
+                                          float* alpha, float* nkl, uint8_t* nkl_mask, float nkl_delta,
+                                          int32_t* greedy_n, int32_t* greedy_tokens, uint32_t* device_status,
+                                          spec_stream_t stream);
 
 /* A static English description of a spec_status value. */
 const char* spec_status_str(spec_status s);

@@ -15,6 +15,8 @@ SPEC_ERR_INVALID_ARG = 1
 SPEC_ERR_DTYPE = 2
 SPEC_ERR_WORKSPACE = 3
 SPEC_ERR_CUDA = 6
+SPEC_ERR_TOO_LARGE = 7
+SPEC_STATIC_SCRATCH_BYTES = 1 << 20
 
 SPEC_DEV_TOKEN_RANGE = 1
 SPEC_DEV_NONFINITE = 2
@@ -47,6 +49,8 @@ SIGNATURES = {
     "spec_tree_depth": (_I, [_P, _I]),
     "spec_verify_stochastic": (ctypes.c_int, [SpecBatch, ctypes.c_int, _P, _P, _P, _F, _P, _P, _P, _P, _P, _P, _P,
                                               _P, _P, _F, _P, _P, _P, _P, _S, _P]),
+    "spec_verify_stochastic_static": (ctypes.c_int, [SpecBatch, ctypes.c_int, _P, _P, _P, _F, _P, _P, _P, _P, _P,
+                                                     _P, _P, _P, _P, _F, _P, _P, _P, _P]),
     "spec_verify_greedy": (ctypes.c_int, [SpecBatch, ctypes.c_int, _P, _P, _P, _P, _P, _P, _S, _P]),
     "spec_verify_tree": (ctypes.c_int, [_I, _I, _I, ctypes.c_int, _P, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
     "spec_nkl": (ctypes.c_int, [SpecBatch, ctypes.c_int, _P, _P, _F, _F, _P, _P, _P, _P, _S, _P]),

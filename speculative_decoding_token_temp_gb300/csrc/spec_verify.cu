@@ -363,8 +363,68 @@ const char* spec_status_str(spec_status s) {
     case SPEC_ERR_DTYPE: return "unknown dtype";
     case SPEC_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case SPEC_ERR_CUDA: return "CUDA launch failed";
+    case SPEC_ERR_TOO_LARGE: return "problem needs more scratch than SPEC_STATIC_SCRATCH_BYTES";
   }
   return "unknown status";
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Stochastic verification for callers that cannot allocate device memory.
+//
+// Some callers are handed their input and output buffers by a host framework and have
+// no device allocator of their own: a plugin inside an inference server whose memory
+// pool is owned by the server, or a decode loop that must not call cudaMalloc/cudaFree
+// because those may synchronise the device or fragment a pool managed elsewhere. For
+// them the scratch memory lives in the library itself: a fixed array in device memory,
+// created when the library is loaded on a GPU and kept until the process exits.
+
+#include <mutex>
+
+static __device__ __align__(256) unsigned char spec_static_scratch[SPEC_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void* g_static_addr[kMaxDevices];  // device address of spec_static_scratch, per device
+
+// Device address of the static scratch on the current device. Host code cannot use the
+// symbol itself (on the host it names a stand-in, not device memory), so the address is
+// looked up once per device with that device current and cached.
+cudaError_t static_scratch_address(void** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (g_static_addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, spec_static_scratch);
+    if (e != cudaSuccess) return e;
+    g_static_addr[dev] = p;
+  }
+  *out = g_static_addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" spec_status spec_verify_stochastic_static(
+    spec_batch g, spec_dtype dtype, const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
+    float temperature, const float* u_accept, const float* u_sample, int32_t* n_accepted, int32_t* out_tokens,
+    float* p_x, float* q_x, float* alpha, float* nkl, uint8_t* nkl_mask, float nkl_delta, int32_t* greedy_n,
+    int32_t* greedy_tokens, uint32_t* device_status, spec_stream_t stream) {
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
+  if (check_batch(g) != SPEC_OK) return SPEC_ERR_INVALID_ARG;
+  // Everything in the scratch that must start at zero (the per-sequence tickets) or in a
+  // known state (the per-sequence records) is reset by the first kernel of every call;
+  // the rest is written before it is read. Nothing carries over between calls.
+  if (spec_workspace_bytes(g, SPEC_MODE_STOCHASTIC) > (size_t)SPEC_STATIC_SCRATCH_BYTES) return SPEC_ERR_TOO_LARGE;
+  void* ws = nullptr;
+  if (static_scratch_address(&ws) != cudaSuccess) return SPEC_ERR_CUDA;
+  return spec_verify_stochastic(g, dtype, target_logits, draft_logits, draft_tokens, temperature, u_accept, u_sample,
+                                n_accepted, out_tokens, p_x, q_x, alpha, nkl, nkl_mask, nkl_delta, greedy_n,
+                                greedy_tokens, device_status, ws, (size_t)SPEC_STATIC_SCRATCH_BYTES, stream);
+}
