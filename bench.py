@@ -273,7 +273,7 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     __graft_entry__.build()
     cfg = synth.CONFIGS[HEADLINE]
-    w = cfg.make(seed=cfg.seed + 1000 * rank)
+    w = cfg.make(seed=cfg.seed + 1000 * rank, B=args.batch)
     call = StochasticCall(w, dev, host_inputs=True)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
@@ -349,7 +349,7 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "B256_g8_V128256_bf16: stochastic verify + NKL(delta=0.15) + greedy, one call",
+        "config": {"workload": f"B{w.B}_g8_V128256_bf16: stochastic verify + NKL(delta=0.15) + greedy, one call",
                    "B": w.B, "gamma": 8, "V": w.V, "T": w.T, "seed": cfg.seed, "rows_per_step": rows_step,
                    "l2": "inputs 1116 MB per step, larger than the 129 MB L2; no flush",
                    "parallelism": f"{world} independent shard(s), no collective"},
@@ -443,6 +443,8 @@ def main():
     ap.add_argument("--no-modes", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--skip-ragged", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="sequences per step (default: the workload's 256); smaller slices serve profiling")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -68,6 +68,7 @@ typedef enum {
 #define SPEC_DEV_TOKEN_RANGE 1u /* a draft or node token outside [0, V) ([PD] section 4.1: token ids must agree) */
 #define SPEC_DEV_NONFINITE 2u   /* a NaN or infinite logit in a row the sequence uses */
 #define SPEC_DEV_OFFSETS 4u     /* cu_draft not non-decreasing from 0 to total_draft, or a gamma_b > gamma */
+#define SPEC_DEV_TIMEOUT 8u     /* an internal wait gave up (bounded waits); the affected sequences are undecided */
 
 typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
 

@@ -21,6 +21,7 @@ SPEC_STATIC_SCRATCH_BYTES = 1 << 20
 SPEC_DEV_TOKEN_RANGE = 1
 SPEC_DEV_NONFINITE = 2
 SPEC_DEV_OFFSETS = 4
+SPEC_DEV_TIMEOUT = 8
 
 SPEC_F32 = 0
 SPEC_BF16 = 1

@@ -4,13 +4,15 @@
 //   prologue_kernel  zeroes the per-sequence tickets, marks every sequence "pending",
 //                    checks packed offsets.
 //   rows_kernel      one block per (row, vocabulary chunk) tile. Streams the target row
-//                    (and, for a pair, the draft row) once with 16-byte read-only loads
-//                    and keeps per-thread online statistics: the raw maximum and its
-//                    lowest index, sum_v exp((z_v - max)/T), and for the draft row also
-//                    sum_v exp((zd_v - max_d)/T) (zd_v - zt_v). Block-reduces them into a
-//                    32-byte partial. The last tile of a sequence to finish (an atomic
-//                    ticket, no waiting) merges the partials of all its rows and applies
-//                    the acceptance rule, NKL, greedy or tree decision.
+//                    (and, for a pair, the draft row) once -- on aligned rows through a
+//                    per-thread 4-stage cp.async ring in shared memory, otherwise with
+//                    scalar read-only loads -- and keeps per-thread online statistics: the
+//                    raw maximum and its lowest index, sum_v exp((z_v - ref)/T), and for
+//                    the draft row also sum_v exp((zd_v - ref_d)/T) (zd_v - zt_v).
+//                    Block-reduces them into a 32-byte partial. The last tile of a
+//                    sequence to finish (an atomic ticket, no waiting) merges the partials
+//                    of all its rows and applies the acceptance rule, NKL, greedy or tree
+//                    decision.
 //   sample_kernel    (stochastic only) one block per (vocabulary segment, sequence):
 //                    masses of the residual max(0, p - q) (or of p for the bonus row) on
 //                    the one row pair the sequence needs; the last segment's block finds
@@ -161,6 +163,18 @@ __device__ __forceinline__ int warp_min_i(int x) {
   return x;
 }
 
+// Barrier policies: the whole block, or only the NT consumer threads of a warp-specialised
+// block (named barrier 1; the producer warp never joins it).
+struct BlockSync {
+  static constexpr int NT = kThreads;
+  __device__ static void sync() { __syncthreads(); }
+};
+template <int N>
+struct NamedSync {
+  static constexpr int NT = N;
+  __device__ static void sync() { asm volatile("bar.sync 1, %0;" ::"n"(N) : "memory"); }
+};
+
 // s was accumulated relative to max m; express it relative to M >= m.
 __device__ __forceinline__ float rescale(float s, float m, float M, float c) {
   return (m == -INFINITY) ? s * 0.f : s * ex2((m - M) * c);
@@ -226,20 +240,116 @@ __device__ __forceinline__ float elem_at<float>(const float* row, int x) {
 }
 
 // ---------------------------------------------------------------------------
-// per-thread online statistics
+// packed arithmetic: two fp32 lanes per instruction (sm_100 family), 3-input min/max
+
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  float2 d;
+  asm("{.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  float2 d;
+  asm("{.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 d;
+  asm("{.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float max3_nan(float a, float b, float c) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float min3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// N-element max / min as a shallow tree of 3-input instructions (N in {1, 4, 8, 16})
+template <int N>
+__device__ __forceinline__ float vmax(const float (&t)[N]) {
+  if constexpr (N == 16)
+    return fmaxf(max3(max3(t[0], t[1], t[2]), max3(t[3], t[4], t[5]), max3(t[6], t[7], t[8])),
+                 max3(max3(t[9], t[10], t[11]), max3(t[12], t[13], t[14]), t[15]));
+  else if constexpr (N == 8) return max3(max3(t[0], t[1], t[2]), max3(t[3], t[4], t[5]), fmaxf(t[6], t[7]));
+  else if constexpr (N == 4) return max3(t[0], t[1], fmaxf(t[2], t[3]));
+  else return t[0];
+}
+template <int N>
+__device__ __forceinline__ float vmax_nan(const float (&t)[N]) {
+  if constexpr (N == 16)
+    return max_nan(max3_nan(max3_nan(t[0], t[1], t[2]), max3_nan(t[3], t[4], t[5]), max3_nan(t[6], t[7], t[8])),
+                   max3_nan(max3_nan(t[9], t[10], t[11]), max3_nan(t[12], t[13], t[14]), t[15]));
+  else if constexpr (N == 8)
+    return max3_nan(max3_nan(t[0], t[1], t[2]), max3_nan(t[3], t[4], t[5]), max_nan(t[6], t[7]));
+  else if constexpr (N == 4) return max3_nan(t[0], t[1], max_nan(t[2], t[3]));
+  else return t[0];
+}
+template <int N>
+__device__ __forceinline__ float vmin(const float (&t)[N]) {
+  if constexpr (N == 16)
+    return fminf(min3(min3(t[0], t[1], t[2]), min3(t[3], t[4], t[5]), min3(t[6], t[7], t[8])),
+                 min3(min3(t[9], t[10], t[11]), min3(t[12], t[13], t[14]), t[15]));
+  else if constexpr (N == 8) return min3(min3(t[0], t[1], t[2]), min3(t[3], t[4], t[5]), fminf(t[6], t[7]));
+  else if constexpr (N == 4) return min3(t[0], t[1], fminf(t[2], t[3]));
+  else return t[0];
+}
+
+// ---------------------------------------------------------------------------
+// per-thread online statistics.
+//
+// m is the exact running maximum of the raw logits (and idx the lowest index holding
+// it). The sums are kept relative to a lazier reference mr <= m: mr moves (and the sums
+// are rescaled) only when a new value exceeds it by more than kLazy in the exponent, so
+// every term stays below 2^kLazy and the common case costs no rescale at all. Sums are
+// kept as two fp32 lanes (even / odd elements) for the packed instructions.
+
+constexpr float kLazy = 32.f;
 
 struct TAcc {
-  float m, s, nmc, lo, hi;
-  int idx;
+  float m, mr, mth, nmc, lo, hi;
+  float2 s;
+  int idx;     // lowest index of m (scalar path), or -1 until resolved
+  int g0, g1;  // element bases of the group that holds m (vector path; resolved at the tile end)
 };
 struct DAcc {
-  float m, s, k, nmc;
+  float mr, mth, nmc;
+  float2 s, k;
 };
 
 __device__ __forceinline__ void init(TAcc& a) {
-  a.m = -INFINITY; a.s = 0.f; a.nmc = 0.f; a.lo = INFINITY; a.hi = -INFINITY; a.idx = INT_MAX;
+  a.m = -INFINITY; a.mr = -INFINITY; a.mth = -INFINITY; a.nmc = 0.f; a.lo = INFINITY; a.hi = -INFINITY;
+  a.s = make_float2(0.f, 0.f); a.idx = INT_MAX; a.g0 = -1; a.g1 = -1;
 }
-__device__ __forceinline__ void init(DAcc& a) { a.m = -INFINITY; a.s = 0.f; a.k = 0.f; a.nmc = 0.f; }
+__device__ __forceinline__ void init(DAcc& a) {
+  a.mr = -INFINITY; a.mth = -INFINITY; a.nmc = 0.f; a.s = make_float2(0.f, 0.f); a.k = make_float2(0.f, 0.f);
+}
 
 template <int VEC>
 __device__ __forceinline__ float tree_sum(const float (&e)[VEC]) {
@@ -261,118 +371,187 @@ __device__ __forceinline__ int lowest_match(const float (&t)[VEC], float v) {
   return k;
 }
 
-// target row with sum (bonus row of the stochastic call); LO tracks the minimum so a
-// -inf entry, which the sum alone cannot see, is still reported
+// Element index of position k of a group whose first H elements start at e0 and whose
+// remaining elements start at e1 (e1 = e0 + H for a contiguous group).
+template <int H>
+__device__ __forceinline__ int group_index(int k, int e0, int e1) {
+  return k < H ? e0 + k : e1 + (k - H);
+}
+
+// exp2(t * c + nmc) for every element, summed into a pair of lanes (pairwise tree)
 template <int VEC>
-__device__ __forceinline__ void tsum_update(TAcc& a, const float (&t)[VEC], int e0, float c) {
-  float vm = t[0], vl = t[0];
+__device__ __forceinline__ float2 exp_sum2(const float (&t)[VEC], float c, float nmc, float (&e)[VEC]) {
+  if constexpr (VEC == 1) {
+    e[0] = ex2(fmaf(t[0], c, nmc));
+    return make_float2(e[0], 0.f);
+  } else {
+    const float2 c2 = make_float2(c, c), n2 = make_float2(nmc, nmc);
+    float2 acc[VEC / 2];
 #pragma unroll
-  for (int k = 1; k < VEC; ++k) {
-    vm = fmaxf(vm, t[k]);
-    vl = fminf(vl, t[k]);
+    for (int j = 0; j < VEC / 2; ++j) {
+      const float2 x = fma2(make_float2(t[2 * j], t[2 * j + 1]), c2, n2);
+      e[2 * j] = ex2(x.x);
+      e[2 * j + 1] = ex2(x.y);
+      acc[j] = make_float2(e[2 * j], e[2 * j + 1]);
+    }
+#pragma unroll
+    for (int w = VEC / 4; w >= 1; w >>= 1)
+#pragma unroll
+      for (int j = 0; j < w; ++j) acc[j] = add2(acc[j], acc[j + w]);
+    return acc[0];
   }
-  a.lo = fminf(a.lo, vl);
-  if (vm > a.m) {
-    a.s *= ex2((a.m - vm) * c);
-    a.m = vm;
-    a.nmc = -vm * c;
-    a.idx = e0 + lowest_match<VEC>(t, vm);
+}
+
+// Exact max. A single-element group (scalar path) records its index directly; a wider
+// group only records where it starts, and the lowest index inside it is found once, at
+// the end of the tile, by the thread that holds the tile's maximum (resolve_index).
+template <int VEC, int H, bool IDX>
+__device__ __forceinline__ void track_max(TAcc& a, const float (&t)[VEC], float vm, int e0, int e1) {
+  if (IDX) {
+    if (vm > a.m) {
+      if constexpr (VEC == 1) {
+        a.idx = e0;
+      } else {
+        a.g0 = e0;
+        a.g1 = (H == VEC) ? e0 + H : e1;
+      }
+    }
   }
+  a.m = fmaxf(a.m, vm);
+}
+
+// move the sum reference when vm exceeds it by more than kLazy (rare; warp-uniform branch)
+__device__ __forceinline__ void lazy_ref(float& mr, float& mth, float& nmc, float2& s, float2* k, float vm, float c) {
+  const bool mv = vm > mth;
+  if (__any_sync(__activemask(), mv)) {
+    if (mv) {
+      const float f = ex2((mr - vm) * c);
+      s = make_float2(s.x * f, s.y * f);
+      if (k) *k = make_float2(k->x * f, k->y * f);
+      mr = vm;
+      mth = vm + kLazy / c;
+      nmc = -vm * c;
+    }
+  }
+}
+
+// target row with sum (bonus row of the stochastic call); lo tracks the minimum so a
+// -inf entry, which the sum alone cannot see, is still reported
+template <int VEC, int H = VEC>
+__device__ __forceinline__ void tsum_update(TAcc& a, const float (&t)[VEC], int e0, float c, int e1 = 0) {
+  const float vm = vmax<VEC>(t);
+  a.lo = fminf(a.lo, vmin<VEC>(t));
+  track_max<VEC, H, true>(a, t, vm, e0, e1);
+  lazy_ref(a.mr, a.mth, a.nmc, a.s, nullptr, vm, c);
   float e[VEC];
-#pragma unroll
-  for (int k = 0; k < VEC; ++k) e[k] = ex2(fmaf(t[k], c, a.nmc));
-  a.s += tree_sum<VEC>(e);
+  a.s = add2(a.s, exp_sum2<VEC>(t, c, a.nmc, e));
 }
 
 // argmax only (greedy and tree rows): no exponentials; hi propagates NaN
-template <int VEC>
-__device__ __forceinline__ void argmax_update(TAcc& a, const float (&t)[VEC], int e0) {
-  float vh = t[0], vl = t[0];
-#pragma unroll
-  for (int k = 1; k < VEC; ++k) {
-    vh = max_nan(vh, t[k]);
-    vl = fminf(vl, t[k]);
-  }
+template <int VEC, int H = VEC>
+__device__ __forceinline__ void argmax_update(TAcc& a, const float (&t)[VEC], int e0, int e1 = 0) {
+  const float vh = vmax_nan<VEC>(t);
   a.hi = max_nan(a.hi, vh);
-  a.lo = fminf(a.lo, vl);
-  if (vh > a.m) {
-    a.m = vh;
-    a.idx = e0 + lowest_match<VEC>(t, vh);
-  }
+  a.lo = fminf(a.lo, vmin<VEC>(t));
+  track_max<VEC, H, true>(a, t, vh, e0, e1);
 }
 
 // (target row, draft row) pair; a -inf or NaN in either makes the KL sum non-finite
-template <int VEC, bool IDX>
+template <int VEC, bool IDX, int H = VEC>
 __device__ __forceinline__ void pair_update(TAcc& a, DAcc& d, const float (&t)[VEC], const float (&z)[VEC], int e0,
-                                            float c) {
-  float tm = t[0], dm = z[0];
-#pragma unroll
-  for (int k = 1; k < VEC; ++k) {
-    tm = fmaxf(tm, t[k]);
-    dm = fmaxf(dm, z[k]);
-  }
-  if (tm > a.m) {
-    a.s *= ex2((a.m - tm) * c);
-    a.m = tm;
-    a.nmc = -tm * c;
-    if (IDX) a.idx = e0 + lowest_match<VEC>(t, tm);
-  }
-  if (dm > d.m) {
-    const float f = ex2((d.m - dm) * c);
-    d.s *= f;
-    d.k *= f;
-    d.m = dm;
-    d.nmc = -dm * c;
-  }
+                                            float c, int e1 = 0) {
+  const float tm = vmax<VEC>(t), dm = vmax<VEC>(z);
+  track_max<VEC, H, IDX>(a, t, tm, e0, e1);
+  lazy_ref(a.mr, a.mth, a.nmc, a.s, nullptr, tm, c);
+  lazy_ref(d.mr, d.mth, d.nmc, d.s, &d.k, dm, c);
   float et[VEC], ed[VEC];
-  float k0 = 0.f, k1 = 0.f;
+  a.s = add2(a.s, exp_sum2<VEC>(t, c, a.nmc, et));
+  d.s = add2(d.s, exp_sum2<VEC>(z, c, d.nmc, ed));
+  if constexpr (VEC == 1) {
+    d.k.x = fmaf(ed[0], z[0] - t[0], d.k.x);
+  } else if constexpr (VEC <= 4) {
 #pragma unroll
-  for (int k = 0; k < VEC; ++k) {
-    et[k] = ex2(fmaf(t[k], c, a.nmc));
-    ed[k] = ex2(fmaf(z[k], c, d.nmc));
-    if (k & 1)
-      k1 = fmaf(ed[k], z[k] - t[k], k1);
-    else
-      k0 = fmaf(ed[k], z[k] - t[k], k0);
+    for (int j = 0; j < VEC / 2; ++j) {
+      const float2 dz = sub2(make_float2(z[2 * j], z[2 * j + 1]), make_float2(t[2 * j], t[2 * j + 1]));
+      d.k = fma2(make_float2(ed[2 * j], ed[2 * j + 1]), dz, d.k);
+    }
+  } else {
+    // two independent accumulation chains, folded at the end of the group
+    float2 k1 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < VEC / 2; j += 2) {
+      const float2 dz0 = sub2(make_float2(z[2 * j], z[2 * j + 1]), make_float2(t[2 * j], t[2 * j + 1]));
+      const float2 dz1 = sub2(make_float2(z[2 * j + 2], z[2 * j + 3]), make_float2(t[2 * j + 2], t[2 * j + 3]));
+      d.k = fma2(make_float2(ed[2 * j], ed[2 * j + 1]), dz0, d.k);
+      k1 = fma2(make_float2(ed[2 * j + 2], ed[2 * j + 3]), dz1, k1);
+    }
+    d.k = add2(d.k, k1);
   }
-  a.s += tree_sum<VEC>(et);
-  d.s += tree_sum<VEC>(ed);
-  d.k += k0 + k1;
 }
 
 // ---------------------------------------------------------------------------
 // block reduction of a tile into a Partial (valid in thread 0)
 
-__device__ __forceinline__ Partial reduce_tile(int kind, const TAcc& ta, const DAcc& da, float c) {
-  __shared__ float s_m[2][kWarps];
-  __shared__ float s_v[5][kWarps];
-  __shared__ int s_i[kWarps];
+// Lowest index of the value m inside the recorded group (g0: first VEC elements, g1:
+// the next VEC), re-read from the row (an L2 hit: the tile has just streamed it).
+template <typename E, int VEC>
+__device__ __forceinline__ int resolve_index(const E* row, int g0, int g1, float m) {
+  if (g0 < 0) return INT_MAX;
+  float f[VEC];
+  IO<E, VEC>::unpack(ld_stream16(row + g0), f);
+#pragma unroll
+  for (int k = 0; k < VEC; ++k)
+    if (f[k] == m) return g0 + k;
+  IO<E, VEC>::unpack(ld_stream16(row + g1), f);
+#pragma unroll
+  for (int k = 0; k < VEC; ++k)
+    if (f[k] == m) return g1 + k;
+  return INT_MAX;
+}
+
+// row != nullptr: the target maximum's index is resolved from the recorded groups
+template <class SY, typename E = float, int VEC = 1>
+__device__ __forceinline__ Partial reduce_tile(int kind, const TAcc& ta, const DAcc& da, float c,
+                                               const E* row = nullptr) {
+  constexpr int NW = SY::NT / 32;
+  __shared__ float s_m[2][NW];
+  __shared__ float s_v[5][NW];
+  __shared__ int s_i[NW];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const float wtm = warp_max(ta.m);
-  const float wdm = (kind == K_PAIR) ? warp_max(da.m) : -INFINITY;
+  const float wdm = (kind == K_PAIR) ? warp_max(da.mr) : -INFINITY;
   if (lane == 0) {
     s_m[0][warp] = wtm;
     s_m[1][warp] = wdm;
   }
-  __syncthreads();
+  SY::sync();
   float TM = s_m[0][0], DM = s_m[1][0];
 #pragma unroll
-  for (int w = 1; w < kWarps; ++w) {
+  for (int w = 1; w < NW; ++w) {
     TM = fmaxf(TM, s_m[0][w]);
     DM = fmaxf(DM, s_m[1][w]);
   }
-  const int wi = warp_min_i(ta.m == TM ? ta.idx : INT_MAX);
+  int my_idx = INT_MAX;
+  if (ta.m == TM) {
+    if constexpr (VEC > 1)
+      my_idx = row ? resolve_index<E, VEC>(row, ta.g0, ta.g1, TM) : INT_MAX;
+    else
+      my_idx = ta.idx;
+  }
+  const int wi = warp_min_i(my_idx);
   float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f, v4 = 0.f;
   if (kind == K_ARGMAX) {
     v0 = warp_max_nan(ta.hi);
     v1 = warp_min(ta.lo);
   } else {
-    v0 = warp_sum(rescale(ta.s, ta.m, TM, c));
+    // target sums are expressed relative to the exact tile maximum TM (mr <= m <= TM);
+    // draft sums relative to DM, the largest draft reference
+    v0 = warp_sum(rescale(ta.s.x + ta.s.y, ta.mr, TM, c));
     if (kind == K_TSUM) v1 = warp_min(ta.lo);
     if (kind == K_PAIR) {
-      const float fd = (da.m == -INFINITY) ? 0.f : ex2((da.m - DM) * c);
-      v2 = warp_sum(da.s * fd);
-      v3 = warp_sum(da.k * fd);
+      const float fd = (da.mr == -INFINITY) ? 0.f : ex2((da.mr - DM) * c);
+      v2 = warp_sum((da.s.x + da.s.y) * fd);
+      v3 = warp_sum((da.k.x + da.k.y) * fd);
     }
   }
   if (lane == 0) {
@@ -383,7 +562,7 @@ __device__ __forceinline__ Partial reduce_tile(int kind, const TAcc& ta, const D
     s_v[4][warp] = v4;
     s_i[warp] = wi;
   }
-  __syncthreads();
+  SY::sync();
   Partial out;
   out.tm = TM;
   out.dm = DM;
@@ -394,16 +573,16 @@ __device__ __forceinline__ Partial reduce_tile(int kind, const TAcc& ta, const D
   if (threadIdx.x == 0) {
     int idx = INT_MAX;
     float a0 = s_v[0][0], a1 = s_v[1][0], a2 = 0.f, a3 = 0.f;
-    for (int w = 0; w < kWarps; ++w) idx = min(idx, s_i[w]);
+    for (int w = 0; w < NW; ++w) idx = min(idx, s_i[w]);
     if (kind == K_ARGMAX) {
-      for (int w = 1; w < kWarps; ++w) {
+      for (int w = 1; w < NW; ++w) {
         a0 = max_nan(a0, s_v[0][w]);
         a1 = fminf(a1, s_v[1][w]);
       }
       out.bad = (isnan(a0) || a0 == INFINITY || a1 == -INFINITY) ? 1 : 0;
     } else {
       a0 = 0.f;
-      for (int w = 0; w < kWarps; ++w) {
+      for (int w = 0; w < NW; ++w) {
         a0 += s_v[0][w];
         a2 += s_v[2][w];
         a3 += s_v[3][w];
@@ -411,7 +590,7 @@ __device__ __forceinline__ Partial reduce_tile(int kind, const TAcc& ta, const D
       out.ts = a0;
       bool bad = !isfinite(a0) || !isfinite(TM);
       if (kind == K_TSUM) {
-        for (int w = 1; w < kWarps; ++w) a1 = fminf(a1, s_v[1][w]);
+        for (int w = 1; w < NW; ++w) a1 = fminf(a1, s_v[1][w]);
         bad = bad || a1 == -INFINITY;
       } else {
         out.ds = a2;

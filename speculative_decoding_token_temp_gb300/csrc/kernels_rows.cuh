@@ -32,9 +32,10 @@ __global__ void prologue_kernel(const __grid_constant__ ProParams p) {
 // ---------------------------------------------------------------------------
 // finalisation, run by the last tile of a sequence
 
-template <typename E, int MODE>
+template <typename E, int MODE, class SY>
 __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int row0, int c0) {
   constexpr int HB = (MODE == M_NKL) ? 0 : 1;
+  constexpr int NT = SY::NT, NW = SY::NT / 32;
   __shared__ RowStat rs[kMaxRows];
   __shared__ int s_n, s_gn;
   __shared__ unsigned s_err;
@@ -47,11 +48,11 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
     s_gn = gb;
     s_err = 0u;
   }
-  for (int i = warp; i < R; i += kWarps) {
+  for (int i = warp; i < R; i += NW) {
     const RowStat r = merge_row(p.part + (size_t)(row0 + i) * p.nchunks, p.nchunks, c);
     if (lane == 0) rs[i] = r;
   }
-  __syncthreads();
+  SY::sync();
 
   const int tb = c0 + b * HB;  // first target row of the sequence (NKL: c0 + b, set below)
   const int db = c0;           // first draft row / token / u_accept entry
@@ -109,7 +110,7 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
     return;
   } else if constexpr (MODE == M_NKL) {
     const int tbn = c0 + b;
-    for (int i = tid; i < gb; i += kThreads) {
+    for (int i = tid; i < gb; i += NT) {
       const RowStat r = rs[i];
       float v = __int_as_float(0x7fc00000);
       uint8_t m = 0;
@@ -128,7 +129,7 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
     return;
   } else {
   // stochastic and greedy: validate the sequence first
-  for (int i = tid; i < R; i += kThreads) {
+  for (int i = tid; i < R; i += NT) {
     unsigned e = rs[i].bad ? SPEC_DEV_NONFINITE : 0u;
     if (i < gb) {
       const int x = p.tokens[db + i];
@@ -136,10 +137,10 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
     }
     if (e) atomicOr(&s_err, e);
   }
-  __syncthreads();
+  SY::sync();
   if (s_err) {
     if (tid == 0) atomicOr(p.status, s_err);
-    for (int k = tid; k <= gb; k += kThreads) {
+    for (int k = tid; k <= gb; k += NT) {
       p.out_tok[tb + k] = -1;
       if (MODE == M_STOCH && p.g_tok) p.g_tok[tb + k] = -1;
       if (MODE == M_STOCH && k < gb) {
@@ -168,17 +169,17 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
   }
 
   if constexpr (MODE == M_GREEDY) {
-    for (int i = tid; i < gb; i += kThreads)
+    for (int i = tid; i < gb; i += NT)
       if (p.tokens[db + i] != rs[i].tidx) atomicMin(&s_gn, i);
-    __syncthreads();
+    SY::sync();
     const int n = s_gn;
-    for (int k = tid; k <= gb; k += kThreads)
+    for (int k = tid; k <= gb; k += NT)
       p.out_tok[tb + k] = (k < n) ? p.tokens[db + k] : (k == n ? rs[n].tidx : -1);
     if (tid == 0) p.n_acc[b] = n;
     return;
   } else {
   // stochastic
-  for (int i = tid; i < gb; i += kThreads) {
+  for (int i = tid; i < gb; i += NT) {
     const RowStat r = rs[i];
     const int x = p.tokens[db + i];
     const float zt = elem_at<E>(target + (size_t)(tb + i) * V, x);
@@ -199,9 +200,9 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
     if (!(p.u_accept[db + i] <= a)) atomicMin(&s_n, i);
     if (x != r.tidx) atomicMin(&s_gn, i);
   }
-  __syncthreads();
+  SY::sync();
   const int n = s_n, gn = s_gn;
-  for (int k = tid; k <= gb; k += kThreads) {
+  for (int k = tid; k <= gb; k += NT) {
     const int xk = (k < gb) ? p.tokens[db + k] : -1;
     if (k != n) p.out_tok[tb + k] = (k < n) ? xk : -1;
     if (p.g_tok) p.g_tok[tb + k] = (k < gn) ? xk : (k == gn ? rs[gn].tidx : -1);
@@ -227,11 +228,116 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
 // ---------------------------------------------------------------------------
 // tile kernel
 
+constexpr int kCS = 4;   // stages of each thread's cp.async ring (vector path)
+constexpr int kCV = 4;   // 16-byte vectors per thread per stage
+constexpr int kRowsSmem = kCS * kCV * kThreads * 16;  // dynamic shared memory of the vector path
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Two vectors of a stage as one 2*VEC-element group (va < vb, element bases va*VEC, vb*VEC).
+template <typename E, int VEC>
+__device__ __forceinline__ void unpack2(const uint4& a, const uint4& b, float (&f)[2 * VEC]) {
+  float fa[VEC], fb[VEC];
+  IO<E, VEC>::unpack(a, fa);
+  IO<E, VEC>::unpack(b, fb);
+#pragma unroll
+  for (int k = 0; k < VEC; ++k) {
+    f[k] = fa[k];
+    f[VEC + k] = fb[k];
+  }
+}
+
+// Vector path: every thread streams its own vectors through a private kCS-stage ring of
+// cp.async copies in shared memory (lane-interleaved, so both the copies and the reads
+// are bank-conflict free), waiting with cp.async.wait_group only -- no barriers, no
+// registers held by loads in flight. A stage is kCV vectors per thread: for a pair the
+// vectors v and v + 256 of the target and of the draft row, for a single row the vectors
+// v, v + 256, v + 512, v + 768; each pair of vectors is folded in as one group.
+template <typename E, int VEC, int MODE, int KIND>
+__device__ __forceinline__ void stream_tile(const E* trow, const E* drow, int v0, int v1, float c, TAcc& ta,
+                                            DAcc& da, unsigned char* smem) {
+  constexpr int PER = (KIND == K_PAIR) ? 2 * kThreads : 4 * kThreads;  // vectors of a row per stage
+  constexpr unsigned SLOT = kCV * kThreads * 16;                         // bytes of one stage
+  const int t = threadIdx.x;
+  const uint32_t base = (uint32_t)__cvta_generic_to_shared(smem) + 16u * t;
+  const int nst = (v1 - v0 + PER - 1) / PER;
+  const int vt = v0 + t;  // this thread's first vector in stage 0
+  const E* tp = trow + (size_t)vt * VEC;
+  const E* dp = drow + (size_t)vt * VEC;
+  auto issue = [&](int k) {
+    if (k < nst) {
+      const uint32_t slot = base + (uint32_t)(k % kCS) * SLOT;
+      const int v = vt + k * PER;
+      const size_t off = (size_t)k * PER * VEC;
+#pragma unroll
+      for (int j = 0; j < kCV; ++j) {
+        const int jv = (KIND == K_PAIR) ? (j & 1) : j;
+        if (v + jv * kThreads < v1) {
+          const E* src = ((KIND == K_PAIR && j >= 2) ? dp : tp) + off + (size_t)jv * kThreads * VEC;
+          cp_async16(slot + (uint32_t)(j * kThreads * 16), src);
+        }
+      }
+    }
+    cp_commit();
+  };
+#pragma unroll
+  for (int k = 0; k < kCS - 1; ++k) issue(k);
+  for (int k = 0; k < nst; ++k) {
+    issue(k + kCS - 1);
+    cp_wait<kCS - 1>();
+    const uint4* q = reinterpret_cast<const uint4*>(smem + (size_t)(k % kCS) * SLOT) + t;
+    const int va = vt + k * PER;
+    if constexpr (KIND == K_PAIR) {
+      const int vb = va + kThreads;
+      if (vb < v1) {
+        float ft[2 * VEC], fd[2 * VEC];
+        unpack2<E, VEC>(q[0], q[kThreads], ft);
+        unpack2<E, VEC>(q[2 * kThreads], q[3 * kThreads], fd);
+        pair_update<2 * VEC, MODE == M_STOCH, VEC>(ta, da, ft, fd, va * VEC, c, vb * VEC);
+      } else if (va < v1) {
+        float ft[VEC], fd[VEC];
+        IO<E, VEC>::unpack(q[0], ft);
+        IO<E, VEC>::unpack(q[2 * kThreads], fd);
+        pair_update<VEC, MODE == M_STOCH>(ta, da, ft, fd, va * VEC, c);
+      }
+    } else {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int pa = va + 2 * h * kThreads, pb = pa + kThreads;
+        if (pb < v1) {
+          float ft[2 * VEC];
+          unpack2<E, VEC>(q[(2 * h) * kThreads], q[(2 * h + 1) * kThreads], ft);
+          if constexpr (KIND == K_TSUM)
+            tsum_update<2 * VEC, VEC>(ta, ft, pa * VEC, c, pb * VEC);
+          else
+            argmax_update<2 * VEC, VEC>(ta, ft, pa * VEC, pb * VEC);
+        } else if (pa < v1) {
+          float ft[VEC];
+          IO<E, VEC>::unpack(q[(2 * h) * kThreads], ft);
+          if constexpr (KIND == K_TSUM)
+            tsum_update<VEC>(ta, ft, pa * VEC, c);
+          else
+            argmax_update<VEC>(ta, ft, pa * VEC);
+        }
+      }
+    }
+  }
+  cp_wait<0>();
+}
+
 template <typename E, int VEC, int MODE>
-__global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant__ RowsParams p) {
+__global__ void __launch_bounds__(kThreads, 3) rows_kernel(const __grid_constant__ RowsParams p) {
   using io = IO<E, VEC>;
   using raw_t = typename io::raw_t;
   constexpr int HB = (MODE == M_NKL) ? 0 : 1;
+  extern __shared__ __align__(128) unsigned char dsm[];
   griddep_launch();
   __shared__ int s_b;
   __shared__ int s_last;
@@ -284,6 +390,18 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
   DAcc da;
   init(ta);
   init(da);
+  if constexpr (VEC > 1) {
+    if constexpr (MODE == M_GREEDY || MODE == M_TREE) {
+      stream_tile<E, VEC, MODE, K_ARGMAX>(trow, drow, e_begin / VEC, v1, c, ta, da, dsm);
+    } else if constexpr (MODE == M_NKL) {
+      stream_tile<E, VEC, MODE, K_PAIR>(trow, drow, e_begin / VEC, v1, c, ta, da, dsm);
+    } else {
+      if (kind == K_PAIR)
+        stream_tile<E, VEC, MODE, K_PAIR>(trow, drow, e_begin / VEC, v1, c, ta, da, dsm);
+      else
+        stream_tile<E, VEC, MODE, K_TSUM>(trow, drow, e_begin / VEC, v1, c, ta, da, dsm);
+    }
+  } else {
   int v = e_begin / VEC + threadIdx.x;
   if (kind == K_PAIR) {
     for (; v + kThreads < v1; v += 2 * kThreads) {
@@ -338,8 +456,9 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
       argmax_update<VEC>(ta, ft, v * VEC);
     }
   }
+  }
 
-  const Partial part = reduce_tile(kind, ta, da, c);
+  const Partial part = reduce_tile<BlockSync, E, VEC>(kind, ta, da, c, trow);
   if (threadIdx.x == 0) {
     float4* dst = reinterpret_cast<float4*>(p.part + tile);
     __stcg(dst, make_float4(part.tm, part.ts, __int_as_float(part.tidx), __int_as_float(part.bad)));
@@ -353,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  finalize<E, MODE>(p, b, gb, r - i, c0);
+  finalize<E, MODE, BlockSync>(p, b, gb, r - i, c0);
 }
 
 }  // namespace sv

@@ -10,17 +10,20 @@
 #include "kernels_sample.cuh"
 #include "spec_verify.h"
 
+#include <atomic>
+
 namespace sv {
 namespace {
 
 inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Vocabulary chunking of the tile kernel: chunks of at most 32768 tokens, split further
+// Vocabulary chunking of the tile kernel: chunks of at most max_chunk tokens (32768 for
+// row pairs, 65536 for single rows: about 128 KB per tile either way), split further
 // (down to 8192) while the grid has fewer tiles than the GPU has block slots. Chunk
 // sizes are multiples of 8 so every chunk starts on a 16-byte vector boundary.
-void chunking(int V, long long rows, int* nchunks, int* chunk_elems) {
-  long long nc = ceil_div(V, 32768);
+void chunking(int V, long long rows, int max_chunk, int* nchunks, int* chunk_elems) {
+  long long nc = ceil_div(V, max_chunk);
   while (rows * nc < kTargetTiles && V / (nc + 1) >= 8192) ++nc;
   long long ce = ceil_div(ceil_div(V, nc), 8) * 8;
   *chunk_elems = (int)ce;
@@ -44,10 +47,10 @@ struct Layout {
   long long rows;
 };
 
-Layout layout(int B, int V, long long rows, bool sample) {
+Layout layout(int B, int V, long long rows, bool sample, bool single_rows = false) {
   Layout L;
   L.rows = rows;
-  chunking(V, rows > 0 ? rows : 1, &L.nchunks, &L.chunk_elems);
+  chunking(V, rows > 0 ? rows : 1, single_rows ? 65536 : 32768, &L.nchunks, &L.chunk_elems);
   if (sample)
     segmenting(V, B, &L.nseg, &L.seg_elems);
   else
@@ -122,15 +125,50 @@ cudaError_t launch_prologue(const spec_batch& g, const Layout& L, char* ws, uint
   return launch(prologue_kernel, dim3((unsigned)ceil_div(g.B, kThreads)), dim3(kThreads), stream, pp, false);
 }
 
+// The vector path of rows_kernel stages its loads in kRowsSmem bytes of dynamic shared
+// memory, above the default 48 KB limit: the limit is raised once per (kernel, device).
+constexpr int kAttrDevices = 64;
+
+template <typename K>
+cudaError_t ensure_smem_attr(K kernel, std::atomic<unsigned long long>& done, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kAttrDevices) return cudaErrorInvalidDevice;
+  const unsigned long long bit = 1ull << dev;
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
+template <typename E, int VEC, int MODE>
+cudaError_t launch_rows_t(const RowsParams& rp, long long tiles, cudaStream_t stream) {
+  auto kern = rows_kernel<E, VEC, MODE>;
+  const int smem = VEC > 1 ? kRowsSmem : 0;
+  if (smem) {
+    static std::atomic<unsigned long long> done{0};
+    const cudaError_t e = ensure_smem_attr(kern, done, smem);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3((unsigned)tiles);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, rp);
+}
+
 template <int MODE>
 cudaError_t launch_rows(bool bf16, bool vec, const RowsParams& rp, long long tiles, cudaStream_t stream) {
-  const dim3 grid((unsigned)tiles), block(kThreads);
-  if (bf16) {
-    if (vec) return launch_pdl(rows_kernel<uint16_t, 8, MODE>, grid, block, stream, rp);
-    return launch_pdl(rows_kernel<uint16_t, 1, MODE>, grid, block, stream, rp);
-  }
-  if (vec) return launch_pdl(rows_kernel<float, 4, MODE>, grid, block, stream, rp);
-  return launch_pdl(rows_kernel<float, 1, MODE>, grid, block, stream, rp);
+  if (bf16) return vec ? launch_rows_t<uint16_t, 8, MODE>(rp, tiles, stream) : launch_rows_t<uint16_t, 1, MODE>(rp, tiles, stream);
+  return vec ? launch_rows_t<float, 4, MODE>(rp, tiles, stream) : launch_rows_t<float, 1, MODE>(rp, tiles, stream);
 }
 
 cudaError_t launch_sample(bool bf16, bool vec, const SampleParams& sp, long long blocks, cudaStream_t stream) {
@@ -178,12 +216,12 @@ extern "C" {
 
 size_t spec_workspace_bytes(spec_batch g, spec_mode mode) {
   if (check_batch(g) != SPEC_OK) return 0;
-  return layout(g.B, g.V, rows_for(mode, g), mode == SPEC_MODE_STOCHASTIC).total;
+  return layout(g.B, g.V, rows_for(mode, g), mode == SPEC_MODE_STOCHASTIC, mode == SPEC_MODE_GREEDY).total;
 }
 
 size_t spec_tree_workspace_bytes(int32_t B, int32_t N, int32_t V) {
   if (B < 0 || N < 1 || N > SPEC_MAX_TREE_NODES || V < 1) return 0;
-  return layout(B, V, (long long)B * (N + 1), false).total;
+  return layout(B, V, (long long)B * (N + 1), false, true).total;
 }
 
 int32_t spec_tree_depth(const int32_t* parent, int32_t N) {
@@ -272,7 +310,7 @@ spec_status spec_verify_greedy(spec_batch g, spec_dtype dtype, const void* targe
   if (g.B == 0) return SPEC_OK;
   if (!target_logits || !n_accepted || !out_tokens || !device_status) return SPEC_ERR_INVALID_ARG;
   if (g.total_draft > 0 && !draft_tokens) return SPEC_ERR_INVALID_ARG;
-  const Layout L = layout(g.B, g.V, rows_for(SPEC_MODE_GREEDY, g), false);
+  const Layout L = layout(g.B, g.V, rows_for(SPEC_MODE_GREEDY, g), false, true);
   if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u)) return SPEC_ERR_WORKSPACE;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   char* ws = static_cast<char*>(workspace);
@@ -307,7 +345,7 @@ spec_status spec_verify_tree(int32_t B, int32_t N, int32_t V, spec_dtype dtype, 
   g.V = V;
   g.total_draft = B * N;
   g.cu_draft = nullptr;
-  const Layout L = layout(B, V, (long long)B * (N + 1), false);
+  const Layout L = layout(B, V, (long long)B * (N + 1), false, true);
   if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u)) return SPEC_ERR_WORKSPACE;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   char* ws = static_cast<char*>(workspace);
