@@ -177,7 +177,7 @@ class StochasticCall:
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.g = _lib.SpecBatch(B, w.gamma_max if not w.dense else int(w.gammas[0]), V, tot,
                                 ctypes.c_void_p(self.cu.data_ptr()) if self.cu is not None else None)
-        nbytes = self.lib.spec_workspace_bytes(self.g, _lib.SPEC_MODE_STOCHASTIC)
+        nbytes = self.lib.spec_workspace_bytes(self.g, _lib.SPEC_BF16 if w.dtype == 'bf16' else _lib.SPEC_F32, _lib.SPEC_MODE_STOCHASTIC)
         self.ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         self.dt = _lib.SPEC_BF16 if w.dtype == "bf16" else _lib.SPEC_F32
         self.host = None

@@ -39,9 +39,9 @@
  *     u_accept entries start at cu_draft[b]; its target rows (gamma_b + 1 of them: one
  *     per draft plus the bonus row) and its out_tokens entries start at cu_draft[b] + b.
  *     cu_draft == NULL means a dense batch with gamma_b = gamma for every b.
- *   - `workspace` is scratch memory of at least spec_workspace_bytes() bytes. Its
- *     contents need no initialisation and are meaningless between calls. Two calls may
- *     not use one workspace at the same time (e.g. on two streams).
+ *   - `workspace` is scratch memory of at least spec_workspace_bytes() bytes, 256-byte
+ *     aligned. Its contents need no initialisation and are meaningless between calls.
+ *     Two calls may not use one workspace at the same time (e.g. on two streams).
  */
 #ifndef SPEC_VERIFY_H
 #define SPEC_VERIFY_H
@@ -87,10 +87,11 @@ typedef struct {
   const int32_t* cu_draft; /* device [B+1], non-decreasing prefix sums of gamma_b; NULL = dense */
 } spec_batch;
 
-/* Bytes of scratch memory a call of `mode` needs for geometry g (dtype-independent). */
-size_t spec_workspace_bytes(spec_batch g, spec_mode mode);
+/* Bytes of scratch memory a call of `mode` needs for geometry g and element type dtype
+ * (0 for an invalid geometry or dtype). The workspace must be 256-byte aligned. */
+size_t spec_workspace_bytes(spec_batch g, spec_dtype dtype, spec_mode mode);
 
-/* Bytes of scratch memory spec_verify_tree needs. */
+/* Bytes of scratch memory spec_verify_tree needs (256-byte aligned, as above). */
 size_t spec_tree_workspace_bytes(int32_t B, int32_t N, int32_t V);
 
 /*
@@ -185,7 +186,7 @@ spec_status spec_nkl(spec_batch g, spec_dtype dtype, const void* target_logits, 
  *
  *   - Nothing is allocated: the scratch is one static device array of
  *     SPEC_STATIC_SCRATCH_BYTES bytes, present on every GPU that loads the library until
- *     the process exits. A problem whose spec_workspace_bytes(g, SPEC_MODE_STOCHASTIC)
+ *     the process exits. A problem whose spec_workspace_bytes(g, dtype, SPEC_MODE_STOCHASTIC)
  *     exceeds it returns SPEC_ERR_TOO_LARGE before anything runs.
  *   - The first call on each device (with that device current) looks up the array's
  *     device address with cudaGetSymbolAddress and caches it; make that first call

@@ -45,7 +45,7 @@ _F = ctypes.c_float
 _S = ctypes.c_size_t
 
 SIGNATURES = {
-    "spec_workspace_bytes": (_S, [SpecBatch, ctypes.c_int]),
+    "spec_workspace_bytes": (_S, [SpecBatch, ctypes.c_int, ctypes.c_int]),
     "spec_tree_workspace_bytes": (_S, [_I, _I, _I]),
     "spec_tree_depth": (_I, [_P, _I]),
     "spec_verify_stochastic": (ctypes.c_int, [SpecBatch, ctypes.c_int, _P, _P, _P, _F, _P, _P, _P, _P, _P, _P, _P,

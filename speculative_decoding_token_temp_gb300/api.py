@@ -98,9 +98,10 @@ def _geometry(target, draft_rows_or_tokens, cu_draft, gamma, has_bonus=True):
     return B, int(gamma), V, total, cu_draft
 
 
-def spec_workspace_bytes(B: int, gamma: int, V: int, total_draft: int, mode: int, packed: bool = False) -> int:
+def spec_workspace_bytes(B: int, gamma: int, V: int, total_draft: int, mode: int, dtype: int = _lib.SPEC_BF16,
+                         packed: bool = False) -> int:
     g = SpecBatch(B, gamma, V, total_draft, ctypes.c_void_p(1) if packed else None)
-    return int(_lib.lib().spec_workspace_bytes(g, mode))
+    return int(_lib.lib().spec_workspace_bytes(g, dtype, mode))
 
 
 def spec_verify_stochastic(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torch.Tensor,
@@ -149,7 +150,7 @@ def spec_verify_stochastic(target: torch.Tensor, draft: torch.Tensor, draft_toke
             device_status = torch.zeros(1, dtype=torch.int32, device=dev)
     o["device_status"] = device_status
     gb = SpecBatch(B, g, V, total, _ptr(cu))
-    nbytes = int(_lib.lib().spec_workspace_bytes(gb, _lib.SPEC_MODE_STOCHASTIC))
+    nbytes = int(_lib.lib().spec_workspace_bytes(gb, dt, _lib.SPEC_MODE_STOCHASTIC))
     ws = _workspace(workspace, nbytes, dev)
     code = _lib.lib().spec_verify_stochastic(
         gb, dt, _ptr(target), _ptr(draft) if total > 0 else None, _ptr(draft_tokens), float(temperature),
@@ -180,7 +181,7 @@ def spec_verify_greedy(target: torch.Tensor, draft_tokens: torch.Tensor, *, cu_d
             device_status = torch.zeros(1, dtype=torch.int32, device=dev)
     o["device_status"] = device_status
     gb = SpecBatch(B, g, V, total, _ptr(cu))
-    nbytes = int(_lib.lib().spec_workspace_bytes(gb, _lib.SPEC_MODE_GREEDY))
+    nbytes = int(_lib.lib().spec_workspace_bytes(gb, dt, _lib.SPEC_MODE_GREEDY))
     ws = _workspace(workspace, nbytes, dev)
     code = _lib.lib().spec_verify_greedy(gb, dt, _ptr(target), _ptr(draft_tokens), _ptr(n_acc), _ptr(out_tok),
                                          _ptr(device_status), _ptr(ws), ws.numel(), _stream(dev))
@@ -246,7 +247,7 @@ def spec_nkl(target: torch.Tensor, draft: torch.Tensor, temperature: float, *, c
             device_status = torch.zeros(1, dtype=torch.int32, device=dev)
     o["device_status"] = device_status
     gb = SpecBatch(B, g, V, total, _ptr(cu))
-    nbytes = int(_lib.lib().spec_workspace_bytes(gb, _lib.SPEC_MODE_NKL))
+    nbytes = int(_lib.lib().spec_workspace_bytes(gb, dt, _lib.SPEC_MODE_NKL))
     ws = _workspace(workspace, nbytes, dev)
     code = _lib.lib().spec_nkl(gb, dt, _ptr(target), _ptr(draft), float(temperature), float(delta), _ptr(nkl),
                                _ptr(mask), _ptr(device_status), _ptr(ws), ws.numel(), _stream(dev))

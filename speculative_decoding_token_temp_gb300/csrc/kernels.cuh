@@ -100,6 +100,8 @@ struct SampleParams {
   unsigned* cnt;
   int32_t* out_tok;
   uint32_t* status;
+  float* table;       // aligned-row sampler: [B, table_stride] slice masses
+  int table_stride;
 };
 
 struct ProParams {
@@ -178,6 +180,20 @@ struct NamedSync {
 // s was accumulated relative to max m; express it relative to M >= m.
 __device__ __forceinline__ float rescale(float s, float m, float M, float c) {
   return (m == -INFINITY) ? s * 0.f : s * ex2((m - M) * c);
+}
+
+// per-thread cp.async staging of the tile kernel's aligned path
+constexpr int kCS = 4;   // stages of each thread's cp.async ring (vector path)
+constexpr int kCV = 4;   // 16-byte vectors per thread per stage
+constexpr int kRowsSmem = kCS * kCV * kThreads * 16;  // dynamic shared memory of the vector path
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // ---------------------------------------------------------------------------

@@ -2,6 +2,7 @@
 #pragma once
 
 #include "kernels.cuh"
+#include "kernels_sample.cuh"
 
 namespace sv {
 
@@ -210,6 +211,8 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
   if (tid == 0) {
     p.n_acc[b] = n;
     if (p.g_n) p.g_n[b] = gn;
+  }
+  if (tid == 0) {
     SeqRec q;
     q.state = REC_READY;
     q.n = n;
@@ -227,19 +230,6 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
 
 // ---------------------------------------------------------------------------
 // tile kernel
-
-constexpr int kCS = 4;   // stages of each thread's cp.async ring (vector path)
-constexpr int kCV = 4;   // 16-byte vectors per thread per stage
-constexpr int kRowsSmem = kCS * kCV * kThreads * 16;  // dynamic shared memory of the vector path
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 
 // Two vectors of a stage as one 2*VEC-element group (va < vb, element bases va*VEC, vb*VEC).
 template <typename E, int VEC>

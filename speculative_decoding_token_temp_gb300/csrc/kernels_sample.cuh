@@ -281,4 +281,260 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const __grid_constant_
   }
 }
 
+
+
+// ---------------------------------------------------------------------------
+// Sampling inside the block that finalised the sequence (aligned rows).
+//
+// The masses of 32-vector slices of the row pair (or bonus row) are stored in `table`
+// (global scratch of the sequence) in token order; warp 0 scans the table in fp64 and
+// locates the slice holding the crossing y = min{v : C(v) > u * Z}; the slice's warp
+// re-reads it from global memory and finds y. Z == 0 on a residual falls back to p of
+// the same row.
+
+constexpr int kSlicesPerStage = 2 * kWarps;
+
+__device__ __forceinline__ void table_crossing(const float* table, int n, double u, double* Z_out, int* entry,
+                                               double* base) {
+  const int lane = threadIdx.x & 31;
+  const int per = (n + 31) / 32;
+  const int lo = min(n, lane * per), hi = min(n, lo + per);
+  double sum = 0.0;
+  for (int e = lo; e < hi; ++e) sum += (double)__ldcg(table + e);
+  double incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const double Z = __shfl_sync(kFull, incl, 31);
+  const double excl = incl - sum;
+  const double target = u * Z;
+  // the first lane whose range takes the running mass past the target, else (rounding
+  // only) the last lane with mass
+  const unsigned hit = __ballot_sync(kFull, lo < hi && incl > target);
+  const unsigned pos = __ballot_sync(kFull, lo < hi && sum > 0.0);
+  const int L = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : 0);
+  int ent = -1;
+  double b = 0.0;
+  if (lane == L) {
+    double acc = excl;
+    int last = -1;
+    double lastb = excl;
+    for (int e = lo; e < hi; ++e) {
+      const double t = (double)__ldcg(table + e);
+      if (t > 0.0) {
+        last = e;
+        lastb = acc;
+        if (hit && acc + t > target) {
+          ent = e;
+          b = acc;
+          break;
+        }
+      }
+      acc += t;
+    }
+    if (ent < 0) {
+      ent = last >= 0 ? last : lo;
+      b = last >= 0 ? lastb : excl;
+    }
+  }
+  *entry = __shfl_sync(kFull, ent, L);
+  *base = __shfl_sync(kFull, b, L);
+  *Z_out = Z;
+}
+
+template <typename E, int VEC>
+__device__ __forceinline__ void vec_weights(const uint4& tv, const uint4* dv, int mode, float lt2, float ld2, float c,
+                                            float (&w)[VEC]) {
+  float ft[VEC], fd[VEC];
+  IO<E, VEC>::unpack(tv, ft);
+  if (mode == S_RESID) IO<E, VEC>::unpack(*dv, fd);
+  weights<VEC>(mode, ft, fd, lt2, ld2, c, w);
+}
+
+// Masses of stages [k0, k1) of the row pair (or row): in each 512-vector stage thread t
+// takes vectors t and t + 256 (lane-contiguous, so every copy instruction moves 512
+// consecutive bytes) through its private cp.async ring; entry (2k + h) * kWarps + w of
+// `table` receives the mass of warp w's 32-vector slice of half h of stage k -- token
+// order.
+template <typename E, int VEC>
+__device__ __forceinline__ void mass_pass(const E* trow, const E* drow, int mode, float lt2, float ld2, float c,
+                                          int NV, int k0, int k1, float* table, unsigned char* smem) {
+  constexpr unsigned SLOT = kCV * kThreads * 16;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem) + 16u * t;
+  const int nst = k1 - k0;
+  auto issue = [&](int k) {
+    if (k < nst) {
+      const uint32_t slot = sbase + (uint32_t)(k % kCS) * SLOT;
+#pragma unroll
+      for (int j = 0; j < kCV; ++j) {
+        if (j >= 2 && mode != S_RESID) continue;
+        const int v = (k0 + k) * 2 * kThreads + (j & 1) * kThreads + t;
+        if (v < NV) cp_async16(slot + (uint32_t)(j * kThreads * 16), ((j >= 2) ? drow : trow) + (size_t)v * VEC);
+      }
+    }
+    cp_commit();
+  };
+#pragma unroll
+  for (int k = 0; k < kCS - 1; ++k) issue(k);
+  for (int k = 0; k < nst; ++k) {
+    issue(k + kCS - 1);
+    cp_wait<kCS - 1>();
+    const uint4* q = reinterpret_cast<const uint4*>(smem + (size_t)(k % kCS) * SLOT) + t;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int v = (k0 + k) * 2 * kThreads + h * kThreads + t;
+      float ls = 0.f;
+      if (v < NV) {
+        float w[VEC];
+        vec_weights<E, VEC>(q[h * kThreads], q + (2 + h) * kThreads, mode, lt2, ld2, c, w);
+        ls = tree_sum<VEC>(w);
+      }
+      const float ws = warp_sum(ls);
+      if (lane == 0) __stcg(table + ((size_t)(k0 + k) * 2 + h) * kWarps + warp, ws);
+    }
+  }
+  cp_wait<0>();
+}
+
+// The warp that owns table entry `ent` (stage k, half h, warp w) re-reads its 32-vector
+// slice -- one vector per lane, in token order -- and returns the token where the
+// running mass passes rem.
+template <typename E, int VEC>
+__device__ __forceinline__ int slice_token(const E* trow, const E* drow, int mode, float lt2, float ld2, float c,
+                                           int V, int NV, int ent, double rem) {
+  const int lane = threadIdx.x & 31;
+  const int k = ent / kSlicesPerStage, h = (ent / kWarps) & 1, w = ent % kWarps;
+  const int v = k * 2 * kThreads + h * kThreads + w * 32 + lane;
+  float wt[VEC];
+#pragma unroll
+  for (int j = 0; j < VEC; ++j) wt[j] = 0.f;
+  if (v < NV) {
+    const uint4 tv = ld_stream16(trow + (size_t)v * VEC);
+    uint4 dv = tv;
+    if (mode == S_RESID) dv = ld_stream16(drow + (size_t)v * VEC);
+    vec_weights<E, VEC>(tv, &dv, mode, lt2, ld2, c, wt);
+  }
+  const float ls = tree_sum<VEC>(wt);
+  float incl = ls;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  float excl = __shfl_up_sync(kFull, incl, 1);
+  if (lane == 0) excl = 0.f;
+  const unsigned hit = __ballot_sync(kFull, (double)incl > rem && ls > 0.f);
+  const unsigned pos = __ballot_sync(kFull, ls > 0.f);
+  const int L = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : 0);
+  int tok = 0;
+  if (lane == L) {
+    int y = -1, lastpos = -1;
+    float run = excl;
+    for (int j = 0; j < VEC; ++j) {
+      run += wt[j];
+      if (wt[j] > 0.f) {
+        lastpos = j;
+        if (hit && y < 0 && (double)run > rem) y = j;
+      }
+    }
+    if (y < 0) y = lastpos >= 0 ? lastpos : 0;
+    tok = v * VEC + y;
+    if (tok >= V) tok = V - 1;
+  }
+  return __shfl_sync(kFull, tok, L);
+}
+
+// Aligned-row sampler. The B rows to sample are cut into 512-vector stages, B * nst of
+// them in sequence order, and block g streams the contiguous range of p.seg_elems stages
+// starting at g * p.seg_elems (the host makes the grid one wave of resident blocks, so
+// every block is busy from start to end). A range may cover the end of one sequence and
+// the start of the next; for each part the block adds the part's stage count to the
+// sequence's ticket, and the block whose part completes the nst stages scans the
+// sequence's table and draws its token.
+template <typename E, int VEC>
+__global__ void __launch_bounds__(kThreads, 3) sample2_kernel(const __grid_constant__ SampleParams p) {
+  extern __shared__ __align__(128) unsigned char dsm[];
+  griddep_wait();  // the per-sequence records are final
+  __shared__ SeqRec s_rec;
+  __shared__ int s_last, s_ent, s_mode;
+  __shared__ double s_Z, s_base;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const size_t V = (size_t)p.V;
+  const int NV = p.V / VEC;
+  const int nst = (NV + 2 * kThreads - 1) / (2 * kThreads);
+  const long long total = (long long)p.B * nst;
+  const long long u0 = (long long)blockIdx.x * p.seg_elems;
+  const long long u1 = min(total, u0 + p.seg_elems);
+  for (long long u = u0; u < u1;) {
+    const int b = (int)(u / nst);
+    const int k0 = (int)(u - (long long)b * nst);
+    const int k1 = (int)min((long long)nst, k0 + (u1 - u));
+    u += k1 - k0;
+    if (tid == 0) {
+      const int4 a = __ldcg(reinterpret_cast<const int4*>(p.rec + b));
+      const int4 z = __ldcg(reinterpret_cast<const int4*>(p.rec + b) + 1);
+      s_rec.state = a.x;
+      s_rec.n = a.y;
+      s_rec.t_row = a.z;
+      s_rec.d_row = a.w;
+      s_rec.lt2 = __int_as_float(z.x);
+      s_rec.ld2 = __int_as_float(z.y);
+      s_rec.us = __int_as_float(z.z);
+      s_rec.mode = z.w;
+    }
+    __syncthreads();
+    const SeqRec q = s_rec;
+    __syncthreads();  // s_rec may be rewritten for the next part
+    if (q.state != REC_READY) continue;
+    if (q.t_row < 0 || q.t_row >= p.total_rows || (q.mode == S_RESID && (q.d_row < 0 || q.d_row >= p.total_draft))) {
+      if (tid == 0) atomicOr(p.status, SPEC_DEV_OFFSETS);
+      continue;
+    }
+    const E* trow = static_cast<const E*>(p.target) + (size_t)q.t_row * V;
+    const E* drow = static_cast<const E*>(p.draft) + (q.mode == S_RESID ? (size_t)q.d_row * V : 0);
+    float* table = p.table + (size_t)b * p.table_stride;
+    mass_pass<E, VEC>(trow, drow, q.mode, q.lt2, q.ld2, p.c, NV, k0, k1, table, dsm);
+    __threadfence();  // every writer's table entries are visible before the ticket
+    __syncthreads();
+    if (tid == 0) {
+      const unsigned part = (unsigned)(k1 - k0);
+      const unsigned old = atomicAdd(p.cnt + b, part);
+      s_last = (old + part == (unsigned)nst) ? 1 : 0;
+    }
+    __syncthreads();
+    if (!s_last) continue;
+    __threadfence();
+    int mode = q.mode;
+    const int nent = nst * kSlicesPerStage;
+    for (int attempt = 0; attempt < 2; ++attempt) {
+      if (warp == 0) {
+        double Z, base;
+        int ent;
+        table_crossing(table, nent, (double)q.us, &Z, &ent, &base);
+        if (lane == 0) {
+          s_Z = Z;
+          s_ent = ent;
+          s_base = base;
+          s_mode = (mode == S_RESID && !(Z > 1e-30)) ? S_P : mode;
+        }
+      }
+      __syncthreads();
+      if (s_mode == mode) break;
+      mode = s_mode;  // zero residual: the masses of p of the same row, whole row in this block
+      mass_pass<E, VEC>(trow, drow, mode, q.lt2, q.ld2, p.c, NV, 0, nst, table, dsm);
+      __syncthreads();
+    }
+    const int ent = s_ent;
+    if (warp == ent % kWarps) {
+      const int y = slice_token<E, VEC>(trow, drow, mode, q.lt2, q.ld2, p.c, p.V, NV, ent,
+                                        (double)q.us * s_Z - s_base);
+      if (lane == 0) p.out_tok[q.t_row] = y;
+    }
+    __syncthreads();
+  }
+}
+
 }  // namespace sv

@@ -42,12 +42,19 @@ void segmenting(int V, int B, int* nseg, int* seg_elems) {
 }
 
 struct Layout {
-  size_t cntA, cntB, rec, part, segtot, total;
-  int nchunks, chunk_elems, nseg, seg_elems;
+  size_t cntA, cntB, rec, part, segtot, table, total;
+  int nchunks, chunk_elems, nseg, seg_elems, table_stride;
   long long rows;
 };
 
-Layout layout(int B, int V, long long rows, bool sample, bool single_rows = false) {
+// The aligned-row sampler keeps one float per 32-vector (one warp, one half-stage) slice
+// of a row: 16 per 512-vector stage.
+int table_stride_for(int V, spec_dtype dt) {
+  const long long nv = ceil_div(V, dt == SPEC_BF16 ? 8 : 4);
+  return (int)(ceil_div(nv, 2 * kThreads) * kSlicesPerStage);
+}
+
+Layout layout(int B, int V, long long rows, bool sample, bool single_rows = false, spec_dtype dt = SPEC_F32) {
   Layout L;
   L.rows = rows;
   chunking(V, rows > 0 ? rows : 1, single_rows ? 65536 : 32768, &L.nchunks, &L.chunk_elems);
@@ -66,6 +73,9 @@ Layout layout(int B, int V, long long rows, bool sample, bool single_rows = fals
   off = align256(off + sizeof(Partial) * (size_t)(rows * L.nchunks));
   L.segtot = off;
   off = align256(off + sizeof(double) * (size_t)B * (size_t)L.nseg);
+  L.table_stride = sample ? table_stride_for(V, dt) : 0;
+  L.table = off;
+  off = align256(off + sizeof(float) * (size_t)B * (size_t)L.table_stride);
   L.total = off;
   return L;
 }
@@ -128,6 +138,7 @@ cudaError_t launch_prologue(const spec_batch& g, const Layout& L, char* ws, uint
 // The vector path of rows_kernel stages its loads in kRowsSmem bytes of dynamic shared
 // memory, above the default 48 KB limit: the limit is raised once per (kernel, device).
 constexpr int kAttrDevices = 64;
+constexpr int kWaveBlocks = 152 * 3;  // resident 256-thread blocks with 64 KB staging on a GB300
 
 template <typename K>
 cudaError_t ensure_smem_attr(K kernel, std::atomic<unsigned long long>& done, int bytes) {
@@ -181,6 +192,30 @@ cudaError_t launch_sample(bool bf16, bool vec, const SampleParams& sp, long long
   return launch_pdl(sample_kernel<float, 1>, grid, block, stream, sp);
 }
 
+template <typename E, int VEC>
+cudaError_t launch_sample2_t(const SampleParams& sp, long long blocks, cudaStream_t stream) {
+  auto kern = sample2_kernel<E, VEC>;
+  static std::atomic<unsigned long long> done{0};
+  const cudaError_t e = ensure_smem_attr(kern, done, kRowsSmem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)kRowsSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, sp);
+}
+
+cudaError_t launch_sample2(bool bf16, const SampleParams& sp, long long blocks, cudaStream_t stream) {
+  return bf16 ? launch_sample2_t<uint16_t, 8>(sp, blocks, stream) : launch_sample2_t<float, 4>(sp, blocks, stream);
+}
+
 RowsParams base_params(const spec_batch& g, const Layout& L, char* ws, uint32_t* status) {
   RowsParams rp;
   memset(&rp, 0, sizeof(rp));
@@ -214,9 +249,9 @@ using namespace sv;
 
 extern "C" {
 
-size_t spec_workspace_bytes(spec_batch g, spec_mode mode) {
-  if (check_batch(g) != SPEC_OK) return 0;
-  return layout(g.B, g.V, rows_for(mode, g), mode == SPEC_MODE_STOCHASTIC, mode == SPEC_MODE_GREEDY).total;
+size_t spec_workspace_bytes(spec_batch g, spec_dtype dtype, spec_mode mode) {
+  if (check_batch(g) != SPEC_OK || (dtype != SPEC_F32 && dtype != SPEC_BF16)) return 0;
+  return layout(g.B, g.V, rows_for(mode, g), mode == SPEC_MODE_STOCHASTIC, mode == SPEC_MODE_GREEDY, dtype).total;
 }
 
 size_t spec_tree_workspace_bytes(int32_t B, int32_t N, int32_t V) {
@@ -252,7 +287,7 @@ spec_status spec_verify_stochastic(spec_batch g, spec_dtype dtype, const void* t
   if (!target_logits || !n_accepted || !out_tokens || !u_sample || !device_status) return SPEC_ERR_INVALID_ARG;
   if (g.total_draft > 0 && (!draft_logits || !draft_tokens || !u_accept)) return SPEC_ERR_INVALID_ARG;
   if ((greedy_n == nullptr) != (greedy_tokens == nullptr)) return SPEC_ERR_INVALID_ARG;
-  const Layout L = layout(g.B, g.V, rows_for(SPEC_MODE_STOCHASTIC, g), true);
+  const Layout L = layout(g.B, g.V, rows_for(SPEC_MODE_STOCHASTIC, g), true, false, dtype);
   if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u)) return SPEC_ERR_WORKSPACE;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   char* ws = static_cast<char*>(workspace);
@@ -296,6 +331,19 @@ spec_status spec_verify_stochastic(spec_batch g, spec_dtype dtype, const void* t
   sp.cnt = reinterpret_cast<unsigned*>(ws + L.cntB);
   sp.out_tok = out_tokens;
   sp.status = device_status;
+  sp.table = reinterpret_cast<float*>(ws + L.table);
+  sp.table_stride = L.table_stride;
+  if (vec) {
+    // aligned rows: one wave of blocks over the B * nst stages, equal ranges
+    const int nv = g.V / (bf16 ? 8 : 4);
+    const long long total = (long long)g.B * ceil_div(nv, 2 * kThreads);
+    long long blocks = total < kWaveBlocks ? total : kWaveBlocks;
+    if (blocks < 1) blocks = 1;
+    sp.seg_elems = (int)ceil_div(total, blocks);  // stages per block
+    sp.nseg = (int)ceil_div(total, sp.seg_elems);  // blocks
+    if (launch_sample2(bf16, sp, (long long)sp.nseg, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+    return SPEC_OK;
+  }
   if (launch_sample(bf16, vec, sp, (long long)g.B * L.nseg, stream) != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;
 }
@@ -459,7 +507,8 @@ extern "C" spec_status spec_verify_stochastic_static(
   // Everything in the scratch that must start at zero (the per-sequence tickets) or in a
   // known state (the per-sequence records) is reset by the first kernel of every call;
   // the rest is written before it is read. Nothing carries over between calls.
-  if (spec_workspace_bytes(g, SPEC_MODE_STOCHASTIC) > (size_t)SPEC_STATIC_SCRATCH_BYTES) return SPEC_ERR_TOO_LARGE;
+  if (spec_workspace_bytes(g, dtype, SPEC_MODE_STOCHASTIC) > (size_t)SPEC_STATIC_SCRATCH_BYTES)
+    return SPEC_ERR_TOO_LARGE;
   void* ws = nullptr;
   if (static_scratch_address(&ws) != cudaSuccess) return SPEC_ERR_CUDA;
   return spec_verify_stochastic(g, dtype, target_logits, draft_logits, draft_tokens, temperature, u_accept, u_sample,

@@ -32,12 +32,17 @@ def _g(B, gamma, V, total=None, cu=None):
 
 
 def test_workspace_sizes(lib):
-    h = lib.spec_workspace_bytes(_g(256, 8, 128256), _lib.SPEC_MODE_STOCHASTIC)
-    # 2304 rows x 4 chunks x 32 B partials, plus tickets, records and segment totals
-    assert 2304 * 4 * 32 <= h < 2304 * 4 * 32 + 256 * 200
-    assert lib.spec_workspace_bytes(_g(256, 8, 128256), _lib.SPEC_MODE_GREEDY) <= h
-    assert lib.spec_workspace_bytes(_g(0, 8, 100), _lib.SPEC_MODE_STOCHASTIC) >= 0
-    assert lib.spec_workspace_bytes(_g(2, 200, 100), 0) == 0        # gamma above the limit
+    BF, F = _lib.SPEC_BF16, _lib.SPEC_F32
+    h = lib.spec_workspace_bytes(_g(256, 8, 128256), BF, _lib.SPEC_MODE_STOCHASTIC)
+    # 2304 rows x 4 chunks x 32 B partials, tickets, records, segment totals, and the
+    # sampler's slice-mass table: 256 sequences x 32 stages x 16 slices x 4 B
+    table = 256 * 32 * 16 * 4
+    assert 2304 * 4 * 32 + table <= h < 2304 * 4 * 32 + table + 256 * 200
+    assert lib.spec_workspace_bytes(_g(256, 8, 128256), F, _lib.SPEC_MODE_STOCHASTIC) > h   # f32: twice the table
+    assert lib.spec_workspace_bytes(_g(256, 8, 128256), BF, _lib.SPEC_MODE_GREEDY) <= h
+    assert lib.spec_workspace_bytes(_g(0, 8, 100), BF, _lib.SPEC_MODE_STOCHASTIC) >= 0
+    assert lib.spec_workspace_bytes(_g(2, 200, 100), BF, 0) == 0        # gamma above the limit
+    assert lib.spec_workspace_bytes(_g(2, 8, 100), 9, 0) == 0           # unknown dtype
     assert lib.spec_tree_workspace_bytes(32, 12, 128256) > 0
     assert lib.spec_tree_workspace_bytes(32, 65, 128256) == 0
 

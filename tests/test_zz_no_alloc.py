@@ -47,7 +47,7 @@ def test_static_scratch_matches_workspace_call(dev):
 
     lib = _lib.lib()
     batch = _lib.SpecBatch(w.B, g, w.V, w.total_draft, None)
-    assert lib.spec_workspace_bytes(batch, _lib.SPEC_MODE_STOCHASTIC) <= _lib.SPEC_STATIC_SCRATCH_BYTES
+    assert lib.spec_workspace_bytes(batch, _lib.SPEC_BF16, _lib.SPEC_MODE_STOCHASTIC) <= _lib.SPEC_STATIC_SCRATCH_BYTES
     P = lambda x: ctypes.c_void_p(x.data_ptr())  # noqa: E731
     stream = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
     rows, tot = w.total_target, w.total_draft
@@ -78,7 +78,7 @@ def test_static_scratch_matches_workspace_call(dev):
 def test_static_scratch_rejects_problems_beyond_its_size(dev):
     lib = _lib.lib()
     big = _lib.SpecBatch(4096, 16, 152064, 4096 * 16, None)
-    assert lib.spec_workspace_bytes(big, _lib.SPEC_MODE_STOCHASTIC) > _lib.SPEC_STATIC_SCRATCH_BYTES
+    assert lib.spec_workspace_bytes(big, _lib.SPEC_BF16, _lib.SPEC_MODE_STOCHASTIC) > _lib.SPEC_STATIC_SCRATCH_BYTES
     one = ctypes.c_void_p(256)
     code = lib.spec_verify_stochastic_static(big, _lib.SPEC_BF16, one, one, one, 1.0, one, one, one, one, None, None,
                                              None, None, None, 0.15, None, None, one, None)
