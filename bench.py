@@ -41,6 +41,43 @@ def peaks():
         return 6800.0, "fallback"
 
 
+PROFILE = os.path.join(ROOT, "profiles", "stochastic_call_B256_g8_V128256.md")
+
+
+def kernel_sources_sha256() -> str:
+    """Hash of the CUDA sources and the C header (the same recipe as the profile summary)."""
+    import glob
+    import hashlib
+    csrc = os.path.join(ROOT, "speculative_decoding_token_temp_gb300", "csrc")
+    files = sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh")))
+    files.append(os.path.join(ROOT, "include", "spec_verify.h"))
+    h = hashlib.sha256()
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def profiled_traffic():
+    """DRAM bytes per call from the committed ncu summary, or None when the kernels have
+    changed since it was taken (or it is missing)."""
+    try:
+        with open(PROFILE) as f:
+            text = f.read()
+        kv = {}
+        for line in text.splitlines():
+            line = line.strip()
+            if ":" in line and line.split(":")[0] in ("sources_sha256", "traffic_bytes_per_call"):
+                k, v = line.split(":", 1)
+                kv[k] = v.strip()
+        if kv.get("sources_sha256") != kernel_sources_sha256():
+            return None
+        return int(kv["traffic_bytes_per_call"])
+    except Exception:
+        return None
+
+
 def algorithmic_bytes(w) -> dict:
     """Bytes the verification must read: every target and draft logit once, plus one
     (target, draft) row pair per sequence for the residual / bonus sample."""
@@ -73,23 +110,13 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int, device) -> float:
-    if world == 1:
-        return x
-    import torch
-    import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+    from speculative_decoding_token_temp_gb300 import sharding
+    return sharding.max_over_ranks(x, world, device)
 
 
 def sum_over_ranks(x: float, world: int, device) -> float:
-    if world == 1:
-        return x
-    import torch
-    import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.SUM)
-    return float(t.item())
+    from speculative_decoding_token_temp_gb300 import sharding
+    return sharding.sum_over_ranks(x, world, device)
 
 
 # ---------------------------------------------------------------- clocks
@@ -273,7 +300,8 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     __graft_entry__.build()
     cfg = synth.CONFIGS[HEADLINE]
-    w = cfg.make(seed=cfg.seed + 1000 * rank, B=args.batch)
+    from speculative_decoding_token_temp_gb300 import sharding
+    w = cfg.make(seed=sharding.rank_seed(cfg.seed, rank), B=args.batch)
     call = StochasticCall(w, dev, host_inputs=True)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
@@ -351,12 +379,15 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"B{w.B}_g8_V128256_bf16: stochastic verify + NKL(delta=0.15) + greedy, one call",
                    "B": w.B, "gamma": 8, "V": w.V, "T": w.T, "seed": cfg.seed, "rows_per_step": rows_step,
-                   "l2": "inputs 1116 MB per step, larger than the 129 MB L2; no flush",
+                   "l2": f"inputs {(w.target.nbytes + w.draft.nbytes) / 1e6:.0f} MB per step, larger than the "
+                         "129 MB L2; no flush",
                    "parallelism": f"{world} independent shard(s), no collective"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": None,
-                     "kernel": "spec_verify_stochastic call (prologue + rows_kernel + sample_kernel)",
-                     "algorithmic_bytes": ab["stochastic"], "peak_source": peak_kind},
+                     "frac": achieved / hbm, "traffic": profiled_traffic() if w.B == 256 else None,
+                     "kernel": "spec_verify_stochastic call (prologue_kernel + rows_kernel + sample2_kernel)",
+                     "algorithmic_bytes": ab["stochastic"], "peak_source": peak_kind,
+                     "note": f"achieved = algorithmic bytes / call time (CUDA events); peak = {peak_kind} "
+                             "MEASURED_PEAKS.json hbm_gbs"},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_val, "unit": "rows/s", "h2d_bytes_per_step": call.h2d_bytes(),
                 "d2h_bytes_per_step": call.d2h_bytes()},
