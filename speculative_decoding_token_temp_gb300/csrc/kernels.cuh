@@ -5,7 +5,7 @@
 //                    checks packed offsets.
 //   rows_kernel      one block per (row, vocabulary chunk) tile. Streams the target row
 //                    (and, for a pair, the draft row) once -- on aligned rows through a
-//                    per-thread 4-stage cp.async ring in shared memory, otherwise with
+//                    per-thread 3-stage cp.async ring in shared memory, otherwise with
 //                    scalar read-only loads -- and keeps per-thread online statistics: the
 //                    raw maximum and its lowest index, sum_v exp((z_v - ref)/T), and for
 //                    the draft row also sum_v exp((zd_v - ref_d)/T) (zd_v - zt_v).
@@ -183,7 +183,7 @@ __device__ __forceinline__ float rescale(float s, float m, float M, float c) {
 }
 
 // per-thread cp.async staging of the tile kernel's aligned path
-constexpr int kCS = 4;   // stages of each thread's cp.async ring (vector path)
+constexpr int kCS = 3;   // stages of each thread's cp.async ring (vector path)
 constexpr int kCV = 4;   // 16-byte vectors per thread per stage
 constexpr int kRowsSmem = kCS * kCV * kThreads * 16;  // dynamic shared memory of the vector path
 
@@ -258,39 +258,12 @@ __device__ __forceinline__ float elem_at<float>(const float* row, int x) {
 // ---------------------------------------------------------------------------
 // packed arithmetic: two fp32 lanes per instruction (sm_100 family), 3-input min/max
 
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-  float2 d;
-  asm("{.reg .b64 ra, rb, rc, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
-      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-  return d;
-}
-__device__ __forceinline__ float2 add2(float2 a, float2 b) {
-  float2 d;
-  asm("{.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return d;
-}
-__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
-  float2 d;
-  asm("{.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-      "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return d;
-}
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
-  float2 d;
-  asm("{.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return d;
-}
+// the compiler's float2 builtins (sm_100 family) pair the operands in registers itself
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+// a - b as one fused multiply-add: b * (-1) + a is exact before its single rounding
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) { return __ffma2_rn(b, make_float2(-1.f, -1.f), a); }
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));

@@ -323,7 +323,7 @@ __device__ __forceinline__ void stream_tile(const E* trow, const E* drow, int v0
 }
 
 template <typename E, int VEC, int MODE>
-__global__ void __launch_bounds__(kThreads, 3) rows_kernel(const __grid_constant__ RowsParams p) {
+__global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant__ RowsParams p) {
   using io = IO<E, VEC>;
   using raw_t = typename io::raw_t;
   constexpr int HB = (MODE == M_NKL) ? 0 : 1;

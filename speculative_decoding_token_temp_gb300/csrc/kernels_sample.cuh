@@ -455,7 +455,7 @@ __device__ __forceinline__ int slice_token(const E* trow, const E* drow, int mod
 // sequence's ticket, and the block whose part completes the nst stages scans the
 // sequence's table and draws its token.
 template <typename E, int VEC>
-__global__ void __launch_bounds__(kThreads, 3) sample2_kernel(const __grid_constant__ SampleParams p) {
+__global__ void __launch_bounds__(kThreads, 4) sample2_kernel(const __grid_constant__ SampleParams p) {
   extern __shared__ __align__(128) unsigned char dsm[];
   griddep_wait();  // the per-sequence records are final
   __shared__ SeqRec s_rec;

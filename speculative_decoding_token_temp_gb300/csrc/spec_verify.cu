@@ -138,7 +138,7 @@ cudaError_t launch_prologue(const spec_batch& g, const Layout& L, char* ws, uint
 // The vector path of rows_kernel stages its loads in kRowsSmem bytes of dynamic shared
 // memory, above the default 48 KB limit: the limit is raised once per (kernel, device).
 constexpr int kAttrDevices = 64;
-constexpr int kWaveBlocks = 152 * 3;  // resident 256-thread blocks with 64 KB staging on a GB300
+constexpr int kWaveBlocks = 152 * 4;  // resident 256-thread blocks with 48 KB staging on a GB300
 
 template <typename K>
 cudaError_t ensure_smem_attr(K kernel, std::atomic<unsigned long long>& done, int bytes) {
