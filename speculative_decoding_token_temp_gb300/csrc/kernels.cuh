@@ -69,8 +69,7 @@ struct RowsParams {
   const int32_t* cu;
   const int32_t* node_tokens;
   int B, V, gamma, total_draft, total_rows, nchunks, chunk_elems, N;
-  float c, invT, delta, pad0;
-  double inv_lnV;
+  float c, invT, delta, inv_lnV;
   int32_t* n_acc;
   int32_t* out_tok;
   float* p_x;
@@ -102,12 +101,14 @@ struct SampleParams {
   uint32_t* status;
   float* table;       // aligned-row sampler: [B, table_stride] slice masses
   int table_stride;
+  const unsigned* tiles_done;  // tiles of the tile kernel that have finished (stochastic)
+  unsigned ntiles;
 };
 
 struct ProParams {
   const int32_t* cu;
   int B, gamma, total_draft;
-  unsigned* cntA;
+  unsigned* cntA;  // B tickets, then the finished-tile count
   unsigned* cntB;
   SeqRec* rec;
   uint32_t* status;
@@ -118,6 +119,15 @@ struct ProParams {
 
 __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* a) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_gpu(int* a, int v) {
+  asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -600,6 +610,15 @@ struct RowStat {
   float tm, ts, dm, ds, dk;
   int tidx, bad;
 };
+
+// NKL of a merged row pair: KL(q || p) / ln V with
+// KL = (K_d / S_d - (m_d - m_t)) / T - ln(S_d / S_t), in fp32 (GB300's fp64 rate is a small
+// fraction of its fp32 rate). The log of the ratio keeps the normaliser term exact to one
+// rounding; the other terms are the fp32 accumulators' own size.
+__device__ __forceinline__ float row_nkl(const RowStat& r, float invT, float inv_lnV) {
+  const float kl = (r.dk / r.ds - (r.dm - r.tm)) * invT - logf(r.ds / r.ts);
+  return kl * inv_lnV;
+}
 
 __device__ __forceinline__ RowStat merge_row(const Partial* pp, int nchunks, float c) {
   const int lane = threadIdx.x & 31;

@@ -9,6 +9,7 @@ namespace sv {
 __global__ void prologue_kernel(const __grid_constant__ ProParams p) {
   griddep_launch();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b == 0) p.cntA[p.B] = 0u;
   if (b >= p.B) return;
   p.cntA[b] = 0u;
   p.cntB[b] = 0u;
@@ -28,6 +29,28 @@ __global__ void prologue_kernel(const __grid_constant__ ProParams p) {
                      (b == p.B - 1 && c1 != p.total_draft);
     if (bad) atomicOr(p.status, SPEC_DEV_OFFSETS);
   }
+}
+
+// A stochastic tile has made its last write (its partial, or its sequence's record): the
+// sampler stops waiting for records that are still pending once every tile has counted
+// itself (a batch whose offsets failed the prologue's check leaves some unpublished).
+template <int MODE>
+__device__ __forceinline__ void tile_done(const RowsParams& p) {
+  if constexpr (MODE == M_STOCH) {
+    __threadfence();
+    atomicAdd(p.cnt + p.B, 1u);
+  }
+}
+
+// Publishes a sequence record to the sampler, which may already be polling it: the
+// payload (with the state still pending), a fence, then the state word -- a release, so a
+// reader that acquires the state sees the payload.
+__device__ __forceinline__ void publish_rec(SeqRec* dst, SeqRec q) {
+  const int state = q.state;
+  q.state = REC_PENDING;
+  *dst = q;
+  __threadfence();
+  st_relaxed_gpu(&dst->state, state);
 }
 
 // ---------------------------------------------------------------------------
@@ -118,9 +141,7 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
       if (r.bad) {
         atomicOr(p.status, SPEC_DEV_NONFINITE);
       } else {
-        const double kl = ((double)r.dk / (double)r.ds - ((double)r.dm - (double)r.tm)) * (double)p.invT -
-                          (log((double)r.ds) - log((double)r.ts));
-        v = (float)(kl * p.inv_lnV);
+        v = row_nkl(r, p.invT, p.inv_lnV);
         m = v < p.delta ? 1 : 0;
       }
       p.nkl[db + i] = v;
@@ -163,7 +184,7 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
         q.t_row = q.d_row = -1;
         q.lt2 = q.ld2 = q.us = 0.f;
         q.mode = 0;
-        p.rec[b] = q;
+        publish_rec(p.rec + b, q);
       }
     }
     return;
@@ -192,9 +213,7 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
     if (p.q_x) p.q_x[db + i] = exp2f(lq2);
     if (p.alpha) p.alpha[db + i] = a;
     if (p.nkl || p.mask) {
-      const double kl = ((double)r.dk / (double)r.ds - ((double)r.dm - (double)r.tm)) * (double)p.invT -
-                        (log((double)r.ds) - log((double)r.ts));
-      const float v = (float)(kl * p.inv_lnV);
+      const float v = row_nkl(r, p.invT, p.inv_lnV);
       if (p.nkl) p.nkl[db + i] = v;
       if (p.mask) p.mask[db + i] = v < p.delta ? 1 : 0;
     }
@@ -222,7 +241,7 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
     q.ld2 = (n < gb) ? rs[n].dm * c + log2f(rs[n].ds) : 0.f;
     q.us = p.u_sample[b];
     q.mode = (n < gb) ? S_RESID : S_P;
-    p.rec[b] = q;
+    publish_rec(p.rec + b, q);
   }
   }  // stochastic
   }  // stochastic and greedy
@@ -328,6 +347,11 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
   using raw_t = typename io::raw_t;
   constexpr int HB = (MODE == M_NKL) ? 0 : 1;
   extern __shared__ __align__(128) unsigned char dsm[];
+  // Stochastic calls: the sampler polls the per-sequence records instead of waiting for
+  // this grid, so it must not start before the prologue has re-armed them. It launches
+  // once every block of this grid has passed the trigger, and every block passes it only
+  // after the prologue has completed.
+  if constexpr (MODE == M_STOCH) griddep_wait();
   griddep_launch();
   __shared__ int s_b;
   __shared__ int s_last;
@@ -353,7 +377,10 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
     __syncthreads();
     b = s_b;
     if (b == INT_MAX) {
-      if (threadIdx.x == 0) atomicOr(p.status, SPEC_DEV_OFFSETS);
+      if (threadIdx.x == 0) {
+        atomicOr(p.status, SPEC_DEV_OFFSETS);
+        tile_done<MODE>(p);
+      }
       return;
     }
     c0 = __ldg(p.cu + b);
@@ -361,7 +388,10 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
     gb = c1 - c0;
     i = r - (c0 + HB * b);
     if (gb < 0 || gb > p.gamma || c0 < 0 || c1 > p.total_draft || i < 0 || i >= gb + HB) {
-      if (threadIdx.x == 0) atomicOr(p.status, SPEC_DEV_OFFSETS);
+      if (threadIdx.x == 0) {
+        atomicOr(p.status, SPEC_DEV_OFFSETS);
+        tile_done<MODE>(p);
+      }
       return;
     }
   }
@@ -460,9 +490,16 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
     s_last = (old + 1u == total) ? 1 : 0;
   }
   __syncthreads();
-  if (!s_last) return;
+  if (!s_last) {
+    if (threadIdx.x == 0) tile_done<MODE>(p);
+    return;
+  }
   __threadfence();
   finalize<E, MODE, BlockSync>(p, b, gb, r - i, c0);
+  if constexpr (MODE == M_STOCH) {
+    __syncthreads();  // the finaliser's writes, made by any thread, precede the count
+    if (threadIdx.x == 0) tile_done<MODE>(p);
+  }
 }
 
 }  // namespace sv

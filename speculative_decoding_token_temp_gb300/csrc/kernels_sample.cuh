@@ -284,64 +284,149 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const __grid_constant_
 
 
 // ---------------------------------------------------------------------------
-// Sampling inside the block that finalised the sequence (aligned rows).
+// Aligned-row sampling.
 //
 // The masses of 32-vector slices of the row pair (or bonus row) are stored in `table`
-// (global scratch of the sequence) in token order; warp 0 scans the table in fp64 and
-// locates the slice holding the crossing y = min{v : C(v) > u * Z}; the slice's warp
-// re-reads it from global memory and finds y. Z == 0 on a residual falls back to p of
-// the same row.
+// (global scratch of the sequence) in token order; the block that completes a sequence
+// scans the table in fp64 and locates the slice holding the crossing
+// y = min{v : C(v) > u * Z}; the slice's warp re-reads it from global memory and finds y.
+// Z == 0 on a residual falls back to p of the same row.
 
 constexpr int kSlicesPerStage = 2 * kWarps;
+// Polls of a sequence record before the sampler gives up (SPEC_DEV_TIMEOUT): each is a
+// 256 ns sleep and two L2 reads, so the wait is bounded at well under a second.
+constexpr int kPollLimit = 1 << 18;
+// Largest table the crossing search stages in shared memory (entry e sits at e + e / 32,
+// which keeps the lanes' contiguous ranges on distinct banks); longer tables are read
+// from global memory.
+constexpr int kTableSmem = 11264;
+static_assert(kTableSmem + kTableSmem / 32 <= kRowsSmem / 4, "staged table exceeds the staging buffer");
 
-__device__ __forceinline__ void table_crossing(const float* table, int n, double u, double* Z_out, int* entry,
-                                               double* base) {
+__device__ __forceinline__ int staged(int e) { return e + (e >> 5); }
+
+// Fixed-point image of a non-negative float mass: m * 2^(150 - eM + top), eM being the
+// biased exponent of the table's largest mass (at least 1). Every image is below
+// 2^(24 + top), so with top = 38 - ceil(log2 n) the sum of n images stays below 2^62 and
+// every sum, scan and comparison over the table is exact integer arithmetic (GB300 runs
+// fp64 at a small fraction of its fp32 rate; a dependent fp64 chain here cost microseconds).
+// Bits below 2^-(24 + top) of the largest mass are dropped. The sign bit is ignored
+// (a -0 mass is 0).
+__device__ __forceinline__ unsigned long long fixed_mass(float m, int eM, int top) {
+  const unsigned bits = __float_as_uint(m) & 0x7fffffffu;
+  const int ex = (int)(bits >> 23);
+  const unsigned long long mant = (bits & 0x7fffffu) | (ex ? 0x800000u : 0u);
+  const int sh = max(ex, 1) - eM + top;
+  return sh >= 0 ? mant << sh : (sh > -24 ? mant >> -sh : 0ull);
+}
+
+// floor(u * Z) for a float u in [0, 1) and an integer Z < 2^63, exactly: u = mu * 2^-s with
+// an integer mu < 2^24 and s >= 24. u >= 1 (or NaN) gives Z, u <= 0 gives 0.
+__device__ __forceinline__ unsigned long long scaled_floor(float u, unsigned long long Z) {
+  if (!(u < 1.f)) return Z;
+  if (!(u > 0.f)) return 0ull;
+  const unsigned bits = __float_as_uint(u);
+  const int eu = (int)(bits >> 23);
+  const unsigned long long mu = (bits & 0x7fffffu) | (eu ? 0x800000u : 0u);
+  const int s = 150 - max(eu, 1);
+  const unsigned long long lo = Z * mu, hi = __umul64hi(Z, mu);
+  if (s >= 128) return 0ull;
+  if (s >= 64) return hi >> (s - 64);
+  return (lo >> s) | (hi << (64 - s));
+}
+
+struct CrossResult {
+  float Z;    // total mass
+  float rem;  // u * Z minus the mass before the chosen entry
+  int ent;    // chosen entry
+};
+
+// Inverse-CDF crossing over the n float masses of `tab` (token order), by one warp, on the
+// fixed-point images: the first entry with mass whose running total (inclusive) exceeds
+// u * Z; when no entry has mass, entry 0. SMEM selects the padded shared-memory layout of
+// `tab`. Lane l owns the contiguous entries [l * per, (l + 1) * per). Lane 0 writes r.
+template <bool SMEM>
+__device__ __forceinline__ void warp_crossing(const float* tab, int n, float u, int eM, CrossResult& r) {
   const int lane = threadIdx.x & 31;
+  auto at = [&](int e) -> float { return SMEM ? tab[staged(e)] : __ldcg(tab + e); };
+  const int lg = n > 1 ? 32 - __clz(n - 1) : 0;
+  const int top = 38 - lg;
   const int per = (n + 31) / 32;
   const int lo = min(n, lane * per), hi = min(n, lo + per);
-  double sum = 0.0;
-  for (int e = lo; e < hi; ++e) sum += (double)__ldcg(table + e);
-  double incl = sum;
+  unsigned long long sum = 0ull;
+  bool mass = false;
+  for (int e = lo; e < hi; ++e) {
+    const float m = at(e);
+    sum += fixed_mass(m, eM, top);
+    mass = mass || m > 0.f;
+  }
+  unsigned long long incl = sum;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const double y = __shfl_up_sync(kFull, incl, o);
+    const unsigned long long y = __shfl_up_sync(kFull, incl, o);
     if (lane >= o) incl += y;
   }
-  const double Z = __shfl_sync(kFull, incl, 31);
-  const double excl = incl - sum;
-  const double target = u * Z;
-  // the first lane whose range takes the running mass past the target, else (rounding
-  // only) the last lane with mass
-  const unsigned hit = __ballot_sync(kFull, lo < hi && incl > target);
-  const unsigned pos = __ballot_sync(kFull, lo < hi && sum > 0.0);
+  const unsigned long long Z = __shfl_sync(kFull, incl, 31);
+  const unsigned long long excl = incl - sum;
+  const unsigned long long target = scaled_floor(u, Z);
+  // integer totals: A + q > floor(u Z) exactly when A + q > u Z. The first lane whose range
+  // passes the target, else (u >= 1 or no mass) the last lane with mass.
+  const unsigned hit = __ballot_sync(kFull, incl > target);
+  const unsigned pos = __ballot_sync(kFull, mass);
   const int L = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : 0);
-  int ent = -1;
-  double b = 0.0;
   if (lane == L) {
-    double acc = excl;
-    int last = -1;
-    double lastb = excl;
+    unsigned long long acc = excl, b = excl, lastb = excl;
+    int ent = -1, last = -1;
     for (int e = lo; e < hi; ++e) {
-      const double t = (double)__ldcg(table + e);
-      if (t > 0.0) {
+      const float m = at(e);
+      const unsigned long long q = fixed_mass(m, eM, top);
+      if (m > 0.f) {
         last = e;
         lastb = acc;
-        if (hit && acc + t > target) {
+        if (hit && acc + q > target) {
           ent = e;
           b = acc;
           break;
         }
       }
-      acc += t;
+      acc += q;
     }
     if (ent < 0) {
       ent = last >= 0 ? last : lo;
       b = last >= 0 ? lastb : excl;
     }
+    const int sc = eM - 150 - top;  // image -> mass
+    r.Z = ldexpf(__ull2float_rn(Z), sc);
+    r.rem = ldexpf(__ull2float_rn(target >= b ? target - b : 0ull), sc);
+    r.ent = ent;
   }
-  *entry = __shfl_sync(kFull, ent, L);
-  *base = __shfl_sync(kFull, b, L);
-  *Z_out = Z;
+}
+
+// Called by every thread of the block: stages the table in shared memory (one coalesced
+// load per entry) when it fits, finds the largest mass, then warp 0 searches the table.
+// Results in r, valid after return.
+__device__ __forceinline__ void block_crossing(const float* table, int n, float u, float* stage, CrossResult& r,
+                                               unsigned* s_max) {
+  const bool fits = n <= kTableSmem;
+  unsigned mx = 0u;
+  for (int e = threadIdx.x; e < n; e += kThreads) {
+    const float m = __ldcg(table + e);
+    if (fits) stage[staged(e)] = m;
+    mx = max(mx, __float_as_uint(m) & 0x7fffffffu);
+  }
+  mx = __reduce_max_sync(kFull, mx);
+  if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  if ((threadIdx.x >> 5) == 0) {
+    unsigned m = 0u;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) m = max(m, s_max[w]);
+    const int eM = max((int)(m >> 23), 1);
+    if (fits)
+      warp_crossing<true>(stage, n, u, eM, r);
+    else
+      warp_crossing<false>(table, n, u, eM, r);
+  }
+  __syncthreads();
 }
 
 template <typename E, int VEC>
@@ -404,7 +489,7 @@ __device__ __forceinline__ void mass_pass(const E* trow, const E* drow, int mode
 // running mass passes rem.
 template <typename E, int VEC>
 __device__ __forceinline__ int slice_token(const E* trow, const E* drow, int mode, float lt2, float ld2, float c,
-                                           int V, int NV, int ent, double rem) {
+                                           int V, int NV, int ent, float rem) {
   const int lane = threadIdx.x & 31;
   const int k = ent / kSlicesPerStage, h = (ent / kWarps) & 1, w = ent % kWarps;
   const int v = k * 2 * kThreads + h * kThreads + w * 32 + lane;
@@ -426,7 +511,7 @@ __device__ __forceinline__ int slice_token(const E* trow, const E* drow, int mod
   }
   float excl = __shfl_up_sync(kFull, incl, 1);
   if (lane == 0) excl = 0.f;
-  const unsigned hit = __ballot_sync(kFull, (double)incl > rem && ls > 0.f);
+  const unsigned hit = __ballot_sync(kFull, incl > rem && ls > 0.f);
   const unsigned pos = __ballot_sync(kFull, ls > 0.f);
   const int L = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : 0);
   int tok = 0;
@@ -437,7 +522,7 @@ __device__ __forceinline__ int slice_token(const E* trow, const E* drow, int mod
       run += wt[j];
       if (wt[j] > 0.f) {
         lastpos = j;
-        if (hit && y < 0 && (double)run > rem) y = j;
+        if (hit && y < 0 && run > rem) y = j;
       }
     }
     if (y < 0) y = lastpos >= 0 ? lastpos : 0;
@@ -457,10 +542,13 @@ __device__ __forceinline__ int slice_token(const E* trow, const E* drow, int mod
 template <typename E, int VEC>
 __global__ void __launch_bounds__(kThreads, 4) sample2_kernel(const __grid_constant__ SampleParams p) {
   extern __shared__ __align__(128) unsigned char dsm[];
-  griddep_wait();  // the per-sequence records are final
+  // No griddepcontrol.wait: the grid starts while the tile kernel drains, and each part
+  // waits only for its own sequence's record (published with release semantics by the
+  // sequence's last tile; the prologue re-armed it before this grid could launch).
   __shared__ SeqRec s_rec;
-  __shared__ int s_last, s_ent, s_mode;
-  __shared__ double s_Z, s_base;
+  __shared__ int s_last;
+  __shared__ CrossResult sc;
+  __shared__ unsigned s_max[kWarps];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const size_t V = (size_t)p.V;
   const int NV = p.V / VEC;
@@ -474,9 +562,21 @@ __global__ void __launch_bounds__(kThreads, 4) sample2_kernel(const __grid_const
     const int k1 = (int)min((long long)nst, k0 + (u1 - u));
     u += k1 - k0;
     if (tid == 0) {
+      int st = ld_acquire_gpu(&p.rec[b].state);
+      for (int it = 0; st == REC_PENDING && it < kPollLimit; ++it) {
+        if ((unsigned)ld_acquire_gpu(reinterpret_cast<const int*>(p.tiles_done)) == p.ntiles) {
+          // every tile has finished: a record still pending now will never be published
+          st = ld_acquire_gpu(&p.rec[b].state);
+          if (st == REC_PENDING) st = REC_SKIP;
+          break;
+        }
+        __nanosleep(256);
+        st = ld_acquire_gpu(&p.rec[b].state);
+      }
+      if (st == REC_PENDING) atomicOr(p.status, SPEC_DEV_TIMEOUT);
       const int4 a = __ldcg(reinterpret_cast<const int4*>(p.rec + b));
       const int4 z = __ldcg(reinterpret_cast<const int4*>(p.rec + b) + 1);
-      s_rec.state = a.x;
+      s_rec.state = st;
       s_rec.n = a.y;
       s_rec.t_row = a.z;
       s_rec.d_row = a.w;
@@ -497,40 +597,28 @@ __global__ void __launch_bounds__(kThreads, 4) sample2_kernel(const __grid_const
     const E* drow = static_cast<const E*>(p.draft) + (q.mode == S_RESID ? (size_t)q.d_row * V : 0);
     float* table = p.table + (size_t)b * p.table_stride;
     mass_pass<E, VEC>(trow, drow, q.mode, q.lt2, q.ld2, p.c, NV, k0, k1, table, dsm);
-    __threadfence();  // every writer's table entries are visible before the ticket
-    __syncthreads();
+    __syncthreads();  // orders every warp's table entries before thread 0's fence
     if (tid == 0) {
+      __threadfence();  // the block's table entries are visible before its ticket
       const unsigned part = (unsigned)(k1 - k0);
       const unsigned old = atomicAdd(p.cnt + b, part);
       s_last = (old + part == (unsigned)nst) ? 1 : 0;
+      if (s_last) __threadfence();  // ... and the other blocks' entries before this block's reads
     }
     __syncthreads();
     if (!s_last) continue;
-    __threadfence();
     int mode = q.mode;
     const int nent = nst * kSlicesPerStage;
     for (int attempt = 0; attempt < 2; ++attempt) {
-      if (warp == 0) {
-        double Z, base;
-        int ent;
-        table_crossing(table, nent, (double)q.us, &Z, &ent, &base);
-        if (lane == 0) {
-          s_Z = Z;
-          s_ent = ent;
-          s_base = base;
-          s_mode = (mode == S_RESID && !(Z > 1e-30)) ? S_P : mode;
-        }
-      }
-      __syncthreads();
-      if (s_mode == mode) break;
-      mode = s_mode;  // zero residual: the masses of p of the same row, whole row in this block
+      block_crossing(table, nent, q.us, reinterpret_cast<float*>(dsm), sc, s_max);
+      if (!(mode == S_RESID && !(sc.Z > 1e-30f))) break;
+      mode = S_P;  // zero residual: the masses of p of the same row, whole row in this block
       mass_pass<E, VEC>(trow, drow, mode, q.lt2, q.ld2, p.c, NV, 0, nst, table, dsm);
       __syncthreads();
     }
-    const int ent = s_ent;
+    const int ent = sc.ent;
     if (warp == ent % kWarps) {
-      const int y = slice_token<E, VEC>(trow, drow, mode, q.lt2, q.ld2, p.c, p.V, NV, ent,
-                                        (double)q.us * s_Z - s_base);
+      const int y = slice_token<E, VEC>(trow, drow, mode, q.lt2, q.ld2, p.c, p.V, NV, ent, sc.rem);
       if (lane == 0) p.out_tok[q.t_row] = y;
     }
     __syncthreads();

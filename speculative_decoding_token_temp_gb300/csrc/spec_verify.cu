@@ -63,8 +63,8 @@ Layout layout(int B, int V, long long rows, bool sample, bool single_rows = fals
   else
     L.nseg = L.seg_elems = 0;
   size_t off = 0;
-  L.cntA = off;
-  off = align256(off + sizeof(unsigned) * (size_t)B);
+  L.cntA = off;  // B tickets, then the count of finished tiles
+  off = align256(off + sizeof(unsigned) * ((size_t)B + 1));
   L.cntB = off;
   off = align256(off + sizeof(unsigned) * (size_t)B);
   L.rec = off;
@@ -231,7 +231,7 @@ RowsParams base_params(const spec_batch& g, const Layout& L, char* ws, uint32_t*
   rp.part = reinterpret_cast<Partial*>(ws + L.part);
   rp.cnt = reinterpret_cast<unsigned*>(ws + L.cntA);
   rp.rec = reinterpret_cast<SeqRec*>(ws + L.rec);
-  rp.inv_lnV = g.V > 1 ? 1.0 / log((double)g.V) : 0.0;
+  rp.inv_lnV = g.V > 1 ? (float)(1.0 / log((double)g.V)) : 0.f;
   return rp;
 }
 
@@ -333,6 +333,8 @@ spec_status spec_verify_stochastic(spec_batch g, spec_dtype dtype, const void* t
   sp.status = device_status;
   sp.table = reinterpret_cast<float*>(ws + L.table);
   sp.table_stride = L.table_stride;
+  sp.tiles_done = reinterpret_cast<const unsigned*>(ws + L.cntA) + g.B;
+  sp.ntiles = (unsigned)(L.rows * L.nchunks);
   if (vec) {
     // aligned rows: one wave of blocks over the B * nst stages, equal ranges
     const int nv = g.V / (bf16 ? 8 : 4);

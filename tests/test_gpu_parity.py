@@ -255,6 +255,53 @@ def test_large_vocab(dev):
     compare_stochastic(w, res, range(w.B))
 
 
+@pytest.mark.parametrize("V,dtype", [(160000, synth.F32), (300000, synth.BF16), (1500000, synth.F32)])
+def test_large_vocab_crossing(dev, V, dtype):
+    """Large vocabularies. At 1.5M f32 tokens the slice-mass table (11728 entries) is
+    longer than the 11264 entries the crossing search stages in shared memory, so the
+    search reads it from global memory."""
+    w = handmade(3, 2, V, dtype, T=1.0, seed=V % 997)
+    res = run_stochastic(w, dev)
+    compare_stochastic(w, res, range(w.B))
+
+
+def _draw_in_band(w, b, n, y, T):
+    """The drawn token has positive mass under the oracle's draw distribution of row n
+    (residual, its p fallback, or the bonus p) and sits at the oracle's inverse-CDF
+    crossing up to the flag band: C(y-1)/Z <= u + band and C(y)/Z >= u - band."""
+    g = int(w.gammas[b])
+    t0, d0 = w.target_base(b), w.draft_base(b)
+    lp = O.log_softmax_T(O.widen(w.target[t0 + n], w.dtype), T)
+    p = np.exp(lp)
+    if n < g:
+        q = np.exp(O.log_softmax_T(O.widen(w.draft[d0 + n], w.dtype), T))
+        wt = O.residual(p, q)
+        if float(np.sum(wt)) <= 1e-30:
+            wt = p
+    else:
+        wt = p
+    u = float(w.u_sample[b])
+    C = np.cumsum(wt)
+    Z = float(C[-1])
+    before = float(C[y - 1]) if y > 0 else 0.0
+    return wt[y] > 0 and before / Z <= u + O.FLAG_BAND and float(C[y]) / Z >= u - O.FLAG_BAND
+
+
+@pytest.mark.parametrize("u", [0.0, 0.5, 0.99999994])
+@pytest.mark.parametrize("V,dtype", [(50000, synth.BF16), (160000, synth.F32)])
+def test_draw_at_cdf_ends(dev, u, V, dtype):
+    """u = 0 takes the first token with mass, u just below 1 the last one. Exact where
+    the oracle does not flag the draw, in band everywhere."""
+    w = handmade(4, 2, V, dtype, T=0.9, seed=61)
+    w.u_sample[:] = np.float32(u)
+    res = run_stochastic(w, dev)
+    compare_stochastic(w, res, range(w.B))
+    for b in range(w.B):
+        n = int(res["n_accepted"][b])
+        y = int(res["out_tokens"][w.target_base(b) + n])
+        assert _draw_in_band(w, b, n, y, w.T), (b, n, y)
+
+
 def test_repeat_calls_reuse_workspace(dev):
     """Tickets are re-armed by every call: two calls on one workspace give the same result,
     also after a call with a different geometry."""
