@@ -1,8 +1,8 @@
 // Device code of the draft-token verification library (sm_103a).
 //
 // Pipeline of one call (all on the caller's stream):
-//   prologue_kernel  zeroes the per-sequence tickets, marks every sequence "pending",
-//                    checks packed offsets.
+//   prologue_kernel  zeroes the per-sequence tickets and the finished-tile count, marks
+//                    every sequence "pending", checks packed offsets.
 //   rows_kernel      one block per (row, vocabulary chunk) tile. Streams the target row
 //                    (and, for a pair, the draft row) once -- on aligned rows through a
 //                    per-thread 3-stage cp.async ring in shared memory, otherwise with
@@ -12,15 +12,22 @@
 //                    Block-reduces them into a 32-byte partial. The last tile of a
 //                    sequence to finish (an atomic ticket, no waiting) merges the partials
 //                    of all its rows and applies the acceptance rule, NKL, greedy or tree
-//                    decision.
-//   sample_kernel    (stochastic only) one block per (vocabulary segment, sequence):
-//                    masses of the residual max(0, p - q) (or of p for the bonus row) on
-//                    the one row pair the sequence needs; the last segment's block finds
-//                    the inverse-CDF crossing by re-reading one segment and one 256-token
-//                    step.
-// Launches after the first use programmatic dependent launch so that a kernel's
-// blocks are resident before its predecessor drains; griddepcontrol.wait guards every
-// read of the predecessor's results.
+//                    decision; a stochastic sequence's record for the sampler is published
+//                    with release semantics.
+//   sample2_kernel   (stochastic, aligned rows) one wave of blocks over the B sampled rows
+//                    cut into 512-vector stages; starts while the tile kernel drains, each
+//                    block waiting (bounded) only for its own sequences' records. Slice
+//                    masses of the residual max(0, p - q) (or of p for the bonus row) go to
+//                    a table; the block completing a sequence finds the inverse-CDF
+//                    crossing in the table (exact fixed-point sums) and re-reads one slice.
+//   sample_kernel    (stochastic, misaligned rows) the same draw by segment blocks, after
+//                    the tile kernel has completed.
+// Every kernel is launched with programmatic dependent launch, so its blocks are resident
+// before its predecessor drains, and executes griddepcontrol.wait before its first access
+// to memory that earlier work on the stream reads or writes (the sampler instead polls
+// the records, which it can only see after the prologue has re-armed them). The last
+// kernel of a call executes griddepcontrol.wait before it exits, so it does not complete
+// before the call's other kernels.
 #pragma once
 
 #include <cuda_runtime.h>

@@ -7,7 +7,11 @@
 namespace sv {
 
 __global__ void prologue_kernel(const __grid_constant__ ProParams p) {
+  // Launched programmatically after whatever precedes the call on the stream: the tile
+  // kernel may be scheduled at once, but nothing here touches memory before the
+  // preceding work has completed.
   griddep_launch();
+  griddep_wait();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b == 0) p.cntA[p.B] = 0u;
   if (b >= p.B) return;
@@ -347,11 +351,11 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
   using raw_t = typename io::raw_t;
   constexpr int HB = (MODE == M_NKL) ? 0 : 1;
   extern __shared__ __align__(128) unsigned char dsm[];
-  // Stochastic calls: the sampler polls the per-sequence records instead of waiting for
-  // this grid, so it must not start before the prologue has re-armed them. It launches
-  // once every block of this grid has passed the trigger, and every block passes it only
-  // after the prologue has completed.
-  if constexpr (MODE == M_STOCH) griddep_wait();
+  // Nothing is read or written before the prologue -- and with it everything earlier on
+  // the stream -- has completed. The stochastic sampler polls the per-sequence records
+  // instead of waiting for this grid; it launches once every block has passed the
+  // trigger, so after the prologue has re-armed the records.
+  griddep_wait();
   griddep_launch();
   __shared__ int s_b;
   __shared__ int s_last;
@@ -484,7 +488,6 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
     __stcg(dst, make_float4(part.tm, part.ts, __int_as_float(part.tidx), __int_as_float(part.bad)));
     __stcg(dst + 1, make_float4(part.dm, part.ds, part.dk, 0.f));
     __threadfence();
-    griddep_wait();  // the prologue has zeroed the tickets
     const unsigned total = (unsigned)((gb + HB) * p.nchunks);
     const unsigned old = atomicAdd(p.cnt + b, 1u);
     s_last = (old + 1u == total) ? 1 : 0;

@@ -623,6 +623,9 @@ __global__ void __launch_bounds__(kThreads, 4) sample2_kernel(const __grid_const
     }
     __syncthreads();
   }
+  // This grid does not complete before the tile kernel has: whatever follows on the
+  // stream and waits for this grid sees every write of the call.
+  griddep_wait();
 }
 
 }  // namespace sv

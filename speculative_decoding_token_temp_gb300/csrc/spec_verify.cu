@@ -98,9 +98,9 @@ spec_status check_batch(const spec_batch& g) {
 }
 
 // Launch with programmatic stream serialisation (pdl = true): the kernel may start while
-// its predecessor in the stream drains; it reads the predecessor's results only after
-// griddepcontrol.wait. The prologue of a call is launched without it, so a call never
-// overlaps the previous call on the same stream.
+// its predecessor in the stream drains; it touches memory that earlier stream work reads
+// or writes only after griddepcontrol.wait (or, in the sampler, after acquiring a record
+// that can only be published after the wait).
 template <typename K, typename P>
 cudaError_t launch(K kernel, dim3 grid, dim3 block, cudaStream_t stream, const P& params, bool pdl) {
   cudaLaunchConfig_t cfg;
@@ -132,7 +132,7 @@ cudaError_t launch_prologue(const spec_batch& g, const Layout& L, char* ws, uint
   pp.cntB = reinterpret_cast<unsigned*>(ws + L.cntB);
   pp.rec = reinterpret_cast<SeqRec*>(ws + L.rec);
   pp.status = status;
-  return launch(prologue_kernel, dim3((unsigned)ceil_div(g.B, kThreads)), dim3(kThreads), stream, pp, false);
+  return launch(prologue_kernel, dim3((unsigned)ceil_div(g.B, kThreads)), dim3(kThreads), stream, pp, true);
 }
 
 // The vector path of rows_kernel stages its loads in kRowsSmem bytes of dynamic shared

@@ -302,6 +302,41 @@ def test_draw_at_cdf_ends(dev, u, V, dtype):
         assert _draw_in_band(w, b, n, y, w.T), (b, n, y)
 
 
+def test_back_to_back_calls_on_shared_buffers(dev):
+    """Calls queued on one stream with no synchronisation between them, all on one
+    workspace, each preceded by torch kernels that overwrite the input buffers the previous
+    call read: every call sees its own inputs, and tickets and records are re-armed between
+    calls of any mode (kernels of adjacent calls may be resident at the same time)."""
+    ws = [handmade(6, 4, 20000, synth.BF16, T=0.9, seed=70 + k) for k in range(6)]
+    src = [dict(t=to_dev(w.target, dev), d=to_dev(w.draft, dev), tok=to_dev(w.tokens, dev),
+                ua=to_dev(w.u_accept, dev), us=to_dev(w.u_sample, dev)) for w in ws]
+    buf = {k: torch.empty_like(v) for k, v in src[0].items()}
+    work = torch.empty(64 << 20, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+    modes = ["stochastic", "stochastic", "greedy", "nkl", "stochastic", "stochastic"]
+    outs = []
+    for k, mode in enumerate(modes):
+        for name, v in src[k].items():
+            buf[name].copy_(v)
+        if mode == "stochastic":
+            outs.append(api.spec_verify_stochastic(buf["t"], buf["d"], buf["tok"], ws[k].T, buf["ua"], buf["us"],
+                                                   gamma=4, workspace=work))
+        elif mode == "greedy":
+            outs.append(api.spec_verify_greedy(buf["t"], buf["tok"], gamma=4, workspace=work))
+        else:
+            outs.append(api.spec_nkl(buf["t"], buf["d"], ws[k].T, gamma=4, workspace=work))
+    torch.cuda.synchronize()
+    for k, mode in enumerate(modes):
+        res = {name: v.cpu().numpy() for name, v in outs[k].items()}
+        assert res["device_status"][0] == 0, (k, mode)
+        if mode == "stochastic":
+            compare_stochastic(ws[k], res, range(ws[k].B))
+        elif mode == "greedy":
+            compare_greedy(ws[k], res, range(ws[k].B))
+        else:
+            compare_nkl(ws[k], res, range(ws[k].B))
+
+
 def test_repeat_calls_reuse_workspace(dev):
     """Tickets are re-armed by every call: two calls on one workspace give the same result,
     also after a call with a different geometry."""
