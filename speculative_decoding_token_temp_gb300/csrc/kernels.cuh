@@ -110,6 +110,10 @@ struct SampleParams {
   int table_stride;
   const unsigned* tiles_done;  // tiles of the tile kernel that have finished (stochastic)
   unsigned ntiles;
+  // aligned-row sampler: the first nb_head blocks take seg_head stages each of the first
+  // head_total stages, the remaining blocks seg_tail stages each of the rest
+  long long head_total;
+  int nb_head, seg_head, seg_tail;
 };
 
 struct ProParams {

@@ -533,9 +533,10 @@ __device__ __forceinline__ int slice_token(const E* trow, const E* drow, int mod
 }
 
 // Aligned-row sampler. The B rows to sample are cut into 512-vector stages, B * nst of
-// them in sequence order, and block g streams the contiguous range of p.seg_elems stages
-// starting at g * p.seg_elems (the host makes the grid one wave of resident blocks, so
-// every block is busy from start to end). A range may cover the end of one sequence and
+// them in sequence order, and every block streams a contiguous range of them: long ranges
+// for the sequences the tile kernel decides first, short ones for the last few, so that
+// the work left once the last sequence is decided is spread over many blocks (the host
+// sizes the grid to one wave of resident blocks). A range may cover the end of one sequence and
 // the start of the next; for each part the block adds the part's stage count to the
 // sequence's ticket, and the block whose part completes the nst stages scans the
 // sequence's table and draws its token.
@@ -554,8 +555,14 @@ __global__ void __launch_bounds__(kThreads, 4) sample2_kernel(const __grid_const
   const int NV = p.V / VEC;
   const int nst = (NV + 2 * kThreads - 1) / (2 * kThreads);
   const long long total = (long long)p.B * nst;
-  const long long u0 = (long long)blockIdx.x * p.seg_elems;
-  const long long u1 = min(total, u0 + p.seg_elems);
+  long long u0, u1;
+  if ((int)blockIdx.x < p.nb_head) {
+    u0 = (long long)blockIdx.x * p.seg_head;
+    u1 = min(p.head_total, u0 + p.seg_head);
+  } else {
+    u0 = p.head_total + (long long)((int)blockIdx.x - p.nb_head) * p.seg_tail;
+    u1 = min(total, u0 + p.seg_tail);
+  }
   for (long long u = u0; u < u1;) {
     const int b = (int)(u / nst);
     const int k0 = (int)(u - (long long)b * nst);

@@ -139,6 +139,8 @@ cudaError_t launch_prologue(const spec_batch& g, const Layout& L, char* ws, uint
 // memory, above the default 48 KB limit: the limit is raised once per (kernel, device).
 constexpr int kAttrDevices = 64;
 constexpr int kWaveBlocks = 152 * 4;  // resident 256-thread blocks with 48 KB staging on a GB300
+constexpr int kTailSeqs = 16;   // sequences the sampler splits finely (the last decided)
+constexpr int kTailStages = 4;  // their shortest range, in 512-vector stages
 
 template <typename K>
 cudaError_t ensure_smem_attr(K kernel, std::atomic<unsigned long long>& done, int bytes) {
@@ -336,14 +338,27 @@ spec_status spec_verify_stochastic(spec_batch g, spec_dtype dtype, const void* t
   sp.tiles_done = reinterpret_cast<const unsigned*>(ws + L.cntA) + g.B;
   sp.ntiles = (unsigned)(L.rows * L.nchunks);
   if (vec) {
-    // aligned rows: one wave of blocks over the B * nst stages, equal ranges
+    // aligned rows: one wave of blocks over the B * nst stages. The last kTailSeqs
+    // sequences (decided last by the tile kernel) take short ranges of at least
+    // kTailStages stages on at most a quarter of the wave, the others equal long ranges.
     const int nv = g.V / (bf16 ? 8 : 4);
-    const long long total = (long long)g.B * ceil_div(nv, 2 * kThreads);
-    long long blocks = total < kWaveBlocks ? total : kWaveBlocks;
-    if (blocks < 1) blocks = 1;
-    sp.seg_elems = (int)ceil_div(total, blocks);  // stages per block
-    sp.nseg = (int)ceil_div(total, sp.seg_elems);  // blocks
-    if (launch_sample2(bf16, sp, (long long)sp.nseg, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+    const long long nst = ceil_div(nv, 2 * kThreads);
+    const long long tail_seqs = g.B < kTailSeqs ? g.B : kTailSeqs;
+    const long long tail_total = tail_seqs * nst, head_total = ((long long)g.B - tail_seqs) * nst;
+    long long seg_tail = ceil_div(tail_total, kWaveBlocks / 4);
+    if (seg_tail < kTailStages) seg_tail = kTailStages;
+    const long long nb_tail = ceil_div(tail_total, seg_tail);
+    long long nb_head = 0, seg_head = 1;
+    if (head_total > 0) {
+      const long long room = kWaveBlocks - nb_tail;
+      seg_head = ceil_div(head_total, room < 1 ? 1 : room);
+      nb_head = ceil_div(head_total, seg_head);
+    }
+    sp.head_total = head_total;
+    sp.nb_head = (int)nb_head;
+    sp.seg_head = (int)seg_head;
+    sp.seg_tail = (int)seg_tail;
+    if (launch_sample2(bf16, sp, nb_head + nb_tail, stream) != cudaSuccess) return SPEC_ERR_CUDA;
     return SPEC_OK;
   }
   if (launch_sample(bf16, vec, sp, (long long)g.B * L.nseg, stream) != cudaSuccess) return SPEC_ERR_CUDA;
