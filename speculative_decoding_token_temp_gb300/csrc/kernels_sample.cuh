@@ -340,73 +340,25 @@ struct CrossResult {
   int ent;    // chosen entry
 };
 
-// Inverse-CDF crossing over the n float masses of `tab` (token order), by one warp, on the
-// fixed-point images: the first entry with mass whose running total (inclusive) exceeds
-// u * Z; when no entry has mass, entry 0. SMEM selects the padded shared-memory layout of
-// `tab`. Lane l owns the contiguous entries [l * per, (l + 1) * per). Lane 0 writes r.
-template <bool SMEM>
-__device__ __forceinline__ void warp_crossing(const float* tab, int n, float u, int eM, CrossResult& r) {
-  const int lane = threadIdx.x & 31;
-  auto at = [&](int e) -> float { return SMEM ? tab[staged(e)] : __ldcg(tab + e); };
-  const int lg = n > 1 ? 32 - __clz(n - 1) : 0;
-  const int top = 38 - lg;
-  const int per = (n + 31) / 32;
-  const int lo = min(n, lane * per), hi = min(n, lo + per);
-  unsigned long long sum = 0ull;
-  bool mass = false;
-  for (int e = lo; e < hi; ++e) {
-    const float m = at(e);
-    sum += fixed_mass(m, eM, top);
-    mass = mass || m > 0.f;
-  }
-  unsigned long long incl = sum;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const unsigned long long y = __shfl_up_sync(kFull, incl, o);
-    if (lane >= o) incl += y;
-  }
-  const unsigned long long Z = __shfl_sync(kFull, incl, 31);
-  const unsigned long long excl = incl - sum;
-  const unsigned long long target = scaled_floor(u, Z);
-  // integer totals: A + q > floor(u Z) exactly when A + q > u Z. The first lane whose range
-  // passes the target, else (u >= 1 or no mass) the last lane with mass.
-  const unsigned hit = __ballot_sync(kFull, incl > target);
-  const unsigned pos = __ballot_sync(kFull, mass);
-  const int L = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : 0);
-  if (lane == L) {
-    unsigned long long acc = excl, b = excl, lastb = excl;
-    int ent = -1, last = -1;
-    for (int e = lo; e < hi; ++e) {
-      const float m = at(e);
-      const unsigned long long q = fixed_mass(m, eM, top);
-      if (m > 0.f) {
-        last = e;
-        lastb = acc;
-        if (hit && acc + q > target) {
-          ent = e;
-          b = acc;
-          break;
-        }
-      }
-      acc += q;
-    }
-    if (ent < 0) {
-      ent = last >= 0 ? last : lo;
-      b = last >= 0 ? lastb : excl;
-    }
-    const int sc = eM - 150 - top;  // image -> mass
-    r.Z = ldexpf(__ull2float_rn(Z), sc);
-    r.rem = ldexpf(__ull2float_rn(target >= b ? target - b : 0ull), sc);
-    r.ent = ent;
-  }
-}
+// Per-thread sums of the two-level crossing search sit after the staged table.
+constexpr int kSumsOffset = (kTableSmem + kTableSmem / 32) * 4;
+static_assert(kSumsOffset % 8 == 0 && kSumsOffset + kThreads * 8 <= kRowsSmem, "crossing sums exceed the staging buffer");
+constexpr unsigned long long kMassBit = 1ull << 63;  // a thread's entries include one with mass
 
-// Called by every thread of the block: stages the table in shared memory (one coalesced
-// load per entry) when it fits, finds the largest mass, then warp 0 searches the table.
-// Results in r, valid after return.
-__device__ __forceinline__ void block_crossing(const float* table, int n, float u, float* stage, CrossResult& r,
+// Inverse-CDF crossing over the n float masses of `table` (token order), called by every
+// thread of the block, on the fixed-point images: the first entry with mass whose running
+// total (inclusive) exceeds u * Z; when none does (u >= 1), the last entry with mass; when
+// no entry has mass, entry 0. Level 1: thread t sums its contiguous entries
+// [t * per, (t + 1) * per). Level 2: warp 0 scans the 256 thread sums (lane l holds those of
+// threads 8l .. 8l + 7), then the chosen lane walks its threads and the chosen thread's
+// entries. The table is staged in shared memory (padded layout) when it fits, and every
+// thread finds the largest mass first. Results in r, valid after return.
+__device__ __forceinline__ void block_crossing(const float* table, int n, float u, unsigned char* smem, CrossResult& r,
                                                unsigned* s_max) {
+  float* stage = reinterpret_cast<float*>(smem);
+  unsigned long long* sums = reinterpret_cast<unsigned long long*>(smem + kSumsOffset);
   const bool fits = n <= kTableSmem;
+  auto at = [&](int e) -> float { return fits ? stage[staged(e)] : __ldcg(table + e); };
   unsigned mx = 0u;
   for (int e = threadIdx.x; e < n; e += kThreads) {
     const float m = __ldcg(table + e);
@@ -416,15 +368,96 @@ __device__ __forceinline__ void block_crossing(const float* table, int n, float 
   mx = __reduce_max_sync(kFull, mx);
   if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = mx;
   __syncthreads();
-  if ((threadIdx.x >> 5) == 0) {
-    unsigned m = 0u;
+  unsigned m = 0u;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) m = max(m, s_max[w]);
-    const int eM = max((int)(m >> 23), 1);
-    if (fits)
-      warp_crossing<true>(stage, n, u, eM, r);
-    else
-      warp_crossing<false>(table, n, u, eM, r);
+  for (int w = 0; w < kWarps; ++w) m = max(m, s_max[w]);
+  const int eM = max((int)(m >> 23), 1);
+  const int lg = n > 1 ? 32 - __clz(n - 1) : 0;
+  const int top = 38 - lg;
+  const int per = (n + kThreads - 1) / kThreads;
+  {
+    const int lo = min(n, (int)threadIdx.x * per), hi = min(n, lo + per);
+    unsigned long long sum = 0ull;
+    bool mass = false;
+    for (int e = lo; e < hi; ++e) {
+      const float x = at(e);
+      sum += fixed_mass(x, eM, top);
+      mass = mass || x > 0.f;
+    }
+    sums[threadIdx.x] = sum | (mass ? kMassBit : 0ull);
+  }
+  __syncthreads();
+  if ((threadIdx.x >> 5) == 0) {
+    const int lane = threadIdx.x & 31;
+    constexpr int TPL = kThreads / 32;  // threads per lane
+    unsigned long long v[TPL];
+    unsigned tmass = 0u;
+    unsigned long long lsum = 0ull;
+#pragma unroll
+    for (int j = 0; j < TPL; ++j) {
+      const unsigned long long x = sums[lane * TPL + j];
+      v[j] = x & ~kMassBit;
+      if (x & kMassBit) tmass |= 1u << j;
+      lsum += v[j];
+    }
+    unsigned long long incl = lsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const unsigned long long Z = __shfl_sync(kFull, incl, 31);
+    const unsigned long long excl = incl - lsum;
+    const unsigned long long target = scaled_floor(u, Z);
+    // integer totals: A + q > floor(u Z) exactly when A + q > u Z
+    const unsigned hit = __ballot_sync(kFull, incl > target);
+    const unsigned pos = __ballot_sync(kFull, tmass != 0u);
+    const int L = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : 0);
+    if (lane == L) {
+      // the thread: the first whose sum passes the target, else the last with mass
+      unsigned long long acc = excl, tb = excl;
+      int T = -1;
+#pragma unroll
+      for (int j = 0; j < TPL; ++j) {
+        if (hit) {
+          if (T < 0 && acc + v[j] > target) {
+            T = L * TPL + j;
+            tb = acc;
+          }
+        } else if (tmass & (1u << j)) {
+          T = L * TPL + j;
+          tb = acc;
+        }
+        acc += v[j];
+      }
+      if (T < 0) T = L * TPL;
+      // the entry of thread T
+      const int lo = min(n, T * per), hi = min(n, lo + per);
+      unsigned long long a = tb, b = tb, lastb = tb;
+      int ent = -1, last = -1;
+      for (int e = lo; e < hi; ++e) {
+        const float x = at(e);
+        const unsigned long long q = fixed_mass(x, eM, top);
+        if (x > 0.f) {
+          last = e;
+          lastb = a;
+          if (hit && a + q > target) {
+            ent = e;
+            b = a;
+            break;
+          }
+        }
+        a += q;
+      }
+      if (ent < 0) {
+        ent = last >= 0 ? last : lo;
+        b = last >= 0 ? lastb : tb;
+      }
+      const int sc = eM - 150 - top;  // image -> mass
+      r.Z = ldexpf(__ull2float_rn(Z), sc);
+      r.rem = ldexpf(__ull2float_rn(target >= b ? target - b : 0ull), sc);
+      r.ent = min(ent, max(n - 1, 0));
+    }
   }
   __syncthreads();
 }
@@ -617,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 4) sample2_kernel(const __grid_const
     int mode = q.mode;
     const int nent = nst * kSlicesPerStage;
     for (int attempt = 0; attempt < 2; ++attempt) {
-      block_crossing(table, nent, q.us, reinterpret_cast<float*>(dsm), sc, s_max);
+      block_crossing(table, nent, q.us, dsm, sc, s_max);
       if (!(mode == S_RESID && !(sc.Z > 1e-30f))) break;
       mode = S_P;  // zero residual: the masses of p of the same row, whole row in this block
       mass_pass<E, VEC>(trow, drow, mode, q.lt2, q.ld2, p.c, NV, 0, nst, table, dsm);
