@@ -59,6 +59,29 @@ Readings taken where the pages are silent, garbled or disagree:
       outside [0, V), makes that sequence an error: its count is -1 and all its
       outputs are -1 (integers) or NaN (reals). For the standalone NKL call the
       error is per row pair.
+  R18 position-adaptive threshold ([CoD] 4.3): delta_pos = min(delta_max,
+      delta_base * (1 + a * log2(pos))) with pos the 1-based position of the token in
+      the generated text (draft i of a sequence whose first draft sits at position P
+      has pos = P + i); the page's printed values fit log2(pos), not log2(pos + 1).
+  R19 separate temperatures ([PD] 4.4: draft 0.3-0.5, target 0.7-0.9): p is
+      softmax(z_t / T_t), q is softmax(z_d / T_d) -- the distribution the drafts were
+      drawn from -- for p(x), q(x), alpha and the residual. NKL keeps [CoD] 3.2's rule
+      that both rows are scaled by one temperature, the target's: KL(softmax(z_d / T_t)
+      || softmax(z_t / T_t)) / ln V.
+  R20 block-accept ([CoD] 3.3): the longest run of consecutive positions where the
+      draft token equals the target's token (the argmax of the target row, R10) counts
+      if it is at least min_len long (3 on the page); among equally long runs the
+      earliest wins. Its end e is the number of draft tokens kept: the output is the
+      draft tokens before e followed by the target's tokens from e on (gamma tokens in
+      all); without such a run the output is the target's tokens and e = 0.
+  R21 acceptance statistics ([MTP] 5.1: the acceptance rate is the accepted draft
+      tokens per speculative round, total accepted / rounds; [PD] 5.2: ARSD, the
+      standard deviation of the acceptance rate in a one-minute window, to be watched
+      beside P99): a round is one sequence with gamma_b > 0 in one
+      call; its acceptance rate is n_b / gamma_b; mean accepted = sum n_b / rounds;
+      ARSD = the population standard deviation of the rates of the rounds in the
+      window. The window is the caller's last W time buckets (a bucket is any
+      monotone label the caller chooses, e.g. whole seconds).
 
 Parity pins for every function: tests/test_oracle_pins.py.
 """
@@ -166,10 +189,16 @@ def nkl_pair(zt: np.ndarray, zd: np.ndarray, T: float):
 # one sequence, stochastic
 
 def verify_stochastic_sequence(t_rows: np.ndarray, d_rows: np.ndarray, tokens: np.ndarray, T: float,
-                               u_accept: np.ndarray, u_sample: float, nkl_delta: float = 0.15) -> dict:
+                               u_accept: np.ndarray, u_sample: float, nkl_delta: float = 0.15, *,
+                               T_draft: float | None = None, position: int | None = None,
+                               delta_alpha: float = 0.08, delta_max: float = 0.3, min_block_len: int = 0) -> dict:
     """Stochastic verification of one sequence ([SpS]; bonus token R1).
 
-    t_rows: float64 [gamma+1, V]; d_rows: float64 [gamma, V]; tokens int [gamma]."""
+    t_rows: float64 [gamma+1, V]; d_rows: float64 [gamma, V]; tokens int [gamma].
+    T_draft: the drafts' temperature when it differs from the target's (R19).
+    position: 1-based position of the first draft; the NKL mask then compares against
+    the position-adaptive threshold (R18). min_block_len > 0 adds the block-accept
+    outputs (R20) computed from the target's argmax tokens."""
     g = d_rows.shape[0]
     V = t_rows.shape[1]
     out = {"n": -1, "tokens": np.full(g + 1, -1, dtype=np.int64),
@@ -184,9 +213,11 @@ def verify_stochastic_sequence(t_rows: np.ndarray, d_rows: np.ndarray, tokens: n
     if out["err"]:
         return out
 
-    # temperature-scaled log-probabilities of every row (one T for both, R9)
+    # temperature-scaled log-probabilities of every row (one T for both, R9, unless the
+    # drafts were drawn at their own temperature, R19)
+    Td = T if T_draft is None else T_draft
     lp = log_softmax_T(t_rows, T)          # [g+1, V]
-    lq = log_softmax_T(d_rows, T)          # [g, V]
+    lq = log_softmax_T(d_rows, Td)         # [g, V]
 
     # gather at the drafted tokens, acceptance probability
     for i in range(g):
@@ -196,8 +227,9 @@ def verify_stochastic_sequence(t_rows: np.ndarray, d_rows: np.ndarray, tokens: n
         out["alpha"][i] = acceptance_prob(lp[i, x], lq[i, x])
         if out["q_x"][i] < 1e-8:
             out["flags"].append(("q_below_1e-8", i))
-        out["nkl"][i], out["nkl_eps"][i] = nkl_pair(t_rows[i], d_rows[i], T)
-        out["mask"][i] = 1 if out["nkl"][i] < nkl_delta else 0
+        out["nkl"][i], out["nkl_eps"][i] = nkl_pair(t_rows[i], d_rows[i], T)   # both rows at T (R19)
+        delta = nkl_delta if position is None else position_delta(position + i, nkl_delta, delta_alpha, delta_max)
+        out["mask"][i] = 1 if out["nkl"][i] < delta else 0
 
     # first rejection
     n = first_rejection(u_accept, out["alpha"])
@@ -226,6 +258,8 @@ def verify_stochastic_sequence(t_rows: np.ndarray, d_rows: np.ndarray, tokens: n
     # greedy mode on the same rows (R10)
     gn, gtok = greedy_sequence_core(t_rows, tokens)
     out["greedy_n"], out["greedy_tokens"] = gn, gtok
+    if min_block_len > 0:
+        out["block_n"], out["block_tokens"] = block_accept(tokens, np.argmax(t_rows[:g], axis=1), min_block_len)
     out["flag"] = bool(out["flags"])
     return out
 
@@ -249,7 +283,7 @@ def greedy_sequence_core(t_rows: np.ndarray, tokens: np.ndarray):
     return n, toks
 
 
-def verify_greedy_sequence(t_rows: np.ndarray, tokens: np.ndarray) -> dict:
+def verify_greedy_sequence(t_rows: np.ndarray, tokens: np.ndarray, min_block_len: int = 0) -> dict:
     g = len(tokens)
     V = t_rows.shape[1]
     err = 0
@@ -258,9 +292,35 @@ def verify_greedy_sequence(t_rows: np.ndarray, tokens: np.ndarray) -> dict:
     if np.any((tokens < 0) | (tokens >= V)):
         err |= ERR_TOKEN_RANGE
     if err:
-        return {"n": -1, "tokens": np.full(g + 1, -1, dtype=np.int64), "err": err}
+        return {"n": -1, "tokens": np.full(g + 1, -1, dtype=np.int64), "err": err,
+                "block_n": -1, "block_tokens": np.full(g, -1, dtype=np.int64)}
     n, toks = greedy_sequence_core(t_rows, tokens)
-    return {"n": n, "tokens": toks, "err": 0}
+    res = {"n": n, "tokens": toks, "err": 0}
+    if min_block_len > 0:
+        res["block_n"], res["block_tokens"] = block_accept(tokens, np.argmax(t_rows[:g], axis=1), min_block_len)
+    return res
+
+
+# ---------------------------------------------------------------------------
+# [CoD] 3.3 block-accept (R20)
+
+def block_accept(draft_tokens, target_tokens, min_len: int = 3):
+    """(e, tokens): the longest run of consecutive positions with draft == target, if it is
+    at least min_len long (the earliest of equally long runs), keeps the draft tokens up
+    to its end e; the target's tokens fill the rest. Without such a run: (0, target)."""
+    d = [int(x) for x in draft_tokens]
+    t = [int(x) for x in target_tokens]
+    g = len(d)
+    best_len, best_start = 0, 0
+    run = 0
+    for i in range(g):
+        run = run + 1 if d[i] == t[i] else 0
+        if run > best_len:                    # a strictly longer run; ties keep the earlier
+            best_len, best_start = run, i - run + 1
+    if best_len < min_len:
+        return 0, np.array(t, dtype=np.int64)
+    e = best_start + best_len
+    return e, np.array(d[:e] + t[e:], dtype=np.int64)
 
 
 # ---------------------------------------------------------------------------
@@ -315,8 +375,10 @@ def verify_tree_sequence(t_rows: np.ndarray, node_tokens: np.ndarray, parent) ->
 # cu_draft[b] + b, draft rows at cu_draft[b])
 
 def verify_stochastic(target_raw, draft_raw, tokens, cu_draft, T, u_accept, u_sample, dtype,
-                      nkl_delta=0.15, seqs=None) -> dict:
-    """Run verify_stochastic_sequence over sequences `seqs` (default: all)."""
+                      nkl_delta=0.15, seqs=None, *, T_draft=None, positions=None, delta_alpha=0.08,
+                      delta_max=0.3, min_block_len=0) -> dict:
+    """Run verify_stochastic_sequence over sequences `seqs` (default: all). positions:
+    per-sequence 1-based position of the first draft (R18), or None."""
     B = len(cu_draft) - 1
     seqs = range(B) if seqs is None else seqs
     res = {}
@@ -328,11 +390,14 @@ def verify_stochastic(target_raw, draft_raw, tokens, cu_draft, T, u_accept, u_sa
         d_rows = widen(draft_raw[d0:d1], dtype)
         res[b] = verify_stochastic_sequence(t_rows, d_rows, np.asarray(tokens[d0:d1]), T,
                                             np.asarray(u_accept[d0:d1], dtype=np.float64),
-                                            float(u_sample[b]), nkl_delta)
+                                            float(u_sample[b]), nkl_delta, T_draft=T_draft,
+                                            position=None if positions is None else int(positions[b]),
+                                            delta_alpha=delta_alpha, delta_max=delta_max,
+                                            min_block_len=min_block_len)
     return res
 
 
-def verify_greedy(target_raw, tokens, cu_draft, dtype, seqs=None) -> dict:
+def verify_greedy(target_raw, tokens, cu_draft, dtype, seqs=None, min_block_len=0) -> dict:
     B = len(cu_draft) - 1
     seqs = range(B) if seqs is None else seqs
     res = {}
@@ -340,7 +405,7 @@ def verify_greedy(target_raw, tokens, cu_draft, dtype, seqs=None) -> dict:
         d0, d1 = int(cu_draft[b]), int(cu_draft[b + 1])
         t0 = d0 + b
         res[b] = verify_greedy_sequence(widen(target_raw[t0:t0 + (d1 - d0) + 1], dtype),
-                                        np.asarray(tokens[d0:d1]))
+                                        np.asarray(tokens[d0:d1]), min_block_len)
     return res
 
 
@@ -355,9 +420,10 @@ def verify_tree(target_raw, node_tokens, parent, dtype, seqs=None) -> dict:
     return res
 
 
-def nkl_rows(target_raw, draft_raw, cu_draft, T, dtype, delta=0.15, seqs=None) -> dict:
+def nkl_rows(target_raw, draft_raw, cu_draft, T, dtype, delta=0.15, seqs=None, *, positions=None,
+             delta_alpha=0.08, delta_max=0.3) -> dict:
     """Standalone NKL over every (target row i, draft row i) pair of the chosen sequences,
-    per-row errors (R16)."""
+    per-row errors (R16); positions: as in verify_stochastic (R18)."""
     B = len(cu_draft) - 1
     seqs = range(B) if seqs is None else seqs
     res = {}
@@ -372,7 +438,8 @@ def nkl_rows(target_raw, draft_raw, cu_draft, T, dtype, delta=0.15, seqs=None) -
                 vals.append(np.nan), eps.append(np.nan), mask.append(0)
                 continue
             a, e = nkl_pair(zt, zd, T)
-            vals.append(a), eps.append(e), mask.append(1 if a < delta else 0)
+            dl = delta if positions is None else position_delta(int(positions[b]) + i, delta, delta_alpha, delta_max)
+            vals.append(a), eps.append(e), mask.append(1 if a < dl else 0)
         res[b] = {"nkl": np.array(vals), "nkl_eps": np.array(eps), "mask": np.array(mask, dtype=np.uint8)}
     return res
 
@@ -382,3 +449,26 @@ def position_delta(pos: int, delta_base: float = 0.15, a: float = 0.08, delta_ma
     delta_max: the page's printed values at pos 1 (0.15) and 1024 (0.27) fit log2(pos),
     not the log2(pos + 1) its formula shows; its 0.192 at pos 128 fits neither."""
     return min(delta_max, delta_base * (1.0 + a * math.log2(pos)))
+
+
+# ---------------------------------------------------------------------------
+# acceptance statistics (R21)
+
+def acceptance_summary(records, bucket_now: int, window: int) -> dict:
+    """records: iterable of (bucket, n_b, gamma_b) per verified sequence. Over the rounds
+    whose bucket lies in (bucket_now - window, bucket_now] and whose gamma_b > 0: rounds,
+    accepted = sum n_b, drafted = sum gamma_b, mean accepted per round, mean rate, and
+    ARSD = the population standard deviation of the rates n_b / gamma_b (two passes)."""
+    rates, acc, drafted = [], 0, 0
+    for bucket, n, g in records:
+        if bucket_now - window < bucket <= bucket_now and g > 0 and n >= 0:
+            rates.append(n / g)
+            acc += n
+            drafted += g
+    R = len(rates)
+    if R == 0:
+        return {"rounds": 0, "accepted": 0, "drafted": 0, "mean_accepted": 0.0, "mean_rate": 0.0, "arsd": 0.0}
+    mean = sum(rates) / R
+    var = sum((r - mean) ** 2 for r in rates) / R
+    return {"rounds": R, "accepted": acc, "drafted": drafted, "mean_accepted": acc / R, "mean_rate": mean,
+            "arsd": math.sqrt(var)}

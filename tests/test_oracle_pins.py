@@ -416,3 +416,132 @@ def test_errors_mark_the_whole_sequence():
     assert r["n"] == -1 and r["err"] == O.ERR_TOKEN_RANGE
     r = O.verify_greedy_sequence(t, np.array([-1, 2, 3]))
     assert r["n"] == -1 and r["err"] == O.ERR_TOKEN_RANGE
+
+
+# ---------------------------------------------------------------- separate temperatures (R19)
+
+@pytest.mark.parametrize("V,Tt,Td", [(3, 0.8, 0.4), (6, 0.7, 0.3), (8, 0.9, 0.5), (5, 1.0, 2.0)])
+def test_separate_temperatures_emit_the_target_distribution(V, Tt, Td):
+    """Drafts drawn from q at T_d, verified against p at T_t: the emitted token's law is
+    softmax(z_t / T_t) within 1e-12, and the acceptance is min(1, p/q) with q at T_d."""
+    rng = np.random.default_rng(200 + V)
+    zt = rng.normal(0, 2, (2, V))
+    zd = rng.normal(0, 2, (1, V))
+    p = sps.softmax(zt[0] / Tt)
+    q = sps.softmax(zd[0] / Td)
+
+    def run(x, u, us):
+        return O.verify_stochastic_sequence(zt, zd, np.array([x]), Tt, np.array([u]), us, T_draft=Td)
+
+    acc = np.array([_measure(lambda u, x=x: run(x, u, 0.5)["n"] >= 1) for x in range(V)])
+    assert np.allclose(acc, np.minimum(1.0, p / q), atol=1e-12, rtol=0)
+    xr = int(np.argmin(acc))
+    assert acc[xr] < 1.0
+    res = _sampler_masses(lambda us: run(xr, np.nextafter(1.0, 0), us)["tokens"][0], V)
+    emitted = q * acc + np.sum(q * (1.0 - acc)) * res
+    assert np.allclose(emitted, p, atol=1e-12, rtol=0)
+
+
+def test_separate_temperatures_nkl_at_the_target_temperature():
+    """p(x) and q(x) use their own temperatures; NKL scales both rows by T_t ([CoD] 3.2)."""
+    rng = np.random.default_rng(17)
+    V, g, Tt, Td = 50, 3, 0.8, 0.4
+    t = rng.normal(0, 2, (g + 1, V))
+    d = rng.normal(0, 2, (g, V))
+    x = np.array([3, 7, 11])
+    r = O.verify_stochastic_sequence(t, d, x, Tt, np.full(g, 0.5), 0.5, T_draft=Td)
+    for i in range(g):
+        assert r["p_x"][i] == pytest.approx(sps.softmax(t[i] / Tt)[x[i]], rel=1e-12)
+        assert r["q_x"][i] == pytest.approx(sps.softmax(d[i] / Td)[x[i]], rel=1e-12)
+        want = scipy.stats.entropy(sps.softmax(d[i] / Tt), sps.softmax(t[i] / Tt)) / math.log(V)
+        assert r["nkl"][i] == pytest.approx(want, rel=1e-9)
+    same = O.verify_stochastic_sequence(t, d, x, Tt, np.full(g, 0.5), 0.5)
+    assert np.allclose(same["nkl"], r["nkl"], rtol=0, atol=0)
+
+
+# ---------------------------------------------------------------- position-adaptive mask (R18)
+
+def _two_point_rows(nkl):
+    """A (target, draft) row pair over V = 2 with KL(q || p) / ln 2 = nkl: q uniform,
+    p = (a, 1 - a) with a(1 - a) = exp(-2 (nkl ln 2 + ln 2))."""
+    prod = math.exp(-2.0 * (nkl * math.log(2) + math.log(2)))
+    a = (1.0 - math.sqrt(1.0 - 4.0 * prod)) / 2.0
+    return np.array([math.log(a), math.log(1.0 - a)]), np.array([0.0, 0.0])
+
+
+def test_position_mask_follows_the_printed_thresholds():
+    """NKL 0.156 lies between delta(1) = 0.15 and delta(2) = 0.162: the first draft (at
+    position 1) is masked out and the second (position 2) in. NKL 0.2 is out at position 1
+    and in at position 1024 (delta 0.27, the page's printed value)."""
+    zt, zd = _two_point_rows(0.156)
+    t = np.stack([zt, zt, zt])
+    d = np.stack([zd, zd])
+    r = O.verify_stochastic_sequence(t, d, np.array([0, 0]), 1.0, np.zeros(2), 0.5, 0.15, position=1)
+    assert r["nkl"] == pytest.approx([0.156, 0.156], abs=1e-12)
+    assert list(r["mask"]) == [0, 1]
+    assert list(O.verify_stochastic_sequence(t, d, np.array([0, 0]), 1.0, np.zeros(2), 0.5, 0.15)["mask"]) == [0, 0]
+    zt, zd = _two_point_rows(0.2)
+    t = np.stack([zt, zt])
+    d = zd[None]
+    lo = O.verify_stochastic_sequence(t, d, np.array([0]), 1.0, np.zeros(1), 0.5, 0.15, position=1)
+    hi = O.verify_stochastic_sequence(t, d, np.array([0]), 1.0, np.zeros(1), 0.5, 0.15, position=1024)
+    assert lo["mask"][0] == 0 and hi["mask"][0] == 1
+    rows = O.nkl_rows(np.stack([zt, zt]), zd[None], np.array([0, 1]), 1.0, "f32", 0.15, positions=np.array([1024]))
+    assert rows[0]["mask"][0] == 1
+
+
+# ---------------------------------------------------------------- block-accept (R20)
+
+def _block_accept_page_loops(d, t, min_len):
+    """The page's search written out: every (start, end) window of length >= min_len whose
+    draft and target slices are equal; a strictly longer one replaces the best."""
+    g = len(d)
+    max_len, best_start = 0, 0
+    for start in range(g):
+        for end in range(start + min_len, g + 1):
+            if list(d[start:end]) == list(t[start:end]) and end - start > max_len:
+                max_len, best_start = end - start, start
+    if max_len >= min_len and max_len > 0:
+        e = best_start + max_len
+        return e, list(d[:e]) + list(t[e:])
+    return 0, list(t)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_block_accept_matches_the_page_search(seed):
+    rng = np.random.default_rng(300 + seed)
+    g = int(rng.integers(0, 13))
+    t = rng.integers(0, 3, g)
+    d = np.where(rng.random(g) < 0.7, t, rng.integers(0, 3, g))
+    for min_len in (1, 2, 3, 4):
+        e, toks = O.block_accept(d, t, min_len)
+        we, wt = _block_accept_page_loops(d, t, min_len)
+        assert e == we and list(toks) == wt, (list(d), list(t), min_len)
+
+
+def test_block_accept_hand_cases():
+    assert O.block_accept([1, 2, 3, 4, 5], [1, 9, 3, 4, 5], 3)[0] == 5       # the run 3,4,5 ends the block
+    e, toks = O.block_accept([7, 2, 3, 4, 8, 8], [1, 2, 3, 4, 5, 6], 3)
+    assert e == 4 and list(toks) == [7, 2, 3, 4, 5, 6]                       # the draft before the run is kept
+    e, toks = O.block_accept([1, 2, 9, 4, 5], [1, 2, 3, 4, 5], 3)
+    assert e == 0 and list(toks) == [1, 2, 3, 4, 5]                          # two runs of 2: fallback
+    assert O.block_accept([5, 5, 0, 5, 5, 5, 0, 5, 5, 5], [5] * 10, 3)[0] == 6  # ties: the earlier run
+    t = np.array([[0.0, 1.0, 0.0], [2.0, 0.0, 0.0], [0.0, 0.0, 3.0], [1.0, 0.0, 0.0]])
+    r = O.verify_greedy_sequence(t, np.array([1, 0, 2]), min_block_len=3)
+    assert r["block_n"] == 3 and list(r["block_tokens"]) == [1, 0, 2]
+
+
+# ---------------------------------------------------------------- acceptance statistics (R21)
+
+def test_acceptance_summary_against_numpy():
+    rng = np.random.default_rng(44)
+    recs = [(int(rng.integers(0, 10)), int(rng.integers(-1, 9)), int(rng.integers(0, 9))) for _ in range(500)]
+    recs = [(bk, min(n, g), g) for bk, n, g in recs]
+    s = O.acceptance_summary(recs, 9, 4)
+    keep = [(n, g) for bk, n, g in recs if 5 < bk <= 9 and g > 0 and n >= 0]
+    rates = np.array([n / g for n, g in keep])
+    assert s["rounds"] == len(keep) and s["accepted"] == sum(n for n, _ in keep)
+    assert s["mean_accepted"] == pytest.approx(np.mean([n for n, _ in keep]), rel=1e-12)
+    assert s["arsd"] == pytest.approx(np.std(rates), rel=1e-9)
+    h = O.acceptance_summary([(0, 2, 4), (0, 4, 4), (1, 3, 4)], 0, 1)
+    assert h["rounds"] == 2 and h["mean_accepted"] == 3.0 and h["arsd"] == pytest.approx(0.25, abs=1e-15)
