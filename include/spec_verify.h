@@ -29,8 +29,9 @@
  *   - Data errors found on the GPU are OR-ed into *device_status (a 32-bit device word,
  *     SPEC_DEV_* bits). The word is sticky: the library never clears it, the caller
  *     zeroes it when it wants a fresh reading. A sequence with a data error reports
- *     n = -1, -1 in its integer outputs and NaN in its real outputs. No kernel traps,
- *     asserts or waits on another block.
+ *     n = -1, -1 in its integer outputs and NaN in its real outputs. No kernel traps
+ *     or asserts; the one wait on other blocks (the sampler polling a sequence's
+ *     decision) is bounded and reports SPEC_DEV_TIMEOUT if it runs out.
  *   - Logits are row-major [rows, V] with V contiguous, fp32 or bf16 (raw bf16 bit
  *     patterns). Rows whose byte size is a multiple of 16 and whose base pointers are
  *     16-byte aligned take the vectorised path; any other layout takes a slower scalar
@@ -69,6 +70,7 @@ typedef enum {
 #define SPEC_DEV_NONFINITE 2u   /* a NaN or infinite logit in a row the sequence uses */
 #define SPEC_DEV_OFFSETS 4u     /* cu_draft not non-decreasing from 0 to total_draft, or a gamma_b > gamma */
 #define SPEC_DEV_TIMEOUT 8u     /* an internal wait gave up (bounded waits); the affected sequences are undecided */
+#define SPEC_DEV_POSITION 16u   /* spec_options.position[b] < 1 */
 
 typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
 
@@ -175,6 +177,89 @@ spec_status spec_nkl(spec_batch g, spec_dtype dtype, const void* target_logits, 
                      float temperature, float delta, float* nkl, uint8_t* nkl_mask,
                      uint32_t* device_status, void* workspace, size_t workspace_bytes,
                      spec_stream_t stream);
+
+/*
+ * Policy variants: each *_ex call takes every argument of the plain call plus `options`
+ * (a HOST pointer, read during the call; NULL = the plain call). Zero-initialise the
+ * struct and set what is used; fields a call does not use are ignored.
+ */
+#define SPEC_STATS_SLOTS 64
+
+/* One time bucket of acceptance statistics. */
+typedef struct {
+  int64_t bucket;    /* the caller's label of the bucket this slot holds */
+  uint64_t rounds;   /* sequences with gamma_b > 0 and no data error verified in it */
+  uint64_t accepted; /* their accepted drafts, sum of n_b */
+  uint64_t drafted;  /* their drafts, sum of gamma_b */
+  uint64_t rate_fx;  /* sum of n_b / gamma_b, each rounded to a multiple of 2^-32, in units of 2^-32 */
+  uint64_t rate2_fx; /* sum of (n_b / gamma_b)^2, likewise */
+} spec_stats_slot;
+
+/* Device-resident acceptance statistics ([MTP] 5.1: accepted drafts per round; [PD] 5.2:
+ * the standard deviation of the acceptance rate over a window, ARSD): a ring in which
+ * bucket k lives in slot k mod SPEC_STATS_SLOTS. Zero-fill it once before first use. */
+typedef struct {
+  spec_stats_slot slot[SPEC_STATS_SLOTS];
+} spec_accept_stats;
+
+typedef struct {
+  /* stochastic: > 0 and finite = the temperature T_d the drafts were drawn at ([PD] 4.4:
+   * draft 0.3-0.5, target 0.7-0.9). q = softmax(draft / T_d) for q(x), alpha and the
+   * residual; NKL still scales both rows by the target temperature ([CoD] 3.2).
+   * 0 = T_d equals the target temperature. */
+  float temperature_draft;
+  /* stochastic, NKL: device [B] or NULL. The 1-based position of each sequence's first
+   * draft in the generated text; the NKL mask of draft i then compares against
+   * delta_pos = min(delta_max, delta * (1 + delta_alpha * log2(position[b] + i)))
+   * ([CoD] 4.3; the page's values 0.08 and 0.3). A position < 1 sets
+   * SPEC_DEV_POSITION and masks that sequence's drafts out (mask 0); its other outputs
+   * are unaffected. */
+  const int32_t* position;
+  float delta_alpha;
+  float delta_max;
+  /* stochastic, greedy: > 0 enables block-accept ([CoD] 3.3; the page's value is 3):
+   * block_n [B] gets e, the end of the longest run of >= min_block_len consecutive
+   * positions where the draft equals the target argmax (the earliest of equally long
+   * runs), or 0 when there is none (-1 on a data error); block_tokens [total_draft] gets
+   * the draft tokens before e and the target argmax from e on. */
+  int32_t min_block_len;
+  int32_t* block_n;
+  int32_t* block_tokens;
+  /* stochastic, greedy: device statistics or NULL. Every sequence with gamma_b > 0 and no
+   * data error adds one round to the slot of stats_bucket, which is first reset if it
+   * holds another bucket. Bucket labels must not decrease from call to call. */
+  spec_accept_stats* stats;
+  int64_t stats_bucket;
+} spec_options;
+
+spec_status spec_verify_stochastic_ex(spec_batch g, spec_dtype dtype, const void* target_logits,
+                                      const void* draft_logits, const int32_t* draft_tokens,
+                                      float temperature, const float* u_accept, const float* u_sample,
+                                      int32_t* n_accepted, int32_t* out_tokens, float* p_x, float* q_x,
+                                      float* alpha, float* nkl, uint8_t* nkl_mask, float nkl_delta,
+                                      int32_t* greedy_n, int32_t* greedy_tokens, const spec_options* options,
+                                      uint32_t* device_status, void* workspace, size_t workspace_bytes,
+                                      spec_stream_t stream);
+
+spec_status spec_verify_greedy_ex(spec_batch g, spec_dtype dtype, const void* target_logits,
+                                  const int32_t* draft_tokens, int32_t* n_accepted, int32_t* out_tokens,
+                                  const spec_options* options, uint32_t* device_status, void* workspace,
+                                  size_t workspace_bytes, spec_stream_t stream);
+
+spec_status spec_nkl_ex(spec_batch g, spec_dtype dtype, const void* target_logits, const void* draft_logits,
+                        float temperature, float delta, float* nkl, uint8_t* nkl_mask,
+                        const spec_options* options, uint32_t* device_status, void* workspace,
+                        size_t workspace_bytes, spec_stream_t stream);
+
+/*
+ * Summary of the statistics over the buckets (bucket_now - window, bucket_now],
+ * 1 <= window <= SPEC_STATS_SLOTS, written to out [6] (device, fp64): rounds, accepted
+ * drafts, drafts, mean accepted drafts per round, mean acceptance rate (n_b / gamma_b),
+ * and ARSD, the population standard deviation of the per-round acceptance rates
+ * (0 when there is no round).
+ */
+spec_status spec_accept_summary(const spec_accept_stats* stats, int64_t bucket_now, int32_t window, double* out,
+                                spec_stream_t stream);
 
 /*
  * spec_verify_stochastic without a workspace argument: the same computation, inputs and

@@ -63,6 +63,8 @@ Readings taken where the pages are silent, garbled or disagree:
       delta_base * (1 + a * log2(pos))) with pos the 1-based position of the token in
       the generated text (draft i of a sequence whose first draft sits at position P
       has pos = P + i); the page's printed values fit log2(pos), not log2(pos + 1).
+      A first position below 1 has no threshold: every mask entry of that sequence
+      is 0 (the other outputs do not depend on positions).
   R19 separate temperatures ([PD] 4.4: draft 0.3-0.5, target 0.7-0.9): p is
       softmax(z_t / T_t), q is softmax(z_d / T_d) -- the distribution the drafts were
       drawn from -- for p(x), q(x), alpha and the residual. NKL keeps [CoD] 3.2's rule
@@ -228,8 +230,12 @@ def verify_stochastic_sequence(t_rows: np.ndarray, d_rows: np.ndarray, tokens: n
         if out["q_x"][i] < 1e-8:
             out["flags"].append(("q_below_1e-8", i))
         out["nkl"][i], out["nkl_eps"][i] = nkl_pair(t_rows[i], d_rows[i], T)   # both rows at T (R19)
-        delta = nkl_delta if position is None else position_delta(position + i, nkl_delta, delta_alpha, delta_max)
-        out["mask"][i] = 1 if out["nkl"][i] < delta else 0
+        if position is not None and position < 1:
+            out["mask"][i] = 0
+        else:
+            delta = nkl_delta if position is None else position_delta(position + i, nkl_delta, delta_alpha,
+                                                                      delta_max)
+            out["mask"][i] = 1 if out["nkl"][i] < delta else 0
 
     # first rejection
     n = first_rejection(u_accept, out["alpha"])
@@ -438,6 +444,9 @@ def nkl_rows(target_raw, draft_raw, cu_draft, T, dtype, delta=0.15, seqs=None, *
                 vals.append(np.nan), eps.append(np.nan), mask.append(0)
                 continue
             a, e = nkl_pair(zt, zd, T)
+            if positions is not None and int(positions[b]) < 1:
+                vals.append(a), eps.append(e), mask.append(0)
+                continue
             dl = delta if positions is None else position_delta(int(positions[b]) + i, delta, delta_alpha, delta_max)
             vals.append(a), eps.append(e), mask.append(1 if a < dl else 0)
         res[b] = {"nkl": np.array(vals), "nkl_eps": np.array(eps), "mask": np.array(mask, dtype=np.uint8)}

@@ -22,6 +22,7 @@ SPEC_DEV_TOKEN_RANGE = 1
 SPEC_DEV_NONFINITE = 2
 SPEC_DEV_OFFSETS = 4
 SPEC_DEV_TIMEOUT = 8
+SPEC_DEV_POSITION = 16
 
 SPEC_F32 = 0
 SPEC_BF16 = 1
@@ -32,11 +33,27 @@ SPEC_MODE_NKL = 2
 
 SPEC_MAX_GAMMA = 128
 SPEC_MAX_TREE_NODES = 64
+SPEC_STATS_SLOTS = 64
 
 
 class SpecBatch(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("gamma", ctypes.c_int32), ("V", ctypes.c_int32),
                 ("total_draft", ctypes.c_int32), ("cu_draft", ctypes.c_void_p)]
+
+
+class SpecStatsSlot(ctypes.Structure):
+    _fields_ = [("bucket", ctypes.c_int64), ("rounds", ctypes.c_uint64), ("accepted", ctypes.c_uint64),
+                ("drafted", ctypes.c_uint64), ("rate_fx", ctypes.c_uint64), ("rate2_fx", ctypes.c_uint64)]
+
+
+STATS_BYTES = ctypes.sizeof(SpecStatsSlot) * SPEC_STATS_SLOTS   # sizeof(spec_accept_stats)
+
+
+class SpecOptions(ctypes.Structure):
+    _fields_ = [("temperature_draft", ctypes.c_float), ("position", ctypes.c_void_p),
+                ("delta_alpha", ctypes.c_float), ("delta_max", ctypes.c_float),
+                ("min_block_len", ctypes.c_int32), ("block_n", ctypes.c_void_p),
+                ("block_tokens", ctypes.c_void_p), ("stats", ctypes.c_void_p), ("stats_bucket", ctypes.c_int64)]
 
 
 _P = ctypes.c_void_p
@@ -55,6 +72,14 @@ SIGNATURES = {
     "spec_verify_greedy": (ctypes.c_int, [SpecBatch, ctypes.c_int, _P, _P, _P, _P, _P, _P, _S, _P]),
     "spec_verify_tree": (ctypes.c_int, [_I, _I, _I, ctypes.c_int, _P, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
     "spec_nkl": (ctypes.c_int, [SpecBatch, ctypes.c_int, _P, _P, _F, _F, _P, _P, _P, _P, _S, _P]),
+    "spec_verify_stochastic_ex": (ctypes.c_int, [SpecBatch, ctypes.c_int, _P, _P, _P, _F, _P, _P, _P, _P, _P, _P,
+                                                 _P, _P, _P, _F, _P, _P, ctypes.POINTER(SpecOptions), _P, _P, _S,
+                                                 _P]),
+    "spec_verify_greedy_ex": (ctypes.c_int, [SpecBatch, ctypes.c_int, _P, _P, _P, _P, ctypes.POINTER(SpecOptions),
+                                             _P, _P, _S, _P]),
+    "spec_nkl_ex": (ctypes.c_int, [SpecBatch, ctypes.c_int, _P, _P, _F, _F, _P, _P, ctypes.POINTER(SpecOptions),
+                                   _P, _P, _S, _P]),
+    "spec_accept_summary": (ctypes.c_int, [_P, ctypes.c_int64, _I, _P, _P]),
     "spec_status_str": (ctypes.c_char_p, [ctypes.c_int]),
 }
 

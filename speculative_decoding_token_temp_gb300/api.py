@@ -109,7 +109,7 @@ def spec_verify_stochastic(target: torch.Tensor, draft: torch.Tensor, draft_toke
                            cu_draft: torch.Tensor | None = None, gamma: int | None = None,
                            nkl_delta: float = 0.15, want_probs: bool = True, want_nkl: bool = True,
                            want_greedy: bool = True, out: dict | None = None, workspace=None,
-                           device_status: torch.Tensor | None = None) -> dict:
+                           device_status: torch.Tensor | None = None, _options: dict | None = None) -> dict:
     """Stochastic verification with residual / bonus resampling; see spec_verify.h.
 
     Returns a dict of device tensors: n_accepted [B], out_tokens [total_draft+B] (dense:
@@ -152,17 +152,23 @@ def spec_verify_stochastic(target: torch.Tensor, draft: torch.Tensor, draft_toke
     gb = SpecBatch(B, g, V, total, _ptr(cu))
     nbytes = int(_lib.lib().spec_workspace_bytes(gb, dt, _lib.SPEC_MODE_STOCHASTIC))
     ws = _workspace(workspace, nbytes, dev)
-    code = _lib.lib().spec_verify_stochastic(
-        gb, dt, _ptr(target), _ptr(draft) if total > 0 else None, _ptr(draft_tokens), float(temperature),
-        _ptr(u_accept), _ptr(u_sample), _ptr(n_acc), _ptr(out_tok), _ptr(p_x), _ptr(q_x), _ptr(alpha),
-        _ptr(nkl), _ptr(mask), float(nkl_delta), _ptr(g_n), _ptr(g_tok), _ptr(device_status), _ptr(ws),
-        ws.numel(), _stream(dev))
-    check("spec_verify_stochastic", code)
+    args = (gb, dt, _ptr(target), _ptr(draft) if total > 0 else None, _ptr(draft_tokens), float(temperature),
+            _ptr(u_accept), _ptr(u_sample), _ptr(n_acc), _ptr(out_tok), _ptr(p_x), _ptr(q_x), _ptr(alpha),
+            _ptr(nkl), _ptr(mask), float(nkl_delta), _ptr(g_n), _ptr(g_tok))
+    tail = (_ptr(device_status), _ptr(ws), ws.numel(), _stream(dev))
+    if _options is None:
+        code = _lib.lib().spec_verify_stochastic(*args, *tail)
+        check("spec_verify_stochastic", code)
+    else:
+        opts = _fill_options(_options, o, dev, B, total)
+        code = _lib.lib().spec_verify_stochastic_ex(*args, ctypes.byref(opts), *tail)
+        check("spec_verify_stochastic_ex", code)
     return o
 
 
 def spec_verify_greedy(target: torch.Tensor, draft_tokens: torch.Tensor, *, cu_draft=None, gamma=None,
-                       out: dict | None = None, workspace=None, device_status=None) -> dict:
+                       out: dict | None = None, workspace=None, device_status=None,
+                       _options: dict | None = None) -> dict:
     """Greedy argmax-match verification; returns n_accepted [B], out_tokens [total_draft+B]."""
     dt = _dtype_code(target)
     dev = target.device
@@ -183,9 +189,13 @@ def spec_verify_greedy(target: torch.Tensor, draft_tokens: torch.Tensor, *, cu_d
     gb = SpecBatch(B, g, V, total, _ptr(cu))
     nbytes = int(_lib.lib().spec_workspace_bytes(gb, dt, _lib.SPEC_MODE_GREEDY))
     ws = _workspace(workspace, nbytes, dev)
-    code = _lib.lib().spec_verify_greedy(gb, dt, _ptr(target), _ptr(draft_tokens), _ptr(n_acc), _ptr(out_tok),
-                                         _ptr(device_status), _ptr(ws), ws.numel(), _stream(dev))
-    check("spec_verify_greedy", code)
+    args = (gb, dt, _ptr(target), _ptr(draft_tokens), _ptr(n_acc), _ptr(out_tok))
+    tail = (_ptr(device_status), _ptr(ws), ws.numel(), _stream(dev))
+    if _options is None:
+        check("spec_verify_greedy", _lib.lib().spec_verify_greedy(*args, *tail))
+    else:
+        opts = _fill_options(_options, o, dev, B, total)
+        check("spec_verify_greedy_ex", _lib.lib().spec_verify_greedy_ex(*args, ctypes.byref(opts), *tail))
     return o
 
 
@@ -229,7 +239,7 @@ def spec_verify_tree(target: torch.Tensor, node_tokens: torch.Tensor, parent, *,
 
 def spec_nkl(target: torch.Tensor, draft: torch.Tensor, temperature: float, *, cu_draft=None, gamma=None,
              delta: float = 0.15, want_mask: bool = True, out: dict | None = None, workspace=None,
-             device_status=None) -> dict:
+             device_status=None, _options: dict | None = None) -> dict:
     """NKL = KL(q||p)/ln V per (target row i, draft row i); returns nkl [total_draft], nkl_mask."""
     dt = _dtype_code(target)
     dev = target.device
@@ -249,7 +259,89 @@ def spec_nkl(target: torch.Tensor, draft: torch.Tensor, temperature: float, *, c
     gb = SpecBatch(B, g, V, total, _ptr(cu))
     nbytes = int(_lib.lib().spec_workspace_bytes(gb, dt, _lib.SPEC_MODE_NKL))
     ws = _workspace(workspace, nbytes, dev)
-    code = _lib.lib().spec_nkl(gb, dt, _ptr(target), _ptr(draft), float(temperature), float(delta), _ptr(nkl),
-                               _ptr(mask), _ptr(device_status), _ptr(ws), ws.numel(), _stream(dev))
-    check("spec_nkl", code)
+    args = (gb, dt, _ptr(target), _ptr(draft), float(temperature), float(delta), _ptr(nkl), _ptr(mask))
+    tail = (_ptr(device_status), _ptr(ws), ws.numel(), _stream(dev))
+    if _options is None:
+        check("spec_nkl", _lib.lib().spec_nkl(*args, *tail))
+    else:
+        opts = _fill_options(_options, o, dev, B, total)
+        check("spec_nkl_ex", _lib.lib().spec_nkl_ex(*args, ctypes.byref(opts), *tail))
     return o
+
+
+# ---------------------------------------------------------------------------
+# policy variants (spec_options)
+
+def _fill_options(opt: dict, o: dict, dev, B: int, total: int) -> _lib.SpecOptions:
+    """A spec_options block from keyword options; block-accept outputs are allocated into o."""
+    so = _lib.SpecOptions()
+    so.temperature_draft = float(opt.get("temperature_draft", 0.0))
+    pos = opt.get("position")
+    if pos is not None:
+        _need(pos, "position", torch.int32, B, dev)
+        so.position = pos.data_ptr()
+    so.delta_alpha = float(opt.get("delta_alpha", 0.08))
+    so.delta_max = float(opt.get("delta_max", 0.3))
+    mb = int(opt.get("min_block_len", 0))
+    so.min_block_len = mb
+    if mb > 0:
+        bn = o.setdefault("block_n", torch.empty(B, dtype=torch.int32, device=dev))
+        bt = o.setdefault("block_tokens", torch.empty(total, dtype=torch.int32, device=dev))
+        _need(bn, "block_n", torch.int32, B, dev)
+        _need(bt, "block_tokens", torch.int32, total, dev)
+        so.block_n = bn.data_ptr()
+        so.block_tokens = bt.data_ptr() if total > 0 else None
+    st = opt.get("stats")
+    if st is not None:
+        _need(st, "stats", torch.uint8, _lib.STATS_BYTES, dev)
+        so.stats = st.data_ptr()
+        so.stats_bucket = int(opt.get("stats_bucket", 0))
+    return so
+
+
+_OPTION_KEYS = ("temperature_draft", "position", "delta_alpha", "delta_max", "min_block_len", "stats",
+                "stats_bucket")
+
+
+def _split(kw: dict):
+    opts = {k: kw.pop(k) for k in list(kw) if k in _OPTION_KEYS}
+    return opts, kw
+
+
+def spec_verify_stochastic_ex(target, draft, draft_tokens, temperature, u_accept, u_sample, **kw) -> dict:
+    """spec_verify_stochastic with spec_options: temperature_draft (T_d, 0 = T), position [B]
+    int32 (1-based position of each sequence's first draft; position-adaptive NKL mask),
+    delta_alpha, delta_max, min_block_len (block-accept: block_n [B], block_tokens
+    [total_draft] in the result), stats (a new_accept_stats() buffer) and stats_bucket."""
+    opts, kw = _split(dict(kw))
+    return spec_verify_stochastic(target, draft, draft_tokens, temperature, u_accept, u_sample, _options=opts, **kw)
+
+
+def spec_verify_greedy_ex(target, draft_tokens, **kw) -> dict:
+    """spec_verify_greedy with spec_options (min_block_len, stats, stats_bucket)."""
+    opts, kw = _split(dict(kw))
+    return spec_verify_greedy(target, draft_tokens, _options=opts, **kw)
+
+
+def spec_nkl_ex(target, draft, temperature, **kw) -> dict:
+    """spec_nkl with spec_options (position, delta_alpha, delta_max)."""
+    opts, kw = _split(dict(kw))
+    return spec_nkl(target, draft, temperature, _options=opts, **kw)
+
+
+def new_accept_stats(device) -> torch.Tensor:
+    """A zero-filled spec_accept_stats buffer on `device` (uint8 [sizeof(spec_accept_stats)])."""
+    return torch.zeros(_lib.STATS_BYTES, dtype=torch.uint8, device=device)
+
+
+def spec_accept_summary(stats: torch.Tensor, bucket_now: int, window: int, out: torch.Tensor | None = None):
+    """Device fp64 [6]: rounds, accepted drafts, drafts, mean accepted per round, mean
+    acceptance rate, ARSD over the buckets (bucket_now - window, bucket_now]."""
+    dev = stats.device
+    _need(stats, "stats", torch.uint8, _lib.STATS_BYTES, dev)
+    if out is None:
+        out = torch.empty(6, dtype=torch.float64, device=dev)
+    _need(out, "out", torch.float64, 6, dev)
+    check("spec_accept_summary", _lib.lib().spec_accept_summary(_ptr(stats), int(bucket_now), int(window),
+                                                                _ptr(out), _stream(dev)))
+    return out

@@ -45,7 +45,10 @@ constexpr int kMaxSteps = 64;        // 256-token steps per warp in one sampling
 constexpr int kSegElems = 16384;     // largest sampling segment (kWarps * kMaxSteps * 32 scalar loads)
 constexpr int kTargetTiles = 1216;   // 152 SMs x 8 resident blocks: enough tiles to fill the GPU
 
-enum Mode : int { M_STOCH = 0, M_GREEDY = 1, M_NKL = 2, M_TREE = 3 };
+// M_STOCH2: stochastic with a draft temperature of its own (the draft row is summed at
+// both temperatures)
+enum Mode : int { M_STOCH = 0, M_GREEDY = 1, M_NKL = 2, M_TREE = 3, M_STOCH2 = 4 };
+__host__ __device__ constexpr bool is_stoch(int mode) { return mode == M_STOCH || mode == M_STOCH2; }
 enum Kind : int { K_PAIR = 0, K_TSUM = 1, K_ARGMAX = 2 };
 enum SampleMode : int { S_RESID = 0, S_P = 1 };
 enum RecState : int { REC_READY = 0, REC_SKIP = 1, REC_PENDING = 2 };
@@ -54,9 +57,9 @@ enum RecState : int { REC_READY = 0, REC_SKIP = 1, REC_PENDING = 2 };
 struct __align__(16) Partial {
   float tm, ts;   // target raw max, sum exp2((z - tm) * c)
   int tidx, bad;  // lowest index of the target max, non-finite seen
-  float dm, ds;   // draft raw max, sum exp2((zd - dm) * c)
+  float dm, ds;   // draft reference (<= raw max), sum exp2((zd - dm) * cd)
   float dk;       // sum exp2((zd - dm) * c) * (zd - zt)
-  int pad;
+  float ds2;      // separate draft temperature: sum exp2((zd - dm) * c); else 0
 };
 
 // What the sampler needs for one sequence (32 bytes).
@@ -77,6 +80,14 @@ struct RowsParams {
   const int32_t* node_tokens;
   int B, V, gamma, total_draft, total_rows, nchunks, chunk_elems, N;
   float c, invT, delta, inv_lnV;
+  float cd;  // log2(e) / T_d, the draft scale (equal to c when the temperatures match)
+  // policy epilogues (finalize)
+  const int32_t* position;  // [B] 1-based position of the first draft, or null
+  float dalpha, dmax;       // position-adaptive threshold
+  int min_block;            // block-accept: shortest run, 0 = off
+  int32_t* block_n;
+  int32_t* block_tok;
+  spec_stats_slot* stats;   // the slot of this call's bucket, or null
   int32_t* n_acc;
   int32_t* out_tok;
   float* p_x;
@@ -100,7 +111,7 @@ struct SampleParams {
   const void* target;
   const void* draft;
   int V, total_rows, total_draft, B, nseg, seg_elems;
-  float c;
+  float c, cd;  // target and draft scales, log2(e) / T
   const SeqRec* rec;
   double* segtot;
   unsigned* cnt;
@@ -123,6 +134,8 @@ struct ProParams {
   unsigned* cntB;
   SeqRec* rec;
   uint32_t* status;
+  spec_stats_slot* stats;  // the slot of this call's bucket, or null
+  long long bucket;
 };
 
 // ---------------------------------------------------------------------------
@@ -351,6 +364,8 @@ struct TAcc {
 struct DAcc {
   float mr, mth, nmc;
   float2 s, k;
+  float nmc2;  // separate draft temperature: the reference at the target scale
+  float2 s2;   // and the draft sum at the target scale (k then uses it too)
 };
 
 __device__ __forceinline__ void init(TAcc& a) {
@@ -359,6 +374,7 @@ __device__ __forceinline__ void init(TAcc& a) {
 }
 __device__ __forceinline__ void init(DAcc& a) {
   a.mr = -INFINITY; a.mth = -INFINITY; a.nmc = 0.f; a.s = make_float2(0.f, 0.f); a.k = make_float2(0.f, 0.f);
+  a.nmc2 = 0.f; a.s2 = make_float2(0.f, 0.f);
 }
 
 template <int VEC>
@@ -445,6 +461,26 @@ __device__ __forceinline__ void lazy_ref(float& mr, float& mth, float& nmc, floa
   }
 }
 
+// The same for a draft row summed at two scales (its own cd for s, the target's c for s2
+// and k): one reference, each sum rescaled at its own scale; the threshold keeps both
+// exponents below kLazy.
+__device__ __forceinline__ void lazy_ref2(float& mr, float& mth, float& nmc, float& nmc2, float2& s, float2& s2,
+                                          float2& k, float vm, float cd, float c) {
+  const bool mv = vm > mth;
+  if (__any_sync(__activemask(), mv)) {
+    if (mv) {
+      const float fd = ex2((mr - vm) * cd), ft = ex2((mr - vm) * c);
+      s = make_float2(s.x * fd, s.y * fd);
+      s2 = make_float2(s2.x * ft, s2.y * ft);
+      k = make_float2(k.x * ft, k.y * ft);
+      mr = vm;
+      mth = vm + kLazy / fmaxf(c, cd);
+      nmc = -vm * cd;
+      nmc2 = -vm * c;
+    }
+  }
+}
+
 // target row with sum (bonus row of the stochastic call); lo tracks the minimum so a
 // -inf entry, which the sum alone cannot see, is still reported
 template <int VEC, int H = VEC>
@@ -466,17 +502,26 @@ __device__ __forceinline__ void argmax_update(TAcc& a, const float (&t)[VEC], in
   track_max<VEC, H, true>(a, t, vh, e0, e1);
 }
 
-// (target row, draft row) pair; a -inf or NaN in either makes the KL sum non-finite
-template <int VEC, bool IDX, int H = VEC>
+// (target row, draft row) pair; a -inf or NaN in either makes the KL sum non-finite.
+// SEPT: the draft row also has its own scale cd (q = softmax(zd / T_d)); its sum at the
+// target scale c (for NKL at the target temperature) goes to s2, and k uses that scale.
+template <int VEC, bool IDX, int H = VEC, bool SEPT = false>
 __device__ __forceinline__ void pair_update(TAcc& a, DAcc& d, const float (&t)[VEC], const float (&z)[VEC], int e0,
-                                            float c, int e1 = 0) {
+                                            float c, int e1 = 0, float cd = 0.f) {
   const float tm = vmax<VEC>(t), dm = vmax<VEC>(z);
   track_max<VEC, H, IDX>(a, t, tm, e0, e1);
   lazy_ref(a.mr, a.mth, a.nmc, a.s, nullptr, tm, c);
-  lazy_ref(d.mr, d.mth, d.nmc, d.s, &d.k, dm, c);
   float et[VEC], ed[VEC];
   a.s = add2(a.s, exp_sum2<VEC>(t, c, a.nmc, et));
-  d.s = add2(d.s, exp_sum2<VEC>(z, c, d.nmc, ed));
+  if constexpr (SEPT) {
+    lazy_ref2(d.mr, d.mth, d.nmc, d.nmc2, d.s, d.s2, d.k, dm, cd, c);
+    float eq[VEC];
+    d.s = add2(d.s, exp_sum2<VEC>(z, cd, d.nmc, eq));
+    d.s2 = add2(d.s2, exp_sum2<VEC>(z, c, d.nmc2, ed));
+  } else {
+    lazy_ref(d.mr, d.mth, d.nmc, d.s, &d.k, dm, c);
+    d.s = add2(d.s, exp_sum2<VEC>(z, c, d.nmc, ed));
+  }
   if constexpr (VEC == 1) {
     d.k.x = fmaf(ed[0], z[0] - t[0], d.k.x);
   } else if constexpr (VEC <= 4) {
@@ -519,10 +564,11 @@ __device__ __forceinline__ int resolve_index(const E* row, int g0, int g1, float
   return INT_MAX;
 }
 
-// row != nullptr: the target maximum's index is resolved from the recorded groups
-template <class SY, typename E = float, int VEC = 1>
+// row != nullptr: the target maximum's index is resolved from the recorded groups.
+// SEPT: the draft sum s is at scale cd, s2 and k at c.
+template <class SY, typename E = float, int VEC = 1, bool SEPT = false>
 __device__ __forceinline__ Partial reduce_tile(int kind, const TAcc& ta, const DAcc& da, float c,
-                                               const E* row = nullptr) {
+                                               const E* row = nullptr, float cd = 0.f) {
   constexpr int NW = SY::NT / 32;
   __shared__ float s_m[2][NW];
   __shared__ float s_v[5][NW];
@@ -559,9 +605,15 @@ __device__ __forceinline__ Partial reduce_tile(int kind, const TAcc& ta, const D
     v0 = warp_sum(rescale(ta.s.x + ta.s.y, ta.mr, TM, c));
     if (kind == K_TSUM) v1 = warp_min(ta.lo);
     if (kind == K_PAIR) {
-      const float fd = (da.mr == -INFINITY) ? 0.f : ex2((da.mr - DM) * c);
+      const float fd = (da.mr == -INFINITY) ? 0.f : ex2((da.mr - DM) * (SEPT ? cd : c));
       v2 = warp_sum((da.s.x + da.s.y) * fd);
-      v3 = warp_sum((da.k.x + da.k.y) * fd);
+      if constexpr (SEPT) {
+        const float ft = (da.mr == -INFINITY) ? 0.f : ex2((da.mr - DM) * c);
+        v3 = warp_sum((da.k.x + da.k.y) * ft);
+        v4 = warp_sum((da.s2.x + da.s2.y) * ft);
+      } else {
+        v3 = warp_sum((da.k.x + da.k.y) * fd);
+      }
     }
   }
   if (lane == 0) {
@@ -576,13 +628,13 @@ __device__ __forceinline__ Partial reduce_tile(int kind, const TAcc& ta, const D
   Partial out;
   out.tm = TM;
   out.dm = DM;
-  out.pad = 0;
+  out.ds2 = 0.f;
   out.tidx = INT_MAX;
   out.ts = out.ds = out.dk = 0.f;
   out.bad = 0;
   if (threadIdx.x == 0) {
     int idx = INT_MAX;
-    float a0 = s_v[0][0], a1 = s_v[1][0], a2 = 0.f, a3 = 0.f;
+    float a0 = s_v[0][0], a1 = s_v[1][0], a2 = 0.f, a3 = 0.f, a4 = 0.f;
     for (int w = 0; w < NW; ++w) idx = min(idx, s_i[w]);
     if (kind == K_ARGMAX) {
       for (int w = 1; w < NW; ++w) {
@@ -596,6 +648,7 @@ __device__ __forceinline__ Partial reduce_tile(int kind, const TAcc& ta, const D
         a0 += s_v[0][w];
         a2 += s_v[2][w];
         a3 += s_v[3][w];
+        a4 += s_v[4][w];
       }
       out.ts = a0;
       bool bad = !isfinite(a0) || !isfinite(TM);
@@ -605,7 +658,8 @@ __device__ __forceinline__ Partial reduce_tile(int kind, const TAcc& ta, const D
       } else {
         out.ds = a2;
         out.dk = a3;
-        bad = bad || !isfinite(a2) || !isfinite(a3) || !isfinite(DM);
+        out.ds2 = a4;
+        bad = bad || !isfinite(a2) || !isfinite(a3) || !isfinite(a4) || !isfinite(DM);
       }
       out.bad = bad ? 1 : 0;
     }
@@ -618,7 +672,7 @@ __device__ __forceinline__ Partial reduce_tile(int kind, const TAcc& ta, const D
 // merging the partials of one row (one warp per row)
 
 struct RowStat {
-  float tm, ts, dm, ds, dk;
+  float tm, ts, dm, ds, dk, ds2;
   int tidx, bad;
 };
 
@@ -626,21 +680,25 @@ struct RowStat {
 // KL = (K_d / S_d - (m_d - m_t)) / T - ln(S_d / S_t), in fp32 (GB300's fp64 rate is a small
 // fraction of its fp32 rate). The log of the ratio keeps the normaliser term exact to one
 // rounding; the other terms are the fp32 accumulators' own size.
+// SEPT: the draft sum at the target scale is ds2 (ds is at the draft's own scale).
+template <bool SEPT = false>
 __device__ __forceinline__ float row_nkl(const RowStat& r, float invT, float inv_lnV) {
-  const float kl = (r.dk / r.ds - (r.dm - r.tm)) * invT - logf(r.ds / r.ts);
+  const float S = SEPT ? r.ds2 : r.ds;
+  const float kl = (r.dk / S - (r.dm - r.tm)) * invT - logf(S / r.ts);
   return kl * inv_lnV;
 }
 
-__device__ __forceinline__ RowStat merge_row(const Partial* pp, int nchunks, float c) {
+// ds is merged at the draft scale cd, dk and ds2 at the target scale c.
+__device__ __forceinline__ RowStat merge_row(const Partial* pp, int nchunks, float c, float cd) {
   const int lane = threadIdx.x & 31;
-  float tm = -INFINITY, ts = 0.f, dm = -INFINITY, ds = 0.f, dk = 0.f;
+  float tm = -INFINITY, ts = 0.f, dm = -INFINITY, ds = 0.f, dk = 0.f, ds2 = 0.f;
   int idx = INT_MAX, bad = 0;
   for (int ch = lane; ch < nchunks; ch += 32) {
     const float4 lo = __ldcg(reinterpret_cast<const float4*>(pp + ch));
     const float4 hi = __ldcg(reinterpret_cast<const float4*>(pp + ch) + 1);
     const float qtm = lo.x, qts = lo.y;
     const int qidx = __float_as_int(lo.z), qbad = __float_as_int(lo.w);
-    const float qdm = hi.x, qds = hi.y, qdk = hi.z;
+    const float qdm = hi.x, qds = hi.y, qdk = hi.z, qds2 = hi.w;
     bad |= qbad;
     if (qtm > tm || (qtm == tm && qidx < idx)) idx = qidx;
     const float M = fmaxf(tm, qtm);
@@ -649,8 +707,11 @@ __device__ __forceinline__ RowStat merge_row(const Partial* pp, int nchunks, flo
     const float D = fmaxf(dm, qdm);
     const float f0 = (dm == -INFINITY) ? 0.f : ex2((dm - D) * c);
     const float f1 = (qdm == -INFINITY) ? 0.f : ex2((qdm - D) * c);
-    ds = ds * f0 + qds * f1;
+    const float g0 = (dm == -INFINITY) ? 0.f : ex2((dm - D) * cd);
+    const float g1 = (qdm == -INFINITY) ? 0.f : ex2((qdm - D) * cd);
+    ds = ds * g0 + qds * g1;
     dk = dk * f0 + qdk * f1;
+    ds2 = ds2 * f0 + qds2 * f1;
     dm = D;
   }
   RowStat r;
@@ -659,8 +720,10 @@ __device__ __forceinline__ RowStat merge_row(const Partial* pp, int nchunks, flo
   r.ts = warp_sum(rescale(ts, tm, r.tm, c));
   r.dm = warp_max(dm);
   const float fd = (dm == -INFINITY) ? 0.f : ex2((dm - r.dm) * c);
-  r.ds = warp_sum(ds * fd);
+  const float gd = (dm == -INFINITY) ? 0.f : ex2((dm - r.dm) * cd);
+  r.ds = warp_sum(ds * gd);
   r.dk = warp_sum(dk * fd);
+  r.ds2 = warp_sum(ds2 * fd);
   r.bad = __any_sync(kFull, bad) ? 1 : 0;
   return r;
 }

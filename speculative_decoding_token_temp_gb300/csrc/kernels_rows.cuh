@@ -13,7 +13,16 @@ __global__ void prologue_kernel(const __grid_constant__ ProParams p) {
   griddep_launch();
   griddep_wait();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b == 0) p.cntA[p.B] = 0u;
+  if (b == 0) {
+    p.cntA[p.B] = 0u;
+    if (p.stats != nullptr && p.stats->bucket != p.bucket) {
+      // a new time bucket takes over the slot (every finaliser of this call runs after
+      // the prologue has completed, and every earlier call has completed)
+      p.stats->rounds = p.stats->accepted = p.stats->drafted = 0;
+      p.stats->rate_fx = p.stats->rate2_fx = 0;
+      p.stats->bucket = p.bucket;
+    }
+  }
   if (b >= p.B) return;
   p.cntA[b] = 0u;
   p.cntB[b] = 0u;
@@ -40,7 +49,7 @@ __global__ void prologue_kernel(const __grid_constant__ ProParams p) {
 // itself (a batch whose offsets failed the prologue's check leaves some unpublished).
 template <int MODE>
 __device__ __forceinline__ void tile_done(const RowsParams& p) {
-  if constexpr (MODE == M_STOCH) {
+  if constexpr (is_stoch(MODE)) {
     __threadfence();
     atomicAdd(p.cnt + p.B, 1u);
   }
@@ -55,6 +64,62 @@ __device__ __forceinline__ void publish_rec(SeqRec* dst, SeqRec q) {
   *dst = q;
   __threadfence();
   st_relaxed_gpu(&dst->state, state);
+}
+
+// ---------------------------------------------------------------------------
+// policy epilogues
+
+// NKL threshold of draft i of sequence b: delta, or with positions the position-adaptive
+// min(dmax, delta * (1 + dalpha * log2(pos))), pos = position[b] + i, 1-based ([CoD] 4.3).
+// Negative (every mask 0) when position[b] < 1.
+__device__ __forceinline__ float nkl_threshold(const RowsParams& p, int b, int i) {
+  if (p.position == nullptr) return p.delta;
+  const long long P = (long long)p.position[b];
+  if (P < 1) return -1.f;
+  return fminf(p.dmax, p.delta * (1.f + p.dalpha * log2f((float)(P + i))));
+}
+
+// Block-accept ([CoD] 3.3): the end of the longest run of at least min_block consecutive
+// positions whose draft equals the target argmax (the earliest of equally long runs), or
+// 0 without one.
+template <class RS>
+__device__ __forceinline__ int block_end(const int32_t* tok, const RS* rs, int gb, int min_block) {
+  int best = 0, start = 0, run = 0;
+  for (int i = 0; i < gb; ++i) {
+    run = (tok[i] == rs[i].tidx) ? run + 1 : 0;
+    if (run > best) {
+      best = run;
+      start = i - run + 1;
+    }
+  }
+  return best >= min_block ? start + best : 0;
+}
+
+// One round of acceptance statistics: n of gamma drafts accepted (gamma > 0). The rates
+// are rounded to multiples of 2^-32 so the sums are exact integers.
+__device__ __forceinline__ void add_round(spec_stats_slot* st, int n, int gamma) {
+  auto* a = reinterpret_cast<unsigned long long*>(st);
+  const unsigned long long un = (unsigned long long)n, ug = (unsigned long long)gamma;
+  atomicAdd(a + 1, 1ull);
+  atomicAdd(a + 2, un);
+  atomicAdd(a + 3, ug);
+  atomicAdd(a + 4, (((un << 33) / ug) + 1ull) >> 1);
+  atomicAdd(a + 5, ((((un * un) << 33) / (ug * ug)) + 1ull) >> 1);
+}
+
+// Block-accept outputs and acceptance statistics of a decided sequence (n of gb drafts
+// accepted; rs[i].tidx is the target argmax of position i). Called by every thread.
+template <class SY, class RS>
+__device__ __forceinline__ void policy_epilogue(const RowsParams& p, int b, int gb, int db, int n, const RS* rs) {
+  if (p.min_block > 0) {
+    __shared__ int s_e;
+    if (threadIdx.x == 0) s_e = block_end(p.tokens + db, rs, gb, p.min_block);
+    SY::sync();
+    const int e = s_e;
+    for (int k = threadIdx.x; k < gb; k += SY::NT) p.block_tok[db + k] = (k < e) ? p.tokens[db + k] : rs[k].tidx;
+    if (threadIdx.x == 0) p.block_n[b] = e;
+  }
+  if (p.stats != nullptr && gb > 0 && threadIdx.x == 0) add_round(p.stats, n, gb);
 }
 
 // ---------------------------------------------------------------------------
@@ -77,7 +142,7 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
     s_err = 0u;
   }
   for (int i = warp; i < R; i += NW) {
-    const RowStat r = merge_row(p.part + (size_t)(row0 + i) * p.nchunks, p.nchunks, c);
+    const RowStat r = merge_row(p.part + (size_t)(row0 + i) * p.nchunks, p.nchunks, c, p.cd);
     if (lane == 0) rs[i] = r;
   }
   SY::sync();
@@ -146,11 +211,12 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
         atomicOr(p.status, SPEC_DEV_NONFINITE);
       } else {
         v = row_nkl(r, p.invT, p.inv_lnV);
-        m = v < p.delta ? 1 : 0;
+        m = v < nkl_threshold(p, b, i) ? 1 : 0;
       }
       p.nkl[db + i] = v;
       if (p.mask) p.mask[db + i] = m;
     }
+    if (tid == 0 && p.position != nullptr && p.position[b] < 1) atomicOr(p.status, SPEC_DEV_POSITION);
     (void)tbn;
     return;
   } else {
@@ -168,8 +234,9 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
     if (tid == 0) atomicOr(p.status, s_err);
     for (int k = tid; k <= gb; k += NT) {
       p.out_tok[tb + k] = -1;
-      if (MODE == M_STOCH && p.g_tok) p.g_tok[tb + k] = -1;
-      if (MODE == M_STOCH && k < gb) {
+      if (is_stoch(MODE) && p.g_tok) p.g_tok[tb + k] = -1;
+      if (p.block_tok != nullptr && k < gb) p.block_tok[db + k] = -1;
+      if (is_stoch(MODE) && k < gb) {
         const float qnan = __int_as_float(0x7fc00000);
         if (p.p_x) p.p_x[db + k] = qnan;
         if (p.q_x) p.q_x[db + k] = qnan;
@@ -180,7 +247,8 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
     }
     if (tid == 0) {
       p.n_acc[b] = -1;
-      if (MODE == M_STOCH) {
+      if (p.block_n != nullptr) p.block_n[b] = -1;
+      if (is_stoch(MODE)) {
         if (p.g_n) p.g_n[b] = -1;
         SeqRec q;
         q.state = REC_SKIP;
@@ -202,6 +270,7 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
     for (int k = tid; k <= gb; k += NT)
       p.out_tok[tb + k] = (k < n) ? p.tokens[db + k] : (k == n ? rs[n].tidx : -1);
     if (tid == 0) p.n_acc[b] = n;
+    policy_epilogue<SY>(p, b, gb, db, n, rs);
     return;
   } else {
   // stochastic
@@ -210,16 +279,16 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
     const int x = p.tokens[db + i];
     const float zt = elem_at<E>(target + (size_t)(tb + i) * V, x);
     const float zd = elem_at<E>(draft + (size_t)(db + i) * V, x);
-    const float lp2 = (zt - r.tm) * c - log2f(r.ts);  // log2 p(x)
-    const float lq2 = (zd - r.dm) * c - log2f(r.ds);  // log2 q(x)
+    const float lp2 = (zt - r.tm) * c - log2f(r.ts);     // log2 p(x)
+    const float lq2 = (zd - r.dm) * p.cd - log2f(r.ds);  // log2 q(x), at the draft's temperature
     const float a = exp2f(fminf(0.f, lp2 - lq2));
     if (p.p_x) p.p_x[db + i] = exp2f(lp2);
     if (p.q_x) p.q_x[db + i] = exp2f(lq2);
     if (p.alpha) p.alpha[db + i] = a;
     if (p.nkl || p.mask) {
-      const float v = row_nkl(r, p.invT, p.inv_lnV);
+      const float v = row_nkl<MODE == M_STOCH2>(r, p.invT, p.inv_lnV);  // both rows at the target's T
       if (p.nkl) p.nkl[db + i] = v;
-      if (p.mask) p.mask[db + i] = v < p.delta ? 1 : 0;
+      if (p.mask) p.mask[db + i] = v < nkl_threshold(p, b, i) ? 1 : 0;
     }
     if (!(p.u_accept[db + i] <= a)) atomicMin(&s_n, i);
     if (x != r.tidx) atomicMin(&s_gn, i);
@@ -234,7 +303,9 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
   if (tid == 0) {
     p.n_acc[b] = n;
     if (p.g_n) p.g_n[b] = gn;
+    if (p.mask && p.position != nullptr && p.position[b] < 1) atomicOr(p.status, SPEC_DEV_POSITION);
   }
+  policy_epilogue<SY>(p, b, gb, db, n, rs);
   if (tid == 0) {
     SeqRec q;
     q.state = REC_READY;
@@ -242,7 +313,7 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
     q.t_row = tb + n;
     q.d_row = (n < gb) ? db + n : -1;
     q.lt2 = rs[n].tm * c + log2f(rs[n].ts);
-    q.ld2 = (n < gb) ? rs[n].dm * c + log2f(rs[n].ds) : 0.f;
+    q.ld2 = (n < gb) ? rs[n].dm * p.cd + log2f(rs[n].ds) : 0.f;
     q.us = p.u_sample[b];
     q.mode = (n < gb) ? S_RESID : S_P;
     publish_rec(p.rec + b, q);
@@ -274,8 +345,9 @@ __device__ __forceinline__ void unpack2(const uint4& a, const uint4& b, float (&
 // vectors v and v + 256 of the target and of the draft row, for a single row the vectors
 // v, v + 256, v + 512, v + 768; each pair of vectors is folded in as one group.
 template <typename E, int VEC, int MODE, int KIND>
-__device__ __forceinline__ void stream_tile(const E* trow, const E* drow, int v0, int v1, float c, TAcc& ta,
-                                            DAcc& da, unsigned char* smem) {
+__device__ __forceinline__ void stream_tile(const E* trow, const E* drow, int v0, int v1, float c, float cd,
+                                            TAcc& ta, DAcc& da, unsigned char* smem) {
+  constexpr bool IDX = is_stoch(MODE), SEPT = MODE == M_STOCH2;
   constexpr int PER = (KIND == K_PAIR) ? 2 * kThreads : 4 * kThreads;  // vectors of a row per stage
   constexpr unsigned SLOT = kCV * kThreads * 16;                         // bytes of one stage
   const int t = threadIdx.x;
@@ -313,12 +385,12 @@ __device__ __forceinline__ void stream_tile(const E* trow, const E* drow, int v0
         float ft[2 * VEC], fd[2 * VEC];
         unpack2<E, VEC>(q[0], q[kThreads], ft);
         unpack2<E, VEC>(q[2 * kThreads], q[3 * kThreads], fd);
-        pair_update<2 * VEC, MODE == M_STOCH, VEC>(ta, da, ft, fd, va * VEC, c, vb * VEC);
+        pair_update<2 * VEC, IDX, VEC, SEPT>(ta, da, ft, fd, va * VEC, c, vb * VEC, cd);
       } else if (va < v1) {
         float ft[VEC], fd[VEC];
         IO<E, VEC>::unpack(q[0], ft);
         IO<E, VEC>::unpack(q[2 * kThreads], fd);
-        pair_update<VEC, MODE == M_STOCH>(ta, da, ft, fd, va * VEC, c);
+        pair_update<VEC, IDX, VEC, SEPT>(ta, da, ft, fd, va * VEC, c, 0, cd);
       }
     } else {
 #pragma unroll
@@ -399,7 +471,8 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
       return;
     }
   }
-  const int kind = (MODE == M_NKL) ? K_PAIR : (MODE == M_STOCH ? (i < gb ? K_PAIR : K_TSUM) : K_ARGMAX);
+  const int kind = (MODE == M_NKL) ? K_PAIR : (is_stoch(MODE) ? (i < gb ? K_PAIR : K_TSUM) : K_ARGMAX);
+  constexpr bool IDX = is_stoch(MODE), SEPT = MODE == M_STOCH2;
   const size_t V = (size_t)p.V;
   const size_t trow_i = (MODE == M_NKL) ? (size_t)r + b : (size_t)r;
   const size_t drow_i = (MODE == M_NKL) ? (size_t)r : (size_t)(r - b);
@@ -408,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
   const int e_begin = chunk * p.chunk_elems;
   const int e_end = min(e_begin + p.chunk_elems, p.V);
   const int v1 = e_end / VEC;
-  const float c = p.c;
+  const float c = p.c, cd = p.cd;
 
   TAcc ta;
   DAcc da;
@@ -416,14 +489,14 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
   init(da);
   if constexpr (VEC > 1) {
     if constexpr (MODE == M_GREEDY || MODE == M_TREE) {
-      stream_tile<E, VEC, MODE, K_ARGMAX>(trow, drow, e_begin / VEC, v1, c, ta, da, dsm);
+      stream_tile<E, VEC, MODE, K_ARGMAX>(trow, drow, e_begin / VEC, v1, c, cd, ta, da, dsm);
     } else if constexpr (MODE == M_NKL) {
-      stream_tile<E, VEC, MODE, K_PAIR>(trow, drow, e_begin / VEC, v1, c, ta, da, dsm);
+      stream_tile<E, VEC, MODE, K_PAIR>(trow, drow, e_begin / VEC, v1, c, cd, ta, da, dsm);
     } else {
       if (kind == K_PAIR)
-        stream_tile<E, VEC, MODE, K_PAIR>(trow, drow, e_begin / VEC, v1, c, ta, da, dsm);
+        stream_tile<E, VEC, MODE, K_PAIR>(trow, drow, e_begin / VEC, v1, c, cd, ta, da, dsm);
       else
-        stream_tile<E, VEC, MODE, K_TSUM>(trow, drow, e_begin / VEC, v1, c, ta, da, dsm);
+        stream_tile<E, VEC, MODE, K_TSUM>(trow, drow, e_begin / VEC, v1, c, cd, ta, da, dsm);
     }
   } else {
   int v = e_begin / VEC + threadIdx.x;
@@ -434,16 +507,16 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
       float ft[VEC], fd[VEC];
       io::unpack(t0, ft);
       io::unpack(d0, fd);
-      pair_update<VEC, MODE == M_STOCH>(ta, da, ft, fd, v * VEC, c);
+      pair_update<VEC, IDX, VEC, SEPT>(ta, da, ft, fd, v * VEC, c, 0, cd);
       io::unpack(t1, ft);
       io::unpack(d1, fd);
-      pair_update<VEC, MODE == M_STOCH>(ta, da, ft, fd, (v + kThreads) * VEC, c);
+      pair_update<VEC, IDX, VEC, SEPT>(ta, da, ft, fd, (v + kThreads) * VEC, c, 0, cd);
     }
     if (v < v1) {
       float ft[VEC], fd[VEC];
       io::unpack(io::load(trow, v), ft);
       io::unpack(io::load(drow, v), fd);
-      pair_update<VEC, MODE == M_STOCH>(ta, da, ft, fd, v * VEC, c);
+      pair_update<VEC, IDX, VEC, SEPT>(ta, da, ft, fd, v * VEC, c, 0, cd);
     }
   } else if (kind == K_TSUM) {
     for (; v + 3 * kThreads < v1; v += 4 * kThreads) {
@@ -482,11 +555,11 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
   }
   }
 
-  const Partial part = reduce_tile<BlockSync, E, VEC>(kind, ta, da, c, trow);
+  const Partial part = reduce_tile<BlockSync, E, VEC, SEPT>(kind, ta, da, c, trow, cd);
   if (threadIdx.x == 0) {
     float4* dst = reinterpret_cast<float4*>(p.part + tile);
     __stcg(dst, make_float4(part.tm, part.ts, __int_as_float(part.tidx), __int_as_float(part.bad)));
-    __stcg(dst + 1, make_float4(part.dm, part.ds, part.dk, 0.f));
+    __stcg(dst + 1, make_float4(part.dm, part.ds, part.dk, part.ds2));
     __threadfence();
     const unsigned total = (unsigned)((gb + HB) * p.nchunks);
     const unsigned old = atomicAdd(p.cnt + b, 1u);
@@ -499,9 +572,48 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
   }
   __threadfence();
   finalize<E, MODE, BlockSync>(p, b, gb, r - i, c0);
-  if constexpr (MODE == M_STOCH) {
+  if constexpr (is_stoch(MODE)) {
     __syncthreads();  // the finaliser's writes, made by any thread, precede the count
     if (threadIdx.x == 0) tile_done<MODE>(p);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// acceptance statistics summary: one thread per slot, then thread 0 combines the slots of
+// the window (integer sums, so the order does not matter)
+
+__global__ void __launch_bounds__(SPEC_STATS_SLOTS) summary_kernel(const spec_accept_stats* st, long long now,
+                                                                  int window, double* out) {
+  griddep_wait();  // the calls it summarises have completed
+  __shared__ unsigned long long s[5][SPEC_STATS_SLOTS];
+  const int t = threadIdx.x;
+  const spec_stats_slot sl = st->slot[t];
+  const bool in = sl.bucket > now - window && sl.bucket <= now;
+  s[0][t] = in ? sl.rounds : 0ull;
+  s[1][t] = in ? sl.accepted : 0ull;
+  s[2][t] = in ? sl.drafted : 0ull;
+  s[3][t] = in ? sl.rate_fx : 0ull;
+  s[4][t] = in ? sl.rate2_fx : 0ull;
+  __syncthreads();
+  if (t == 0) {
+    unsigned long long a[5] = {0ull, 0ull, 0ull, 0ull, 0ull};
+    for (int k = 0; k < SPEC_STATS_SLOTS; ++k)
+      for (int j = 0; j < 5; ++j) a[j] += s[j][k];
+    const double R = (double)a[0];
+    double mean_acc = 0.0, mean_rate = 0.0, arsd = 0.0;
+    if (a[0] > 0) {
+      const double unit = 1.0 / 4294967296.0;  // 2^-32
+      mean_acc = (double)a[1] / R;
+      mean_rate = (double)a[3] * unit / R;
+      const double var = (double)a[4] * unit / R - mean_rate * mean_rate;
+      arsd = var > 0.0 ? sqrt(var) : 0.0;
+    }
+    out[0] = R;
+    out[1] = (double)a[1];
+    out[2] = (double)a[2];
+    out[3] = mean_acc;
+    out[4] = mean_rate;
+    out[5] = arsd;
   }
 }
 

@@ -11,12 +11,12 @@ namespace sv {
 // Weights of one loaded vector.
 template <int VEC>
 __device__ __forceinline__ void weights(int mode, const float (&t)[VEC], const float (&d)[VEC], float lt2, float ld2,
-                                        float c, float (&w)[VEC]) {
+                                        float c, float cd, float (&w)[VEC]) {
   if (mode == S_RESID) {
 #pragma unroll
     for (int k = 0; k < VEC; ++k) {
       const float pv = ex2(fmaf(t[k], c, -lt2));
-      const float qv = ex2(fmaf(d[k], c, -ld2));
+      const float qv = ex2(fmaf(d[k], cd, -ld2));
       w[k] = fmaxf(pv - qv, 0.f);
     }
   } else {
@@ -31,7 +31,7 @@ __device__ __forceinline__ void weights(int mode, const float (&t)[VEC], const f
 // at steps[warp * kMaxSteps + s].
 template <typename E, int VEC>
 __device__ __forceinline__ double segment_pass(const E* trow, const E* drow, int mode, float lt2, float ld2, float c,
-                                               int e_begin, int e_end, float* steps) {
+                                               float cd, int e_begin, int e_end, float* steps) {
   using io = IO<E, VEC>;
   using raw_t = typename io::raw_t;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -61,7 +61,7 @@ __device__ __forceinline__ double segment_pass(const E* trow, const E* drow, int
         float ft[VEC], fd[VEC], w[VEC];
         io::unpack(rt[u], ft);
         if (mode == S_RESID) io::unpack(rd[u], fd);
-        weights<VEC>(mode, ft, fd, lt2, ld2, c, w);
+        weights<VEC>(mode, ft, fd, lt2, ld2, c, cd, w);
         ls = tree_sum<VEC>(w);
       }
       const float st = warp_sum(ls);
@@ -76,7 +76,7 @@ __device__ __forceinline__ double segment_pass(const E* trow, const E* drow, int
       float ft[VEC], fd[VEC], w[VEC];
       io::unpack(io::load(trow, v), ft);
       if (mode == S_RESID) io::unpack(io::load(drow, v), fd);
-      weights<VEC>(mode, ft, fd, lt2, ld2, c, w);
+      weights<VEC>(mode, ft, fd, lt2, ld2, c, cd, w);
       ls = tree_sum<VEC>(w);
     }
     const float st = warp_sum(ls);
@@ -118,12 +118,12 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const __grid_constant_
   const size_t V = (size_t)p.V;
   const E* trow = static_cast<const E*>(p.target) + (size_t)q.t_row * V;
   const E* drow = static_cast<const E*>(p.draft) + (q.mode == S_RESID ? (size_t)q.d_row * V : 0);
-  const float c = p.c;
+  const float c = p.c, cd = p.cd;
   double* tot = p.segtot + (size_t)b * p.nseg;
 
   {
     const int e0 = seg * p.seg_elems, e1 = min(e0 + p.seg_elems, p.V);
-    const double ws = segment_pass<E, VEC>(trow, drow, q.mode, q.lt2, q.ld2, c, e0, e1, nullptr);
+    const double ws = segment_pass<E, VEC>(trow, drow, q.mode, q.lt2, q.ld2, c, cd, e0, e1, nullptr);
     if (lane == 0) s_w[warp] = ws;
     __syncthreads();
     if (tid == 0) {
@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const __grid_constant_
     mode = s_mode;
     for (int s = 0; s < p.nseg; ++s) {
       const int e0 = s * p.seg_elems, e1 = min(e0 + p.seg_elems, p.V);
-      const double ws = segment_pass<E, VEC>(trow, drow, mode, q.lt2, q.ld2, c, e0, e1, nullptr);
+      const double ws = segment_pass<E, VEC>(trow, drow, mode, q.lt2, q.ld2, c, cd, e0, e1, nullptr);
       if (lane == 0) s_w[warp] = ws;
       __syncthreads();
       if (tid == 0) {
@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const __grid_constant_
   __syncthreads();
   const int sel = s_seg;
   const int e0 = sel * p.seg_elems, e1 = min(e0 + p.seg_elems, p.V);
-  segment_pass<E, VEC>(trow, drow, mode, q.lt2, q.ld2, c, e0, e1, s_steps);
+  segment_pass<E, VEC>(trow, drow, mode, q.lt2, q.ld2, c, cd, e0, e1, s_steps);
   __syncthreads();
   const int v0 = e0 / VEC, v1 = e1 / VEC;
   const int W = (v1 - v0 + kWarps - 1) / kWarps;
@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const __grid_constant_
       float ft[VEC], fd[VEC];
       io::unpack(io::load(trow, v), ft);
       if (mode == S_RESID) io::unpack(io::load(drow, v), fd);
-      weights<VEC>(mode, ft, fd, q.lt2, q.ld2, c, w);
+      weights<VEC>(mode, ft, fd, q.lt2, q.ld2, c, cd, w);
     }
     const float ls = tree_sum<VEC>(w);
     float incl = ls;
@@ -464,11 +464,11 @@ __device__ __forceinline__ void block_crossing(const float* table, int n, float 
 
 template <typename E, int VEC>
 __device__ __forceinline__ void vec_weights(const uint4& tv, const uint4* dv, int mode, float lt2, float ld2, float c,
-                                            float (&w)[VEC]) {
+                                            float cd, float (&w)[VEC]) {
   float ft[VEC], fd[VEC];
   IO<E, VEC>::unpack(tv, ft);
   if (mode == S_RESID) IO<E, VEC>::unpack(*dv, fd);
-  weights<VEC>(mode, ft, fd, lt2, ld2, c, w);
+  weights<VEC>(mode, ft, fd, lt2, ld2, c, cd, w);
 }
 
 // Masses of stages [k0, k1) of the row pair (or row): in each 512-vector stage thread t
@@ -477,7 +477,7 @@ __device__ __forceinline__ void vec_weights(const uint4& tv, const uint4* dv, in
 // `table` receives the mass of warp w's 32-vector slice of half h of stage k -- token
 // order.
 template <typename E, int VEC>
-__device__ __forceinline__ void mass_pass(const E* trow, const E* drow, int mode, float lt2, float ld2, float c,
+__device__ __forceinline__ void mass_pass(const E* trow, const E* drow, int mode, float lt2, float ld2, float c, float cd,
                                           int NV, int k0, int k1, float* table, unsigned char* smem) {
   constexpr unsigned SLOT = kCV * kThreads * 16;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -507,7 +507,7 @@ __device__ __forceinline__ void mass_pass(const E* trow, const E* drow, int mode
       float ls = 0.f;
       if (v < NV) {
         float w[VEC];
-        vec_weights<E, VEC>(q[h * kThreads], q + (2 + h) * kThreads, mode, lt2, ld2, c, w);
+        vec_weights<E, VEC>(q[h * kThreads], q + (2 + h) * kThreads, mode, lt2, ld2, c, cd, w);
         ls = tree_sum<VEC>(w);
       }
       const float ws = warp_sum(ls);
@@ -521,7 +521,7 @@ __device__ __forceinline__ void mass_pass(const E* trow, const E* drow, int mode
 // slice -- one vector per lane, in token order -- and returns the token where the
 // running mass passes rem.
 template <typename E, int VEC>
-__device__ __forceinline__ int slice_token(const E* trow, const E* drow, int mode, float lt2, float ld2, float c,
+__device__ __forceinline__ int slice_token(const E* trow, const E* drow, int mode, float lt2, float ld2, float c, float cd,
                                            int V, int NV, int ent, float rem) {
   const int lane = threadIdx.x & 31;
   const int k = ent / kSlicesPerStage, h = (ent / kWarps) & 1, w = ent % kWarps;
@@ -533,7 +533,7 @@ __device__ __forceinline__ int slice_token(const E* trow, const E* drow, int mod
     const uint4 tv = ld_stream16(trow + (size_t)v * VEC);
     uint4 dv = tv;
     if (mode == S_RESID) dv = ld_stream16(drow + (size_t)v * VEC);
-    vec_weights<E, VEC>(tv, &dv, mode, lt2, ld2, c, wt);
+    vec_weights<E, VEC>(tv, &dv, mode, lt2, ld2, c, cd, wt);
   }
   const float ls = tree_sum<VEC>(wt);
   float incl = ls;
@@ -636,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, 4) sample2_kernel(const __grid_const
     const E* trow = static_cast<const E*>(p.target) + (size_t)q.t_row * V;
     const E* drow = static_cast<const E*>(p.draft) + (q.mode == S_RESID ? (size_t)q.d_row * V : 0);
     float* table = p.table + (size_t)b * p.table_stride;
-    mass_pass<E, VEC>(trow, drow, q.mode, q.lt2, q.ld2, p.c, NV, k0, k1, table, dsm);
+    mass_pass<E, VEC>(trow, drow, q.mode, q.lt2, q.ld2, p.c, p.cd, NV, k0, k1, table, dsm);
     __syncthreads();  // orders every warp's table entries before thread 0's fence
     if (tid == 0) {
       __threadfence();  // the block's table entries are visible before its ticket
@@ -653,12 +653,12 @@ __global__ void __launch_bounds__(kThreads, 4) sample2_kernel(const __grid_const
       block_crossing(table, nent, q.us, dsm, sc, s_max);
       if (!(mode == S_RESID && !(sc.Z > 1e-30f))) break;
       mode = S_P;  // zero residual: the masses of p of the same row, whole row in this block
-      mass_pass<E, VEC>(trow, drow, mode, q.lt2, q.ld2, p.c, NV, 0, nst, table, dsm);
+      mass_pass<E, VEC>(trow, drow, mode, q.lt2, q.ld2, p.c, p.cd, NV, 0, nst, table, dsm);
       __syncthreads();
     }
     const int ent = sc.ent;
     if (warp == ent % kWarps) {
-      const int y = slice_token<E, VEC>(trow, drow, mode, q.lt2, q.ld2, p.c, p.V, NV, ent, sc.rem);
+      const int y = slice_token<E, VEC>(trow, drow, mode, q.lt2, q.ld2, p.c, p.cd, p.V, NV, ent, sc.rem);
       if (lane == 0) p.out_tok[q.t_row] = y;
     }
     __syncthreads();

@@ -122,7 +122,14 @@ cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, cudaStream_t stream, con
   return launch(kernel, grid, block, stream, params, true);
 }
 
-cudaError_t launch_prologue(const spec_batch& g, const Layout& L, char* ws, uint32_t* status, cudaStream_t stream) {
+// slot of a statistics bucket (labels may be negative)
+int stats_slot(int64_t bucket) {
+  const int64_t m = bucket % SPEC_STATS_SLOTS;
+  return (int)(m < 0 ? m + SPEC_STATS_SLOTS : m);
+}
+
+cudaError_t launch_prologue(const spec_batch& g, const Layout& L, char* ws, uint32_t* status, cudaStream_t stream,
+                            const spec_options* opt = nullptr) {
   ProParams pp;
   pp.cu = g.cu_draft;
   pp.B = g.B;
@@ -132,6 +139,8 @@ cudaError_t launch_prologue(const spec_batch& g, const Layout& L, char* ws, uint
   pp.cntB = reinterpret_cast<unsigned*>(ws + L.cntB);
   pp.rec = reinterpret_cast<SeqRec*>(ws + L.rec);
   pp.status = status;
+  pp.stats = (opt && opt->stats) ? &opt->stats->slot[stats_slot(opt->stats_bucket)] : nullptr;
+  pp.bucket = opt ? (long long)opt->stats_bucket : 0;
   return launch(prologue_kernel, dim3((unsigned)ceil_div(g.B, kThreads)), dim3(kThreads), stream, pp, true);
 }
 
@@ -244,6 +253,40 @@ bool vec_path(spec_dtype dt, int V, const void* a, const void* b) {
 
 bool temperature_ok(float T) { return isfinite(T) && T > 0.f; }
 
+// Host checks of an options block for a call of the given kind (stochastic, greedy or
+// NKL); fields the call does not use are not looked at.
+spec_status check_options(const spec_options* o, spec_mode mode) {
+  if (o == nullptr) return SPEC_OK;
+  if (mode == SPEC_MODE_STOCHASTIC && !(o->temperature_draft == 0.f || temperature_ok(o->temperature_draft)))
+    return SPEC_ERR_INVALID_ARG;
+  if (mode != SPEC_MODE_GREEDY && o->position != nullptr &&
+      !(isfinite(o->delta_alpha) && isfinite(o->delta_max)))
+    return SPEC_ERR_INVALID_ARG;
+  if (mode != SPEC_MODE_NKL) {
+    if (o->min_block_len < 0) return SPEC_ERR_INVALID_ARG;
+    if (o->min_block_len > 0 && (!o->block_n || !o->block_tokens)) return SPEC_ERR_INVALID_ARG;
+  }
+  return SPEC_OK;
+}
+
+// Copies the options a tile kernel uses into its parameters.
+void apply_options(RowsParams& rp, const spec_options* o, spec_mode mode) {
+  if (o == nullptr) return;
+  if (mode != SPEC_MODE_GREEDY && o->position != nullptr) {
+    rp.position = o->position;
+    rp.dalpha = o->delta_alpha;
+    rp.dmax = o->delta_max;
+  }
+  if (mode != SPEC_MODE_NKL) {
+    if (o->min_block_len > 0) {
+      rp.min_block = o->min_block_len;
+      rp.block_n = o->block_n;
+      rp.block_tok = o->block_tokens;
+    }
+    if (o->stats) rp.stats = &o->stats->slot[stats_slot(o->stats_bucket)];
+  }
+}
+
 }  // namespace
 }  // namespace sv
 
@@ -280,11 +323,26 @@ spec_status spec_verify_stochastic(spec_batch g, spec_dtype dtype, const void* t
                                    int32_t* out_tokens, float* p_x, float* q_x, float* alpha, float* nkl,
                                    uint8_t* nkl_mask, float nkl_delta, int32_t* greedy_n, int32_t* greedy_tokens,
                                    uint32_t* device_status, void* workspace, size_t workspace_bytes,
-                                   spec_stream_t stream_) {
+                                   spec_stream_t stream) {
+  return spec_verify_stochastic_ex(g, dtype, target_logits, draft_logits, draft_tokens, temperature, u_accept,
+                                   u_sample, n_accepted, out_tokens, p_x, q_x, alpha, nkl, nkl_mask, nkl_delta,
+                                   greedy_n, greedy_tokens, nullptr, device_status, workspace, workspace_bytes,
+                                   stream);
+}
+
+spec_status spec_verify_stochastic_ex(spec_batch g, spec_dtype dtype, const void* target_logits,
+                                      const void* draft_logits, const int32_t* draft_tokens, float temperature,
+                                      const float* u_accept, const float* u_sample, int32_t* n_accepted,
+                                      int32_t* out_tokens, float* p_x, float* q_x, float* alpha, float* nkl,
+                                      uint8_t* nkl_mask, float nkl_delta, int32_t* greedy_n,
+                                      int32_t* greedy_tokens, const spec_options* options, uint32_t* device_status,
+                                      void* workspace, size_t workspace_bytes, spec_stream_t stream_) {
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
   spec_status st = check_batch(g);
   if (st != SPEC_OK) return st;
   if (!temperature_ok(temperature)) return SPEC_ERR_INVALID_ARG;
+  st = check_options(options, SPEC_MODE_STOCHASTIC);
+  if (st != SPEC_OK) return st;
   if (g.B == 0) return SPEC_OK;
   if (!target_logits || !n_accepted || !out_tokens || !u_sample || !device_status) return SPEC_ERR_INVALID_ARG;
   if (g.total_draft > 0 && (!draft_logits || !draft_tokens || !u_accept)) return SPEC_ERR_INVALID_ARG;
@@ -296,7 +354,7 @@ spec_status spec_verify_stochastic(spec_batch g, spec_dtype dtype, const void* t
   const bool bf16 = dtype == SPEC_BF16;
   const bool vec = vec_path(dtype, g.V, target_logits, draft_logits);
 
-  if (launch_prologue(g, L, ws, device_status, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (launch_prologue(g, L, ws, device_status, stream, options) != cudaSuccess) return SPEC_ERR_CUDA;
   RowsParams rp = base_params(g, L, ws, device_status);
   rp.target = target_logits;
   rp.draft = draft_logits;
@@ -305,7 +363,11 @@ spec_status spec_verify_stochastic(spec_batch g, spec_dtype dtype, const void* t
   rp.u_sample = u_sample;
   rp.c = (float)(1.4426950408889634 / (double)temperature);
   rp.invT = (float)(1.0 / (double)temperature);
+  const float Td = (options && options->temperature_draft > 0.f) ? options->temperature_draft : temperature;
+  const bool sept = Td != temperature;
+  rp.cd = sept ? (float)(1.4426950408889634 / (double)Td) : rp.c;
   rp.delta = nkl_delta;
+  apply_options(rp, options, SPEC_MODE_STOCHASTIC);
   rp.n_acc = n_accepted;
   rp.out_tok = out_tokens;
   rp.p_x = p_x;
@@ -315,7 +377,9 @@ spec_status spec_verify_stochastic(spec_batch g, spec_dtype dtype, const void* t
   rp.mask = nkl_mask;
   rp.g_n = greedy_n;
   rp.g_tok = greedy_tokens;
-  if (launch_rows<M_STOCH>(bf16, vec, rp, L.rows * L.nchunks, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  const cudaError_t le = sept ? launch_rows<M_STOCH2>(bf16, vec, rp, L.rows * L.nchunks, stream)
+                              : launch_rows<M_STOCH>(bf16, vec, rp, L.rows * L.nchunks, stream);
+  if (le != cudaSuccess) return SPEC_ERR_CUDA;
 
   SampleParams sp;
   memset(&sp, 0, sizeof(sp));
@@ -328,6 +392,7 @@ spec_status spec_verify_stochastic(spec_batch g, spec_dtype dtype, const void* t
   sp.nseg = L.nseg;
   sp.seg_elems = L.seg_elems;
   sp.c = rp.c;
+  sp.cd = rp.cd;
   sp.rec = rp.rec;
   sp.segtot = reinterpret_cast<double*>(ws + L.segtot);
   sp.cnt = reinterpret_cast<unsigned*>(ws + L.cntB);
@@ -368,9 +433,19 @@ spec_status spec_verify_stochastic(spec_batch g, spec_dtype dtype, const void* t
 spec_status spec_verify_greedy(spec_batch g, spec_dtype dtype, const void* target_logits,
                                const int32_t* draft_tokens, int32_t* n_accepted, int32_t* out_tokens,
                                uint32_t* device_status, void* workspace, size_t workspace_bytes,
-                               spec_stream_t stream_) {
+                               spec_stream_t stream) {
+  return spec_verify_greedy_ex(g, dtype, target_logits, draft_tokens, n_accepted, out_tokens, nullptr,
+                               device_status, workspace, workspace_bytes, stream);
+}
+
+spec_status spec_verify_greedy_ex(spec_batch g, spec_dtype dtype, const void* target_logits,
+                                  const int32_t* draft_tokens, int32_t* n_accepted, int32_t* out_tokens,
+                                  const spec_options* options, uint32_t* device_status, void* workspace,
+                                  size_t workspace_bytes, spec_stream_t stream_) {
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
   spec_status st = check_batch(g);
+  if (st != SPEC_OK) return st;
+  st = check_options(options, SPEC_MODE_GREEDY);
   if (st != SPEC_OK) return st;
   if (g.B == 0) return SPEC_OK;
   if (!target_logits || !n_accepted || !out_tokens || !device_status) return SPEC_ERR_INVALID_ARG;
@@ -379,13 +454,14 @@ spec_status spec_verify_greedy(spec_batch g, spec_dtype dtype, const void* targe
   if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u)) return SPEC_ERR_WORKSPACE;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   char* ws = static_cast<char*>(workspace);
-  if (launch_prologue(g, L, ws, device_status, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (launch_prologue(g, L, ws, device_status, stream, options) != cudaSuccess) return SPEC_ERR_CUDA;
   RowsParams rp = base_params(g, L, ws, device_status);
   rp.target = target_logits;
   rp.tokens = draft_tokens;
   rp.n_acc = n_accepted;
   rp.out_tok = out_tokens;
-  rp.c = 1.f;
+  rp.c = rp.cd = 1.f;
+  apply_options(rp, options, SPEC_MODE_GREEDY);
   if (launch_rows<M_GREEDY>(dtype == SPEC_BF16, vec_path(dtype, g.V, target_logits, nullptr), rp,
                             L.rows * L.nchunks, stream) != cudaSuccess)
     return SPEC_ERR_CUDA;
@@ -424,7 +500,7 @@ spec_status spec_verify_tree(int32_t B, int32_t N, int32_t V, spec_dtype dtype, 
   rp.accept_len = accept_len;
   rp.path_nodes = path_nodes;
   rp.out_tok = out_tokens;
-  rp.c = 1.f;
+  rp.c = rp.cd = 1.f;
   if (launch_rows<M_TREE>(dtype == SPEC_BF16, vec_path(dtype, V, target_logits, nullptr), rp, L.rows * L.nchunks,
                           stream) != cudaSuccess)
     return SPEC_ERR_CUDA;
@@ -433,11 +509,20 @@ spec_status spec_verify_tree(int32_t B, int32_t N, int32_t V, spec_dtype dtype, 
 
 spec_status spec_nkl(spec_batch g, spec_dtype dtype, const void* target_logits, const void* draft_logits,
                      float temperature, float delta, float* nkl, uint8_t* nkl_mask, uint32_t* device_status,
-                     void* workspace, size_t workspace_bytes, spec_stream_t stream_) {
+                     void* workspace, size_t workspace_bytes, spec_stream_t stream) {
+  return spec_nkl_ex(g, dtype, target_logits, draft_logits, temperature, delta, nkl, nkl_mask, nullptr,
+                     device_status, workspace, workspace_bytes, stream);
+}
+
+spec_status spec_nkl_ex(spec_batch g, spec_dtype dtype, const void* target_logits, const void* draft_logits,
+                        float temperature, float delta, float* nkl, uint8_t* nkl_mask, const spec_options* options,
+                        uint32_t* device_status, void* workspace, size_t workspace_bytes, spec_stream_t stream_) {
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
   spec_status st = check_batch(g);
   if (st != SPEC_OK) return st;
   if (!temperature_ok(temperature)) return SPEC_ERR_INVALID_ARG;
+  st = check_options(options, SPEC_MODE_NKL);
+  if (st != SPEC_OK) return st;
   if (g.B == 0 || g.total_draft == 0) return SPEC_OK;
   if (!target_logits || !draft_logits || !nkl || !device_status) return SPEC_ERR_INVALID_ARG;
   const Layout L = layout(g.B, g.V, rows_for(SPEC_MODE_NKL, g), false);
@@ -448,14 +533,34 @@ spec_status spec_nkl(spec_batch g, spec_dtype dtype, const void* target_logits, 
   RowsParams rp = base_params(g, L, ws, device_status);
   rp.target = target_logits;
   rp.draft = draft_logits;
-  rp.c = (float)(1.4426950408889634 / (double)temperature);
+  rp.c = rp.cd = (float)(1.4426950408889634 / (double)temperature);
   rp.invT = (float)(1.0 / (double)temperature);
   rp.delta = delta;
   rp.nkl = nkl;
   rp.mask = nkl_mask;
+  apply_options(rp, options, SPEC_MODE_NKL);
   if (launch_rows<M_NKL>(dtype == SPEC_BF16, vec_path(dtype, g.V, target_logits, draft_logits), rp,
                          L.rows * L.nchunks, stream) != cudaSuccess)
     return SPEC_ERR_CUDA;
+  return SPEC_OK;
+}
+
+spec_status spec_accept_summary(const spec_accept_stats* stats, int64_t bucket_now, int32_t window, double* out,
+                                spec_stream_t stream_) {
+  if (!stats || !out || window < 1 || window > SPEC_STATS_SLOTS) return SPEC_ERR_INVALID_ARG;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(SPEC_STATS_SLOTS);
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream_);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const long long now = (long long)bucket_now;
+  const int w = (int)window;
+  if (cudaLaunchKernelEx(&cfg, summary_kernel, stats, now, w, out) != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;
 }
 

@@ -15,9 +15,10 @@ def to_dev(a, dev):
     return torch.from_numpy(a).to(dev)
 
 
-def run_stochastic(w, dev, T=None, delta=0.15, offset=0):
-    """Call spec_verify_stochastic on a workload; offset > 0 shifts the logit buffers by
-    that many elements (misaligned base pointers force the scalar path)."""
+def run_stochastic(w, dev, T=None, delta=0.15, offset=0, options=None):
+    """Call spec_verify_stochastic (spec_verify_stochastic_ex when `options` is given: a
+    dict of its keywords, numpy arrays for position) on a workload; offset > 0 shifts the
+    logit buffers by that many elements (misaligned base pointers force the scalar path)."""
     T = w.T if T is None else T
 
     def put(a):
@@ -31,20 +32,30 @@ def run_stochastic(w, dev, T=None, delta=0.15, offset=0):
     t = put(w.target)
     d = put(w.draft)
     cu = None if w.dense else torch.from_numpy(w.cu_draft).to(dev)
-    res = api.spec_verify_stochastic(t, d, to_dev(w.tokens, dev), T, to_dev(w.u_accept, dev),
-                                     to_dev(w.u_sample, dev), cu_draft=cu, gamma=w.gamma_max if not w.dense
-                                     else int(w.gammas[0]) if w.B else 0, nkl_delta=delta)
+    kw = dict(cu_draft=cu, gamma=w.gamma_max if not w.dense else int(w.gammas[0]) if w.B else 0, nkl_delta=delta)
+    if options is None:
+        res = api.spec_verify_stochastic(t, d, to_dev(w.tokens, dev), T, to_dev(w.u_accept, dev),
+                                         to_dev(w.u_sample, dev), **kw)
+    else:
+        opts = {k: (torch.from_numpy(np.asarray(v, dtype=np.int32)).to(dev) if k == "position" else v)
+                for k, v in options.items()}
+        res = api.spec_verify_stochastic_ex(t, d, to_dev(w.tokens, dev), T, to_dev(w.u_accept, dev),
+                                            to_dev(w.u_sample, dev), **kw, **opts)
     torch.cuda.synchronize()
-    return {k: v.cpu().numpy() for k, v in res.items()}
+    return {k: v.cpu().numpy() for k, v in res.items() if k != "stats"}
 
 
-def compare_stochastic(w, res, seqs, T=None, delta=0.15, check_greedy=True):
+def compare_stochastic(w, res, seqs, T=None, delta=0.15, check_greedy=True, T_draft=None, positions=None,
+                       min_block_len=0):
     """n / tokens bit-exact for every sequence the oracle does not flag; a flagged sequence
     (a decision within 1e-5 of its boundary) may differ, but at most max(1, 1e-4 of the
-    sequences compared) may. Reals within REL. Returns (compared, flagged, mismatched)."""
+    sequences compared) may. Reals within REL; the NKL mask equal except within the NKL
+    tolerance of its threshold (delta, or the position-adaptive one); block-accept outputs
+    bit-exact. Returns (compared, flagged, mismatched)."""
     T = w.T if T is None else T
     ref = O.verify_stochastic(w.target, w.draft, w.tokens, w.cu_draft, T, w.u_accept, w.u_sample, w.dtype,
-                              nkl_delta=delta, seqs=seqs)
+                              nkl_delta=delta, seqs=seqs, T_draft=T_draft, positions=positions,
+                              min_block_len=min_block_len)
     flagged = mismatched = 0
     seqs = list(seqs)
     for b in seqs:
@@ -65,8 +76,16 @@ def compare_stochastic(w, res, seqs, T=None, delta=0.15, check_greedy=True):
             got = res["nkl"][d0:d0 + g].astype(np.float64)
             assert np.allclose(got, r["nkl"], rtol=REL, atol=NKL_ABS), (b, got, r["nkl"])
             m = res["nkl_mask"][d0:d0 + g]
-            near = np.abs(r["nkl"] - delta) <= REL * delta + NKL_ABS
-            assert np.all((m == r["mask"]) | near), (b, m, r["mask"])
+            thr = np.array([delta if positions is None or positions[b] < 1 else
+                            O.position_delta(int(positions[b]) + i, delta) for i in range(g)])
+            near = np.abs(r["nkl"] - thr) <= REL * thr + NKL_ABS
+            if positions is not None and positions[b] < 1:
+                assert np.all(m == 0), (b, m)
+            else:
+                assert np.all((m == r["mask"]) | near), (b, m, r["mask"])
+        if min_block_len > 0:
+            assert int(res["block_n"][b]) == r["block_n"], (b, res["block_n"][b], r["block_n"])
+            assert list(res["block_tokens"][d0:d0 + g]) == list(r["block_tokens"]), b
         if check_greedy:
             assert int(res["greedy_n"][b]) == r["greedy_n"]
             assert list(res["greedy_tokens"][t0:t0 + g + 1]) == list(r["greedy_tokens"])
@@ -74,41 +93,54 @@ def compare_stochastic(w, res, seqs, T=None, delta=0.15, check_greedy=True):
     return len(seqs), flagged, mismatched
 
 
-def run_greedy(w, dev):
+def run_greedy(w, dev, options=None):
     cu = None if w.dense else torch.from_numpy(w.cu_draft).to(dev)
-    res = api.spec_verify_greedy(to_dev(w.target, dev), to_dev(w.tokens, dev), cu_draft=cu,
-                                 gamma=w.gamma_max if not w.dense else int(w.gammas[0]))
+    kw = dict(cu_draft=cu, gamma=w.gamma_max if not w.dense else int(w.gammas[0]))
+    if options is None:
+        res = api.spec_verify_greedy(to_dev(w.target, dev), to_dev(w.tokens, dev), **kw)
+    else:
+        res = api.spec_verify_greedy_ex(to_dev(w.target, dev), to_dev(w.tokens, dev), **kw, **options)
     torch.cuda.synchronize()
     return {k: v.cpu().numpy() for k, v in res.items()}
 
 
-def compare_greedy(w, res, seqs):
-    ref = O.verify_greedy(w.target, w.tokens, w.cu_draft, w.dtype, seqs=seqs)
+def compare_greedy(w, res, seqs, min_block_len=0):
+    ref = O.verify_greedy(w.target, w.tokens, w.cu_draft, w.dtype, seqs=seqs, min_block_len=min_block_len)
     for b in seqs:
         g = int(w.gammas[b])
         t0 = w.target_base(b)
         assert int(res["n_accepted"][b]) == ref[b]["n"], b
         assert list(res["out_tokens"][t0:t0 + g + 1]) == list(ref[b]["tokens"]), b
+        if min_block_len > 0:
+            d0 = w.draft_base(b)
+            assert int(res["block_n"][b]) == ref[b]["block_n"], b
+            assert list(res["block_tokens"][d0:d0 + g]) == list(ref[b]["block_tokens"]), b
 
 
-def run_nkl(w, dev, delta=0.15):
+def run_nkl(w, dev, delta=0.15, positions=None):
     cu = None if w.dense else torch.from_numpy(w.cu_draft).to(dev)
-    res = api.spec_nkl(to_dev(w.target, dev), to_dev(w.draft, dev), w.T, cu_draft=cu,
-                       gamma=w.gamma_max if not w.dense else int(w.gammas[0]), delta=delta)
+    kw = dict(cu_draft=cu, gamma=w.gamma_max if not w.dense else int(w.gammas[0]), delta=delta)
+    if positions is None:
+        res = api.spec_nkl(to_dev(w.target, dev), to_dev(w.draft, dev), w.T, **kw)
+    else:
+        pos = torch.from_numpy(np.asarray(positions, dtype=np.int32)).to(dev)
+        res = api.spec_nkl_ex(to_dev(w.target, dev), to_dev(w.draft, dev), w.T, position=pos, **kw)
     torch.cuda.synchronize()
     return {k: v.cpu().numpy() for k, v in res.items()}
 
 
-def compare_nkl(w, res, seqs, delta=0.15):
-    ref = O.nkl_rows(w.target, w.draft, w.cu_draft, w.T, w.dtype, delta=delta, seqs=seqs)
+def compare_nkl(w, res, seqs, delta=0.15, positions=None):
+    ref = O.nkl_rows(w.target, w.draft, w.cu_draft, w.T, w.dtype, delta=delta, seqs=seqs, positions=positions)
     for b in seqs:
         g = int(w.gammas[b])
         d0 = w.draft_base(b)
         got = res["nkl"][d0:d0 + g].astype(np.float64)
         assert np.allclose(got, ref[b]["nkl"], rtol=REL, atol=NKL_ABS, equal_nan=True), (b, got, ref[b]["nkl"])
         m = res["nkl_mask"][d0:d0 + g]
-        near = np.abs(ref[b]["nkl"] - delta) <= REL * delta + NKL_ABS
-        assert np.all((m == ref[b]["mask"]) | near)
+        thr = np.array([delta if positions is None or positions[b] < 1 else
+                        O.position_delta(int(positions[b]) + i, delta) for i in range(g)])
+        near = np.abs(ref[b]["nkl"] - thr) <= REL * thr + NKL_ABS
+        assert np.all((m == ref[b]["mask"]) | near), (b, m, ref[b]["mask"])
 
 
 def run_tree(w, dev):

@@ -89,3 +89,71 @@ def test_host_validation_without_launch(lib):
     bad_parent = (ctypes.c_int32 * 2)(-1, 5)
     assert lib.spec_verify_tree(2, 2, 100, _lib.SPEC_BF16, one, one, ctypes.cast(bad_parent, P), one, one, one,
                                 one, one, 1 << 30, None) == _lib.SPEC_ERR_INVALID_ARG
+
+
+def test_option_checks_without_launch(lib):
+    """Options are checked before anything is launched: a bad draft temperature, block-accept
+    without its outputs, a non-finite threshold parameter, a bad summary window."""
+    P = ctypes.c_void_p
+    one = P(256)
+    g = _g(4, 3, 1000)
+
+    def stoch(opts, T=0.6):
+        return lib.spec_verify_stochastic_ex(g, _lib.SPEC_BF16, one, one, one, T, one, one, one, one, None, None,
+                                             None, None, None, 0.15, None, None, ctypes.byref(opts), one, None,
+                                             1 << 30, None)
+
+    def greedy(opts):
+        return lib.spec_verify_greedy_ex(g, _lib.SPEC_BF16, one, one, one, one, ctypes.byref(opts), one, None,
+                                         1 << 30, None)
+
+    o = _lib.SpecOptions()
+    o.temperature_draft = -0.5
+    assert stoch(o) == _lib.SPEC_ERR_INVALID_ARG
+    o.temperature_draft = float("inf")
+    assert stoch(o) == _lib.SPEC_ERR_INVALID_ARG
+    o = _lib.SpecOptions()
+    o.min_block_len = 3
+    assert stoch(o) == _lib.SPEC_ERR_INVALID_ARG           # block_n / block_tokens missing
+    assert greedy(o) == _lib.SPEC_ERR_INVALID_ARG
+    o.min_block_len = -1
+    assert greedy(o) == _lib.SPEC_ERR_INVALID_ARG
+    o = _lib.SpecOptions()
+    o.position = 256
+    o.delta_alpha = float("nan")
+    assert stoch(o) == _lib.SPEC_ERR_INVALID_ARG
+    assert lib.spec_nkl_ex(g, _lib.SPEC_BF16, one, one, 0.6, 0.15, one, None, ctypes.byref(o), one, None, 1 << 30,
+                           None) == _lib.SPEC_ERR_INVALID_ARG
+    assert greedy(o) == _lib.SPEC_ERR_WORKSPACE            # greedy ignores the position fields
+    assert lib.spec_accept_summary(one, 5, 0, one, None) == _lib.SPEC_ERR_INVALID_ARG
+    assert lib.spec_accept_summary(one, 5, _lib.SPEC_STATS_SLOTS + 1, one, None) == _lib.SPEC_ERR_INVALID_ARG
+    assert lib.spec_accept_summary(None, 5, 4, one, None) == _lib.SPEC_ERR_INVALID_ARG
+
+
+def test_option_structs_match_the_header(tmp_path):
+    """The ctypes mirrors of spec_options and spec_accept_stats have the C layout (sizes and
+    offsets printed by a program compiled against the header)."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "layout.c"
+    src.write_text('''#include <stdio.h>
+#include <stddef.h>
+#include "spec_verify.h"
+int main(void) {
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\\n", sizeof(spec_options), sizeof(spec_accept_stats),
+         offsetof(spec_options, position), offsetof(spec_options, delta_alpha), offsetof(spec_options, min_block_len),
+         offsetof(spec_options, block_n), offsetof(spec_options, block_tokens), offsetof(spec_options, stats),
+         offsetof(spec_options, stats_bucket), sizeof(spec_stats_slot), offsetof(spec_stats_slot, rate2_fx));
+  return 0;
+}
+''')
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", build.INCLUDE, "-o", str(exe), str(src)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()]
+    O, S = _lib.SpecOptions, _lib.SpecStatsSlot
+    want = [ctypes.sizeof(O), _lib.STATS_BYTES, O.position.offset, O.delta_alpha.offset, O.min_block_len.offset,
+            O.block_n.offset, O.block_tokens.offset, O.stats.offset, O.stats_bucket.offset, ctypes.sizeof(S),
+            S.rate2_fx.offset]
+    assert got == want

@@ -488,6 +488,8 @@ def test_position_mask_follows_the_printed_thresholds():
     assert lo["mask"][0] == 0 and hi["mask"][0] == 1
     rows = O.nkl_rows(np.stack([zt, zt]), zd[None], np.array([0, 1]), 1.0, "f32", 0.15, positions=np.array([1024]))
     assert rows[0]["mask"][0] == 1
+    bad = O.verify_stochastic_sequence(t, d, np.array([0]), 1.0, np.zeros(1), 0.5, 0.15, position=0)
+    assert bad["mask"][0] == 0 and bad["nkl"][0] == pytest.approx(0.2, abs=1e-12)
 
 
 # ---------------------------------------------------------------- block-accept (R20)
