@@ -341,6 +341,35 @@ def run_ours(args):
         nfn = lambda: api.spec_nkl(call.t, call.d, w.T, gamma=8, out=n_out)  # noqa: E731
         t_n = time_mode(nfn, 200, 10, dev)
         modes["nkl_B256_g8_V128256"] = {"us_per_call": t_n * 1e6, "GBps": ab["nkl"] / t_n / 1e9}
+        # policy variants (spec_options) on the same inputs
+        st = api.new_accept_stats(dev)
+        pos = torch.arange(1, w.B + 1, dtype=torch.int32, device=dev) * 37
+        gam = int(w.gammas[0])
+        x_out = {}
+        xfn = lambda: api.spec_verify_stochastic_ex(call.t, call.d, call.tok, w.T, call.ua, call.us,  # noqa: E731
+                                                    gamma=gam, out=x_out, temperature_draft=0.4)
+        t_x = time_mode(xfn, 200, 10, dev)
+        modes["stochastic_draft_T0.4_B256_g8_V128256"] = {
+            "us_per_call": t_x * 1e6, "GBps": ab["stochastic"] / t_x / 1e9,
+            "frac_of_peak": ab["stochastic"] / t_x / 1e9 / hbm,
+            "note": "target T 0.6, drafts at T_d 0.4: the draft rows are summed at both temperatures"}
+        a_out = {}
+        afn = lambda: api.spec_verify_stochastic_ex(call.t, call.d, call.tok, w.T, call.ua, call.us,  # noqa: E731
+                                                    gamma=gam, out=a_out, position=pos, min_block_len=3,
+                                                    stats=st, stats_bucket=1)
+        t_a = time_mode(afn, 200, 10, dev)
+        modes["stochastic_position_block_stats_B256_g8_V128256"] = {
+            "us_per_call": t_a * 1e6, "GBps": ab["stochastic"] / t_a / 1e9,
+            "frac_of_peak": ab["stochastic"] / t_a / 1e9 / hbm}
+        gp_out = {}
+        gpfn = lambda: api.spec_verify_greedy_ex(call.t, call.tok, gamma=gam, out=gp_out,  # noqa: E731
+                                                 min_block_len=3, stats=st, stats_bucket=2)
+        t_gp = time_mode(gpfn, 200, 10, dev)
+        modes["greedy_block_stats_B256_g8_V128256"] = {"us_per_call": t_gp * 1e6, "GBps": ab["greedy"] / t_gp / 1e9}
+        sm_out = torch.empty(6, dtype=torch.float64, device=dev)
+        t_sm = time_mode(lambda: api.spec_accept_summary(st, 2, 64, out=sm_out), 200, 10, dev)
+        modes["accept_summary_64_slots"] = {"us_per_call": t_sm * 1e6,
+                                            "note": "one 64-thread block; the figure includes the host's enqueue rate"}
         del res
         tw = synth.CONFIGS[3].make()
         tt = _to_dev(tw.target, dev)

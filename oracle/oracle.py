@@ -85,6 +85,19 @@ Readings taken where the pages are silent, garbled or disagree:
       window. The window is the caller's last W time buckets (a bucket is any
       monotone label the caller chooses, e.g. whole seconds).
 
+  R22 multi-draft ([MTP] 6.2: several drafters each propose a draft, the target
+      verifies all of them and the longest accepted path is kept; [CoD] 4.4: the
+      pairwise NKL matrix of the drafts, consensus below 0.1, divergence above 0.15;
+      the page's comparison operators are lost): a group holds K candidate
+      sequences verified independently (greedy or stochastic); the kept candidate is
+      the one with the most accepted drafts, the lowest index among equals (with
+      stochastic verification this choice is not distribution-preserving; the page
+      asks for it as stated). At draft position i the matrix is
+      M[a][b] = KL(q_a || q_b) / ln V between the candidates' draft rows i at the one
+      temperature T. Consensus at i: some pair a != b is below the consensus
+      threshold in both directions; divergence at i: every entry off the diagonal is
+      above the divergence threshold.
+
 Parity pins for every function: tests/test_oracle_pins.py.
 """
 from __future__ import annotations
@@ -481,3 +494,57 @@ def acceptance_summary(records, bucket_now: int, window: int) -> dict:
     var = sum((r - mean) ** 2 for r in rates) / R
     return {"rounds": R, "accepted": acc, "drafted": drafted, "mean_accepted": acc / R, "mean_rate": mean,
             "arsd": math.sqrt(var)}
+
+
+# ---------------------------------------------------------------------------
+# multi-draft verification (R22)
+
+def pairwise_nkl(d_rows: np.ndarray, T: float) -> np.ndarray:
+    """M[a][b] = KL(q_a || q_b) / ln V for the K draft rows d_rows [K, V] at temperature T
+    (q_k = softmax(d_rows[k] / T)); zero diagonal."""
+    K = d_rows.shape[0]
+    M = np.zeros((K, K))
+    for a in range(K):
+        for b in range(K):
+            if a != b:
+                M[a, b] = nkl_pair(d_rows[b], d_rows[a], T)[0]    # nkl_pair(target=p, draft=q)
+    return M
+
+
+def consensus_divergence(M: np.ndarray, c_thr: float = 0.1, d_thr: float = 0.15):
+    K = M.shape[0]
+    off = [(a, b) for a in range(K) for b in range(K) if a != b]
+    cons = any(M[a, b] < c_thr and M[b, a] < c_thr for a, b in off)
+    div = all(M[a, b] > d_thr for a, b in off)
+    return cons, div
+
+
+def verify_multi(target_raw, draft_raw, tokens, G: int, K: int, gamma: int, T: float, dtype, stochastic: bool,
+                 u_accept=None, u_sample=None, c_thr=0.1, d_thr=0.15, groups=None) -> dict:
+    """Groups of K candidate sequences (sequence g*K + k, dense gamma drafts each, laid out
+    like verify_stochastic's dense batches). Per group: the candidates' results, the kept
+    candidate (most accepted drafts, lowest index among equals), its tokens, and per draft
+    position the pairwise NKL matrix with the consensus and divergence flags."""
+    groups = range(G) if groups is None else groups
+    res = {}
+    for g in groups:
+        seqs = [g * K + k for k in range(K)]
+        cu = np.arange(G * K + 1, dtype=np.int64) * gamma
+        if stochastic:
+            r = verify_stochastic(target_raw, draft_raw, tokens, cu, T, u_accept, u_sample, dtype, seqs=seqs)
+            cand = [{"n": r[b]["n"], "tokens": r[b]["tokens"], "flag": r[b]["flag"]} for b in seqs]
+        else:
+            r = verify_greedy(target_raw, tokens, cu, dtype, seqs=seqs)
+            cand = [{"n": r[b]["n"], "tokens": r[b]["tokens"], "flag": False} for b in seqs]
+        ns = [c["n"] for c in cand]
+        best = int(np.argmax(ns))                      # first maximal index
+        mats, cons, div = [], [], []
+        for i in range(gamma):
+            rows = np.stack([widen(draft_raw[(g * K + k) * gamma + i], dtype) for k in range(K)])
+            M = pairwise_nkl(rows, T)
+            c, d = consensus_divergence(M, c_thr, d_thr)
+            mats.append(M), cons.append(c), div.append(d)
+        res[g] = {"cand": cand, "best_k": best if ns[best] >= 0 else -1, "best_n": ns[best],
+                  "best_tokens": cand[best]["tokens"], "pair_nkl": np.array(mats).reshape(gamma, K, K),
+                  "consensus": np.array(cons, dtype=np.uint8), "divergence": np.array(div, dtype=np.uint8)}
+    return res

@@ -547,3 +547,60 @@ def test_acceptance_summary_against_numpy():
     assert s["arsd"] == pytest.approx(np.std(rates), rel=1e-9)
     h = O.acceptance_summary([(0, 2, 4), (0, 4, 4), (1, 3, 4)], 0, 1)
     assert h["rounds"] == 2 and h["mean_accepted"] == 3.0 and h["arsd"] == pytest.approx(0.25, abs=1e-15)
+
+
+# ---------------------------------------------------------------- multi-draft (R22)
+
+def test_pairwise_nkl_against_scipy():
+    rng = np.random.default_rng(51)
+    K, V, T = 4, 300, 0.7
+    d = rng.normal(0, 2, (K, V))
+    M = O.pairwise_nkl(d, T)
+    for a in range(K):
+        assert M[a, a] == 0.0
+        for b in range(K):
+            if a != b:
+                want = scipy.stats.entropy(sps.softmax(d[a] / T), sps.softmax(d[b] / T)) / math.log(V)
+                assert M[a, b] == pytest.approx(want, rel=1e-9)
+    assert not np.allclose(M, M.T)                        # KL is not symmetric: both directions kept
+    same = O.pairwise_nkl(np.stack([d[0]] * 3), T)
+    assert np.all(np.abs(same) < 1e-12)
+    assert O.consensus_divergence(same) == (True, False)
+
+
+def test_consensus_and_divergence_flags():
+    M = np.full((3, 3), 0.5)
+    np.fill_diagonal(M, 0.0)
+    assert O.consensus_divergence(M) == (False, True)
+    M[0, 2] = 0.05
+    assert O.consensus_divergence(M) == (False, False)    # one direction alone is not consensus
+    M[2, 0] = 0.09
+    assert O.consensus_divergence(M) == (True, False)
+    M = np.full((2, 2), 0.15)
+    np.fill_diagonal(M, 0.0)
+    assert O.consensus_divergence(M) == (False, False)    # 0.15 is not above 0.15
+    M[0, 1] = M[1, 0] = 0.1
+    assert O.consensus_divergence(M)[0] is False          # 0.1 is not below 0.1
+
+
+def test_multi_draft_keeps_the_longest_accepted_candidate():
+    """Greedy groups of K = 3 candidates with known argmax rows: accepted counts 0, 2, 2
+    -> candidate 1 (the lower index of the tie) and its tokens."""
+    V, g, K = 5, 3, 3
+    rows_t, rows_d, toks = [], [], []
+    am = [1, 2, 3, 4]
+    for k, n in enumerate([0, 2, 2]):
+        t = np.zeros((g + 1, V))
+        for i in range(g + 1):
+            t[i, am[i]] = 5.0
+        rows_t.append(t)
+        rows_d.append(np.zeros((g, V)) + k)
+        toks.append([am[i] if i < n else (am[i] + 1) % V for i in range(g)])
+    target = np.concatenate(rows_t).astype(np.float32)
+    draft = np.concatenate(rows_d).astype(np.float32)
+    tokens = np.array(toks, dtype=np.int64).reshape(-1)
+    r = O.verify_multi(target, draft, tokens, 1, K, g, 1.0, "f32", stochastic=False)[0]
+    assert [c["n"] for c in r["cand"]] == [0, 2, 2]
+    assert r["best_k"] == 1 and r["best_n"] == 2
+    assert list(r["best_tokens"]) == [1, 2, 3, -1]       # the target argmax replaces the mismatch
+    assert np.all(r["pair_nkl"] == 0.0) and np.all(r["consensus"] == 1)   # constant draft rows: identical q
