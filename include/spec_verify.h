@@ -262,6 +262,52 @@ spec_status spec_accept_summary(const spec_accept_stats* stats, int64_t bucket_n
                                 spec_stream_t stream);
 
 /*
+ * Multi-draft verification ([MTP] 6.2: several drafters each propose a draft, the target
+ * verifies all of them and the longest accepted path is kept; [CoD] 4.4: the pairwise NKL
+ * matrix of the drafts, consensus below 0.1 and divergence above 0.15).
+ *
+ * G groups of K candidate sequences, each with gamma drafts, laid out as a dense batch of
+ * G*K sequences (candidate k of group g is sequence g*K + k): target_logits
+ * [G*K*(gamma+1), V], draft_logits [G*K*gamma, V], draft_tokens [G*K*gamma]. Every
+ * candidate is verified as by spec_verify_stochastic (stochastic != 0; u_accept
+ * [G*K*gamma], u_sample [G*K]) or spec_verify_greedy (stochastic == 0; the uniforms
+ * are not read). Outputs:
+ *   n_accepted [G*K], out_tokens [G*K*(gamma+1)]   every candidate's result
+ *   best_k [G], best_n [G], best_tokens [G*(gamma+1)]  the kept candidate: the most
+ *                                      accepted drafts, the lowest k among equals (-1
+ *                                      when every candidate of the group had a data
+ *                                      error). With stochastic verification this choice
+ *                                      does not preserve the target distribution.
+ *   pair_nkl [G*gamma*K*K]             optional: at draft position i of group g,
+ *                                      M[a][b] = KL(q_a || q_b) / ln V between the
+ *                                      candidates' draft rows i, q = softmax(row / T);
+ *                                      zero diagonal; NaN for a non-finite row
+ *   consensus, divergence [G*gamma]    optional: some pair a != b below consensus_nkl in
+ *                                      both directions; every entry off the diagonal
+ *                                      above divergence_nkl
+ * 2 <= K <= SPEC_MAX_CANDIDATES. The draft rows are read twice (once by the verification,
+ * once for the matrix).
+ */
+#define SPEC_MAX_CANDIDATES 4
+
+typedef struct {
+  int32_t G;     /* groups, >= 0 */
+  int32_t K;     /* candidates per group, 2..SPEC_MAX_CANDIDATES */
+  int32_t gamma; /* drafts per candidate, 0..SPEC_MAX_GAMMA */
+  int32_t V;     /* vocabulary size, >= 1 */
+} spec_multi_batch;
+
+size_t spec_multi_workspace_bytes(spec_multi_batch m, spec_dtype dtype, int32_t stochastic);
+
+spec_status spec_verify_multi(spec_multi_batch m, spec_dtype dtype, int32_t stochastic, const void* target_logits,
+                              const void* draft_logits, const int32_t* draft_tokens, float temperature,
+                              const float* u_accept, const float* u_sample, float consensus_nkl,
+                              float divergence_nkl, int32_t* n_accepted, int32_t* out_tokens, int32_t* best_k,
+                              int32_t* best_n, int32_t* best_tokens, float* pair_nkl, uint8_t* consensus,
+                              uint8_t* divergence, uint32_t* device_status, void* workspace,
+                              size_t workspace_bytes, spec_stream_t stream);
+
+/*
  * spec_verify_stochastic without a workspace argument: the same computation, inputs and
  * outputs, with its scratch memory inside the library. The pages have no counterpart to
  * this entry point; it exists for callers that cannot allocate device memory -- code that

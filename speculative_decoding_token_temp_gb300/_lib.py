@@ -34,11 +34,16 @@ SPEC_MODE_NKL = 2
 SPEC_MAX_GAMMA = 128
 SPEC_MAX_TREE_NODES = 64
 SPEC_STATS_SLOTS = 64
+SPEC_MAX_CANDIDATES = 4
 
 
 class SpecBatch(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("gamma", ctypes.c_int32), ("V", ctypes.c_int32),
                 ("total_draft", ctypes.c_int32), ("cu_draft", ctypes.c_void_p)]
+
+
+class SpecMultiBatch(ctypes.Structure):
+    _fields_ = [("G", ctypes.c_int32), ("K", ctypes.c_int32), ("gamma", ctypes.c_int32), ("V", ctypes.c_int32)]
 
 
 class SpecStatsSlot(ctypes.Structure):
@@ -80,6 +85,9 @@ SIGNATURES = {
     "spec_nkl_ex": (ctypes.c_int, [SpecBatch, ctypes.c_int, _P, _P, _F, _F, _P, _P, ctypes.POINTER(SpecOptions),
                                    _P, _P, _S, _P]),
     "spec_accept_summary": (ctypes.c_int, [_P, ctypes.c_int64, _I, _P, _P]),
+    "spec_multi_workspace_bytes": (_S, [SpecMultiBatch, ctypes.c_int, _I]),
+    "spec_verify_multi": (ctypes.c_int, [SpecMultiBatch, ctypes.c_int, _I, _P, _P, _P, _F, _P, _P, _F, _F, _P, _P,
+                                         _P, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
     "spec_status_str": (ctypes.c_char_p, [ctypes.c_int]),
 }
 

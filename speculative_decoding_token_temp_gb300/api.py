@@ -345,3 +345,65 @@ def spec_accept_summary(stats: torch.Tensor, bucket_now: int, window: int, out: 
     check("spec_accept_summary", _lib.lib().spec_accept_summary(_ptr(stats), int(bucket_now), int(window),
                                                                 _ptr(out), _stream(dev)))
     return out
+
+
+# ---------------------------------------------------------------------------
+# multi-draft verification
+
+def spec_multi_workspace_bytes(G: int, K: int, gamma: int, V: int, dtype: int = _lib.SPEC_BF16,
+                               stochastic: bool = True) -> int:
+    return int(_lib.lib().spec_multi_workspace_bytes(_lib.SpecMultiBatch(G, K, gamma, V), dtype, int(stochastic)))
+
+
+def spec_verify_multi(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torch.Tensor, K: int,
+                      temperature: float, *, stochastic: bool = True, u_accept: torch.Tensor | None = None,
+                      u_sample: torch.Tensor | None = None, consensus_nkl: float = 0.1, divergence_nkl: float = 0.15,
+                      want_matrix: bool = True, out: dict | None = None, workspace=None,
+                      device_status=None) -> dict:
+    """G groups of K candidates (candidate k of group g is sequence g*K + k of a dense batch):
+    target [G*K*(gamma+1), V], draft [G*K*gamma, V], draft_tokens [G*K*gamma] int32. Returns
+    n_accepted [G*K], out_tokens [G*K*(gamma+1)], best_k / best_n [G], best_tokens
+    [G*(gamma+1)] and, with want_matrix, pair_nkl [G*gamma*K*K], consensus / divergence
+    [G*gamma]."""
+    dt = _dtype_code(target)
+    dev = target.device
+    V = target.shape[-1]
+    seqs = draft_tokens.numel()
+    rows = target.numel() // V
+    if K < 2 or (rows - seqs) % K:
+        raise ValueError("target rows must be G*K*(gamma+1)")
+    G = (rows - seqs) // K
+    gamma = seqs // (G * K) if G else 0
+    _need(target, "target", target.dtype, G * K * (gamma + 1) * V, dev)
+    if gamma:
+        _need(draft, "draft", target.dtype, G * K * gamma * V, dev)
+    _need(draft_tokens, "draft_tokens", torch.int32, G * K * gamma, dev)
+    if stochastic:
+        _need(u_sample, "u_sample", torch.float32, G * K, dev)
+        _need(u_accept, "u_accept", torch.float32, G * K * gamma, dev)
+    o = {} if out is None else out
+    i32 = lambda n: torch.empty(n, dtype=torch.int32, device=dev)  # noqa: E731
+    n_acc = o.setdefault("n_accepted", i32(G * K))
+    out_tok = o.setdefault("out_tokens", i32(G * K * (gamma + 1)))
+    bk, bn = o.setdefault("best_k", i32(G)), o.setdefault("best_n", i32(G))
+    bt = o.setdefault("best_tokens", i32(G * (gamma + 1)))
+    pn = cons = div = None
+    if want_matrix:
+        pn = o.setdefault("pair_nkl", torch.empty(G * gamma * K * K, dtype=torch.float32, device=dev))
+        cons = o.setdefault("consensus", torch.empty(G * gamma, dtype=torch.uint8, device=dev))
+        div = o.setdefault("divergence", torch.empty(G * gamma, dtype=torch.uint8, device=dev))
+    if device_status is None:
+        device_status = o.get("device_status")
+        if device_status is None:
+            device_status = torch.zeros(1, dtype=torch.int32, device=dev)
+    o["device_status"] = device_status
+    mb = _lib.SpecMultiBatch(G, K, gamma, V)
+    nbytes = int(_lib.lib().spec_multi_workspace_bytes(mb, dt, int(stochastic)))
+    ws = _workspace(workspace, nbytes, dev)
+    code = _lib.lib().spec_verify_multi(
+        mb, dt, int(stochastic), _ptr(target), _ptr(draft) if gamma else None, _ptr(draft_tokens),
+        float(temperature), _ptr(u_accept) if stochastic else None, _ptr(u_sample) if stochastic else None,
+        float(consensus_nkl), float(divergence_nkl), _ptr(n_acc), _ptr(out_tok), _ptr(bk), _ptr(bn), _ptr(bt),
+        _ptr(pn), _ptr(cons), _ptr(div), _ptr(device_status), _ptr(ws), ws.numel(), _stream(dev))
+    check("spec_verify_multi", code)
+    return o

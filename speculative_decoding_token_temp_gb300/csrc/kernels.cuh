@@ -136,6 +136,8 @@ struct ProParams {
   uint32_t* status;
   spec_stats_slot* stats;  // the slot of this call's bucket, or null
   long long bucket;
+  unsigned* zero2;  // further tickets to zero (multi-draft matrix), or null
+  int nzero2;
 };
 
 // ---------------------------------------------------------------------------

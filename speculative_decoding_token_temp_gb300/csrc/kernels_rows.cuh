@@ -13,6 +13,7 @@ __global__ void prologue_kernel(const __grid_constant__ ProParams p) {
   griddep_launch();
   griddep_wait();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < p.nzero2) p.zero2[b] = 0u;
   if (b == 0) {
     p.cntA[p.B] = 0u;
     if (p.stats != nullptr && p.stats->bucket != p.bucket) {

@@ -7,6 +7,7 @@
 
 #include "kernels.cuh"
 #include "kernels_rows.cuh"
+#include "kernels_multi.cuh"
 #include "kernels_sample.cuh"
 #include "spec_verify.h"
 
@@ -128,8 +129,14 @@ int stats_slot(int64_t bucket) {
   return (int)(m < 0 ? m + SPEC_STATS_SLOTS : m);
 }
 
+// Extra tickets the prologue of a call zeroes (the multi-draft matrix's).
+struct ZeroRegion {
+  unsigned* ptr = nullptr;
+  int n = 0;
+};
+
 cudaError_t launch_prologue(const spec_batch& g, const Layout& L, char* ws, uint32_t* status, cudaStream_t stream,
-                            const spec_options* opt = nullptr) {
+                            const spec_options* opt = nullptr, ZeroRegion z = ZeroRegion()) {
   ProParams pp;
   pp.cu = g.cu_draft;
   pp.B = g.B;
@@ -141,7 +148,10 @@ cudaError_t launch_prologue(const spec_batch& g, const Layout& L, char* ws, uint
   pp.status = status;
   pp.stats = (opt && opt->stats) ? &opt->stats->slot[stats_slot(opt->stats_bucket)] : nullptr;
   pp.bucket = opt ? (long long)opt->stats_bucket : 0;
-  return launch(prologue_kernel, dim3((unsigned)ceil_div(g.B, kThreads)), dim3(kThreads), stream, pp, true);
+  pp.zero2 = z.ptr;
+  pp.nzero2 = z.n;
+  const int threads = g.B > z.n ? g.B : z.n;
+  return launch(prologue_kernel, dim3((unsigned)ceil_div(threads, kThreads)), dim3(kThreads), stream, pp, true);
 }
 
 // The vector path of rows_kernel stages its loads in kRowsSmem bytes of dynamic shared
@@ -287,56 +297,12 @@ void apply_options(RowsParams& rp, const spec_options* o, spec_mode mode) {
   }
 }
 
-}  // namespace
-}  // namespace sv
-
-using namespace sv;
-
-extern "C" {
-
-size_t spec_workspace_bytes(spec_batch g, spec_dtype dtype, spec_mode mode) {
-  if (check_batch(g) != SPEC_OK || (dtype != SPEC_F32 && dtype != SPEC_BF16)) return 0;
-  return layout(g.B, g.V, rows_for(mode, g), mode == SPEC_MODE_STOCHASTIC, mode == SPEC_MODE_GREEDY, dtype).total;
-}
-
-size_t spec_tree_workspace_bytes(int32_t B, int32_t N, int32_t V) {
-  if (B < 0 || N < 1 || N > SPEC_MAX_TREE_NODES || V < 1) return 0;
-  return layout(B, V, (long long)B * (N + 1), false, true).total;
-}
-
-int32_t spec_tree_depth(const int32_t* parent, int32_t N) {
-  if (parent == nullptr || N < 1 || N > SPEC_MAX_TREE_NODES) return -1;
-  int depth[SPEC_MAX_TREE_NODES];
-  int D = 0;
-  for (int j = 0; j < N; ++j) {
-    const int pj = parent[j];
-    if (pj < -1 || pj >= j) return -1;
-    depth[j] = pj < 0 ? 1 : depth[pj] + 1;
-    if (depth[j] > D) D = depth[j];
-  }
-  return D;
-}
-
-spec_status spec_verify_stochastic(spec_batch g, spec_dtype dtype, const void* target_logits,
-                                   const void* draft_logits, const int32_t* draft_tokens, float temperature,
-                                   const float* u_accept, const float* u_sample, int32_t* n_accepted,
-                                   int32_t* out_tokens, float* p_x, float* q_x, float* alpha, float* nkl,
-                                   uint8_t* nkl_mask, float nkl_delta, int32_t* greedy_n, int32_t* greedy_tokens,
-                                   uint32_t* device_status, void* workspace, size_t workspace_bytes,
-                                   spec_stream_t stream) {
-  return spec_verify_stochastic_ex(g, dtype, target_logits, draft_logits, draft_tokens, temperature, u_accept,
-                                   u_sample, n_accepted, out_tokens, p_x, q_x, alpha, nkl, nkl_mask, nkl_delta,
-                                   greedy_n, greedy_tokens, nullptr, device_status, workspace, workspace_bytes,
-                                   stream);
-}
-
-spec_status spec_verify_stochastic_ex(spec_batch g, spec_dtype dtype, const void* target_logits,
-                                      const void* draft_logits, const int32_t* draft_tokens, float temperature,
-                                      const float* u_accept, const float* u_sample, int32_t* n_accepted,
-                                      int32_t* out_tokens, float* p_x, float* q_x, float* alpha, float* nkl,
-                                      uint8_t* nkl_mask, float nkl_delta, int32_t* greedy_n,
-                                      int32_t* greedy_tokens, const spec_options* options, uint32_t* device_status,
-                                      void* workspace, size_t workspace_bytes, spec_stream_t stream_) {
+spec_status stochastic_impl(spec_batch g, spec_dtype dtype, const void* target_logits, const void* draft_logits,
+                            const int32_t* draft_tokens, float temperature, const float* u_accept,
+                            const float* u_sample, int32_t* n_accepted, int32_t* out_tokens, float* p_x, float* q_x,
+                            float* alpha, float* nkl, uint8_t* nkl_mask, float nkl_delta, int32_t* greedy_n,
+                            int32_t* greedy_tokens, const spec_options* options, uint32_t* device_status,
+                            void* workspace, size_t workspace_bytes, spec_stream_t stream_, ZeroRegion zr) {
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
   spec_status st = check_batch(g);
   if (st != SPEC_OK) return st;
@@ -354,7 +320,7 @@ spec_status spec_verify_stochastic_ex(spec_batch g, spec_dtype dtype, const void
   const bool bf16 = dtype == SPEC_BF16;
   const bool vec = vec_path(dtype, g.V, target_logits, draft_logits);
 
-  if (launch_prologue(g, L, ws, device_status, stream, options) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (launch_prologue(g, L, ws, device_status, stream, options, zr) != cudaSuccess) return SPEC_ERR_CUDA;
   RowsParams rp = base_params(g, L, ws, device_status);
   rp.target = target_logits;
   rp.draft = draft_logits;
@@ -430,18 +396,10 @@ spec_status spec_verify_stochastic_ex(spec_batch g, spec_dtype dtype, const void
   return SPEC_OK;
 }
 
-spec_status spec_verify_greedy(spec_batch g, spec_dtype dtype, const void* target_logits,
-                               const int32_t* draft_tokens, int32_t* n_accepted, int32_t* out_tokens,
-                               uint32_t* device_status, void* workspace, size_t workspace_bytes,
-                               spec_stream_t stream) {
-  return spec_verify_greedy_ex(g, dtype, target_logits, draft_tokens, n_accepted, out_tokens, nullptr,
-                               device_status, workspace, workspace_bytes, stream);
-}
-
-spec_status spec_verify_greedy_ex(spec_batch g, spec_dtype dtype, const void* target_logits,
-                                  const int32_t* draft_tokens, int32_t* n_accepted, int32_t* out_tokens,
-                                  const spec_options* options, uint32_t* device_status, void* workspace,
-                                  size_t workspace_bytes, spec_stream_t stream_) {
+spec_status greedy_impl(spec_batch g, spec_dtype dtype, const void* target_logits, const int32_t* draft_tokens,
+                        int32_t* n_accepted, int32_t* out_tokens, const spec_options* options,
+                        uint32_t* device_status, void* workspace, size_t workspace_bytes, spec_stream_t stream_,
+                        ZeroRegion zr) {
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
   spec_status st = check_batch(g);
   if (st != SPEC_OK) return st;
@@ -454,7 +412,7 @@ spec_status spec_verify_greedy_ex(spec_batch g, spec_dtype dtype, const void* ta
   if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u)) return SPEC_ERR_WORKSPACE;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   char* ws = static_cast<char*>(workspace);
-  if (launch_prologue(g, L, ws, device_status, stream, options) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (launch_prologue(g, L, ws, device_status, stream, options, zr) != cudaSuccess) return SPEC_ERR_CUDA;
   RowsParams rp = base_params(g, L, ws, device_status);
   rp.target = target_logits;
   rp.tokens = draft_tokens;
@@ -466,6 +424,130 @@ spec_status spec_verify_greedy_ex(spec_batch g, spec_dtype dtype, const void* ta
                             L.rows * L.nchunks, stream) != cudaSuccess)
     return SPEC_ERR_CUDA;
   return SPEC_OK;
+}
+
+// ---------------------------------------------------------------------------
+// multi-draft verification: the candidates' verification workspace, then the matrix's
+// tickets and partials
+
+struct MultiLayout {
+  size_t verify, tickets, part, total;
+  int nchunks, chunk_elems;
+};
+
+spec_batch multi_as_batch(const spec_multi_batch& m) {
+  spec_batch g;
+  g.B = m.G * m.K;
+  g.gamma = m.gamma;
+  g.V = m.V;
+  g.total_draft = m.G * m.K * m.gamma;
+  g.cu_draft = nullptr;
+  return g;
+}
+
+spec_status check_multi(const spec_multi_batch& m) {
+  if (m.G < 0 || m.K < 2 || m.K > SPEC_MAX_CANDIDATES || m.gamma < 0 || m.gamma > SPEC_MAX_GAMMA || m.V < 1)
+    return SPEC_ERR_INVALID_ARG;
+  if ((long long)m.G * m.K * (m.gamma + 1) > (1LL << 30)) return SPEC_ERR_INVALID_ARG;
+  return check_batch(multi_as_batch(m));
+}
+
+MultiLayout multi_layout(const spec_multi_batch& m, spec_dtype dt, bool stochastic) {
+  const spec_batch g = multi_as_batch(m);
+  const spec_mode mode = stochastic ? SPEC_MODE_STOCHASTIC : SPEC_MODE_GREEDY;
+  MultiLayout M;
+  M.verify = align256(layout(g.B, g.V, rows_for(mode, g), stochastic, !stochastic, dt).total);
+  const long long rows = (long long)m.G * m.gamma;
+  // a tile reads K rows of one chunk: about 64 K elements in all
+  chunking(m.V, rows > 0 ? rows : 1, 65536 / (m.K > 0 ? m.K : 1), &M.nchunks, &M.chunk_elems);
+  M.tickets = M.verify;
+  M.part = align256(M.tickets + sizeof(unsigned) * (size_t)rows);
+  M.total = align256(M.part + sizeof(PairPartial) * (size_t)rows * M.nchunks);
+  return M;
+}
+
+template <typename E, int VEC>
+cudaError_t launch_pair_t(int K, const PairParams& pp, long long tiles, cudaStream_t stream) {
+  const dim3 grid((unsigned)tiles), block(kThreads);
+  if (K == 2) return launch(pair_kernel<E, VEC, 2>, grid, block, stream, pp, true);
+  if (K == 3) return launch(pair_kernel<E, VEC, 3>, grid, block, stream, pp, true);
+  return launch(pair_kernel<E, VEC, 4>, grid, block, stream, pp, true);
+}
+
+cudaError_t launch_pair(bool bf16, bool vec, int K, const PairParams& pp, long long tiles, cudaStream_t stream) {
+  if (bf16) return vec ? launch_pair_t<uint16_t, 8>(K, pp, tiles, stream) : launch_pair_t<uint16_t, 1>(K, pp, tiles, stream);
+  return vec ? launch_pair_t<float, 4>(K, pp, tiles, stream) : launch_pair_t<float, 1>(K, pp, tiles, stream);
+}
+
+}  // namespace
+}  // namespace sv
+
+using namespace sv;
+
+extern "C" {
+
+size_t spec_workspace_bytes(spec_batch g, spec_dtype dtype, spec_mode mode) {
+  if (check_batch(g) != SPEC_OK || (dtype != SPEC_F32 && dtype != SPEC_BF16)) return 0;
+  return layout(g.B, g.V, rows_for(mode, g), mode == SPEC_MODE_STOCHASTIC, mode == SPEC_MODE_GREEDY, dtype).total;
+}
+
+size_t spec_tree_workspace_bytes(int32_t B, int32_t N, int32_t V) {
+  if (B < 0 || N < 1 || N > SPEC_MAX_TREE_NODES || V < 1) return 0;
+  return layout(B, V, (long long)B * (N + 1), false, true).total;
+}
+
+int32_t spec_tree_depth(const int32_t* parent, int32_t N) {
+  if (parent == nullptr || N < 1 || N > SPEC_MAX_TREE_NODES) return -1;
+  int depth[SPEC_MAX_TREE_NODES];
+  int D = 0;
+  for (int j = 0; j < N; ++j) {
+    const int pj = parent[j];
+    if (pj < -1 || pj >= j) return -1;
+    depth[j] = pj < 0 ? 1 : depth[pj] + 1;
+    if (depth[j] > D) D = depth[j];
+  }
+  return D;
+}
+
+spec_status spec_verify_stochastic(spec_batch g, spec_dtype dtype, const void* target_logits,
+                                   const void* draft_logits, const int32_t* draft_tokens, float temperature,
+                                   const float* u_accept, const float* u_sample, int32_t* n_accepted,
+                                   int32_t* out_tokens, float* p_x, float* q_x, float* alpha, float* nkl,
+                                   uint8_t* nkl_mask, float nkl_delta, int32_t* greedy_n, int32_t* greedy_tokens,
+                                   uint32_t* device_status, void* workspace, size_t workspace_bytes,
+                                   spec_stream_t stream) {
+  return spec_verify_stochastic_ex(g, dtype, target_logits, draft_logits, draft_tokens, temperature, u_accept,
+                                   u_sample, n_accepted, out_tokens, p_x, q_x, alpha, nkl, nkl_mask, nkl_delta,
+                                   greedy_n, greedy_tokens, nullptr, device_status, workspace, workspace_bytes,
+                                   stream);
+}
+
+spec_status spec_verify_stochastic_ex(spec_batch g, spec_dtype dtype, const void* target_logits,
+                                      const void* draft_logits, const int32_t* draft_tokens, float temperature,
+                                      const float* u_accept, const float* u_sample, int32_t* n_accepted,
+                                      int32_t* out_tokens, float* p_x, float* q_x, float* alpha, float* nkl,
+                                      uint8_t* nkl_mask, float nkl_delta, int32_t* greedy_n,
+                                      int32_t* greedy_tokens, const spec_options* options, uint32_t* device_status,
+                                      void* workspace, size_t workspace_bytes, spec_stream_t stream) {
+  return stochastic_impl(g, dtype, target_logits, draft_logits, draft_tokens, temperature, u_accept, u_sample,
+                         n_accepted, out_tokens, p_x, q_x, alpha, nkl, nkl_mask, nkl_delta, greedy_n, greedy_tokens,
+                         options, device_status, workspace, workspace_bytes, stream, ZeroRegion());
+}
+
+spec_status spec_verify_greedy(spec_batch g, spec_dtype dtype, const void* target_logits,
+                               const int32_t* draft_tokens, int32_t* n_accepted, int32_t* out_tokens,
+                               uint32_t* device_status, void* workspace, size_t workspace_bytes,
+                               spec_stream_t stream) {
+  return spec_verify_greedy_ex(g, dtype, target_logits, draft_tokens, n_accepted, out_tokens, nullptr,
+                               device_status, workspace, workspace_bytes, stream);
+}
+
+spec_status spec_verify_greedy_ex(spec_batch g, spec_dtype dtype, const void* target_logits,
+                                  const int32_t* draft_tokens, int32_t* n_accepted, int32_t* out_tokens,
+                                  const spec_options* options, uint32_t* device_status, void* workspace,
+                                  size_t workspace_bytes, spec_stream_t stream) {
+  return greedy_impl(g, dtype, target_logits, draft_tokens, n_accepted, out_tokens, options, device_status,
+                     workspace, workspace_bytes, stream, ZeroRegion());
 }
 
 spec_status spec_verify_tree(int32_t B, int32_t N, int32_t V, spec_dtype dtype, const void* target_logits,
@@ -541,6 +623,86 @@ spec_status spec_nkl_ex(spec_batch g, spec_dtype dtype, const void* target_logit
   apply_options(rp, options, SPEC_MODE_NKL);
   if (launch_rows<M_NKL>(dtype == SPEC_BF16, vec_path(dtype, g.V, target_logits, draft_logits), rp,
                          L.rows * L.nchunks, stream) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  return SPEC_OK;
+}
+
+size_t spec_multi_workspace_bytes(spec_multi_batch m, spec_dtype dtype, int32_t stochastic) {
+  if (check_multi(m) != SPEC_OK || (dtype != SPEC_F32 && dtype != SPEC_BF16)) return 0;
+  return multi_layout(m, dtype, stochastic != 0).total;
+}
+
+spec_status spec_verify_multi(spec_multi_batch m, spec_dtype dtype, int32_t stochastic, const void* target_logits,
+                              const void* draft_logits, const int32_t* draft_tokens, float temperature,
+                              const float* u_accept, const float* u_sample, float consensus_nkl,
+                              float divergence_nkl, int32_t* n_accepted, int32_t* out_tokens, int32_t* best_k,
+                              int32_t* best_n, int32_t* best_tokens, float* pair_nkl, uint8_t* consensus,
+                              uint8_t* divergence, uint32_t* device_status, void* workspace,
+                              size_t workspace_bytes, spec_stream_t stream_) {
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
+  spec_status st = check_multi(m);
+  if (st != SPEC_OK) return st;
+  if (!temperature_ok(temperature) || !isfinite(consensus_nkl) || !isfinite(divergence_nkl))
+    return SPEC_ERR_INVALID_ARG;
+  if (m.G == 0) return SPEC_OK;
+  if (!target_logits || !n_accepted || !out_tokens || !best_k || !best_n || !best_tokens || !device_status)
+    return SPEC_ERR_INVALID_ARG;
+  if (m.gamma > 0 && (!draft_logits || !draft_tokens)) return SPEC_ERR_INVALID_ARG;
+  if (stochastic && (!u_sample || (m.gamma > 0 && !u_accept))) return SPEC_ERR_INVALID_ARG;
+  const MultiLayout ML = multi_layout(m, dtype, stochastic != 0);
+  if (!workspace || workspace_bytes < ML.total || ((uintptr_t)workspace & 255u)) return SPEC_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const spec_batch g = multi_as_batch(m);
+  ZeroRegion zr;
+  zr.ptr = reinterpret_cast<unsigned*>(ws + ML.tickets);
+  zr.n = m.G * m.gamma;
+  st = stochastic ? stochastic_impl(g, dtype, target_logits, draft_logits, draft_tokens, temperature, u_accept,
+                                    u_sample, n_accepted, out_tokens, nullptr, nullptr, nullptr, nullptr, nullptr,
+                                    0.15f, nullptr, nullptr, nullptr, device_status, workspace, ML.verify, stream_,
+                                    zr)
+                  : greedy_impl(g, dtype, target_logits, draft_tokens, n_accepted, out_tokens, nullptr,
+                                device_status, workspace, ML.verify, stream_, zr);
+  if (st != SPEC_OK) return st;
+  if (m.gamma > 0) {
+    PairParams pp;
+    memset(&pp, 0, sizeof(pp));
+    pp.draft = draft_logits;
+    pp.V = m.V;
+    pp.gamma = m.gamma;
+    pp.K = m.K;
+    pp.G = m.G;
+    pp.nchunks = ML.nchunks;
+    pp.chunk_elems = ML.chunk_elems;
+    pp.c = (float)(1.4426950408889634 / (double)temperature);
+    pp.invT = (float)(1.0 / (double)temperature);
+    pp.inv_lnV = m.V > 1 ? (float)(1.0 / log((double)m.V)) : 0.f;
+    pp.c_thr = consensus_nkl;
+    pp.d_thr = divergence_nkl;
+    pp.part = reinterpret_cast<PairPartial*>(ws + ML.part);
+    pp.cnt = zr.ptr;
+    pp.pair_nkl = pair_nkl;
+    pp.cons = consensus;
+    pp.div = divergence;
+    pp.status = device_status;
+    const long long tiles = (long long)m.G * m.gamma * ML.nchunks;
+    if (launch_pair(dtype == SPEC_BF16, vec_path(dtype, m.V, draft_logits, nullptr), m.K, pp, tiles, stream) !=
+        cudaSuccess)
+      return SPEC_ERR_CUDA;
+  }
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3((unsigned)ceil_div(m.G, kThreads));
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const int G = m.G, K = m.K, gm = m.gamma;
+  if (cudaLaunchKernelEx(&cfg, select_kernel, (const int32_t*)n_accepted, (const int32_t*)out_tokens, G, K, gm,
+                         best_k, best_n, best_tokens) != cudaSuccess)
     return SPEC_ERR_CUDA;
   return SPEC_OK;
 }

@@ -215,6 +215,50 @@ def make_stochastic(B: int, V: int, dtype: str, T: float, seed: int, gamma: int 
                               u_sample=u_smp, dense=dense, name=name)
 
 
+def make_multi(G: int, K: int, gamma: int, V: int, dtype: str, T: float, seed: int,
+               spreads=(0.02, 0.3, 1.5)) -> StochasticWorkload:
+    """Multi-draft groups: G groups of K candidate sequences (candidate k of group g is
+    sequence g*K + k of the dense batch returned). The candidates of a group share a
+    context: their target rows are one base plus a small per-candidate perturbation, and
+    their draft rows one shared draft plus per-candidate noise of standard deviation
+    spreads[g % len(spreads)] -- small spreads give candidates that agree, large ones
+    candidates that diverge. Draft tokens are Gumbel-max samples of softmax(draft / T)."""
+    B = G * K
+    sdt = np.uint16 if dtype == BF16 else np.float32
+    target = np.empty((B * (gamma + 1), V), dtype=sdt)
+    draft = np.empty((B * gamma, V), dtype=sdt)
+    tokens = np.empty(B * gamma, dtype=np.int32)
+    u_acc = np.empty(B * gamma, dtype=np.float32)
+    u_smp = np.empty(B, dtype=np.float32)
+
+    def one(g):
+        rng = np.random.default_rng([seed, g])
+        spread = np.float32(spreads[g % len(spreads)])
+        base = rng.standard_normal((gamma + 1, V), dtype=np.float32) * np.float32(TARGET_SIGMA)
+        peak_t = rng.integers(0, V, size=gamma + 1)
+        base[np.arange(gamma + 1), peak_t] += np.float32(PEAK_BONUS)
+        shared = np.float32(DRAFT_SCALE) * base[:gamma] + rng.standard_normal((gamma, V), dtype=np.float32)
+        for k in range(K):
+            b = g * K + k
+            t32 = base + np.float32(0.1) * rng.standard_normal((gamma + 1, V), dtype=np.float32)
+            d32 = shared + spread * rng.standard_normal((gamma, V), dtype=np.float32)
+            expo = rng.standard_exponential((gamma, V), dtype=np.float32)
+            target[b * (gamma + 1):(b + 1) * (gamma + 1)] = storage(t32, dtype)
+            d_st = storage(d32, dtype)
+            draft[b * gamma:(b + 1) * gamma] = d_st
+            gumbel = -np.log(np.maximum(expo, np.float32(np.finfo(np.float32).tiny)))
+            tokens[b * gamma:(b + 1) * gamma] = np.argmax(stored_as_f32(d_st, dtype) / np.float32(T) + gumbel, axis=1)
+            u_acc[b * gamma:(b + 1) * gamma] = rng.random(gamma, dtype=np.float32)
+            u_smp[b] = rng.random(dtype=np.float32)
+
+    _for_each(one, G)
+    gammas = np.full(B, gamma, dtype=np.int32)
+    cu = np.arange(B + 1, dtype=np.int32) * gamma
+    return StochasticWorkload(B=B, V=V, dtype=dtype, T=float(T), gammas=gammas, cu_draft=cu, target=target,
+                              draft=draft, tokens=tokens, u_accept=u_acc, u_sample=u_smp, dense=True,
+                              name=f"multi G={G} K={K}")
+
+
 def make_tree(B: int, V: int, dtype: str, seed: int, parent=TREE_PARENT, agreement: float = 0.8,
               name: str = "") -> TreeWorkload:
     """Tree batch: a draft row is drawn beside every target row; root candidates are the

@@ -157,3 +157,28 @@ int main(void) {
             O.block_n.offset, O.block_tokens.offset, O.stats.offset, O.stats_bucket.offset, ctypes.sizeof(S),
             S.rate2_fx.offset]
     assert got == want
+
+
+def test_multi_draft_checks_without_launch(lib):
+    P = ctypes.c_void_p
+    one = P(256)
+
+    def multi(G=4, K=3, gamma=2, V=1000, stochastic=1, T=0.8, ws=one, wsb=1 << 30, c=0.1, d=0.15, ua=one):
+        m = _lib.SpecMultiBatch(G, K, gamma, V)
+        return lib.spec_verify_multi(m, _lib.SPEC_BF16, stochastic, one, one, one, T, ua, one, c, d, one, one, one,
+                                     one, one, None, None, None, one, ws, wsb, None)
+
+    assert multi(K=1) == _lib.SPEC_ERR_INVALID_ARG
+    assert multi(K=_lib.SPEC_MAX_CANDIDATES + 1) == _lib.SPEC_ERR_INVALID_ARG
+    assert multi(gamma=_lib.SPEC_MAX_GAMMA + 1) == _lib.SPEC_ERR_INVALID_ARG
+    assert multi(T=0.0) == _lib.SPEC_ERR_INVALID_ARG
+    assert multi(c=float("nan")) == _lib.SPEC_ERR_INVALID_ARG
+    assert multi(ua=None) == _lib.SPEC_ERR_INVALID_ARG          # stochastic needs u_accept
+    assert multi(ws=None) == _lib.SPEC_ERR_WORKSPACE
+    assert multi(wsb=1024) == _lib.SPEC_ERR_WORKSPACE
+    assert multi(G=0) == _lib.SPEC_OK
+    mb = _lib.SpecMultiBatch(64, 3, 8, 128256)
+    sto = lib.spec_multi_workspace_bytes(mb, _lib.SPEC_BF16, 1)
+    single = lib.spec_workspace_bytes(_g(192, 8, 128256), _lib.SPEC_BF16, _lib.SPEC_MODE_STOCHASTIC)
+    assert sto > single and lib.spec_multi_workspace_bytes(mb, _lib.SPEC_BF16, 0) < sto
+    assert lib.spec_multi_workspace_bytes(_lib.SpecMultiBatch(4, 1, 2, 100), _lib.SPEC_BF16, 1) == 0
