@@ -366,6 +366,21 @@ def run_ours(args):
                                                  min_block_len=3, stats=st, stats_bucket=2)
         t_gp = time_mode(gpfn, 200, 10, dev)
         modes["greedy_block_stats_B256_g8_V128256"] = {"us_per_call": t_gp * 1e6, "GBps": ab["greedy"] / t_gp / 1e9}
+        # multi-draft: 64 groups of 3 candidates with the headline's gamma, V and dtype
+        wm = synth.make_multi(64, 3, gam, w.V, w.dtype, w.T, seed=5)
+        tm, dm, km = _to_dev(wm.target, dev), _to_dev(wm.draft, dev), _to_dev(wm.tokens, dev)
+        uam, usm = _to_dev(wm.u_accept, dev), _to_dev(wm.u_sample, dev)
+        m_out = {}
+        mfn = lambda: api.spec_verify_multi(tm, dm, km, 3, wm.T, stochastic=True, u_accept=uam,  # noqa: E731
+                                            u_sample=usm, out=m_out)
+        t_m = time_mode(mfn, 100, 5, dev)
+        eb = 2 if w.dtype == synth.BF16 else 4
+        mb_min = (wm.target.size + wm.draft.size + 2 * wm.B * wm.V) * eb
+        modes["multi_draft_G64_K3_g8_V128256"] = {
+            "us_per_call": t_m * 1e6, "GBps": mb_min / t_m / 1e9, "frac_of_peak": mb_min / t_m / 1e9 / hbm,
+            "note": "algorithmic bytes: every logit once + one row pair per candidate; the design reads the "
+                    f"draft rows a second time for the pairwise matrix (+{wm.draft.size * eb / 1e6:.0f} MB)"}
+        del tm, dm, km, uam, usm, m_out
         sm_out = torch.empty(6, dtype=torch.float64, device=dev)
         t_sm = time_mode(lambda: api.spec_accept_summary(st, 2, 64, out=sm_out), 200, 10, dev)
         modes["accept_summary_64_slots"] = {"us_per_call": t_sm * 1e6,
