@@ -65,6 +65,16 @@ class Workspace:
 _DEFAULT_WS = {}
 
 
+def _out(o: dict, name: str, make):
+    """o[name], allocated by make() only when the caller has not passed one (no allocation
+    on the repeated-call path)."""
+    t = o.get(name)
+    if t is None:
+        t = make()
+        o[name] = t
+    return t
+
+
 def _workspace(ws, nbytes, device):
     if isinstance(ws, torch.Tensor):
         if ws.numel() < nbytes:
@@ -177,8 +187,8 @@ def spec_verify_greedy(target: torch.Tensor, draft_tokens: torch.Tensor, *, cu_d
     _need(target, "target", target.dtype, rows * V, dev)
     _need(draft_tokens, "draft_tokens", torch.int32, total, dev)
     o = {} if out is None else out
-    n_acc = o.setdefault("n_accepted", torch.empty(B, dtype=torch.int32, device=dev))
-    out_tok = o.setdefault("out_tokens", torch.empty(rows, dtype=torch.int32, device=dev))
+    n_acc = _out(o, "n_accepted", lambda: torch.empty(B, dtype=torch.int32, device=dev))
+    out_tok = _out(o, "out_tokens", lambda: torch.empty(rows, dtype=torch.int32, device=dev))
     _need(n_acc, "n_accepted", torch.int32, B, dev)
     _need(out_tok, "out_tokens", torch.int32, rows, dev)
     if device_status is None:
@@ -219,9 +229,9 @@ def spec_verify_tree(target: torch.Tensor, node_tokens: torch.Tensor, parent, *,
     _need(target, "target", target.dtype, B * (N + 1) * V, dev)
     _need(node_tokens, "node_tokens", torch.int32, B * N, dev)
     o = {} if out is None else out
-    acc = o.setdefault("accept_len", torch.empty(B, dtype=torch.int32, device=dev))
-    path = o.setdefault("path_nodes", torch.empty(B, D, dtype=torch.int32, device=dev))
-    tok = o.setdefault("out_tokens", torch.empty(B, D + 1, dtype=torch.int32, device=dev))
+    acc = _out(o, "accept_len", lambda: torch.empty(B, dtype=torch.int32, device=dev))
+    path = _out(o, "path_nodes", lambda: torch.empty(B, D, dtype=torch.int32, device=dev))
+    tok = _out(o, "out_tokens", lambda: torch.empty(B, D + 1, dtype=torch.int32, device=dev))
     if device_status is None:
         device_status = o.get("device_status")
         if device_status is None:
@@ -249,8 +259,8 @@ def spec_nkl(target: torch.Tensor, draft: torch.Tensor, temperature: float, *, c
     _need(target, "target", target.dtype, (total + B) * V, dev)
     _need(draft, "draft", target.dtype, total * V, dev)
     o = {} if out is None else out
-    nkl = o.setdefault("nkl", torch.empty(total, dtype=torch.float32, device=dev))
-    mask = o.setdefault("nkl_mask", torch.empty(total, dtype=torch.uint8, device=dev)) if want_mask else None
+    nkl = _out(o, "nkl", lambda: torch.empty(total, dtype=torch.float32, device=dev))
+    mask = _out(o, "nkl_mask", lambda: torch.empty(total, dtype=torch.uint8, device=dev)) if want_mask else None
     if device_status is None:
         device_status = o.get("device_status")
         if device_status is None:
@@ -285,8 +295,8 @@ def _fill_options(opt: dict, o: dict, dev, B: int, total: int) -> _lib.SpecOptio
     mb = int(opt.get("min_block_len", 0))
     so.min_block_len = mb
     if mb > 0:
-        bn = o.setdefault("block_n", torch.empty(B, dtype=torch.int32, device=dev))
-        bt = o.setdefault("block_tokens", torch.empty(total, dtype=torch.int32, device=dev))
+        bn = _out(o, "block_n", lambda: torch.empty(B, dtype=torch.int32, device=dev))
+        bt = _out(o, "block_tokens", lambda: torch.empty(total, dtype=torch.int32, device=dev))
         _need(bn, "block_n", torch.int32, B, dev)
         _need(bt, "block_tokens", torch.int32, total, dev)
         so.block_n = bn.data_ptr()
@@ -383,15 +393,15 @@ def spec_verify_multi(target: torch.Tensor, draft: torch.Tensor, draft_tokens: t
         _need(u_accept, "u_accept", torch.float32, G * K * gamma, dev)
     o = {} if out is None else out
     i32 = lambda n: torch.empty(n, dtype=torch.int32, device=dev)  # noqa: E731
-    n_acc = o.setdefault("n_accepted", i32(G * K))
-    out_tok = o.setdefault("out_tokens", i32(G * K * (gamma + 1)))
-    bk, bn = o.setdefault("best_k", i32(G)), o.setdefault("best_n", i32(G))
-    bt = o.setdefault("best_tokens", i32(G * (gamma + 1)))
+    n_acc = _out(o, "n_accepted", lambda: i32(G * K))
+    out_tok = _out(o, "out_tokens", lambda: i32(G * K * (gamma + 1)))
+    bk, bn = _out(o, "best_k", lambda: i32(G)), _out(o, "best_n", lambda: i32(G))
+    bt = _out(o, "best_tokens", lambda: i32(G * (gamma + 1)))
     pn = cons = div = None
     if want_matrix:
-        pn = o.setdefault("pair_nkl", torch.empty(G * gamma * K * K, dtype=torch.float32, device=dev))
-        cons = o.setdefault("consensus", torch.empty(G * gamma, dtype=torch.uint8, device=dev))
-        div = o.setdefault("divergence", torch.empty(G * gamma, dtype=torch.uint8, device=dev))
+        pn = _out(o, "pair_nkl", lambda: torch.empty(G * gamma * K * K, dtype=torch.float32, device=dev))
+        cons = _out(o, "consensus", lambda: torch.empty(G * gamma, dtype=torch.uint8, device=dev))
+        div = _out(o, "divergence", lambda: torch.empty(G * gamma, dtype=torch.uint8, device=dev))
     if device_status is None:
         device_status = o.get("device_status")
         if device_status is None:

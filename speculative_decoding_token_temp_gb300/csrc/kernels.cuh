@@ -43,7 +43,7 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr int kMaxRows = SPEC_MAX_GAMMA + 1;
 constexpr int kMaxSteps = 64;        // 256-token steps per warp in one sampling segment
 constexpr int kSegElems = 16384;     // largest sampling segment (kWarps * kMaxSteps * 32 scalar loads)
-constexpr int kTargetTiles = 1216;   // 152 SMs x 8 resident blocks: enough tiles to fill the GPU
+constexpr int kTargetTiles = 2432;   // 4 waves of the 608 resident blocks (152 SMs x 4): a partial last wave costs little
 
 // M_STOCH2: stochastic with a draft temperature of its own (the draft row is summed at
 // both temperatures)
