@@ -14,7 +14,7 @@
 // drafts (the lowest index among equals) and copies its tokens.
 #pragma once
 
-#include "kernels.cuh"
+#include "kernels_rows.cuh"
 
 namespace sv {
 
@@ -39,16 +39,105 @@ struct PairParams {
   uint32_t* status;
 };
 
+// The last tile of a (group, position): merge the chunks' partials (thread (a, j) owns
+// S_a for j == K, else K_aj), then the K x K matrix and the flags. Every thread calls it.
+template <int K>
+__device__ __forceinline__ void pair_merge(const PairParams& p, int gi) {
+  __shared__ float s_M[K], s_S[K], s_K[K * K], s_N[K * K];
+  const float c = p.c;
+  const PairPartial* pp = p.part + (size_t)gi * p.nchunks;
+  if (threadIdx.x < K * (K + 1)) {
+    const int a = threadIdx.x / (K + 1), j = threadIdx.x - a * (K + 1);
+    float M = -INFINITY;
+    for (int ch = 0; ch < p.nchunks; ++ch) M = fmaxf(M, __ldcg(&pp[ch].ref[a]));
+    float t = 0.f;
+    for (int ch = 0; ch < p.nchunks; ++ch) {
+      const float r = __ldcg(&pp[ch].ref[a]);
+      const float f = (r == -INFINITY) ? 0.f : ex2((r - M) * c);
+      t += f * (j == K ? __ldcg(&pp[ch].s[a]) : __ldcg(&pp[ch].k[a * K + j]));
+    }
+    if (j == K) {
+      s_S[a] = t;
+      s_M[a] = M;
+    } else {
+      s_K[a * K + j] = t;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < K * K) {
+    const int a = threadIdx.x / K, b = threadIdx.x - a * K;
+    float n = 0.f;
+    if (a != b) {
+      const float kl = (s_K[a * K + b] / s_S[a] - (s_M[a] - s_M[b])) * p.invT - logf(s_S[a] / s_S[b]);
+      n = isfinite(kl) ? kl * p.inv_lnV : __int_as_float(0x7fc00000);
+    }
+    s_N[threadIdx.x] = n;
+    if (p.pair_nkl) p.pair_nkl[(size_t)gi * K * K + threadIdx.x] = n;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    bool cons = false, div = true, bad = false;
+    for (int a = 0; a < K; ++a)
+      for (int b = 0; b < K; ++b) {
+        if (a == b) continue;
+        const float ab = s_N[a * K + b], ba = s_N[b * K + a];
+        bad = bad || isnan(ab);
+        cons = cons || (ab < p.c_thr && ba < p.c_thr);
+        div = div && (ab > p.d_thr);
+      }
+    if (bad) atomicOr(p.status, SPEC_DEV_NONFINITE);
+    if (p.cons) p.cons[gi] = cons ? 1 : 0;
+    if (p.div) p.div[gi] = div ? 1 : 0;
+  }
+}
+
+// Block reduction of the per-thread pairwise sums of one tile (per row a: reference mr,
+// sum s; per ordered pair: kk) into the tile's PairPartial. Every thread calls it.
+template <int K>
+__device__ __forceinline__ void pair_partial_write(PairPartial* dst, const float (&mr)[K], const float (&s)[K],
+                                                   const float (&kk)[K][K], float c) {
+  __shared__ float s_red[kWarps][K + K * K];
+  __shared__ float s_ref[kWarps][K];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int a = 0; a < K; ++a) {
+    const float wm = warp_max(mr[a]);
+    if (lane == 0) s_ref[warp][a] = wm;
+  }
+  __syncthreads();
+  float DM[K];
+#pragma unroll
+  for (int a = 0; a < K; ++a) {
+    DM[a] = s_ref[0][a];
+    for (int w = 1; w < kWarps; ++w) DM[a] = fmaxf(DM[a], s_ref[w][a]);
+    const float f = (mr[a] == -INFINITY) ? 0.f : ex2((mr[a] - DM[a]) * c);
+    const float ws = warp_sum(s[a] * f);
+    if (lane == 0) s_red[warp][a] = ws;
+#pragma unroll
+    for (int b = 0; b < K; ++b) {
+      const float wk = warp_sum(kk[a][b] * f);
+      if (lane == 0) s_red[warp][K + a * K + b] = wk;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < K + K * K) {
+    float t = 0.f;
+    for (int w = 0; w < kWarps; ++w) t += s_red[w][threadIdx.x];
+    if (threadIdx.x < K)
+      __stcg(&dst->s[threadIdx.x], t);
+    else
+      __stcg(&dst->k[threadIdx.x - K], t);
+  }
+  if (threadIdx.x < K) __stcg(&dst->ref[threadIdx.x], DM[threadIdx.x]);
+}
+
 template <typename E, int VEC, int K>
 __global__ void __launch_bounds__(kThreads, 2) pair_kernel(const __grid_constant__ PairParams p) {
   using io = IO<E, VEC>;
   using raw_t = typename io::raw_t;
   griddep_wait();  // earlier work on the stream (the verification, the prologue) has completed
   griddep_launch();
-  __shared__ float s_red[kWarps][K + K * K];
-  __shared__ float s_ref[kWarps][K];
   __shared__ int s_last;
-  __shared__ float s_M[K], s_S[K], s_K[K * K], s_N[K * K];
   const int tile = blockIdx.x;
   const int gi = tile / p.nchunks, chunk = tile - gi * p.nchunks;
   const int g = gi / p.gamma, i = gi - g * p.gamma;
@@ -124,39 +213,7 @@ __global__ void __launch_bounds__(kThreads, 2) pair_kernel(const __grid_constant
     fold(z);
   }
 
-  // block reduction: per row the largest reference, the sums moved to it
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int a = 0; a < K; ++a) {
-    const float wm = warp_max(mr[a]);
-    if (lane == 0) s_ref[warp][a] = wm;
-  }
-  __syncthreads();
-  float DM[K];
-#pragma unroll
-  for (int a = 0; a < K; ++a) {
-    DM[a] = s_ref[0][a];
-    for (int w = 1; w < kWarps; ++w) DM[a] = fmaxf(DM[a], s_ref[w][a]);
-    const float f = (mr[a] == -INFINITY) ? 0.f : ex2((mr[a] - DM[a]) * c);
-    const float ws = warp_sum(s[a] * f);
-    if (lane == 0) s_red[warp][a] = ws;
-#pragma unroll
-    for (int b = 0; b < K; ++b) {
-      const float wk = warp_sum(kk[a][b] * f);
-      if (lane == 0) s_red[warp][K + a * K + b] = wk;
-    }
-  }
-  __syncthreads();
-  PairPartial* dst = p.part + tile;
-  if (threadIdx.x < K + K * K) {
-    float t = 0.f;
-    for (int w = 0; w < kWarps; ++w) t += s_red[w][threadIdx.x];
-    if (threadIdx.x < K)
-      __stcg(&dst->s[threadIdx.x], t);
-    else
-      __stcg(&dst->k[threadIdx.x - K], t);
-  }
-  if (threadIdx.x < K) __stcg(&dst->ref[threadIdx.x], DM[threadIdx.x]);
+  pair_partial_write<K>(p.part + tile, mr, s, kk, c);
   __syncthreads();  // every writer's partial entries precede thread 0's fence
   if (threadIdx.x == 0) {
     __threadfence();
@@ -167,50 +224,203 @@ __global__ void __launch_bounds__(kThreads, 2) pair_kernel(const __grid_constant
   __syncthreads();
   if (!s_last) return;
 
-  // merge the chunks of this (group, position): thread (a, j) owns S_a (j == K) or K_aj
-  const PairPartial* pp = p.part + (size_t)gi * p.nchunks;
-  if (threadIdx.x < K * (K + 1)) {
-    const int a = threadIdx.x / (K + 1), j = threadIdx.x - a * (K + 1);
-    float M = -INFINITY;
-    for (int ch = 0; ch < p.nchunks; ++ch) M = fmaxf(M, __ldcg(&pp[ch].ref[a]));
-    float t = 0.f;
-    for (int ch = 0; ch < p.nchunks; ++ch) {
-      const float r = __ldcg(&pp[ch].ref[a]);
-      const float f = (r == -INFINITY) ? 0.f : ex2((r - M) * c);
-      t += f * (j == K ? __ldcg(&pp[ch].s[a]) : __ldcg(&pp[ch].k[a * K + j]));
-    }
-    if (j == K) {
-      s_S[a] = t;
-      s_M[a] = M;
-    } else {
-      s_K[a * K + j] = t;
-    }
+  pair_merge<K>(p, gi);
+}
+
+// ---------------------------------------------------------------------------
+// Fused multi-draft tiles (aligned rows): one block per (group, row r, vocabulary chunk)
+// reads the K candidates' target rows r and, for r < gamma, their draft rows r, each
+// logit once, through a per-thread 3- or 4-stage cp.async ring (one 16-byte vector per row
+// per stage, lane-interleaved as in the tile kernel). Per candidate it keeps the tile
+// kernel's statistics (target maximum, index and, stochastic, sum; draft sum and the KL
+// sum against the candidate's own target row) and writes them as that candidate's
+// partial, so the ordinary per-sequence tickets and finalisation decide the candidates;
+// from the same draft exponentials it keeps the pairwise sums of the matrix.
+template <int K>
+__host__ __device__ constexpr int multi_stages() {
+  return 3;  // two blocks per SM: 3 x 24 KB (K = 3) or 3 x 32 KB (K = 4) each
+}
+
+template <int K>
+__host__ __device__ constexpr int multi_smem() {
+  return multi_stages<K>() * 2 * K * kThreads * 16;
+}
+
+template <typename E, int VEC, int K, int MODE>
+__global__ void __launch_bounds__(kThreads, 2) multi_rows_kernel(const __grid_constant__ RowsParams p,
+                                                                 const __grid_constant__ PairParams q) {
+  using io = IO<E, VEC>;
+  constexpr bool STOCH = MODE == M_STOCH;
+  constexpr int kMS = multi_stages<K>();
+  extern __shared__ __align__(128) unsigned char dsm[];
+  griddep_wait();  // the prologue, and everything earlier on the stream, has completed
+  griddep_launch();
+  __shared__ int s_last[K + 1];
+  const int gamma = p.gamma, nchunks = p.nchunks;
+  const int per = (gamma + 1) * nchunks;
+  const int tile = blockIdx.x;
+  const int g = tile / per, rem = tile - g * per;
+  const int r = rem / nchunks, chunk = rem - r * nchunks;
+  const bool pair = r < gamma;
+  const size_t V = (size_t)p.V;
+  const E* trow[K];
+  const E* drow[K];
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    const size_t b = (size_t)g * K + k;
+    trow[k] = static_cast<const E*>(p.target) + (b * (gamma + 1) + r) * V;
+    drow[k] = pair ? static_cast<const E*>(p.draft) + (b * gamma + r) * V : trow[k];
   }
-  __syncthreads();
-  if (threadIdx.x < K * K) {
-    const int a = threadIdx.x / K, b = threadIdx.x - a * K;
-    float n = 0.f;
-    if (a != b) {
-      const float kl = (s_K[a * K + b] / s_S[a] - (s_M[a] - s_M[b])) * p.invT - logf(s_S[a] / s_S[b]);
-      n = isfinite(kl) ? kl * p.inv_lnV : __int_as_float(0x7fc00000);
-    }
-    s_N[threadIdx.x] = n;
-    if (p.pair_nkl) p.pair_nkl[(size_t)gi * K * K + threadIdx.x] = n;
+  const int e_begin = chunk * p.chunk_elems;
+  const int e_end = min(e_begin + p.chunk_elems, p.V);
+  const int v0 = e_begin / VEC, v1 = e_end / VEC;
+  const float c = p.c;   // target scale (the greedy call's argmax needs none)
+  const float cq = q.c;  // draft scale, log2(e) / T: the matrix's and, stochastic, the verification's
+
+  TAcc ta[K];
+  DAcc da[K];
+  float kk[K][K];
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    init(ta[k]);
+    init(da[k]);
+#pragma unroll
+    for (int b = 0; b < K; ++b) kk[k][b] = 0.f;
   }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    bool cons = false, div = true, bad = false;
-    for (int a = 0; a < K; ++a)
-      for (int b = 0; b < K; ++b) {
-        if (a == b) continue;
-        const float ab = s_N[a * K + b], ba = s_N[b * K + a];
-        bad = bad || isnan(ab);
-        cons = cons || (ab < p.c_thr && ba < p.c_thr);
-        div = div && (ab > p.d_thr);
+
+  constexpr unsigned SLOT = 2 * K * kThreads * 16;
+  const int t = threadIdx.x;
+  const uint32_t base = (uint32_t)__cvta_generic_to_shared(dsm) + 16u * t;
+  const int nst = (v1 - v0 + kThreads - 1) / kThreads;
+  const int nr = pair ? 2 * K : K;
+  auto issue = [&](int st) {
+    if (st < nst) {
+      const int v = v0 + t + st * kThreads;
+      if (v < v1) {
+        const uint32_t slot = base + (uint32_t)(st % kMS) * SLOT;
+#pragma unroll
+        for (int j = 0; j < 2 * K; ++j)
+          if (j < nr)
+            cp_async16(slot + (uint32_t)(j * kThreads * 16), (j < K ? trow[j] : drow[j - K]) + (size_t)v * VEC);
       }
-    if (bad) atomicOr(p.status, SPEC_DEV_NONFINITE);
-    if (p.cons) p.cons[gi] = cons ? 1 : 0;
-    if (p.div) p.div[gi] = div ? 1 : 0;
+    }
+    cp_commit();
+  };
+#pragma unroll
+  for (int st = 0; st < kMS - 1; ++st) issue(st);
+  for (int st = 0; st < nst; ++st) {
+    issue(st + kMS - 1);
+    cp_wait<kMS - 1>();
+    const int v = v0 + t + st * kThreads;
+    if (v >= v1) continue;
+    const uint4* sq = reinterpret_cast<const uint4*>(dsm + (size_t)(st % kMS) * SLOT) + t;
+    const int e0 = v * VEC;
+#pragma unroll
+    for (int a = 0; a < K; ++a) {
+      float ft[VEC];
+      io::unpack(sq[a * kThreads], ft);
+      if (!pair || !STOCH) {
+        if (STOCH)
+          tsum_update<VEC>(ta[a], ft, e0, c);  // the stochastic bonus row
+        else
+          argmax_update<VEC>(ta[a], ft, e0);   // greedy rows
+      } else {
+        const float vm = vmax<VEC>(ft);
+        track_max<VEC, VEC, true>(ta[a], ft, vm, e0, 0);
+        lazy_ref(ta[a].mr, ta[a].mth, ta[a].nmc, ta[a].s, nullptr, vm, c);
+        float et[VEC];
+        ta[a].s = add2(ta[a].s, exp_sum2<VEC>(ft, c, ta[a].nmc, et));
+      }
+      if (pair) {
+        float fd[VEC], ed[VEC];
+        io::unpack(sq[(K + a) * kThreads], fd);
+        const float vm = vmax<VEC>(fd);
+        const bool mv = vm > da[a].mth;
+        if (__any_sync(__activemask(), mv)) {
+          if (mv) {
+            const float f = ex2((da[a].mr - vm) * cq);
+            da[a].s = make_float2(da[a].s.x * f, da[a].s.y * f);
+            da[a].k = make_float2(da[a].k.x * f, da[a].k.y * f);
+#pragma unroll
+            for (int b = 0; b < K; ++b) kk[a][b] *= f;
+            da[a].mr = vm;
+            da[a].mth = vm + kLazy / cq;
+            da[a].nmc = -vm * cq;
+          }
+        }
+        da[a].s = add2(da[a].s, exp_sum2<VEC>(fd, cq, da[a].nmc, ed));
+        if (STOCH) {
+          float kx = 0.f;
+#pragma unroll
+          for (int j = 0; j < VEC; ++j) kx = fmaf(ed[j], fd[j] - ft[j], kx);
+          da[a].k.x += kx;
+        }
+#pragma unroll
+        for (int b = 0; b < K; ++b) {
+          if (b == a) continue;
+          float fb[VEC];
+          io::unpack(sq[(K + b) * kThreads], fb);
+          float kx = 0.f;
+#pragma unroll
+          for (int j = 0; j < VEC; ++j) kx = fmaf(ed[j], fd[j] - fb[j], kx);
+          kk[a][b] += kx;
+        }
+      }
+    }
+  }
+  cp_wait<0>();
+
+  // partials: one per candidate in the tile kernel's layout, one pairwise partial
+  const int kind = pair ? (STOCH ? K_PAIR : K_ARGMAX) : (STOCH ? K_TSUM : K_ARGMAX);
+#pragma unroll
+  for (int a = 0; a < K; ++a) {
+    const Partial part = reduce_tile<BlockSync, E, VEC>(kind, ta[a], da[a], c, trow[a]);
+    if (threadIdx.x == 0) {
+      const size_t row = ((size_t)g * K + a) * (gamma + 1) + r;
+      float4* dst = reinterpret_cast<float4*>(p.part + row * nchunks + chunk);
+      __stcg(dst, make_float4(part.tm, part.ts, __int_as_float(part.tidx), __int_as_float(part.bad)));
+      __stcg(dst + 1, make_float4(part.dm, part.ds, part.dk, part.ds2));
+    }
+    __syncthreads();  // reduce_tile's shared arrays are reused by the next candidate
+  }
+  if (pair) {
+    float mr[K], sm[K];
+#pragma unroll
+    for (int a = 0; a < K; ++a) {
+      mr[a] = da[a].mr;
+      sm[a] = da[a].s.x + da[a].s.y;
+    }
+    pair_partial_write<K>(q.part + ((size_t)g * gamma + r) * nchunks + chunk, mr, sm, kk, cq);
+  }
+  __syncthreads();  // every writer's partial entries precede thread 0's fence
+  if (threadIdx.x == 0) {
+    __threadfence();
+    bool any = false;
+    for (int a = 0; a < K; ++a) {
+      const unsigned old = atomicAdd(p.cnt + (size_t)g * K + a, 1u);
+      s_last[a] = (old + 1u == (unsigned)per) ? 1 : 0;
+      any = any || s_last[a];
+    }
+    s_last[K] = 0;
+    if (pair) {
+      const unsigned old = atomicAdd(q.cnt + (size_t)g * gamma + r, 1u);
+      s_last[K] = (old + 1u == (unsigned)nchunks) ? 1 : 0;
+      any = any || s_last[K];
+    }
+    if (any) __threadfence();  // ... and the other tiles' partials before this block's reads
+  }
+  __syncthreads();
+  for (int a = 0; a < K; ++a) {
+    if (s_last[a]) {
+      const int b = g * K + a;
+      finalize<E, MODE, BlockSync>(p, b, gamma, b * (gamma + 1), b * gamma);
+      __syncthreads();
+    }
+  }
+  if (s_last[K]) pair_merge<K>(q, g * gamma + r);
+  if constexpr (STOCH) {
+    __syncthreads();  // the finalisers' writes precede the count
+    if (threadIdx.x == 0) tile_done<MODE>(p);
   }
 }
 

@@ -55,10 +55,14 @@ int table_stride_for(int V, spec_dtype dt) {
   return (int)(ceil_div(nv, 2 * kThreads) * kSlicesPerStage);
 }
 
-Layout layout(int B, int V, long long rows, bool sample, bool single_rows = false, spec_dtype dt = SPEC_F32) {
+// max_chunk: the longest vocabulary chunk of a tile (0 = 65536 tokens for single-row
+// tiles, 32768 for row pairs)
+Layout layout(int B, int V, long long rows, bool sample, bool single_rows = false, spec_dtype dt = SPEC_F32,
+              int max_chunk = 0) {
   Layout L;
   L.rows = rows;
-  chunking(V, rows > 0 ? rows : 1, single_rows ? 65536 : 32768, &L.nchunks, &L.chunk_elems);
+  chunking(V, rows > 0 ? rows : 1, max_chunk > 0 ? max_chunk : (single_rows ? 65536 : 32768), &L.nchunks,
+           &L.chunk_elems);
   if (sample)
     segmenting(V, B, &L.nseg, &L.seg_elems);
   else
@@ -237,6 +241,47 @@ cudaError_t launch_sample2(bool bf16, const SampleParams& sp, long long blocks, 
   return bf16 ? launch_sample2_t<uint16_t, 8>(sp, blocks, stream) : launch_sample2_t<float, 4>(sp, blocks, stream);
 }
 
+// Fused multi-draft tiles: when given, the verification launches multi_rows_kernel over
+// (group, row, chunk) tiles instead of rows_kernel over (row, chunk) tiles. A fused tile
+// reads 2K rows of a chunk as long as a pair tile's (shorter chunks measured slower: more per-tile fixed work).
+constexpr int kMultiChunk = 32768;
+struct MultiTiles {
+  int K = 0;
+  PairParams pp;
+};
+
+template <typename E, int VEC, int K, int MODE>
+cudaError_t launch_multi_t(const RowsParams& rp, const PairParams& pp, long long tiles, cudaStream_t stream) {
+  auto kern = multi_rows_kernel<E, VEC, K, MODE>;
+  static std::atomic<unsigned long long> done{0};
+  const cudaError_t e = ensure_smem_attr(kern, done, multi_smem<K>());
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3((unsigned)tiles);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)multi_smem<K>();
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, rp, pp);
+}
+
+template <int MODE>
+cudaError_t launch_multi(bool bf16, const MultiTiles& mt, const RowsParams& rp, long long tiles, cudaStream_t stream) {
+  if (bf16) {
+    if (mt.K == 2) return launch_multi_t<uint16_t, 8, 2, MODE>(rp, mt.pp, tiles, stream);
+    if (mt.K == 3) return launch_multi_t<uint16_t, 8, 3, MODE>(rp, mt.pp, tiles, stream);
+    return launch_multi_t<uint16_t, 8, 4, MODE>(rp, mt.pp, tiles, stream);
+  }
+  if (mt.K == 2) return launch_multi_t<float, 4, 2, MODE>(rp, mt.pp, tiles, stream);
+  if (mt.K == 3) return launch_multi_t<float, 4, 3, MODE>(rp, mt.pp, tiles, stream);
+  return launch_multi_t<float, 4, 4, MODE>(rp, mt.pp, tiles, stream);
+}
+
 RowsParams base_params(const spec_batch& g, const Layout& L, char* ws, uint32_t* status) {
   RowsParams rp;
   memset(&rp, 0, sizeof(rp));
@@ -302,7 +347,8 @@ spec_status stochastic_impl(spec_batch g, spec_dtype dtype, const void* target_l
                             const float* u_sample, int32_t* n_accepted, int32_t* out_tokens, float* p_x, float* q_x,
                             float* alpha, float* nkl, uint8_t* nkl_mask, float nkl_delta, int32_t* greedy_n,
                             int32_t* greedy_tokens, const spec_options* options, uint32_t* device_status,
-                            void* workspace, size_t workspace_bytes, spec_stream_t stream_, ZeroRegion zr) {
+                            void* workspace, size_t workspace_bytes, spec_stream_t stream_, ZeroRegion zr,
+                            const MultiTiles* mt = nullptr) {
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
   spec_status st = check_batch(g);
   if (st != SPEC_OK) return st;
@@ -313,7 +359,7 @@ spec_status stochastic_impl(spec_batch g, spec_dtype dtype, const void* target_l
   if (!target_logits || !n_accepted || !out_tokens || !u_sample || !device_status) return SPEC_ERR_INVALID_ARG;
   if (g.total_draft > 0 && (!draft_logits || !draft_tokens || !u_accept)) return SPEC_ERR_INVALID_ARG;
   if ((greedy_n == nullptr) != (greedy_tokens == nullptr)) return SPEC_ERR_INVALID_ARG;
-  const Layout L = layout(g.B, g.V, rows_for(SPEC_MODE_STOCHASTIC, g), true, false, dtype);
+  const Layout L = layout(g.B, g.V, rows_for(SPEC_MODE_STOCHASTIC, g), true, false, dtype, mt ? kMultiChunk : 0);
   if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u)) return SPEC_ERR_WORKSPACE;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   char* ws = static_cast<char*>(workspace);
@@ -343,8 +389,11 @@ spec_status stochastic_impl(spec_batch g, spec_dtype dtype, const void* target_l
   rp.mask = nkl_mask;
   rp.g_n = greedy_n;
   rp.g_tok = greedy_tokens;
-  const cudaError_t le = sept ? launch_rows<M_STOCH2>(bf16, vec, rp, L.rows * L.nchunks, stream)
-                              : launch_rows<M_STOCH>(bf16, vec, rp, L.rows * L.nchunks, stream);
+  // fused multi-draft tiles: (group, row, chunk), one per group row instead of per sequence row
+  const long long tiles = mt ? (long long)(g.B / mt->K) * (g.gamma + 1) * L.nchunks : L.rows * L.nchunks;
+  const cudaError_t le = mt     ? launch_multi<M_STOCH>(bf16, *mt, rp, tiles, stream)
+                         : sept ? launch_rows<M_STOCH2>(bf16, vec, rp, tiles, stream)
+                                : launch_rows<M_STOCH>(bf16, vec, rp, tiles, stream);
   if (le != cudaSuccess) return SPEC_ERR_CUDA;
 
   SampleParams sp;
@@ -367,7 +416,7 @@ spec_status stochastic_impl(spec_batch g, spec_dtype dtype, const void* target_l
   sp.table = reinterpret_cast<float*>(ws + L.table);
   sp.table_stride = L.table_stride;
   sp.tiles_done = reinterpret_cast<const unsigned*>(ws + L.cntA) + g.B;
-  sp.ntiles = (unsigned)(L.rows * L.nchunks);
+  sp.ntiles = (unsigned)tiles;
   if (vec) {
     // aligned rows: one wave of blocks over the B * nst stages. The last kTailSeqs
     // sequences (decided last by the tile kernel) take short ranges of at least
@@ -399,7 +448,7 @@ spec_status stochastic_impl(spec_batch g, spec_dtype dtype, const void* target_l
 spec_status greedy_impl(spec_batch g, spec_dtype dtype, const void* target_logits, const int32_t* draft_tokens,
                         int32_t* n_accepted, int32_t* out_tokens, const spec_options* options,
                         uint32_t* device_status, void* workspace, size_t workspace_bytes, spec_stream_t stream_,
-                        ZeroRegion zr) {
+                        ZeroRegion zr, const MultiTiles* mt = nullptr) {
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
   spec_status st = check_batch(g);
   if (st != SPEC_OK) return st;
@@ -408,7 +457,7 @@ spec_status greedy_impl(spec_batch g, spec_dtype dtype, const void* target_logit
   if (g.B == 0) return SPEC_OK;
   if (!target_logits || !n_accepted || !out_tokens || !device_status) return SPEC_ERR_INVALID_ARG;
   if (g.total_draft > 0 && !draft_tokens) return SPEC_ERR_INVALID_ARG;
-  const Layout L = layout(g.B, g.V, rows_for(SPEC_MODE_GREEDY, g), false, true);
+  const Layout L = layout(g.B, g.V, rows_for(SPEC_MODE_GREEDY, g), false, true, SPEC_F32, mt ? kMultiChunk : 0);
   if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u)) return SPEC_ERR_WORKSPACE;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   char* ws = static_cast<char*>(workspace);
@@ -420,6 +469,13 @@ spec_status greedy_impl(spec_batch g, spec_dtype dtype, const void* target_logit
   rp.out_tok = out_tokens;
   rp.c = rp.cd = 1.f;
   apply_options(rp, options, SPEC_MODE_GREEDY);
+  if (mt) {
+    rp.draft = mt->pp.draft;  // the fused tiles also read the draft rows (for the matrix)
+    if (launch_multi<M_GREEDY>(dtype == SPEC_BF16, *mt, rp, (long long)(g.B / mt->K) * (g.gamma + 1) * L.nchunks,
+                               stream) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+    return SPEC_OK;
+  }
   if (launch_rows<M_GREEDY>(dtype == SPEC_BF16, vec_path(dtype, g.V, target_logits, nullptr), rp,
                             L.rows * L.nchunks, stream) != cudaSuccess)
     return SPEC_ERR_CUDA;
@@ -432,7 +488,8 @@ spec_status greedy_impl(spec_batch g, spec_dtype dtype, const void* target_logit
 
 struct MultiLayout {
   size_t verify, tickets, part, total;
-  int nchunks, chunk_elems;
+  int nchunks, chunk_elems;    // two-pass matrix (pair_kernel) chunking
+  int vchunks, vchunk_elems;   // the verification's chunking, used by the fused tiles
 };
 
 spec_batch multi_as_batch(const spec_multi_batch& m) {
@@ -456,13 +513,18 @@ MultiLayout multi_layout(const spec_multi_batch& m, spec_dtype dt, bool stochast
   const spec_batch g = multi_as_batch(m);
   const spec_mode mode = stochastic ? SPEC_MODE_STOCHASTIC : SPEC_MODE_GREEDY;
   MultiLayout M;
-  M.verify = align256(layout(g.B, g.V, rows_for(mode, g), stochastic, !stochastic, dt).total);
+  const Layout Lv = layout(g.B, g.V, rows_for(mode, g), stochastic, !stochastic, dt, kMultiChunk);
+  const Layout Lp = layout(g.B, g.V, rows_for(mode, g), stochastic, !stochastic, dt);  // two-pass: plain tiles
+  M.verify = align256(Lv.total > Lp.total ? Lv.total : Lp.total);
+  M.vchunks = Lv.nchunks;
+  M.vchunk_elems = Lv.chunk_elems;
   const long long rows = (long long)m.G * m.gamma;
-  // a tile reads K rows of one chunk: about 64 K elements in all
+  // a two-pass tile reads K rows of one chunk: about 64 K elements in all
   chunking(m.V, rows > 0 ? rows : 1, 65536 / (m.K > 0 ? m.K : 1), &M.nchunks, &M.chunk_elems);
+  const int pchunks = M.nchunks > M.vchunks ? M.nchunks : M.vchunks;
   M.tickets = M.verify;
   M.part = align256(M.tickets + sizeof(unsigned) * (size_t)rows);
-  M.total = align256(M.part + sizeof(PairPartial) * (size_t)rows * M.nchunks);
+  M.total = align256(M.part + sizeof(PairPartial) * (size_t)rows * pchunks);
   return M;
 }
 
@@ -657,34 +719,42 @@ spec_status spec_verify_multi(spec_multi_batch m, spec_dtype dtype, int32_t stoc
   ZeroRegion zr;
   zr.ptr = reinterpret_cast<unsigned*>(ws + ML.tickets);
   zr.n = m.G * m.gamma;
+  PairParams pp;
+  memset(&pp, 0, sizeof(pp));
+  pp.draft = draft_logits;
+  pp.V = m.V;
+  pp.gamma = m.gamma;
+  pp.K = m.K;
+  pp.G = m.G;
+  pp.c = (float)(1.4426950408889634 / (double)temperature);
+  pp.invT = (float)(1.0 / (double)temperature);
+  pp.inv_lnV = m.V > 1 ? (float)(1.0 / log((double)m.V)) : 0.f;
+  pp.c_thr = consensus_nkl;
+  pp.d_thr = divergence_nkl;
+  pp.part = reinterpret_cast<PairPartial*>(ws + ML.part);
+  pp.cnt = zr.ptr;
+  pp.pair_nkl = pair_nkl;
+  pp.cons = consensus;
+  pp.div = divergence;
+  pp.status = device_status;
+  // aligned rows: fused (group, row, chunk) tiles read every logit once and fill the
+  // matrix on the way; otherwise the batch kernels, then a second pass over the drafts
+  const bool fused = m.gamma > 0 && vec_path(dtype, m.V, target_logits, draft_logits);
+  MultiTiles mt;
+  mt.K = m.K;
+  mt.pp = pp;
+  mt.pp.nchunks = ML.vchunks;
+  mt.pp.chunk_elems = ML.vchunk_elems;
   st = stochastic ? stochastic_impl(g, dtype, target_logits, draft_logits, draft_tokens, temperature, u_accept,
                                     u_sample, n_accepted, out_tokens, nullptr, nullptr, nullptr, nullptr, nullptr,
                                     0.15f, nullptr, nullptr, nullptr, device_status, workspace, ML.verify, stream_,
-                                    zr)
+                                    zr, fused ? &mt : nullptr)
                   : greedy_impl(g, dtype, target_logits, draft_tokens, n_accepted, out_tokens, nullptr,
-                                device_status, workspace, ML.verify, stream_, zr);
+                                device_status, workspace, ML.verify, stream_, zr, fused ? &mt : nullptr);
   if (st != SPEC_OK) return st;
-  if (m.gamma > 0) {
-    PairParams pp;
-    memset(&pp, 0, sizeof(pp));
-    pp.draft = draft_logits;
-    pp.V = m.V;
-    pp.gamma = m.gamma;
-    pp.K = m.K;
-    pp.G = m.G;
+  if (m.gamma > 0 && !fused) {
     pp.nchunks = ML.nchunks;
     pp.chunk_elems = ML.chunk_elems;
-    pp.c = (float)(1.4426950408889634 / (double)temperature);
-    pp.invT = (float)(1.0 / (double)temperature);
-    pp.inv_lnV = m.V > 1 ? (float)(1.0 / log((double)m.V)) : 0.f;
-    pp.c_thr = consensus_nkl;
-    pp.d_thr = divergence_nkl;
-    pp.part = reinterpret_cast<PairPartial*>(ws + ML.part);
-    pp.cnt = zr.ptr;
-    pp.pair_nkl = pair_nkl;
-    pp.cons = consensus;
-    pp.div = divergence;
-    pp.status = device_status;
     const long long tiles = (long long)m.G * m.gamma * ML.nchunks;
     if (launch_pair(dtype == SPEC_BF16, vec_path(dtype, m.V, draft_logits, nullptr), m.K, pp, tiles, stream) !=
         cudaSuccess)
