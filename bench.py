@@ -540,13 +540,42 @@ def main():
     ap.add_argument("--skip-ragged", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
                     help="sequences per step (default: the workload's 256); smaller slices serve profiling")
+    ap.add_argument("--multi", type=int, default=None, metavar="G",
+                    help="time only the multi-draft call on G groups of 3 candidates (gamma 8, V 128256, bf16): "
+                         "a secondary line for profiling, not the headline metric")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.multi is not None:
+        run_multi_only(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
+
+
+def run_multi_only(args):
+    """spec_verify_multi (stochastic) on make_multi(G, 3, 8, 128256, bf16): per-call device
+    time and GB/s of the minimal bytes (every logit once + one row pair per candidate)."""
+    import torch
+
+    import __graft_entry__
+    from speculative_decoding_token_temp_gb300 import api, synth
+    __graft_entry__.build()
+    dev = torch.device("cuda:0")
+    w = synth.make_multi(args.multi, 3, 8, 128256, synth.BF16, 0.6, seed=5)
+    t, d, k = _to_dev(w.target, dev), _to_dev(w.draft, dev), _to_dev(w.tokens, dev)
+    ua, us = _to_dev(w.u_accept, dev), _to_dev(w.u_sample, dev)
+    out = {}
+    fn = lambda: api.spec_verify_multi(t, d, k, 3, w.T, stochastic=True, u_accept=ua, u_sample=us,  # noqa: E731
+                                       out=out)
+    sec = time_mode(fn, args.steps, args.warmup, dev)
+    minimal = (w.target.size + w.draft.size + 2 * w.B * w.V) * 2
+    hbm, _ = peaks()
+    print(json.dumps({"metric": "multi_draft_us_per_call", "value": sec * 1e6, "unit": "us",
+                      "GBps": minimal / sec / 1e9, "frac_of_peak": minimal / sec / 1e9 / hbm,
+                      "status": int(out["device_status"][0]),
+                      "config": {"workload": f"multi-draft G={args.multi} K=3 gamma=8 V=128256 bf16"}}))
 
 
 if __name__ == "__main__":
