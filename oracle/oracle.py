@@ -98,6 +98,12 @@ Readings taken where the pages are silent, garbled or disagree:
       threshold in both directions; divergence at i: every entry off the diagonal is
       above the divergence threshold.
 
+  R23 a row split over vocabulary shards (logits sharded over tensor-parallel ranks; the
+      pages do not treat it): every statistic is a maximum, a log-sum-exp or a sum, so
+      per-shard statistics merge associatively (sums moved to the larger maximum, the
+      argmax by value then lowest index); the inverse-CDF draw takes the shard whose
+      exclusive prefix of shard masses passes u * Z and that shard's own running sum.
+
 Parity pins for every function: tests/test_oracle_pins.py.
 """
 from __future__ import annotations
@@ -548,3 +554,66 @@ def verify_multi(target_raw, draft_raw, tokens, G: int, K: int, gamma: int, T: f
                   "best_tokens": cand[best]["tokens"], "pair_nkl": np.array(mats).reshape(gamma, K, K),
                   "consensus": np.array(cons, dtype=np.uint8), "divergence": np.array(div, dtype=np.uint8)}
     return res
+
+
+# ---------------------------------------------------------------------------
+# the same definitions over a partition of the vocabulary (shards of a row, e.g. logits
+# split over tensor-parallel ranks): every statistic above is a log-sum-exp, a maximum or
+# a sum, so per-shard statistics combine associatively into the full row's
+
+def shard_stats(z_t: np.ndarray, z_d: np.ndarray, T: float, v0: int) -> dict:
+    """Statistics of one shard [v0, v0 + len) of a (target row, draft row) pair at T:
+    target maximum m_t of z_t / T and S_t = sum exp(z_t / T - m_t); the lowest global index
+    of the raw target maximum; draft m_d, S_d likewise; K = sum exp(z_d / T - m_d) *
+    (z_d - z_t) / T."""
+    st, sd = z_t / T, z_d / T
+    m_t, m_d = float(np.max(st)), float(np.max(sd))
+    e_d = np.exp(sd - m_d)
+    return {"m_t": m_t, "S_t": float(np.sum(np.exp(st - m_t))), "amax_v": float(np.max(z_t)),
+            "amax_i": v0 + int(np.argmax(z_t)), "m_d": m_d, "S_d": float(np.sum(e_d)),
+            "K": float(np.sum(e_d * (sd - st)))}
+
+
+def merge_stats(a: dict, b: dict) -> dict:
+    """Associative combination of two shards' statistics (sums moved to the larger maximum;
+    argmax by value, then the lower index)."""
+    m_t = max(a["m_t"], b["m_t"])
+    m_d = max(a["m_d"], b["m_d"])
+    fa, fb = math.exp(a["m_d"] - m_d), math.exp(b["m_d"] - m_d)
+    if a["amax_v"] > b["amax_v"] or (a["amax_v"] == b["amax_v"] and a["amax_i"] < b["amax_i"]):
+        av, ai = a["amax_v"], a["amax_i"]
+    else:
+        av, ai = b["amax_v"], b["amax_i"]
+    return {"m_t": m_t, "S_t": a["S_t"] * math.exp(a["m_t"] - m_t) + b["S_t"] * math.exp(b["m_t"] - m_t),
+            "amax_v": av, "amax_i": ai, "m_d": m_d, "S_d": a["S_d"] * fa + b["S_d"] * fb,
+            "K": a["K"] * fa + b["K"] * fb}
+
+
+def stats_outputs(st: dict, V: int) -> dict:
+    """Full-row quantities from merged statistics: lse_t, lse_d (of z / T, lse = m + ln S),
+    the argmax, and NKL with KL(q || p) = K / S_d - lse_d + lse_t."""
+    lse_t = st["m_t"] + math.log(st["S_t"])
+    lse_d = st["m_d"] + math.log(st["S_d"])
+    kl = st["K"] / st["S_d"] - lse_d + lse_t
+    return {"lse_t": lse_t, "lse_d": lse_d, "argmax": st["amax_i"], "nkl": 0.0 if V == 1 else kl / math.log(V)}
+
+
+def sharded_draw(weights_per_shard, u: float):
+    """Inverse-CDF draw over a row split into shards (token order = shard order): Z_s per
+    shard, an exclusive scan picks the shard whose range passes u * Z, and that shard's
+    own running sum finds the token. Returns (global token, Z)."""
+    Zs = [float(np.sum(w)) for w in weights_per_shard]
+    Z = float(sum(Zs))
+    target = u * Z
+    base, off = 0.0, 0
+    for s, w in enumerate(weights_per_shard):
+        if base + Zs[s] > target or s == len(weights_per_shard) - 1:
+            C = base + np.cumsum(w)
+            hit = np.nonzero(C > target)[0]
+            if hit.size:
+                return off + int(hit[0]), Z
+            nz = np.nonzero(w > 0)[0]
+            return off + (int(nz[-1]) if nz.size else len(w) - 1), Z
+        base += Zs[s]
+        off += len(w)
+    return off - 1, Z

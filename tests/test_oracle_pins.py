@@ -604,3 +604,46 @@ def test_multi_draft_keeps_the_longest_accepted_candidate():
     assert r["best_k"] == 1 and r["best_n"] == 2
     assert list(r["best_tokens"]) == [1, 2, 3, -1]       # the target argmax replaces the mismatch
     assert np.all(np.abs(r["pair_nkl"]) < 1e-12) and np.all(r["consensus"] == 1)   # constant rows: identical q
+
+
+# ---------------------------------------------------------------- vocabulary shards (R23)
+
+@pytest.mark.parametrize("seed", range(6))
+def test_shard_merge_equals_the_whole_row(seed):
+    rng = np.random.default_rng(600 + seed)
+    V, T = int(rng.integers(2, 3000)), float(rng.uniform(0.3, 1.5))
+    zt = np.round(rng.normal(0, 3, V), 1)              # rounded: ties of the maximum across shards occur
+    zd = 0.9 * zt + rng.normal(0, 1, V)
+    cuts = sorted(set(int(c) for c in rng.integers(1, V, int(rng.integers(0, 5))))) if V > 1 else []
+    bounds = [0] + cuts + [V]
+    parts = [O.shard_stats(zt[a:b], zd[a:b], T, a) for a, b in zip(bounds, bounds[1:])]
+    left = parts[0]
+    for p in parts[1:]:
+        left = O.merge_stats(left, p)
+    right = parts[-1]
+    for p in reversed(parts[:-1]):
+        right = O.merge_stats(p, right)
+    for st in (left, right):
+        out = O.stats_outputs(st, V)
+        assert out["argmax"] == int(np.argmax(zt))                     # lowest index among ties
+        assert out["lse_t"] == pytest.approx(float(zt[0] / T - O.log_softmax_T(zt, T)[0]), rel=1e-12)
+        assert out["lse_d"] == pytest.approx(float(zd[0] / T - O.log_softmax_T(zd, T)[0]), rel=1e-12)
+        assert out["nkl"] == pytest.approx(O.nkl_pair(zt, zd, T)[0], rel=1e-9, abs=1e-13)
+
+
+def test_sharded_draw_equals_the_whole_row():
+    rng = np.random.default_rng(61)
+    for _ in range(200):
+        V = int(rng.integers(1, 60))
+        w = np.where(rng.random(V) < 0.5, 0.0, rng.random(V))
+        if not np.any(w > 0):
+            w[int(rng.integers(0, V))] = 1.0
+        u = float(rng.random())
+        cuts = sorted(set(int(c) for c in rng.integers(1, V, 3))) if V > 1 else []
+        bounds = [0] + cuts + [V]
+        y, Z = O.sharded_draw([w[a:b] for a, b in zip(bounds, bounds[1:])], u)
+        y0, Z0, c0, c1 = O.inverse_cdf(w, u)
+        assert Z == pytest.approx(Z0, rel=1e-12)
+        if abs(c0 / Z0 - u) > 1e-9 and abs(c1 / Z0 - u) > 1e-9:    # away from a boundary: exactly the token
+            assert y == y0
+        assert w[y] > 0
