@@ -227,6 +227,21 @@ __global__ void __launch_bounds__(kThreads, 2) pair_kernel(const __grid_constant
   pair_merge<K>(p, gi);
 }
 
+// sum_j e[j] (x[j] - y[j]) with packed f32x2 subtractions and FMAs
+template <int VEC>
+__device__ __forceinline__ float dot_diff(const float (&e)[VEC], const float (&x)[VEC], const float (&y)[VEC]) {
+  if constexpr (VEC == 1) {
+    return e[0] * (x[0] - y[0]);
+  } else {
+    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < VEC / 2; ++j)
+      acc = fma2(make_float2(e[2 * j], e[2 * j + 1]),
+                 sub2(make_float2(x[2 * j], x[2 * j + 1]), make_float2(y[2 * j], y[2 * j + 1])), acc);
+    return acc.x + acc.y;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Fused multi-draft tiles (aligned rows): one block per (group, row r, vocabulary chunk)
 // reads the K candidates' target rows r and, for r < gamma, their draft rows r, each
@@ -349,21 +364,13 @@ __global__ void __launch_bounds__(kThreads, 2) multi_rows_kernel(const __grid_co
           }
         }
         da[a].s = add2(da[a].s, exp_sum2<VEC>(fd, cq, da[a].nmc, ed));
-        if (STOCH) {
-          float kx = 0.f;
-#pragma unroll
-          for (int j = 0; j < VEC; ++j) kx = fmaf(ed[j], fd[j] - ft[j], kx);
-          da[a].k.x += kx;
-        }
+        if (STOCH) da[a].k.x += dot_diff<VEC>(ed, fd, ft);
 #pragma unroll
         for (int b = 0; b < K; ++b) {
           if (b == a) continue;
           float fb[VEC];
           io::unpack(sq[(K + b) * kThreads], fb);
-          float kx = 0.f;
-#pragma unroll
-          for (int j = 0; j < VEC; ++j) kx = fmaf(ed[j], fd[j] - fb[j], kx);
-          kk[a][b] += kx;
+          kk[a][b] += dot_diff<VEC>(ed, fd, fb);
         }
       }
     }
