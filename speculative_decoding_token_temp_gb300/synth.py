@@ -176,6 +176,14 @@ def _draw_sequence(rng, gamma: int, V: int, dtype: str, T: float, agreement: flo
     return t_st, d_st, tokens, u_acc
 
 
+def sequence_data(seed: int, b: int, gamma: int, V: int, dtype: str, T: float, agreement: float):
+    """Sequence b of a make_stochastic batch with this seed, on its own (its random stream
+    depends only on (seed, b)): target rows, draft rows, tokens, u_accept, u_sample."""
+    rng = np.random.default_rng([seed, b])
+    t_st, d_st, tok, ua = _draw_sequence(rng, gamma, V, dtype, T, agreement)
+    return t_st, d_st, tok, ua, rng.random(dtype=np.float32)
+
+
 def make_stochastic(B: int, V: int, dtype: str, T: float, seed: int, gamma: int | None = None,
                     gamma_range: tuple[int, int] | None = None, agreement: float = 0.8,
                     name: str = "") -> StochasticWorkload:
@@ -199,15 +207,14 @@ def make_stochastic(B: int, V: int, dtype: str, T: float, seed: int, gamma: int 
     u_acc = np.empty(tot_d, dtype=np.float32)
     u_smp = np.empty(B, dtype=np.float32)
     def one(b):
-        rng = np.random.default_rng([seed, b])
         g = int(gammas[b])
-        t_st, d_st, tok, ua = _draw_sequence(rng, g, V, dtype, T, agreement)
+        t_st, d_st, tok, ua, us = sequence_data(seed, b, g, V, dtype, T, agreement)
         t0, d0 = int(cu[b]) + b, int(cu[b])
         target[t0:t0 + g + 1] = t_st
         draft[d0:d0 + g] = d_st
         tokens[d0:d0 + g] = tok
         u_acc[d0:d0 + g] = ua
-        u_smp[b] = rng.random(dtype=np.float32)
+        u_smp[b] = us
 
     _for_each(one, B)
     return StochasticWorkload(B=B, V=V, dtype=dtype, T=float(T), gammas=gammas, cu_draft=cu,
