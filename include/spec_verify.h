@@ -34,8 +34,13 @@
  *     decision) is bounded and reports SPEC_DEV_TIMEOUT if it runs out.
  *   - Logits are row-major [rows, V] with V contiguous, fp32 or bf16 (raw bf16 bit
  *     patterns). Rows whose byte size is a multiple of 16 and whose base pointers are
- *     16-byte aligned take the vectorised path; any other layout takes a slower scalar
- *     path with the same results.
+ *     16-byte aligned take the vectorised path. Any other layout takes the staged path,
+ *     with the same results: it reads whole aligned 16-byte blocks, so it may read up to
+ *     15 bytes before a row's first or after its last element, always inside a 16-byte
+ *     block that holds one of the row's elements (never used, never written).
+ *   - Every pointer is aligned to its element type: logits to 2 (bf16) or 4 (fp32)
+ *     bytes, int32 and float arrays to 4, the statistics block and double outputs to 8.
+ *     A misaligned pointer is SPEC_ERR_INVALID_ARG.
  *   - Packed batches: sequence b has gamma_b drafts. Its draft rows, draft tokens and
  *     u_accept entries start at cu_draft[b]; its target rows (gamma_b + 1 of them: one
  *     per draft plus the bonus row) and its out_tokens entries start at cu_draft[b] + b.

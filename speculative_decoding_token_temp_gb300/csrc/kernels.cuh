@@ -5,8 +5,9 @@
 //                    every sequence "pending", checks packed offsets.
 //   rows_kernel      one block per (row, vocabulary chunk) tile. Streams the target row
 //                    (and, for a pair, the draft row) once -- on aligned rows through a
-//                    per-thread 3-stage cp.async ring in shared memory, otherwise with
-//                    scalar read-only loads -- and keeps per-thread online statistics: the
+//                    per-thread 3-stage cp.async ring in shared memory, otherwise through a
+//                    block-wide ring of whole aligned 16-byte blocks read back at the row's
+//                    phase -- and keeps per-thread online statistics: the
 //                    raw maximum and its lowest index, sum_v exp((z_v - ref)/T), and for
 //                    the draft row also sum_v exp((zd_v - ref_d)/T) (zd_v - zt_v).
 //                    Block-reduces them into a 32-byte partial. The last tile of a
@@ -14,14 +15,14 @@
 //                    of all its rows and applies the acceptance rule, NKL, greedy or tree
 //                    decision; a stochastic sequence's record for the sampler is published
 //                    with release semantics.
-//   sample2_kernel   (stochastic, aligned rows) one wave of blocks over the B sampled rows
+//   sample2_kernel   (stochastic) one wave of blocks over the B sampled rows
 //                    cut into 512-vector stages; starts while the tile kernel drains, each
 //                    block waiting (bounded) only for its own sequences' records. Slice
 //                    masses of the residual max(0, p - q) (or of p for the bonus row) go to
 //                    a table; the block completing a sequence finds the inverse-CDF
 //                    crossing in the table (exact fixed-point sums) and re-reads one slice.
-//   sample_kernel    (stochastic, misaligned rows) the same draw by segment blocks, after
-//                    the tile kernel has completed.
+//                    Rows off the 16-byte grid stream through the same block-wide ring as
+//                    in the tile kernel.
 // Every kernel is launched with programmatic dependent launch, so its blocks are resident
 // before its predecessor drains, and executes griddepcontrol.wait before its first access
 // to memory that earlier work on the stream reads or writes (the sampler instead polls
@@ -41,8 +42,6 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kMaxRows = SPEC_MAX_GAMMA + 1;
-constexpr int kMaxSteps = 64;        // 256-token steps per warp in one sampling segment
-constexpr int kSegElems = 16384;     // largest sampling segment (kWarps * kMaxSteps * 32 scalar loads)
 constexpr int kTargetTiles = 2432;   // 4 waves of the 608 resident blocks (152 SMs x 4): a partial last wave costs little
 
 // M_STOCH2: stochastic with a draft temperature of its own (the draft row is summed at
@@ -110,10 +109,9 @@ struct RowsParams {
 struct SampleParams {
   const void* target;
   const void* draft;
-  int V, total_rows, total_draft, B, nseg, seg_elems;
+  int V, total_rows, total_draft, B;
   float c, cd;  // target and draft scales, log2(e) / T
   const SeqRec* rec;
-  double* segtot;
   unsigned* cnt;
   int32_t* out_tok;
   uint32_t* status;
@@ -292,6 +290,50 @@ __device__ __forceinline__ float elem_at<float>(const float* row, int x) {
 }
 
 // ---------------------------------------------------------------------------
+// staged path, for rows that do not start on a 16-byte boundary (an offset base pointer,
+// or a row length whose byte size is not a multiple of 16): the block copies the whole
+// aligned 16-byte blocks that cover a stretch of a row into shared memory with cp.async,
+// and every thread then reads single elements at the stretch's phase. The first and last
+// block may reach up to 15 bytes before the stretch's first element or after its last;
+// each block holds at least one element of the stretch, so it lies on the same mapped
+// page, and the extra bytes are never used.
+
+constexpr int kStageRowBytes = 8192;                 // one row of a pair in one stage (twice that for a single row)
+constexpr int kStageSlot = kStageRowBytes + 16;      // with room for the phase
+constexpr int kStagedSmem = kCS * 2 * kStageSlot;    // dynamic shared memory of the staged path
+
+// Elements of the 16-byte block holding p that precede p.
+template <typename E>
+__device__ __forceinline__ int phase16(const E* p) {
+  return (int)((reinterpret_cast<uintptr_t>(p) & 15u) / sizeof(E));
+}
+
+// Block-wide: copies the blocks covering elements [e0, e0 + n) of `row` to the shared
+// address dst, thread t taking blocks t, t + kThreads, ...; element e0 + x then sits at
+// element phase16(row + e0) + x of the copy.
+template <typename E>
+__device__ __forceinline__ void stage_copy(uint32_t dst, const E* row, int e0, int n) {
+  if (n <= 0) return;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(row + e0);
+  const uintptr_t b0 = a0 & ~(uintptr_t)15;
+  const int nb = (int)(((a0 + (uintptr_t)n * sizeof(E) - 1) >> 4) - (b0 >> 4)) + 1;
+  for (int j = threadIdx.x; j < nb; j += kThreads)
+    cp_async16(dst + 16u * (uint32_t)j, reinterpret_cast<const void*>(b0 + 16u * (uintptr_t)j));
+}
+
+// one element of a staged copy, as float
+template <typename E>
+__device__ __forceinline__ float sh_elem(const E* s, int x);
+template <>
+__device__ __forceinline__ float sh_elem<uint16_t>(const uint16_t* s, int x) {
+  return __uint_as_float(((unsigned)s[x]) << 16);
+}
+template <>
+__device__ __forceinline__ float sh_elem<float>(const float* s, int x) {
+  return s[x];
+}
+
+// ---------------------------------------------------------------------------
 // packed arithmetic: two fp32 lanes per instruction (sm_100 family), 3-input min/max
 
 // the compiler's float2 builtins (sm_100 family) pair the operands in registers itself
@@ -433,11 +475,16 @@ __device__ __forceinline__ float2 exp_sum2(const float (&t)[VEC], float c, float
 // Exact max. A single-element group (scalar path) records its index directly; a wider
 // group only records where it starts, and the lowest index inside it is found once, at
 // the end of the tile, by the thread that holds the tile's maximum (resolve_index).
+// H == 0 marks a strided group (staged path): its VEC elements sit at e0 + k * kThreads,
+// and g1 records their count (resolve_strided).
 template <int VEC, int H, bool IDX>
 __device__ __forceinline__ void track_max(TAcc& a, const float (&t)[VEC], float vm, int e0, int e1) {
   if (IDX) {
     if (vm > a.m) {
-      if constexpr (VEC == 1) {
+      if constexpr (H == 0) {
+        a.g0 = e0;
+        a.g1 = VEC;
+      } else if constexpr (VEC == 1) {
         a.idx = e0;
       } else {
         a.g0 = e0;
@@ -566,9 +613,20 @@ __device__ __forceinline__ int resolve_index(const E* row, int g0, int g1, float
   return INT_MAX;
 }
 
-// row != nullptr: the target maximum's index is resolved from the recorded groups.
-// SEPT: the draft sum s is at scale cd, s2 and k at c.
-template <class SY, typename E = float, int VEC = 1, bool SEPT = false>
+// Lowest index of the value m among the g1 elements g0, g0 + GS, ... of a strided group
+// (staged path), re-read one by one from the row.
+template <typename E, int GS>
+__device__ __forceinline__ int resolve_strided(const E* row, int g0, int g1, float m) {
+  if (g0 < 0) return INT_MAX;
+  for (int k = 0; k < g1; ++k)
+    if (elem_at<E>(row, g0 + k * GS) == m) return g0 + k * GS;
+  return INT_MAX;
+}
+
+// row != nullptr: the target maximum's index is resolved from the recorded groups
+// (strided groups of stride GS when GS > 0). SEPT: the draft sum s is at scale cd, s2
+// and k at c.
+template <class SY, typename E = float, int VEC = 1, bool SEPT = false, int GS = 0>
 __device__ __forceinline__ Partial reduce_tile(int kind, const TAcc& ta, const DAcc& da, float c,
                                                const E* row = nullptr, float cd = 0.f) {
   constexpr int NW = SY::NT / 32;
@@ -591,7 +649,9 @@ __device__ __forceinline__ Partial reduce_tile(int kind, const TAcc& ta, const D
   }
   int my_idx = INT_MAX;
   if (ta.m == TM) {
-    if constexpr (VEC > 1)
+    if constexpr (GS > 0)
+      my_idx = row ? resolve_strided<E, GS>(row, ta.g0, ta.g1, TM) : INT_MAX;
+    else if constexpr (VEC > 1)
       my_idx = row ? resolve_index<E, VEC>(row, ta.g0, ta.g1, TM) : INT_MAX;
     else
       my_idx = ta.idx;

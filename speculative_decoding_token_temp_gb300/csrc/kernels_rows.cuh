@@ -418,10 +418,85 @@ __device__ __forceinline__ void stream_tile(const E* trow, const E* drow, int v0
   cp_wait<0>();
 }
 
+// Staged path: the tile [e_begin, e_end) in stages of kStageRowBytes per row of a pair
+// (twice that for a single row) through a block-wide kCS-slot ring of whole aligned
+// 16-byte blocks (stage_copy), with one barrier per stage. Thread t takes elements
+// t, t + kThreads, ... of each stage (consecutive lanes read consecutive elements, so the
+// shared-memory reads are conflict free), folded in as strided groups of kGroup.
+constexpr int kGroup = 8;
+
+template <typename E, int MODE, int KIND>
+__device__ __forceinline__ void stream_staged(const E* trow, const E* drow, int e_begin, int e_end, float c, float cd,
+                                              TAcc& ta, DAcc& da, unsigned char* smem) {
+  constexpr bool IDX = is_stoch(MODE), SEPT = MODE == M_STOCH2, PAIR = KIND == K_PAIR;
+  constexpr int S = (PAIR ? kStageRowBytes : 2 * kStageRowBytes) / (int)sizeof(E);  // elements of a row per stage
+  constexpr int NG = S / (kGroup * kThreads);                                         // groups per thread per stage
+  constexpr unsigned SLOT = 2 * kStageSlot;
+  static_assert(S % (kGroup * kThreads) == 0, "stage of whole groups");
+  const int t = threadIdx.x;
+  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem);
+  const int nst = (e_end - e_begin + S - 1) / S;
+  // S * sizeof(E) is a multiple of 16: every stage of a row has the same phase
+  const int ph_t = phase16(trow + e_begin), ph_d = PAIR ? phase16(drow + e_begin) : 0;
+  auto issue = [&](int k) {
+    if (k < nst) {
+      const uint32_t slot = sbase + (uint32_t)(k % kCS) * SLOT;
+      const int e0 = e_begin + k * S, n = min(S, e_end - e0);
+      stage_copy<E>(slot, trow, e0, n);
+      if constexpr (PAIR) stage_copy<E>(slot + kStageSlot, drow, e0, n);
+    }
+    cp_commit();
+  };
+#pragma unroll
+  for (int k = 0; k < kCS - 1; ++k) issue(k);
+  for (int k = 0; k < nst; ++k) {
+    cp_wait<kCS - 2>();  // this thread's copies of stage k have landed
+    __syncthreads();     // ... and every thread's; every thread is done with stage k - 1
+    issue(k + kCS - 1);  // into the slot of stage k - 1
+    const unsigned char* slot = smem + (size_t)(k % kCS) * SLOT;
+    const E* sT = reinterpret_cast<const E*>(slot) + ph_t;
+    const E* sD = reinterpret_cast<const E*>(slot + kStageSlot) + ph_d;
+    const int eb = e_begin + k * S, n = min(S, e_end - eb);
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      const int x0 = g * kGroup * kThreads + t;  // this thread's first element of the group
+      if ((g + 1) * kGroup * kThreads <= n) {    // the whole group is inside the stage, for every thread
+        float ft[kGroup], fd[kGroup];
+#pragma unroll
+        for (int j = 0; j < kGroup; ++j) {
+          ft[j] = sh_elem<E>(sT, x0 + j * kThreads);
+          if constexpr (PAIR) fd[j] = sh_elem<E>(sD, x0 + j * kThreads);
+        }
+        if constexpr (PAIR)
+          pair_update<kGroup, IDX, 0, SEPT>(ta, da, ft, fd, eb + x0, c, 0, cd);
+        else if constexpr (KIND == K_TSUM)
+          tsum_update<kGroup, 0>(ta, ft, eb + x0, c);
+        else
+          argmax_update<kGroup, 0>(ta, ft, eb + x0);
+      } else {
+        for (int j = 0; j < kGroup; ++j) {
+          const int x = x0 + j * kThreads;
+          if (x < n) {
+            float ft[1], fd[1];
+            ft[0] = sh_elem<E>(sT, x);
+            if constexpr (PAIR) {
+              fd[0] = sh_elem<E>(sD, x);
+              pair_update<1, IDX, 0, SEPT>(ta, da, ft, fd, eb + x, c, 0, cd);
+            } else if constexpr (KIND == K_TSUM) {
+              tsum_update<1, 0>(ta, ft, eb + x, c);
+            } else {
+              argmax_update<1, 0>(ta, ft, eb + x);
+            }
+          }
+        }
+      }
+    }
+  }
+  cp_wait<0>();
+}
+
 template <typename E, int VEC, int MODE>
 __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant__ RowsParams p) {
-  using io = IO<E, VEC>;
-  using raw_t = typename io::raw_t;
   constexpr int HB = (MODE == M_NKL) ? 0 : 1;
   extern __shared__ __align__(128) unsigned char dsm[];
   // Nothing is read or written before the prologue -- and with it everything earlier on
@@ -500,63 +575,23 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
         stream_tile<E, VEC, MODE, K_TSUM>(trow, drow, e_begin / VEC, v1, c, cd, ta, da, dsm);
     }
   } else {
-  int v = e_begin / VEC + threadIdx.x;
-  if (kind == K_PAIR) {
-    for (; v + kThreads < v1; v += 2 * kThreads) {
-      const raw_t t0 = io::load(trow, v), t1 = io::load(trow, v + kThreads);
-      const raw_t d0 = io::load(drow, v), d1 = io::load(drow, v + kThreads);
-      float ft[VEC], fd[VEC];
-      io::unpack(t0, ft);
-      io::unpack(d0, fd);
-      pair_update<VEC, IDX, VEC, SEPT>(ta, da, ft, fd, v * VEC, c, 0, cd);
-      io::unpack(t1, ft);
-      io::unpack(d1, fd);
-      pair_update<VEC, IDX, VEC, SEPT>(ta, da, ft, fd, (v + kThreads) * VEC, c, 0, cd);
+    if constexpr (MODE == M_GREEDY || MODE == M_TREE) {
+      stream_staged<E, MODE, K_ARGMAX>(trow, drow, e_begin, e_end, c, cd, ta, da, dsm);
+    } else if constexpr (MODE == M_NKL) {
+      stream_staged<E, MODE, K_PAIR>(trow, drow, e_begin, e_end, c, cd, ta, da, dsm);
+    } else {
+      if (kind == K_PAIR)
+        stream_staged<E, MODE, K_PAIR>(trow, drow, e_begin, e_end, c, cd, ta, da, dsm);
+      else
+        stream_staged<E, MODE, K_TSUM>(trow, drow, e_begin, e_end, c, cd, ta, da, dsm);
     }
-    if (v < v1) {
-      float ft[VEC], fd[VEC];
-      io::unpack(io::load(trow, v), ft);
-      io::unpack(io::load(drow, v), fd);
-      pair_update<VEC, IDX, VEC, SEPT>(ta, da, ft, fd, v * VEC, c, 0, cd);
-    }
-  } else if (kind == K_TSUM) {
-    for (; v + 3 * kThreads < v1; v += 4 * kThreads) {
-      raw_t t[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) t[u] = io::load(trow, v + u * kThreads);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        float ft[VEC];
-        io::unpack(t[u], ft);
-        tsum_update<VEC>(ta, ft, (v + u * kThreads) * VEC, c);
-      }
-    }
-    for (; v < v1; v += kThreads) {
-      float ft[VEC];
-      io::unpack(io::load(trow, v), ft);
-      tsum_update<VEC>(ta, ft, v * VEC, c);
-    }
-  } else {
-    for (; v + 3 * kThreads < v1; v += 4 * kThreads) {
-      raw_t t[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) t[u] = io::load(trow, v + u * kThreads);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        float ft[VEC];
-        io::unpack(t[u], ft);
-        argmax_update<VEC>(ta, ft, (v + u * kThreads) * VEC);
-      }
-    }
-    for (; v < v1; v += kThreads) {
-      float ft[VEC];
-      io::unpack(io::load(trow, v), ft);
-      argmax_update<VEC>(ta, ft, v * VEC);
-    }
-  }
   }
 
-  const Partial part = reduce_tile<BlockSync, E, VEC, SEPT>(kind, ta, da, c, trow, cd);
+  Partial part;
+  if constexpr (VEC > 1)
+    part = reduce_tile<BlockSync, E, VEC, SEPT>(kind, ta, da, c, trow, cd);
+  else
+    part = reduce_tile<BlockSync, E, 1, SEPT, kThreads>(kind, ta, da, c, trow, cd);
   if (threadIdx.x == 0) {
     float4* dst = reinterpret_cast<float4*>(p.part + tile);
     __stcg(dst, make_float4(part.tm, part.ts, __int_as_float(part.tidx), __int_as_float(part.bad)));

@@ -12,6 +12,7 @@
 #include "spec_verify.h"
 
 #include <atomic>
+#include <initializer_list>
 
 namespace sv {
 namespace {
@@ -31,20 +32,9 @@ void chunking(int V, long long rows, int max_chunk, int* nchunks, int* chunk_ele
   *nchunks = (int)ceil_div(V, ce);
 }
 
-// Sampling segments: at most kSegElems tokens (so a warp's step table fits), more while
-// the sampling grid is small.
-void segmenting(int V, int B, int* nseg, int* seg_elems) {
-  long long ns = ceil_div(V, kSegElems);
-  const long long want = ceil_div(kTargetTiles, B > 0 ? B : 1);
-  while (ns < want && V / (ns + 1) >= 2048) ++ns;
-  long long se = ceil_div(ceil_div(V, ns), 8) * 8;
-  *seg_elems = (int)se;
-  *nseg = (int)ceil_div(V, se);
-}
-
 struct Layout {
-  size_t cntA, cntB, rec, part, segtot, table, total;
-  int nchunks, chunk_elems, nseg, seg_elems, table_stride;
+  size_t cntA, cntB, rec, part, table, total;
+  int nchunks, chunk_elems, table_stride;
   long long rows;
 };
 
@@ -63,10 +53,6 @@ Layout layout(int B, int V, long long rows, bool sample, bool single_rows = fals
   L.rows = rows;
   chunking(V, rows > 0 ? rows : 1, max_chunk > 0 ? max_chunk : (single_rows ? 65536 : 32768), &L.nchunks,
            &L.chunk_elems);
-  if (sample)
-    segmenting(V, B, &L.nseg, &L.seg_elems);
-  else
-    L.nseg = L.seg_elems = 0;
   size_t off = 0;
   L.cntA = off;  // B tickets, then the count of finished tiles
   off = align256(off + sizeof(unsigned) * ((size_t)B + 1));
@@ -76,8 +62,6 @@ Layout layout(int B, int V, long long rows, bool sample, bool single_rows = fals
   off = align256(off + sizeof(SeqRec) * (size_t)B);
   L.part = off;
   off = align256(off + sizeof(Partial) * (size_t)(rows * L.nchunks));
-  L.segtot = off;
-  off = align256(off + sizeof(double) * (size_t)B * (size_t)L.nseg);
   L.table_stride = sample ? table_stride_for(V, dt) : 0;
   L.table = off;
   off = align256(off + sizeof(float) * (size_t)B * (size_t)L.table_stride);
@@ -91,6 +75,15 @@ long long rows_for(spec_mode mode, const spec_batch& g) {
 }
 
 bool aligned16(const void* p) { return p == nullptr || ((uintptr_t)p & 15u) == 0; }
+
+// every non-null pointer of the list on an n-byte boundary (its element size)
+bool aligned_to(size_t n, std::initializer_list<const void*> ps) {
+  for (const void* p : ps)
+    if (p != nullptr && ((uintptr_t)p % n) != 0) return false;
+  return true;
+}
+
+size_t elem_bytes(spec_dtype dt) { return dt == SPEC_BF16 ? 2 : 4; }
 
 spec_status check_batch(const spec_batch& g) {
   if (g.B < 0 || g.V < 1 || g.gamma < 0 || g.gamma > SPEC_MAX_GAMMA || g.total_draft < 0) return SPEC_ERR_INVALID_ARG;
@@ -181,12 +174,10 @@ cudaError_t ensure_smem_attr(K kernel, std::atomic<unsigned long long>& done, in
 template <typename E, int VEC, int MODE>
 cudaError_t launch_rows_t(const RowsParams& rp, long long tiles, cudaStream_t stream) {
   auto kern = rows_kernel<E, VEC, MODE>;
-  const int smem = VEC > 1 ? kRowsSmem : 0;
-  if (smem) {
-    static std::atomic<unsigned long long> done{0};
-    const cudaError_t e = ensure_smem_attr(kern, done, smem);
-    if (e != cudaSuccess) return e;
-  }
+  const int smem = VEC > 1 ? kRowsSmem : kStagedSmem;
+  static std::atomic<unsigned long long> done{0};
+  const cudaError_t e = ensure_smem_attr(kern, done, smem);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3((unsigned)tiles);
@@ -207,27 +198,18 @@ cudaError_t launch_rows(bool bf16, bool vec, const RowsParams& rp, long long til
   return vec ? launch_rows_t<float, 4, MODE>(rp, tiles, stream) : launch_rows_t<float, 1, MODE>(rp, tiles, stream);
 }
 
-cudaError_t launch_sample(bool bf16, bool vec, const SampleParams& sp, long long blocks, cudaStream_t stream) {
-  const dim3 grid((unsigned)blocks), block(kThreads);
-  if (bf16) {
-    if (vec) return launch_pdl(sample_kernel<uint16_t, 8>, grid, block, stream, sp);
-    return launch_pdl(sample_kernel<uint16_t, 1>, grid, block, stream, sp);
-  }
-  if (vec) return launch_pdl(sample_kernel<float, 4>, grid, block, stream, sp);
-  return launch_pdl(sample_kernel<float, 1>, grid, block, stream, sp);
-}
-
-template <typename E, int VEC>
+template <typename E, int VEC, bool STAGED>
 cudaError_t launch_sample2_t(const SampleParams& sp, long long blocks, cudaStream_t stream) {
-  auto kern = sample2_kernel<E, VEC>;
+  auto kern = sample2_kernel<E, VEC, STAGED>;
+  const int smem = STAGED ? kStagedSmem : kRowsSmem;
   static std::atomic<unsigned long long> done{0};
-  const cudaError_t e = ensure_smem_attr(kern, done, kRowsSmem);
+  const cudaError_t e = ensure_smem_attr(kern, done, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3((unsigned)blocks);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = (size_t)kRowsSmem;
+  cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -237,8 +219,11 @@ cudaError_t launch_sample2_t(const SampleParams& sp, long long blocks, cudaStrea
   return cudaLaunchKernelEx(&cfg, kern, sp);
 }
 
-cudaError_t launch_sample2(bool bf16, const SampleParams& sp, long long blocks, cudaStream_t stream) {
-  return bf16 ? launch_sample2_t<uint16_t, 8>(sp, blocks, stream) : launch_sample2_t<float, 4>(sp, blocks, stream);
+cudaError_t launch_sample2(bool bf16, bool vec, const SampleParams& sp, long long blocks, cudaStream_t stream) {
+  if (bf16)
+    return vec ? launch_sample2_t<uint16_t, 8, false>(sp, blocks, stream)
+               : launch_sample2_t<uint16_t, 8, true>(sp, blocks, stream);
+  return vec ? launch_sample2_t<float, 4, false>(sp, blocks, stream) : launch_sample2_t<float, 4, true>(sp, blocks, stream);
 }
 
 // Fused multi-draft tiles: when given, the verification launches multi_rows_kernel over
@@ -321,6 +306,8 @@ spec_status check_options(const spec_options* o, spec_mode mode) {
     if (o->min_block_len < 0) return SPEC_ERR_INVALID_ARG;
     if (o->min_block_len > 0 && (!o->block_n || !o->block_tokens)) return SPEC_ERR_INVALID_ARG;
   }
+  if (!aligned_to(4, {o->position, o->block_n, o->block_tokens}) || !aligned_to(8, {o->stats}))
+    return SPEC_ERR_INVALID_ARG;
   return SPEC_OK;
 }
 
@@ -359,6 +346,10 @@ spec_status stochastic_impl(spec_batch g, spec_dtype dtype, const void* target_l
   if (!target_logits || !n_accepted || !out_tokens || !u_sample || !device_status) return SPEC_ERR_INVALID_ARG;
   if (g.total_draft > 0 && (!draft_logits || !draft_tokens || !u_accept)) return SPEC_ERR_INVALID_ARG;
   if ((greedy_n == nullptr) != (greedy_tokens == nullptr)) return SPEC_ERR_INVALID_ARG;
+  if (!aligned_to(elem_bytes(dtype), {target_logits, draft_logits}) ||
+      !aligned_to(4, {draft_tokens, u_accept, u_sample, n_accepted, out_tokens, p_x, q_x, alpha, nkl, greedy_n,
+                      greedy_tokens, device_status, g.cu_draft}))
+    return SPEC_ERR_INVALID_ARG;
   const Layout L = layout(g.B, g.V, rows_for(SPEC_MODE_STOCHASTIC, g), true, false, dtype, mt ? kMultiChunk : 0);
   if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u)) return SPEC_ERR_WORKSPACE;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
@@ -404,12 +395,9 @@ spec_status stochastic_impl(spec_batch g, spec_dtype dtype, const void* target_l
   sp.total_rows = (int)L.rows;
   sp.total_draft = g.total_draft;
   sp.B = g.B;
-  sp.nseg = L.nseg;
-  sp.seg_elems = L.seg_elems;
   sp.c = rp.c;
   sp.cd = rp.cd;
   sp.rec = rp.rec;
-  sp.segtot = reinterpret_cast<double*>(ws + L.segtot);
   sp.cnt = reinterpret_cast<unsigned*>(ws + L.cntB);
   sp.out_tok = out_tokens;
   sp.status = device_status;
@@ -417,31 +405,27 @@ spec_status stochastic_impl(spec_batch g, spec_dtype dtype, const void* target_l
   sp.table_stride = L.table_stride;
   sp.tiles_done = reinterpret_cast<const unsigned*>(ws + L.cntA) + g.B;
   sp.ntiles = (unsigned)tiles;
-  if (vec) {
-    // aligned rows: one wave of blocks over the B * nst stages. The last kTailSeqs
-    // sequences (decided last by the tile kernel) take short ranges of at least
-    // kTailStages stages on at most a quarter of the wave, the others equal long ranges.
-    const int nv = g.V / (bf16 ? 8 : 4);
-    const long long nst = ceil_div(nv, 2 * kThreads);
-    const long long tail_seqs = g.B < kTailSeqs ? g.B : kTailSeqs;
-    const long long tail_total = tail_seqs * nst, head_total = ((long long)g.B - tail_seqs) * nst;
-    long long seg_tail = ceil_div(tail_total, kWaveBlocks / 4);
-    if (seg_tail < kTailStages) seg_tail = kTailStages;
-    const long long nb_tail = ceil_div(tail_total, seg_tail);
-    long long nb_head = 0, seg_head = 1;
-    if (head_total > 0) {
-      const long long room = kWaveBlocks - nb_tail;
-      seg_head = ceil_div(head_total, room < 1 ? 1 : room);
-      nb_head = ceil_div(head_total, seg_head);
-    }
-    sp.head_total = head_total;
-    sp.nb_head = (int)nb_head;
-    sp.seg_head = (int)seg_head;
-    sp.seg_tail = (int)seg_tail;
-    if (launch_sample2(bf16, sp, nb_head + nb_tail, stream) != cudaSuccess) return SPEC_ERR_CUDA;
-    return SPEC_OK;
+  // One wave of blocks over the B * nst stages. The last kTailSeqs sequences (decided last
+  // by the tile kernel) take short ranges of at least kTailStages stages on at most a
+  // quarter of the wave, the others equal long ranges.
+  const long long nv = ceil_div(g.V, bf16 ? 8 : 4);
+  const long long nst = ceil_div(nv, 2 * kThreads);
+  const long long tail_seqs = g.B < kTailSeqs ? g.B : kTailSeqs;
+  const long long tail_total = tail_seqs * nst, head_total = ((long long)g.B - tail_seqs) * nst;
+  long long seg_tail = ceil_div(tail_total, kWaveBlocks / 4);
+  if (seg_tail < kTailStages) seg_tail = kTailStages;
+  const long long nb_tail = ceil_div(tail_total, seg_tail);
+  long long nb_head = 0, seg_head = 1;
+  if (head_total > 0) {
+    const long long room = kWaveBlocks - nb_tail;
+    seg_head = ceil_div(head_total, room < 1 ? 1 : room);
+    nb_head = ceil_div(head_total, seg_head);
   }
-  if (launch_sample(bf16, vec, sp, (long long)g.B * L.nseg, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  sp.head_total = head_total;
+  sp.nb_head = (int)nb_head;
+  sp.seg_head = (int)seg_head;
+  sp.seg_tail = (int)seg_tail;
+  if (launch_sample2(bf16, vec, sp, nb_head + nb_tail, stream) != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;
 }
 
@@ -457,6 +441,9 @@ spec_status greedy_impl(spec_batch g, spec_dtype dtype, const void* target_logit
   if (g.B == 0) return SPEC_OK;
   if (!target_logits || !n_accepted || !out_tokens || !device_status) return SPEC_ERR_INVALID_ARG;
   if (g.total_draft > 0 && !draft_tokens) return SPEC_ERR_INVALID_ARG;
+  if (!aligned_to(elem_bytes(dtype), {target_logits}) ||
+      !aligned_to(4, {draft_tokens, n_accepted, out_tokens, device_status, g.cu_draft}))
+    return SPEC_ERR_INVALID_ARG;
   const Layout L = layout(g.B, g.V, rows_for(SPEC_MODE_GREEDY, g), false, true, SPEC_F32, mt ? kMultiChunk : 0);
   if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u)) return SPEC_ERR_WORKSPACE;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
@@ -624,6 +611,9 @@ spec_status spec_verify_tree(int32_t B, int32_t N, int32_t V, spec_dtype dtype, 
   if (B == 0) return SPEC_OK;
   if (!target_logits || !node_tokens || !accept_len || !path_nodes || !out_tokens || !device_status)
     return SPEC_ERR_INVALID_ARG;
+  if (!aligned_to(elem_bytes(dtype), {target_logits}) ||
+      !aligned_to(4, {node_tokens, accept_len, path_nodes, out_tokens, device_status}))
+    return SPEC_ERR_INVALID_ARG;
   spec_batch g;
   g.B = B;
   g.gamma = N;
@@ -669,6 +659,8 @@ spec_status spec_nkl_ex(spec_batch g, spec_dtype dtype, const void* target_logit
   if (st != SPEC_OK) return st;
   if (g.B == 0 || g.total_draft == 0) return SPEC_OK;
   if (!target_logits || !draft_logits || !nkl || !device_status) return SPEC_ERR_INVALID_ARG;
+  if (!aligned_to(elem_bytes(dtype), {target_logits, draft_logits}) || !aligned_to(4, {nkl, device_status, g.cu_draft}))
+    return SPEC_ERR_INVALID_ARG;
   const Layout L = layout(g.B, g.V, rows_for(SPEC_MODE_NKL, g), false);
   if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u)) return SPEC_ERR_WORKSPACE;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
@@ -711,6 +703,10 @@ spec_status spec_verify_multi(spec_multi_batch m, spec_dtype dtype, int32_t stoc
     return SPEC_ERR_INVALID_ARG;
   if (m.gamma > 0 && (!draft_logits || !draft_tokens)) return SPEC_ERR_INVALID_ARG;
   if (stochastic && (!u_sample || (m.gamma > 0 && !u_accept))) return SPEC_ERR_INVALID_ARG;
+  if (!aligned_to(elem_bytes(dtype), {target_logits, draft_logits}) ||
+      !aligned_to(4, {draft_tokens, u_accept, u_sample, n_accepted, out_tokens, best_k, best_n, best_tokens, pair_nkl,
+                      device_status}))
+    return SPEC_ERR_INVALID_ARG;
   const MultiLayout ML = multi_layout(m, dtype, stochastic != 0);
   if (!workspace || workspace_bytes < ML.total || ((uintptr_t)workspace & 255u)) return SPEC_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
@@ -779,7 +775,8 @@ spec_status spec_verify_multi(spec_multi_batch m, spec_dtype dtype, int32_t stoc
 
 spec_status spec_accept_summary(const spec_accept_stats* stats, int64_t bucket_now, int32_t window, double* out,
                                 spec_stream_t stream_) {
-  if (!stats || !out || window < 1 || window > SPEC_STATS_SLOTS) return SPEC_ERR_INVALID_ARG;
+  if (!stats || !out || window < 1 || window > SPEC_STATS_SLOTS || !aligned_to(8, {stats, out}))
+    return SPEC_ERR_INVALID_ARG;
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3(1);

@@ -15,22 +15,29 @@ def to_dev(a, dev):
     return torch.from_numpy(a).to(dev)
 
 
+def put(a, dev, offset=0):
+    """A device copy of `a` that starts `offset` elements into its buffer (offset > 0 puts
+    the rows off the 16-byte grid: the staged path)."""
+    if offset == 0:
+        return to_dev(a, dev)
+    flat = to_dev(np.ascontiguousarray(a).reshape(-1), dev)
+    buf = torch.empty(flat.numel() + offset, dtype=flat.dtype, device=dev)
+    buf[offset:] = flat
+    return buf[offset:].view(a.shape)
+
+
+def _offsets(offset):
+    return offset if isinstance(offset, tuple) else (offset, offset)
+
+
 def run_stochastic(w, dev, T=None, delta=0.15, offset=0, options=None):
     """Call spec_verify_stochastic (spec_verify_stochastic_ex when `options` is given: a
-    dict of its keywords, numpy arrays for position) on a workload; offset > 0 shifts the
-    logit buffers by that many elements (misaligned base pointers force the scalar path)."""
+    dict of its keywords, numpy arrays for position) on a workload; offset (an int, or a
+    (target, draft) pair) shifts the logit buffers by that many elements."""
     T = w.T if T is None else T
-
-    def put(a):
-        if offset == 0:
-            return to_dev(a, dev)
-        flat = to_dev(np.ascontiguousarray(a).reshape(-1), dev)
-        buf = torch.empty(flat.numel() + offset, dtype=flat.dtype, device=dev)
-        buf[offset:] = flat
-        return buf[offset:].view(a.shape)
-
-    t = put(w.target)
-    d = put(w.draft)
+    ot, od = _offsets(offset)
+    t = put(w.target, dev, ot)
+    d = put(w.draft, dev, od)
     cu = None if w.dense else torch.from_numpy(w.cu_draft).to(dev)
     kw = dict(cu_draft=cu, gamma=w.gamma_max if not w.dense else int(w.gammas[0]) if w.B else 0, nkl_delta=delta)
     if options is None:
@@ -93,13 +100,14 @@ def compare_stochastic(w, res, seqs, T=None, delta=0.15, check_greedy=True, T_dr
     return len(seqs), flagged, mismatched
 
 
-def run_greedy(w, dev, options=None):
+def run_greedy(w, dev, options=None, offset=0):
     cu = None if w.dense else torch.from_numpy(w.cu_draft).to(dev)
     kw = dict(cu_draft=cu, gamma=w.gamma_max if not w.dense else int(w.gammas[0]))
+    t = put(w.target, dev, offset)
     if options is None:
-        res = api.spec_verify_greedy(to_dev(w.target, dev), to_dev(w.tokens, dev), **kw)
+        res = api.spec_verify_greedy(t, to_dev(w.tokens, dev), **kw)
     else:
-        res = api.spec_verify_greedy_ex(to_dev(w.target, dev), to_dev(w.tokens, dev), **kw, **options)
+        res = api.spec_verify_greedy_ex(t, to_dev(w.tokens, dev), **kw, **options)
     torch.cuda.synchronize()
     return {k: v.cpu().numpy() for k, v in res.items()}
 
@@ -117,14 +125,16 @@ def compare_greedy(w, res, seqs, min_block_len=0):
             assert list(res["block_tokens"][d0:d0 + g]) == list(ref[b]["block_tokens"]), b
 
 
-def run_nkl(w, dev, delta=0.15, positions=None):
+def run_nkl(w, dev, delta=0.15, positions=None, offset=0):
     cu = None if w.dense else torch.from_numpy(w.cu_draft).to(dev)
     kw = dict(cu_draft=cu, gamma=w.gamma_max if not w.dense else int(w.gammas[0]), delta=delta)
+    ot, od = _offsets(offset)
+    t, d = put(w.target, dev, ot), put(w.draft, dev, od)
     if positions is None:
-        res = api.spec_nkl(to_dev(w.target, dev), to_dev(w.draft, dev), w.T, **kw)
+        res = api.spec_nkl(t, d, w.T, **kw)
     else:
         pos = torch.from_numpy(np.asarray(positions, dtype=np.int32)).to(dev)
-        res = api.spec_nkl_ex(to_dev(w.target, dev), to_dev(w.draft, dev), w.T, position=pos, **kw)
+        res = api.spec_nkl_ex(t, d, w.T, position=pos, **kw)
     torch.cuda.synchronize()
     return {k: v.cpu().numpy() for k, v in res.items()}
 
@@ -143,8 +153,8 @@ def compare_nkl(w, res, seqs, delta=0.15, positions=None):
         assert np.all((m == ref[b]["mask"]) | near), (b, m, ref[b]["mask"])
 
 
-def run_tree(w, dev):
-    res = api.spec_verify_tree(to_dev(w.target, dev), to_dev(w.node_tokens, dev), list(w.parent))
+def run_tree(w, dev, offset=0):
+    res = api.spec_verify_tree(put(w.target, dev, offset), to_dev(w.node_tokens, dev), list(w.parent))
     torch.cuda.synchronize()
     return {k: v.cpu().numpy() for k, v in res.items()}
 

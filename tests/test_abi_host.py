@@ -86,6 +86,21 @@ def test_host_validation_without_launch(lib):
     assert lib.spec_verify_greedy(g, 5, one, one, one, one, one, one, 1 << 30, None) == _lib.SPEC_ERR_DTYPE
     assert lib.spec_nkl(g, _lib.SPEC_F32, one, one, 0.0, 0.15, one, None, one, one, 1 << 30, None) == \
         _lib.SPEC_ERR_INVALID_ARG
+    # every pointer on its element's grid
+    assert stoch(g, target=P(257)) == _lib.SPEC_ERR_INVALID_ARG                    # bf16 logits: 2 bytes
+    assert stoch(g, dt=_lib.SPEC_F32, target=P(258)) == _lib.SPEC_ERR_INVALID_ARG  # fp32 logits: 4 bytes
+    assert stoch(g, status=P(258)) == _lib.SPEC_ERR_INVALID_ARG                    # 32-bit words: 4 bytes
+    assert lib.spec_verify_greedy(g, _lib.SPEC_BF16, P(257), one, one, one, one, one, 1 << 30, None) == \
+        _lib.SPEC_ERR_INVALID_ARG
+    assert lib.spec_verify_greedy(g, _lib.SPEC_BF16, one, P(258), one, one, one, one, 1 << 30, None) == \
+        _lib.SPEC_ERR_INVALID_ARG
+    assert lib.spec_nkl(g, _lib.SPEC_F32, one, P(258), 0.7, 0.15, one, None, one, one, 1 << 30, None) == \
+        _lib.SPEC_ERR_INVALID_ARG
+    chain = (ctypes.c_int32 * 2)(-1, 0)
+    assert lib.spec_verify_tree(2, 2, 100, _lib.SPEC_BF16, P(257), one, ctypes.cast(chain, P), one, one, one,
+                                one, one, 1 << 30, None) == _lib.SPEC_ERR_INVALID_ARG
+    out = (ctypes.c_double * 6)()
+    assert lib.spec_accept_summary(P(260), 0, 4, ctypes.cast(out, P), None) == _lib.SPEC_ERR_INVALID_ARG
     bad_parent = (ctypes.c_int32 * 2)(-1, 5)
     assert lib.spec_verify_tree(2, 2, 100, _lib.SPEC_BF16, one, one, ctypes.cast(bad_parent, P), one, one, one,
                                 one, one, 1 << 30, None) == _lib.SPEC_ERR_INVALID_ARG
@@ -128,6 +143,12 @@ def test_option_checks_without_launch(lib):
     assert lib.spec_accept_summary(one, 5, 0, one, None) == _lib.SPEC_ERR_INVALID_ARG
     assert lib.spec_accept_summary(one, 5, _lib.SPEC_STATS_SLOTS + 1, one, None) == _lib.SPEC_ERR_INVALID_ARG
     assert lib.spec_accept_summary(None, 5, 4, one, None) == _lib.SPEC_ERR_INVALID_ARG
+    o = _lib.SpecOptions()
+    o.position = 258                                       # int32 array off its 4-byte grid
+    assert stoch(o) == _lib.SPEC_ERR_INVALID_ARG
+    o = _lib.SpecOptions()
+    o.stats = 260                                          # 64-bit counters off their 8-byte grid
+    assert greedy(o) == _lib.SPEC_ERR_INVALID_ARG
 
 
 def test_option_structs_match_the_header(tmp_path):

@@ -120,11 +120,71 @@ def test_odd_vocab_sizes(dev, V, dtype):
     compare_nkl(w, run_nkl(w, dev), range(w.B))
 
 
-@pytest.mark.parametrize("offset", [1, 3])
-def test_misaligned_buffers_take_scalar_path(dev, offset):
-    w = handmade(4, 5, 4096, synth.BF16, T=0.7, seed=11)
+# ---------------------------------------------------------------- staged path (rows off the 16-byte grid)
+
+@pytest.mark.parametrize("offset", [0, 1, (0, 3), (5, 2)])
+@pytest.mark.parametrize("V", [3 * 4096, 3 * 4096 + 37])
+@pytest.mark.parametrize("dtype", [synth.F32, synth.BF16])
+def test_staged_path_offsets(dev, offset, V, dtype):
+    """Base pointers shifted by whole elements (target and draft alike or apart), and row
+    lengths off the 16-byte grid: several stages per tile and a ragged last stage, in every
+    mode."""
+    if offset == 0 and V % 8 == 0:
+        pytest.skip("the aligned path")
+    w = handmade(4, 5, V, dtype, T=0.7, seed=11 + V % 7)
     res = run_stochastic(w, dev, offset=offset)
+    assert res["device_status"][0] == 0
     compare_stochastic(w, res, range(w.B))
+    compare_nkl(w, run_nkl(w, dev, offset=offset), range(w.B))
+    ot = offset[0] if isinstance(offset, tuple) else offset
+    compare_greedy(w, run_greedy(w, dev, offset=ot), range(w.B))
+
+
+def test_staged_path_ties_and_flat_rows(dev):
+    """Lowest index of a tied maximum when the tied entries share one thread's strided
+    group, sit in different groups, or fill a whole (flat) row."""
+    V = 3000
+    t = np.zeros((3, V), dtype=np.float32)
+    t[0, [1256, 1000, 2900]] = 3.0       # 1000 and 1256 are one thread's elements, 256 apart
+    t[2, [2999, 2998, 2742]] = 1.0       # 2742 = 2998 - 256: lowest is 2742
+    d = np.zeros((2, V), dtype=np.float32)
+    for dtype in (synth.F32, synth.BF16):
+        w = synth.StochasticWorkload(B=1, V=V, dtype=dtype, T=1.0, gammas=np.array([2], np.int32),
+                                     cu_draft=np.array([0, 2], np.int32), target=synth.storage(t, dtype),
+                                     draft=synth.storage(d, dtype), tokens=np.array([1000, 0], np.int32),
+                                     u_accept=np.array([0.1, 0.2], np.float32),
+                                     u_sample=np.array([0.3], np.float32))
+        for off in (1, 3):
+            res = run_greedy(w, dev, offset=off)
+            assert res["n_accepted"][0] == 2 and list(res["out_tokens"]) == [1000, 0, 2742]
+            compare_stochastic(w, run_stochastic(w, dev, offset=off), [0])
+
+
+def test_staged_path_headline_shape(dev):
+    """The headline batch (B=256, gamma=8, V=128256, bf16) with the logits one element off
+    the 16-byte grid: every sampler range and tier, sampled against the oracle."""
+    w = workload(2)
+    res = run_stochastic(w, dev, offset=1)
+    assert res["device_status"][0] == 0
+    compare_stochastic(w, res, sample_seqs(w.B, 8, seed=12))
+    g = run_greedy(w, dev, offset=1)
+    compare_greedy(w, g, range(w.B))
+    assert np.array_equal(g["n_accepted"], res["greedy_n"])
+    aligned = run_stochastic(w, dev)
+    # the two paths sum in different orders: decisions agree except at a boundary tie
+    assert np.mean(aligned["n_accepted"] == res["n_accepted"]) > 0.99
+    np.testing.assert_allclose(res["alpha"], aligned["alpha"], rtol=1e-4)
+
+
+def test_staged_path_odd_vocabulary(dev):
+    """A vocabulary whose bf16 rows are not a multiple of 16 bytes (V = 50257): every row
+    has its own phase, target and draft rows of one position differ in phase."""
+    w = synth.make_stochastic(64, 50257, synth.BF16, 0.8, seed=27, gamma=5)
+    res = run_stochastic(w, dev)
+    assert res["device_status"][0] == 0
+    compare_stochastic(w, res, sample_seqs(w.B, 16, seed=13))
+    compare_greedy(w, run_greedy(w, dev), range(w.B))
+    compare_nkl(w, run_nkl(w, dev), sample_seqs(w.B, 8, seed=14))
 
 
 def test_gamma_zero_and_one(dev):
