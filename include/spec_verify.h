@@ -30,8 +30,9 @@
  *     SPEC_DEV_* bits). The word is sticky: the library never clears it, the caller
  *     zeroes it when it wants a fresh reading. A sequence with a data error reports
  *     n = -1, -1 in its integer outputs and NaN in its real outputs. No kernel traps
- *     or asserts; the one wait on other blocks (the sampler polling a sequence's
- *     decision) is bounded and reports SPEC_DEV_TIMEOUT if it runs out.
+ *     or asserts; every wait (the sampler polling a sequence's decision, a warp of the
+ *     staged path waiting for its bulk copies) is bounded and reports SPEC_DEV_TIMEOUT
+ *     if it runs out.
  *   - Logits are row-major [rows, V] with V contiguous, fp32 or bf16 (raw bf16 bit
  *     patterns). Rows whose byte size is a multiple of 16 and whose base pointers are
  *     16-byte aligned take the vectorised path. Any other layout takes the staged path,

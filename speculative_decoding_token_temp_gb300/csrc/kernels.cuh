@@ -5,9 +5,9 @@
 //                    every sequence "pending", checks packed offsets.
 //   rows_kernel      one block per (row, vocabulary chunk) tile. Streams the target row
 //                    (and, for a pair, the draft row) once -- on aligned rows through a
-//                    per-thread 3-stage cp.async ring in shared memory, otherwise through a
-//                    block-wide ring of whole aligned 16-byte blocks read back at the row's
-//                    phase -- and keeps per-thread online statistics: the
+//                    per-thread 3-stage cp.async ring in shared memory, otherwise through
+//                    per-warp rings of bulk copies of whole aligned 16-byte blocks, read
+//                    back at the row's phase -- and keeps per-thread online statistics: the
 //                    raw maximum and its lowest index, sum_v exp((z_v - ref)/T), and for
 //                    the draft row also sum_v exp((zd_v - ref_d)/T) (zd_v - zt_v).
 //                    Block-reduces them into a 32-byte partial. The last tile of a
@@ -21,7 +21,7 @@
 //                    masses of the residual max(0, p - q) (or of p for the bonus row) go to
 //                    a table; the block completing a sequence finds the inverse-CDF
 //                    crossing in the table (exact fixed-point sums) and re-reads one slice.
-//                    Rows off the 16-byte grid stream through the same block-wide ring as
+//                    Rows off the 16-byte grid stream through per-warp bulk-copy rings as
 //                    in the tile kernel.
 // Every kernel is launched with programmatic dependent launch, so its blocks are resident
 // before its predecessor drains, and executes griddepcontrol.wait before its first access
@@ -291,16 +291,20 @@ __device__ __forceinline__ float elem_at<float>(const float* row, int x) {
 
 // ---------------------------------------------------------------------------
 // staged path, for rows that do not start on a 16-byte boundary (an offset base pointer,
-// or a row length whose byte size is not a multiple of 16): the block copies the whole
-// aligned 16-byte blocks that cover a stretch of a row into shared memory with cp.async,
-// and every thread then reads single elements at the stretch's phase. The first and last
-// block may reach up to 15 bytes before the stretch's first element or after its last;
-// each block holds at least one element of the stretch, so it lies on the same mapped
-// page, and the extra bytes are never used.
+// or a row length whose byte size is not a multiple of 16): each warp streams its own
+// runs of a row through a private ring of shared-memory slots, filled by bulk copies
+// (cp.async.bulk, completion counted in bytes on one mbarrier per slot) of the whole
+// aligned 16-byte blocks that cover a run; its lanes then read single elements at the
+// run's phase. The first and last block may reach up to 15 bytes before the run's first
+// element or after its last; each block holds at least one element of the run, so it
+// lies on the same mapped page, and the extra bytes are never used.
 
-constexpr int kStageRowBytes = 8192;                 // one row of a pair in one stage (twice that for a single row)
-constexpr int kStageSlot = kStageRowBytes + 16;      // with room for the phase
-constexpr int kStagedSmem = kCS * 2 * kStageSlot;    // dynamic shared memory of the staged path
+constexpr int kStageRowBytes = 8192;                      // one row of a pair in one block stage (twice that for a single row)
+constexpr int kWarpRowBytes = kStageRowBytes / kWarps;    // a warp's run of a row of a pair in one stage
+constexpr int kWarpSlot = kWarpRowBytes + 16;             // with room for the phase
+constexpr int kWarpStage = 2 * kWarpSlot;                 // a warp's part of one stage (two rows, or one of twice the run)
+constexpr int kStagedSmem = kCS * kWarps * kWarpStage;    // dynamic shared memory of the staged path
+constexpr int kRingPollLimit = 1 << 20;                   // bounded wait for a slot's bytes (SPEC_DEV_TIMEOUT)
 
 // Elements of the 16-byte block holding p that precede p.
 template <typename E>
@@ -308,18 +312,82 @@ __device__ __forceinline__ int phase16(const E* p) {
   return (int)((reinterpret_cast<uintptr_t>(p) & 15u) / sizeof(E));
 }
 
-// Block-wide: copies the blocks covering elements [e0, e0 + n) of `row` to the shared
-// address dst, thread t taking blocks t, t + kThreads, ...; element e0 + x then sits at
-// element phase16(row + e0) + x of the copy.
+// First aligned block and byte count of the blocks covering elements [e0, e0 + n) of row
+// (0 bytes for n <= 0); element e0 + x then sits at element phase16(row + e0) + x of a copy.
 template <typename E>
-__device__ __forceinline__ void stage_copy(uint32_t dst, const E* row, int e0, int n) {
-  if (n <= 0) return;
+__device__ __forceinline__ uint32_t run_blocks(const E* row, int e0, int n, const void** src) {
+  if (n <= 0) return 0u;
   const uintptr_t a0 = reinterpret_cast<uintptr_t>(row + e0);
   const uintptr_t b0 = a0 & ~(uintptr_t)15;
-  const int nb = (int)(((a0 + (uintptr_t)n * sizeof(E) - 1) >> 4) - (b0 >> 4)) + 1;
-  for (int j = threadIdx.x; j < nb; j += kThreads)
-    cp_async16(dst + 16u * (uint32_t)j, reinterpret_cast<const void*>(b0 + 16u * (uintptr_t)j));
+  *src = reinterpret_cast<const void*>(b0);
+  return (uint32_t)((((a0 + (uintptr_t)n * sizeof(E) - 1) >> 4) - (b0 >> 4) + 1) << 4);
 }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_arrive(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, unsigned parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// A warp's ring of kCS slots, initialised once per block. Its stages are numbered over
+// the block's lifetime: stage q uses slot q % kCS, and its mbarrier completes phase
+// q / kCS once the stage's bytes have landed. Every produced stage is waited for.
+struct WarpRing {
+  uint32_t bars;  // shared address of the warp's kCS mbarriers (8 bytes each)
+  int next;       // stages produced before the current pass
+
+  // lane 0 initialises the barriers (one arrival each: lane 0's, with the byte count)
+  __device__ __forceinline__ void init(uint64_t* warp_bars) {
+    bars = (uint32_t)__cvta_generic_to_shared(warp_bars);
+    next = 0;
+    if ((threadIdx.x & 31) == 0) {
+#pragma unroll
+      for (int j = 0; j < kCS; ++j) mbar_init(bars + 8u * j, 1u);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+  }
+  // Called by lane 0 only: the copies of stage k (up to two runs) into slot addresses d0
+  // and d1. The warp's lanes are done with the slot's previous stage (a __syncwarp before
+  // this call).
+  __device__ __forceinline__ void produce(int k, uint32_t d0, const void* s0, uint32_t n0, uint32_t d1,
+                                          const void* s1, uint32_t n1) const {
+    const uint32_t bar = bars + 8u * (uint32_t)(k % kCS);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the reads of the slot precede the copies
+    mbar_expect_arrive(bar, n0 + n1);
+    if (n0) bulk_copy(d0, s0, n0, bar);
+    if (n1) bulk_copy(d1, s1, n1, bar);
+  }
+  // Every lane: waits (bounded) until stage k's bytes have landed.
+  __device__ __forceinline__ void wait(int k, uint32_t* status) const {
+    const uint32_t bar = bars + 8u * (uint32_t)(k % kCS);
+    const unsigned parity = (unsigned)(k / kCS) & 1u;
+    for (int it = 0; !mbar_try_wait(bar, parity); ++it) {
+      if (it == kRingPollLimit) {
+        if ((threadIdx.x & 31) == 0) atomicOr(status, SPEC_DEV_TIMEOUT);
+        break;
+      }
+    }
+  }
+};
 
 // one element of a staged copy, as float
 template <typename E>
@@ -475,8 +543,8 @@ __device__ __forceinline__ float2 exp_sum2(const float (&t)[VEC], float c, float
 // Exact max. A single-element group (scalar path) records its index directly; a wider
 // group only records where it starts, and the lowest index inside it is found once, at
 // the end of the tile, by the thread that holds the tile's maximum (resolve_index).
-// H == 0 marks a strided group (staged path): its VEC elements sit at e0 + k * kThreads,
-// and g1 records their count (resolve_strided).
+// H == 0 marks a strided group (staged path): its VEC elements sit at e0 + k * GS, GS
+// the stride the tile's reduction is given, and g1 records their count (resolve_strided).
 template <int VEC, int H, bool IDX>
 __device__ __forceinline__ void track_max(TAcc& a, const float (&t)[VEC], float vm, int e0, int e1) {
   if (IDX) {

@@ -419,80 +419,83 @@ __device__ __forceinline__ void stream_tile(const E* trow, const E* drow, int v0
 }
 
 // Staged path: the tile [e_begin, e_end) in stages of kStageRowBytes per row of a pair
-// (twice that for a single row) through a block-wide kCS-slot ring of whole aligned
-// 16-byte blocks (stage_copy), with one barrier per stage. Thread t takes elements
-// t, t + kThreads, ... of each stage (consecutive lanes read consecutive elements, so the
-// shared-memory reads are conflict free), folded in as strided groups of kGroup.
-constexpr int kGroup = 8;
-
+// (twice that for a single row); warp w takes the w-th contiguous run of every stage
+// through its own kCS-slot ring (WarpRing: bulk copies of whole aligned 16-byte blocks),
+// so no block-wide barrier orders the copies and the reads. Lane l takes elements
+// l, l + 32, ... of the run (consecutive lanes read consecutive elements: conflict free),
+// folded in as strided groups of up to 16; a group that the run's end cuts is folded in
+// element by element.
 template <typename E, int MODE, int KIND>
 __device__ __forceinline__ void stream_staged(const E* trow, const E* drow, int e_begin, int e_end, float c, float cd,
-                                              TAcc& ta, DAcc& da, unsigned char* smem) {
+                                              TAcc& ta, DAcc& da, unsigned char* smem, uint32_t* status) {
   constexpr bool IDX = is_stoch(MODE), SEPT = MODE == M_STOCH2, PAIR = KIND == K_PAIR;
-  constexpr int S = (PAIR ? kStageRowBytes : 2 * kStageRowBytes) / (int)sizeof(E);  // elements of a row per stage
-  constexpr int NG = S / (kGroup * kThreads);                                         // groups per thread per stage
-  constexpr unsigned SLOT = 2 * kStageSlot;
-  static_assert(S % (kGroup * kThreads) == 0, "stage of whole groups");
-  const int t = threadIdx.x;
-  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem);
+  constexpr int SW = (PAIR ? kWarpRowBytes : 2 * kWarpRowBytes) / (int)sizeof(E);  // elements of a warp's run
+  constexpr int S = SW * kWarps;                                                     // elements of a stage
+  constexpr int U = SW / 32;                                                         // per lane per run
+  constexpr int G = U < 16 ? U : 16;                                                 // elements of a group
+  constexpr int NG = U / G;
+  static_assert(U % G == 0, "runs of whole groups");
+  __shared__ __align__(8) uint64_t s_bars[kWarps][kCS];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  WarpRing ring;  // one pass per block: stage k is ring stage k
+  ring.init(s_bars[warp]);
+  const uint32_t wbase = (uint32_t)__cvta_generic_to_shared(smem) + (uint32_t)(warp * kWarpStage);
   const int nst = (e_end - e_begin + S - 1) / S;
-  // S * sizeof(E) is a multiple of 16: every stage of a row has the same phase
+  // S and SW elements are whole 16-byte blocks: every run of a row has the same phase
   const int ph_t = phase16(trow + e_begin), ph_d = PAIR ? phase16(drow + e_begin) : 0;
   auto issue = [&](int k) {
-    if (k < nst) {
-      const uint32_t slot = sbase + (uint32_t)(k % kCS) * SLOT;
-      const int e0 = e_begin + k * S, n = min(S, e_end - e0);
-      stage_copy<E>(slot, trow, e0, n);
-      if constexpr (PAIR) stage_copy<E>(slot + kStageSlot, drow, e0, n);
+    if (lane == 0 && k < nst) {
+      const uint32_t slot = wbase + (uint32_t)((k % kCS) * kWarps * kWarpStage);
+      const int e0 = e_begin + k * S + warp * SW, n = min(SW, e_end - e0);
+      const void* s0 = nullptr;
+      const void* s1 = nullptr;
+      const uint32_t n0 = run_blocks<E>(trow, e0, n, &s0);
+      const uint32_t n1 = PAIR ? run_blocks<E>(drow, e0, n, &s1) : 0u;
+      ring.produce(k, slot, s0, n0, slot + kWarpSlot, s1, n1);
     }
-    cp_commit();
   };
 #pragma unroll
   for (int k = 0; k < kCS - 1; ++k) issue(k);
   for (int k = 0; k < nst; ++k) {
-    cp_wait<kCS - 2>();  // this thread's copies of stage k have landed
-    __syncthreads();     // ... and every thread's; every thread is done with stage k - 1
+    __syncwarp();        // every lane is done with stage k - 1
     issue(k + kCS - 1);  // into the slot of stage k - 1
-    const unsigned char* slot = smem + (size_t)(k % kCS) * SLOT;
+    ring.wait(k, status);
+    const unsigned char* slot = smem + (size_t)(warp * kWarpStage + (k % kCS) * kWarps * kWarpStage);
     const E* sT = reinterpret_cast<const E*>(slot) + ph_t;
-    const E* sD = reinterpret_cast<const E*>(slot + kStageSlot) + ph_d;
-    const int eb = e_begin + k * S, n = min(S, e_end - eb);
+    const E* sD = reinterpret_cast<const E*>(slot + kWarpSlot) + ph_d;
+    const int eb = e_begin + k * S + warp * SW, n = min(SW, e_end - eb);
 #pragma unroll
     for (int g = 0; g < NG; ++g) {
-      const int x0 = g * kGroup * kThreads + t;  // this thread's first element of the group
-      if ((g + 1) * kGroup * kThreads <= n) {    // the whole group is inside the stage, for every thread
-        float ft[kGroup], fd[kGroup];
+      const int x0 = g * G * 32 + lane;  // this lane's first element of the group
+      if (x0 + (G - 1) * 32 < n) {       // the whole group is inside the run
+        float ft[G], fd[G];
 #pragma unroll
-        for (int j = 0; j < kGroup; ++j) {
-          ft[j] = sh_elem<E>(sT, x0 + j * kThreads);
-          if constexpr (PAIR) fd[j] = sh_elem<E>(sD, x0 + j * kThreads);
+        for (int j = 0; j < G; ++j) {
+          ft[j] = sh_elem<E>(sT, x0 + j * 32);
+          if constexpr (PAIR) fd[j] = sh_elem<E>(sD, x0 + j * 32);
         }
         if constexpr (PAIR)
-          pair_update<kGroup, IDX, 0, SEPT>(ta, da, ft, fd, eb + x0, c, 0, cd);
+          pair_update<G, IDX, 0, SEPT>(ta, da, ft, fd, eb + x0, c, 0, cd);
         else if constexpr (KIND == K_TSUM)
-          tsum_update<kGroup, 0>(ta, ft, eb + x0, c);
+          tsum_update<G, 0>(ta, ft, eb + x0, c);
         else
-          argmax_update<kGroup, 0>(ta, ft, eb + x0);
+          argmax_update<G, 0>(ta, ft, eb + x0);
       } else {
-        for (int j = 0; j < kGroup; ++j) {
-          const int x = x0 + j * kThreads;
-          if (x < n) {
-            float ft[1], fd[1];
-            ft[0] = sh_elem<E>(sT, x);
-            if constexpr (PAIR) {
-              fd[0] = sh_elem<E>(sD, x);
-              pair_update<1, IDX, 0, SEPT>(ta, da, ft, fd, eb + x, c, 0, cd);
-            } else if constexpr (KIND == K_TSUM) {
-              tsum_update<1, 0>(ta, ft, eb + x, c);
-            } else {
-              argmax_update<1, 0>(ta, ft, eb + x);
-            }
+        for (int x = x0; x < n; x += 32) {
+          float ft[1], fd[1];
+          ft[0] = sh_elem<E>(sT, x);
+          if constexpr (PAIR) {
+            fd[0] = sh_elem<E>(sD, x);
+            pair_update<1, IDX, 0, SEPT>(ta, da, ft, fd, eb + x, c, 0, cd);
+          } else if constexpr (KIND == K_TSUM) {
+            tsum_update<1, 0>(ta, ft, eb + x, c);
+          } else {
+            argmax_update<1, 0>(ta, ft, eb + x);
           }
         }
       }
     }
   }
-  cp_wait<0>();
 }
 
 template <typename E, int VEC, int MODE>
@@ -576,14 +579,14 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
     }
   } else {
     if constexpr (MODE == M_GREEDY || MODE == M_TREE) {
-      stream_staged<E, MODE, K_ARGMAX>(trow, drow, e_begin, e_end, c, cd, ta, da, dsm);
+      stream_staged<E, MODE, K_ARGMAX>(trow, drow, e_begin, e_end, c, cd, ta, da, dsm, p.status);
     } else if constexpr (MODE == M_NKL) {
-      stream_staged<E, MODE, K_PAIR>(trow, drow, e_begin, e_end, c, cd, ta, da, dsm);
+      stream_staged<E, MODE, K_PAIR>(trow, drow, e_begin, e_end, c, cd, ta, da, dsm, p.status);
     } else {
       if (kind == K_PAIR)
-        stream_staged<E, MODE, K_PAIR>(trow, drow, e_begin, e_end, c, cd, ta, da, dsm);
+        stream_staged<E, MODE, K_PAIR>(trow, drow, e_begin, e_end, c, cd, ta, da, dsm, p.status);
       else
-        stream_staged<E, MODE, K_TSUM>(trow, drow, e_begin, e_end, c, cd, ta, da, dsm);
+        stream_staged<E, MODE, K_TSUM>(trow, drow, e_begin, e_end, c, cd, ta, da, dsm, p.status);
     }
   }
 
@@ -591,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
   if constexpr (VEC > 1)
     part = reduce_tile<BlockSync, E, VEC, SEPT>(kind, ta, da, c, trow, cd);
   else
-    part = reduce_tile<BlockSync, E, 1, SEPT, kThreads>(kind, ta, da, c, trow, cd);
+    part = reduce_tile<BlockSync, E, 1, SEPT, 32>(kind, ta, da, c, trow, cd);
   if (threadIdx.x == 0) {
     float4* dst = reinterpret_cast<float4*>(p.part + tile);
     __stcg(dst, make_float4(part.tm, part.ts, __int_as_float(part.tidx), __int_as_float(part.bad)));

@@ -201,6 +201,8 @@ __device__ __forceinline__ void block_crossing(const float* table, int n, float 
       r.ent = min(ent, max(n - 1, 0));
     }
   }
+  // the staged sampler's bulk copies (async proxy) may rewrite this shared memory next
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   __syncthreads();
 }
 
@@ -259,58 +261,63 @@ __device__ __forceinline__ void mass_pass(const E* trow, const E* drow, int mode
   cp_wait<0>();
 }
 
-// The same masses for rows off the 16-byte grid: each stage (the elements of 512 vectors)
-// of the row pair goes through a block-wide ring of whole aligned 16-byte blocks
-// (stage_copy, one barrier per stage); in the slice of warp w, half h, lane l weighs the
-// elements l, l + 32, ... (conflict-free reads). Elements past the row end weigh 0.
+// The same masses for rows off the 16-byte grid: in each stage (the elements of 512
+// vectors) warp w takes the contiguous run of slices 2w and 2w + 1 of the row pair (or
+// row) through its own ring (WarpRing: bulk copies of whole aligned 16-byte blocks); in
+// each slice lane l weighs the elements l, l + 32, ... (conflict-free reads). Elements
+// past the row end weigh 0.
 template <typename E, int VEC>
 __device__ __forceinline__ void mass_pass_staged(const E* trow, const E* drow, int mode, float lt2, float ld2, float c,
-                                                 float cd, int V, int k0, int k1, float* table, unsigned char* smem) {
+                                                 float cd, int V, int k0, int k1, float* table, unsigned char* smem,
+                                                 WarpRing& ring, uint32_t* status) {
   constexpr int S = 2 * kThreads * VEC;  // elements of a stage
   constexpr int SL = 32 * VEC;           // elements of a slice
-  constexpr unsigned SLOT = 2 * kStageSlot;
-  static_assert(S * (int)sizeof(E) == kStageRowBytes, "a stage is one staged row slot");
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  constexpr int SW = 2 * SL;             // a warp's run: two slices
+  static_assert(SW * (int)sizeof(E) == kWarpRowBytes, "a warp's run fills its staged row slot");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bool resid = mode == S_RESID;
-  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem);
+  const uint32_t wbase = (uint32_t)__cvta_generic_to_shared(smem) + (uint32_t)(warp * kWarpStage);
   const int nst = k1 - k0;
   const int ph_t = phase16(trow + (size_t)k0 * S), ph_d = resid ? phase16(drow + (size_t)k0 * S) : 0;
+  const int q0 = ring.next;  // ring stage of this pass's stage 0
   auto issue = [&](int k) {
-    if (k < nst) {
-      const uint32_t slot = sbase + (uint32_t)(k % kCS) * SLOT;
-      const int e0 = (k0 + k) * S, n = min(S, V - e0);
-      stage_copy<E>(slot, trow, e0, n);
-      if (resid) stage_copy<E>(slot + kStageSlot, drow, e0, n);
+    if (lane == 0 && k < nst) {
+      const uint32_t slot = wbase + (uint32_t)(((q0 + k) % kCS) * kWarps * kWarpStage);
+      const int e0 = (k0 + k) * S + warp * SW, n = min(SW, V - e0);
+      const void* s0 = nullptr;
+      const void* s1 = nullptr;
+      const uint32_t n0 = run_blocks<E>(trow, e0, n, &s0);
+      const uint32_t n1 = resid ? run_blocks<E>(drow, e0, n, &s1) : 0u;
+      ring.produce(q0 + k, slot, s0, n0, slot + kWarpSlot, s1, n1);
     }
-    cp_commit();
   };
+  __syncwarp();  // the warp's lanes are done with every slot (the previous pass, the crossing search)
 #pragma unroll
   for (int k = 0; k < kCS - 1; ++k) issue(k);
   for (int k = 0; k < nst; ++k) {
-    cp_wait<kCS - 2>();
-    __syncthreads();
+    __syncwarp();
     issue(k + kCS - 1);
-    const unsigned char* slot = smem + (size_t)(k % kCS) * SLOT;
+    ring.wait(q0 + k, status);
+    const unsigned char* slot = smem + (size_t)(warp * kWarpStage + ((q0 + k) % kCS) * kWarps * kWarpStage);
     const E* sT = reinterpret_cast<const E*>(slot) + ph_t;
-    const E* sD = reinterpret_cast<const E*>(slot + kStageSlot) + ph_d;
-    const int n = min(S, V - (k0 + k) * S);
+    const E* sD = reinterpret_cast<const E*>(slot + kWarpSlot) + ph_d;
+    const int n = min(SW, V - ((k0 + k) * S + warp * SW));  // <= 0 past the row end
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const int x0 = (h * kWarps + warp) * SL + lane;
       float ft[VEC], fd[VEC], w[VEC];
 #pragma unroll
       for (int j = 0; j < VEC; ++j) {
-        const int x = x0 + 32 * j;
+        const int x = h * SL + lane + 32 * j;
         const bool in = x < n;
         ft[j] = in ? sh_elem<E>(sT, x) : -INFINITY;
         fd[j] = (in && resid) ? sh_elem<E>(sD, x) : -INFINITY;
       }
       weights<VEC>(mode, ft, fd, lt2, ld2, c, cd, w);
       const float ws = warp_sum(tree_sum<VEC>(w));
-      if (lane == 0) __stcg(table + ((size_t)(k0 + k) * 2 + h) * kWarps + warp, ws);
+      if (lane == 0) __stcg(table + (size_t)(k0 + k) * kSlicesPerStage + 2 * warp + h, ws);
     }
   }
-  cp_wait<0>();
+  ring.next = q0 + nst;
 }
 
 // The warp that owns table entry `ent` (stage k, half h, warp w) re-reads its 32-vector
@@ -392,7 +399,10 @@ __global__ void __launch_bounds__(kThreads, 4) sample2_kernel(const __grid_const
   __shared__ int s_last;
   __shared__ CrossResult sc;
   __shared__ unsigned s_max[kWarps];
+  __shared__ __align__(8) uint64_t s_bars[kWarps][kCS];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  WarpRing ring;  // staged rows: the warp's bulk-copy ring, over every pass of the block
+  if constexpr (STAGED) ring.init(s_bars[warp]);
   const size_t V = (size_t)p.V;
   const int NV = (p.V + VEC - 1) / VEC;  // vectors of a row (the last one partial off the grid)
   const int nst = (NV + 2 * kThreads - 1) / (2 * kThreads);
@@ -446,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 4) sample2_kernel(const __grid_const
     const E* drow = static_cast<const E*>(p.draft) + (q.mode == S_RESID ? (size_t)q.d_row * V : 0);
     float* table = p.table + (size_t)b * p.table_stride;
     if constexpr (STAGED)
-      mass_pass_staged<E, VEC>(trow, drow, q.mode, q.lt2, q.ld2, p.c, p.cd, p.V, k0, k1, table, dsm);
+      mass_pass_staged<E, VEC>(trow, drow, q.mode, q.lt2, q.ld2, p.c, p.cd, p.V, k0, k1, table, dsm, ring, p.status);
     else
       mass_pass<E, VEC>(trow, drow, q.mode, q.lt2, q.ld2, p.c, p.cd, NV, k0, k1, table, dsm);
     __syncthreads();  // orders every warp's table entries before thread 0's fence
@@ -466,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 4) sample2_kernel(const __grid_const
       if (!(mode == S_RESID && !(sc.Z > 1e-30f))) break;
       mode = S_P;  // zero residual: the masses of p of the same row, whole row in this block
       if constexpr (STAGED)
-        mass_pass_staged<E, VEC>(trow, drow, mode, q.lt2, q.ld2, p.c, p.cd, p.V, 0, nst, table, dsm);
+        mass_pass_staged<E, VEC>(trow, drow, mode, q.lt2, q.ld2, p.c, p.cd, p.V, 0, nst, table, dsm, ring, p.status);
       else
         mass_pass<E, VEC>(trow, drow, mode, q.lt2, q.ld2, p.c, p.cd, NV, 0, nst, table, dsm);
       __syncthreads();
