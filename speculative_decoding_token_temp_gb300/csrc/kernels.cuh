@@ -42,7 +42,7 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kMaxRows = SPEC_MAX_GAMMA + 1;
-constexpr int kTargetTiles = 2432;   // 4 waves of the 608 resident blocks (152 SMs x 4): a partial last wave costs little
+constexpr int kTargetTiles = 608;    // one wave of the resident blocks (152 SMs x 4): tiles are split no further, every tile adds a latency-bound epilogue
 
 // M_STOCH2: stochastic with a draft temperature of its own (the draft row is summed at
 // both temperatures)
@@ -173,9 +173,11 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
   return r;
 }
 
+// Reductions over groups of W lanes (W = 32: the whole warp)
+template <int W = 32>
 __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
-  for (int o = 16; o; o >>= 1) x = fmaxf(x, __shfl_xor_sync(kFull, x, o));
+  for (int o = W / 2; o; o >>= 1) x = fmaxf(x, __shfl_xor_sync(kFull, x, o));
   return x;
 }
 __device__ __forceinline__ float warp_max_nan(float x) {
@@ -188,14 +190,22 @@ __device__ __forceinline__ float warp_min(float x) {
   for (int o = 16; o; o >>= 1) x = fminf(x, __shfl_xor_sync(kFull, x, o));
   return x;
 }
+template <int W = 32>
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
-  for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
+  for (int o = W / 2; o; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
   return x;
 }
+template <int W = 32>
 __device__ __forceinline__ int warp_min_i(int x) {
 #pragma unroll
-  for (int o = 16; o; o >>= 1) x = min(x, __shfl_xor_sync(kFull, x, o));
+  for (int o = W / 2; o; o >>= 1) x = min(x, __shfl_xor_sync(kFull, x, o));
+  return x;
+}
+template <int W = 32>
+__device__ __forceinline__ int warp_or(int x) {
+#pragma unroll
+  for (int o = W / 2; o; o >>= 1) x |= __shfl_xor_sync(kFull, x, o);
   return x;
 }
 
@@ -818,12 +828,14 @@ __device__ __forceinline__ float row_nkl(const RowStat& r, float invT, float inv
   return kl * inv_lnV;
 }
 
-// ds is merged at the draft scale cd, dk and ds2 at the target scale c.
+// ds is merged at the draft scale cd, dk and ds2 at the target scale c. A group of W
+// lanes (aligned within the warp; every lane of the warp calls it) merges one row.
+template <int W = 32>
 __device__ __forceinline__ RowStat merge_row(const Partial* pp, int nchunks, float c, float cd) {
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & (W - 1);
   float tm = -INFINITY, ts = 0.f, dm = -INFINITY, ds = 0.f, dk = 0.f, ds2 = 0.f;
   int idx = INT_MAX, bad = 0;
-  for (int ch = lane; ch < nchunks; ch += 32) {
+  for (int ch = lane; ch < nchunks; ch += W) {
     const float4 lo = __ldcg(reinterpret_cast<const float4*>(pp + ch));
     const float4 hi = __ldcg(reinterpret_cast<const float4*>(pp + ch) + 1);
     const float qtm = lo.x, qts = lo.y;
@@ -845,16 +857,16 @@ __device__ __forceinline__ RowStat merge_row(const Partial* pp, int nchunks, flo
     dm = D;
   }
   RowStat r;
-  r.tm = warp_max(tm);
-  r.tidx = warp_min_i(tm == r.tm ? idx : INT_MAX);
-  r.ts = warp_sum(rescale(ts, tm, r.tm, c));
-  r.dm = warp_max(dm);
+  r.tm = warp_max<W>(tm);
+  r.tidx = warp_min_i<W>(tm == r.tm ? idx : INT_MAX);
+  r.ts = warp_sum<W>(rescale(ts, tm, r.tm, c));
+  r.dm = warp_max<W>(dm);
   const float fd = (dm == -INFINITY) ? 0.f : ex2((dm - r.dm) * c);
   const float gd = (dm == -INFINITY) ? 0.f : ex2((dm - r.dm) * cd);
-  r.ds = warp_sum(ds * gd);
-  r.dk = warp_sum(dk * fd);
-  r.ds2 = warp_sum(ds2 * fd);
-  r.bad = __any_sync(kFull, bad) ? 1 : 0;
+  r.ds = warp_sum<W>(ds * gd);
+  r.dk = warp_sum<W>(dk * fd);
+  r.ds2 = warp_sum<W>(ds2 * fd);
+  r.bad = warp_or<W>(bad) ? 1 : 0;
   return r;
 }
 

@@ -131,6 +131,8 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
   constexpr int HB = (MODE == M_NKL) ? 0 : 1;
   constexpr int NT = SY::NT, NW = SY::NT / 32;
   __shared__ RowStat rs[kMaxRows];
+  __shared__ int s_tok[MODE == M_TREE ? SPEC_MAX_TREE_NODES : 1], s_par[MODE == M_TREE ? SPEC_MAX_TREE_NODES : 1];
+  __shared__ int depth[MODE == M_TREE ? SPEC_MAX_TREE_NODES : 1];
   __shared__ int s_n, s_gn;
   __shared__ unsigned s_err;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -142,9 +144,27 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
     s_gn = gb;
     s_err = 0u;
   }
-  for (int i = warp; i < R; i += NW) {
-    const RowStat r = merge_row(p.part + (size_t)(row0 + i) * p.nchunks, p.nchunks, c, p.cd);
-    if (lane == 0) rs[i] = r;
+  if constexpr (MODE == M_TREE) {
+    // the node tokens and parents go to shared memory in one coalesced read, in flight
+    // while the rows merge
+    for (int j = tid; j < p.N; j += NT) {
+      s_tok[j] = p.node_tokens[(size_t)b * p.N + j];
+      s_par[j] = p.parent[j];
+    }
+  }
+  if (p.nchunks <= 16) {
+    // two rows per warp (one per half-warp): one round of partial reads for up to 2 NW rows
+    const int half = lane >> 4;
+    for (int i = 2 * warp; i < R; i += 2 * NW) {
+      const int ii = min(i + half, R - 1);
+      const RowStat r = merge_row<16>(p.part + (size_t)(row0 + ii) * p.nchunks, p.nchunks, c, p.cd);
+      if ((lane & 15) == 0 && i + half < R) rs[i + half] = r;
+    }
+  } else {
+    for (int i = warp; i < R; i += NW) {
+      const RowStat r = merge_row(p.part + (size_t)(row0 + i) * p.nchunks, p.nchunks, c, p.cd);
+      if (lane == 0) rs[i] = r;
+    }
   }
   SY::sync();
 
@@ -154,10 +174,10 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
   const E* draft = static_cast<const E*>(p.draft);
 
   if constexpr (MODE == M_TREE) {
-    // one thread walks the (at most 64-node) tree
+    // one thread walks the (at most 64-node) tree in shared memory
     if (tid == 0) {
       const int N = p.N, D = p.depth;
-      const int32_t* tok = p.node_tokens + (size_t)b * N;
+      const int* tok = s_tok;
       unsigned err = 0u;
       for (int r = 0; r <= N; ++r)
         if (rs[r].bad) err |= SPEC_DEV_NONFINITE;
@@ -175,10 +195,9 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
         return;
       }
       unsigned long long ok = 0ull;
-      int depth[SPEC_MAX_TREE_NODES];
       int pick = -1, best = 0;
       for (int j = 0; j < N; ++j) {
-        const int pj = p.parent[j];
+        const int pj = s_par[j];
         depth[j] = (pj < 0) ? 1 : depth[pj] + 1;
         const int prow = (pj < 0) ? 0 : pj + 1;
         const bool acc = tok[j] == rs[prow].tidx && (pj < 0 || ((ok >> pj) & 1ull));
@@ -195,7 +214,7 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
       for (int d = best - 1; d >= 0; --d) {
         path[d] = k;
         out[d] = tok[k];
-        k = p.parent[k];
+        k = s_par[k];
       }
       for (int d = best; d < D; ++d) path[d] = -1;
       out[best] = rs[pick + 1].tidx;  // pick == -1 gives row 0
