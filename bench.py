@@ -174,10 +174,22 @@ def _to_dev(a, dev):
     return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
 
-class StochasticCall:
-    """Preallocated inputs/outputs for repeated spec_verify_stochastic calls."""
+def _shifted(t, offset):
+    """A copy of device tensor t that starts `offset` elements into its buffer (offset > 0
+    puts the rows off the 16-byte grid: the library's staged path)."""
+    import torch
+    if offset == 0:
+        return t
+    buf = torch.empty(t.numel() + offset, dtype=t.dtype, device=t.device)
+    buf[offset:].copy_(t.reshape(-1))
+    return buf[offset:].view(t.shape)
 
-    def __init__(self, w, dev, host_inputs=False):
+
+class StochasticCall:
+    """Preallocated inputs/outputs for repeated spec_verify_stochastic calls (logits
+    shifted by `offset` elements when offset > 0)."""
+
+    def __init__(self, w, dev, host_inputs=False, offset=0):
         import ctypes
 
         import torch
@@ -188,8 +200,8 @@ class StochasticCall:
         self.lib = _lib.lib()
         B, V = w.B, w.V
         rows, tot = w.total_target, w.total_draft
-        self.t = _to_dev(w.target, dev)
-        self.d = _to_dev(w.draft, dev)
+        self.t = _shifted(_to_dev(w.target, dev), offset)
+        self.d = _shifted(_to_dev(w.draft, dev), offset)
         self.tok = _to_dev(w.tokens, dev)
         self.ua = _to_dev(w.u_accept, dev)
         self.us = _to_dev(w.u_sample, dev)
@@ -375,7 +387,7 @@ def run_ours(args):
     cfg = synth.CONFIGS[HEADLINE]
     from speculative_decoding_token_temp_gb300 import sharding
     w = cfg.make(seed=sharding.rank_seed(cfg.seed, rank), B=args.batch)
-    call = StochasticCall(w, dev, host_inputs=True)
+    call = StochasticCall(w, dev, host_inputs=True, offset=args.offset)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
     step = lambda: call(sh)  # noqa: E731
@@ -458,6 +470,21 @@ def run_ours(args):
         t_sm = time_mode(lambda: api.spec_accept_summary(st, 2, 64, out=sm_out), 200, 10, dev)
         modes["accept_summary_64_slots"] = {"us_per_call": t_sm * 1e6,
                                             "note": "one 64-thread block; the figure includes the host's enqueue rate"}
+        if args.offset == 0:
+            # the same call with the logits one element off the 16-byte grid: the staged path
+            ts, ds = _shifted(call.t, 1), _shifted(call.d, 1)
+            s_out = {}
+            sfn = lambda: api.spec_verify_stochastic(ts, ds, call.tok, w.T, call.ua, call.us,  # noqa: E731
+                                                     gamma=gam, out=s_out)
+            t_s = time_mode(sfn, 200, 10, dev)
+            sg_out = {}
+            t_sg = time_mode(lambda: api.spec_verify_greedy(ts, call.tok, gamma=gam, out=sg_out), 200, 10, dev)
+            modes["stochastic_staged_offset1_B256_g8_V128256"] = {
+                "us_per_call": t_s * 1e6, "GBps": ab["stochastic"] / t_s / 1e9,
+                "frac_of_peak": ab["stochastic"] / t_s / 1e9 / hbm, "greedy_us_per_call": t_sg * 1e6,
+                "note": "logits one element off the 16-byte grid (as for a vocabulary whose row is not a "
+                        "multiple of 16 bytes): per-warp bulk-copy rings read back at the row's phase"}
+            del ts, ds, s_out, sg_out
         del res
         tw = synth.CONFIGS[3].make()
         tt = _to_dev(tw.target, dev)
@@ -500,13 +527,16 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"B{w.B}_g8_V128256_bf16: stochastic verify + NKL(delta=0.15) + greedy, one call",
+        "config": {"workload": f"B{w.B}_g8_V128256_bf16: stochastic verify + NKL(delta=0.15) + greedy, one call"
+                               + (f" (logits {args.offset} element(s) off the 16-byte grid: staged path)"
+                                  if args.offset else ""),
                    "B": w.B, "gamma": 8, "V": w.V, "T": w.T, "seed": cfg.seed, "rows_per_step": rows_step,
                    "l2": f"inputs {(w.target.nbytes + w.draft.nbytes) / 1e6:.0f} MB per step, larger than the "
                          "129 MB L2; no flush",
                    "parallelism": f"{world} independent shard(s), no collective"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": profiled_traffic() if w.B == 256 else None,
+                     "frac": achieved / hbm,
+                     "traffic": profiled_traffic() if w.B == 256 and args.offset == 0 else None,
                      "kernel": "spec_verify_stochastic call (prologue_kernel + rows_kernel + sample2_kernel)",
                      "algorithmic_bytes": ab["stochastic"], "peak_source": peak_kind,
                      "note": f"achieved = algorithmic bytes / call time (CUDA events); peak = {peak_kind} "
@@ -597,6 +627,8 @@ def main():
     ap.add_argument("--no-modes", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--skip-ragged", action="store_true")
+    ap.add_argument("--offset", type=int, default=0, metavar="N",
+                    help="shift the timed call's logits by N elements (N % 8 != 0: the staged path)")
     ap.add_argument("--batch", type=int, default=None,
                     help="sequences per step (default: the workload's 256); smaller slices serve profiling")
     ap.add_argument("--multi", type=int, default=None, metavar="G",
