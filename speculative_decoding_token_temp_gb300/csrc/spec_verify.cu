@@ -20,10 +20,9 @@ namespace {
 inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Vocabulary chunking of the tile kernel: chunks of at most max_chunk tokens (32768 for
-// row pairs, 65536 for single rows: about 128 KB per tile either way), split further
-// (down to 8192) while the grid has fewer tiles than the GPU has block slots. Chunk
-// sizes are multiples of 8 so every chunk starts on a 16-byte vector boundary.
+// Vocabulary chunking of the tile kernel: chunks of at most max_chunk tokens, split
+// further (down to 8192) while the grid has fewer tiles than the GPU has block slots.
+// Chunk sizes are multiples of 8 so every chunk starts on a 16-byte vector boundary.
 void chunking(int V, long long rows, int max_chunk, int* nchunks, int* chunk_elems) {
   long long nc = ceil_div(V, max_chunk);
   while (rows * nc < kTargetTiles && V / (nc + 1) >= 8192) ++nc;
@@ -45,14 +44,16 @@ int table_stride_for(int V, spec_dtype dt) {
   return (int)(ceil_div(nv, 2 * kThreads) * kSlicesPerStage);
 }
 
-// max_chunk: the longest vocabulary chunk of a tile (0 = 65536 tokens for single-row
-// tiles, 32768 for row pairs)
+// max_chunk: the longest vocabulary chunk of a tile. 0 = the measured best: 65536 tokens
+// for single-row tiles and for the stochastic call's pairs (256 KB pair tiles: fewer
+// tile epilogues; 185.6 against 191.7 us at the headline, same box), 32768 for the NKL
+// call's pairs (153.7 against 155.4 us).
 Layout layout(int B, int V, long long rows, bool sample, bool single_rows = false, spec_dtype dt = SPEC_F32,
               int max_chunk = 0) {
   Layout L;
   L.rows = rows;
-  chunking(V, rows > 0 ? rows : 1, max_chunk > 0 ? max_chunk : (single_rows ? 65536 : 32768), &L.nchunks,
-           &L.chunk_elems);
+  chunking(V, rows > 0 ? rows : 1, max_chunk > 0 ? max_chunk : ((single_rows || sample) ? 65536 : 32768),
+           &L.nchunks, &L.chunk_elems);
   size_t off = 0;
   L.cntA = off;  // B tickets, then the count of finished tiles
   off = align256(off + sizeof(unsigned) * ((size_t)B + 1));

@@ -34,10 +34,10 @@ def _g(B, gamma, V, total=None, cu=None):
 def test_workspace_sizes(lib):
     BF, F = _lib.SPEC_BF16, _lib.SPEC_F32
     h = lib.spec_workspace_bytes(_g(256, 8, 128256), BF, _lib.SPEC_MODE_STOCHASTIC)
-    # 2304 rows x 4 chunks x 32 B partials, tickets, records, segment totals, and the
-    # sampler's slice-mass table: 256 sequences x 32 stages x 16 slices x 4 B
+    # 2304 rows x 2 chunks (of at most 65536 tokens) x 32 B partials, tickets, records,
+    # and the sampler's slice-mass table: 256 sequences x 32 stages x 16 slices x 4 B
     table = 256 * 32 * 16 * 4
-    assert 2304 * 4 * 32 + table <= h < 2304 * 4 * 32 + table + 256 * 200
+    assert 2304 * 2 * 32 + table <= h < 2304 * 2 * 32 + table + 256 * 200
     assert lib.spec_workspace_bytes(_g(256, 8, 128256), F, _lib.SPEC_MODE_STOCHASTIC) > h   # f32: twice the table
     assert lib.spec_workspace_bytes(_g(256, 8, 128256), BF, _lib.SPEC_MODE_GREEDY) <= h
     assert lib.spec_workspace_bytes(_g(0, 8, 100), BF, _lib.SPEC_MODE_STOCHASTIC) >= 0
