@@ -46,13 +46,13 @@ int table_stride_for(int V, spec_dtype dt) {
 
 // max_chunk: the longest vocabulary chunk of a tile. 0 = the measured best: 65536 tokens
 // for single-row tiles and for the stochastic call's pairs (256 KB pair tiles: fewer
-// tile epilogues; 185.6 against 191.7 us at the headline, same box), 32768 for the NKL
-// call's pairs (153.7 against 155.4 us).
+// tile epilogues; 185.6 against 191.7 us at the headline, same box), 49152 for the NKL
+// call's pairs (150.3 us, against 152.0 with 32768 and 155.4 with 65536).
 Layout layout(int B, int V, long long rows, bool sample, bool single_rows = false, spec_dtype dt = SPEC_F32,
               int max_chunk = 0) {
   Layout L;
   L.rows = rows;
-  chunking(V, rows > 0 ? rows : 1, max_chunk > 0 ? max_chunk : ((single_rows || sample) ? 65536 : 32768),
+  chunking(V, rows > 0 ? rows : 1, max_chunk > 0 ? max_chunk : ((single_rows || sample) ? 65536 : 49152),
            &L.nchunks, &L.chunk_elems);
   size_t off = 0;
   L.cntA = off;  // B tickets, then the count of finished tiles
@@ -229,8 +229,10 @@ cudaError_t launch_sample2(bool bf16, bool vec, const SampleParams& sp, long lon
 
 // Fused multi-draft tiles: when given, the verification launches multi_rows_kernel over
 // (group, row, chunk) tiles instead of rows_kernel over (row, chunk) tiles. A fused tile
-// reads 2K rows of a chunk as long as a pair tile's (shorter chunks measured slower: more per-tile fixed work).
-constexpr int kMultiChunk = 32768;
+// reads 2K rows of a chunk of up to 131072 tokens, whole rows at the usual vocabulary
+// sizes (G=64, K=3, same box: 222.5 us, against 229.5 with 65536-token chunks and 242.1
+// with 32768; shorter chunks cost more per-tile fixed work).
+constexpr int kMultiChunk = 131072;
 struct MultiTiles {
   int K = 0;
   PairParams pp;
