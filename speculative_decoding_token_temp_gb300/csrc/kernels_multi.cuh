@@ -330,6 +330,14 @@ __global__ void __launch_bounds__(kThreads, 2) multi_rows_kernel(const __grid_co
     if (v >= v1) continue;
     const uint4* sq = reinterpret_cast<const uint4*>(dsm + (size_t)(st % kMS) * SLOT) + t;
     const int e0 = v * VEC;
+    // K <= 3: every candidate's draft vector unpacked once, for its own sums and the K - 1
+    // pairs (at K = 4 the extra registers spill; its draft vectors are unpacked per use)
+    constexpr bool PRE = K <= 3;
+    float fdk[PRE ? K : 1][VEC];
+    if (PRE && pair) {
+#pragma unroll
+      for (int a = 0; a < (PRE ? K : 0); ++a) io::unpack(sq[(K + a) * kThreads], fdk[a]);
+    }
 #pragma unroll
     for (int a = 0; a < K; ++a) {
       float ft[VEC];
@@ -347,8 +355,10 @@ __global__ void __launch_bounds__(kThreads, 2) multi_rows_kernel(const __grid_co
         ta[a].s = add2(ta[a].s, exp_sum2<VEC>(ft, c, ta[a].nmc, et));
       }
       if (pair) {
-        float fd[VEC], ed[VEC];
-        io::unpack(sq[(K + a) * kThreads], fd);
+        float fdu[VEC];
+        if constexpr (!PRE) io::unpack(sq[(K + a) * kThreads], fdu);
+        const float (&fd)[VEC] = PRE ? fdk[PRE ? a : 0] : fdu;
+        float ed[VEC];
         const float vm = vmax<VEC>(fd);
         const bool mv = vm > da[a].mth;
         if (__any_sync(__activemask(), mv)) {
@@ -368,9 +378,13 @@ __global__ void __launch_bounds__(kThreads, 2) multi_rows_kernel(const __grid_co
 #pragma unroll
         for (int b = 0; b < K; ++b) {
           if (b == a) continue;
-          float fb[VEC];
-          io::unpack(sq[(K + b) * kThreads], fb);
-          kk[a][b] += dot_diff<VEC>(ed, fd, fb);
+          if constexpr (PRE) {
+            kk[a][b] += dot_diff<VEC>(ed, fd, fdk[b]);
+          } else {
+            float fb[VEC];
+            io::unpack(sq[(K + b) * kThreads], fb);
+            kk[a][b] += dot_diff<VEC>(ed, fd, fb);
+          }
         }
       }
     }
