@@ -65,7 +65,8 @@ def compare_multi(w, res, G, K, gamma, stochastic, c_thr=0.1, d_thr=0.15):
 
 @pytest.mark.parametrize("K,V,dtype,stochastic", [(2, 4096, synth.BF16, False), (3, 32000, synth.BF16, True),
                                                   (4, 128256, synth.BF16, False), (3, 5001, synth.F32, True),
-                                                  (4, 40000, synth.F32, True), (3, 128256, synth.BF16, True)])
+                                                  (4, 40000, synth.F32, True), (3, 128256, synth.BF16, True),
+                                                  (2, 50257, synth.BF16, False), (3, 50257, synth.BF16, True)])
 def test_multi_draft(dev, K, V, dtype, stochastic):
     G, gamma = 6, 4
     w = synth.make_multi(G, K, gamma, V, dtype, 0.8, seed=K * 1000 + V % 997)
