@@ -160,6 +160,26 @@ def test_staged_path_ties_and_flat_rows(dev):
             compare_stochastic(w, run_stochastic(w, dev, offset=off), [0])
 
 
+@pytest.mark.parametrize("V,dtype,offset", [(3001, synth.BF16, 0), (128256, synth.BF16, 3), (5001, synth.F32, 1)])
+def test_staged_path_tree(dev, V, dtype, offset):
+    """The tree call on rows off the 16-byte grid (an odd vocabulary, a shifted buffer):
+    the argmax of every node's row, its lowest index on ties, the deepest accepted path."""
+    w = synth.make_tree(12, V, dtype, seed=V % 1000 + offset)
+    res = run_tree(w, dev, offset=offset)
+    assert res["device_status"][0] == 0
+    compare_tree(w, res, range(w.B))
+    assert np.any(res["accept_len"] > 1)
+
+
+def test_staged_path_nkl_positions(dev):
+    """The position-adaptive NKL mask on an odd vocabulary (staged pairs)."""
+    w = synth.make_stochastic(12, 50257, synth.BF16, 0.8, seed=88, gamma_range=(1, 6), agreement=0.8)
+    pos = np.random.default_rng(88).integers(1, 3000, w.B).astype(np.int32)
+    compare_nkl(w, run_nkl(w, dev, positions=pos), range(w.B), positions=pos)
+    res = run_stochastic(w, dev, options={"position": pos, "min_block_len": 2})
+    compare_stochastic(w, res, range(w.B), positions=pos, min_block_len=2)
+
+
 def test_staged_path_headline_shape(dev):
     """The headline batch (B=256, gamma=8, V=128256, bf16) with the logits one element off
     the 16-byte grid: every sampler range and tier, sampled against the oracle."""
