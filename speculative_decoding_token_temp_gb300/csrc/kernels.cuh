@@ -274,20 +274,6 @@ struct IO<float, 4> {
   }
 };
 
-template <>
-struct IO<uint16_t, 1> {
-  using raw_t = unsigned short;
-  __device__ static raw_t load(const uint16_t* row, int v) { return __ldg(reinterpret_cast<const unsigned short*>(row) + v); }
-  __device__ static void unpack(const raw_t& r, float (&f)[1]) { f[0] = __uint_as_float(((unsigned)r) << 16); }
-};
-
-template <>
-struct IO<float, 1> {
-  using raw_t = float;
-  __device__ static raw_t load(const float* row, int v) { return __ldg(row + v); }
-  __device__ static void unpack(const raw_t& r, float (&f)[1]) { f[0] = r; }
-};
-
 template <typename E>
 __device__ __forceinline__ float elem_at(const E* row, int x);
 template <>
@@ -480,8 +466,7 @@ constexpr float kLazy = 32.f;
 struct TAcc {
   float m, mr, mth, nmc, lo, hi;
   float2 s;
-  int idx;     // lowest index of m (scalar path), or -1 until resolved
-  int g0, g1;  // element bases of the group that holds m (vector path; resolved at the tile end)
+  int g0, g1;  // the group that holds m (resolved to the lowest index at the tile end; g0 < 0: none)
 };
 struct DAcc {
   float mr, mth, nmc;
@@ -492,7 +477,7 @@ struct DAcc {
 
 __device__ __forceinline__ void init(TAcc& a) {
   a.m = -INFINITY; a.mr = -INFINITY; a.mth = -INFINITY; a.nmc = 0.f; a.lo = INFINITY; a.hi = -INFINITY;
-  a.s = make_float2(0.f, 0.f); a.idx = INT_MAX; a.g0 = -1; a.g1 = -1;
+  a.s = make_float2(0.f, 0.f); a.g0 = -1; a.g1 = -1;
 }
 __device__ __forceinline__ void init(DAcc& a) {
   a.mr = -INFINITY; a.mth = -INFINITY; a.nmc = 0.f; a.s = make_float2(0.f, 0.f); a.k = make_float2(0.f, 0.f);
@@ -550,20 +535,20 @@ __device__ __forceinline__ float2 exp_sum2(const float (&t)[VEC], float c, float
   }
 }
 
-// Exact max. A single-element group (scalar path) records its index directly; a wider
-// group only records where it starts, and the lowest index inside it is found once, at
-// the end of the tile, by the thread that holds the tile's maximum (resolve_index).
-// H == 0 marks a strided group (staged path): its VEC elements sit at e0 + k * GS, GS
-// the stride the tile's reduction is given, and g1 records their count (resolve_strided).
+// Exact max. A group only records where it starts, and the lowest index inside it is
+// found once, at the end of the tile, by the thread that holds the tile's maximum: a
+// contiguous group of 16-byte vectors (the first H elements from e0, the rest from e1)
+// by resolve_index; a strided group (H == 0, staged path: its VEC elements at
+// e0 + k * GS, GS the stride the tile's reduction is given; g1 records their count) by
+// resolve_strided.
 template <int VEC, int H, bool IDX>
 __device__ __forceinline__ void track_max(TAcc& a, const float (&t)[VEC], float vm, int e0, int e1) {
+  static_assert(H == 0 || VEC > 1, "a contiguous group is at least one vector");
   if (IDX) {
     if (vm > a.m) {
       if constexpr (H == 0) {
         a.g0 = e0;
         a.g1 = VEC;
-      } else if constexpr (VEC == 1) {
-        a.idx = e0;
       } else {
         a.g0 = e0;
         a.g1 = (H == VEC) ? e0 + H : e1;
@@ -725,14 +710,13 @@ __device__ __forceinline__ Partial reduce_tile(int kind, const TAcc& ta, const D
     TM = fmaxf(TM, s_m[0][w]);
     DM = fmaxf(DM, s_m[1][w]);
   }
+  static_assert(GS > 0 || VEC > 1, "groups are strided (GS) or whole vectors (VEC)");
   int my_idx = INT_MAX;
   if (ta.m == TM) {
     if constexpr (GS > 0)
       my_idx = row ? resolve_strided<E, GS>(row, ta.g0, ta.g1, TM) : INT_MAX;
-    else if constexpr (VEC > 1)
-      my_idx = row ? resolve_index<E, VEC>(row, ta.g0, ta.g1, TM) : INT_MAX;
     else
-      my_idx = ta.idx;
+      my_idx = row ? resolve_index<E, VEC>(row, ta.g0, ta.g1, TM) : INT_MAX;
   }
   const int wi = warp_min_i(my_idx);
   float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f, v4 = 0.f;

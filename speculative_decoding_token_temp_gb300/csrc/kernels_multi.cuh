@@ -227,6 +227,150 @@ __global__ void __launch_bounds__(kThreads, 2) pair_kernel(const __grid_constant
   pair_merge<K>(p, gi);
 }
 
+// Rows off the 16-byte grid: the same pairwise sums through per-warp bulk-copy rings (as
+// the tile kernel's staged path). Warp w takes the w-th contiguous run of every stage of
+// the K rows, one slot per row (each with its own phase); lane l reads the elements
+// l, l + 32, ... of a run and folds them in as strided groups.
+template <int K>
+__host__ __device__ constexpr int pair_staged_smem() {
+  return kCS * kWarps * K * kWarpSlot;
+}
+
+// The lazy-reference update and the sums of one group of G elements of every row.
+template <int K, int G>
+__device__ __forceinline__ void pair_fold(float (&mr)[K], float (&mth)[K], float (&nmc)[K], float (&s)[K],
+                                          float (&kk)[K][K], const float (&z)[K][G], float c) {
+#pragma unroll
+  for (int a = 0; a < K; ++a) {
+    const float vm = vmax<G>(z[a]);
+    const bool mv = vm > mth[a];
+    if (__any_sync(__activemask(), mv)) {
+      if (mv) {
+        const float f = ex2((mr[a] - vm) * c);
+        s[a] *= f;
+#pragma unroll
+        for (int b = 0; b < K; ++b) kk[a][b] *= f;
+        mr[a] = vm;
+        mth[a] = vm + kLazy / c;
+        nmc[a] = -vm * c;
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < G; ++j) {
+#pragma unroll
+    for (int a = 0; a < K; ++a) {
+      const float e = ex2(fmaf(z[a][j], c, nmc[a]));
+      s[a] += e;
+#pragma unroll
+      for (int b = 0; b < K; ++b)
+        if (b != a) kk[a][b] = fmaf(e, z[a][j] - z[b][j], kk[a][b]);
+    }
+  }
+}
+
+template <typename E, int K>
+__global__ void __launch_bounds__(kThreads, 2) pair_staged_kernel(const __grid_constant__ PairParams p) {
+  extern __shared__ __align__(128) unsigned char dsm[];
+  griddep_wait();  // earlier work on the stream (the verification, the prologue) has completed
+  griddep_launch();
+  __shared__ int s_last;
+  __shared__ __align__(8) uint64_t s_bars[kWarps][kCS];
+  constexpr int SW = kWarpRowBytes / (int)sizeof(E);  // elements of a warp's run of a row
+  constexpr int S = SW * kWarps;                      // elements of a stage
+  constexpr int U = SW / 32;                          // per lane per run and row
+  constexpr unsigned WSTAGE = K * kWarpSlot;          // a warp's part of one stage
+  const int tile = blockIdx.x;
+  const int gi = tile / p.nchunks, chunk = tile - gi * p.nchunks;
+  const int g = gi / p.gamma, i = gi - g * p.gamma;
+  const size_t V = (size_t)p.V;
+  const E* rows[K];
+#pragma unroll
+  for (int a = 0; a < K; ++a)
+    rows[a] = static_cast<const E*>(p.draft) + ((size_t)(g * K + a) * p.gamma + i) * V;
+  const int e_begin = chunk * p.chunk_elems;
+  const int e_end = min(e_begin + p.chunk_elems, p.V);
+  const float c = p.c;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+  float mr[K], mth[K], nmc[K], s[K], kk[K][K];
+  int ph[K];  // S and SW elements are whole 16-byte blocks: every run of a row has its phase
+#pragma unroll
+  for (int a = 0; a < K; ++a) {
+    mr[a] = -INFINITY;
+    mth[a] = -INFINITY;
+    nmc[a] = 0.f;
+    s[a] = 0.f;
+    ph[a] = phase16(rows[a] + e_begin);
+#pragma unroll
+    for (int b = 0; b < K; ++b) kk[a][b] = 0.f;
+  }
+  WarpRing ring;
+  ring.init(s_bars[warp]);
+  const uint32_t wbase = (uint32_t)__cvta_generic_to_shared(dsm) + (uint32_t)warp * WSTAGE;
+  const int nst = (e_end - e_begin + S - 1) / S;
+  auto issue = [&](int k) {
+    if (lane == 0 && k < nst) {
+      const uint32_t slot = wbase + (uint32_t)((k % kCS) * kWarps) * WSTAGE;
+      const int e0 = e_begin + k * S + warp * SW, n = min(SW, e_end - e0);
+      const void* src[K];
+      uint32_t nb[K], total = 0u;
+#pragma unroll
+      for (int a = 0; a < K; ++a) {
+        src[a] = nullptr;
+        nb[a] = run_blocks<E>(rows[a], e0, n, &src[a]);
+        total += nb[a];
+      }
+      const uint32_t bar = ring.bars + 8u * (uint32_t)(k % kCS);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the reads of the slot precede the copies
+      mbar_expect_arrive(bar, total);
+#pragma unroll
+      for (int a = 0; a < K; ++a)
+        if (nb[a]) bulk_copy(slot + (uint32_t)a * kWarpSlot, src[a], nb[a], bar);
+    }
+  };
+#pragma unroll
+  for (int k = 0; k < kCS - 1; ++k) issue(k);
+  for (int k = 0; k < nst; ++k) {
+    __syncwarp();        // every lane is done with stage k - 1
+    issue(k + kCS - 1);  // into the slot of stage k - 1
+    ring.wait(k, p.status);
+    const unsigned char* slot = dsm + (size_t)(warp + (k % kCS) * kWarps) * WSTAGE;
+    const int n = min(SW, e_end - (e_begin + k * S + warp * SW));
+    if (lane + (U - 1) * 32 < n) {  // the whole strided group is inside the run
+      float z[K][U];
+#pragma unroll
+      for (int a = 0; a < K; ++a) {
+        const E* sr = reinterpret_cast<const E*>(slot + a * kWarpSlot) + ph[a];
+#pragma unroll
+        for (int j = 0; j < U; ++j) z[a][j] = sh_elem<E>(sr, lane + 32 * j);
+      }
+      pair_fold<K, U>(mr, mth, nmc, s, kk, z, c);
+    } else {
+      for (int x = lane; x < n; x += 32) {
+        float z[K][1];
+#pragma unroll
+        for (int a = 0; a < K; ++a)
+          z[a][0] = sh_elem<E>(reinterpret_cast<const E*>(slot + a * kWarpSlot) + ph[a], x);
+        pair_fold<K, 1>(mr, mth, nmc, s, kk, z, c);
+      }
+    }
+  }
+
+  pair_partial_write<K>(p.part + tile, mr, s, kk, c);
+  __syncthreads();  // every writer's partial entries precede thread 0's fence
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned old = atomicAdd(p.cnt + gi, 1u);
+    s_last = (old + 1u == (unsigned)p.nchunks) ? 1 : 0;
+    if (s_last) __threadfence();
+  }
+  __syncthreads();
+  if (!s_last) return;
+
+  pair_merge<K>(p, gi);
+}
+
 // sum_j e[j] (x[j] - y[j]) with packed f32x2 subtractions and FMAs
 template <int VEC>
 __device__ __forceinline__ float dot_diff(const float (&e)[VEC], const float (&x)[VEC], const float (&y)[VEC]) {

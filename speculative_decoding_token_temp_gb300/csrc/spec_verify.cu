@@ -526,9 +526,38 @@ cudaError_t launch_pair_t(int K, const PairParams& pp, long long tiles, cudaStre
   return launch(pair_kernel<E, VEC, 4>, grid, block, stream, pp, true);
 }
 
+template <typename E, int K>
+cudaError_t launch_pair_staged_k(const PairParams& pp, long long tiles, cudaStream_t stream) {
+  auto kern = pair_staged_kernel<E, K>;
+  constexpr int smem = pair_staged_smem<K>();
+  static std::atomic<unsigned long long> done{0};
+  const cudaError_t e = ensure_smem_attr(kern, done, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3((unsigned)tiles);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, pp);
+}
+
+template <typename E>
+cudaError_t launch_pair_staged(int K, const PairParams& pp, long long tiles, cudaStream_t stream) {
+  if (K == 2) return launch_pair_staged_k<E, 2>(pp, tiles, stream);
+  if (K == 3) return launch_pair_staged_k<E, 3>(pp, tiles, stream);
+  return launch_pair_staged_k<E, 4>(pp, tiles, stream);
+}
+
+// aligned rows: 16-byte vector loads; any other layout: the staged kernel
 cudaError_t launch_pair(bool bf16, bool vec, int K, const PairParams& pp, long long tiles, cudaStream_t stream) {
-  if (bf16) return vec ? launch_pair_t<uint16_t, 8>(K, pp, tiles, stream) : launch_pair_t<uint16_t, 1>(K, pp, tiles, stream);
-  return vec ? launch_pair_t<float, 4>(K, pp, tiles, stream) : launch_pair_t<float, 1>(K, pp, tiles, stream);
+  if (bf16) return vec ? launch_pair_t<uint16_t, 8>(K, pp, tiles, stream) : launch_pair_staged<uint16_t>(K, pp, tiles, stream);
+  return vec ? launch_pair_t<float, 4>(K, pp, tiles, stream) : launch_pair_staged<float>(K, pp, tiles, stream);
 }
 
 }  // namespace
