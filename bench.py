@@ -28,7 +28,6 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "verified rows/s & HBM GB/s vs GB300 peak (B=256, gamma=8, V=128256, bf16)"
-HEADLINE = 2
 
 
 def peaks():
@@ -384,7 +383,7 @@ def run_ours(args):
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
     __graft_entry__.build()
-    cfg = synth.CONFIGS[HEADLINE]
+    cfg = synth.HEADLINE
     from speculative_decoding_token_temp_gb300 import sharding
     w = cfg.make(seed=sharding.rank_seed(cfg.seed, rank), B=args.batch)
     call = StochasticCall(w, dev, host_inputs=True, offset=args.offset)
@@ -486,7 +485,7 @@ def run_ours(args):
                         "multiple of 16 bytes): per-warp bulk-copy rings read back at the row's phase"}
             del ts, ds, s_out, sg_out
         del res
-        tw = synth.CONFIGS[3].make()
+        tw = synth.TREE.make()
         tt = _to_dev(tw.target, dev)
         tn = _to_dev(tw.node_tokens, dev)
         t_out = {}
@@ -496,7 +495,7 @@ def run_ours(args):
         modes["tree_B32_N12_V128256"] = {"us_per_call": t_t * 1e6, "GBps": tbytes / t_t / 1e9,
                                          "rows_per_s": tw.B * (tw.N + 1) / t_t}
         del tt, tn
-        w1 = synth.CONFIGS[1].make(T=0.6)
+        w1 = synth.MID.make(T=0.6)
         c1 = StochasticCall(w1, dev)
         t_1 = time_mode(lambda: c1(sh), 500, 10, dev)
         b1 = algorithmic_bytes(w1)["stochastic"]
@@ -505,7 +504,7 @@ def run_ours(args):
                                                      "note": "53 MB of inputs fit in L2: warm-cache figure"}
         del c1
         if not args.skip_ragged:
-            w4 = synth.CONFIGS[4].make()
+            w4 = synth.RAGGED.make()
             c4 = StochasticCall(w4, dev)
             t_4 = time_mode(lambda: c4(sh), 100, 5, dev)
             b4 = algorithmic_bytes(w4)["stochastic"]
@@ -566,7 +565,7 @@ def run_reference(args):
         return
     from oracle import oracle as O
     from speculative_decoding_token_temp_gb300 import synth
-    cfg = synth.CONFIGS[HEADLINE]
+    cfg = synth.HEADLINE
     g = cfg.gamma
     budget = 120.0
     cal = synth.make_stochastic(1, cfg.V, cfg.dtype, cfg.T[0], cfg.seed + 77, gamma=g)

@@ -305,7 +305,6 @@ def make_tree(B: int, V: int, dtype: str, seed: int, parent=TREE_PARENT, agreeme
 
 @dataclass
 class Config:
-    index: int
     name: str
     kind: str                    # "stochastic" or "tree"
     B: int
@@ -331,11 +330,10 @@ class Config:
 # The five workloads: a tiny fp32 case, a mid-size bf16 case at two temperatures,
 # the B=256 / gamma=8 / V=128256 headline, the 12-node tree, and the ragged
 # multi-token-head batch with gamma_b ~ U{1..16} over a 152064-token vocabulary.
-CONFIGS = {
-    0: Config(0, "tiny_B1_g4_V1000_f32", "stochastic", B=1, V=1000, dtype=F32, T=(1.0,), gamma=4, seed=0),
-    1: Config(1, "B64_g5_V32000_bf16", "stochastic", B=64, V=32000, dtype=BF16, T=(0.6, 1.0), gamma=5, seed=1),
-    2: Config(2, "B256_g8_V128256_bf16", "stochastic", B=256, V=128256, dtype=BF16, T=(0.6,), gamma=8, seed=2),
-    3: Config(3, "tree_B32_N12_V128256_bf16", "tree", B=32, V=128256, dtype=BF16, seed=3),
-    4: Config(4, "ragged_B512_g1-16_V152064_bf16", "stochastic", B=512, V=152064, dtype=BF16, T=(0.8,),
-              gamma_range=(1, 16), agreement=0.7, seed=4),
-}
+TINY = Config("tiny_B1_g4_V1000_f32", "stochastic", B=1, V=1000, dtype=F32, T=(1.0,), gamma=4, seed=0)
+MID = Config("B64_g5_V32000_bf16", "stochastic", B=64, V=32000, dtype=BF16, T=(0.6, 1.0), gamma=5, seed=1)
+HEADLINE = Config("B256_g8_V128256_bf16", "stochastic", B=256, V=128256, dtype=BF16, T=(0.6,), gamma=8, seed=2)
+TREE = Config("tree_B32_N12_V128256_bf16", "tree", B=32, V=128256, dtype=BF16, seed=3)
+RAGGED = Config("ragged_B512_g1-16_V152064_bf16", "stochastic", B=512, V=152064, dtype=BF16, T=(0.8,),
+                gamma_range=(1, 16), agreement=0.7, seed=4)
+WORKLOADS = {c.name: c for c in (TINY, MID, HEADLINE, TREE, RAGGED)}

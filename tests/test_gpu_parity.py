@@ -30,16 +30,16 @@ def dev():
 _CACHE = {}
 
 
-def workload(i):
-    if i not in _CACHE:
-        _CACHE[i] = synth.CONFIGS[i].make()
-    return _CACHE[i]
+def workload(cfg):
+    if cfg.name not in _CACHE:
+        _CACHE[cfg.name] = cfg.make()
+    return _CACHE[cfg.name]
 
 
 # ---------------------------------------------------------------- the five workloads
 
-def test_config0_tiny_f32(dev):
-    w = workload(0)
+def test_tiny_B1_g4_V1000_f32(dev):
+    w = workload(synth.TINY)
     res = run_stochastic(w, dev)
     compare_stochastic(w, res, range(w.B))
     assert res["device_status"][0] == 0
@@ -48,18 +48,18 @@ def test_config0_tiny_f32(dev):
 
 
 @pytest.mark.parametrize("T", [0.6, 1.0])
-def test_config1_bf16_all_sequences(dev, T):
-    w = synth.CONFIGS[1].make(T=T)
+def test_B64_g5_V32000_bf16_all_sequences(dev, T):
+    w = synth.MID.make(T=T)
     res = run_stochastic(w, dev)
     n, flagged, mismatched = compare_stochastic(w, res, range(w.B))
-    print(f"config 1 T={T}: {flagged} of {n} sequences flagged, {mismatched} differ")
+    print(f"B=64 workload, T={T}: {flagged} of {n} sequences flagged, {mismatched} differ")
     assert res["device_status"][0] == 0
     compare_greedy(w, run_greedy(w, dev), range(w.B))
     compare_nkl(w, run_nkl(w, dev), range(w.B))
 
 
-def test_config2_headline_sampled(dev):
-    w = workload(2)
+def test_headline_B256_g8_V128256_sampled(dev):
+    w = workload(synth.HEADLINE)
     res = run_stochastic(w, dev)
     assert res["device_status"][0] == 0
     seqs = sample_seqs(w.B, 12, seed=2)
@@ -84,21 +84,21 @@ def test_config2_headline_sampled(dev):
 NKL_FLOOR = 1e-6
 
 
-def test_config2_nkl_standalone_sampled(dev):
-    w = workload(2)
+def test_headline_nkl_standalone_sampled(dev):
+    w = workload(synth.HEADLINE)
     res = run_nkl(w, dev)
     compare_nkl(w, res, sample_seqs(w.B, 6, seed=5))
 
 
-def test_config3_tree_all_sequences(dev):
-    w = synth.CONFIGS[3].make()
+def test_tree_B32_N12_V128256_all_sequences(dev):
+    w = synth.TREE.make()
     res = run_tree(w, dev)
     assert res["device_status"][0] == 0
     compare_tree(w, res, range(w.B))
 
 
-def test_config4_ragged_sampled(dev):
-    w = synth.CONFIGS[4].make()
+def test_ragged_B512_V152064_sampled(dev):
+    w = synth.RAGGED.make()
     assert not w.dense
     res = run_stochastic(w, dev)
     assert res["device_status"][0] == 0
@@ -183,7 +183,7 @@ def test_staged_path_nkl_positions(dev):
 def test_staged_path_headline_shape(dev):
     """The headline batch (B=256, gamma=8, V=128256, bf16) with the logits one element off
     the 16-byte grid: every sampler range and tier, sampled against the oracle."""
-    w = workload(2)
+    w = workload(synth.HEADLINE)
     res = run_stochastic(w, dev, offset=1)
     assert res["device_status"][0] == 0
     compare_stochastic(w, res, sample_seqs(w.B, 8, seed=12))

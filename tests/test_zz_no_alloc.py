@@ -36,7 +36,7 @@ def _t(a, dev):
 
 
 def test_static_scratch_matches_workspace_call(dev):
-    w = synth.CONFIGS[1].make(T=0.6)
+    w = synth.MID.make(T=0.6)
     g = int(w.gammas[0])
     t, d = _t(w.target, dev), _t(w.draft, dev)
     tok, ua, us = _t(w.tokens, dev), _t(w.u_accept, dev), _t(w.u_sample, dev)
