@@ -343,6 +343,16 @@ spec_status spec_verify_stochastic_static(spec_batch g, spec_dtype dtype, const 
                                           int32_t* greedy_n, int32_t* greedy_tokens, uint32_t* device_status,
                                           spec_stream_t stream);
 
+/* Self-test of the bounded waits (failure detection without a GPU fault): re-arms one
+ * sequence in `workspace` and launches the stochastic call's sampler over it with no tile
+ * kernel, so the sequence's decision is never published and the tile count never
+ * completes. The sampler gives up after its poll limit (well under a second), ORs
+ * SPEC_DEV_TIMEOUT into *device_status and returns; the context stays usable. Nothing is
+ * read from any logits. workspace: at least spec_workspace_bytes() of a dense bf16 batch
+ * with B = 1, gamma = 1, V = 8, 256-byte aligned. Host errors as for the other calls. */
+spec_status spec_selftest_wait_timeout(uint32_t* device_status, void* workspace, size_t workspace_bytes,
+                                       spec_stream_t stream);
+
 /* A static English description of a spec_status value. */
 const char* spec_status_str(spec_status s);
 

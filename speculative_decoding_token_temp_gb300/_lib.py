@@ -88,6 +88,7 @@ SIGNATURES = {
     "spec_multi_workspace_bytes": (_S, [SpecMultiBatch, ctypes.c_int, _I]),
     "spec_verify_multi": (ctypes.c_int, [SpecMultiBatch, ctypes.c_int, _I, _P, _P, _P, _F, _P, _P, _F, _F, _P, _P,
                                          _P, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
+    "spec_selftest_wait_timeout": (ctypes.c_int, [_P, _P, _S, _P]),
     "spec_status_str": (ctypes.c_char_p, [ctypes.c_int]),
 }
 

@@ -825,6 +825,51 @@ spec_status spec_accept_summary(const spec_accept_stats* stats, int64_t bucket_n
   return SPEC_OK;
 }
 
+spec_status spec_selftest_wait_timeout(uint32_t* device_status, void* workspace, size_t workspace_bytes,
+                                       spec_stream_t stream_) {
+  // one dense sequence, one draft, an 8-token bf16 vocabulary: the prologue re-arms its
+  // record, and the sampler waits for a decision and a tile count that no tile kernel
+  // ever provides (nothing is read from the logits: the record never becomes ready)
+  spec_batch g;
+  g.B = 1;
+  g.gamma = 1;
+  g.V = 8;
+  g.total_draft = 1;
+  g.cu_draft = nullptr;
+  if (!device_status || !aligned_to(4, {device_status})) return SPEC_ERR_INVALID_ARG;
+  const Layout L = layout(g.B, g.V, rows_for(SPEC_MODE_STOCHASTIC, g), true, false, SPEC_BF16);
+  if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u)) return SPEC_ERR_WORKSPACE;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  char* ws = static_cast<char*>(workspace);
+  if (launch_prologue(g, L, ws, device_status, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  SampleParams sp;
+  memset(&sp, 0, sizeof(sp));
+  sp.V = g.V;
+  sp.total_rows = (int)L.rows;
+  sp.total_draft = g.total_draft;
+  sp.B = g.B;
+  sp.c = sp.cd = 1.f;
+  sp.rec = reinterpret_cast<SeqRec*>(ws + L.rec);
+  sp.cnt = reinterpret_cast<unsigned*>(ws + L.cntB);
+  sp.status = device_status;
+  sp.table = reinterpret_cast<float*>(ws + L.table);
+  sp.table_stride = L.table_stride;
+  sp.tiles_done = reinterpret_cast<const unsigned*>(ws + L.cntA) + g.B;  // zeroed by the prologue, never counted
+  sp.ntiles = 1u;
+  sp.head_total = 0;
+  sp.nb_head = 0;
+  sp.seg_head = 1;
+  sp.seg_tail = kTailStages;
+  // an ordinary stream-ordered launch (no programmatic dependent launch): the sampler
+  // starts only after the prologue has completed, so the record it polls is re-armed
+  auto kern = sample2_kernel<uint16_t, 8, false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowsSmem) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  kern<<<1, kThreads, kRowsSmem, stream>>>(sp);
+  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  return SPEC_OK;
+}
+
 const char* spec_status_str(spec_status s) {
   switch (s) {
     case SPEC_OK: return "ok";

@@ -101,6 +101,10 @@ def test_host_validation_without_launch(lib):
                                 one, one, 1 << 30, None) == _lib.SPEC_ERR_INVALID_ARG
     out = (ctypes.c_double * 6)()
     assert lib.spec_accept_summary(P(260), 0, 4, ctypes.cast(out, P), None) == _lib.SPEC_ERR_INVALID_ARG
+    assert lib.spec_selftest_wait_timeout(None, one, 1 << 30, None) == _lib.SPEC_ERR_INVALID_ARG
+    assert lib.spec_selftest_wait_timeout(P(258), one, 1 << 30, None) == _lib.SPEC_ERR_INVALID_ARG
+    assert lib.spec_selftest_wait_timeout(one, None, 1 << 30, None) == _lib.SPEC_ERR_WORKSPACE
+    assert lib.spec_selftest_wait_timeout(one, one, 16, None) == _lib.SPEC_ERR_WORKSPACE
     bad_parent = (ctypes.c_int32 * 2)(-1, 5)
     assert lib.spec_verify_tree(2, 2, 100, _lib.SPEC_BF16, one, one, ctypes.cast(bad_parent, P), one, one, one,
                                 one, one, 1 << 30, None) == _lib.SPEC_ERR_INVALID_ARG
