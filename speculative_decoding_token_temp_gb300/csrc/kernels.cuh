@@ -687,9 +687,9 @@ __device__ __forceinline__ int resolve_strided(const E* row, int g0, int g1, flo
 }
 
 // row != nullptr: the target maximum's index is resolved from the recorded groups
-// (strided groups of stride GS when GS > 0). SEPT: the draft sum s is at scale cd, s2
-// and k at c.
-template <class SY, typename E = float, int VEC = 1, bool SEPT = false, int GS = 0>
+// (strided groups of stride GS when GS > 0); PRE: the caller has already resolved it into
+// ta.g0. SEPT: the draft sum s is at scale cd, s2 and k at c.
+template <class SY, typename E = float, int VEC = 1, bool SEPT = false, int GS = 0, bool PRE = false>
 __device__ __forceinline__ Partial reduce_tile(int kind, const TAcc& ta, const DAcc& da, float c,
                                                const E* row = nullptr, float cd = 0.f) {
   constexpr int NW = SY::NT / 32;
@@ -713,7 +713,9 @@ __device__ __forceinline__ Partial reduce_tile(int kind, const TAcc& ta, const D
   static_assert(GS > 0 || VEC > 1, "groups are strided (GS) or whole vectors (VEC)");
   int my_idx = INT_MAX;
   if (ta.m == TM) {
-    if constexpr (GS > 0)
+    if constexpr (PRE)
+      my_idx = ta.g0 >= 0 ? ta.g0 : INT_MAX;
+    else if constexpr (GS > 0)
       my_idx = row ? resolve_strided<E, GS>(row, ta.g0, ta.g1, TM) : INT_MAX;
     else
       my_idx = row ? resolve_index<E, VEC>(row, ta.g0, ta.g1, TM) : INT_MAX;

@@ -364,9 +364,12 @@ __device__ __forceinline__ void unpack2(const uint4& a, const uint4& b, float (&
 // registers held by loads in flight. A stage is kCV vectors per thread: for a pair the
 // vectors v and v + 256 of the target and of the draft row, for a single row the vectors
 // v, v + 256, v + 512, v + 768; each pair of vectors is folded in as one group.
+// Argmax rows (KIND == K_ARGMAX) also keep, in `best`, the raw vectors of the group that
+// holds the thread's maximum, so the tile end resolves its lowest index without
+// re-reading the row.
 template <typename E, int VEC, int MODE, int KIND>
 __device__ __forceinline__ void stream_tile(const E* trow, const E* drow, int v0, int v1, float c, float cd,
-                                            TAcc& ta, DAcc& da, unsigned char* smem) {
+                                            TAcc& ta, DAcc& da, unsigned char* smem, uint4 (&best)[2]) {
   constexpr bool IDX = is_stoch(MODE), SEPT = MODE == M_STOCH2;
   constexpr int PER = (KIND == K_PAIR) ? 2 * kThreads : 4 * kThreads;  // vectors of a row per stage
   constexpr unsigned SLOT = kCV * kThreads * 16;                         // bytes of one stage
@@ -418,18 +421,27 @@ __device__ __forceinline__ void stream_tile(const E* trow, const E* drow, int v0
         const int pa = va + 2 * h * kThreads, pb = pa + kThreads;
         if (pb < v1) {
           float ft[2 * VEC];
-          unpack2<E, VEC>(q[(2 * h) * kThreads], q[(2 * h + 1) * kThreads], ft);
-          if constexpr (KIND == K_TSUM)
+          const uint4 r0 = q[(2 * h) * kThreads], r1 = q[(2 * h + 1) * kThreads];
+          unpack2<E, VEC>(r0, r1, ft);
+          if constexpr (KIND == K_TSUM) {
             tsum_update<2 * VEC, VEC>(ta, ft, pa * VEC, c, pb * VEC);
-          else
+          } else {
+            if (vmax_nan<2 * VEC>(ft) > ta.m) {
+              best[0] = r0;
+              best[1] = r1;
+            }
             argmax_update<2 * VEC, VEC>(ta, ft, pa * VEC, pb * VEC);
+          }
         } else if (pa < v1) {
           float ft[VEC];
-          IO<E, VEC>::unpack(q[(2 * h) * kThreads], ft);
-          if constexpr (KIND == K_TSUM)
+          const uint4 r0 = q[(2 * h) * kThreads];
+          IO<E, VEC>::unpack(r0, ft);
+          if constexpr (KIND == K_TSUM) {
             tsum_update<VEC>(ta, ft, pa * VEC, c);
-          else
+          } else {
+            if (vmax_nan<VEC>(ft) > ta.m) best[0] = best[1] = r0;  // a one-vector group: its first VEC
             argmax_update<VEC>(ta, ft, pa * VEC);
+          }
         }
       }
     }
@@ -585,16 +597,28 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
   DAcc da;
   init(ta);
   init(da);
+  constexpr bool ARGMAX = MODE == M_GREEDY || MODE == M_TREE;
   if constexpr (VEC > 1) {
-    if constexpr (MODE == M_GREEDY || MODE == M_TREE) {
-      stream_tile<E, VEC, MODE, K_ARGMAX>(trow, drow, e_begin / VEC, v1, c, cd, ta, da, dsm);
+    uint4 best[2];
+    if constexpr (ARGMAX) {
+      stream_tile<E, VEC, MODE, K_ARGMAX>(trow, drow, e_begin / VEC, v1, c, cd, ta, da, dsm, best);
+      // the lowest index of the thread's maximum, from the raw vectors of its group
+      if (ta.g0 >= 0) {
+        float f[2 * VEC];
+        unpack2<E, VEC>(best[0], best[1], f);
+        int k = 2 * VEC - 1;
+#pragma unroll
+        for (int j = 2 * VEC - 2; j >= 0; --j)
+          if (f[j] == ta.m) k = j;
+        ta.g0 = k < VEC ? ta.g0 + k : ta.g1 + (k - VEC);
+      }
     } else if constexpr (MODE == M_NKL) {
-      stream_tile<E, VEC, MODE, K_PAIR>(trow, drow, e_begin / VEC, v1, c, cd, ta, da, dsm);
+      stream_tile<E, VEC, MODE, K_PAIR>(trow, drow, e_begin / VEC, v1, c, cd, ta, da, dsm, best);
     } else {
       if (kind == K_PAIR)
-        stream_tile<E, VEC, MODE, K_PAIR>(trow, drow, e_begin / VEC, v1, c, cd, ta, da, dsm);
+        stream_tile<E, VEC, MODE, K_PAIR>(trow, drow, e_begin / VEC, v1, c, cd, ta, da, dsm, best);
       else
-        stream_tile<E, VEC, MODE, K_TSUM>(trow, drow, e_begin / VEC, v1, c, cd, ta, da, dsm);
+        stream_tile<E, VEC, MODE, K_TSUM>(trow, drow, e_begin / VEC, v1, c, cd, ta, da, dsm, best);
     }
   } else {
     if constexpr (MODE == M_GREEDY || MODE == M_TREE) {
@@ -611,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
 
   Partial part;
   if constexpr (VEC > 1)
-    part = reduce_tile<BlockSync, E, VEC, SEPT>(kind, ta, da, c, trow, cd);
+    part = reduce_tile<BlockSync, E, VEC, SEPT, 0, ARGMAX>(kind, ta, da, c, trow, cd);
   else
     part = reduce_tile<BlockSync, E, 1, SEPT, 32>(kind, ta, da, c, trow, cd);
   if (threadIdx.x == 0) {
