@@ -132,7 +132,6 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
   constexpr int NT = SY::NT, NW = SY::NT / 32;
   __shared__ RowStat rs[kMaxRows];
   __shared__ int s_tok[MODE == M_TREE ? SPEC_MAX_TREE_NODES : 1], s_par[MODE == M_TREE ? SPEC_MAX_TREE_NODES : 1];
-  __shared__ int depth[MODE == M_TREE ? SPEC_MAX_TREE_NODES : 1];
   __shared__ int s_n, s_gn;
   __shared__ unsigned s_err;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -174,51 +173,73 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
   const E* draft = static_cast<const E*>(p.draft);
 
   if constexpr (MODE == M_TREE) {
-    // one thread walks the (at most 64-node) tree in shared memory
-    if (tid == 0) {
+    // The first warp decides the (at most 64-node) tree: lane l holds nodes l and l + 32.
+    // A node is accepted when its token is its parent row's argmax and its parent is
+    // accepted; acceptance and depth settle from the roots down, one shuffle round per
+    // level (after round r every node of depth <= r + 1 is final).
+    if (warp == 0) {
       const int N = p.N, D = p.depth;
-      const int* tok = s_tok;
-      unsigned err = 0u;
-      for (int r = 0; r <= N; ++r)
-        if (rs[r].bad) err |= SPEC_DEV_NONFINITE;
-      for (int j = 0; j < N; ++j) {
-        const int x = tok[j];
-        if (x < 0 || x >= p.V) err |= SPEC_DEV_TOKEN_RANGE;
-      }
       int32_t* path = p.path_nodes + (size_t)b * D;
       int32_t* out = p.out_tok + (size_t)b * (D + 1);
+      int err = 0;
+      for (int r = lane; r <= N; r += 32)
+        if (rs[r].bad) err |= (int)SPEC_DEV_NONFINITE;
+      for (int j = lane; j < N; j += 32) {
+        const int x = s_tok[j];
+        if (x < 0 || x >= p.V) err |= (int)SPEC_DEV_TOKEN_RANGE;
+      }
+      err = warp_or<32>(err);
       if (err) {
-        atomicOr(p.status, err);
-        p.accept_len[b] = -1;
-        for (int k = 0; k < D; ++k) path[k] = -1;
-        for (int k = 0; k <= D; ++k) out[k] = -1;
+        if (lane == 0) {
+          atomicOr(p.status, (unsigned)err);
+          p.accept_len[b] = -1;
+        }
+        for (int k = lane; k < D; k += 32) path[k] = -1;
+        for (int k = lane; k <= D; k += 32) out[k] = -1;
         return;
       }
-      unsigned long long ok = 0ull;
-      int pick = -1, best = 0;
-      for (int j = 0; j < N; ++j) {
-        const int pj = s_par[j];
-        depth[j] = (pj < 0) ? 1 : depth[pj] + 1;
-        const int prow = (pj < 0) ? 0 : pj + 1;
-        const bool acc = tok[j] == rs[prow].tidx && (pj < 0 || ((ok >> pj) & 1ull));
-        if (acc) {
-          ok |= 1ull << j;
-          if (depth[j] > best) {
-            best = depth[j];
-            pick = j;
+      int par[2], match[2], acc[2], dep[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int j = lane + 32 * h;
+        const bool valid = j < N;
+        par[h] = valid ? s_par[j] : -1;
+        match[h] = valid && s_tok[j] == rs[par[h] < 0 ? 0 : par[h] + 1].tidx;
+        acc[h] = match[h] && par[h] < 0;
+        dep[h] = valid ? 1 : 0;
+      }
+      for (int it = 1; it < D; ++it) {
+        const int a0 = acc[0], a1 = acc[1], d0 = dep[0], d1 = dep[1];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int q = par[h] < 0 ? 0 : par[h];
+          const int sa0 = __shfl_sync(kFull, a0, q & 31), sa1 = __shfl_sync(kFull, a1, q & 31);
+          const int sd0 = __shfl_sync(kFull, d0, q & 31), sd1 = __shfl_sync(kFull, d1, q & 31);
+          if (par[h] >= 0) {
+            acc[h] = match[h] && ((q >> 5) ? sa1 : sa0);
+            dep[h] = ((q >> 5) ? sd1 : sd0) + 1;
           }
         }
       }
-      p.accept_len[b] = best;
-      int k = pick;
-      for (int d = best - 1; d >= 0; --d) {
-        path[d] = k;
-        out[d] = tok[k];
-        k = s_par[k];
+      // the deepest accepted node, ties to the lowest index: the largest (depth, -node)
+      int key = -1;
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        if (acc[h]) key = max(key, (dep[h] << 7) | (127 - (lane + 32 * h)));
+      key = __reduce_max_sync(kFull, key);
+      const int best = key >= 0 ? key >> 7 : 0, pick = key >= 0 ? 127 - (key & 127) : -1;
+      for (int d = best + lane; d < D; d += 32) path[d] = -1;
+      for (int d = best + 1 + lane; d <= D; d += 32) out[d] = -1;
+      if (lane == 0) {
+        p.accept_len[b] = best;
+        int k = pick;
+        for (int d = best - 1; d >= 0; --d) {
+          path[d] = k;
+          out[d] = s_tok[k];
+          k = s_par[k];
+        }
+        out[best] = rs[pick + 1].tidx;  // pick == -1 gives row 0
       }
-      for (int d = best; d < D; ++d) path[d] = -1;
-      out[best] = rs[pick + 1].tidx;  // pick == -1 gives row 0
-      for (int d = best + 1; d <= D; ++d) out[d] = -1;
     }
     return;
   } else if constexpr (MODE == M_NKL) {
@@ -646,13 +667,13 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
     const unsigned total = (unsigned)((gb + HB) * p.nchunks);
     const unsigned old = atomicAdd(p.cnt + b, 1u);
     s_last = (old + 1u == total) ? 1 : 0;
+    if (s_last) __threadfence();  // the other tiles' partials (read with ld.cg) precede this block's reads
   }
   __syncthreads();
   if (!s_last) {
     if (threadIdx.x == 0) tile_done<MODE>(p);
     return;
   }
-  __threadfence();
   finalize<E, MODE, BlockSync>(p, b, gb, r - i, c0);
   if constexpr (is_stoch(MODE)) {
     __syncthreads();  // the finaliser's writes, made by any thread, precede the count
