@@ -143,6 +143,27 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
     s_gn = gb;
     s_err = 0u;
   }
+  const int tb = c0 + b * HB;  // first target row of the sequence (NKL: c0 + b, set below)
+  const int db = c0;           // first draft row / token / u_accept entry
+  const E* target = static_cast<const E*>(p.target);
+  const E* draft = static_cast<const E*>(p.draft);
+  // Thread i < gb: draft position i's token and, stochastic, its uniform and z(x) of both
+  // rows, in flight while the rows merge (none of it depends on the merged statistics).
+  static_assert(NT > SPEC_MAX_GAMMA, "one draft position per thread");
+  int px = 0;
+  float pu = 0.f, pzt = 0.f, pzd = 0.f;
+  if constexpr (MODE != M_TREE && MODE != M_NKL) {
+    if (tid < gb) {
+      px = p.tokens[db + tid];
+      if constexpr (is_stoch(MODE)) {
+        pu = p.u_accept[db + tid];
+        if (px >= 0 && px < p.V) {
+          pzt = elem_at<E>(target + (size_t)(tb + tid) * V, px);
+          pzd = elem_at<E>(draft + (size_t)(db + tid) * V, px);
+        }
+      }
+    }
+  }
   if constexpr (MODE == M_TREE) {
     // the node tokens and parents go to shared memory in one coalesced read, in flight
     // while the rows merge
@@ -166,11 +187,6 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
     }
   }
   SY::sync();
-
-  const int tb = c0 + b * HB;  // first target row of the sequence (NKL: c0 + b, set below)
-  const int db = c0;           // first draft row / token / u_accept entry
-  const E* target = static_cast<const E*>(p.target);
-  const E* draft = static_cast<const E*>(p.draft);
 
   if constexpr (MODE == M_TREE) {
     // The first warp decides the (at most 64-node) tree: lane l holds nodes l and l + 32.
@@ -262,12 +278,9 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
     return;
   } else {
   // stochastic and greedy: validate the sequence first
-  for (int i = tid; i < R; i += NT) {
-    unsigned e = rs[i].bad ? SPEC_DEV_NONFINITE : 0u;
-    if (i < gb) {
-      const int x = p.tokens[db + i];
-      if (x < 0 || x >= p.V) e |= SPEC_DEV_TOKEN_RANGE;
-    }
+  if (tid < R) {  // R <= SPEC_MAX_GAMMA + 1 <= NT
+    unsigned e = rs[tid].bad ? SPEC_DEV_NONFINITE : 0u;
+    if (tid < gb && (px < 0 || px >= p.V)) e |= SPEC_DEV_TOKEN_RANGE;
     if (e) atomicOr(&s_err, e);
   }
   SY::sync();
@@ -304,22 +317,19 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
   }
 
   if constexpr (MODE == M_GREEDY) {
-    for (int i = tid; i < gb; i += NT)
-      if (p.tokens[db + i] != rs[i].tidx) atomicMin(&s_gn, i);
+    if (tid < gb && px != rs[tid].tidx) atomicMin(&s_gn, tid);
     SY::sync();
     const int n = s_gn;
-    for (int k = tid; k <= gb; k += NT)
-      p.out_tok[tb + k] = (k < n) ? p.tokens[db + k] : (k == n ? rs[n].tidx : -1);
+    if (tid <= gb) p.out_tok[tb + tid] = (tid < n) ? px : (tid == n ? rs[n].tidx : -1);
     if (tid == 0) p.n_acc[b] = n;
     policy_epilogue<SY>(p, b, gb, db, n, rs);
     return;
   } else {
   // stochastic
-  for (int i = tid; i < gb; i += NT) {
+  if (tid < gb) {
+    const int i = tid, x = px;
     const RowStat r = rs[i];
-    const int x = p.tokens[db + i];
-    const float zt = elem_at<E>(target + (size_t)(tb + i) * V, x);
-    const float zd = elem_at<E>(draft + (size_t)(db + i) * V, x);
+    const float zt = pzt, zd = pzd;
     const float lp2 = (zt - r.tm) * c - log2f(r.ts);     // log2 p(x)
     const float lq2 = (zd - r.dm) * p.cd - log2f(r.ds);  // log2 q(x), at the draft's temperature
     const float a = exp2f(fminf(0.f, lp2 - lq2));
@@ -331,13 +341,13 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
       if (p.nkl) p.nkl[db + i] = v;
       if (p.mask) p.mask[db + i] = v < nkl_threshold(p, b, i) ? 1 : 0;
     }
-    if (!(p.u_accept[db + i] <= a)) atomicMin(&s_n, i);
+    if (!(pu <= a)) atomicMin(&s_n, i);
     if (x != r.tidx) atomicMin(&s_gn, i);
   }
   SY::sync();
   const int n = s_n, gn = s_gn;
-  for (int k = tid; k <= gb; k += NT) {
-    const int xk = (k < gb) ? p.tokens[db + k] : -1;
+  if (tid <= gb) {
+    const int k = tid, xk = (k < gb) ? px : -1;
     if (k != n) p.out_tok[tb + k] = (k < n) ? xk : -1;
     if (p.g_tok) p.g_tok[tb + k] = (k < gn) ? xk : (k == gn ? rs[gn].tidx : -1);
   }

@@ -157,7 +157,7 @@ cudaError_t launch_prologue(const spec_batch& g, const Layout& L, char* ws, uint
 constexpr int kAttrDevices = 64;
 constexpr int kWaveBlocks = 152 * 4;  // resident 256-thread blocks with 48 KB staging on a GB300
 constexpr int kTailSeqs = 16;   // sequences the sampler splits finely (the last decided)
-constexpr int kTailStages = 4;  // their shortest range, in 512-vector stages
+constexpr int kTailStages = 1;  // their shortest range, in 512-vector stages (small batches split the last sequences finely)
 
 template <typename K>
 cudaError_t ensure_smem_attr(K kernel, std::atomic<unsigned long long>& done, int bytes) {
