@@ -42,7 +42,7 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kMaxRows = SPEC_MAX_GAMMA + 1;
-constexpr int kTargetTiles = 608;    // one wave of the resident blocks (152 SMs x 4): tiles are split no further, every tile adds a latency-bound epilogue
+constexpr int kTargetTiles = 608;    // one wave of the resident blocks (152 SMs x 4): chunk splits stop before the grid exceeds it
 
 // M_STOCH2: stochastic with a draft temperature of its own (the draft row is summed at
 // both temperatures)

@@ -21,11 +21,14 @@ inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Vocabulary chunking of the tile kernel: chunks of at most max_chunk tokens, split
-// further (down to 8192) while the grid has fewer tiles than the GPU has block slots.
-// Chunk sizes are multiples of 8 so every chunk starts on a 16-byte vector boundary.
+// further (down to 8192) only while the grid still fits in one wave of resident blocks: a
+// partial second wave of tiles ends after the first (B=64, gamma=5, V=32000: 384 whole-row
+// tiles 24.0 us against 25.5 for 768 half rows; B=8, gamma=5, V=128256: 576 tiles 19.6
+// against 20.4 for 624; same box). Chunk sizes are multiples of 8 so every chunk starts on
+// a 16-byte vector boundary.
 void chunking(int V, long long rows, int max_chunk, int* nchunks, int* chunk_elems) {
   long long nc = ceil_div(V, max_chunk);
-  while (rows * nc < kTargetTiles && V / (nc + 1) >= 8192) ++nc;
+  while (rows * (nc + 1) <= kTargetTiles && V / (nc + 1) >= 8192) ++nc;
   long long ce = ceil_div(ceil_div(V, nc), 8) * 8;
   *chunk_elems = (int)ce;
   *nchunks = (int)ceil_div(V, ce);
