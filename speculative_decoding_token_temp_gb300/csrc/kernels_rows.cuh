@@ -151,8 +151,9 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
   // rows, in flight while the rows merge (none of it depends on the merged statistics).
   static_assert(NT > SPEC_MAX_GAMMA, "one draft position per thread");
   int px = 0;
-  float pu = 0.f, pzt = 0.f, pzd = 0.f;
+  float pu = 0.f, pzt = 0.f, pzd = 0.f, pus = 0.f;
   if constexpr (MODE != M_TREE && MODE != M_NKL) {
+    if (is_stoch(MODE) && tid == 0) pus = p.u_sample[b];  // for the sampler's record
     if (tid < gb) {
       px = p.tokens[db + tid];
       if constexpr (is_stoch(MODE)) {
@@ -326,26 +327,42 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
     return;
   } else {
   // stochastic
+  float lp2 = 0.f, lq2 = 0.f, a = 0.f;
   if (tid < gb) {
-    const int i = tid, x = px;
-    const RowStat r = rs[i];
-    const float zt = pzt, zd = pzd;
-    const float lp2 = (zt - r.tm) * c - log2f(r.ts);     // log2 p(x)
-    const float lq2 = (zd - r.dm) * p.cd - log2f(r.ds);  // log2 q(x), at the draft's temperature
-    const float a = exp2f(fminf(0.f, lp2 - lq2));
+    const RowStat& r = rs[tid];
+    lp2 = (pzt - r.tm) * c - log2f(r.ts);     // log2 p(x)
+    lq2 = (pzd - r.dm) * p.cd - log2f(r.ds);  // log2 q(x), at the draft's temperature
+    a = exp2f(fminf(0.f, lp2 - lq2));
+    if (!(pu <= a)) atomicMin(&s_n, tid);
+    if (px != r.tidx) atomicMin(&s_gn, tid);
+  }
+  SY::sync();
+  const int n = s_n, gn = s_gn;
+  if (tid == 0) {
+    // the sampler waits on this record: published before any other output of the sequence,
+    // so that the fence orders only the record's payload
+    SeqRec q;
+    q.state = REC_READY;
+    q.n = n;
+    q.t_row = tb + n;
+    q.d_row = (n < gb) ? db + n : -1;
+    q.lt2 = rs[n].tm * c + log2f(rs[n].ts);
+    q.ld2 = (n < gb) ? rs[n].dm * p.cd + log2f(rs[n].ds) : 0.f;
+    q.us = pus;
+    q.mode = (n < gb) ? S_RESID : S_P;
+    publish_rec(p.rec + b, q);
+  }
+  if (tid < gb) {
+    const int i = tid;
     if (p.p_x) p.p_x[db + i] = exp2f(lp2);
     if (p.q_x) p.q_x[db + i] = exp2f(lq2);
     if (p.alpha) p.alpha[db + i] = a;
     if (p.nkl || p.mask) {
-      const float v = row_nkl<MODE == M_STOCH2>(r, p.invT, p.inv_lnV);  // both rows at the target's T
+      const float v = row_nkl<MODE == M_STOCH2>(rs[i], p.invT, p.inv_lnV);  // both rows at the target's T
       if (p.nkl) p.nkl[db + i] = v;
       if (p.mask) p.mask[db + i] = v < nkl_threshold(p, b, i) ? 1 : 0;
     }
-    if (!(pu <= a)) atomicMin(&s_n, i);
-    if (x != r.tidx) atomicMin(&s_gn, i);
   }
-  SY::sync();
-  const int n = s_n, gn = s_gn;
   if (tid <= gb) {
     const int k = tid, xk = (k < gb) ? px : -1;
     if (k != n) p.out_tok[tb + k] = (k < n) ? xk : -1;
@@ -357,18 +374,6 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
     if (p.mask && p.position != nullptr && p.position[b] < 1) atomicOr(p.status, SPEC_DEV_POSITION);
   }
   policy_epilogue<SY>(p, b, gb, db, n, rs);
-  if (tid == 0) {
-    SeqRec q;
-    q.state = REC_READY;
-    q.n = n;
-    q.t_row = tb + n;
-    q.d_row = (n < gb) ? db + n : -1;
-    q.lt2 = rs[n].tm * c + log2f(rs[n].ts);
-    q.ld2 = (n < gb) ? rs[n].dm * p.cd + log2f(rs[n].ds) : 0.f;
-    q.us = p.u_sample[b];
-    q.mode = (n < gb) ? S_RESID : S_P;
-    publish_rec(p.rec + b, q);
-  }
   }  // stochastic
   }  // stochastic and greedy
 }
