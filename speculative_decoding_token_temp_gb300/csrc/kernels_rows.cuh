@@ -147,28 +147,32 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
   const int db = c0;           // first draft row / token / u_accept entry
   const E* target = static_cast<const E*>(p.target);
   const E* draft = static_cast<const E*>(p.draft);
-  // Thread i < gb: draft position i's token and, stochastic, its uniform and z(x) of both
-  // rows, in flight while the rows merge (none of it depends on the merged statistics).
+  // Draft position i is owned by thread NT - gb + i (the last warps, while the rows merge
+  // from the first): its token and, stochastic, its uniform and z(x) of both rows are read
+  // there, the dependent loads of z(x) in flight beside the merge's reads.
   static_assert(NT > SPEC_MAX_GAMMA, "one draft position per thread");
+  const int i_own = tid - (NT - gb);  // this thread's draft position, or < 0
   int px = 0;
   float pu = 0.f, pzt = 0.f, pzd = 0.f, pus = 0.f;
   if constexpr (MODE != M_TREE && MODE != M_NKL) {
     if (is_stoch(MODE) && tid == 0) pus = p.u_sample[b];  // for the sampler's record
-    if (tid < gb) {
-      px = p.tokens[db + tid];
+    if (i_own >= 0) {
+      px = p.tokens[db + i_own];
       if constexpr (is_stoch(MODE)) {
-        pu = p.u_accept[db + tid];
+        pu = p.u_accept[db + i_own];
         if (px >= 0 && px < p.V) {
-          pzt = elem_at<E>(target + (size_t)(tb + tid) * V, px);
-          pzd = elem_at<E>(draft + (size_t)(db + tid) * V, px);
+          pzt = elem_at<E>(target + (size_t)(tb + i_own) * V, px);
+          pzd = elem_at<E>(draft + (size_t)(db + i_own) * V, px);
         }
       }
     }
   }
   if constexpr (MODE == M_TREE) {
-    // the node tokens and parents go to shared memory in one coalesced read, in flight
-    // while the rows merge
-    for (int j = tid; j < p.N; j += NT) {
+    // the node tokens and parents go to shared memory from the last warps (node j: thread
+    // NT - N + j), in flight while the first warps merge the rows
+    static_assert(NT >= SPEC_MAX_TREE_NODES, "one node per thread");
+    const int j = tid - (NT - p.N);
+    if (j >= 0) {
       s_tok[j] = p.node_tokens[(size_t)b * p.N + j];
       s_par[j] = p.parent[j];
     }
@@ -279,9 +283,9 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
     return;
   } else {
   // stochastic and greedy: validate the sequence first
-  if (tid < R) {  // R <= SPEC_MAX_GAMMA + 1 <= NT
-    unsigned e = rs[tid].bad ? SPEC_DEV_NONFINITE : 0u;
-    if (tid < gb && (px < 0 || px >= p.V)) e |= SPEC_DEV_TOKEN_RANGE;
+  {
+    unsigned e = (tid < R && rs[tid].bad) ? SPEC_DEV_NONFINITE : 0u;  // R <= SPEC_MAX_GAMMA + 1 <= NT
+    if (i_own >= 0 && (px < 0 || px >= p.V)) e |= SPEC_DEV_TOKEN_RANGE;
     if (e) atomicOr(&s_err, e);
   }
   SY::sync();
@@ -318,23 +322,26 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
   }
 
   if constexpr (MODE == M_GREEDY) {
-    if (tid < gb && px != rs[tid].tidx) atomicMin(&s_gn, tid);
+    if (i_own >= 0 && px != rs[i_own].tidx) atomicMin(&s_gn, i_own);
     SY::sync();
     const int n = s_gn;
-    if (tid <= gb) p.out_tok[tb + tid] = (tid < n) ? px : (tid == n ? rs[n].tidx : -1);
-    if (tid == 0) p.n_acc[b] = n;
+    if (i_own >= 0) p.out_tok[tb + i_own] = (i_own < n) ? px : (i_own == n ? rs[n].tidx : -1);
+    if (tid == 0) {
+      p.out_tok[tb + gb] = (n == gb) ? rs[gb].tidx : -1;  // the bonus position
+      p.n_acc[b] = n;
+    }
     policy_epilogue<SY>(p, b, gb, db, n, rs);
     return;
   } else {
   // stochastic
   float lp2 = 0.f, lq2 = 0.f, a = 0.f;
-  if (tid < gb) {
-    const RowStat& r = rs[tid];
+  if (i_own >= 0) {
+    const RowStat& r = rs[i_own];
     lp2 = (pzt - r.tm) * c - log2f(r.ts);     // log2 p(x)
     lq2 = (pzd - r.dm) * p.cd - log2f(r.ds);  // log2 q(x), at the draft's temperature
     a = exp2f(fminf(0.f, lp2 - lq2));
-    if (!(pu <= a)) atomicMin(&s_n, tid);
-    if (px != r.tidx) atomicMin(&s_gn, tid);
+    if (!(pu <= a)) atomicMin(&s_n, i_own);
+    if (px != r.tidx) atomicMin(&s_gn, i_own);
   }
   SY::sync();
   const int n = s_n, gn = s_gn;
@@ -352,8 +359,8 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
     q.mode = (n < gb) ? S_RESID : S_P;
     publish_rec(p.rec + b, q);
   }
-  if (tid < gb) {
-    const int i = tid;
+  if (i_own >= 0) {
+    const int i = i_own;
     if (p.p_x) p.p_x[db + i] = exp2f(lp2);
     if (p.q_x) p.q_x[db + i] = exp2f(lq2);
     if (p.alpha) p.alpha[db + i] = a;
@@ -363,12 +370,15 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
       if (p.mask) p.mask[db + i] = v < nkl_threshold(p, b, i) ? 1 : 0;
     }
   }
-  if (tid <= gb) {
-    const int k = tid, xk = (k < gb) ? px : -1;
-    if (k != n) p.out_tok[tb + k] = (k < n) ? xk : -1;
-    if (p.g_tok) p.g_tok[tb + k] = (k < gn) ? xk : (k == gn ? rs[gn].tidx : -1);
+  if (i_own >= 0) {
+    const int k = i_own;
+    if (k != n) p.out_tok[tb + k] = (k < n) ? px : -1;
+    if (p.g_tok) p.g_tok[tb + k] = (k < gn) ? px : (k == gn ? rs[gn].tidx : -1);
   }
   if (tid == 0) {
+    // the bonus position: the sampler's token when every draft is accepted
+    if (n != gb) p.out_tok[tb + gb] = -1;
+    if (p.g_tok) p.g_tok[tb + gb] = (gn == gb) ? rs[gb].tidx : -1;
     p.n_acc[b] = n;
     if (p.g_n) p.g_n[b] = gn;
     if (p.mask && p.position != nullptr && p.position[b] < 1) atomicOr(p.status, SPEC_DEV_POSITION);
