@@ -149,6 +149,17 @@ __device__ __forceinline__ int ld_acquire_gpu(const int* a) {
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
   return v;
 }
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* a, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(a), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ void red_add_release_gpu(unsigned* a, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_release_gpu(int* a, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
 __device__ __forceinline__ void st_relaxed_gpu(int* a, int v) {
   asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
 }

@@ -214,12 +214,12 @@ __global__ void __launch_bounds__(kThreads, 2) pair_kernel(const __grid_constant
   }
 
   pair_partial_write<K>(p.part + tile, mr, s, kk, c);
-  __syncthreads();  // every writer's partial entries precede thread 0's fence
+  __syncthreads();  // every writer's partial entries precede thread 0's ticket
   if (threadIdx.x == 0) {
-    __threadfence();
-    const unsigned old = atomicAdd(p.cnt + gi, 1u);
+    // release: the tile's partial before its ticket; acquire: the other tiles' partials
+    // before this block's reads
+    const unsigned old = atom_add_acq_rel_gpu(p.cnt + gi, 1u);
     s_last = (old + 1u == (unsigned)p.nchunks) ? 1 : 0;
-    if (s_last) __threadfence();
   }
   __syncthreads();
   if (!s_last) return;
@@ -358,12 +358,12 @@ __global__ void __launch_bounds__(kThreads, 2) pair_staged_kernel(const __grid_c
   }
 
   pair_partial_write<K>(p.part + tile, mr, s, kk, c);
-  __syncthreads();  // every writer's partial entries precede thread 0's fence
+  __syncthreads();  // every writer's partial entries precede thread 0's ticket
   if (threadIdx.x == 0) {
-    __threadfence();
-    const unsigned old = atomicAdd(p.cnt + gi, 1u);
+    // release: the tile's partial before its ticket; acquire: the other tiles' partials
+    // before this block's reads
+    const unsigned old = atom_add_acq_rel_gpu(p.cnt + gi, 1u);
     s_last = (old + 1u == (unsigned)p.nchunks) ? 1 : 0;
-    if (s_last) __threadfence();
   }
   __syncthreads();
   if (!s_last) return;

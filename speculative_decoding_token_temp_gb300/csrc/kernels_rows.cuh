@@ -50,21 +50,17 @@ __global__ void prologue_kernel(const __grid_constant__ ProParams p) {
 // itself (a batch whose offsets failed the prologue's check leaves some unpublished).
 template <int MODE>
 __device__ __forceinline__ void tile_done(const RowsParams& p) {
-  if constexpr (is_stoch(MODE)) {
-    __threadfence();
-    atomicAdd(p.cnt + p.B, 1u);
-  }
+  if constexpr (is_stoch(MODE)) red_add_release_gpu(p.cnt + p.B, 1u);
 }
 
 // Publishes a sequence record to the sampler, which may already be polling it: the
-// payload (with the state still pending), a fence, then the state word -- a release, so a
+// payload (with the state still pending), then the state word with release semantics, so a
 // reader that acquires the state sees the payload.
 __device__ __forceinline__ void publish_rec(SeqRec* dst, SeqRec q) {
   const int state = q.state;
   q.state = REC_PENDING;
   *dst = q;
-  __threadfence();
-  st_relaxed_gpu(&dst->state, state);
+  st_release_gpu(&dst->state, state);
 }
 
 // ---------------------------------------------------------------------------
@@ -688,11 +684,11 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
     float4* dst = reinterpret_cast<float4*>(p.part + tile);
     __stcg(dst, make_float4(part.tm, part.ts, __int_as_float(part.tidx), __int_as_float(part.bad)));
     __stcg(dst + 1, make_float4(part.dm, part.ds, part.dk, part.ds2));
-    __threadfence();
     const unsigned total = (unsigned)((gb + HB) * p.nchunks);
-    const unsigned old = atomicAdd(p.cnt + b, 1u);
+    // release: this tile's partial before its ticket; acquire: the other tiles' partials
+    // (read with ld.cg) before this block's reads
+    const unsigned old = atom_add_acq_rel_gpu(p.cnt + b, 1u);
     s_last = (old + 1u == total) ? 1 : 0;
-    if (s_last) __threadfence();  // the other tiles' partials (read with ld.cg) precede this block's reads
   }
   __syncthreads();
   if (!s_last) {

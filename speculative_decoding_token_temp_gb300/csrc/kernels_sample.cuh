@@ -461,11 +461,11 @@ __global__ void __launch_bounds__(kThreads, 4) sample2_kernel(const __grid_const
       mass_pass<E, VEC>(trow, drow, q.mode, q.lt2, q.ld2, p.c, p.cd, NV, k0, k1, table, dsm);
     __syncthreads();  // orders every warp's table entries before thread 0's fence
     if (tid == 0) {
-      __threadfence();  // the block's table entries are visible before its ticket
+      // release: the block's table entries before its ticket; acquire: the other blocks'
+      // entries before this block's reads
       const unsigned part = (unsigned)(k1 - k0);
-      const unsigned old = atomicAdd(p.cnt + b, part);
+      const unsigned old = atom_add_acq_rel_gpu(p.cnt + b, part);
       s_last = (old + part == (unsigned)nst) ? 1 : 0;
-      if (s_last) __threadfence();  // ... and the other blocks' entries before this block's reads
     }
     __syncthreads();
     if (!s_last) continue;
