@@ -462,8 +462,9 @@ def run_ours(args):
         mb_min = (wm.target.size + wm.draft.size + 2 * wm.B * wm.V) * eb
         modes["multi_draft_G64_K3_g8_V128256"] = {
             "us_per_call": t_m * 1e6, "GBps": mb_min / t_m / 1e9, "frac_of_peak": mb_min / t_m / 1e9 / hbm,
-            "note": "algorithmic bytes: every logit once + one row pair per candidate; the design reads the "
-                    f"draft rows a second time for the pairwise matrix (+{wm.draft.size * eb / 1e6:.0f} MB)"}
+            "note": "algorithmic bytes: every logit once + one row pair per candidate; the fused K-way tiles "
+                    "read every logit once (rows off the 16-byte grid take the two-pass form, which reads "
+                    f"the draft rows a second time: +{wm.draft.size * eb / 1e6:.0f} MB)"}
         del tm, dm, km, uam, usm, m_out
         sm_out = torch.empty(6, dtype=torch.float64, device=dev)
         t_sm = time_mode(lambda: api.spec_accept_summary(st, 2, 64, out=sm_out), 200, 10, dev)

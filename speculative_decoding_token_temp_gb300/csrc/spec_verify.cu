@@ -26,9 +26,9 @@ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 // tiles 24.0 us against 25.5 for 768 half rows; B=8, gamma=5, V=128256: 576 tiles 19.6
 // against 20.4 for 624; same box). Chunk sizes are multiples of 8 so every chunk starts on
 // a 16-byte vector boundary.
-void chunking(int V, long long rows, int max_chunk, int* nchunks, int* chunk_elems) {
+void chunking(int V, long long rows, int max_chunk, int* nchunks, int* chunk_elems, int slots = kTargetTiles) {
   long long nc = ceil_div(V, max_chunk);
-  while (rows * (nc + 1) <= kTargetTiles && V / (nc + 1) >= 8192) ++nc;
+  while (rows * (nc + 1) <= slots && V / (nc + 1) >= 8192) ++nc;
   long long ce = ceil_div(ceil_div(V, nc), 8) * 8;
   *chunk_elems = (int)ce;
   *nchunks = (int)ceil_div(V, ce);
@@ -47,16 +47,19 @@ int table_stride_for(int V, spec_dtype dt) {
   return (int)(ceil_div(nv, 2 * kThreads) * kSlicesPerStage);
 }
 
+// fused_k > 0: fused multi-draft tiles, each holding the rows of fused_k candidates, two
+// blocks per SM.
 // max_chunk: the longest vocabulary chunk of a tile. 0 = the measured best: 65536 tokens
 // for single-row tiles and for the stochastic call's pairs (256 KB pair tiles: fewer
 // tile epilogues; 185.6 against 191.7 us at the headline, same box), 49152 for the NKL
 // call's pairs (150.3 us, against 152.0 with 32768 and 155.4 with 65536).
 Layout layout(int B, int V, long long rows, bool sample, bool single_rows = false, spec_dtype dt = SPEC_F32,
-              int max_chunk = 0) {
+              int max_chunk = 0, int fused_k = 0) {
   Layout L;
   L.rows = rows;
-  chunking(V, rows > 0 ? rows : 1, max_chunk > 0 ? max_chunk : ((single_rows || sample) ? 65536 : 49152),
-           &L.nchunks, &L.chunk_elems);
+  const long long trows = fused_k > 0 ? rows / fused_k : rows;  // tiles per chunk
+  chunking(V, trows > 0 ? trows : 1, max_chunk > 0 ? max_chunk : ((single_rows || sample) ? 65536 : 49152),
+           &L.nchunks, &L.chunk_elems, fused_k > 0 ? kTargetTiles / 2 : kTargetTiles);
   size_t off = 0;
   L.cntA = off;  // B tickets, then the count of finished tiles
   off = align256(off + sizeof(unsigned) * ((size_t)B + 1));
@@ -356,7 +359,8 @@ spec_status stochastic_impl(spec_batch g, spec_dtype dtype, const void* target_l
       !aligned_to(4, {draft_tokens, u_accept, u_sample, n_accepted, out_tokens, p_x, q_x, alpha, nkl, greedy_n,
                       greedy_tokens, device_status, g.cu_draft}))
     return SPEC_ERR_INVALID_ARG;
-  const Layout L = layout(g.B, g.V, rows_for(SPEC_MODE_STOCHASTIC, g), true, false, dtype, mt ? kMultiChunk : 0);
+  const Layout L = layout(g.B, g.V, rows_for(SPEC_MODE_STOCHASTIC, g), true, false, dtype, mt ? kMultiChunk : 0,
+                          mt ? mt->K : 0);
   if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u)) return SPEC_ERR_WORKSPACE;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   char* ws = static_cast<char*>(workspace);
@@ -450,7 +454,8 @@ spec_status greedy_impl(spec_batch g, spec_dtype dtype, const void* target_logit
   if (!aligned_to(elem_bytes(dtype), {target_logits}) ||
       !aligned_to(4, {draft_tokens, n_accepted, out_tokens, device_status, g.cu_draft}))
     return SPEC_ERR_INVALID_ARG;
-  const Layout L = layout(g.B, g.V, rows_for(SPEC_MODE_GREEDY, g), false, true, SPEC_F32, mt ? kMultiChunk : 0);
+  const Layout L = layout(g.B, g.V, rows_for(SPEC_MODE_GREEDY, g), false, true, SPEC_F32, mt ? kMultiChunk : 0,
+                          mt ? mt->K : 0);
   if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u)) return SPEC_ERR_WORKSPACE;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   char* ws = static_cast<char*>(workspace);
@@ -506,7 +511,7 @@ MultiLayout multi_layout(const spec_multi_batch& m, spec_dtype dt, bool stochast
   const spec_batch g = multi_as_batch(m);
   const spec_mode mode = stochastic ? SPEC_MODE_STOCHASTIC : SPEC_MODE_GREEDY;
   MultiLayout M;
-  const Layout Lv = layout(g.B, g.V, rows_for(mode, g), stochastic, !stochastic, dt, kMultiChunk);
+  const Layout Lv = layout(g.B, g.V, rows_for(mode, g), stochastic, !stochastic, dt, kMultiChunk, m.K);
   const Layout Lp = layout(g.B, g.V, rows_for(mode, g), stochastic, !stochastic, dt);  // two-pass: plain tiles
   M.verify = align256(Lv.total > Lp.total ? Lv.total : Lp.total);
   M.vchunks = Lv.nchunks;
