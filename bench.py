@@ -628,7 +628,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--skip-ragged", action="store_true")
     ap.add_argument("--offset", type=int, default=0, metavar="N",
-                    help="shift the timed call's logits by N elements (N % 8 != 0: the staged path)")
+                    help="shift the timed call's logits by N elements (N not a multiple of 8: the staged path)")
     ap.add_argument("--batch", type=int, default=None,
                     help="sequences per step (default: the workload's 256); smaller slices serve profiling")
     ap.add_argument("--multi", type=int, default=None, metavar="G",
