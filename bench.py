@@ -483,7 +483,9 @@ def run_ours(args):
                 "us_per_call": t_s * 1e6, "GBps": ab["stochastic"] / t_s / 1e9,
                 "frac_of_peak": ab["stochastic"] / t_s / 1e9 / hbm, "greedy_us_per_call": t_sg * 1e6,
                 "note": "logits one element off the 16-byte grid (as for a vocabulary whose row is not a "
-                        "multiple of 16 bytes): per-warp bulk-copy rings read back at the row's phase"}
+                        "multiple of 16 bytes): the stochastic call's pairs through per-warp bulk-copy rings "
+                        "read back at the row's phase; the greedy call's rows as aligned vectors with the "
+                        "phase applied to the indices"}
             del ts, ds, s_out, sg_out
         del res
         tw = synth.TREE.make()

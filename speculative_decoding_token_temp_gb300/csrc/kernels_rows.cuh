@@ -571,7 +571,8 @@ __device__ __forceinline__ void stream_staged(const E* trow, const E* drow, int 
   }
 }
 
-template <typename E, int VEC, int MODE>
+// PH (argmax rows only): rows at any element alignment, each tile applying its row's phase.
+template <typename E, int VEC, int MODE, bool PH = false>
 __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant__ RowsParams p) {
   constexpr int HB = (MODE == M_NKL) ? 0 : 1;
   extern __shared__ __align__(128) unsigned char dsm[];
@@ -640,10 +641,25 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
   init(ta);
   init(da);
   constexpr bool ARGMAX = MODE == M_GREEDY || MODE == M_TREE;
+  static_assert(VEC > 1 || !ARGMAX, "argmax rows at any alignment take the vector path");
+  static_assert(!PH || (ARGMAX && VEC > 1), "the phased tiles are argmax tiles");
   if constexpr (VEC > 1) {
     uint4 best[2];
     if constexpr (ARGMAX) {
-      stream_tile<E, VEC, MODE, K_ARGMAX>(trow, drow, e_begin / VEC, v1, c, cd, ta, da, dsm, best);
+      // Rows at any element alignment: the whole aligned 16-byte blocks of the chunk are
+      // streamed as vectors of the aligned base trv (row element e is element e + ph of
+      // trv); the partial blocks at the chunk's ends, head [e_begin, hend) and tail
+      // [tbeg, e_end), are copied beside the ring and folded in element by element.
+      const int ph = PH ? (int)(((uintptr_t)trow & 15u) / sizeof(E)) : 0;
+      const E* trv = trow - ph;
+      const int vf0 = (e_begin + ph + VEC - 1) / VEC, vf1 = (e_end + ph) / VEC;
+      const int hend = min(e_end, vf0 * VEC - ph), tbeg = max(hend, vf1 * VEC - ph);
+      __shared__ uint4 s_edge[2];
+      const int elo = threadIdx.x == 0 ? e_begin : tbeg, ehi = threadIdx.x == 0 ? hend : e_end;
+      const bool edge = PH && threadIdx.x < 2 && elo < ehi;
+      if (edge)
+        cp_async16((uint32_t)__cvta_generic_to_shared(&s_edge[threadIdx.x]), trv + (size_t)((elo + ph) / VEC) * VEC);
+      stream_tile<E, VEC, MODE, K_ARGMAX>(trv, drow, vf0, vf1, c, cd, ta, da, dsm, best);  // waits for the edge copies too
       // the lowest index of the thread's maximum, from the raw vectors of its group
       if (ta.g0 >= 0) {
         float f[2 * VEC];
@@ -652,7 +668,25 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
 #pragma unroll
         for (int j = 2 * VEC - 2; j >= 0; --j)
           if (f[j] == ta.m) k = j;
-        ta.g0 = k < VEC ? ta.g0 + k : ta.g1 + (k - VEC);
+        ta.g0 = (k < VEC ? ta.g0 + k : ta.g1 + (k - VEC)) - ph;
+      }
+      if (PH && edge) {
+        float f[VEC];
+        IO<E, VEC>::unpack(s_edge[threadIdx.x], f);
+        const int e0 = ((elo + ph) / VEC) * VEC - ph;  // row index of f[0]
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) {
+          const int e = e0 + j;
+          if (e >= elo && e < ehi) {
+            const float x = f[j];
+            ta.hi = max_nan(ta.hi, x);
+            ta.lo = fminf(ta.lo, x);
+            if (x > ta.m || (x == ta.m && ta.g0 >= 0 && e < ta.g0)) {
+              ta.m = x;
+              ta.g0 = e;
+            }
+          }
+        }
       }
     } else if constexpr (MODE == M_NKL) {
       stream_tile<E, VEC, MODE, K_PAIR>(trow, drow, e_begin / VEC, v1, c, cd, ta, da, dsm, best);
@@ -663,9 +697,7 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
         stream_tile<E, VEC, MODE, K_TSUM>(trow, drow, e_begin / VEC, v1, c, cd, ta, da, dsm, best);
     }
   } else {
-    if constexpr (MODE == M_GREEDY || MODE == M_TREE) {
-      stream_staged<E, MODE, K_ARGMAX>(trow, drow, e_begin, e_end, c, cd, ta, da, dsm, p.status);
-    } else if constexpr (MODE == M_NKL) {
+    if constexpr (MODE == M_NKL) {
       stream_staged<E, MODE, K_PAIR>(trow, drow, e_begin, e_end, c, cd, ta, da, dsm, p.status);
     } else {
       if (kind == K_PAIR)

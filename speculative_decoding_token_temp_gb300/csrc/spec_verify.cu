@@ -178,9 +178,9 @@ cudaError_t ensure_smem_attr(K kernel, std::atomic<unsigned long long>& done, in
   return e;
 }
 
-template <typename E, int VEC, int MODE>
+template <typename E, int VEC, int MODE, bool PH = false>
 cudaError_t launch_rows_t(const RowsParams& rp, long long tiles, cudaStream_t stream) {
-  auto kern = rows_kernel<E, VEC, MODE>;
+  auto kern = rows_kernel<E, VEC, MODE, PH>;
   const int smem = VEC > 1 ? kRowsSmem : kStagedSmem;
   static std::atomic<unsigned long long> done{0};
   const cudaError_t e = ensure_smem_attr(kern, done, smem);
@@ -199,10 +199,18 @@ cudaError_t launch_rows_t(const RowsParams& rp, long long tiles, cudaStream_t st
   return cudaLaunchKernelEx(&cfg, kern, rp);
 }
 
+// vec: every row on the 16-byte grid. Argmax rows (greedy, tree) off the grid take the
+// phased vector tiles (each tile applies its row's phase); pairs off the grid take the
+// staged path.
 template <int MODE>
 cudaError_t launch_rows(bool bf16, bool vec, const RowsParams& rp, long long tiles, cudaStream_t stream) {
-  if (bf16) return vec ? launch_rows_t<uint16_t, 8, MODE>(rp, tiles, stream) : launch_rows_t<uint16_t, 1, MODE>(rp, tiles, stream);
-  return vec ? launch_rows_t<float, 4, MODE>(rp, tiles, stream) : launch_rows_t<float, 1, MODE>(rp, tiles, stream);
+  if constexpr (MODE == M_GREEDY || MODE == M_TREE) {
+    if (bf16) return vec ? launch_rows_t<uint16_t, 8, MODE>(rp, tiles, stream) : launch_rows_t<uint16_t, 8, MODE, true>(rp, tiles, stream);
+    return vec ? launch_rows_t<float, 4, MODE>(rp, tiles, stream) : launch_rows_t<float, 4, MODE, true>(rp, tiles, stream);
+  } else {
+    if (bf16) return vec ? launch_rows_t<uint16_t, 8, MODE>(rp, tiles, stream) : launch_rows_t<uint16_t, 1, MODE>(rp, tiles, stream);
+    return vec ? launch_rows_t<float, 4, MODE>(rp, tiles, stream) : launch_rows_t<float, 1, MODE>(rp, tiles, stream);
+  }
 }
 
 template <typename E, int VEC, bool STAGED>

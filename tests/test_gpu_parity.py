@@ -160,6 +160,48 @@ def test_staged_path_ties_and_flat_rows(dev):
             compare_stochastic(w, run_stochastic(w, dev, offset=off), [0])
 
 
+@pytest.mark.parametrize("dtype", [synth.F32, synth.BF16])
+@pytest.mark.parametrize("V", [13, 4101, 70003])
+def test_argmax_rows_at_every_phase(dev, V, dtype):
+    """Greedy rows at every element phase of the 16-byte grid. Maxima sit in the partial
+    blocks at the ends of the vocabulary chunks (the first and last elements of a row; ties
+    at every multiple of 8, where chunks start, or at every 8j + 7, where they end, from a
+    third of the row on) and tie with maxima inside the chunks, so the lowest index must
+    come out of the element-by-element edge folds and the chunk merge."""
+    rng = np.random.default_rng(V)
+    R = 9
+    t = rng.normal(0.0, 1.0, (R, V)).astype(np.float32)
+    m0 = V // 3
+    plant = [
+        [0, V // 2],                                  # a tie: the first element wins
+        [V - 1],                                      # the last element alone
+        [V // 2, V - 1],                              # a tie with the last element: the middle wins
+        [min(1, V - 1), min(2, V - 1)],               # a tie inside the head block
+        [j for j in range(0, V, 8) if j >= m0],       # chunk starts
+        [j for j in range(7, V, 8) if j >= m0],       # chunk ends
+        [],                                           # a flat row: index 0
+        [V // 2 + 1, V // 2],
+        [V - 3, V - 2, V - 1],
+    ]
+    for i, idx in enumerate(plant):
+        if i == 6:
+            t[i] = 0.0
+        t[i, idx] = 9.0
+    t64 = O.widen(synth.storage(t, dtype), dtype)
+    expect = [int(np.argmax(t64[i])) for i in range(R)]
+    tokens = np.array(expect[:R - 1], np.int32)  # every draft the target's argmax: all must match
+    w = synth.StochasticWorkload(B=1, V=V, dtype=dtype, T=1.0, gammas=np.array([R - 1], np.int32),
+                                 cu_draft=np.array([0, R - 1], np.int32), target=synth.storage(t, dtype),
+                                 draft=synth.storage(np.zeros((R - 1, V), np.float32), dtype), tokens=tokens,
+                                 u_accept=np.full(R - 1, 0.5, np.float32), u_sample=np.array([0.5], np.float32))
+    for off in range(8 if dtype == synth.BF16 else 4):
+        res = run_greedy(w, dev, offset=off)
+        assert res["device_status"][0] == 0
+        assert int(res["n_accepted"][0]) == R - 1, off
+        assert list(res["out_tokens"][:R]) == expect, off
+        compare_greedy(w, res, [0])
+
+
 @pytest.mark.parametrize("V,dtype,offset", [(3001, synth.BF16, 0), (128256, synth.BF16, 3), (5001, synth.F32, 1)])
 def test_staged_path_tree(dev, V, dtype, offset):
     """The tree call on rows off the 16-byte grid (an odd vocabulary, a shifted buffer):
