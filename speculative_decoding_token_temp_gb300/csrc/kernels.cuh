@@ -123,6 +123,7 @@ struct SampleParams {
   // head_total stages, the remaining blocks seg_tail stages each of the rest
   long long head_total;
   int nb_head, seg_head, seg_tail;
+  int ph;  // aligned-row sampler: the rows' common offset in elements within the 16-byte grid
 };
 
 struct ProParams {
@@ -479,6 +480,8 @@ struct TAcc {
   float2 s;
   int g0, g1;  // the group that holds m (resolved to the lowest index at the tile end; g0 < 0: none)
 };
+// TAcc::g1 of an exact index: g0 is the index of m itself (an element folded in alone)
+constexpr int kExactIdx = INT_MIN;
 struct DAcc {
   float mr, mth, nmc;
   float2 s, k;
@@ -728,6 +731,8 @@ __device__ __forceinline__ Partial reduce_tile(int kind, const TAcc& ta, const D
       my_idx = ta.g0 >= 0 ? ta.g0 : INT_MAX;
     else if constexpr (GS > 0)
       my_idx = row ? resolve_strided<E, GS>(row, ta.g0, ta.g1, TM) : INT_MAX;
+    else if (ta.g1 == kExactIdx)
+      my_idx = row ? ta.g0 : INT_MAX;
     else
       my_idx = row ? resolve_index<E, VEC>(row, ta.g0, ta.g1, TM) : INT_MAX;
   }

@@ -633,7 +633,6 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
   const E* drow = static_cast<const E*>(p.draft) + ((kind == K_PAIR) ? drow_i * V : 0);
   const int e_begin = chunk * p.chunk_elems;
   const int e_end = min(e_begin + p.chunk_elems, p.V);
-  const int v1 = e_end / VEC;
   const float c = p.c, cd = p.cd;
 
   TAcc ta;
@@ -642,24 +641,41 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
   init(da);
   constexpr bool ARGMAX = MODE == M_GREEDY || MODE == M_TREE;
   static_assert(VEC > 1 || !ARGMAX, "argmax rows at any alignment take the vector path");
-  static_assert(!PH || (ARGMAX && VEC > 1), "the phased tiles are argmax tiles");
+  static_assert(!PH || VEC > 1, "the phased tiles are vector tiles");
+  // PH: the row's offset in elements within the 16-byte grid (the rows of a pair share it);
+  // indices are counted from the aligned base until the partial is written
+  int ph = 0;
   if constexpr (VEC > 1) {
     uint4 best[2];
-    if constexpr (ARGMAX) {
-      // Rows at any element alignment: the whole aligned 16-byte blocks of the chunk are
-      // streamed as vectors of the aligned base trv (row element e is element e + ph of
-      // trv); the partial blocks at the chunk's ends, head [e_begin, hend) and tail
-      // [tbeg, e_end), are copied beside the ring and folded in element by element.
-      const int ph = PH ? (int)(((uintptr_t)trow & 15u) / sizeof(E)) : 0;
-      const E* trv = trow - ph;
-      const int vf0 = (e_begin + ph + VEC - 1) / VEC, vf1 = (e_end + ph) / VEC;
+    // Rows at any element alignment (PH): the whole aligned 16-byte blocks of the chunk are
+    // streamed as vectors of the aligned bases trv and drv (row element e is element
+    // e + ph there); the partial blocks at the chunk's ends, head [e_begin, hend) and tail
+    // [tbeg, e_end), are copied beside the ring by threads 0 and 1 and folded in element by
+    // element.
+    if constexpr (PH) ph = (int)(((uintptr_t)trow & 15u) / sizeof(E));
+    const E* trv = trow - ph;
+    const E* drv = drow - ph;
+    const int vf0 = (e_begin + ph + VEC - 1) / VEC, vf1 = (e_end + ph) / VEC;
+    __shared__ uint4 s_edge[2][2];  // [head, tail][target, draft]
+    // thread 0 takes the head, thread 1 the tail (the bounds are recomputed after the
+    // stream, so that none of them is held through it)
+    auto edge_range = [&](int& elo, int& ehi) {
       const int hend = min(e_end, vf0 * VEC - ph), tbeg = max(hend, vf1 * VEC - ph);
-      __shared__ uint4 s_edge[2];
-      const int elo = threadIdx.x == 0 ? e_begin : tbeg, ehi = threadIdx.x == 0 ? hend : e_end;
-      const bool edge = PH && threadIdx.x < 2 && elo < ehi;
-      if (edge)
-        cp_async16((uint32_t)__cvta_generic_to_shared(&s_edge[threadIdx.x]), trv + (size_t)((elo + ph) / VEC) * VEC);
-      stream_tile<E, VEC, MODE, K_ARGMAX>(trv, drow, vf0, vf1, c, cd, ta, da, dsm, best);  // waits for the edge copies too
+      elo = threadIdx.x == 0 ? e_begin : tbeg;
+      ehi = threadIdx.x == 0 ? hend : e_end;
+    };
+    if (PH && threadIdx.x < 2) {
+      int elo, ehi;
+      edge_range(elo, ehi);
+      if (elo < ehi) {
+        const size_t eb = (size_t)((elo + ph) / VEC) * VEC;
+        cp_async16((uint32_t)__cvta_generic_to_shared(&s_edge[threadIdx.x][0]), trv + eb);
+        if (kind == K_PAIR) cp_async16((uint32_t)__cvta_generic_to_shared(&s_edge[threadIdx.x][1]), drv + eb);
+      }
+    }
+    // (stream_tile's last wait covers the edge copies too)
+    if constexpr (ARGMAX) {
+      stream_tile<E, VEC, MODE, K_ARGMAX>(trv, drv, vf0, vf1, c, cd, ta, da, dsm, best);
       // the lowest index of the thread's maximum, from the raw vectors of its group
       if (ta.g0 >= 0) {
         float f[2 * VEC];
@@ -668,33 +684,55 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
 #pragma unroll
         for (int j = 2 * VEC - 2; j >= 0; --j)
           if (f[j] == ta.m) k = j;
-        ta.g0 = (k < VEC ? ta.g0 + k : ta.g1 + (k - VEC)) - ph;
-      }
-      if (PH && edge) {
-        float f[VEC];
-        IO<E, VEC>::unpack(s_edge[threadIdx.x], f);
-        const int e0 = ((elo + ph) / VEC) * VEC - ph;  // row index of f[0]
-#pragma unroll
-        for (int j = 0; j < VEC; ++j) {
-          const int e = e0 + j;
-          if (e >= elo && e < ehi) {
-            const float x = f[j];
-            ta.hi = max_nan(ta.hi, x);
-            ta.lo = fminf(ta.lo, x);
-            if (x > ta.m || (x == ta.m && ta.g0 >= 0 && e < ta.g0)) {
-              ta.m = x;
-              ta.g0 = e;
-            }
-          }
-        }
+        ta.g0 = k < VEC ? ta.g0 + k : ta.g1 + (k - VEC);
       }
     } else if constexpr (MODE == M_NKL) {
-      stream_tile<E, VEC, MODE, K_PAIR>(trow, drow, e_begin / VEC, v1, c, cd, ta, da, dsm, best);
+      stream_tile<E, VEC, MODE, K_PAIR>(trv, drv, vf0, vf1, c, cd, ta, da, dsm, best);
     } else {
       if (kind == K_PAIR)
-        stream_tile<E, VEC, MODE, K_PAIR>(trow, drow, e_begin / VEC, v1, c, cd, ta, da, dsm, best);
+        stream_tile<E, VEC, MODE, K_PAIR>(trv, drv, vf0, vf1, c, cd, ta, da, dsm, best);
       else
-        stream_tile<E, VEC, MODE, K_TSUM>(trow, drow, e_begin / VEC, v1, c, cd, ta, da, dsm, best);
+        stream_tile<E, VEC, MODE, K_TSUM>(trv, drv, vf0, vf1, c, cd, ta, da, dsm, best);
+    }
+    int elo = 0, ehi = 0;
+    if (PH && threadIdx.x < 2) edge_range(elo, ehi);
+    if (PH && elo < ehi) {
+      float ft[VEC], fd[VEC];
+      IO<E, VEC>::unpack(s_edge[threadIdx.x][0], ft);
+      if (kind == K_PAIR) IO<E, VEC>::unpack(s_edge[threadIdx.x][1], fd);
+      const int e0 = ((elo + ph) / VEC) * VEC - ph;  // row index of ft[0]
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) {
+        const int e = e0 + j;
+        if (e < elo || e >= ehi) continue;
+        const float x = ft[j];
+        if constexpr (ARGMAX) {
+          ta.hi = max_nan(ta.hi, x);
+          ta.lo = fminf(ta.lo, x);
+        } else {
+          // the sums; the maximum and its index are kept apart (the recorded group
+          // stays the one that holds the thread's maximum over whole vectors)
+          const float m0 = ta.m;
+          const int g0 = ta.g0, g1 = ta.g1;
+          const float xt[1] = {x};
+          if (kind == K_PAIR) {
+            const float xd[1] = {fd[j]};
+            pair_update<1, false, 0, SEPT>(ta, da, xt, xd, 0, c, 0, cd);
+          } else {
+            tsum_update<1, 0>(ta, xt, 0, c);
+          }
+          ta.m = m0;
+          ta.g0 = g0;
+          ta.g1 = g1;
+        }
+        // an edge element holding the thread's maximum carries its exact index (the head
+        // block precedes every whole vector of the chunk: it wins ties)
+        if (x > ta.m || (x == ta.m && ta.g0 >= 0 && e + ph < ta.g0)) {
+          ta.m = x;
+          ta.g0 = e + ph;
+          if constexpr (!ARGMAX) ta.g1 = kExactIdx;
+        }
+      }
     }
   } else {
     if constexpr (MODE == M_NKL) {
@@ -708,10 +746,12 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
   }
 
   Partial part;
-  if constexpr (VEC > 1)
-    part = reduce_tile<BlockSync, E, VEC, SEPT, 0, ARGMAX>(kind, ta, da, c, trow, cd);
-  else
+  if constexpr (VEC > 1) {
+    part = reduce_tile<BlockSync, E, VEC, SEPT, 0, ARGMAX>(kind, ta, da, c, trow - ph, cd);
+    if (PH && part.tidx != INT_MAX) part.tidx -= ph;  // from the aligned base to the row
+  } else {
     part = reduce_tile<BlockSync, E, 1, SEPT, 32>(kind, ta, da, c, trow, cd);
+  }
   if (threadIdx.x == 0) {
     float4* dst = reinterpret_cast<float4*>(p.part + tile);
     __stcg(dst, make_float4(part.tm, part.ts, __int_as_float(part.tidx), __int_as_float(part.bad)));

@@ -206,23 +206,23 @@ __device__ __forceinline__ void block_crossing(const float* table, int n, float 
   __syncthreads();
 }
 
-template <typename E, int VEC>
-__device__ __forceinline__ void vec_weights(const uint4& tv, const uint4* dv, int mode, float lt2, float ld2, float c,
-                                            float cd, float (&w)[VEC]) {
-  float ft[VEC], fd[VEC];
-  IO<E, VEC>::unpack(tv, ft);
-  if (mode == S_RESID) IO<E, VEC>::unpack(*dv, fd);
-  weights<VEC>(mode, ft, fd, lt2, ld2, c, cd, w);
+// Elements e0 + j outside the row [0, V) weigh nothing.
+template <int VEC>
+__device__ __forceinline__ void edge_mask(float (&ft)[VEC], float (&fd)[VEC], int e0, int V) {
+#pragma unroll
+  for (int j = 0; j < VEC; ++j)
+    if (e0 + j < 0 || e0 + j >= V) ft[j] = fd[j] = -INFINITY;
 }
 
 // Masses of stages [k0, k1) of the row pair (or row): in each 512-vector stage thread t
 // takes vectors t and t + 256 (lane-contiguous, so every copy instruction moves 512
 // consecutive bytes) through its private cp.async ring; entry (2k + h) * kWarps + w of
 // `table` receives the mass of warp w's 32-vector slice of half h of stage k -- token
-// order.
-template <typename E, int VEC>
+// order. PH: trow and drow are the rows' aligned bases (row element e is their element
+// e + ph), and the elements of the first and last vectors outside the row weigh 0.
+template <typename E, int VEC, bool PH>
 __device__ __forceinline__ void mass_pass(const E* trow, const E* drow, int mode, float lt2, float ld2, float c, float cd,
-                                          int NV, int k0, int k1, float* table, unsigned char* smem) {
+                                          int NV, int k0, int k1, float* table, unsigned char* smem, int ph, int V) {
   constexpr unsigned SLOT = kCV * kThreads * 16;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem) + 16u * t;
@@ -250,8 +250,11 @@ __device__ __forceinline__ void mass_pass(const E* trow, const E* drow, int mode
       const int v = (k0 + k) * 2 * kThreads + h * kThreads + t;
       float ls = 0.f;
       if (v < NV) {
-        float w[VEC];
-        vec_weights<E, VEC>(q[h * kThreads], q + (2 + h) * kThreads, mode, lt2, ld2, c, cd, w);
+        float ft[VEC], fd[VEC], w[VEC];
+        IO<E, VEC>::unpack(q[h * kThreads], ft);
+        if (mode == S_RESID) IO<E, VEC>::unpack(q[(2 + h) * kThreads], fd);
+        if (PH && (v == 0 || v == NV - 1)) edge_mask<VEC>(ft, fd, v * VEC - ph, V);
+        weights<VEC>(mode, ft, fd, lt2, ld2, c, cd, w);
         ls = tree_sum<VEC>(w);
       }
       const float ws = warp_sum(ls);
@@ -324,10 +327,11 @@ __device__ __forceinline__ void mass_pass_staged(const E* trow, const E* drow, i
 // slice -- one vector per lane, in token order -- and returns the token where the
 // running mass passes rem.
 // STAGED (rows off the 16-byte grid): the lane reads its VEC elements one by one, and
-// those past the row end weigh 0.
-template <typename E, int VEC, bool STAGED>
+// those past the row end weigh 0. PH: trow and drow are the rows' aligned bases (row
+// element e is their element e + ph).
+template <typename E, int VEC, bool STAGED, bool PH>
 __device__ __forceinline__ int slice_token(const E* trow, const E* drow, int mode, float lt2, float ld2, float c, float cd,
-                                           int V, int NV, int ent, float rem) {
+                                           int V, int NV, int ent, float rem, int ph = 0) {
   const int lane = threadIdx.x & 31;
   const int k = ent / kSlicesPerStage, h = (ent / kWarps) & 1, w = ent % kWarps;
   const int v = k * 2 * kThreads + h * kThreads + w * 32 + lane;
@@ -345,10 +349,11 @@ __device__ __forceinline__ int slice_token(const E* trow, const E* drow, int mod
       }
       weights<VEC>(mode, ft, fd, lt2, ld2, c, cd, wt);
     } else {
-      const uint4 tv = ld_stream16(trow + (size_t)v * VEC);
-      uint4 dv = tv;
-      if (mode == S_RESID) dv = ld_stream16(drow + (size_t)v * VEC);
-      vec_weights<E, VEC>(tv, &dv, mode, lt2, ld2, c, cd, wt);
+      float ft[VEC], fd[VEC];
+      IO<E, VEC>::unpack(ld_stream16(trow + (size_t)v * VEC), ft);
+      if (mode == S_RESID) IO<E, VEC>::unpack(ld_stream16(drow + (size_t)v * VEC), fd);
+      if (PH && (v == 0 || v == NV - 1)) edge_mask<VEC>(ft, fd, v * VEC - ph, V);
+      weights<VEC>(mode, ft, fd, lt2, ld2, c, cd, wt);
     }
   }
   const float ls = tree_sum<VEC>(wt);
@@ -375,8 +380,9 @@ __device__ __forceinline__ int slice_token(const E* trow, const E* drow, int mod
       }
     }
     if (y < 0) y = lastpos >= 0 ? lastpos : 0;
-    tok = v * VEC + y;
+    tok = v * VEC + y - ph;
     if (tok >= V) tok = V - 1;
+    if (tok < 0) tok = 0;
   }
   return __shfl_sync(kFull, tok, L);
 }
@@ -389,8 +395,10 @@ __device__ __forceinline__ int slice_token(const E* trow, const E* drow, int mod
 // the start of the next; for each part the block adds the part's stage count to the
 // sequence's ticket, and the block whose part completes the nst stages scans the
 // sequence's table and draws its token.
-template <typename E, int VEC, bool STAGED>
+// PH (aligned sampler): rows at one offset within the 16-byte grid, p.ph.
+template <typename E, int VEC, bool STAGED, bool PH = false>
 __global__ void __launch_bounds__(kThreads, 4) sample2_kernel(const __grid_constant__ SampleParams p) {
+  static_assert(!(STAGED && PH), "the staged sampler reads rows at any alignment");
   extern __shared__ __align__(128) unsigned char dsm[];
   // No griddepcontrol.wait: the grid starts while the tile kernel drains, and each part
   // waits only for its own sequence's record (published with release semantics by the
@@ -404,7 +412,8 @@ __global__ void __launch_bounds__(kThreads, 4) sample2_kernel(const __grid_const
   WarpRing ring;  // staged rows: the warp's bulk-copy ring, over every pass of the block
   if constexpr (STAGED) ring.init(s_bars[warp]);
   const size_t V = (size_t)p.V;
-  const int NV = (p.V + VEC - 1) / VEC;  // vectors of a row (the last one partial off the grid)
+  const int ph = PH ? p.ph : 0;               // the rows' offset within the 16-byte grid
+  const int NV = (p.V + ph + VEC - 1) / VEC;  // vectors of a row's aligned blocks
   const int nst = (NV + 2 * kThreads - 1) / (2 * kThreads);
   const long long total = (long long)p.B * nst;
   long long u0, u1;
@@ -458,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 4) sample2_kernel(const __grid_const
     if constexpr (STAGED)
       mass_pass_staged<E, VEC>(trow, drow, q.mode, q.lt2, q.ld2, p.c, p.cd, p.V, k0, k1, table, dsm, ring, p.status);
     else
-      mass_pass<E, VEC>(trow, drow, q.mode, q.lt2, q.ld2, p.c, p.cd, NV, k0, k1, table, dsm);
+      mass_pass<E, VEC, PH>(trow - ph, drow - ph, q.mode, q.lt2, q.ld2, p.c, p.cd, NV, k0, k1, table, dsm, ph, p.V);
     __syncthreads();  // orders every warp's table entries before thread 0's fence
     if (tid == 0) {
       // release: the block's table entries before its ticket; acquire: the other blocks'
@@ -478,12 +487,12 @@ __global__ void __launch_bounds__(kThreads, 4) sample2_kernel(const __grid_const
       if constexpr (STAGED)
         mass_pass_staged<E, VEC>(trow, drow, mode, q.lt2, q.ld2, p.c, p.cd, p.V, 0, nst, table, dsm, ring, p.status);
       else
-        mass_pass<E, VEC>(trow, drow, mode, q.lt2, q.ld2, p.c, p.cd, NV, 0, nst, table, dsm);
+        mass_pass<E, VEC, PH>(trow - ph, drow - ph, mode, q.lt2, q.ld2, p.c, p.cd, NV, 0, nst, table, dsm, ph, p.V);
       __syncthreads();
     }
     const int ent = sc.ent;
     if (warp == ent % kWarps) {
-      const int y = slice_token<E, VEC, STAGED>(trow, drow, mode, q.lt2, q.ld2, p.c, p.cd, p.V, NV, ent, sc.rem);
+      const int y = slice_token<E, VEC, STAGED, PH>(trow - ph, drow - ph, mode, q.lt2, q.ld2, p.c, p.cd, p.V, NV, ent, sc.rem, ph);
       if (lane == 0) p.out_tok[q.t_row] = y;
     }
     __syncthreads();

@@ -41,9 +41,11 @@ struct Layout {
 };
 
 // The aligned-row sampler keeps one float per 32-vector (one warp, one half-stage) slice
-// of a row: 16 per 512-vector stage.
+// of a row's aligned blocks: 16 per 512-vector stage, with room for rows at any offset
+// within the 16-byte grid.
 int table_stride_for(int V, spec_dtype dt) {
-  const long long nv = ceil_div(V, dt == SPEC_BF16 ? 8 : 4);
+  const int vec = dt == SPEC_BF16 ? 8 : 4;
+  const long long nv = ceil_div((long long)V + vec - 1, vec);
   return (int)(ceil_div(nv, 2 * kThreads) * kSlicesPerStage);
 }
 
@@ -199,23 +201,32 @@ cudaError_t launch_rows_t(const RowsParams& rp, long long tiles, cudaStream_t st
   return cudaLaunchKernelEx(&cfg, kern, rp);
 }
 
-// vec: every row on the 16-byte grid. Argmax rows (greedy, tree) off the grid take the
-// phased vector tiles (each tile applies its row's phase); pairs off the grid take the
-// staged path.
+// The tile kernel's layout of the rows: every row on the 16-byte grid (vector tiles); rows
+// off the grid with one offset within it for both rows of every pair (phased vector
+// tiles: each tile applies its row's offset; single rows always qualify); any other
+// layout (staged tiles).
+enum RowPath { P_VEC, P_PHASED, P_STAGED };
+
 template <int MODE>
-cudaError_t launch_rows(bool bf16, bool vec, const RowsParams& rp, long long tiles, cudaStream_t stream) {
+cudaError_t launch_rows(bool bf16, RowPath path, const RowsParams& rp, long long tiles, cudaStream_t stream) {
   if constexpr (MODE == M_GREEDY || MODE == M_TREE) {
-    if (bf16) return vec ? launch_rows_t<uint16_t, 8, MODE>(rp, tiles, stream) : launch_rows_t<uint16_t, 8, MODE, true>(rp, tiles, stream);
-    return vec ? launch_rows_t<float, 4, MODE>(rp, tiles, stream) : launch_rows_t<float, 4, MODE, true>(rp, tiles, stream);
+    if (bf16) return path == P_VEC ? launch_rows_t<uint16_t, 8, MODE>(rp, tiles, stream) : launch_rows_t<uint16_t, 8, MODE, true>(rp, tiles, stream);
+    return path == P_VEC ? launch_rows_t<float, 4, MODE>(rp, tiles, stream) : launch_rows_t<float, 4, MODE, true>(rp, tiles, stream);
   } else {
-    if (bf16) return vec ? launch_rows_t<uint16_t, 8, MODE>(rp, tiles, stream) : launch_rows_t<uint16_t, 1, MODE>(rp, tiles, stream);
-    return vec ? launch_rows_t<float, 4, MODE>(rp, tiles, stream) : launch_rows_t<float, 1, MODE>(rp, tiles, stream);
+    if (bf16) {
+      if (path == P_VEC) return launch_rows_t<uint16_t, 8, MODE>(rp, tiles, stream);
+      if (path == P_PHASED) return launch_rows_t<uint16_t, 8, MODE, true>(rp, tiles, stream);
+      return launch_rows_t<uint16_t, 1, MODE>(rp, tiles, stream);
+    }
+    if (path == P_VEC) return launch_rows_t<float, 4, MODE>(rp, tiles, stream);
+    if (path == P_PHASED) return launch_rows_t<float, 4, MODE, true>(rp, tiles, stream);
+    return launch_rows_t<float, 1, MODE>(rp, tiles, stream);
   }
 }
 
-template <typename E, int VEC, bool STAGED>
+template <typename E, int VEC, bool STAGED, bool PH = false>
 cudaError_t launch_sample2_t(const SampleParams& sp, long long blocks, cudaStream_t stream) {
-  auto kern = sample2_kernel<E, VEC, STAGED>;
+  auto kern = sample2_kernel<E, VEC, STAGED, PH>;
   const int smem = STAGED ? kStagedSmem : kRowsSmem;
   static std::atomic<unsigned long long> done{0};
   const cudaError_t e = ensure_smem_attr(kern, done, smem);
@@ -234,11 +245,16 @@ cudaError_t launch_sample2_t(const SampleParams& sp, long long blocks, cudaStrea
   return cudaLaunchKernelEx(&cfg, kern, sp);
 }
 
+// vec: the aligned sampler (rows on the 16-byte grid, or all at the offset sp.ph within it)
 cudaError_t launch_sample2(bool bf16, bool vec, const SampleParams& sp, long long blocks, cudaStream_t stream) {
-  if (bf16)
-    return vec ? launch_sample2_t<uint16_t, 8, false>(sp, blocks, stream)
-               : launch_sample2_t<uint16_t, 8, true>(sp, blocks, stream);
-  return vec ? launch_sample2_t<float, 4, false>(sp, blocks, stream) : launch_sample2_t<float, 4, true>(sp, blocks, stream);
+  if (bf16) {
+    if (!vec) return launch_sample2_t<uint16_t, 8, true>(sp, blocks, stream);
+    return sp.ph ? launch_sample2_t<uint16_t, 8, false, true>(sp, blocks, stream)
+                 : launch_sample2_t<uint16_t, 8, false>(sp, blocks, stream);
+  }
+  if (!vec) return launch_sample2_t<float, 4, true>(sp, blocks, stream);
+  return sp.ph ? launch_sample2_t<float, 4, false, true>(sp, blocks, stream)
+               : launch_sample2_t<float, 4, false>(sp, blocks, stream);
 }
 
 // Fused multi-draft tiles: when given, the verification launches multi_rows_kernel over
@@ -308,6 +324,16 @@ bool vec_path(spec_dtype dt, int V, const void* a, const void* b) {
   return ((long long)V * es) % 16 == 0 && aligned16(a) && aligned16(b);
 }
 
+// b == nullptr: single rows. Rows of a whole number of 16-byte blocks keep their base's
+// offset within the grid, so the rows of every pair share it when the bases do.
+RowPath row_path(spec_dtype dt, int V, const void* a, const void* b) {
+  if (vec_path(dt, V, a, b)) return P_VEC;
+  if (b == nullptr) return P_PHASED;
+  const int es = dt == SPEC_BF16 ? 2 : 4;
+  if (((long long)V * es) % 16 == 0 && (((uintptr_t)a ^ (uintptr_t)b) & 15u) == 0) return P_PHASED;
+  return P_STAGED;
+}
+
 bool temperature_ok(float T) { return isfinite(T) && T > 0.f; }
 
 // Host checks of an options block for a call of the given kind (stochastic, greedy or
@@ -373,7 +399,7 @@ spec_status stochastic_impl(spec_batch g, spec_dtype dtype, const void* target_l
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   char* ws = static_cast<char*>(workspace);
   const bool bf16 = dtype == SPEC_BF16;
-  const bool vec = vec_path(dtype, g.V, target_logits, draft_logits);
+  const RowPath path = row_path(dtype, g.V, target_logits, draft_logits);
 
   if (launch_prologue(g, L, ws, device_status, stream, options, zr) != cudaSuccess) return SPEC_ERR_CUDA;
   RowsParams rp = base_params(g, L, ws, device_status);
@@ -401,8 +427,8 @@ spec_status stochastic_impl(spec_batch g, spec_dtype dtype, const void* target_l
   // fused multi-draft tiles: (group, row, chunk), one per group row instead of per sequence row
   const long long tiles = mt ? (long long)(g.B / mt->K) * (g.gamma + 1) * L.nchunks : L.rows * L.nchunks;
   const cudaError_t le = mt     ? launch_multi<M_STOCH>(bf16, *mt, rp, tiles, stream)
-                         : sept ? launch_rows<M_STOCH2>(bf16, vec, rp, tiles, stream)
-                                : launch_rows<M_STOCH>(bf16, vec, rp, tiles, stream);
+                         : sept ? launch_rows<M_STOCH2>(bf16, path, rp, tiles, stream)
+                                : launch_rows<M_STOCH>(bf16, path, rp, tiles, stream);
   if (le != cudaSuccess) return SPEC_ERR_CUDA;
 
   SampleParams sp;
@@ -423,10 +449,15 @@ spec_status stochastic_impl(spec_batch g, spec_dtype dtype, const void* target_l
   sp.table_stride = L.table_stride;
   sp.tiles_done = reinterpret_cast<const unsigned*>(ws + L.cntA) + g.B;
   sp.ntiles = (unsigned)tiles;
+  // the aligned sampler takes phased rows only when every row sits at its base's offset
+  // (rows of a whole number of 16-byte blocks); single rows may be phased row by row
+  const bool uniform = ((long long)g.V * (long long)elem_bytes(dtype)) % 16 == 0;
+  const bool sampler_vec = path == P_VEC || (path == P_PHASED && uniform);
+  sp.ph = (path == P_PHASED && uniform) ? (int)(((uintptr_t)target_logits & 15u) / elem_bytes(dtype)) : 0;
   // One wave of blocks over the B * nst stages. The last kTailSeqs sequences (decided last
   // by the tile kernel) take short ranges of at least kTailStages stages on at most a
   // quarter of the wave, the others equal long ranges.
-  const long long nv = ceil_div(g.V, bf16 ? 8 : 4);
+  const long long nv = ceil_div((long long)g.V + sp.ph, bf16 ? 8 : 4);  // the rows' aligned blocks
   const long long nst = ceil_div(nv, 2 * kThreads);
   const long long tail_seqs = g.B < kTailSeqs ? g.B : kTailSeqs;
   const long long tail_total = tail_seqs * nst, head_total = ((long long)g.B - tail_seqs) * nst;
@@ -443,7 +474,7 @@ spec_status stochastic_impl(spec_batch g, spec_dtype dtype, const void* target_l
   sp.nb_head = (int)nb_head;
   sp.seg_head = (int)seg_head;
   sp.seg_tail = (int)seg_tail;
-  if (launch_sample2(bf16, vec, sp, nb_head + nb_tail, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (launch_sample2(bf16, sampler_vec, sp, nb_head + nb_tail, stream) != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;
 }
 
@@ -482,7 +513,7 @@ spec_status greedy_impl(spec_batch g, spec_dtype dtype, const void* target_logit
       return SPEC_ERR_CUDA;
     return SPEC_OK;
   }
-  if (launch_rows<M_GREEDY>(dtype == SPEC_BF16, vec_path(dtype, g.V, target_logits, nullptr), rp,
+  if (launch_rows<M_GREEDY>(dtype == SPEC_BF16, row_path(dtype, g.V, target_logits, nullptr), rp,
                             L.rows * L.nchunks, stream) != cudaSuccess)
     return SPEC_ERR_CUDA;
   return SPEC_OK;
@@ -683,7 +714,7 @@ spec_status spec_verify_tree(int32_t B, int32_t N, int32_t V, spec_dtype dtype, 
   rp.path_nodes = path_nodes;
   rp.out_tok = out_tokens;
   rp.c = rp.cd = 1.f;
-  if (launch_rows<M_TREE>(dtype == SPEC_BF16, vec_path(dtype, V, target_logits, nullptr), rp, L.rows * L.nchunks,
+  if (launch_rows<M_TREE>(dtype == SPEC_BF16, row_path(dtype, V, target_logits, nullptr), rp, L.rows * L.nchunks,
                           stream) != cudaSuccess)
     return SPEC_ERR_CUDA;
   return SPEC_OK;
@@ -723,7 +754,7 @@ spec_status spec_nkl_ex(spec_batch g, spec_dtype dtype, const void* target_logit
   rp.nkl = nkl;
   rp.mask = nkl_mask;
   apply_options(rp, options, SPEC_MODE_NKL);
-  if (launch_rows<M_NKL>(dtype == SPEC_BF16, vec_path(dtype, g.V, target_logits, draft_logits), rp,
+  if (launch_rows<M_NKL>(dtype == SPEC_BF16, row_path(dtype, g.V, target_logits, draft_logits), rp,
                          L.rows * L.nchunks, stream) != cudaSuccess)
     return SPEC_ERR_CUDA;
   return SPEC_OK;

@@ -161,16 +161,19 @@ def test_staged_path_ties_and_flat_rows(dev):
 
 
 @pytest.mark.parametrize("dtype", [synth.F32, synth.BF16])
-@pytest.mark.parametrize("V", [13, 4101, 70003])
-def test_argmax_rows_at_every_phase(dev, V, dtype):
-    """Greedy rows at every element phase of the 16-byte grid. Maxima sit in the partial
-    blocks at the ends of the vocabulary chunks (the first and last elements of a row; ties
-    at every multiple of 8, where chunks start, or at every 8j + 7, where they end, from a
-    third of the row on) and tie with maxima inside the chunks, so the lowest index must
-    come out of the element-by-element edge folds and the chunk merge."""
+@pytest.mark.parametrize("V", [13, 4101, 4104, 70003, 70008])
+def test_rows_at_every_phase(dev, V, dtype):
+    """Rows at every element phase of the 16-byte grid, through the greedy, stochastic and
+    NKL calls (both buffers shifted alike: phased vector tiles when the row is a whole
+    number of 16-byte blocks, else the staged path). Maxima sit in the partial blocks at
+    the ends of the vocabulary chunks (the first and last elements of a row; ties at every
+    multiple of 8, where chunks start, or at every 8j + 7, where they end, from a third of
+    the row on) and tie with maxima inside the chunks, so the lowest index must come out
+    of the element-by-element edge folds and the chunk merge."""
     rng = np.random.default_rng(V)
     R = 9
     t = rng.normal(0.0, 1.0, (R, V)).astype(np.float32)
+    d = rng.normal(0.0, 1.0, (R - 1, V)).astype(np.float32)
     m0 = V // 3
     plant = [
         [0, V // 2],                                  # a tie: the first element wins
@@ -192,7 +195,7 @@ def test_argmax_rows_at_every_phase(dev, V, dtype):
     tokens = np.array(expect[:R - 1], np.int32)  # every draft the target's argmax: all must match
     w = synth.StochasticWorkload(B=1, V=V, dtype=dtype, T=1.0, gammas=np.array([R - 1], np.int32),
                                  cu_draft=np.array([0, R - 1], np.int32), target=synth.storage(t, dtype),
-                                 draft=synth.storage(np.zeros((R - 1, V), np.float32), dtype), tokens=tokens,
+                                 draft=synth.storage(d, dtype), tokens=tokens,
                                  u_accept=np.full(R - 1, 0.5, np.float32), u_sample=np.array([0.5], np.float32))
     for off in range(8 if dtype == synth.BF16 else 4):
         res = run_greedy(w, dev, offset=off)
@@ -200,6 +203,11 @@ def test_argmax_rows_at_every_phase(dev, V, dtype):
         assert int(res["n_accepted"][0]) == R - 1, off
         assert list(res["out_tokens"][:R]) == expect, off
         compare_greedy(w, res, [0])
+        rs = run_stochastic(w, dev, offset=off)
+        assert rs["device_status"][0] == 0
+        assert list(rs["greedy_tokens"][:R]) == expect, off
+        compare_stochastic(w, rs, [0])
+        compare_nkl(w, run_nkl(w, dev, offset=off), [0])
 
 
 @pytest.mark.parametrize("V,dtype,offset", [(3001, synth.BF16, 0), (128256, synth.BF16, 3), (5001, synth.F32, 1)])
