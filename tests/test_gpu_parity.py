@@ -120,15 +120,15 @@ def test_odd_vocab_sizes(dev, V, dtype):
     compare_nkl(w, run_nkl(w, dev), range(w.B))
 
 
-# ---------------------------------------------------------------- staged path (rows off the 16-byte grid)
+# ---------------------------------------------------------------- rows off the 16-byte grid (phased and staged paths)
 
 @pytest.mark.parametrize("offset", [0, 1, (0, 3), (5, 2)])
 @pytest.mark.parametrize("V", [3 * 4096, 3 * 4096 + 37])
 @pytest.mark.parametrize("dtype", [synth.F32, synth.BF16])
-def test_staged_path_offsets(dev, offset, V, dtype):
-    """Base pointers shifted by whole elements (target and draft alike or apart), and row
-    lengths off the 16-byte grid: several stages per tile and a ragged last stage, in every
-    mode."""
+def test_off_grid_offsets(dev, offset, V, dtype):
+    """Base pointers shifted by whole elements (target and draft alike: the phased path when
+    the rows are whole 16-byte blocks; apart: the staged path), and row lengths off the
+    16-byte grid: several stages per tile and a ragged last stage, in every mode."""
     if offset == 0 and V % 8 == 0:
         pytest.skip("the aligned path")
     w = handmade(4, 5, V, dtype, T=0.7, seed=11 + V % 7)
@@ -140,7 +140,7 @@ def test_staged_path_offsets(dev, offset, V, dtype):
     compare_greedy(w, run_greedy(w, dev, offset=ot), range(w.B))
 
 
-def test_staged_path_ties_and_flat_rows(dev):
+def test_off_grid_ties_and_flat_rows(dev):
     """Lowest index of a tied maximum when the tied entries share one thread's strided
     group, sit in different groups, or fill a whole (flat) row."""
     V = 3000
@@ -211,7 +211,7 @@ def test_rows_at_every_phase(dev, V, dtype):
 
 
 @pytest.mark.parametrize("V,dtype,offset", [(3001, synth.BF16, 0), (128256, synth.BF16, 3), (5001, synth.F32, 1)])
-def test_staged_path_tree(dev, V, dtype, offset):
+def test_off_grid_tree(dev, V, dtype, offset):
     """The tree call on rows off the 16-byte grid (an odd vocabulary, a shifted buffer):
     the argmax of every node's row, its lowest index on ties, the deepest accepted path."""
     w = synth.make_tree(12, V, dtype, seed=V % 1000 + offset)
@@ -221,7 +221,7 @@ def test_staged_path_tree(dev, V, dtype, offset):
     assert np.any(res["accept_len"] > 1)
 
 
-def test_staged_path_nkl_positions(dev):
+def test_off_grid_nkl_positions(dev):
     """The position-adaptive NKL mask on an odd vocabulary (staged pairs)."""
     w = synth.make_stochastic(12, 50257, synth.BF16, 0.8, seed=88, gamma_range=(1, 6), agreement=0.8)
     pos = np.random.default_rng(88).integers(1, 3000, w.B).astype(np.int32)
@@ -230,9 +230,10 @@ def test_staged_path_nkl_positions(dev):
     compare_stochastic(w, res, range(w.B), positions=pos, min_block_len=2)
 
 
-def test_staged_path_headline_shape(dev):
+def test_off_grid_headline_shape(dev):
     """The headline batch (B=256, gamma=8, V=128256, bf16) with the logits one element off
-    the 16-byte grid: every sampler range and tier, sampled against the oracle."""
+    the 16-byte grid (phased tiles and sampler): every sampler range and tier, sampled
+    against the oracle."""
     w = workload(synth.HEADLINE)
     res = run_stochastic(w, dev, offset=1)
     assert res["device_status"][0] == 0
@@ -246,7 +247,7 @@ def test_staged_path_headline_shape(dev):
     np.testing.assert_allclose(res["alpha"], aligned["alpha"], rtol=1e-4)
 
 
-def test_staged_path_odd_vocabulary(dev):
+def test_off_grid_odd_vocabulary(dev):
     """A vocabulary whose bf16 rows are not a multiple of 16 bytes (V = 50257): every row
     has its own phase, target and draft rows of one position differ in phase."""
     w = synth.make_stochastic(64, 50257, synth.BF16, 0.8, seed=27, gamma=5)
