@@ -175,7 +175,8 @@ def _to_dev(a, dev):
 
 def _shifted(t, offset):
     """A copy of device tensor t that starts `offset` elements into its buffer (offset > 0
-    puts the rows off the 16-byte grid: the library's staged path)."""
+    puts the rows off the 16-byte grid: the library's phased path, every row at one
+    offset)."""
     import torch
     if offset == 0:
         return t
@@ -471,7 +472,7 @@ def run_ours(args):
         modes["accept_summary_64_slots"] = {"us_per_call": t_sm * 1e6,
                                             "note": "one 64-thread block; the figure includes the host's enqueue rate"}
         if args.offset == 0:
-            # the same call with the logits one element off the 16-byte grid: the staged path
+            # the same call with the logits one element off the 16-byte grid: the phased path
             ts, ds = _shifted(call.t, 1), _shifted(call.d, 1)
             s_out = {}
             sfn = lambda: api.spec_verify_stochastic(ts, ds, call.tok, w.T, call.ua, call.us,  # noqa: E731
@@ -479,7 +480,7 @@ def run_ours(args):
             t_s = time_mode(sfn, 200, 10, dev)
             sg_out = {}
             t_sg = time_mode(lambda: api.spec_verify_greedy(ts, call.tok, gamma=gam, out=sg_out), 200, 10, dev)
-            modes["stochastic_staged_offset1_B256_g8_V128256"] = {
+            modes["stochastic_offset1_B256_g8_V128256"] = {
                 "us_per_call": t_s * 1e6, "GBps": ab["stochastic"] / t_s / 1e9,
                 "frac_of_peak": ab["stochastic"] / t_s / 1e9 / hbm, "greedy_us_per_call": t_sg * 1e6,
                 "note": "logits one element off the 16-byte grid (as for a vocabulary whose row is not a "
@@ -530,7 +531,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"B{w.B}_g8_V128256_bf16: stochastic verify + NKL(delta=0.15) + greedy, one call"
-                               + (f" (logits {args.offset} element(s) off the 16-byte grid: staged path)"
+                               + (f" (logits {args.offset} element(s) off the 16-byte grid: phased path)"
                                   if args.offset else ""),
                    "B": w.B, "gamma": 8, "V": w.V, "T": w.T, "seed": cfg.seed, "rows_per_step": rows_step,
                    "l2": f"inputs {(w.target.nbytes + w.draft.nbytes) / 1e6:.0f} MB per step, larger than the "
@@ -630,7 +631,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--skip-ragged", action="store_true")
     ap.add_argument("--offset", type=int, default=0, metavar="N",
-                    help="shift the timed call's logits by N elements (N not a multiple of 8: the staged path)")
+                    help="shift the timed call's logits by N elements (N not a multiple of 8: the phased path)")
     ap.add_argument("--batch", type=int, default=None,
                     help="sequences per step (default: the workload's 256); smaller slices serve profiling")
     ap.add_argument("--multi", type=int, default=None, metavar="G",

@@ -43,7 +43,8 @@ def _argmax_drafts(w, frac, seed):
                                             (4097, synth.BF16, 0), (5000, synth.BF16, 1)])
 def test_separate_draft_temperature(dev, V, dtype, offset):
     """T_t = 0.8, T_d = 0.4 ([PD] 4.4's ranges): q(x), alpha and the residual at T_d, NKL at
-    T_t; vector path (one and several chunks), staged path (odd V, misaligned rows)."""
+    T_t; vector path (one and several chunks), staged path (odd V), phased tiles (rows
+    shifted by one element)."""
     w = handmade(4, 5, V, dtype, T=0.8, seed=V + offset)
     w.draft[:] = synth.storage(0.5 * O.widen(w.draft, w.dtype), dtype)  # a peakier drafter at T_d = 0.4
     res = run_stochastic(w, dev, offset=offset, options={"temperature_draft": 0.4})
