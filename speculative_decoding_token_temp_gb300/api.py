@@ -119,7 +119,8 @@ def spec_verify_stochastic(target: torch.Tensor, draft: torch.Tensor, draft_toke
                            cu_draft: torch.Tensor | None = None, gamma: int | None = None,
                            nkl_delta: float = 0.15, want_probs: bool = True, want_nkl: bool = True,
                            want_greedy: bool = True, out: dict | None = None, workspace=None,
-                           device_status: torch.Tensor | None = None, _options: dict | None = None) -> dict:
+                           device_status: torch.Tensor | None = None, _options: dict | None = None,
+                           _static: bool = False) -> dict:
     """Stochastic verification with residual / bonus resampling; see spec_verify.h.
 
     Returns a dict of device tensors: n_accepted [B], out_tokens [total_draft+B] (dense:
@@ -160,11 +161,17 @@ def spec_verify_stochastic(target: torch.Tensor, draft: torch.Tensor, draft_toke
             device_status = torch.zeros(1, dtype=torch.int32, device=dev)
     o["device_status"] = device_status
     gb = SpecBatch(B, g, V, total, _ptr(cu))
-    nbytes = int(_lib.lib().spec_workspace_bytes(gb, dt, _lib.SPEC_MODE_STOCHASTIC))
-    ws = _workspace(workspace, nbytes, dev)
     args = (gb, dt, _ptr(target), _ptr(draft) if total > 0 else None, _ptr(draft_tokens), float(temperature),
             _ptr(u_accept), _ptr(u_sample), _ptr(n_acc), _ptr(out_tok), _ptr(p_x), _ptr(q_x), _ptr(alpha),
             _ptr(nkl), _ptr(mask), float(nkl_delta), _ptr(g_n), _ptr(g_tok))
+    if _static:
+        if _options is not None or workspace is not None:
+            raise ValueError("the static-scratch call takes neither options nor a workspace")
+        code = _lib.lib().spec_verify_stochastic_static(*args, _ptr(device_status), _stream(dev))
+        check("spec_verify_stochastic_static", code)
+        return o
+    nbytes = int(_lib.lib().spec_workspace_bytes(gb, dt, _lib.SPEC_MODE_STOCHASTIC))
+    ws = _workspace(workspace, nbytes, dev)
     tail = (_ptr(device_status), _ptr(ws), ws.numel(), _stream(dev))
     if _options is None:
         code = _lib.lib().spec_verify_stochastic(*args, *tail)
@@ -174,6 +181,12 @@ def spec_verify_stochastic(target: torch.Tensor, draft: torch.Tensor, draft_toke
         code = _lib.lib().spec_verify_stochastic_ex(*args, ctypes.byref(opts), *tail)
         check("spec_verify_stochastic_ex", code)
     return o
+
+
+def spec_verify_stochastic_static(target, draft, draft_tokens, temperature, u_accept, u_sample, **kw) -> dict:
+    """spec_verify_stochastic on the library's static device scratch instead of a workspace
+    (for callers that cannot allocate; one such call in flight per GPU); see spec_verify.h."""
+    return spec_verify_stochastic(target, draft, draft_tokens, temperature, u_accept, u_sample, _static=True, **kw)
 
 
 def spec_verify_greedy(target: torch.Tensor, draft_tokens: torch.Tensor, *, cu_draft=None, gamma=None,
@@ -207,6 +220,35 @@ def spec_verify_greedy(target: torch.Tensor, draft_tokens: torch.Tensor, *, cu_d
         opts = _fill_options(_options, o, dev, B, total)
         check("spec_verify_greedy_ex", _lib.lib().spec_verify_greedy_ex(*args, ctypes.byref(opts), *tail))
     return o
+
+
+def spec_tree_workspace_bytes(B: int, N: int, V: int) -> int:
+    """Workspace bytes of spec_verify_tree for B sequences of N nodes over V tokens (0 when
+    the geometry is invalid)."""
+    return int(_lib.lib().spec_tree_workspace_bytes(int(B), int(N), int(V)))
+
+
+def spec_status_str(code: int) -> str:
+    """The library's description of a spec_status value."""
+    return _lib.lib().spec_status_str(int(code)).decode()
+
+
+def spec_selftest_wait_timeout(device=None, *, device_status: torch.Tensor | None = None) -> torch.Tensor:
+    """The failure-detection self-test: the sampler's bounded wait runs against a decision
+    that nothing publishes and gives up after its limit. Returns the device status word
+    (SPEC_DEV_TIMEOUT set once the stream has reached it); see spec_verify.h."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    if device_status is None:
+        device_status = torch.zeros(1, dtype=torch.int32, device=dev)
+    _need(device_status, "device_status", torch.int32, 1, dev)
+    g = SpecBatch(1, 1, 8, 1, None)
+    nbytes = int(_lib.lib().spec_workspace_bytes(g, _lib.SPEC_BF16, _lib.SPEC_MODE_STOCHASTIC))
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    code = _lib.lib().spec_selftest_wait_timeout(_ptr(device_status), _ptr(ws), ws.numel(), _stream(dev))
+    check("spec_selftest_wait_timeout", code)
+    # the workspace stays referenced until the stream has passed the self-test
+    torch.cuda.current_stream(dev).synchronize()
+    return device_status
 
 
 def spec_tree_depth(parent) -> int:

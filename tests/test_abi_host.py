@@ -207,3 +207,15 @@ def test_multi_draft_checks_without_launch(lib):
     single = lib.spec_workspace_bytes(_g(192, 8, 128256), _lib.SPEC_BF16, _lib.SPEC_MODE_STOCHASTIC)
     assert sto > single and lib.spec_multi_workspace_bytes(mb, _lib.SPEC_BF16, 0) < sto
     assert lib.spec_multi_workspace_bytes(_lib.SpecMultiBatch(4, 1, 2, 100), _lib.SPEC_BF16, 1) == 0
+
+
+def test_python_binding_names_every_entry_point(lib):
+    """The binding has a same-named function for every entry point the header declares;
+    the host-only ones answer without a GPU."""
+    from speculative_decoding_token_temp_gb300 import api
+    assert [n for n in _lib.declared_functions() if not callable(getattr(api, n, None))] == []
+    assert api.spec_status_str(0) == "ok"
+    assert "workspace" in api.spec_status_str(_lib.SPEC_ERR_WORKSPACE)
+    assert api.spec_tree_workspace_bytes(32, 12, 128256) == lib.spec_tree_workspace_bytes(32, 12, 128256) > 0
+    assert api.spec_tree_workspace_bytes(32, 65, 128256) == 0
+    assert api.spec_tree_depth([-1, -1, -1, 0, 1, 2, 3, 4, 5, 6, 7, 8]) == 4
