@@ -647,3 +647,128 @@ def test_sharded_draw_equals_the_whole_row():
         if abs(c0 / Z0 - u) > 1e-9 and abs(c1 / Z0 - u) > 1e-9:    # away from a boundary: exactly the token
             assert y == y0
         assert w[y] > 0
+
+
+# ---------------------------------------------------------------- R6: a rejection that meets Z = 0
+
+def test_zero_residual_draws_from_p_of_the_rejected_row():
+    """R6. Identical target and draft rows give alpha = 1 and max(0, p - q) = 0 exactly; a
+    uniform above 1 forces the rejection all the same (accept iff u <= alpha), so the
+    residual has Z = 0 and the correction comes from p of the rejected position's own
+    target row. V = 2 closed form: y = 1 iff u_sample >= sigmoid((z0 - z1) / T) of that
+    row. The next target row and the bonus row lean the other way, so drawing from either
+    (or reading the wrong position) changes y."""
+    T = 0.9
+    same = np.array([2.0, 0.0])                  # p0 = sigmoid(2 / T) = 0.902
+    other = np.array([0.0, 2.0])                 # p0 = 0.098
+    for n_rej in (0, 1):
+        t = np.stack([other, other, other])
+        t[n_rej] = same
+        d = t[:2].copy()                          # draft rows equal to the target rows: alpha = 1
+        u = np.array([0.0, 0.0])
+        u[n_rej] = 1.5
+        p0 = 1.0 / (1.0 + math.exp(-2.0 / T))
+        for us in (0.05, 0.5, p0 - 1e-6, p0 + 1e-6, 0.99):
+            r = O.verify_stochastic_sequence(t, d, np.array([1, 0]), T, u, us)
+            assert r["alpha"][n_rej] == 1.0
+            assert r["n"] == n_rej
+            assert ("zero_residual", n_rej) in r["flags"] and r["flag"]
+            assert r["tokens"][n_rej] == (1 if us >= p0 else 0), (n_rej, us)
+            assert list(r["tokens"][:n_rej]) == [1, 0][:n_rej] and np.all(r["tokens"][n_rej + 1:] == -1)
+
+
+def test_zero_residual_inverse_cdf_over_p_matches_scipy():
+    """R6 with a longer row: the correction after a rejection on identical rows is the
+    inverse CDF of scipy's softmax of that row at T, for uniforms away from its steps."""
+    rng = np.random.default_rng(91)
+    V, T = 7, 0.7
+    row = rng.normal(0, 1.5, V)
+    t = np.stack([row, rng.normal(0, 1.5, V)])
+    p = sps.softmax(row / T)
+    C = np.cumsum(p)
+    for us in rng.random(40):
+        if np.min(np.abs(C - us)) < 1e-9:
+            continue
+        r = O.verify_stochastic_sequence(t, row[None, :].copy(), np.array([3]), T, np.array([2.0]), float(us))
+        assert r["n"] == 0 and r["tokens"][0] == int(np.argmax(C > us))
+
+
+# ---------------------------------------------------------------- batch drivers over the packed layout
+
+def _packed_ragged(seed, gammas, V):
+    """A packed batch built by concatenating per-sequence arrays, so each sequence's rows
+    are known without the layout's index arithmetic."""
+    rng = np.random.default_rng(seed)
+    per = []
+    for g in gammas:
+        t = rng.normal(0, 2, (g + 1, V)).astype(np.float32)
+        d = (0.9 * t[:g] + rng.normal(0, 1, (g, V))).astype(np.float32)
+        tok = rng.integers(0, V, g).astype(np.int32)
+        amax = np.argmax(t[:g], axis=1) if g else np.zeros(0, np.int64)
+        tok = np.where(rng.random(g) < 0.6, amax, tok).astype(np.int32)   # greedy runs of matches
+        per.append((t, d, tok, rng.random(g).astype(np.float32), np.float32(rng.random())))
+    target = np.concatenate([p[0] for p in per])
+    draft = np.concatenate([p[1] for p in per]) if sum(gammas) else np.zeros((0, V), np.float32)
+    tokens = np.concatenate([p[2] for p in per])
+    u_acc = np.concatenate([p[3] for p in per])
+    u_smp = np.array([p[4] for p in per], np.float32)
+    cu = np.zeros(len(gammas) + 1, np.int32)
+    cu[1:] = np.cumsum(gammas)
+    return per, target, draft, tokens, u_acc, u_smp, cu
+
+
+def _same(a, b):
+    if isinstance(a, np.ndarray) or isinstance(b, np.ndarray):
+        return np.array_equal(np.asarray(a), np.asarray(b), equal_nan=True)
+    return a == b
+
+
+def test_packed_drivers_index_every_sequence():
+    """verify_stochastic, verify_greedy and nkl_rows on a ragged batch with empty sequences
+    (first, middle and last) give, for every sequence, exactly the per-sequence functions'
+    results on that sequence's own arrays: a slip in the target base cu[b] + b, the draft
+    base cu[b] or the per-sequence uniform fails here."""
+    gammas = [0, 3, 5, 0, 1, 4, 2, 0]
+    V, T = 23, 0.8
+    per, target, draft, tokens, u_acc, u_smp, cu = _packed_ragged(5, gammas, V)
+    pos = np.arange(1, len(gammas) + 1, dtype=np.int32) * 7
+    st = O.verify_stochastic(target, draft, tokens, cu, T, u_acc, u_smp, "f32", positions=pos, min_block_len=2)
+    gr = O.verify_greedy(target, tokens, cu, "f32", min_block_len=2)
+    nk = O.nkl_rows(target, draft, cu, T, "f32", positions=pos)
+    assert sorted(st) == sorted(gr) == sorted(nk) == list(range(len(gammas)))
+    for b, (t, d, tok, ua, us) in enumerate(per):
+        t64, d64 = t.astype(np.float64), d.astype(np.float64)
+        ref = O.verify_stochastic_sequence(t64, d64, tok, T, ua.astype(np.float64), float(us), position=int(pos[b]),
+                                           min_block_len=2)
+        for k in ("n", "tokens", "p_x", "q_x", "alpha", "nkl", "mask", "greedy_n", "greedy_tokens", "block_n",
+                  "block_tokens", "flags"):
+            assert _same(st[b][k], ref[k]), (b, k)
+        gref = O.verify_greedy_sequence(t64, tok, min_block_len=2)
+        for k in ("n", "tokens", "block_n", "block_tokens"):
+            assert _same(gr[b][k], gref[k]), (b, k)
+        want = [O.nkl_pair(t64[i], d64[i], T)[0] for i in range(len(tok))]
+        assert np.array_equal(nk[b]["nkl"], np.array(want)), b
+        thr = [O.position_delta(int(pos[b]) + i) for i in range(len(tok))]
+        assert list(nk[b]["mask"]) == [1 if a < th else 0 for a, th in zip(want, thr)], b
+    # the uniform each sequence draws with is its own: sequence b's u_sample drives its draw
+    assert len({float(x) for x in u_smp}) == len(gammas)
+
+
+def test_packed_tree_driver_indexes_every_sequence():
+    """verify_tree over B packed trees equals verify_tree_sequence on each tree's own
+    N + 1 rows (a slip in the row base b * (N + 1) or in the node-token row fails)."""
+    rng = np.random.default_rng(6)
+    parent = [-1, -1, 0, 1, 2, 2, 4]
+    N, V, B = len(parent), 11, 5
+    rows = [rng.normal(0, 1, (N + 1, V)).astype(np.float32) for _ in range(B)]
+    for r in rows:
+        r[:, 3] += 2.5                             # most argmaxes at token 3: deep accepted paths
+    node = np.where(rng.random((B, N)) < 0.8, 3, rng.integers(0, V, (B, N))).astype(np.int32)
+    res = O.verify_tree(np.concatenate(rows), node, parent, "f32")
+    deepest = 0
+    for b in range(B):
+        ref = O.verify_tree_sequence(rows[b].astype(np.float64), node[b], parent)
+        assert res[b]["len"] == ref["len"]
+        assert np.array_equal(res[b]["path"], ref["path"]) and np.array_equal(res[b]["tokens"], ref["tokens"])
+        deepest = max(deepest, ref["len"])
+    assert deepest >= 3
