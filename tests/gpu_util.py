@@ -6,6 +6,10 @@ from oracle import oracle as O
 from speculative_decoding_token_temp_gb300 import api, synth
 
 REL = 1e-4        # p(x), q(x), alpha, NKL: relative to fp64
+# Oracle flags that mark a decision within the band of its boundary (|u - alpha|, or the
+# CDF gap to u, below 1e-5; and reading R6's zero residual). Only these excuse a differing
+# sequence; the informational q(x) < 1e-8 flag (reading R3) does not.
+BAND_FLAGS = ("accept_band", "cdf_band", "zero_residual")
 NKL_ABS = 2e-6    # NKL near zero: fp32 terms of size ~|E_q[a]| ~ 10 carry ~1e-6 absolute error, / ln V
 
 
@@ -54,18 +58,21 @@ def run_stochastic(w, dev, T=None, delta=0.15, offset=0, options=None):
 
 
 def compare_stochastic(w, res, seqs, T=None, delta=0.15, check_greedy=True, T_draft=None, positions=None,
-                       min_block_len=0):
-    """n / tokens bit-exact for every sequence the oracle does not flag; a flagged sequence
-    (a decision within 1e-5 of its boundary) may differ, but at most max(1, 1e-4 of the
-    sequences compared) may. Reals within REL; the NKL mask equal except within the NKL
+                       min_block_len=0, ref=None):
+    """n / tokens bit-exact for every sequence without a band flag; a sequence with one (a
+    decision within 1e-5 of its boundary, BAND_FLAGS) may differ, but at most max(1, 1e-4
+    of the target rows compared) may. Reals within REL; the NKL mask equal except within the NKL
     tolerance of its threshold (delta, or the position-adaptive one); block-accept outputs
-    bit-exact. Returns (compared, flagged, mismatched)."""
+    bit-exact. ref: the oracle's results for these sequences when already computed (e.g.
+    by oracle_pool), else computed here. Returns (compared, band-flagged, mismatched)."""
     T = w.T if T is None else T
-    ref = O.verify_stochastic(w.target, w.draft, w.tokens, w.cu_draft, T, w.u_accept, w.u_sample, w.dtype,
-                              nkl_delta=delta, seqs=seqs, T_draft=T_draft, positions=positions,
-                              min_block_len=min_block_len)
+    if ref is None:
+        ref = O.verify_stochastic(w.target, w.draft, w.tokens, w.cu_draft, T, w.u_accept, w.u_sample, w.dtype,
+                                  nkl_delta=delta, seqs=seqs, T_draft=T_draft, positions=positions,
+                                  min_block_len=min_block_len)
     flagged = mismatched = 0
     seqs = list(seqs)
+    rows = sum(int(w.gammas[b]) + 1 for b in seqs)
     for b in seqs:
         r = ref[b]
         g = int(w.gammas[b])
@@ -73,9 +80,11 @@ def compare_stochastic(w, res, seqs, T=None, delta=0.15, check_greedy=True, T_dr
         n = int(res["n_accepted"][b])
         toks = res["out_tokens"][t0:t0 + g + 1]
         same = n == r["n"] and list(toks) == list(r["tokens"])
-        flagged += int(r["flag"])
+        banded = any(f[0] in BAND_FLAGS for f in r["flags"])
+        flagged += int(banded)
         if not same:
-            assert r["flag"], (b, n, r["n"], list(toks), list(r["tokens"]), r["alpha"], w.u_accept[d0:d0 + g])
+            assert banded, (b, n, r["n"], list(toks), list(r["tokens"]), r["flags"], r["alpha"],
+                            w.u_accept[d0:d0 + g])
             mismatched += 1
         if g:
             for k in ("p_x", "q_x", "alpha"):
@@ -97,7 +106,7 @@ def compare_stochastic(w, res, seqs, T=None, delta=0.15, check_greedy=True, T_dr
         if check_greedy:
             assert int(res["greedy_n"][b]) == r["greedy_n"]
             assert list(res["greedy_tokens"][t0:t0 + g + 1]) == list(r["greedy_tokens"])
-    assert mismatched <= max(1, int(1e-4 * len(seqs))), (mismatched, len(seqs))
+    assert mismatched <= max(1, int(1e-4 * rows)), (mismatched, len(seqs), rows)
     return len(seqs), flagged, mismatched
 
 
@@ -113,8 +122,9 @@ def run_greedy(w, dev, options=None, offset=0):
     return {k: v.cpu().numpy() for k, v in res.items()}
 
 
-def compare_greedy(w, res, seqs, min_block_len=0):
-    ref = O.verify_greedy(w.target, w.tokens, w.cu_draft, w.dtype, seqs=seqs, min_block_len=min_block_len)
+def compare_greedy(w, res, seqs, min_block_len=0, ref=None):
+    if ref is None:
+        ref = O.verify_greedy(w.target, w.tokens, w.cu_draft, w.dtype, seqs=seqs, min_block_len=min_block_len)
     for b in seqs:
         g = int(w.gammas[b])
         t0 = w.target_base(b)
@@ -140,8 +150,9 @@ def run_nkl(w, dev, delta=0.15, positions=None, offset=0):
     return {k: v.cpu().numpy() for k, v in res.items()}
 
 
-def compare_nkl(w, res, seqs, delta=0.15, positions=None):
-    ref = O.nkl_rows(w.target, w.draft, w.cu_draft, w.T, w.dtype, delta=delta, seqs=seqs, positions=positions)
+def compare_nkl(w, res, seqs, delta=0.15, positions=None, ref=None):
+    if ref is None:
+        ref = O.nkl_rows(w.target, w.draft, w.cu_draft, w.T, w.dtype, delta=delta, seqs=seqs, positions=positions)
     for b in seqs:
         g = int(w.gammas[b])
         d0 = w.draft_base(b)

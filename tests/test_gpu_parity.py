@@ -12,8 +12,9 @@ import torch
 from oracle import oracle as O
 from speculative_decoding_token_temp_gb300 import _lib, api, synth
 
+import oracle_pool
 from gpu_util import (compare_greedy, compare_nkl, compare_stochastic, compare_tree, handmade, run_greedy,
-                      run_nkl, run_stochastic, run_tree, sample_seqs, to_dev)
+                      run_nkl, run_stochastic, run_tree, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -52,25 +53,46 @@ def test_B64_g5_V32000_bf16_all_sequences(dev, T):
     w = synth.MID.make(T=T)
     res = run_stochastic(w, dev)
     n, flagged, mismatched = compare_stochastic(w, res, range(w.B))
-    print(f"B=64 workload, T={T}: {flagged} of {n} sequences flagged, {mismatched} differ")
+    _report(f"B=64 stochastic T={T}", w, n, flagged, mismatched)
     assert res["device_status"][0] == 0
     compare_greedy(w, run_greedy(w, dev), range(w.B))
     compare_nkl(w, run_nkl(w, dev), range(w.B))
 
 
-def test_headline_B256_g8_V128256_sampled(dev):
+def _oracle(kind, w, key=None, **kw):
+    """The oracle over every sequence of w, on every host core, cached per workload."""
+    k = (w.name, w.B, w.V, w.T, w.dtype, kind, key)
+    if k not in _ORACLE:
+        _ORACLE[k] = oracle_pool.oracle_batch(kind, w, **kw)
+    return _ORACLE[k]
+
+
+_ORACLE = {}
+
+
+def _report(label, w, n, flagged, mismatched):
+    """One line per workload: sequences compared, band-flagged by the oracle (a decision
+    within 1e-5 of its boundary), and differing (at most max(1, 1e-4 of the rows))."""
+    rows = int(w.total_target)
+    print(f"PARITY {label}: {n} sequences ({rows} target rows) compared, {flagged} band-flagged by the oracle "
+          f"({flagged / max(rows, 1):.2e} of rows), {mismatched} differ (budget max(1, 1e-4 of rows) = "
+          f"{max(1, int(1e-4 * rows))})")
+
+
+def test_headline_B256_g8_V128256_all_sequences(dev):
+    """Every sequence of the headline batch against the oracle: the stochastic decisions
+    (count and tokens bit-exact except flagged sequences, at most max(1, 1e-4 of the rows)
+    of them differing), p(x), q(x), alpha, NKL and its mask, and the fused greedy outputs;
+    the standalone greedy call; properties that hold at any size."""
     w = workload(synth.HEADLINE)
     res = run_stochastic(w, dev)
     assert res["device_status"][0] == 0
-    seqs = sample_seqs(w.B, 12, seed=2)
-    compare_stochastic(w, res, seqs)
-    # greedy: every sequence
-    compare_greedy(w, run_greedy(w, dev), range(w.B))
-    # fused greedy outputs agree with the standalone call
+    n_cmp, flagged, mismatched = compare_stochastic(w, res, range(w.B), ref=_oracle("stochastic", w))
+    _report("headline stochastic", w, n_cmp, flagged, mismatched)
     g = run_greedy(w, dev)
+    compare_greedy(w, g, range(w.B), ref=_oracle("greedy", w))
     assert np.array_equal(g["n_accepted"], res["greedy_n"])
     assert np.array_equal(g["out_tokens"], res["greedy_tokens"])
-    # properties that hold at every size
     n = res["n_accepted"]
     assert np.all((n >= 0) & (n <= 8))
     out = res["out_tokens"].reshape(w.B, 9)
@@ -84,10 +106,12 @@ def test_headline_B256_g8_V128256_sampled(dev):
 NKL_FLOOR = 1e-6
 
 
-def test_headline_nkl_standalone_sampled(dev):
+def test_headline_nkl_standalone_all_pairs(dev):
+    """spec_nkl on all 2048 (target, draft) row pairs of the headline batch."""
     w = workload(synth.HEADLINE)
     res = run_nkl(w, dev)
-    compare_nkl(w, res, sample_seqs(w.B, 6, seed=5))
+    assert res["device_status"][0] == 0
+    compare_nkl(w, res, range(w.B), ref=_oracle("nkl", w))
 
 
 def test_tree_B32_N12_V128256_all_sequences(dev):
@@ -97,15 +121,66 @@ def test_tree_B32_N12_V128256_all_sequences(dev):
     compare_tree(w, res, range(w.B))
 
 
-def test_ragged_B512_V152064_sampled(dev):
-    w = synth.RAGGED.make()
+def test_ragged_B512_V152064_all_sequences(dev):
+    """Every sequence of the ragged batch (gamma_b ~ U{1..16}, packed): stochastic with its
+    fused NKL and greedy outputs, and the standalone greedy call."""
+    w = workload(synth.RAGGED)
     assert not w.dense
     res = run_stochastic(w, dev)
     assert res["device_status"][0] == 0
-    compare_stochastic(w, res, sample_seqs(w.B, 10, seed=4))
-    compare_greedy(w, run_greedy(w, dev), sample_seqs(w.B, 64, seed=6))
+    n_cmp, flagged, mismatched = compare_stochastic(w, res, range(w.B), ref=_oracle("stochastic", w))
+    _report("ragged stochastic", w, n_cmp, flagged, mismatched)
+    compare_greedy(w, run_greedy(w, dev), range(w.B), ref=_oracle("greedy", w))
     n = res["n_accepted"]
     assert np.all((n >= 0) & (n <= w.gammas))
+
+
+def _live_rows(R, V, live, dtype):
+    """R rows whose only live tokens (logit 0) are `live`; every other logit is -200, so
+    that exp((-200 - 0) / T) underflows in fp32 and the rows' softmax is exact on both
+    sides: 1/len(live) at the live tokens."""
+    z = np.full((R, V), -200.0, np.float32)
+    z[:, live] = 0.0
+    return synth.storage(z, dtype)
+
+
+@pytest.mark.parametrize("V,dtype", [(50000, synth.BF16), (50001, synth.BF16), (30000, synth.F32)])
+def test_zero_residual_draws_from_p(dev, V, dtype):
+    """Reading R6 on the GPU: a rejection whose residual max(0, p - q) is zero everywhere
+    (identical target and draft rows) takes the sampler's second pass, which draws from p
+    of the same row. Identical rows give alpha = 1, so a uniform above 1 forces the
+    rejection (accept iff u <= alpha); the live tokens make the draw exact on both sides.
+    V = 50001 (rows off the 16-byte grid) takes the staged sampler."""
+    live = [3, 1000, 20000, V - 17, V - 1]
+    B, g = 6, 3
+    rng = np.random.default_rng(V)
+    t = rng.normal(0, 2, (B * (g + 1), V)).astype(np.float32)
+    d = rng.normal(0, 2, (B * g, V)).astype(np.float32)
+    t_st, d_st = synth.storage(t, dtype), synth.storage(d, dtype)
+    u_acc = np.zeros(B * g, np.float32)                      # u = 0 accepts every other position
+    rej = [b % g for b in range(B)]                          # the rejected position of sequence b
+    same = _live_rows(1, V, live, dtype)[0]
+    tokens = rng.integers(0, V, B * g).astype(np.int32)
+    for b in range(B):
+        i = rej[b]
+        t_st[b * (g + 1) + i] = same
+        d_st[b * g + i] = same
+        u_acc[b * g + i] = 1.5
+    u_smp = np.array([0.1, 0.3, 0.5, 0.7, 0.9, 0.55], np.float32)
+    w = synth.StochasticWorkload(B=B, V=V, dtype=dtype, T=1.0, gammas=np.full(B, g, np.int32),
+                                 cu_draft=np.arange(B + 1, dtype=np.int32) * g, target=t_st, draft=d_st,
+                                 tokens=tokens, u_accept=u_acc, u_sample=u_smp, name=f"zero residual V={V}")
+    res = run_stochastic(w, dev)
+    assert res["device_status"][0] == 0
+    ref = O.verify_stochastic(w.target, w.draft, w.tokens, w.cu_draft, w.T, w.u_accept, w.u_sample, w.dtype)
+    for b in range(B):
+        r = ref[b]
+        assert ("zero_residual", rej[b]) in r["flags"]
+        want_y = live[int(u_smp[b] * len(live))]
+        assert r["tokens"][rej[b]] == want_y                   # the oracle draws from p of that row
+        assert int(res["n_accepted"][b]) == r["n"] == rej[b]
+        t0 = b * (g + 1)
+        assert list(res["out_tokens"][t0:t0 + g + 1]) == list(r["tokens"]), b
 
 
 # ---------------------------------------------------------------- edge cases
@@ -232,14 +307,14 @@ def test_off_grid_nkl_positions(dev):
 
 def test_off_grid_headline_shape(dev):
     """The headline batch (B=256, gamma=8, V=128256, bf16) with the logits one element off
-    the 16-byte grid (phased tiles and sampler): every sampler range and tier, sampled
-    against the oracle."""
+    the 16-byte grid (phased tiles and sampler): every sequence against the oracle."""
     w = workload(synth.HEADLINE)
     res = run_stochastic(w, dev, offset=1)
     assert res["device_status"][0] == 0
-    compare_stochastic(w, res, sample_seqs(w.B, 8, seed=12))
+    n_cmp, flagged, mismatched = compare_stochastic(w, res, range(w.B), ref=_oracle("stochastic", w))
+    _report("headline stochastic, logits one element off the 16-byte grid", w, n_cmp, flagged, mismatched)
     g = run_greedy(w, dev, offset=1)
-    compare_greedy(w, g, range(w.B))
+    compare_greedy(w, g, range(w.B), ref=_oracle("greedy", w))
     assert np.array_equal(g["n_accepted"], res["greedy_n"])
     aligned = run_stochastic(w, dev)
     # the two paths sum in different orders: decisions agree except at a boundary tie
@@ -250,12 +325,13 @@ def test_off_grid_headline_shape(dev):
 def test_off_grid_odd_vocabulary(dev):
     """A vocabulary whose bf16 rows are not a multiple of 16 bytes (V = 50257): every row
     has its own phase, target and draft rows of one position differ in phase."""
-    w = synth.make_stochastic(64, 50257, synth.BF16, 0.8, seed=27, gamma=5)
+    w = synth.make_stochastic(64, 50257, synth.BF16, 0.8, seed=27, gamma=5, name="odd_vocab_B64_g5_V50257")
     res = run_stochastic(w, dev)
     assert res["device_status"][0] == 0
-    compare_stochastic(w, res, sample_seqs(w.B, 16, seed=13))
-    compare_greedy(w, run_greedy(w, dev), range(w.B))
-    compare_nkl(w, run_nkl(w, dev), sample_seqs(w.B, 8, seed=14))
+    n_cmp, flagged, mismatched = compare_stochastic(w, res, range(w.B), ref=_oracle("stochastic", w))
+    _report("V=50257 stochastic (staged pairs)", w, n_cmp, flagged, mismatched)
+    compare_greedy(w, run_greedy(w, dev), range(w.B), ref=_oracle("greedy", w))
+    compare_nkl(w, run_nkl(w, dev), range(w.B), ref=_oracle("nkl", w))
 
 
 def test_gamma_zero_and_one(dev):
