@@ -119,7 +119,8 @@ size_t spec_tree_workspace_bytes(int32_t B, int32_t N, int32_t V);
  *
  *   target_logits [total_draft + B, V], draft_logits [total_draft, V], draft_tokens
  *   [total_draft] int32, u_accept [total_draft] fp32 in [0,1), u_sample [B] fp32 in [0,1),
- *   temperature: finite, > 0, applied to both rows.
+ *   temperature: finite, > 0, applied to both rows. Uniforms are used as given: a u_accept
+ *   above 1 rejects its draft whatever alpha is.
  * Outputs (caller-allocated):
  *   n_accepted [B]                     required: n per sequence (-1 on a data error)
  *   out_tokens [total_draft + B]       required: per sequence x_0..x_{n-1}, then the
@@ -293,8 +294,10 @@ spec_status spec_accept_summary(const spec_accept_stats* stats, int64_t bucket_n
  *   consensus, divergence [G*gamma]    optional: some pair a != b below consensus_nkl in
  *                                      both directions; every entry off the diagonal
  *                                      above divergence_nkl
- * 2 <= K <= SPEC_MAX_CANDIDATES. The draft rows are read twice (once by the verification,
- * once for the matrix).
+ * 2 <= K <= SPEC_MAX_CANDIDATES. Rows on the 16-byte grid (V * element size a multiple of 16,
+ * 16-byte aligned bases) are read once: one pass verifies the K candidates of a position and
+ * fills their matrix. Rows off the grid are verified by the batch kernels and the draft rows
+ * are then read a second time for the matrix.
  */
 #define SPEC_MAX_CANDIDATES 4
 
@@ -329,7 +332,9 @@ spec_status spec_verify_multi(spec_multi_batch m, spec_dtype dtype, int32_t stoc
  *     exceeds it returns SPEC_ERR_TOO_LARGE before anything runs.
  *   - The first call on each device (with that device current) looks up the array's
  *     device address with cudaGetSymbolAddress and caches it; make that first call
- *     before any stream capture.
+ *     before any stream capture. The cached address belongs to the device's primary
+ *     context: after cudaDeviceReset on that device the address is stale, so do not call
+ *     this entry point again in a process that has reset the device.
  *   - Every call on a device shares the one array. Calls on the same stream are ordered
  *     and safe; calls that overlap on the GPU (other streams, other host threads) race
  *     on it and give undefined results. Each call re-initialises what it needs, so no
