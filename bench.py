@@ -55,11 +55,13 @@ PROFILE = os.path.join(ROOT, "profiles", "stochastic_call_B256_g8_V128256.md")
 
 
 def kernel_sources_sha256() -> str:
-    """Hash of the CUDA sources and the C header (the same recipe as the profile summary)."""
+    """Hash of the CUDA sources, the host planning header and the C header (the same recipe
+    as the profile summary)."""
     import glob
     import hashlib
     csrc = os.path.join(ROOT, "speculative_decoding_token_temp_gb300", "csrc")
-    files = sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh")))
+    files = sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh")) +
+                   glob.glob(os.path.join(csrc, "*.h")))
     files.append(os.path.join(ROOT, "include", "spec_verify.h"))
     h = hashlib.sha256()
     for f in files:

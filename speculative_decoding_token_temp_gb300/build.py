@@ -14,7 +14,7 @@ INCLUDE = os.path.join(ROOT, "include")
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libspecverify.so")
 SOURCES = ["spec_verify.cu"]
-HEADERS = ["kernels.cuh", "kernels_rows.cuh", "kernels_sample.cuh", "kernels_multi.cuh"]
+HEADERS = ["kernels.cuh", "kernels_rows.cuh", "kernels_sample.cuh", "kernels_multi.cuh", "plan.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

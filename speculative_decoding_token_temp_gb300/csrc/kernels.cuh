@@ -42,7 +42,6 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kMaxRows = SPEC_MAX_GAMMA + 1;
-constexpr int kTargetTiles = 608;    // one wave of the resident blocks (152 SMs x 4): chunk splits stop before the grid exceeds it
 
 // M_STOCH2: stochastic with a draft temperature of its own (the draft row is summed at
 // both temperatures)
@@ -76,6 +75,7 @@ struct RowsParams {
   const float* u_accept;
   const float* u_sample;
   const int32_t* cu;
+  const int32_t* row_seq;  // packed batches: the sequence of every row, written by the prologue
   const int32_t* node_tokens;
   int B, V, gamma, total_draft, total_rows, nchunks, chunk_elems, N;
   float c, invT, delta, inv_lnV;
@@ -129,6 +129,9 @@ struct SampleParams {
 struct ProParams {
   const int32_t* cu;
   int B, gamma, total_draft;
+  int32_t* row_seq;  // packed batches: [total_rows] the sequence of every row (written here), or null
+  int hb;            // target rows per sequence beyond its drafts (1; the NKL call's pairs: 0)
+  int total_rows;
   unsigned* cntA;  // B tickets, then the finished-tile count
   unsigned* cntB;
   SeqRec* rec;

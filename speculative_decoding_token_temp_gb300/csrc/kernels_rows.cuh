@@ -39,9 +39,16 @@ __global__ void prologue_kernel(const __grid_constant__ ProParams p) {
   p.rec[b] = q;
   if (p.cu != nullptr) {
     const int c0 = __ldg(p.cu + b), c1 = __ldg(p.cu + b + 1);
-    const bool bad = c1 < c0 || c1 - c0 > p.gamma || c0 < 0 || c1 > p.total_draft || (b == 0 && c0 != 0) ||
-                     (b == p.B - 1 && c1 != p.total_draft);
+    const bool own = c1 >= c0 && c1 - c0 <= p.gamma && c0 >= 0 && c1 <= p.total_draft;  // its rows are in range
+    const bool bad = !own || (b == 0 && c0 != 0) || (b == p.B - 1 && c1 != p.total_draft);
     if (bad) atomicOr(p.status, SPEC_DEV_OFFSETS);
+    // the row -> sequence table the tiles look themselves up in: rows [c0 + hb b, c1 + hb (b+1))
+    // (with offsets out of order a row may keep an older entry: the tile's own checks of
+    // the offsets then report it)
+    if (own && p.row_seq != nullptr) {
+      const int r1 = min(c1 + p.hb * (b + 1), p.total_rows);
+      for (int r = c0 + p.hb * b; r < r1; ++r) p.row_seq[r] = b;
+    }
   }
 }
 
@@ -582,7 +589,6 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
   // trigger, so after the prologue has re-armed the records.
   griddep_wait();
   griddep_launch();
-  __shared__ int s_b;
   __shared__ int s_last;
   const int tile = blockIdx.x;
   const int r = tile / p.nchunks;
@@ -595,17 +601,10 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
     gb = p.gamma;
     c0 = b * p.gamma;
   } else {
-    // locate the sequence owning row r: one coalesced pass over the offsets
-    if (threadIdx.x == 0) s_b = INT_MAX;
-    __syncthreads();
-    for (int k = threadIdx.x; k < p.B; k += kThreads) {
-      const int lo = __ldg(p.cu + k) + HB * k;
-      const int hi = __ldg(p.cu + k + 1) + HB * (k + 1);
-      if (lo <= r && r < hi) atomicMin(&s_b, k);
-    }
-    __syncthreads();
-    b = s_b;
-    if (b == INT_MAX) {
+    // the sequence owning row r, from the prologue's table (written before this grid's
+    // griddepcontrol.wait returned); checked against the offsets below
+    b = __ldcg(p.row_seq + r);
+    if (b < 0 || b >= p.B) {
       if (threadIdx.x == 0) {
         atomicOr(p.status, SPEC_DEV_OFFSETS);
         tile_done<MODE>(p);

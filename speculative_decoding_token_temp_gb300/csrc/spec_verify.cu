@@ -9,10 +9,12 @@
 #include "kernels_rows.cuh"
 #include "kernels_multi.cuh"
 #include "kernels_sample.cuh"
+#include "plan.h"
 #include "spec_verify.h"
 
 #include <atomic>
 #include <initializer_list>
+#include <mutex>
 
 namespace sv {
 namespace {
@@ -20,23 +22,26 @@ namespace {
 inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Vocabulary chunking of the tile kernel: chunks of at most max_chunk tokens, split
-// further (down to 8192) only while the grid still fits in one wave of resident blocks: a
-// partial second wave of tiles ends after the first (B=64, gamma=5, V=32000: 384 whole-row
-// tiles 24.0 us against 25.5 for 768 half rows; B=8, gamma=5, V=128256: 576 tiles 19.6
-// against 20.4 for 624; same box). Chunk sizes are multiples of 8 so every chunk starts on
-// a 16-byte vector boundary.
-void chunking(int V, long long rows, int max_chunk, int* nchunks, int* chunk_elems, int slots = kTargetTiles) {
-  long long nc = ceil_div(V, max_chunk);
-  while (rows * (nc + 1) <= slots && V / (nc + 1) >= 8192) ++nc;
-  long long ce = ceil_div(ceil_div(V, nc), 8) * 8;
-  *chunk_elems = (int)ce;
-  *nchunks = (int)ceil_div(V, ce);
-}
+// One wave of resident blocks of each kernel family on a device: the SM count times the
+// blocks of that kernel one SM holds (cudaOccupancyMaxActiveBlocksPerMultiprocessor at its
+// block size and shared memory), looked up once per device. bound() is the largest wave
+// the workspace layout allows for (plan::kMaxWaveSlots), used where no device is involved
+// (workspace sizes).
+struct Geometry {
+  long long tile_slots;      // rows_kernel tiles (one wave)
+  long long fused_slots;     // multi_rows_kernel tiles
+  long long sampler_blocks;  // sample2_kernel blocks
+  static Geometry bound() {
+    Geometry g;
+    g.tile_slots = g.fused_slots = g.sampler_blocks = plan::kMaxWaveSlots;
+    return g;
+  }
+};
 
 struct Layout {
-  size_t cntA, cntB, rec, part, table, total;
+  size_t cntA, cntB, rec, part, table, seqmap, total;
   int nchunks, chunk_elems, table_stride;
+  int cap_nchunks;  // chunks per row the partials are sized for (the largest wave's chunking)
   long long rows;
 };
 
@@ -49,19 +54,25 @@ int table_stride_for(int V, spec_dtype dt) {
   return (int)(ceil_div(nv, 2 * kThreads) * kSlicesPerStage);
 }
 
-// fused_k > 0: fused multi-draft tiles, each holding the rows of fused_k candidates, two
-// blocks per SM.
+// fused_k > 0: fused multi-draft tiles, each holding the rows of fused_k candidates.
 // max_chunk: the longest vocabulary chunk of a tile. 0 = the measured best: 65536 tokens
 // for single-row tiles and for the stochastic call's pairs (256 KB pair tiles: fewer
 // tile epilogues; 185.6 against 191.7 us at the headline, same box), 49152 for the NKL
 // call's pairs (150.3 us, against 152.0 with 32768 and 155.4 with 65536).
+// geo: the device's waves; the chunking follows them, while the offsets (and the total)
+// are those of the largest wave allowed, so the workspace size does not depend on the
+// device.
 Layout layout(int B, int V, long long rows, bool sample, bool single_rows = false, spec_dtype dt = SPEC_F32,
-              int max_chunk = 0, int fused_k = 0) {
+              int max_chunk = 0, int fused_k = 0, const Geometry& geo = Geometry::bound()) {
   Layout L;
   L.rows = rows;
   const long long trows = fused_k > 0 ? rows / fused_k : rows;  // tiles per chunk
-  chunking(V, trows > 0 ? trows : 1, max_chunk > 0 ? max_chunk : ((single_rows || sample) ? 65536 : 49152),
-           &L.nchunks, &L.chunk_elems, fused_k > 0 ? kTargetTiles / 2 : kTargetTiles);
+  const int mc = max_chunk > 0 ? max_chunk : ((single_rows || sample) ? 65536 : 49152);
+  const plan::Chunking run = plan::chunking(V, trows, mc, fused_k > 0 ? geo.fused_slots : geo.tile_slots);
+  const plan::Chunking cap = plan::chunking(V, trows, mc, plan::kMaxWaveSlots);
+  L.nchunks = run.nchunks;
+  L.chunk_elems = run.chunk_elems;
+  L.cap_nchunks = cap.nchunks;
   size_t off = 0;
   L.cntA = off;  // B tickets, then the count of finished tiles
   off = align256(off + sizeof(unsigned) * ((size_t)B + 1));
@@ -70,10 +81,12 @@ Layout layout(int B, int V, long long rows, bool sample, bool single_rows = fals
   L.rec = off;
   off = align256(off + sizeof(SeqRec) * (size_t)B);
   L.part = off;
-  off = align256(off + sizeof(Partial) * (size_t)(rows * L.nchunks));
+  off = align256(off + sizeof(Partial) * (size_t)(rows * cap.nchunks));
   L.table_stride = sample ? table_stride_for(V, dt) : 0;
   L.table = off;
   off = align256(off + sizeof(float) * (size_t)B * (size_t)L.table_stride);
+  L.seqmap = off;  // packed batches: the sequence of every row
+  off = align256(off + sizeof(int32_t) * (size_t)rows);
   L.total = off;
   return L;
 }
@@ -84,6 +97,11 @@ long long rows_for(spec_mode mode, const spec_batch& g) {
 }
 
 bool aligned16(const void* p) { return p == nullptr || ((uintptr_t)p & 15u) == 0; }
+
+// A workspace pointer that is set, 256-byte aligned and of at least `need` bytes.
+bool workspace_ok(const void* ws, size_t bytes, size_t need) {
+  return ws != nullptr && bytes >= need && ((uintptr_t)ws & 255u) == 0;
+}
 
 // every non-null pointer of the list on an n-byte boundary (its element size)
 bool aligned_to(size_t n, std::initializer_list<const void*> ps) {
@@ -141,8 +159,10 @@ struct ZeroRegion {
   int n = 0;
 };
 
+// hb: target rows per sequence beyond its drafts (1: the bonus row; 0 for the NKL call,
+// whose rows are the draft pairs).
 cudaError_t launch_prologue(const spec_batch& g, const Layout& L, char* ws, uint32_t* status, cudaStream_t stream,
-                            const spec_options* opt = nullptr, ZeroRegion z = ZeroRegion()) {
+                            const spec_options* opt = nullptr, ZeroRegion z = ZeroRegion(), int hb = 1) {
   ProParams pp;
   pp.cu = g.cu_draft;
   pp.B = g.B;
@@ -156,6 +176,9 @@ cudaError_t launch_prologue(const spec_batch& g, const Layout& L, char* ws, uint
   pp.bucket = opt ? (long long)opt->stats_bucket : 0;
   pp.zero2 = z.ptr;
   pp.nzero2 = z.n;
+  pp.row_seq = g.cu_draft != nullptr ? reinterpret_cast<int32_t*>(ws + L.seqmap) : nullptr;
+  pp.total_rows = (int)L.rows;
+  pp.hb = hb;
   const int threads = g.B > z.n ? g.B : z.n;
   return launch(prologue_kernel, dim3((unsigned)ceil_div(threads, kThreads)), dim3(kThreads), stream, pp, true);
 }
@@ -163,7 +186,6 @@ cudaError_t launch_prologue(const spec_batch& g, const Layout& L, char* ws, uint
 // The vector path of rows_kernel stages its loads in kRowsSmem bytes of dynamic shared
 // memory, above the default 48 KB limit: the limit is raised once per (kernel, device).
 constexpr int kAttrDevices = 64;
-constexpr int kWaveBlocks = 152 * 4;  // resident 256-thread blocks with 48 KB staging on a GB300
 constexpr int kTailSeqs = 16;   // sequences the sampler splits finely (the last decided)
 constexpr int kTailStages = 1;  // their shortest range, in 512-vector stages (small batches split the last sequences finely)
 
@@ -300,10 +322,55 @@ cudaError_t launch_multi(bool bf16, const MultiTiles& mt, const RowsParams& rp, 
   return launch_multi_t<float, 4, 4, MODE>(rp, mt.pp, tiles, stream);
 }
 
+// Resident blocks of one kernel per SM at kThreads threads and `smem` bytes of dynamic
+// shared memory (the attribute that allows more than 48 KB is set first).
+template <typename K>
+cudaError_t blocks_per_sm(K kernel, int smem, int* out) {
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, kernel, kThreads, (size_t)smem);
+}
+
+// The current device's waves, looked up once per device: the SM count times the resident
+// blocks per SM of the tile kernel, of the fused multi-draft kernel (the fewest over K) and
+// of the sampler. Every instance of a family shares its launch bounds and staging size.
+cudaError_t device_geometry(Geometry* out) {
+  static std::mutex mu;
+  static Geometry cache[kAttrDevices];
+  static std::atomic<unsigned long long> have{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kAttrDevices) return cudaErrorInvalidDevice;
+  const unsigned long long bit = 1ull << dev;
+  if (!(have.load(std::memory_order_acquire) & bit)) {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!(have.load(std::memory_order_acquire) & bit)) {
+      int sms = 0, ot = 0, os = 0, o2 = 0, o3 = 0, o4 = 0;
+      if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+      if ((e = blocks_per_sm(rows_kernel<uint16_t, 8, M_STOCH, false>, kRowsSmem, &ot)) != cudaSuccess) return e;
+      if ((e = blocks_per_sm(sample2_kernel<uint16_t, 8, false, false>, kRowsSmem, &os)) != cudaSuccess) return e;
+      if ((e = blocks_per_sm(multi_rows_kernel<uint16_t, 8, 2, M_STOCH>, multi_smem<2>(), &o2)) != cudaSuccess) return e;
+      if ((e = blocks_per_sm(multi_rows_kernel<uint16_t, 8, 3, M_STOCH>, multi_smem<3>(), &o3)) != cudaSuccess) return e;
+      if ((e = blocks_per_sm(multi_rows_kernel<uint16_t, 8, 4, M_STOCH>, multi_smem<4>(), &o4)) != cudaSuccess) return e;
+      const int om = o2 < o3 ? (o2 < o4 ? o2 : o4) : (o3 < o4 ? o3 : o4);
+      Geometry g;
+      g.tile_slots = (long long)sms * (ot > 0 ? ot : 1);
+      g.fused_slots = (long long)sms * (om > 0 ? om : 1);
+      g.sampler_blocks = (long long)sms * (os > 0 ? os : 1);
+      cache[dev] = g;
+      have.fetch_or(bit, std::memory_order_acq_rel);
+    }
+  }
+  *out = cache[dev];
+  return cudaSuccess;
+}
+
 RowsParams base_params(const spec_batch& g, const Layout& L, char* ws, uint32_t* status) {
   RowsParams rp;
   memset(&rp, 0, sizeof(rp));
   rp.cu = g.cu_draft;
+  rp.row_seq = g.cu_draft != nullptr ? reinterpret_cast<const int32_t*>(ws + L.seqmap) : nullptr;
   rp.B = g.B;
   rp.V = g.V;
   rp.gamma = g.gamma;
@@ -393,9 +460,16 @@ spec_status stochastic_impl(spec_batch g, spec_dtype dtype, const void* target_l
       !aligned_to(4, {draft_tokens, u_accept, u_sample, n_accepted, out_tokens, p_x, q_x, alpha, nkl, greedy_n,
                       greedy_tokens, device_status, g.cu_draft}))
     return SPEC_ERR_INVALID_ARG;
+  // the workspace is checked first (its size does not depend on the device), then the
+  // device's waves plan the chunks
+  if (!workspace_ok(workspace, workspace_bytes,
+                    layout(g.B, g.V, rows_for(SPEC_MODE_STOCHASTIC, g), true, false, dtype, mt ? kMultiChunk : 0,
+                           mt ? mt->K : 0).total))
+    return SPEC_ERR_WORKSPACE;
+  Geometry geo;
+  if (device_geometry(&geo) != cudaSuccess) return SPEC_ERR_CUDA;
   const Layout L = layout(g.B, g.V, rows_for(SPEC_MODE_STOCHASTIC, g), true, false, dtype, mt ? kMultiChunk : 0,
-                          mt ? mt->K : 0);
-  if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u)) return SPEC_ERR_WORKSPACE;
+                          mt ? mt->K : 0, geo);
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   char* ws = static_cast<char*>(workspace);
   const bool bf16 = dtype == SPEC_BF16;
@@ -459,22 +533,12 @@ spec_status stochastic_impl(spec_batch g, spec_dtype dtype, const void* target_l
   // quarter of the wave, the others equal long ranges.
   const long long nv = ceil_div((long long)g.V + sp.ph, bf16 ? 8 : 4);  // the rows' aligned blocks
   const long long nst = ceil_div(nv, 2 * kThreads);
-  const long long tail_seqs = g.B < kTailSeqs ? g.B : kTailSeqs;
-  const long long tail_total = tail_seqs * nst, head_total = ((long long)g.B - tail_seqs) * nst;
-  long long seg_tail = ceil_div(tail_total, kWaveBlocks / 4);
-  if (seg_tail < kTailStages) seg_tail = kTailStages;
-  const long long nb_tail = ceil_div(tail_total, seg_tail);
-  long long nb_head = 0, seg_head = 1;
-  if (head_total > 0) {
-    const long long room = kWaveBlocks - nb_tail;
-    seg_head = ceil_div(head_total, room < 1 ? 1 : room);
-    nb_head = ceil_div(head_total, seg_head);
-  }
-  sp.head_total = head_total;
-  sp.nb_head = (int)nb_head;
-  sp.seg_head = (int)seg_head;
-  sp.seg_tail = (int)seg_tail;
-  if (launch_sample2(bf16, sampler_vec, sp, nb_head + nb_tail, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  const plan::SamplerPlan sg = plan::sampler_plan(g.B, nst, geo.sampler_blocks, kTailSeqs, kTailStages);
+  sp.head_total = sg.head_total;
+  sp.nb_head = (int)sg.nb_head;
+  sp.seg_head = (int)sg.seg_head;
+  sp.seg_tail = (int)sg.seg_tail;
+  if (launch_sample2(bf16, sampler_vec, sp, sg.nb_head + sg.nb_tail, stream) != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;
 }
 
@@ -493,9 +557,14 @@ spec_status greedy_impl(spec_batch g, spec_dtype dtype, const void* target_logit
   if (!aligned_to(elem_bytes(dtype), {target_logits}) ||
       !aligned_to(4, {draft_tokens, n_accepted, out_tokens, device_status, g.cu_draft}))
     return SPEC_ERR_INVALID_ARG;
+  if (!workspace_ok(workspace, workspace_bytes,
+                    layout(g.B, g.V, rows_for(SPEC_MODE_GREEDY, g), false, true, SPEC_F32, mt ? kMultiChunk : 0,
+                           mt ? mt->K : 0).total))
+    return SPEC_ERR_WORKSPACE;
+  Geometry geo;
+  if (device_geometry(&geo) != cudaSuccess) return SPEC_ERR_CUDA;
   const Layout L = layout(g.B, g.V, rows_for(SPEC_MODE_GREEDY, g), false, true, SPEC_F32, mt ? kMultiChunk : 0,
-                          mt ? mt->K : 0);
-  if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u)) return SPEC_ERR_WORKSPACE;
+                          mt ? mt->K : 0, geo);
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   char* ws = static_cast<char*>(workspace);
   if (launch_prologue(g, L, ws, device_status, stream, options, zr) != cudaSuccess) return SPEC_ERR_CUDA;
@@ -546,19 +615,26 @@ spec_status check_multi(const spec_multi_batch& m) {
   return check_batch(multi_as_batch(m));
 }
 
-MultiLayout multi_layout(const spec_multi_batch& m, spec_dtype dt, bool stochastic) {
+// geo: the device's waves (the chunkings follow them; sizes and offsets are those of the
+// largest wave allowed, as in layout()).
+MultiLayout multi_layout(const spec_multi_batch& m, spec_dtype dt, bool stochastic,
+                         const Geometry& geo = Geometry::bound()) {
   const spec_batch g = multi_as_batch(m);
   const spec_mode mode = stochastic ? SPEC_MODE_STOCHASTIC : SPEC_MODE_GREEDY;
   MultiLayout M;
-  const Layout Lv = layout(g.B, g.V, rows_for(mode, g), stochastic, !stochastic, dt, kMultiChunk, m.K);
+  const Layout Lv = layout(g.B, g.V, rows_for(mode, g), stochastic, !stochastic, dt, kMultiChunk, m.K, geo);
   const Layout Lp = layout(g.B, g.V, rows_for(mode, g), stochastic, !stochastic, dt);  // two-pass: plain tiles
   M.verify = align256(Lv.total > Lp.total ? Lv.total : Lp.total);
   M.vchunks = Lv.nchunks;
   M.vchunk_elems = Lv.chunk_elems;
   const long long rows = (long long)m.G * m.gamma;
   // a two-pass tile reads K rows of one chunk: about 64 K elements in all
-  chunking(m.V, rows > 0 ? rows : 1, 65536 / (m.K > 0 ? m.K : 1), &M.nchunks, &M.chunk_elems);
-  const int pchunks = M.nchunks > M.vchunks ? M.nchunks : M.vchunks;
+  const int pmax = 65536 / (m.K > 0 ? m.K : 1);
+  const plan::Chunking run = plan::chunking(m.V, rows, pmax, geo.tile_slots);
+  const plan::Chunking cap = plan::chunking(m.V, rows, pmax, plan::kMaxWaveSlots);
+  M.nchunks = run.nchunks;
+  M.chunk_elems = run.chunk_elems;
+  const int pchunks = cap.nchunks > Lv.cap_nchunks ? cap.nchunks : Lv.cap_nchunks;
   M.tickets = M.verify;
   M.part = align256(M.tickets + sizeof(unsigned) * (size_t)rows);
   M.total = align256(M.part + sizeof(PairPartial) * (size_t)rows * pchunks);
@@ -699,8 +775,11 @@ spec_status spec_verify_tree(int32_t B, int32_t N, int32_t V, spec_dtype dtype, 
   g.V = V;
   g.total_draft = B * N;
   g.cu_draft = nullptr;
-  const Layout L = layout(B, V, (long long)B * (N + 1), false, true);
-  if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u)) return SPEC_ERR_WORKSPACE;
+  if (!workspace_ok(workspace, workspace_bytes, layout(B, V, (long long)B * (N + 1), false, true).total))
+    return SPEC_ERR_WORKSPACE;
+  Geometry geo;
+  if (device_geometry(&geo) != cudaSuccess) return SPEC_ERR_CUDA;
+  const Layout L = layout(B, V, (long long)B * (N + 1), false, true, SPEC_F32, 0, 0, geo);
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   char* ws = static_cast<char*>(workspace);
   if (launch_prologue(g, L, ws, device_status, stream) != cudaSuccess) return SPEC_ERR_CUDA;
@@ -740,11 +819,14 @@ spec_status spec_nkl_ex(spec_batch g, spec_dtype dtype, const void* target_logit
   if (!target_logits || !draft_logits || !nkl || !device_status) return SPEC_ERR_INVALID_ARG;
   if (!aligned_to(elem_bytes(dtype), {target_logits, draft_logits}) || !aligned_to(4, {nkl, device_status, g.cu_draft}))
     return SPEC_ERR_INVALID_ARG;
-  const Layout L = layout(g.B, g.V, rows_for(SPEC_MODE_NKL, g), false);
-  if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u)) return SPEC_ERR_WORKSPACE;
+  if (!workspace_ok(workspace, workspace_bytes, layout(g.B, g.V, rows_for(SPEC_MODE_NKL, g), false).total))
+    return SPEC_ERR_WORKSPACE;
+  Geometry geo;
+  if (device_geometry(&geo) != cudaSuccess) return SPEC_ERR_CUDA;
+  const Layout L = layout(g.B, g.V, rows_for(SPEC_MODE_NKL, g), false, false, SPEC_F32, 0, 0, geo);
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   char* ws = static_cast<char*>(workspace);
-  if (launch_prologue(g, L, ws, device_status, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (launch_prologue(g, L, ws, device_status, stream, nullptr, ZeroRegion(), 0) != cudaSuccess) return SPEC_ERR_CUDA;
   RowsParams rp = base_params(g, L, ws, device_status);
   rp.target = target_logits;
   rp.draft = draft_logits;
@@ -786,8 +868,11 @@ spec_status spec_verify_multi(spec_multi_batch m, spec_dtype dtype, int32_t stoc
       !aligned_to(4, {draft_tokens, u_accept, u_sample, n_accepted, out_tokens, best_k, best_n, best_tokens, pair_nkl,
                       device_status}))
     return SPEC_ERR_INVALID_ARG;
-  const MultiLayout ML = multi_layout(m, dtype, stochastic != 0);
-  if (!workspace || workspace_bytes < ML.total || ((uintptr_t)workspace & 255u)) return SPEC_ERR_WORKSPACE;
+  if (!workspace_ok(workspace, workspace_bytes, multi_layout(m, dtype, stochastic != 0).total))
+    return SPEC_ERR_WORKSPACE;
+  Geometry geo;
+  if (device_geometry(&geo) != cudaSuccess) return SPEC_ERR_CUDA;
+  const MultiLayout ML = multi_layout(m, dtype, stochastic != 0, geo);
   char* ws = static_cast<char*>(workspace);
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   const spec_batch g = multi_as_batch(m);
