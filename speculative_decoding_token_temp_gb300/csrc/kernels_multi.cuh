@@ -405,6 +405,81 @@ __host__ __device__ constexpr int multi_smem() {
   return multi_stages<K>() * 2 * K * kThreads * 16;
 }
 
+// One stage of a fused tile on a draft position (K <= 3), thread-local: the K draft vectors
+// unpacked and their lazy references checked with one vote; every draft exponential
+// computed before the pairwise sums, so that one difference z_a - z_b feeds both K_ab and
+// K_ba (each pair sum chained from its accumulator and folded once per vector); then per
+// candidate its target vector -- stochastic: the maximum (no index: nothing reads the
+// argmax of a stochastic multi-draft row) and the sum, and the verification's KL sum
+// against the candidate's own target row; greedy: the argmax.
+template <typename E, int VEC, int K, bool STOCH>
+__device__ __forceinline__ void multi_pair_stage(const uint4* sq, int e0, float c, float cq, TAcc (&ta)[K],
+                                                 DAcc (&da)[K], float (&kk)[K][K]) {
+  using io = IO<E, VEC>;
+  static_assert(VEC % 2 == 0, "packed pairs of elements");
+  float fd[K][VEC], vm[K];
+  bool mv = false;
+#pragma unroll
+  for (int a = 0; a < K; ++a) {
+    io::unpack(sq[(K + a) * kThreads], fd[a]);
+    vm[a] = vmax<VEC>(fd[a]);
+    mv = mv || vm[a] > da[a].mth;
+  }
+  if (__any_sync(__activemask(), mv)) {
+#pragma unroll
+    for (int a = 0; a < K; ++a) {
+      if (vm[a] > da[a].mth) {
+        const float f = ex2((da[a].mr - vm[a]) * cq);
+        da[a].s = make_float2(da[a].s.x * f, da[a].s.y * f);
+        da[a].k = make_float2(da[a].k.x * f, da[a].k.y * f);
+#pragma unroll
+        for (int b = 0; b < K; ++b) kk[a][b] *= f;
+        da[a].mr = vm[a];
+        da[a].mth = vm[a] + kLazy / cq;
+        da[a].nmc = -vm[a] * cq;
+      }
+    }
+  }
+  float ed[K][VEC];
+#pragma unroll
+  for (int a = 0; a < K; ++a) da[a].s = add2(da[a].s, exp_sum2<VEC>(fd[a], cq, da[a].nmc, ed[a]));
+#pragma unroll
+  for (int a = 0; a < K; ++a) {
+#pragma unroll
+    for (int b = a + 1; b < K; ++b) {
+      // K_ab += sum e_a (z_a - z_b); K_ba += sum e_b (z_b - z_a), kept negated in the chain
+      float2 pab = make_float2(kk[a][b], 0.f), nba = make_float2(-kk[b][a], 0.f);
+#pragma unroll
+      for (int j = 0; j < VEC / 2; ++j) {
+        const float2 d = sub2(make_float2(fd[a][2 * j], fd[a][2 * j + 1]), make_float2(fd[b][2 * j], fd[b][2 * j + 1]));
+        pab = fma2(make_float2(ed[a][2 * j], ed[a][2 * j + 1]), d, pab);
+        nba = fma2(make_float2(ed[b][2 * j], ed[b][2 * j + 1]), d, nba);
+      }
+      kk[a][b] = pab.x + pab.y;
+      kk[b][a] = -(nba.x + nba.y);
+    }
+  }
+#pragma unroll
+  for (int a = 0; a < K; ++a) {
+    float ft[VEC];
+    io::unpack(sq[a * kThreads], ft);
+    if constexpr (STOCH) {
+      const float tm = vmax<VEC>(ft);
+      ta[a].m = fmaxf(ta[a].m, tm);
+      lazy_ref(ta[a].mr, ta[a].mth, ta[a].nmc, ta[a].s, nullptr, tm, c);
+      float et[VEC];
+      ta[a].s = add2(ta[a].s, exp_sum2<VEC>(ft, c, ta[a].nmc, et));
+#pragma unroll
+      for (int j = 0; j < VEC / 2; ++j)
+        da[a].k = fma2(make_float2(ed[a][2 * j], ed[a][2 * j + 1]),
+                       sub2(make_float2(fd[a][2 * j], fd[a][2 * j + 1]), make_float2(ft[2 * j], ft[2 * j + 1])),
+                       da[a].k);
+    } else {
+      argmax_update<VEC>(ta[a], ft, e0);
+    }
+  }
+}
+
 template <typename E, int VEC, int K, int MODE>
 __global__ void __launch_bounds__(kThreads, 2) multi_rows_kernel(const __grid_constant__ RowsParams p,
                                                                  const __grid_constant__ PairParams q) {
@@ -474,8 +549,14 @@ __global__ void __launch_bounds__(kThreads, 2) multi_rows_kernel(const __grid_co
     if (v >= v1) continue;
     const uint4* sq = reinterpret_cast<const uint4*>(dsm + (size_t)(st % kMS) * SLOT) + t;
     const int e0 = v * VEC;
-    // K <= 3: every candidate's draft vector unpacked once, for its own sums and the K - 1
-    // pairs (at K = 4 the extra registers spill; its draft vectors are unpacked per use)
+    if constexpr (K <= 3) {
+      if (pair) {
+        multi_pair_stage<E, VEC, K, STOCH>(sq, e0, c, cq, ta, da, kk);
+        continue;
+      }
+    }
+    // K = 4 pairs (every candidate's draft vectors held at once would spill: they are
+    // unpacked per use) and the bonus row of every K
     constexpr bool PRE = K <= 3;
     float fdk[PRE ? K : 1][VEC];
     if (PRE && pair) {
