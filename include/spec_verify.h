@@ -79,6 +79,8 @@ typedef enum {
 #define SPEC_DEV_OFFSETS 4u     /* cu_draft not non-decreasing from 0 to total_draft, or a gamma_b > gamma */
 #define SPEC_DEV_TIMEOUT 8u     /* an internal wait gave up (bounded waits); the affected sequences are undecided */
 #define SPEC_DEV_POSITION 16u   /* spec_options.position[b] < 1 */
+#define SPEC_DEV_BOUNDS 32u     /* only in a library built with SPEC_BOUNDS_CHECK=1: a computed memory access fell
+                                   outside its buffer (that access was skipped); never set by the ordinary build */
 
 typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
 

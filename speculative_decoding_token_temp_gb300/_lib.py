@@ -8,7 +8,7 @@ import ctypes
 import os
 import re
 
-from .build import INCLUDE, LIB
+from .build import INCLUDE, LIB, LIB_BOUNDS
 
 SPEC_OK = 0
 SPEC_ERR_INVALID_ARG = 1
@@ -23,6 +23,7 @@ SPEC_DEV_NONFINITE = 2
 SPEC_DEV_OFFSETS = 4
 SPEC_DEV_TIMEOUT = 8
 SPEC_DEV_POSITION = 16
+SPEC_DEV_BOUNDS = 32  # only set by the bounds-checked build
 
 SPEC_F32 = 0
 SPEC_BF16 = 1
@@ -103,19 +104,30 @@ def declared_functions() -> list:
     return sorted(set(re.findall(r"\b(spec_[a-z_]+)\s*\(", text)))
 
 
+def load(path: str) -> ctypes.CDLL:
+    """The library at `path` with every declared function's signature set."""
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build the CUDA library first "
+                           "(python -c 'import __graft_entry__ as g; g.build()')")
+    handle = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(handle, name)
+        fn.restype = res
+        fn.argtypes = args
+    return handle
+
+
 def lib() -> ctypes.CDLL:
     global _LIB
     if _LIB is None:
-        if not os.path.exists(LIB):
-            raise RuntimeError(f"{LIB} is missing: build the CUDA library first "
-                               "(python -c 'import __graft_entry__ as g; g.build()')")
-        handle = ctypes.CDLL(LIB)
-        for name, (res, args) in SIGNATURES.items():
-            fn = getattr(handle, name)
-            fn.restype = res
-            fn.argtypes = args
-        _LIB = handle
+        _LIB = load(LIB)
     return _LIB
+
+
+def bounds_lib() -> ctypes.CDLL:
+    """The bounds-checked debug variant (SPEC_BOUNDS_CHECK=1), for tests: every computed
+    access is checked against its buffer and one outside it sets SPEC_DEV_BOUNDS."""
+    return load(LIB_BOUNDS)
 
 
 def status_str(code: int) -> str:

@@ -36,7 +36,50 @@
 
 #include "spec_verify.h"
 
+#ifndef SPEC_BOUNDS_CHECK
+#define SPEC_BOUNDS_CHECK 0
+#endif
+
 namespace sv {
+
+// ---------------------------------------------------------------------------
+// Bounds-checked build (SPEC_BOUNDS_CHECK=1, a debug variant of the library): every
+// computed global access is first checked against its buffer -- a byte range widened to
+// the 16-byte blocks that hold its first and last byte, since the vector paths read whole
+// aligned blocks -- or its index against its array's length; a failed check ORs
+// SPEC_DEV_BOUNDS into the status word and the access is skipped. In the ordinary build
+// both checks are the constant true and generate no code.
+
+// a buffer: its base and its length in bytes
+struct Ext {
+  const void* base;
+  size_t bytes;
+};
+
+__device__ __forceinline__ bool in_ext(const void* p, size_t n, const Ext& e, uint32_t* status) {
+#if SPEC_BOUNDS_CHECK
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p), b0 = reinterpret_cast<uintptr_t>(e.base);
+  const uintptr_t lo = b0 & ~(uintptr_t)15, hi = (b0 + e.bytes + 15) & ~(uintptr_t)15;
+  if (e.base != nullptr && a >= lo && a + n <= hi) return true;
+  atomicOr(status, SPEC_DEV_BOUNDS);
+  return false;
+#else
+  (void)p, (void)n, (void)e, (void)status;
+  return true;
+#endif
+}
+
+// index i of an array of n elements
+__device__ __forceinline__ bool in_idx(long long i, long long n, uint32_t* status) {
+#if SPEC_BOUNDS_CHECK
+  if (i >= 0 && i < n) return true;
+  atomicOr(status, SPEC_DEV_BOUNDS);
+  return false;
+#else
+  (void)i, (void)n, (void)status;
+  return true;
+#endif
+}
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
@@ -104,6 +147,8 @@ struct RowsParams {
   SeqRec* rec;
   int depth;
   int8_t parent[SPEC_MAX_TREE_NODES];
+  Ext x_target, x_draft, x_ws;  // the logit buffers and the workspace (bounds-checked build)
+  int out_rows;                 // entries of out_tok and g_tok (tree: B * (depth + 1))
 };
 
 struct SampleParams {
@@ -124,6 +169,7 @@ struct SampleParams {
   long long head_total;
   int nb_head, seg_head, seg_tail;
   int ph;  // aligned-row sampler: the rows' common offset in elements within the 16-byte grid
+  Ext x_target, x_draft, x_ws;  // the logit buffers and the workspace (bounds-checked build)
 };
 
 struct ProParams {
@@ -140,6 +186,7 @@ struct ProParams {
   long long bucket;
   unsigned* zero2;  // further tickets to zero (multi-draft matrix), or null
   int nzero2;
+  Ext x_ws;  // the workspace (bounds-checked build)
 };
 
 // ---------------------------------------------------------------------------
@@ -245,6 +292,10 @@ __device__ __forceinline__ float rescale(float s, float m, float M, float c) {
 constexpr int kCS = 3;   // stages of each thread's cp.async ring (vector path)
 constexpr int kCV = 4;   // 16-byte vectors per thread per stage
 constexpr int kRowsSmem = kCS * kCV * kThreads * 16;  // dynamic shared memory of the vector path
+// pairs at two phases: lane 31 of every warp also stages the draft vectors after its own
+// (its neighbours read theirs from the next lane's slots), two per stage
+constexpr int kShiftXSlot = kWarps * 2 * 16;
+constexpr int kShiftSmem = kRowsSmem + kCS * kShiftXSlot;
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -288,6 +339,31 @@ struct IO<float, 4> {
     f[3] = __uint_as_float(r.w);
   }
 };
+
+// Elements S .. S + VEC - 1 of the 2 VEC elements held by the aligned vector a and the one
+// after it, b: a row's vector at another phase within the 16-byte grid. bf16: 32-bit words
+// of two elements, whole words for even S, a byte permutation of two words for odd S;
+// fp32: whole words.
+template <typename E, int S>
+__device__ __forceinline__ uint4 shift_vec(const uint4& a, const uint4& b) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint4 r;
+  if constexpr (sizeof(E) == 2) {
+    static_assert(S > 0 && S < 8, "a shift within one bf16 vector");
+    constexpr int m = S / 2;
+    if constexpr (S % 2 == 0) {
+      r = make_uint4(w[m], w[m + 1], w[m + 2], w[m + 3]);
+    } else {
+      // the high element of word m + i, then the low element of word m + i + 1
+      r = make_uint4(__byte_perm(w[m], w[m + 1], 0x5432), __byte_perm(w[m + 1], w[m + 2], 0x5432),
+                     __byte_perm(w[m + 2], w[m + 3], 0x5432), __byte_perm(w[m + 3], w[m + 4], 0x5432));
+    }
+  } else {
+    static_assert(S > 0 && S < 4, "a shift within one fp32 vector");
+    r = make_uint4(w[S], w[S + 1], w[S + 2], w[S + 3]);
+  }
+  return r;
+}
 
 template <typename E>
 __device__ __forceinline__ float elem_at(const E* row, int x);
@@ -679,13 +755,16 @@ __device__ __forceinline__ void pair_update(TAcc& a, DAcc& d, const float (&t)[V
 // Lowest index of the value m inside the recorded group (g0: first VEC elements, g1:
 // the next VEC), re-read from the row (an L2 hit: the tile has just streamed it).
 template <typename E, int VEC>
-__device__ __forceinline__ int resolve_index(const E* row, int g0, int g1, float m) {
+__device__ __forceinline__ int resolve_index(const E* row, int g0, int g1, float m, const Ext* xr = nullptr,
+                                             uint32_t* status = nullptr) {
   if (g0 < 0) return INT_MAX;
   float f[VEC];
+  if (xr != nullptr && !in_ext(row + g0, 16, *xr, status)) return INT_MAX;
   IO<E, VEC>::unpack(ld_stream16(row + g0), f);
 #pragma unroll
   for (int k = 0; k < VEC; ++k)
     if (f[k] == m) return g0 + k;
+  if (xr != nullptr && !in_ext(row + g1, 16, *xr, status)) return INT_MAX;
   IO<E, VEC>::unpack(ld_stream16(row + g1), f);
 #pragma unroll
   for (int k = 0; k < VEC; ++k)
@@ -706,9 +785,11 @@ __device__ __forceinline__ int resolve_strided(const E* row, int g0, int g1, flo
 // row != nullptr: the target maximum's index is resolved from the recorded groups
 // (strided groups of stride GS when GS > 0); PRE: the caller has already resolved it into
 // ta.g0. SEPT: the draft sum s is at scale cd, s2 and k at c.
+// xr, status: the row's buffer for the bounds-checked build (null: unchecked).
 template <class SY, typename E = float, int VEC = 1, bool SEPT = false, int GS = 0, bool PRE = false>
 __device__ __forceinline__ Partial reduce_tile(int kind, const TAcc& ta, const DAcc& da, float c,
-                                               const E* row = nullptr, float cd = 0.f) {
+                                               const E* row = nullptr, float cd = 0.f, const Ext* xr = nullptr,
+                                               uint32_t* status = nullptr) {
   constexpr int NW = SY::NT / 32;
   __shared__ float s_m[2][NW];
   __shared__ float s_v[5][NW];
@@ -737,7 +818,7 @@ __device__ __forceinline__ Partial reduce_tile(int kind, const TAcc& ta, const D
     else if (ta.g1 == kExactIdx)
       my_idx = row ? ta.g0 : INT_MAX;
     else
-      my_idx = row ? resolve_index<E, VEC>(row, ta.g0, ta.g1, TM) : INT_MAX;
+      my_idx = row ? resolve_index<E, VEC>(row, ta.g0, ta.g1, TM, xr, status) : INT_MAX;
   }
   const int wi = warp_min_i(my_idx);
   float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f, v4 = 0.f;

@@ -37,6 +37,7 @@ struct PairParams {
   uint8_t* cons;
   uint8_t* div;
   uint32_t* status;
+  Ext x_draft, x_ws;  // the draft rows and the workspace (bounds-checked build)
 };
 
 // The last tile of a (group, position): merge the chunks' partials (thread (a, j) owns
@@ -46,6 +47,9 @@ __device__ __forceinline__ void pair_merge(const PairParams& p, int gi) {
   __shared__ float s_M[K], s_S[K], s_K[K * K], s_N[K * K];
   const float c = p.c;
   const PairPartial* pp = p.part + (size_t)gi * p.nchunks;
+  if (!in_ext(pp, sizeof(PairPartial) * p.nchunks, p.x_ws, p.status) ||
+      !in_idx((long long)gi, (long long)p.G * p.gamma, p.status))
+    return;  // (every thread: the condition is uniform)
   if (threadIdx.x < K * (K + 1)) {
     const int a = threadIdx.x / (K + 1), j = threadIdx.x - a * (K + 1);
     float M = -INFINITY;
@@ -95,7 +99,7 @@ __device__ __forceinline__ void pair_merge(const PairParams& p, int gi) {
 // sum s; per ordered pair: kk) into the tile's PairPartial. Every thread calls it.
 template <int K>
 __device__ __forceinline__ void pair_partial_write(PairPartial* dst, const float (&mr)[K], const float (&s)[K],
-                                                   const float (&kk)[K][K], float c) {
+                                                   const float (&kk)[K][K], float c, const PairParams& q) {
   __shared__ float s_red[kWarps][K + K * K];
   __shared__ float s_ref[kWarps][K];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -120,7 +124,8 @@ __device__ __forceinline__ void pair_partial_write(PairPartial* dst, const float
     }
   }
   __syncthreads();
-  if (threadIdx.x < K + K * K) {
+  const bool ok = in_ext(dst, sizeof(PairPartial), q.x_ws, q.status);
+  if (ok && threadIdx.x < K + K * K) {
     float t = 0.f;
     for (int w = 0; w < kWarps; ++w) t += s_red[w][threadIdx.x];
     if (threadIdx.x < K)
@@ -128,7 +133,7 @@ __device__ __forceinline__ void pair_partial_write(PairPartial* dst, const float
     else
       __stcg(&dst->k[threadIdx.x - K], t);
   }
-  if (threadIdx.x < K) __stcg(&dst->ref[threadIdx.x], DM[threadIdx.x]);
+  if (ok && threadIdx.x < K) __stcg(&dst->ref[threadIdx.x], DM[threadIdx.x]);
 }
 
 template <typename E, int VEC, int K>
@@ -195,8 +200,9 @@ __global__ void __launch_bounds__(kThreads, 2) pair_kernel(const __grid_constant
     raw_t r0[K], r1[K];
 #pragma unroll
     for (int a = 0; a < K; ++a) {
-      r0[a] = io::load(rows[a], v);
-      r1[a] = io::load(rows[a], v + kThreads);
+      r0[a] = in_ext(rows[a] + (size_t)v * VEC, 16, p.x_draft, p.status) ? io::load(rows[a], v) : make_uint4(0, 0, 0, 0);
+      r1[a] = in_ext(rows[a] + (size_t)(v + kThreads) * VEC, 16, p.x_draft, p.status) ? io::load(rows[a], v + kThreads)
+                                                                                        : make_uint4(0, 0, 0, 0);
     }
     float z[K][VEC];
 #pragma unroll
@@ -209,11 +215,13 @@ __global__ void __launch_bounds__(kThreads, 2) pair_kernel(const __grid_constant
   if (v < v1) {
     float z[K][VEC];
 #pragma unroll
-    for (int a = 0; a < K; ++a) io::unpack(io::load(rows[a], v), z[a]);
+    for (int a = 0; a < K; ++a)
+      io::unpack(in_ext(rows[a] + (size_t)v * VEC, 16, p.x_draft, p.status) ? io::load(rows[a], v) : make_uint4(0, 0, 0, 0),
+                 z[a]);
     fold(z);
   }
 
-  pair_partial_write<K>(p.part + tile, mr, s, kk, c);
+  pair_partial_write<K>(p.part + tile, mr, s, kk, c, p);
   __syncthreads();  // every writer's partial entries precede thread 0's ticket
   if (threadIdx.x == 0) {
     // release: the tile's partial before its ticket; acquire: the other tiles' partials
@@ -319,6 +327,7 @@ __global__ void __launch_bounds__(kThreads, 2) pair_staged_kernel(const __grid_c
       for (int a = 0; a < K; ++a) {
         src[a] = nullptr;
         nb[a] = run_blocks<E>(rows[a], e0, n, &src[a]);
+        if (nb[a] && !in_ext(src[a], nb[a], p.x_draft, p.status)) nb[a] = 0;
         total += nb[a];
       }
       const uint32_t bar = ring.bars + 8u * (uint32_t)(k % kCS);
@@ -357,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 2) pair_staged_kernel(const __grid_c
     }
   }
 
-  pair_partial_write<K>(p.part + tile, mr, s, kk, c);
+  pair_partial_write<K>(p.part + tile, mr, s, kk, c, p);
   __syncthreads();  // every writer's partial entries precede thread 0's ticket
   if (threadIdx.x == 0) {
     // release: the tile's partial before its ticket; acquire: the other tiles' partials
@@ -480,31 +489,21 @@ __device__ __forceinline__ void multi_pair_stage(const uint4* sq, int e0, float 
   }
 }
 
-template <typename E, int VEC, int K, int MODE>
-__global__ void __launch_bounds__(kThreads, 2) multi_rows_kernel(const __grid_constant__ RowsParams p,
-                                                                 const __grid_constant__ PairParams q) {
+// The stream and the partials of one fused tile: (group g, row r, chunk) of a draft
+// position (PAIR: the K target rows and the K draft rows) or of the bonus row (the K target
+// rows). PAIR is a template argument so that each kind keeps only its own accumulators.
+// The candidates' rows are addressed from one base and a row stride.
+template <typename E, int VEC, int K, int MODE, bool PAIR>
+__device__ __forceinline__ void multi_tile(const RowsParams& p, const PairParams& q, int g, int r, int chunk,
+                                           unsigned char* dsm) {
   using io = IO<E, VEC>;
   constexpr bool STOCH = MODE == M_STOCH;
   constexpr int kMS = multi_stages<K>();
-  extern __shared__ __align__(128) unsigned char dsm[];
-  griddep_wait();  // the prologue, and everything earlier on the stream, has completed
-  griddep_launch();
-  __shared__ int s_last[K + 1];
   const int gamma = p.gamma, nchunks = p.nchunks;
-  const int per = (gamma + 1) * nchunks;
-  const int tile = blockIdx.x;
-  const int g = tile / per, rem = tile - g * per;
-  const int r = rem / nchunks, chunk = rem - r * nchunks;
-  const bool pair = r < gamma;
   const size_t V = (size_t)p.V;
-  const E* trow[K];
-  const E* drow[K];
-#pragma unroll
-  for (int k = 0; k < K; ++k) {
-    const size_t b = (size_t)g * K + k;
-    trow[k] = static_cast<const E*>(p.target) + (b * (gamma + 1) + r) * V;
-    drow[k] = pair ? static_cast<const E*>(p.draft) + (b * gamma + r) * V : trow[k];
-  }
+  const E* tbase = static_cast<const E*>(p.target) + ((size_t)g * K * (gamma + 1) + r) * V;
+  const E* dbase = PAIR ? static_cast<const E*>(p.draft) + ((size_t)g * K * gamma + r) * V : tbase;
+  const size_t tstride = (size_t)(gamma + 1) * V, dstride = (size_t)gamma * V;
   const int e_begin = chunk * p.chunk_elems;
   const int e_end = min(e_begin + p.chunk_elems, p.V);
   const int v0 = e_begin / VEC, v1 = e_end / VEC;
@@ -523,19 +522,20 @@ __global__ void __launch_bounds__(kThreads, 2) multi_rows_kernel(const __grid_co
   }
 
   constexpr unsigned SLOT = 2 * K * kThreads * 16;
+  constexpr int NR = PAIR ? 2 * K : K;
   const int t = threadIdx.x;
   const uint32_t base = (uint32_t)__cvta_generic_to_shared(dsm) + 16u * t;
   const int nst = (v1 - v0 + kThreads - 1) / kThreads;
-  const int nr = pair ? 2 * K : K;
   auto issue = [&](int st) {
     if (st < nst) {
       const int v = v0 + t + st * kThreads;
       if (v < v1) {
         const uint32_t slot = base + (uint32_t)(st % kMS) * SLOT;
 #pragma unroll
-        for (int j = 0; j < 2 * K; ++j)
-          if (j < nr)
-            cp_async16(slot + (uint32_t)(j * kThreads * 16), (j < K ? trow[j] : drow[j - K]) + (size_t)v * VEC);
+        for (int j = 0; j < NR; ++j) {
+          const E* src = (j < K ? tbase + j * tstride : dbase + (j - K) * dstride) + (size_t)v * VEC;
+          if (in_ext(src, 16, j < K ? p.x_target : p.x_draft, p.status)) cp_async16(slot + (uint32_t)(j * kThreads * 16), src);
+        }
       }
     }
     cp_commit();
@@ -549,41 +549,26 @@ __global__ void __launch_bounds__(kThreads, 2) multi_rows_kernel(const __grid_co
     if (v >= v1) continue;
     const uint4* sq = reinterpret_cast<const uint4*>(dsm + (size_t)(st % kMS) * SLOT) + t;
     const int e0 = v * VEC;
-    if constexpr (K <= 3) {
-      if (pair) {
-        multi_pair_stage<E, VEC, K, STOCH>(sq, e0, c, cq, ta, da, kk);
-        continue;
-      }
-    }
-    // K = 4 pairs (every candidate's draft vectors held at once would spill: they are
-    // unpacked per use) and the bonus row of every K
-    constexpr bool PRE = K <= 3;
-    float fdk[PRE ? K : 1][VEC];
-    if (PRE && pair) {
+    if constexpr (PAIR && K <= 3) {
+      multi_pair_stage<E, VEC, K, STOCH>(sq, e0, c, cq, ta, da, kk);
+    } else if constexpr (PAIR) {
+      // K = 4: every candidate's draft vectors held at once would spill; they are
+      // unpacked per use
 #pragma unroll
-      for (int a = 0; a < (PRE ? K : 0); ++a) io::unpack(sq[(K + a) * kThreads], fdk[a]);
-    }
-#pragma unroll
-    for (int a = 0; a < K; ++a) {
-      float ft[VEC];
-      io::unpack(sq[a * kThreads], ft);
-      if (!pair || !STOCH) {
-        if (STOCH)
-          tsum_update<VEC>(ta[a], ft, e0, c);  // the stochastic bonus row
-        else
-          argmax_update<VEC>(ta[a], ft, e0);   // greedy rows
-      } else {
-        const float vm = vmax<VEC>(ft);
-        track_max<VEC, VEC, true>(ta[a], ft, vm, e0, 0);
-        lazy_ref(ta[a].mr, ta[a].mth, ta[a].nmc, ta[a].s, nullptr, vm, c);
-        float et[VEC];
-        ta[a].s = add2(ta[a].s, exp_sum2<VEC>(ft, c, ta[a].nmc, et));
-      }
-      if (pair) {
-        float fdu[VEC];
-        if constexpr (!PRE) io::unpack(sq[(K + a) * kThreads], fdu);
-        const float (&fd)[VEC] = PRE ? fdk[PRE ? a : 0] : fdu;
-        float ed[VEC];
+      for (int a = 0; a < K; ++a) {
+        float ft[VEC];
+        io::unpack(sq[a * kThreads], ft);
+        if constexpr (STOCH) {
+          const float vm = vmax<VEC>(ft);
+          track_max<VEC, VEC, true>(ta[a], ft, vm, e0, 0);
+          lazy_ref(ta[a].mr, ta[a].mth, ta[a].nmc, ta[a].s, nullptr, vm, c);
+          float et[VEC];
+          ta[a].s = add2(ta[a].s, exp_sum2<VEC>(ft, c, ta[a].nmc, et));
+        } else {
+          argmax_update<VEC>(ta[a], ft, e0);
+        }
+        float fd[VEC], ed[VEC];
+        io::unpack(sq[(K + a) * kThreads], fd);
         const float vm = vmax<VEC>(fd);
         const bool mv = vm > da[a].mth;
         if (__any_sync(__activemask(), mv)) {
@@ -603,53 +588,83 @@ __global__ void __launch_bounds__(kThreads, 2) multi_rows_kernel(const __grid_co
 #pragma unroll
         for (int b = 0; b < K; ++b) {
           if (b == a) continue;
-          if constexpr (PRE) {
-            kk[a][b] += dot_diff<VEC>(ed, fd, fdk[b]);
-          } else {
-            float fb[VEC];
-            io::unpack(sq[(K + b) * kThreads], fb);
-            kk[a][b] += dot_diff<VEC>(ed, fd, fb);
-          }
+          float fb[VEC];
+          io::unpack(sq[(K + b) * kThreads], fb);
+          kk[a][b] += dot_diff<VEC>(ed, fd, fb);
         }
+      }
+    } else {
+      // the bonus row: stochastic sums, greedy argmax
+#pragma unroll
+      for (int a = 0; a < K; ++a) {
+        float ft[VEC];
+        io::unpack(sq[a * kThreads], ft);
+        if constexpr (STOCH)
+          tsum_update<VEC>(ta[a], ft, e0, c);
+        else
+          argmax_update<VEC>(ta[a], ft, e0);
       }
     }
   }
   cp_wait<0>();
 
   // partials: one per candidate in the tile kernel's layout, one pairwise partial
-  const int kind = pair ? (STOCH ? K_PAIR : K_ARGMAX) : (STOCH ? K_TSUM : K_ARGMAX);
+  constexpr int kind = PAIR ? (STOCH ? K_PAIR : K_ARGMAX) : (STOCH ? K_TSUM : K_ARGMAX);
 #pragma unroll
   for (int a = 0; a < K; ++a) {
-    const Partial part = reduce_tile<BlockSync, E, VEC>(kind, ta[a], da[a], c, trow[a]);
-    if (threadIdx.x == 0) {
-      const size_t row = ((size_t)g * K + a) * (gamma + 1) + r;
-      float4* dst = reinterpret_cast<float4*>(p.part + row * nchunks + chunk);
+    const Partial part = reduce_tile<BlockSync, E, VEC>(kind, ta[a], da[a], c, tbase + a * tstride, 0.f, &p.x_target,
+                                                        p.status);
+    const size_t row = ((size_t)g * K + a) * (gamma + 1) + r;
+    float4* dst = reinterpret_cast<float4*>(p.part + row * nchunks + chunk);
+    if (threadIdx.x == 0 && in_ext(dst, sizeof(Partial), p.x_ws, p.status)) {
       __stcg(dst, make_float4(part.tm, part.ts, __int_as_float(part.tidx), __int_as_float(part.bad)));
       __stcg(dst + 1, make_float4(part.dm, part.ds, part.dk, part.ds2));
     }
     __syncthreads();  // reduce_tile's shared arrays are reused by the next candidate
   }
-  if (pair) {
+  if constexpr (PAIR) {
     float mr[K], sm[K];
 #pragma unroll
     for (int a = 0; a < K; ++a) {
       mr[a] = da[a].mr;
       sm[a] = da[a].s.x + da[a].s.y;
     }
-    pair_partial_write<K>(q.part + ((size_t)g * gamma + r) * nchunks + chunk, mr, sm, kk, cq);
+    pair_partial_write<K>(q.part + ((size_t)g * gamma + r) * nchunks + chunk, mr, sm, kk, cq, q);
   }
+}
+
+template <typename E, int VEC, int K, int MODE>
+__global__ void __launch_bounds__(kThreads, 2) multi_rows_kernel(const __grid_constant__ RowsParams p,
+                                                                 const __grid_constant__ PairParams q) {
+  constexpr bool STOCH = MODE == M_STOCH;
+  extern __shared__ __align__(128) unsigned char dsm[];
+  griddep_wait();  // the prologue, and everything earlier on the stream, has completed
+  griddep_launch();
+  __shared__ int s_last[K + 1];
+  const int gamma = p.gamma, nchunks = p.nchunks;
+  const int per = (gamma + 1) * nchunks;
+  const int tile = blockIdx.x;
+  const int g = tile / per, rem = tile - g * per;
+  const int r = rem / nchunks, chunk = rem - r * nchunks;
+  const bool pair = r < gamma;
+  if (pair)
+    multi_tile<E, VEC, K, MODE, true>(p, q, g, r, chunk, dsm);
+  else
+    multi_tile<E, VEC, K, MODE, false>(p, q, g, r, chunk, dsm);
   __syncthreads();  // every writer's partial entries precede thread 0's fence
   if (threadIdx.x == 0) {
     __threadfence();
     bool any = false;
     for (int a = 0; a < K; ++a) {
-      const unsigned old = atomicAdd(p.cnt + (size_t)g * K + a, 1u);
+      const unsigned old = in_ext(p.cnt + (size_t)g * K + a, sizeof(unsigned), p.x_ws, p.status)
+                               ? atomicAdd(p.cnt + (size_t)g * K + a, 1u) : 0u;
       s_last[a] = (old + 1u == (unsigned)per) ? 1 : 0;
       any = any || s_last[a];
     }
     s_last[K] = 0;
     if (pair) {
-      const unsigned old = atomicAdd(q.cnt + (size_t)g * gamma + r, 1u);
+      const unsigned old = in_ext(q.cnt + (size_t)g * gamma + r, sizeof(unsigned), q.x_ws, q.status)
+                               ? atomicAdd(q.cnt + (size_t)g * gamma + r, 1u) : 0u;
       s_last[K] = (old + 1u == (unsigned)nchunks) ? 1 : 0;
       any = any || s_last[K];
     }

@@ -14,7 +14,7 @@ __global__ void prologue_kernel(const __grid_constant__ ProParams p) {
   griddep_wait();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b < p.nzero2) p.zero2[b] = 0u;
-  if (b == 0) {
+  if (b == 0 && in_ext(p.cntA + p.B, sizeof(unsigned), p.x_ws, p.status)) {
     p.cntA[p.B] = 0u;
     if (p.stats != nullptr && p.stats->bucket != p.bucket) {
       // a new time bucket takes over the slot (every finaliser of this call runs after
@@ -25,6 +25,9 @@ __global__ void prologue_kernel(const __grid_constant__ ProParams p) {
     }
   }
   if (b >= p.B) return;
+  if (!in_ext(p.cntA + b, sizeof(unsigned), p.x_ws, p.status) || !in_ext(p.cntB + b, sizeof(unsigned), p.x_ws, p.status) ||
+      !in_ext(p.rec + b, sizeof(SeqRec), p.x_ws, p.status))
+    return;
   p.cntA[b] = 0u;
   p.cntB[b] = 0u;
   SeqRec q;
@@ -47,7 +50,8 @@ __global__ void prologue_kernel(const __grid_constant__ ProParams p) {
     // the offsets then report it)
     if (own && p.row_seq != nullptr) {
       const int r1 = min(c1 + p.hb * (b + 1), p.total_rows);
-      for (int r = c0 + p.hb * b; r < r1; ++r) p.row_seq[r] = b;
+      for (int r = c0 + p.hb * b; r < r1; ++r)
+        if (in_ext(p.row_seq + r, sizeof(int32_t), p.x_ws, p.status)) p.row_seq[r] = b;
     }
   }
 }
@@ -157,6 +161,11 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
   const int i_own = tid - (NT - gb);  // this thread's draft position, or < 0
   int px = 0;
   float pu = 0.f, pzt = 0.f, pzd = 0.f, pus = 0.f;
+  // bounds-checked build: every output of the sequence lies in [tb, tb + gb] of the target-row
+  // outputs and [db, db + gb) of the per-draft ones, its records at index b
+  if (!in_idx(b, p.B, p.status) || !in_idx(db + gb - 1 + HB, p.total_draft + HB, p.status) ||
+      !in_idx(tb + gb - 1 + HB, p.out_rows, p.status))
+    return;
   if constexpr (MODE != M_TREE && MODE != M_NKL) {
     if (is_stoch(MODE) && tid == 0) pus = p.u_sample[b];  // for the sampler's record
     if (i_own >= 0) {
@@ -164,8 +173,10 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
       if constexpr (is_stoch(MODE)) {
         pu = p.u_accept[db + i_own];
         if (px >= 0 && px < p.V) {
-          pzt = elem_at<E>(target + (size_t)(tb + i_own) * V, px);
-          pzd = elem_at<E>(draft + (size_t)(db + i_own) * V, px);
+          const E* at = target + (size_t)(tb + i_own) * V + px;
+          const E* ad = draft + (size_t)(db + i_own) * V + px;
+          if (in_ext(at, sizeof(E), p.x_target, p.status)) pzt = elem_at<E>(at, 0);
+          if (in_ext(ad, sizeof(E), p.x_draft, p.status)) pzd = elem_at<E>(ad, 0);
         }
       }
     }
@@ -176,7 +187,7 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
     static_assert(NT >= SPEC_MAX_TREE_NODES, "one node per thread");
     const int j = tid - (NT - p.N);
     if (j >= 0) {
-      s_tok[j] = p.node_tokens[(size_t)b * p.N + j];
+      s_tok[j] = in_idx((long long)b * p.N + j, (long long)p.B * p.N, p.status) ? p.node_tokens[(size_t)b * p.N + j] : -1;
       s_par[j] = p.parent[j];
     }
   }
@@ -185,12 +196,16 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
     const int half = lane >> 4;
     for (int i = 2 * warp; i < R; i += 2 * NW) {
       const int ii = min(i + half, R - 1);
-      const RowStat r = merge_row<16>(p.part + (size_t)(row0 + ii) * p.nchunks, p.nchunks, c, p.cd);
+      const Partial* pr = p.part + (size_t)(row0 + ii) * p.nchunks;
+      const bool okp = in_ext(pr, sizeof(Partial) * p.nchunks, p.x_ws, p.status);
+      const RowStat r = merge_row<16>(okp ? pr : p.part, okp ? p.nchunks : 0, c, p.cd);
       if ((lane & 15) == 0 && i + half < R) rs[i + half] = r;
     }
   } else {
     for (int i = warp; i < R; i += NW) {
-      const RowStat r = merge_row(p.part + (size_t)(row0 + i) * p.nchunks, p.nchunks, c, p.cd);
+      const Partial* pr = p.part + (size_t)(row0 + i) * p.nchunks;
+      const bool okp = in_ext(pr, sizeof(Partial) * p.nchunks, p.x_ws, p.status);
+      const RowStat r = merge_row(okp ? pr : p.part, okp ? p.nchunks : 0, c, p.cd);
       if (lane == 0) rs[i] = r;
     }
   }
@@ -418,7 +433,8 @@ __device__ __forceinline__ void unpack2(const uint4& a, const uint4& b, float (&
 // re-reading the row.
 template <typename E, int VEC, int MODE, int KIND>
 __device__ __forceinline__ void stream_tile(const E* trow, const E* drow, int v0, int v1, float c, float cd,
-                                            TAcc& ta, DAcc& da, unsigned char* smem, uint4 (&best)[2]) {
+                                            TAcc& ta, DAcc& da, unsigned char* smem, uint4 (&best)[2],
+                                            const RowsParams& p) {
   constexpr bool IDX = is_stoch(MODE), SEPT = MODE == M_STOCH2;
   constexpr int PER = (KIND == K_PAIR) ? 2 * kThreads : 4 * kThreads;  // vectors of a row per stage
   constexpr unsigned SLOT = kCV * kThreads * 16;                         // bytes of one stage
@@ -438,7 +454,8 @@ __device__ __forceinline__ void stream_tile(const E* trow, const E* drow, int v0
         const int jv = (KIND == K_PAIR) ? (j & 1) : j;
         if (v + jv * kThreads < v1) {
           const E* src = ((KIND == K_PAIR && j >= 2) ? dp : tp) + off + (size_t)jv * kThreads * VEC;
-          cp_async16(slot + (uint32_t)(j * kThreads * 16), src);
+          if (in_ext(src, 16, (KIND == K_PAIR && j >= 2) ? p.x_draft : p.x_target, p.status))
+            cp_async16(slot + (uint32_t)(j * kThreads * 16), src);
         }
       }
     }
@@ -498,88 +515,105 @@ __device__ __forceinline__ void stream_tile(const E* trow, const E* drow, int v0
   cp_wait<0>();
 }
 
-// Staged path: the tile [e_begin, e_end) in stages of kStageRowBytes per row of a pair
-// (twice that for a single row); warp w takes the w-th contiguous run of every stage
-// through its own kCS-slot ring (WarpRing: bulk copies of whole aligned 16-byte blocks),
-// so no block-wide barrier orders the copies and the reads. Lane l takes elements
-// l, l + 32, ... of the run (consecutive lanes read consecutive elements: conflict free),
-// folded in as strided groups of up to 16; a group that the run's end cuts is folded in
-// element by element.
-template <typename E, int MODE, int KIND>
-__device__ __forceinline__ void stream_staged(const E* trow, const E* drow, int e_begin, int e_end, float c, float cd,
-                                              TAcc& ta, DAcc& da, unsigned char* smem, uint32_t* status) {
-  constexpr bool IDX = is_stoch(MODE), SEPT = MODE == M_STOCH2, PAIR = KIND == K_PAIR;
-  constexpr int SW = (PAIR ? kWarpRowBytes : 2 * kWarpRowBytes) / (int)sizeof(E);  // elements of a warp's run
-  constexpr int S = SW * kWarps;                                                     // elements of a stage
-  constexpr int U = SW / 32;                                                         // per lane per run
-  constexpr int G = U < 16 ? U : 16;                                                 // elements of a group
-  constexpr int NG = U / G;
-  static_assert(U % G == 0, "runs of whole groups");
-  __shared__ __align__(8) uint64_t s_bars[kWarps][kCS];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  WarpRing ring;  // one pass per block: stage k is ring stage k
-  ring.init(s_bars[warp]);
-  const uint32_t wbase = (uint32_t)__cvta_generic_to_shared(smem) + (uint32_t)(warp * kWarpStage);
-  const int nst = (e_end - e_begin + S - 1) / S;
-  // S and SW elements are whole 16-byte blocks: every run of a row has the same phase
-  const int ph_t = phase16(trow + e_begin), ph_d = PAIR ? phase16(drow + e_begin) : 0;
+// Row pairs whose two rows sit at different offsets within the 16-byte grid (a vocabulary
+// whose row is not a whole number of 16-byte blocks): the stream of stream_tile over the
+// target's aligned vectors v in [v0, v1), and for each the draft's elements at the same
+// row indices, which lie in the draft's aligned vectors w = v + dw and w + 1, shifted by S
+// elements (dw * VEC + S = the draft's offset minus the target's, 0 < S < VEC). Each lane
+// copies its own w; after a warp barrier it takes w + 1 from the next lane's slot, and lane
+// 31 copies its w + 1 itself into a small ring of its own (kShiftXSlot bytes per stage
+// after the main ring). Lanes one vector past the end still copy their draft vector (the
+// lane before needs it as its w + 1): it holds the last element of the last whole target
+// vector, so it lies in the row. Two warp barriers per stage: before a slot is refilled
+// (every lane has read it) and after the copies land (they are visible to the warp).
+template <typename E, int VEC, int MODE, int S>
+__device__ __forceinline__ void stream_tile_sh(const E* trv, const E* drv, int v0, int v1, int dw, float c, float cd,
+                                               TAcc& ta, DAcc& da, unsigned char* smem, const RowsParams& p) {
+  constexpr bool IDX = is_stoch(MODE), SEPT = MODE == M_STOCH2;
+  constexpr int PER = 2 * kThreads;            // vectors of a row per stage
+  constexpr unsigned SLOT = kCV * kThreads * 16;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const uint32_t base = (uint32_t)__cvta_generic_to_shared(smem) + 16u * t;
+  unsigned char* xring = smem + kCS * SLOT;
+  const uint32_t xbase = (uint32_t)__cvta_generic_to_shared(xring) + (uint32_t)(warp * 32);
+  const int nst = (v1 - v0 + PER - 1) / PER;
+  const int vt = v0 + t;
+  const E* tp = trv + (size_t)vt * VEC;
+  const E* dp = drv + (ptrdiff_t)(vt + dw) * VEC;
   auto issue = [&](int k) {
-    if (lane == 0 && k < nst) {
-      const uint32_t slot = wbase + (uint32_t)((k % kCS) * kWarps * kWarpStage);
-      const int e0 = e_begin + k * S + warp * SW, n = min(SW, e_end - e0);
-      const void* s0 = nullptr;
-      const void* s1 = nullptr;
-      const uint32_t n0 = run_blocks<E>(trow, e0, n, &s0);
-      const uint32_t n1 = PAIR ? run_blocks<E>(drow, e0, n, &s1) : 0u;
-      ring.produce(k, slot, s0, n0, slot + kWarpSlot, s1, n1);
+    if (k < nst) {
+      const uint32_t slot = base + (uint32_t)(k % kCS) * SLOT;
+      const uint32_t xs = xbase + (uint32_t)(k % kCS) * kShiftXSlot;
+      const int v = vt + k * PER;
+      const size_t off = (size_t)k * PER * VEC;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int vh = v + h * kThreads;
+        const size_t o = off + (size_t)h * kThreads * VEC;
+        if (vh < v1 && in_ext(tp + o, 16, p.x_target, p.status)) cp_async16(slot + (uint32_t)(h * kThreads * 16), tp + o);
+        if (vh <= v1 && in_ext(dp + o, 16, p.x_draft, p.status))
+          cp_async16(slot + (uint32_t)((2 + h) * kThreads * 16), dp + o);
+        if (lane == 31 && vh < v1 && in_ext(dp + o + VEC, 16, p.x_draft, p.status)) cp_async16(xs + 16u * h, dp + o + VEC);
+      }
     }
+    cp_commit();
   };
 #pragma unroll
   for (int k = 0; k < kCS - 1; ++k) issue(k);
   for (int k = 0; k < nst; ++k) {
-    __syncwarp();        // every lane is done with stage k - 1
-    issue(k + kCS - 1);  // into the slot of stage k - 1
-    ring.wait(k, status);
-    const unsigned char* slot = smem + (size_t)(warp * kWarpStage + (k % kCS) * kWarps * kWarpStage);
-    const E* sT = reinterpret_cast<const E*>(slot) + ph_t;
-    const E* sD = reinterpret_cast<const E*>(slot + kWarpSlot) + ph_d;
-    const int eb = e_begin + k * S + warp * SW, n = min(SW, e_end - eb);
-#pragma unroll
-    for (int g = 0; g < NG; ++g) {
-      const int x0 = g * G * 32 + lane;  // this lane's first element of the group
-      if (x0 + (G - 1) * 32 < n) {       // the whole group is inside the run
-        float ft[G], fd[G];
-#pragma unroll
-        for (int j = 0; j < G; ++j) {
-          ft[j] = sh_elem<E>(sT, x0 + j * 32);
-          if constexpr (PAIR) fd[j] = sh_elem<E>(sD, x0 + j * 32);
-        }
-        if constexpr (PAIR)
-          pair_update<G, IDX, 0, SEPT>(ta, da, ft, fd, eb + x0, c, 0, cd);
-        else if constexpr (KIND == K_TSUM)
-          tsum_update<G, 0>(ta, ft, eb + x0, c);
-        else
-          argmax_update<G, 0>(ta, ft, eb + x0);
-      } else {
-        for (int x = x0; x < n; x += 32) {
-          float ft[1], fd[1];
-          ft[0] = sh_elem<E>(sT, x);
-          if constexpr (PAIR) {
-            fd[0] = sh_elem<E>(sD, x);
-            pair_update<1, IDX, 0, SEPT>(ta, da, ft, fd, eb + x, c, 0, cd);
-          } else if constexpr (KIND == K_TSUM) {
-            tsum_update<1, 0>(ta, ft, eb + x, c);
-          } else {
-            argmax_update<1, 0>(ta, ft, eb + x);
-          }
-        }
-      }
+    __syncwarp();  // every lane has read the slot issue() refills (stage k - 1)
+    issue(k + kCS - 1);
+    cp_wait<kCS - 1>();
+    __syncwarp();  // the lanes' copies of stage k are visible to the whole warp
+    const uint4* q = reinterpret_cast<const uint4*>(smem + (size_t)(k % kCS) * SLOT) + t;
+    const uint4* qx = reinterpret_cast<const uint4*>(xring + (size_t)(k % kCS) * kShiftXSlot) + warp * 2;
+    const int va = vt + k * PER, vb = va + kThreads;
+    if (vb < v1) {
+      float ft[2 * VEC], fd[2 * VEC];
+      unpack2<E, VEC>(q[0], q[kThreads], ft);
+      const uint4 n0 = lane < 31 ? q[2 * kThreads + 1] : qx[0];
+      const uint4 n1 = lane < 31 ? q[3 * kThreads + 1] : qx[1];
+      unpack2<E, VEC>(shift_vec<E, S>(q[2 * kThreads], n0), shift_vec<E, S>(q[3 * kThreads], n1), fd);
+      pair_update<2 * VEC, IDX, VEC, SEPT>(ta, da, ft, fd, va * VEC, c, vb * VEC, cd);
+    } else if (va < v1) {
+      float ft[VEC], fd[VEC];
+      IO<E, VEC>::unpack(q[0], ft);
+      const uint4 n0 = lane < 31 ? q[2 * kThreads + 1] : qx[0];
+      IO<E, VEC>::unpack(shift_vec<E, S>(q[2 * kThreads], n0), fd);
+      pair_update<VEC, IDX, VEC, SEPT>(ta, da, ft, fd, va * VEC, c, 0, cd);
+    }
+  }
+  cp_wait<0>();
+}
+
+// The shifted stream for the tile's shift s (0 < s < VEC), one instance per shift.
+template <typename E, int VEC, int MODE>
+__device__ __forceinline__ void stream_tile_shifted(int s, const E* trv, const E* drv, int v0, int v1, int dw, float c,
+                                                    float cd, TAcc& ta, DAcc& da, unsigned char* smem,
+                                                    const RowsParams& p) {
+  if constexpr (VEC == 8) {
+    switch (s) {
+      case 1: stream_tile_sh<E, VEC, MODE, 1>(trv, drv, v0, v1, dw, c, cd, ta, da, smem, p); break;
+      case 2: stream_tile_sh<E, VEC, MODE, 2>(trv, drv, v0, v1, dw, c, cd, ta, da, smem, p); break;
+      case 3: stream_tile_sh<E, VEC, MODE, 3>(trv, drv, v0, v1, dw, c, cd, ta, da, smem, p); break;
+      case 4: stream_tile_sh<E, VEC, MODE, 4>(trv, drv, v0, v1, dw, c, cd, ta, da, smem, p); break;
+      case 5: stream_tile_sh<E, VEC, MODE, 5>(trv, drv, v0, v1, dw, c, cd, ta, da, smem, p); break;
+      case 6: stream_tile_sh<E, VEC, MODE, 6>(trv, drv, v0, v1, dw, c, cd, ta, da, smem, p); break;
+      default: stream_tile_sh<E, VEC, MODE, 7>(trv, drv, v0, v1, dw, c, cd, ta, da, smem, p); break;
+    }
+  } else {
+    switch (s) {
+      case 1: stream_tile_sh<E, VEC, MODE, 1>(trv, drv, v0, v1, dw, c, cd, ta, da, smem, p); break;
+      case 2: stream_tile_sh<E, VEC, MODE, 2>(trv, drv, v0, v1, dw, c, cd, ta, da, smem, p); break;
+      default: stream_tile_sh<E, VEC, MODE, 3>(trv, drv, v0, v1, dw, c, cd, ta, da, smem, p); break;
     }
   }
 }
 
-// PH (argmax rows only): rows at any element alignment, each tile applying its row's phase.
-template <typename E, int VEC, int MODE, bool PH = false>
+// PH: rows at any element alignment, each tile applying its row's phase (the rows of a
+// pair at one phase). SH (with PH): the rows of a pair may sit at different phases; a pair
+// tile whose draft row is off its target row's phase takes the shifted stream.
+template <typename E, int VEC, int MODE, bool PH = false, bool SH = false>
 __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant__ RowsParams p) {
   constexpr int HB = (MODE == M_NKL) ? 0 : 1;
   extern __shared__ __align__(128) unsigned char dsm[];
@@ -603,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
   } else {
     // the sequence owning row r, from the prologue's table (written before this grid's
     // griddepcontrol.wait returned); checked against the offsets below
-    b = __ldcg(p.row_seq + r);
+    b = in_ext(p.row_seq + r, sizeof(int32_t), p.x_ws, p.status) ? __ldcg(p.row_seq + r) : -1;
     if (b < 0 || b >= p.B) {
       if (threadIdx.x == 0) {
         atomicOr(p.status, SPEC_DEV_OFFSETS);
@@ -639,23 +673,28 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
   init(ta);
   init(da);
   constexpr bool ARGMAX = MODE == M_GREEDY || MODE == M_TREE;
-  static_assert(VEC > 1 || !ARGMAX, "argmax rows at any alignment take the vector path");
-  static_assert(!PH || VEC > 1, "the phased tiles are vector tiles");
-  // PH: the row's offset in elements within the 16-byte grid (the rows of a pair share it);
-  // indices are counted from the aligned base until the partial is written
+  static_assert(VEC > 1, "tiles stream 16-byte vectors");
+  static_assert(!SH || (PH && !ARGMAX), "shifted pairs are phased pair tiles");
+  // PH: the row's offset in elements within the 16-byte grid; indices are counted from the
+  // aligned base until the partial is written
   int ph = 0;
-  if constexpr (VEC > 1) {
+  {
     uint4 best[2];
     // Rows at any element alignment (PH): the whole aligned 16-byte blocks of the chunk are
     // streamed as vectors of the aligned bases trv and drv (row element e is element
-    // e + ph there); the partial blocks at the chunk's ends, head [e_begin, hend) and tail
-    // [tbeg, e_end), are copied beside the ring by threads 0 and 1 and folded in element by
-    // element.
+    // e + ph of trv, e + phd of drv); the partial blocks at the chunk's ends, head
+    // [e_begin, hend) and tail [tbeg, e_end), are copied beside the ring by threads 0 and 1
+    // (the target's block, and the one or two draft blocks holding the same elements) and
+    // folded in element by element.
     if constexpr (PH) ph = (int)(((uintptr_t)trow & 15u) / sizeof(E));
+    const int phd = (PH && kind == K_PAIR) ? (int)(((uintptr_t)drow & 15u) / sizeof(E)) : ph;
     const E* trv = trow - ph;
-    const E* drv = drow - ph;
+    const E* drv = drow - phd;
+    // shifted pairs: the draft elements of target vector v lie in draft vectors v + dw and
+    // v + dw + 1, from element sft on
+    const int sft = (phd - ph + VEC) % VEC, dw = (phd - ph - sft) / VEC;
     const int vf0 = (e_begin + ph + VEC - 1) / VEC, vf1 = (e_end + ph) / VEC;
-    __shared__ uint4 s_edge[2][2];  // [head, tail][target, draft]
+    __shared__ uint4 s_edge[2][3];  // [head, tail][target, draft, next draft]
     // thread 0 takes the head, thread 1 the tail (the bounds are recomputed after the
     // stream, so that none of them is held through it)
     auto edge_range = [&](int& elo, int& ehi) {
@@ -668,13 +707,21 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
       edge_range(elo, ehi);
       if (elo < ehi) {
         const size_t eb = (size_t)((elo + ph) / VEC) * VEC;
-        cp_async16((uint32_t)__cvta_generic_to_shared(&s_edge[threadIdx.x][0]), trv + eb);
-        if (kind == K_PAIR) cp_async16((uint32_t)__cvta_generic_to_shared(&s_edge[threadIdx.x][1]), drv + eb);
+        if (in_ext(trv + eb, 16, p.x_target, p.status))
+          cp_async16((uint32_t)__cvta_generic_to_shared(&s_edge[threadIdx.x][0]), trv + eb);
+        if (kind == K_PAIR) {
+          // the draft blocks holding elements elo and ehi - 1 (one block at equal phases)
+          const int w0 = (elo + phd) / VEC, w1 = (ehi - 1 + phd) / VEC;
+          if (in_ext(drv + (size_t)w0 * VEC, 16, p.x_draft, p.status))
+            cp_async16((uint32_t)__cvta_generic_to_shared(&s_edge[threadIdx.x][1]), drv + (size_t)w0 * VEC);
+          if (w1 > w0 && in_ext(drv + (size_t)w1 * VEC, 16, p.x_draft, p.status))
+            cp_async16((uint32_t)__cvta_generic_to_shared(&s_edge[threadIdx.x][2]), drv + (size_t)w1 * VEC);
+        }
       }
     }
     // (stream_tile's last wait covers the edge copies too)
     if constexpr (ARGMAX) {
-      stream_tile<E, VEC, MODE, K_ARGMAX>(trv, drv, vf0, vf1, c, cd, ta, da, dsm, best);
+      stream_tile<E, VEC, MODE, K_ARGMAX>(trv, drv, vf0, vf1, c, cd, ta, da, dsm, best, p);
       // the lowest index of the thread's maximum, from the raw vectors of its group
       if (ta.g0 >= 0) {
         float f[2 * VEC];
@@ -685,20 +732,24 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
           if (f[j] == ta.m) k = j;
         ta.g0 = k < VEC ? ta.g0 + k : ta.g1 + (k - VEC);
       }
-    } else if constexpr (MODE == M_NKL) {
-      stream_tile<E, VEC, MODE, K_PAIR>(trv, drv, vf0, vf1, c, cd, ta, da, dsm, best);
     } else {
-      if (kind == K_PAIR)
-        stream_tile<E, VEC, MODE, K_PAIR>(trv, drv, vf0, vf1, c, cd, ta, da, dsm, best);
-      else
-        stream_tile<E, VEC, MODE, K_TSUM>(trv, drv, vf0, vf1, c, cd, ta, da, dsm, best);
+      if (kind == K_PAIR) {
+        if (SH && sft != 0)
+          stream_tile_shifted<E, VEC, MODE>(sft, trv, drv, vf0, vf1, dw, c, cd, ta, da, dsm, p);
+        else
+          stream_tile<E, VEC, MODE, K_PAIR>(trv, drv, vf0, vf1, c, cd, ta, da, dsm, best, p);
+      } else if constexpr (MODE != M_NKL) {
+        stream_tile<E, VEC, MODE, K_TSUM>(trv, drv, vf0, vf1, c, cd, ta, da, dsm, best, p);
+      }
     }
     int elo = 0, ehi = 0;
     if (PH && threadIdx.x < 2) edge_range(elo, ehi);
     if (PH && elo < ehi) {
-      float ft[VEC], fd[VEC];
+      float ft[VEC];
       IO<E, VEC>::unpack(s_edge[threadIdx.x][0], ft);
-      if (kind == K_PAIR) IO<E, VEC>::unpack(s_edge[threadIdx.x][1], fd);
+      // the draft element of row index e sits at e + phd - w0 * VEC in the two draft blocks
+      const E* dsh = reinterpret_cast<const E*>(&s_edge[threadIdx.x][1]);
+      const int dbase = ((elo + phd) / VEC) * VEC - phd;
       const int e0 = ((elo + ph) / VEC) * VEC - ph;  // row index of ft[0]
 #pragma unroll
       for (int j = 0; j < VEC; ++j) {
@@ -715,7 +766,7 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
           const int g0 = ta.g0, g1 = ta.g1;
           const float xt[1] = {x};
           if (kind == K_PAIR) {
-            const float xd[1] = {fd[j]};
+            const float xd[1] = {sh_elem<E>(dsh, e - dbase)};
             pair_update<1, false, 0, SEPT>(ta, da, xt, xd, 0, c, 0, cd);
           } else {
             tsum_update<1, 0>(ta, xt, 0, c);
@@ -733,33 +784,22 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
         }
       }
     }
-  } else {
-    if constexpr (MODE == M_NKL) {
-      stream_staged<E, MODE, K_PAIR>(trow, drow, e_begin, e_end, c, cd, ta, da, dsm, p.status);
-    } else {
-      if (kind == K_PAIR)
-        stream_staged<E, MODE, K_PAIR>(trow, drow, e_begin, e_end, c, cd, ta, da, dsm, p.status);
-      else
-        stream_staged<E, MODE, K_TSUM>(trow, drow, e_begin, e_end, c, cd, ta, da, dsm, p.status);
-    }
   }
 
-  Partial part;
-  if constexpr (VEC > 1) {
-    part = reduce_tile<BlockSync, E, VEC, SEPT, 0, ARGMAX>(kind, ta, da, c, trow - ph, cd);
-    if (PH && part.tidx != INT_MAX) part.tidx -= ph;  // from the aligned base to the row
-  } else {
-    part = reduce_tile<BlockSync, E, 1, SEPT, 32>(kind, ta, da, c, trow, cd);
-  }
+  Partial part = reduce_tile<BlockSync, E, VEC, SEPT, 0, ARGMAX>(kind, ta, da, c, trow - ph, cd, &p.x_target, p.status);
+  if (PH && part.tidx != INT_MAX) part.tidx -= ph;  // from the aligned base to the row
   if (threadIdx.x == 0) {
     float4* dst = reinterpret_cast<float4*>(p.part + tile);
-    __stcg(dst, make_float4(part.tm, part.ts, __int_as_float(part.tidx), __int_as_float(part.bad)));
-    __stcg(dst + 1, make_float4(part.dm, part.ds, part.dk, part.ds2));
+    const bool okw = in_ext(dst, sizeof(Partial), p.x_ws, p.status) && in_ext(p.cnt + b, sizeof(unsigned), p.x_ws, p.status);
+    if (okw) {
+      __stcg(dst, make_float4(part.tm, part.ts, __int_as_float(part.tidx), __int_as_float(part.bad)));
+      __stcg(dst + 1, make_float4(part.dm, part.ds, part.dk, part.ds2));
+    }
     const unsigned total = (unsigned)((gb + HB) * p.nchunks);
     // release: this tile's partial before its ticket; acquire: the other tiles' partials
     // (read with ld.cg) before this block's reads
-    const unsigned old = atom_add_acq_rel_gpu(p.cnt + b, 1u);
-    s_last = (old + 1u == total) ? 1 : 0;
+    const unsigned old = okw ? atom_add_acq_rel_gpu(p.cnt + b, 1u) : 0u;
+    s_last = (okw && old + 1u == total) ? 1 : 0;
   }
   __syncthreads();
   if (!s_last) {

@@ -206,6 +206,15 @@ __device__ __forceinline__ void block_crossing(const float* table, int n, float 
   __syncthreads();
 }
 
+// The 16-byte blocks covering row [row, row + V) lie in buffer x (bounds-checked build; the
+// mass passes and the slice re-read read nothing else of the row).
+template <typename E>
+__device__ __forceinline__ bool row_ok(const E* row, int V, const Ext& x, uint32_t* status) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(row);
+  const uintptr_t lo = a & ~(uintptr_t)15, hi = (a + (uintptr_t)V * sizeof(E) + 15) & ~(uintptr_t)15;
+  return in_ext(reinterpret_cast<const void*>(lo), (size_t)(hi - lo), x, status);
+}
+
 // Elements e0 + j outside the row [0, V) weigh nothing.
 template <int VEC>
 __device__ __forceinline__ void edge_mask(float (&ft)[VEC], float (&fd)[VEC], int e0, int V) {
@@ -429,6 +438,10 @@ __global__ void __launch_bounds__(kThreads, 4) sample2_kernel(const __grid_const
     const int k0 = (int)(u - (long long)b * nst);
     const int k1 = (int)min((long long)nst, k0 + (u1 - u));
     u += k1 - k0;
+    if (!in_ext(p.rec + b, sizeof(SeqRec), p.x_ws, p.status) ||
+        !in_ext(p.table + (size_t)b * p.table_stride, sizeof(float) * p.table_stride, p.x_ws, p.status) ||
+        !in_ext(p.cnt + b, sizeof(unsigned), p.x_ws, p.status))
+      continue;  // (uniform over the block)
     if (tid == 0) {
       int st = ld_acquire_gpu(&p.rec[b].state);
       for (int it = 0; st == REC_PENDING && it < kPollLimit; ++it) {
@@ -463,6 +476,8 @@ __global__ void __launch_bounds__(kThreads, 4) sample2_kernel(const __grid_const
     }
     const E* trow = static_cast<const E*>(p.target) + (size_t)q.t_row * V;
     const E* drow = static_cast<const E*>(p.draft) + (q.mode == S_RESID ? (size_t)q.d_row * V : 0);
+    if (!row_ok(trow, p.V, p.x_target, p.status) || (q.mode == S_RESID && !row_ok(drow, p.V, p.x_draft, p.status)))
+      continue;
     float* table = p.table + (size_t)b * p.table_stride;
     if constexpr (STAGED)
       mass_pass_staged<E, VEC>(trow, drow, q.mode, q.lt2, q.ld2, p.c, p.cd, p.V, k0, k1, table, dsm, ring, p.status);
@@ -493,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 4) sample2_kernel(const __grid_const
     const int ent = sc.ent;
     if (warp == ent % kWarps) {
       const int y = slice_token<E, VEC, STAGED, PH>(trow - ph, drow - ph, mode, q.lt2, q.ld2, p.c, p.cd, p.V, NV, ent, sc.rem, ph);
-      if (lane == 0) p.out_tok[q.t_row] = y;
+      if (lane == 0 && in_idx(q.t_row, p.total_rows, p.status)) p.out_tok[q.t_row] = y;
     }
     __syncthreads();
   }

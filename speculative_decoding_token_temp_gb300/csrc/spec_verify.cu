@@ -172,6 +172,7 @@ cudaError_t launch_prologue(const spec_batch& g, const Layout& L, char* ws, uint
   pp.cntB = reinterpret_cast<unsigned*>(ws + L.cntB);
   pp.rec = reinterpret_cast<SeqRec*>(ws + L.rec);
   pp.status = status;
+  pp.x_ws = Ext{ws, L.total};
   pp.stats = (opt && opt->stats) ? &opt->stats->slot[stats_slot(opt->stats_bucket)] : nullptr;
   pp.bucket = opt ? (long long)opt->stats_bucket : 0;
   pp.zero2 = z.ptr;
@@ -202,10 +203,10 @@ cudaError_t ensure_smem_attr(K kernel, std::atomic<unsigned long long>& done, in
   return e;
 }
 
-template <typename E, int VEC, int MODE, bool PH = false>
+template <typename E, int VEC, int MODE, bool PH = false, bool SH = false>
 cudaError_t launch_rows_t(const RowsParams& rp, long long tiles, cudaStream_t stream) {
-  auto kern = rows_kernel<E, VEC, MODE, PH>;
-  const int smem = VEC > 1 ? kRowsSmem : kStagedSmem;
+  auto kern = rows_kernel<E, VEC, MODE, PH, SH>;
+  const int smem = SH ? kShiftSmem : kRowsSmem;
   static std::atomic<unsigned long long> done{0};
   const cudaError_t e = ensure_smem_attr(kern, done, smem);
   if (e != cudaSuccess) return e;
@@ -224,10 +225,11 @@ cudaError_t launch_rows_t(const RowsParams& rp, long long tiles, cudaStream_t st
 }
 
 // The tile kernel's layout of the rows: every row on the 16-byte grid (vector tiles); rows
-// off the grid with one offset within it for both rows of every pair (phased vector
-// tiles: each tile applies its row's offset; single rows always qualify); any other
-// layout (staged tiles).
-enum RowPath { P_VEC, P_PHASED, P_STAGED };
+// off the grid with one offset within it for both rows of every pair (phased vector tiles:
+// each tile applies its row's offset; single rows always qualify); pairs whose two rows sit
+// at different offsets within the grid (phased tiles whose draft vectors are shifted to the
+// target's offset).
+enum RowPath { P_VEC, P_PHASED, P_SHIFT };
 
 template <int MODE>
 cudaError_t launch_rows(bool bf16, RowPath path, const RowsParams& rp, long long tiles, cudaStream_t stream) {
@@ -238,11 +240,11 @@ cudaError_t launch_rows(bool bf16, RowPath path, const RowsParams& rp, long long
     if (bf16) {
       if (path == P_VEC) return launch_rows_t<uint16_t, 8, MODE>(rp, tiles, stream);
       if (path == P_PHASED) return launch_rows_t<uint16_t, 8, MODE, true>(rp, tiles, stream);
-      return launch_rows_t<uint16_t, 1, MODE>(rp, tiles, stream);
+      return launch_rows_t<uint16_t, 8, MODE, true, true>(rp, tiles, stream);
     }
     if (path == P_VEC) return launch_rows_t<float, 4, MODE>(rp, tiles, stream);
     if (path == P_PHASED) return launch_rows_t<float, 4, MODE, true>(rp, tiles, stream);
-    return launch_rows_t<float, 1, MODE>(rp, tiles, stream);
+    return launch_rows_t<float, 4, MODE, true, true>(rp, tiles, stream);
   }
 }
 
@@ -366,6 +368,22 @@ cudaError_t device_geometry(Geometry* out) {
   return cudaSuccess;
 }
 
+// The buffers a call's kernels may touch, for the bounds-checked build: target rows
+// [total_draft + B, V], draft rows [total_draft, V] (absent: null), the workspace.
+struct Extents {
+  Ext target, draft, ws;
+};
+
+Extents call_extents(const spec_batch& g, spec_dtype dt, const void* target, const void* draft, const void* ws,
+                     size_t ws_bytes) {
+  const size_t es = dt == SPEC_BF16 ? 2 : 4, V = (size_t)g.V;
+  Extents x;
+  x.target = Ext{target, target ? ((size_t)g.total_draft + (size_t)g.B) * V * es : 0};
+  x.draft = Ext{draft, draft ? (size_t)g.total_draft * V * es : 0};
+  x.ws = Ext{ws, ws_bytes};
+  return x;
+}
+
 RowsParams base_params(const spec_batch& g, const Layout& L, char* ws, uint32_t* status) {
   RowsParams rp;
   memset(&rp, 0, sizeof(rp));
@@ -383,6 +401,8 @@ RowsParams base_params(const spec_batch& g, const Layout& L, char* ws, uint32_t*
   rp.cnt = reinterpret_cast<unsigned*>(ws + L.cntA);
   rp.rec = reinterpret_cast<SeqRec*>(ws + L.rec);
   rp.inv_lnV = g.V > 1 ? (float)(1.0 / log((double)g.V)) : 0.f;
+  rp.x_ws = Ext{ws, L.total};
+  rp.out_rows = (int)L.rows;
   return rp;
 }
 
@@ -398,7 +418,7 @@ RowPath row_path(spec_dtype dt, int V, const void* a, const void* b) {
   if (b == nullptr) return P_PHASED;
   const int es = dt == SPEC_BF16 ? 2 : 4;
   if (((long long)V * es) % 16 == 0 && (((uintptr_t)a ^ (uintptr_t)b) & 15u) == 0) return P_PHASED;
-  return P_STAGED;
+  return P_SHIFT;
 }
 
 bool temperature_ok(float T) { return isfinite(T) && T > 0.f; }
@@ -479,6 +499,9 @@ spec_status stochastic_impl(spec_batch g, spec_dtype dtype, const void* target_l
   RowsParams rp = base_params(g, L, ws, device_status);
   rp.target = target_logits;
   rp.draft = draft_logits;
+  const Extents xs = call_extents(g, dtype, target_logits, draft_logits, workspace, L.total);
+  rp.x_target = xs.target;
+  rp.x_draft = xs.draft;
   rp.tokens = draft_tokens;
   rp.u_accept = u_accept;
   rp.u_sample = u_sample;
@@ -509,6 +532,9 @@ spec_status stochastic_impl(spec_batch g, spec_dtype dtype, const void* target_l
   memset(&sp, 0, sizeof(sp));
   sp.target = target_logits;
   sp.draft = draft_logits;
+  sp.x_target = xs.target;
+  sp.x_draft = xs.draft;
+  sp.x_ws = xs.ws;
   sp.V = g.V;
   sp.total_rows = (int)L.rows;
   sp.total_draft = g.total_draft;
@@ -570,6 +596,7 @@ spec_status greedy_impl(spec_batch g, spec_dtype dtype, const void* target_logit
   if (launch_prologue(g, L, ws, device_status, stream, options, zr) != cudaSuccess) return SPEC_ERR_CUDA;
   RowsParams rp = base_params(g, L, ws, device_status);
   rp.target = target_logits;
+  rp.x_target = call_extents(g, dtype, target_logits, nullptr, workspace, L.total).target;
   rp.tokens = draft_tokens;
   rp.n_acc = n_accepted;
   rp.out_tok = out_tokens;
@@ -577,6 +604,7 @@ spec_status greedy_impl(spec_batch g, spec_dtype dtype, const void* target_logit
   apply_options(rp, options, SPEC_MODE_GREEDY);
   if (mt) {
     rp.draft = mt->pp.draft;  // the fused tiles also read the draft rows (for the matrix)
+    rp.x_draft = mt->pp.x_draft;
     if (launch_multi<M_GREEDY>(dtype == SPEC_BF16, *mt, rp, (long long)(g.B / mt->K) * (g.gamma + 1) * L.nchunks,
                                stream) != cudaSuccess)
       return SPEC_ERR_CUDA;
@@ -785,6 +813,7 @@ spec_status spec_verify_tree(int32_t B, int32_t N, int32_t V, spec_dtype dtype, 
   if (launch_prologue(g, L, ws, device_status, stream) != cudaSuccess) return SPEC_ERR_CUDA;
   RowsParams rp = base_params(g, L, ws, device_status);
   rp.target = target_logits;
+  rp.x_target = call_extents(g, dtype, target_logits, nullptr, workspace, L.total).target;
   rp.node_tokens = node_tokens;
   rp.N = N;
   rp.depth = D;
@@ -830,6 +859,9 @@ spec_status spec_nkl_ex(spec_batch g, spec_dtype dtype, const void* target_logit
   RowsParams rp = base_params(g, L, ws, device_status);
   rp.target = target_logits;
   rp.draft = draft_logits;
+  const Extents xs = call_extents(g, dtype, target_logits, draft_logits, workspace, L.total);
+  rp.x_target = xs.target;
+  rp.x_draft = xs.draft;
   rp.c = rp.cd = (float)(1.4426950408889634 / (double)temperature);
   rp.invT = (float)(1.0 / (double)temperature);
   rp.delta = delta;
@@ -897,6 +929,8 @@ spec_status spec_verify_multi(spec_multi_batch m, spec_dtype dtype, int32_t stoc
   pp.cons = consensus;
   pp.div = divergence;
   pp.status = device_status;
+  pp.x_draft = call_extents(multi_as_batch(m), dtype, nullptr, draft_logits, workspace, ML.total).draft;
+  pp.x_ws = Ext{workspace, ML.total};
   // aligned rows: fused (group, row, chunk) tiles read every logit once and fill the
   // matrix on the way; otherwise the batch kernels, then a second pass over the drafts
   const bool fused = m.gamma > 0 && vec_path(dtype, m.V, target_logits, draft_logits);
@@ -987,6 +1021,7 @@ spec_status spec_selftest_wait_timeout(uint32_t* device_status, void* workspace,
   sp.table = reinterpret_cast<float*>(ws + L.table);
   sp.table_stride = L.table_stride;
   sp.tiles_done = reinterpret_cast<const unsigned*>(ws + L.cntA) + g.B;  // zeroed by the prologue, never counted
+  sp.x_ws = Ext{workspace, L.total};
   sp.ntiles = 1u;
   sp.head_total = 0;
   sp.nb_head = 0;

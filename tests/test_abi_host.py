@@ -22,6 +22,15 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(_lib.SIGNATURES) >= set(names)
 
 
+def test_bounds_checked_variant_exports_the_same_symbols(lib):
+    """The debug build (every computed access checked against its buffer) has the same ABI."""
+    checked = _lib.bounds_lib()
+    for n in _lib.declared_functions():
+        assert hasattr(checked, n), n
+    assert _lib.SPEC_DEV_BOUNDS not in (_lib.SPEC_DEV_TOKEN_RANGE, _lib.SPEC_DEV_NONFINITE, _lib.SPEC_DEV_OFFSETS,
+                                        _lib.SPEC_DEV_TIMEOUT, _lib.SPEC_DEV_POSITION)
+
+
 def test_status_strings(lib):
     assert lib.spec_status_str(0) == b"ok"
     assert b"workspace" in lib.spec_status_str(3)
