@@ -708,18 +708,47 @@ def main():
                     help="shift the timed call's logits by N elements (N not a multiple of 8: the phased path)")
     ap.add_argument("--batch", type=int, default=None,
                     help="sequences per step (default: the workload's 256); smaller slices serve profiling")
+    ap.add_argument("--tree", action="store_true",
+                    help="time only the tree call (B=32, 12 nodes, V=128256, bf16): back-to-back and with L2 flushed "
+                         "before every call; a secondary line for profiling, not the headline metric")
     ap.add_argument("--multi", type=int, default=None, metavar="G",
                     help="time only the multi-draft call on G groups of 3 candidates (gamma 8, V 128256, bf16): "
                          "a secondary line for profiling, not the headline metric")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.multi is not None:
+    if args.tree:
+        run_tree_only(args)
+    elif args.multi is not None:
         run_multi_only(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
+
+
+def run_tree_only(args):
+    """spec_verify_tree on the 12-node tree workload (B=32, V=128256, bf16): per-call device
+    time back to back (the rows stay mostly in L2) and cold (L2 flushed before every call),
+    with GB/s of the target rows."""
+    import torch
+
+    import __graft_entry__
+    from speculative_decoding_token_temp_gb300 import api, synth
+    __graft_entry__.build()
+    dev = torch.device("cuda:0")
+    tw = synth.TREE.make()
+    tt, tn = _to_dev(tw.target, dev), _to_dev(tw.node_tokens, dev)
+    out = {}
+    fn = lambda: api.spec_verify_tree(tt, tn, list(tw.parent), out=out)  # noqa: E731
+    warm = time_mode(fn, args.steps, args.warmup, dev)
+    cold, c10, c90 = time_cold(fn, max(args.steps, 10), args.warmup, dev)
+    hbm, _ = peaks()
+    print(json.dumps({"metric": "tree_us_per_call", "value": cold * 1e6, "unit": "us", "warm_us": warm * 1e6,
+                      "cold_p10_us": c10 * 1e6, "cold_p90_us": c90 * 1e6,
+                      "cold_frac_of_peak": tw.target.nbytes / cold / 1e9 / hbm,
+                      "status": int(out["device_status"][0]),
+                      "config": {"workload": "tree B=32 N=12 V=128256 bf16"}}))
 
 
 def run_multi_only(args):

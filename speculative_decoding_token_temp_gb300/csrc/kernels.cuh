@@ -340,29 +340,23 @@ struct IO<float, 4> {
   }
 };
 
-// Elements S .. S + VEC - 1 of the 2 VEC elements held by the aligned vector a and the one
-// after it, b: a row's vector at another phase within the 16-byte grid. bf16: 32-bit words
-// of two elements, whole words for even S, a byte permutation of two words for odd S;
-// fp32: whole words.
-template <typename E, int S>
-__device__ __forceinline__ uint4 shift_vec(const uint4& a, const uint4& b) {
+// Elements s .. s + VEC - 1 of the 2 VEC elements held by the aligned vector a and the one
+// after it, b: a row's vector at another phase within the 16-byte grid. The shift is split
+// into M whole 32-bit words (a template argument) and, for bf16, a half word applied by a
+// byte permutation with the uniform selector sel (0x3210: none, 0x5432: the high element of
+// one word, then the low element of the next).
+template <typename E, int M>
+__device__ __forceinline__ uint4 shift_vec(const uint4& a, const uint4& b, unsigned sel) {
   const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-  uint4 r;
   if constexpr (sizeof(E) == 2) {
-    static_assert(S > 0 && S < 8, "a shift within one bf16 vector");
-    constexpr int m = S / 2;
-    if constexpr (S % 2 == 0) {
-      r = make_uint4(w[m], w[m + 1], w[m + 2], w[m + 3]);
-    } else {
-      // the high element of word m + i, then the low element of word m + i + 1
-      r = make_uint4(__byte_perm(w[m], w[m + 1], 0x5432), __byte_perm(w[m + 1], w[m + 2], 0x5432),
-                     __byte_perm(w[m + 2], w[m + 3], 0x5432), __byte_perm(w[m + 3], w[m + 4], 0x5432));
-    }
+    static_assert(M >= 0 && M < 4, "a shift within one bf16 vector");
+    return make_uint4(__byte_perm(w[M], w[M + 1], sel), __byte_perm(w[M + 1], w[M + 2], sel),
+                      __byte_perm(w[M + 2], w[M + 3], sel), __byte_perm(w[M + 3], w[M + 4], sel));
   } else {
-    static_assert(S > 0 && S < 4, "a shift within one fp32 vector");
-    r = make_uint4(w[S], w[S + 1], w[S + 2], w[S + 3]);
+    static_assert(M > 0 && M < 4, "a shift within one fp32 vector");
+    (void)sel;
+    return make_uint4(w[M], w[M + 1], w[M + 2], w[M + 3]);
   }
-  return r;
 }
 
 template <typename E>

@@ -519,16 +519,18 @@ __device__ __forceinline__ void stream_tile(const E* trow, const E* drow, int v0
 // whose row is not a whole number of 16-byte blocks): the stream of stream_tile over the
 // target's aligned vectors v in [v0, v1), and for each the draft's elements at the same
 // row indices, which lie in the draft's aligned vectors w = v + dw and w + 1, shifted by S
-// elements (dw * VEC + S = the draft's offset minus the target's, 0 < S < VEC). Each lane
+// elements (dw * VEC + S = the draft's offset minus the target's, 0 < S < VEC; M whole
+// words and the half-word permutation sel). Each lane
 // copies its own w; after a warp barrier it takes w + 1 from the next lane's slot, and lane
 // 31 copies its w + 1 itself into a small ring of its own (kShiftXSlot bytes per stage
 // after the main ring). Lanes one vector past the end still copy their draft vector (the
 // lane before needs it as its w + 1): it holds the last element of the last whole target
 // vector, so it lies in the row. Two warp barriers per stage: before a slot is refilled
 // (every lane has read it) and after the copies land (they are visible to the warp).
-template <typename E, int VEC, int MODE, int S>
-__device__ __forceinline__ void stream_tile_sh(const E* trv, const E* drv, int v0, int v1, int dw, float c, float cd,
-                                               TAcc& ta, DAcc& da, unsigned char* smem, const RowsParams& p) {
+template <typename E, int VEC, int MODE, int M>
+__device__ __forceinline__ void stream_tile_sh(const E* trv, const E* drv, int v0, int v1, int dw, unsigned sel,
+                                               float c, float cd, TAcc& ta, DAcc& da, unsigned char* smem,
+                                               const RowsParams& p) {
   constexpr bool IDX = is_stoch(MODE), SEPT = MODE == M_STOCH2;
   constexpr int PER = 2 * kThreads;            // vectors of a row per stage
   constexpr unsigned SLOT = kCV * kThreads * 16;
@@ -573,39 +575,38 @@ __device__ __forceinline__ void stream_tile_sh(const E* trv, const E* drv, int v
       unpack2<E, VEC>(q[0], q[kThreads], ft);
       const uint4 n0 = lane < 31 ? q[2 * kThreads + 1] : qx[0];
       const uint4 n1 = lane < 31 ? q[3 * kThreads + 1] : qx[1];
-      unpack2<E, VEC>(shift_vec<E, S>(q[2 * kThreads], n0), shift_vec<E, S>(q[3 * kThreads], n1), fd);
+      unpack2<E, VEC>(shift_vec<E, M>(q[2 * kThreads], n0, sel), shift_vec<E, M>(q[3 * kThreads], n1, sel), fd);
       pair_update<2 * VEC, IDX, VEC, SEPT>(ta, da, ft, fd, va * VEC, c, vb * VEC, cd);
     } else if (va < v1) {
       float ft[VEC], fd[VEC];
       IO<E, VEC>::unpack(q[0], ft);
       const uint4 n0 = lane < 31 ? q[2 * kThreads + 1] : qx[0];
-      IO<E, VEC>::unpack(shift_vec<E, S>(q[2 * kThreads], n0), fd);
+      IO<E, VEC>::unpack(shift_vec<E, M>(q[2 * kThreads], n0, sel), fd);
       pair_update<VEC, IDX, VEC, SEPT>(ta, da, ft, fd, va * VEC, c, 0, cd);
     }
   }
   cp_wait<0>();
 }
 
-// The shifted stream for the tile's shift s (0 < s < VEC), one instance per shift.
+// The shifted stream for the tile's shift s (0 < s < VEC): one instance per whole-word part
+// of the shift (four for bf16, three for fp32), the half word a uniform runtime selector.
 template <typename E, int VEC, int MODE>
 __device__ __forceinline__ void stream_tile_shifted(int s, const E* trv, const E* drv, int v0, int v1, int dw, float c,
                                                     float cd, TAcc& ta, DAcc& da, unsigned char* smem,
                                                     const RowsParams& p) {
   if constexpr (VEC == 8) {
-    switch (s) {
-      case 1: stream_tile_sh<E, VEC, MODE, 1>(trv, drv, v0, v1, dw, c, cd, ta, da, smem, p); break;
-      case 2: stream_tile_sh<E, VEC, MODE, 2>(trv, drv, v0, v1, dw, c, cd, ta, da, smem, p); break;
-      case 3: stream_tile_sh<E, VEC, MODE, 3>(trv, drv, v0, v1, dw, c, cd, ta, da, smem, p); break;
-      case 4: stream_tile_sh<E, VEC, MODE, 4>(trv, drv, v0, v1, dw, c, cd, ta, da, smem, p); break;
-      case 5: stream_tile_sh<E, VEC, MODE, 5>(trv, drv, v0, v1, dw, c, cd, ta, da, smem, p); break;
-      case 6: stream_tile_sh<E, VEC, MODE, 6>(trv, drv, v0, v1, dw, c, cd, ta, da, smem, p); break;
-      default: stream_tile_sh<E, VEC, MODE, 7>(trv, drv, v0, v1, dw, c, cd, ta, da, smem, p); break;
+    const unsigned sel = (s & 1) ? 0x5432u : 0x3210u;
+    switch (s >> 1) {
+      case 0: stream_tile_sh<E, VEC, MODE, 0>(trv, drv, v0, v1, dw, sel, c, cd, ta, da, smem, p); break;
+      case 1: stream_tile_sh<E, VEC, MODE, 1>(trv, drv, v0, v1, dw, sel, c, cd, ta, da, smem, p); break;
+      case 2: stream_tile_sh<E, VEC, MODE, 2>(trv, drv, v0, v1, dw, sel, c, cd, ta, da, smem, p); break;
+      default: stream_tile_sh<E, VEC, MODE, 3>(trv, drv, v0, v1, dw, sel, c, cd, ta, da, smem, p); break;
     }
   } else {
     switch (s) {
-      case 1: stream_tile_sh<E, VEC, MODE, 1>(trv, drv, v0, v1, dw, c, cd, ta, da, smem, p); break;
-      case 2: stream_tile_sh<E, VEC, MODE, 2>(trv, drv, v0, v1, dw, c, cd, ta, da, smem, p); break;
-      default: stream_tile_sh<E, VEC, MODE, 3>(trv, drv, v0, v1, dw, c, cd, ta, da, smem, p); break;
+      case 1: stream_tile_sh<E, VEC, MODE, 1>(trv, drv, v0, v1, dw, 0u, c, cd, ta, da, smem, p); break;
+      case 2: stream_tile_sh<E, VEC, MODE, 2>(trv, drv, v0, v1, dw, 0u, c, cd, ta, da, smem, p); break;
+      default: stream_tile_sh<E, VEC, MODE, 3>(trv, drv, v0, v1, dw, 0u, c, cd, ta, da, smem, p); break;
     }
   }
 }
@@ -694,29 +695,28 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
     // v + dw + 1, from element sft on
     const int sft = (phd - ph + VEC) % VEC, dw = (phd - ph - sft) / VEC;
     const int vf0 = (e_begin + ph + VEC - 1) / VEC, vf1 = (e_end + ph) / VEC;
-    __shared__ uint4 s_edge[2][3];  // [head, tail][target, draft, next draft]
-    // thread 0 takes the head, thread 1 the tail (the bounds are recomputed after the
-    // stream, so that none of them is held through it)
-    auto edge_range = [&](int& elo, int& ehi) {
+    // The partial blocks at the chunk's ends, head [e_begin, hend) and tail [tbeg, e_end),
+    // fewer than VEC elements each: element j of the head is thread j's, element j of the
+    // tail thread VEC + j's; each copies the target block and the draft block holding its
+    // element beside the ring and folds the element in after the stream.
+    __shared__ uint4 s_edge[2 * VEC][2];  // [thread][target, draft]
+    // this thread's edge element, or -1 (recomputed after the stream, so that it is not held
+    // through it)
+    auto edge_elem = [&]() -> int {
+      if (threadIdx.x >= 2 * VEC) return -1;
+      const int side = threadIdx.x / VEC;
       const int hend = min(e_end, vf0 * VEC - ph), tbeg = max(hend, vf1 * VEC - ph);
-      elo = threadIdx.x == 0 ? e_begin : tbeg;
-      ehi = threadIdx.x == 0 ? hend : e_end;
+      const int e = (side == 0 ? e_begin : tbeg) + (int)(threadIdx.x % VEC);
+      return e < (side == 0 ? hend : e_end) ? e : -1;
     };
-    if (PH && threadIdx.x < 2) {
-      int elo, ehi;
-      edge_range(elo, ehi);
-      if (elo < ehi) {
-        const size_t eb = (size_t)((elo + ph) / VEC) * VEC;
-        if (in_ext(trv + eb, 16, p.x_target, p.status))
-          cp_async16((uint32_t)__cvta_generic_to_shared(&s_edge[threadIdx.x][0]), trv + eb);
-        if (kind == K_PAIR) {
-          // the draft blocks holding elements elo and ehi - 1 (one block at equal phases)
-          const int w0 = (elo + phd) / VEC, w1 = (ehi - 1 + phd) / VEC;
-          if (in_ext(drv + (size_t)w0 * VEC, 16, p.x_draft, p.status))
-            cp_async16((uint32_t)__cvta_generic_to_shared(&s_edge[threadIdx.x][1]), drv + (size_t)w0 * VEC);
-          if (w1 > w0 && in_ext(drv + (size_t)w1 * VEC, 16, p.x_draft, p.status))
-            cp_async16((uint32_t)__cvta_generic_to_shared(&s_edge[threadIdx.x][2]), drv + (size_t)w1 * VEC);
-        }
+    if (PH) {
+      const int e = edge_elem();
+      if (e >= 0) {
+        const size_t tb = (size_t)((e + ph) / VEC) * VEC, db = (size_t)((e + phd) / VEC) * VEC;
+        if (in_ext(trv + tb, 16, p.x_target, p.status))
+          cp_async16((uint32_t)__cvta_generic_to_shared(&s_edge[threadIdx.x][0]), trv + tb);
+        if (kind == K_PAIR && in_ext(drv + db, 16, p.x_draft, p.status))
+          cp_async16((uint32_t)__cvta_generic_to_shared(&s_edge[threadIdx.x][1]), drv + db);
       }
     }
     // (stream_tile's last wait covers the edge copies too)
@@ -742,46 +742,34 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
         stream_tile<E, VEC, MODE, K_TSUM>(trv, drv, vf0, vf1, c, cd, ta, da, dsm, best, p);
       }
     }
-    int elo = 0, ehi = 0;
-    if (PH && threadIdx.x < 2) edge_range(elo, ehi);
-    if (PH && elo < ehi) {
-      float ft[VEC];
-      IO<E, VEC>::unpack(s_edge[threadIdx.x][0], ft);
-      // the draft element of row index e sits at e + phd - w0 * VEC in the two draft blocks
-      const E* dsh = reinterpret_cast<const E*>(&s_edge[threadIdx.x][1]);
-      const int dbase = ((elo + phd) / VEC) * VEC - phd;
-      const int e0 = ((elo + ph) / VEC) * VEC - ph;  // row index of ft[0]
-#pragma unroll
-      for (int j = 0; j < VEC; ++j) {
-        const int e = e0 + j;
-        if (e < elo || e >= ehi) continue;
-        const float x = ft[j];
-        if constexpr (ARGMAX) {
-          ta.hi = max_nan(ta.hi, x);
-          ta.lo = fminf(ta.lo, x);
+    const int e = PH ? edge_elem() : -1;
+    if (e >= 0) {
+      const float x = sh_elem<E>(reinterpret_cast<const E*>(&s_edge[threadIdx.x][0]), (e + ph) % VEC);
+      if constexpr (ARGMAX) {
+        ta.hi = max_nan(ta.hi, x);
+        ta.lo = fminf(ta.lo, x);
+      } else {
+        // the sums; the maximum and its index are kept apart (the recorded group stays
+        // the one that holds the thread's maximum over whole vectors)
+        const float m0 = ta.m;
+        const int g0 = ta.g0, g1 = ta.g1;
+        const float xt[1] = {x};
+        if (kind == K_PAIR) {
+          const float xd[1] = {sh_elem<E>(reinterpret_cast<const E*>(&s_edge[threadIdx.x][1]), (e + phd) % VEC)};
+          pair_update<1, false, 0, SEPT>(ta, da, xt, xd, 0, c, 0, cd);
         } else {
-          // the sums; the maximum and its index are kept apart (the recorded group
-          // stays the one that holds the thread's maximum over whole vectors)
-          const float m0 = ta.m;
-          const int g0 = ta.g0, g1 = ta.g1;
-          const float xt[1] = {x};
-          if (kind == K_PAIR) {
-            const float xd[1] = {sh_elem<E>(dsh, e - dbase)};
-            pair_update<1, false, 0, SEPT>(ta, da, xt, xd, 0, c, 0, cd);
-          } else {
-            tsum_update<1, 0>(ta, xt, 0, c);
-          }
-          ta.m = m0;
-          ta.g0 = g0;
-          ta.g1 = g1;
+          tsum_update<1, 0>(ta, xt, 0, c);
         }
-        // an edge element holding the thread's maximum carries its exact index (the head
-        // block precedes every whole vector of the chunk: it wins ties)
-        if (x > ta.m || (x == ta.m && ta.g0 >= 0 && e + ph < ta.g0)) {
-          ta.m = x;
-          ta.g0 = e + ph;
-          if constexpr (!ARGMAX) ta.g1 = kExactIdx;
-        }
+        ta.m = m0;
+        ta.g0 = g0;
+        ta.g1 = g1;
+      }
+      // an edge element holding the thread's maximum carries its exact index (a head
+      // element precedes every whole vector of the chunk: it wins ties)
+      if (x > ta.m || (x == ta.m && ta.g0 >= 0 && e + ph < ta.g0)) {
+        ta.m = x;
+        ta.g0 = e + ph;
+        if constexpr (!ARGMAX) ta.g1 = kExactIdx;
       }
     }
   }
