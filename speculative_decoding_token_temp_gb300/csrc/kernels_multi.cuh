@@ -489,21 +489,31 @@ __device__ __forceinline__ void multi_pair_stage(const uint4* sq, int e0, float 
   }
 }
 
-// The stream and the partials of one fused tile: (group g, row r, chunk) of a draft
-// position (PAIR: the K target rows and the K draft rows) or of the bonus row (the K target
-// rows). PAIR is a template argument so that each kind keeps only its own accumulators.
-// The candidates' rows are addressed from one base and a row stride.
-template <typename E, int VEC, int K, int MODE, bool PAIR>
-__device__ __forceinline__ void multi_tile(const RowsParams& p, const PairParams& q, int g, int r, int chunk,
-                                           unsigned char* dsm) {
+template <typename E, int VEC, int K, int MODE>
+__global__ void __launch_bounds__(kThreads, 2) multi_rows_kernel(const __grid_constant__ RowsParams p,
+                                                                 const __grid_constant__ PairParams q) {
   using io = IO<E, VEC>;
   constexpr bool STOCH = MODE == M_STOCH;
   constexpr int kMS = multi_stages<K>();
+  extern __shared__ __align__(128) unsigned char dsm[];
+  griddep_wait();  // the prologue, and everything earlier on the stream, has completed
+  griddep_launch();
+  __shared__ int s_last[K + 1];
   const int gamma = p.gamma, nchunks = p.nchunks;
+  const int per = (gamma + 1) * nchunks;
+  const int tile = blockIdx.x;
+  const int g = tile / per, rem = tile - g * per;
+  const int r = rem / nchunks, chunk = rem - r * nchunks;
+  const bool pair = r < gamma;
   const size_t V = (size_t)p.V;
-  const E* tbase = static_cast<const E*>(p.target) + ((size_t)g * K * (gamma + 1) + r) * V;
-  const E* dbase = PAIR ? static_cast<const E*>(p.draft) + ((size_t)g * K * gamma + r) * V : tbase;
-  const size_t tstride = (size_t)(gamma + 1) * V, dstride = (size_t)gamma * V;
+  const E* trow[K];
+  const E* drow[K];
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    const size_t b = (size_t)g * K + k;
+    trow[k] = static_cast<const E*>(p.target) + (b * (gamma + 1) + r) * V;
+    drow[k] = pair ? static_cast<const E*>(p.draft) + (b * gamma + r) * V : trow[k];
+  }
   const int e_begin = chunk * p.chunk_elems;
   const int e_end = min(e_begin + p.chunk_elems, p.V);
   const int v0 = e_begin / VEC, v1 = e_end / VEC;
@@ -522,19 +532,20 @@ __device__ __forceinline__ void multi_tile(const RowsParams& p, const PairParams
   }
 
   constexpr unsigned SLOT = 2 * K * kThreads * 16;
-  constexpr int NR = PAIR ? 2 * K : K;
   const int t = threadIdx.x;
   const uint32_t base = (uint32_t)__cvta_generic_to_shared(dsm) + 16u * t;
   const int nst = (v1 - v0 + kThreads - 1) / kThreads;
+  const int nr = pair ? 2 * K : K;
   auto issue = [&](int st) {
     if (st < nst) {
       const int v = v0 + t + st * kThreads;
       if (v < v1) {
         const uint32_t slot = base + (uint32_t)(st % kMS) * SLOT;
 #pragma unroll
-        for (int j = 0; j < NR; ++j) {
-          const E* src = (j < K ? tbase + j * tstride : dbase + (j - K) * dstride) + (size_t)v * VEC;
-          if (in_ext(src, 16, j < K ? p.x_target : p.x_draft, p.status)) cp_async16(slot + (uint32_t)(j * kThreads * 16), src);
+        for (int j = 0; j < 2 * K; ++j) {
+          const E* src = (j < K ? trow[j] : drow[j - K]) + (size_t)v * VEC;
+          if (j < nr && in_ext(src, 16, j < K ? p.x_target : p.x_draft, p.status))
+            cp_async16(slot + (uint32_t)(j * kThreads * 16), src);
         }
       }
     }
@@ -549,26 +560,41 @@ __device__ __forceinline__ void multi_tile(const RowsParams& p, const PairParams
     if (v >= v1) continue;
     const uint4* sq = reinterpret_cast<const uint4*>(dsm + (size_t)(st % kMS) * SLOT) + t;
     const int e0 = v * VEC;
-    if constexpr (PAIR && K <= 3) {
-      multi_pair_stage<E, VEC, K, STOCH>(sq, e0, c, cq, ta, da, kk);
-    } else if constexpr (PAIR) {
-      // K = 4: every candidate's draft vectors held at once would spill; they are
-      // unpacked per use
+    if constexpr (K <= 3) {
+      if (pair) {
+        multi_pair_stage<E, VEC, K, STOCH>(sq, e0, c, cq, ta, da, kk);
+        continue;
+      }
+    }
+    // K = 4 pairs (every candidate's draft vectors held at once would spill: they are
+    // unpacked per use) and the bonus row of every K
+    constexpr bool PRE = K <= 3;
+    float fdk[PRE ? K : 1][VEC];
+    if (PRE && pair) {
 #pragma unroll
-      for (int a = 0; a < K; ++a) {
-        float ft[VEC];
-        io::unpack(sq[a * kThreads], ft);
-        if constexpr (STOCH) {
-          const float vm = vmax<VEC>(ft);
-          track_max<VEC, VEC, true>(ta[a], ft, vm, e0, 0);
-          lazy_ref(ta[a].mr, ta[a].mth, ta[a].nmc, ta[a].s, nullptr, vm, c);
-          float et[VEC];
-          ta[a].s = add2(ta[a].s, exp_sum2<VEC>(ft, c, ta[a].nmc, et));
-        } else {
-          argmax_update<VEC>(ta[a], ft, e0);
-        }
-        float fd[VEC], ed[VEC];
-        io::unpack(sq[(K + a) * kThreads], fd);
+      for (int a = 0; a < (PRE ? K : 0); ++a) io::unpack(sq[(K + a) * kThreads], fdk[a]);
+    }
+#pragma unroll
+    for (int a = 0; a < K; ++a) {
+      float ft[VEC];
+      io::unpack(sq[a * kThreads], ft);
+      if (!pair || !STOCH) {
+        if (STOCH)
+          tsum_update<VEC>(ta[a], ft, e0, c);  // the stochastic bonus row
+        else
+          argmax_update<VEC>(ta[a], ft, e0);   // greedy rows
+      } else {
+        const float vm = vmax<VEC>(ft);
+        track_max<VEC, VEC, true>(ta[a], ft, vm, e0, 0);
+        lazy_ref(ta[a].mr, ta[a].mth, ta[a].nmc, ta[a].s, nullptr, vm, c);
+        float et[VEC];
+        ta[a].s = add2(ta[a].s, exp_sum2<VEC>(ft, c, ta[a].nmc, et));
+      }
+      if (pair) {
+        float fdu[VEC];
+        if constexpr (!PRE) io::unpack(sq[(K + a) * kThreads], fdu);
+        const float (&fd)[VEC] = PRE ? fdk[PRE ? a : 0] : fdu;
+        float ed[VEC];
         const float vm = vmax<VEC>(fd);
         const bool mv = vm > da[a].mth;
         if (__any_sync(__activemask(), mv)) {
@@ -588,32 +614,24 @@ __device__ __forceinline__ void multi_tile(const RowsParams& p, const PairParams
 #pragma unroll
         for (int b = 0; b < K; ++b) {
           if (b == a) continue;
-          float fb[VEC];
-          io::unpack(sq[(K + b) * kThreads], fb);
-          kk[a][b] += dot_diff<VEC>(ed, fd, fb);
+          if constexpr (PRE) {
+            kk[a][b] += dot_diff<VEC>(ed, fd, fdk[b]);
+          } else {
+            float fb[VEC];
+            io::unpack(sq[(K + b) * kThreads], fb);
+            kk[a][b] += dot_diff<VEC>(ed, fd, fb);
+          }
         }
-      }
-    } else {
-      // the bonus row: stochastic sums, greedy argmax
-#pragma unroll
-      for (int a = 0; a < K; ++a) {
-        float ft[VEC];
-        io::unpack(sq[a * kThreads], ft);
-        if constexpr (STOCH)
-          tsum_update<VEC>(ta[a], ft, e0, c);
-        else
-          argmax_update<VEC>(ta[a], ft, e0);
       }
     }
   }
   cp_wait<0>();
 
   // partials: one per candidate in the tile kernel's layout, one pairwise partial
-  constexpr int kind = PAIR ? (STOCH ? K_PAIR : K_ARGMAX) : (STOCH ? K_TSUM : K_ARGMAX);
+  const int kind = pair ? (STOCH ? K_PAIR : K_ARGMAX) : (STOCH ? K_TSUM : K_ARGMAX);
 #pragma unroll
   for (int a = 0; a < K; ++a) {
-    const Partial part = reduce_tile<BlockSync, E, VEC>(kind, ta[a], da[a], c, tbase + a * tstride, 0.f, &p.x_target,
-                                                        p.status);
+    const Partial part = reduce_tile<BlockSync, E, VEC>(kind, ta[a], da[a], c, trow[a], 0.f, &p.x_target, p.status);
     const size_t row = ((size_t)g * K + a) * (gamma + 1) + r;
     float4* dst = reinterpret_cast<float4*>(p.part + row * nchunks + chunk);
     if (threadIdx.x == 0 && in_ext(dst, sizeof(Partial), p.x_ws, p.status)) {
@@ -622,7 +640,7 @@ __device__ __forceinline__ void multi_tile(const RowsParams& p, const PairParams
     }
     __syncthreads();  // reduce_tile's shared arrays are reused by the next candidate
   }
-  if constexpr (PAIR) {
+  if (pair) {
     float mr[K], sm[K];
 #pragma unroll
     for (int a = 0; a < K; ++a) {
@@ -631,26 +649,6 @@ __device__ __forceinline__ void multi_tile(const RowsParams& p, const PairParams
     }
     pair_partial_write<K>(q.part + ((size_t)g * gamma + r) * nchunks + chunk, mr, sm, kk, cq, q);
   }
-}
-
-template <typename E, int VEC, int K, int MODE>
-__global__ void __launch_bounds__(kThreads, 2) multi_rows_kernel(const __grid_constant__ RowsParams p,
-                                                                 const __grid_constant__ PairParams q) {
-  constexpr bool STOCH = MODE == M_STOCH;
-  extern __shared__ __align__(128) unsigned char dsm[];
-  griddep_wait();  // the prologue, and everything earlier on the stream, has completed
-  griddep_launch();
-  __shared__ int s_last[K + 1];
-  const int gamma = p.gamma, nchunks = p.nchunks;
-  const int per = (gamma + 1) * nchunks;
-  const int tile = blockIdx.x;
-  const int g = tile / per, rem = tile - g * per;
-  const int r = rem / nchunks, chunk = rem - r * nchunks;
-  const bool pair = r < gamma;
-  if (pair)
-    multi_tile<E, VEC, K, MODE, true>(p, q, g, r, chunk, dsm);
-  else
-    multi_tile<E, VEC, K, MODE, false>(p, q, g, r, chunk, dsm);
   __syncthreads();  // every writer's partial entries precede thread 0's fence
   if (threadIdx.x == 0) {
     __threadfence();
