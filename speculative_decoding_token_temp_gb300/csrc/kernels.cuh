@@ -359,6 +359,27 @@ __device__ __forceinline__ uint4 shift_vec(const uint4& a, const uint4& b, unsig
   }
 }
 
+// shift_vec with the whole shift s (0 < s < VEC) a runtime value: the whole words by two
+// select stages (2 words, then 1), the half word (bf16) by the byte permutation. One code
+// path for every shift, at a dozen more instructions per vector than the template.
+template <typename E>
+__device__ __forceinline__ uint4 shift_vec_rt(const uint4& a, const uint4& b, int s) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  const int m = sizeof(E) == 2 ? (s >> 1) : s;
+  uint32_t u[6], v[5];
+#pragma unroll
+  for (int i = 0; i < 6; ++i) u[i] = (m & 2) ? w[i + 2] : w[i];
+#pragma unroll
+  for (int i = 0; i < 5; ++i) v[i] = (m & 1) ? u[i + 1] : u[i];
+  if constexpr (sizeof(E) == 2) {
+    const unsigned sel = (s & 1) ? 0x5432u : 0x3210u;
+    return make_uint4(__byte_perm(v[0], v[1], sel), __byte_perm(v[1], v[2], sel), __byte_perm(v[2], v[3], sel),
+                      __byte_perm(v[3], v[4], sel));
+  } else {
+    return make_uint4(v[0], v[1], v[2], v[3]);
+  }
+}
+
 template <typename E>
 __device__ __forceinline__ float elem_at(const E* row, int x);
 template <>
@@ -384,7 +405,6 @@ constexpr int kStageRowBytes = 8192;                      // one row of a pair i
 constexpr int kWarpRowBytes = kStageRowBytes / kWarps;    // a warp's run of a row of a pair in one stage
 constexpr int kWarpSlot = kWarpRowBytes + 16;             // with room for the phase
 constexpr int kWarpStage = 2 * kWarpSlot;                 // a warp's part of one stage (two rows, or one of twice the run)
-constexpr int kStagedSmem = kCS * kWarps * kWarpStage;    // dynamic shared memory of the staged path
 constexpr int kRingPollLimit = 1 << 20;                   // bounded wait for a slot's bytes (SPEC_DEV_TIMEOUT)
 
 // Elements of the 16-byte block holding p that precede p.

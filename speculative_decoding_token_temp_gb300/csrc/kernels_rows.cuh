@@ -570,19 +570,29 @@ __device__ __forceinline__ void stream_tile_sh(const E* trv, const E* drv, int v
     const uint4* q = reinterpret_cast<const uint4*>(smem + (size_t)(k % kCS) * SLOT) + t;
     const uint4* qx = reinterpret_cast<const uint4*>(xring + (size_t)(k % kCS) * kShiftXSlot) + warp * 2;
     const int va = vt + k * PER, vb = va + kThreads;
-    if (vb < v1) {
+    if (MODE == M_NKL && vb < v1) {
+      // NKL: both vectors of each row as one 2·VEC group, as the aligned tiles do
       float ft[2 * VEC], fd[2 * VEC];
       unpack2<E, VEC>(q[0], q[kThreads], ft);
       const uint4 n0 = lane < 31 ? q[2 * kThreads + 1] : qx[0];
       const uint4 n1 = lane < 31 ? q[3 * kThreads + 1] : qx[1];
       unpack2<E, VEC>(shift_vec<E, M>(q[2 * kThreads], n0, sel), shift_vec<E, M>(q[3 * kThreads], n1, sel), fd);
       pair_update<2 * VEC, IDX, VEC, SEPT>(ta, da, ft, fd, va * VEC, c, vb * VEC, cd);
-    } else if (va < v1) {
-      float ft[VEC], fd[VEC];
-      IO<E, VEC>::unpack(q[0], ft);
-      const uint4 n0 = lane < 31 ? q[2 * kThreads + 1] : qx[0];
-      IO<E, VEC>::unpack(shift_vec<E, M>(q[2 * kThreads], n0, sel), fd);
-      pair_update<VEC, IDX, VEC, SEPT>(ta, da, ft, fd, va * VEC, c, 0, cd);
+      continue;
+    }
+    // stochastic rows (and the NKL tile's last odd vector): one vector of each row at a time,
+    // groups of VEC elements -- the argmax index and the shift's registers on top of a
+    // two-vector group spilled at the 64-register limit
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int v = va + h * kThreads;
+      if (v < v1) {
+        float ft[VEC], fd[VEC];
+        IO<E, VEC>::unpack(q[h * kThreads], ft);
+        const uint4 n = lane < 31 ? q[(2 + h) * kThreads + 1] : qx[h];
+        IO<E, VEC>::unpack(shift_vec<E, M>(q[(2 + h) * kThreads], n, sel), fd);
+        pair_update<VEC, IDX, VEC, SEPT>(ta, da, ft, fd, v * VEC, c, 0, cd);
+      }
     }
   }
   cp_wait<0>();

@@ -201,9 +201,7 @@ __device__ __forceinline__ void block_crossing(const float* table, int n, float 
       r.ent = min(ent, max(n - 1, 0));
     }
   }
-  // the staged sampler's bulk copies (async proxy) may rewrite this shared memory next
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  __syncthreads();
+  __syncthreads();  // the next pass's copies may rewrite this shared memory
 }
 
 // The 16-byte blocks covering row [row, row + V) lie in buffer x (bounds-checked build; the
@@ -273,72 +271,11 @@ __device__ __forceinline__ void mass_pass(const E* trow, const E* drow, int mode
   cp_wait<0>();
 }
 
-// The same masses for rows off the 16-byte grid: in each stage (the elements of 512
-// vectors) warp w takes the contiguous run of slices 2w and 2w + 1 of the row pair (or
-// row) through its own ring (WarpRing: bulk copies of whole aligned 16-byte blocks); in
-// each slice lane l weighs the elements l, l + 32, ... (conflict-free reads). Elements
-// past the row end weigh 0.
-template <typename E, int VEC>
-__device__ __forceinline__ void mass_pass_staged(const E* trow, const E* drow, int mode, float lt2, float ld2, float c,
-                                                 float cd, int V, int k0, int k1, float* table, unsigned char* smem,
-                                                 WarpRing& ring, uint32_t* status) {
-  constexpr int S = 2 * kThreads * VEC;  // elements of a stage
-  constexpr int SL = 32 * VEC;           // elements of a slice
-  constexpr int SW = 2 * SL;             // a warp's run: two slices
-  static_assert(SW * (int)sizeof(E) == kWarpRowBytes, "a warp's run fills its staged row slot");
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const bool resid = mode == S_RESID;
-  const uint32_t wbase = (uint32_t)__cvta_generic_to_shared(smem) + (uint32_t)(warp * kWarpStage);
-  const int nst = k1 - k0;
-  const int ph_t = phase16(trow + (size_t)k0 * S), ph_d = resid ? phase16(drow + (size_t)k0 * S) : 0;
-  const int q0 = ring.next;  // ring stage of this pass's stage 0
-  auto issue = [&](int k) {
-    if (lane == 0 && k < nst) {
-      const uint32_t slot = wbase + (uint32_t)(((q0 + k) % kCS) * kWarps * kWarpStage);
-      const int e0 = (k0 + k) * S + warp * SW, n = min(SW, V - e0);
-      const void* s0 = nullptr;
-      const void* s1 = nullptr;
-      const uint32_t n0 = run_blocks<E>(trow, e0, n, &s0);
-      const uint32_t n1 = resid ? run_blocks<E>(drow, e0, n, &s1) : 0u;
-      ring.produce(q0 + k, slot, s0, n0, slot + kWarpSlot, s1, n1);
-    }
-  };
-  __syncwarp();  // the warp's lanes are done with every slot (the previous pass, the crossing search)
-#pragma unroll
-  for (int k = 0; k < kCS - 1; ++k) issue(k);
-  for (int k = 0; k < nst; ++k) {
-    __syncwarp();
-    issue(k + kCS - 1);
-    ring.wait(q0 + k, status);
-    const unsigned char* slot = smem + (size_t)(warp * kWarpStage + ((q0 + k) % kCS) * kWarps * kWarpStage);
-    const E* sT = reinterpret_cast<const E*>(slot) + ph_t;
-    const E* sD = reinterpret_cast<const E*>(slot + kWarpSlot) + ph_d;
-    const int n = min(SW, V - ((k0 + k) * S + warp * SW));  // <= 0 past the row end
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      float ft[VEC], fd[VEC], w[VEC];
-#pragma unroll
-      for (int j = 0; j < VEC; ++j) {
-        const int x = h * SL + lane + 32 * j;
-        const bool in = x < n;
-        ft[j] = in ? sh_elem<E>(sT, x) : -INFINITY;
-        fd[j] = (in && resid) ? sh_elem<E>(sD, x) : -INFINITY;
-      }
-      weights<VEC>(mode, ft, fd, lt2, ld2, c, cd, w);
-      const float ws = warp_sum(tree_sum<VEC>(w));
-      if (lane == 0) __stcg(table + (size_t)(k0 + k) * kSlicesPerStage + 2 * warp + h, ws);
-    }
-  }
-  ring.next = q0 + nst;
-}
-
 // The warp that owns table entry `ent` (stage k, half h, warp w) re-reads its 32-vector
 // slice -- one vector per lane, in token order -- and returns the token where the
-// running mass passes rem.
-// STAGED (rows off the 16-byte grid): the lane reads its VEC elements one by one, and
-// those past the row end weigh 0. PH: trow and drow are the rows' aligned bases (row
-// element e is their element e + ph).
-template <typename E, int VEC, bool STAGED, bool PH>
+// running mass passes rem. PH: trow and drow are the rows' aligned bases (row element e is
+// their element e + ph).
+template <typename E, int VEC, bool PH>
 __device__ __forceinline__ int slice_token(const E* trow, const E* drow, int mode, float lt2, float ld2, float c, float cd,
                                            int V, int NV, int ent, float rem, int ph = 0) {
   const int lane = threadIdx.x & 31;
@@ -348,22 +285,11 @@ __device__ __forceinline__ int slice_token(const E* trow, const E* drow, int mod
 #pragma unroll
   for (int j = 0; j < VEC; ++j) wt[j] = 0.f;
   if (v < NV) {
-    if constexpr (STAGED) {
-      float ft[VEC], fd[VEC];
-#pragma unroll
-      for (int j = 0; j < VEC; ++j) {
-        const int x = v * VEC + j;
-        ft[j] = x < V ? elem_at<E>(trow, x) : -INFINITY;
-        fd[j] = (x < V && mode == S_RESID) ? elem_at<E>(drow, x) : -INFINITY;
-      }
-      weights<VEC>(mode, ft, fd, lt2, ld2, c, cd, wt);
-    } else {
-      float ft[VEC], fd[VEC];
-      IO<E, VEC>::unpack(ld_stream16(trow + (size_t)v * VEC), ft);
-      if (mode == S_RESID) IO<E, VEC>::unpack(ld_stream16(drow + (size_t)v * VEC), fd);
-      if (PH && (v == 0 || v == NV - 1)) edge_mask<VEC>(ft, fd, v * VEC - ph, V);
-      weights<VEC>(mode, ft, fd, lt2, ld2, c, cd, wt);
-    }
+    float ft[VEC], fd[VEC];
+    IO<E, VEC>::unpack(ld_stream16(trow + (size_t)v * VEC), ft);
+    if (mode == S_RESID) IO<E, VEC>::unpack(ld_stream16(drow + (size_t)v * VEC), fd);
+    if (PH && (v == 0 || v == NV - 1)) edge_mask<VEC>(ft, fd, v * VEC - ph, V);
+    weights<VEC>(mode, ft, fd, lt2, ld2, c, cd, wt);
   }
   const float ls = tree_sum<VEC>(wt);
   float incl = ls;
@@ -396,6 +322,129 @@ __device__ __forceinline__ int slice_token(const E* trow, const E* drow, int mod
   return __shfl_sync(kFull, tok, L);
 }
 
+// ---------------------------------------------------------------------------
+// Residual masses of a row pair whose two rows sit at different offsets within the 16-byte
+// grid (pht for the target row, phd for the draft row; the rows' aligned bases trv, drv):
+// the aligned sampler's stages over the target's vectors v < NVt, and for each the draft's
+// elements at the same row indices, which lie in the draft's aligned vectors w = v + dw
+// and w + 1 (dw * VEC + s = phd - pht, 0 < s < VEC), shifted in registers (one code path
+// for every shift: a block samples sequences of different shifts one after another, and
+// per-shift instances measured slower here through the instruction cache): each lane copies its own w
+// (when it is one of the draft row's NVd blocks), takes w + 1 from the next lane's slot
+// after a warp barrier, and lane 31 copies its own w + 1 into a ring beside the main one
+// (kShiftXSlot bytes per stage). Only the first and last target vectors hold elements
+// outside the row, and only their draft elements can come from blocks that were not
+// copied; those elements are masked. Elements outside the row weigh 0.
+template <typename E, int VEC>
+__device__ __forceinline__ void mass_pass_shifted(int sft, const E* trv, const E* drv, int dw, float lt2, float ld2,
+                                                  float c, float cd, int NVt, int NVd, int k0, int k1, float* table,
+                                                  unsigned char* smem, int pht, int V) {
+  constexpr unsigned SLOT = kCV * kThreads * 16;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem) + 16u * t;
+  unsigned char* xring = smem + kCS * SLOT;
+  const uint32_t xbase = (uint32_t)__cvta_generic_to_shared(xring) + (uint32_t)(warp * 32);
+  const int nst = k1 - k0;
+  auto issue = [&](int k) {
+    if (k < nst) {
+      const uint32_t slot = sbase + (uint32_t)(k % kCS) * SLOT;
+      const uint32_t xs = xbase + (uint32_t)(k % kCS) * kShiftXSlot;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int v = (k0 + k) * 2 * kThreads + h * kThreads + t, w = v + dw;
+        if (v < NVt) cp_async16(slot + (uint32_t)(h * kThreads * 16), trv + (size_t)v * VEC);
+        if (w >= 0 && w < NVd) cp_async16(slot + (uint32_t)((2 + h) * kThreads * 16), drv + (ptrdiff_t)w * VEC);
+        if (lane == 31 && w + 1 >= 0 && w + 1 < NVd) cp_async16(xs + 16u * h, drv + (ptrdiff_t)(w + 1) * VEC);
+      }
+    }
+    cp_commit();
+  };
+  __syncwarp();  // the warp's lanes are done with every slot (the previous pass, the crossing search)
+#pragma unroll
+  for (int k = 0; k < kCS - 1; ++k) issue(k);
+  for (int k = 0; k < nst; ++k) {
+    __syncwarp();  // every lane has read the slot issue() refills
+    issue(k + kCS - 1);
+    cp_wait<kCS - 1>();
+    __syncwarp();  // the lanes' copies of stage k are visible to the whole warp
+    const uint4* q = reinterpret_cast<const uint4*>(smem + (size_t)(k % kCS) * SLOT) + t;
+    const uint4* qx = reinterpret_cast<const uint4*>(xring + (size_t)(k % kCS) * kShiftXSlot) + warp * 2;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int v = (k0 + k) * 2 * kThreads + h * kThreads + t;
+      float ls = 0.f;
+      if (v < NVt) {
+        float ft[VEC], fd[VEC], w[VEC];
+        IO<E, VEC>::unpack(q[h * kThreads], ft);
+        const uint4 n = lane < 31 ? q[(2 + h) * kThreads + 1] : qx[h];
+        IO<E, VEC>::unpack(shift_vec_rt<E>(q[(2 + h) * kThreads], n, sft), fd);
+        if (v == 0 || v == NVt - 1) edge_mask<VEC>(ft, fd, v * VEC - pht, V);
+        weights<VEC>(S_RESID, ft, fd, lt2, ld2, c, cd, w);
+        ls = tree_sum<VEC>(w);
+      }
+      const float ws = warp_sum(ls);
+      if (lane == 0) __stcg(table + ((size_t)(k0 + k) * 2 + h) * kWarps + warp, ws);
+    }
+  }
+  cp_wait<0>();
+}
+
+// The slice re-read of a row pair at two offsets: lane l takes target vector v and the
+// draft's vectors w = v + dw and w + 1 straight from global memory (each when it is one of
+// the row's blocks), shifted as in mass_pass_sh; then as slice_token.
+template <typename E, int VEC>
+__device__ __forceinline__ int slice_token_shifted(int s, const E* trv, const E* drv, int dw, float lt2, float ld2,
+                                                   float c, float cd, int V, int NVt, int NVd, int ent, float rem,
+                                                   int pht) {
+  const int lane = threadIdx.x & 31;
+  const int k = ent / kSlicesPerStage, h = (ent / kWarps) & 1, w = ent % kWarps;
+  const int v = k * 2 * kThreads + h * kThreads + w * 32 + lane;
+  float wt[VEC];
+#pragma unroll
+  for (int j = 0; j < VEC; ++j) wt[j] = 0.f;
+  if (v < NVt) {
+    float ft[VEC], fd[VEC];
+    IO<E, VEC>::unpack(ld_stream16(trv + (size_t)v * VEC), ft);
+    const int wv = v + dw;
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    const uint4 a = (wv >= 0 && wv < NVd) ? ld_stream16(drv + (ptrdiff_t)wv * VEC) : zero;
+    const uint4 b = (wv + 1 >= 0 && wv + 1 < NVd) ? ld_stream16(drv + (ptrdiff_t)(wv + 1) * VEC) : zero;
+    const uint4 sh = shift_vec_rt<E>(a, b, s);
+    IO<E, VEC>::unpack(sh, fd);
+    if (v == 0 || v == NVt - 1) edge_mask<VEC>(ft, fd, v * VEC - pht, V);
+    weights<VEC>(S_RESID, ft, fd, lt2, ld2, c, cd, wt);
+  }
+  const float ls = tree_sum<VEC>(wt);
+  float incl = ls;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  float excl = __shfl_up_sync(kFull, incl, 1);
+  if (lane == 0) excl = 0.f;
+  const unsigned hit = __ballot_sync(kFull, incl > rem && ls > 0.f);
+  const unsigned pos = __ballot_sync(kFull, ls > 0.f);
+  const int L = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : 0);
+  int tok = 0;
+  if (lane == L) {
+    int y = -1, lastpos = -1;
+    float run = excl;
+    for (int j = 0; j < VEC; ++j) {
+      run += wt[j];
+      if (wt[j] > 0.f) {
+        lastpos = j;
+        if (hit && y < 0 && run > rem) y = j;
+      }
+    }
+    if (y < 0) y = lastpos >= 0 ? lastpos : 0;
+    tok = v * VEC + y - pht;
+    if (tok >= V) tok = V - 1;
+    if (tok < 0) tok = 0;
+  }
+  return __shfl_sync(kFull, tok, L);
+}
+
 // Aligned-row sampler. The B rows to sample are cut into 512-vector stages, B * nst of
 // them in sequence order, and every block streams a contiguous range of them: long ranges
 // for the sequences the tile kernel decides first, short ones for the last few, so that
@@ -404,10 +453,12 @@ __device__ __forceinline__ int slice_token(const E* trow, const E* drow, int mod
 // the start of the next; for each part the block adds the part's stage count to the
 // sequence's ticket, and the block whose part completes the nst stages scans the
 // sequence's table and draws its token.
-// PH (aligned sampler): rows at one offset within the 16-byte grid, p.ph.
-template <typename E, int VEC, bool STAGED, bool PH = false>
+// PH (aligned sampler): rows at one offset within the 16-byte grid, p.ph. SH (with PH):
+// every row at its own offset (p.ph = VEC - 1 sizes the stages for the largest); a row
+// pair whose two rows differ in offset takes the shifted pass.
+template <typename E, int VEC, bool PH = false, bool SH = false>
 __global__ void __launch_bounds__(kThreads, 4) sample2_kernel(const __grid_constant__ SampleParams p) {
-  static_assert(!(STAGED && PH), "the staged sampler reads rows at any alignment");
+  static_assert(!SH || PH, "rows at their own offsets are phased rows");
   extern __shared__ __align__(128) unsigned char dsm[];
   // No griddepcontrol.wait: the grid starts while the tile kernel drains, and each part
   // waits only for its own sequence's record (published with release semantics by the
@@ -416,10 +467,7 @@ __global__ void __launch_bounds__(kThreads, 4) sample2_kernel(const __grid_const
   __shared__ int s_last;
   __shared__ CrossResult sc;
   __shared__ unsigned s_max[kWarps];
-  __shared__ __align__(8) uint64_t s_bars[kWarps][kCS];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  WarpRing ring;  // staged rows: the warp's bulk-copy ring, over every pass of the block
-  if constexpr (STAGED) ring.init(s_bars[warp]);
   const size_t V = (size_t)p.V;
   const int ph = PH ? p.ph : 0;               // the rows' offset within the 16-byte grid
   const int NV = (p.V + ph + VEC - 1) / VEC;  // vectors of a row's aligned blocks
@@ -479,10 +527,22 @@ __global__ void __launch_bounds__(kThreads, 4) sample2_kernel(const __grid_const
     if (!row_ok(trow, p.V, p.x_target, p.status) || (q.mode == S_RESID && !row_ok(drow, p.V, p.x_draft, p.status)))
       continue;
     float* table = p.table + (size_t)b * p.table_stride;
-    if constexpr (STAGED)
-      mass_pass_staged<E, VEC>(trow, drow, q.mode, q.lt2, q.ld2, p.c, p.cd, p.V, k0, k1, table, dsm, ring, p.status);
+    // SH: the target row's own offset and vectors, and for a residual the draft row's shift
+    // against it (sft = 0: one offset, the phased pass)
+    int pht = ph, phd = ph, NVt = NV, NVd = NV, sft = 0, dwv = 0;
+    if constexpr (SH) {
+      pht = phase16(trow);
+      phd = q.mode == S_RESID ? phase16(drow) : pht;
+      NVt = (p.V + pht + VEC - 1) / VEC;
+      NVd = (p.V + phd + VEC - 1) / VEC;
+      sft = (phd - pht + VEC) % VEC;
+      dwv = (phd - pht - sft) / VEC;
+    }
+    if (SH && sft != 0)
+      mass_pass_shifted<E, VEC>(sft, trow - pht, drow - phd, dwv, q.lt2, q.ld2, p.c, p.cd, NVt, NVd, k0, k1, table, dsm,
+                                pht, p.V);
     else
-      mass_pass<E, VEC, PH>(trow - ph, drow - ph, q.mode, q.lt2, q.ld2, p.c, p.cd, NV, k0, k1, table, dsm, ph, p.V);
+      mass_pass<E, VEC, PH>(trow - pht, drow - pht, q.mode, q.lt2, q.ld2, p.c, p.cd, NVt, k0, k1, table, dsm, pht, p.V);
     __syncthreads();  // orders every warp's table entries before thread 0's fence
     if (tid == 0) {
       // release: the block's table entries before its ticket; acquire: the other blocks'
@@ -499,15 +559,16 @@ __global__ void __launch_bounds__(kThreads, 4) sample2_kernel(const __grid_const
       block_crossing(table, nent, q.us, dsm, sc, s_max);
       if (!(mode == S_RESID && !(sc.Z > 1e-30f))) break;
       mode = S_P;  // zero residual: the masses of p of the same row, whole row in this block
-      if constexpr (STAGED)
-        mass_pass_staged<E, VEC>(trow, drow, mode, q.lt2, q.ld2, p.c, p.cd, p.V, 0, nst, table, dsm, ring, p.status);
-      else
-        mass_pass<E, VEC, PH>(trow - ph, drow - ph, mode, q.lt2, q.ld2, p.c, p.cd, NV, 0, nst, table, dsm, ph, p.V);
+      mass_pass<E, VEC, PH>(trow - pht, drow - pht, mode, q.lt2, q.ld2, p.c, p.cd, NVt, 0, nst, table, dsm, pht, p.V);
       __syncthreads();
     }
     const int ent = sc.ent;
     if (warp == ent % kWarps) {
-      const int y = slice_token<E, VEC, STAGED, PH>(trow - ph, drow - ph, mode, q.lt2, q.ld2, p.c, p.cd, p.V, NV, ent, sc.rem, ph);
+      const int y = (SH && mode == S_RESID && sft != 0)
+                        ? slice_token_shifted<E, VEC>(sft, trow - pht, drow - phd, dwv, q.lt2, q.ld2, p.c, p.cd, p.V,
+                                                      NVt, NVd, ent, sc.rem, pht)
+                        : slice_token<E, VEC, PH>(trow - pht, drow - pht, mode, q.lt2, q.ld2, p.c, p.cd, p.V,
+                                                          NVt, ent, sc.rem, pht);
       if (lane == 0 && in_idx(q.t_row, p.total_rows, p.status)) p.out_tok[q.t_row] = y;
     }
     __syncthreads();

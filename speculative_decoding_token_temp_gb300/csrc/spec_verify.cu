@@ -58,7 +58,9 @@ int table_stride_for(int V, spec_dtype dt) {
 // max_chunk: the longest vocabulary chunk of a tile. 0 = the measured best: 65536 tokens
 // for single-row tiles and for the stochastic call's pairs (256 KB pair tiles: fewer
 // tile epilogues; 185.6 against 191.7 us at the headline, same box), 49152 for the NKL
-// call's pairs (150.3 us, against 152.0 with 32768 and 155.4 with 65536).
+// call's pairs (150.3 us, against 152.0 with 32768 and 155.4 with 65536) unless a whole
+// row fits in 65536 (B=256, gamma=8, V=50257: whole rows 74.4 against 79.1 us in two
+// chunks, which also folds two sets of partial edge blocks per row).
 // geo: the device's waves; the chunking follows them, while the offsets (and the total)
 // are those of the largest wave allowed, so the workspace size does not depend on the
 // device.
@@ -67,7 +69,7 @@ Layout layout(int B, int V, long long rows, bool sample, bool single_rows = fals
   Layout L;
   L.rows = rows;
   const long long trows = fused_k > 0 ? rows / fused_k : rows;  // tiles per chunk
-  const int mc = max_chunk > 0 ? max_chunk : ((single_rows || sample) ? 65536 : 49152);
+  const int mc = max_chunk > 0 ? max_chunk : ((single_rows || sample || V <= 65536) ? 65536 : 49152);
   const plan::Chunking run = plan::chunking(V, trows, mc, fused_k > 0 ? geo.fused_slots : geo.tile_slots);
   const plan::Chunking cap = plan::chunking(V, trows, mc, plan::kMaxWaveSlots);
   L.nchunks = run.nchunks;
@@ -248,10 +250,10 @@ cudaError_t launch_rows(bool bf16, RowPath path, const RowsParams& rp, long long
   }
 }
 
-template <typename E, int VEC, bool STAGED, bool PH = false>
+template <typename E, int VEC, bool PH = false, bool SH = false>
 cudaError_t launch_sample2_t(const SampleParams& sp, long long blocks, cudaStream_t stream) {
-  auto kern = sample2_kernel<E, VEC, STAGED, PH>;
-  const int smem = STAGED ? kStagedSmem : kRowsSmem;
+  auto kern = sample2_kernel<E, VEC, PH, SH>;
+  const int smem = SH ? kShiftSmem : kRowsSmem;
   static std::atomic<unsigned long long> done{0};
   const cudaError_t e = ensure_smem_attr(kern, done, smem);
   if (e != cudaSuccess) return e;
@@ -269,16 +271,18 @@ cudaError_t launch_sample2_t(const SampleParams& sp, long long blocks, cudaStrea
   return cudaLaunchKernelEx(&cfg, kern, sp);
 }
 
-// vec: the aligned sampler (rows on the 16-byte grid, or all at the offset sp.ph within it)
-cudaError_t launch_sample2(bool bf16, bool vec, const SampleParams& sp, long long blocks, cudaStream_t stream) {
+// The sampler for the tile kernel's row layout: rows on the 16-byte grid, or all at the
+// offset sp.ph within it (P_VEC, P_PHASED with rows of whole blocks); every row at its own
+// offset (shifted: single rows, and pairs shifted to the target's offset).
+enum SamplePath { S_VEC, S_SHIFT };
+
+cudaError_t launch_sample2(bool bf16, SamplePath path, const SampleParams& sp, long long blocks, cudaStream_t stream) {
   if (bf16) {
-    if (!vec) return launch_sample2_t<uint16_t, 8, true>(sp, blocks, stream);
-    return sp.ph ? launch_sample2_t<uint16_t, 8, false, true>(sp, blocks, stream)
-                 : launch_sample2_t<uint16_t, 8, false>(sp, blocks, stream);
+    if (path == S_SHIFT) return launch_sample2_t<uint16_t, 8, true, true>(sp, blocks, stream);
+    return sp.ph ? launch_sample2_t<uint16_t, 8, true>(sp, blocks, stream) : launch_sample2_t<uint16_t, 8>(sp, blocks, stream);
   }
-  if (!vec) return launch_sample2_t<float, 4, true>(sp, blocks, stream);
-  return sp.ph ? launch_sample2_t<float, 4, false, true>(sp, blocks, stream)
-               : launch_sample2_t<float, 4, false>(sp, blocks, stream);
+  if (path == S_SHIFT) return launch_sample2_t<float, 4, true, true>(sp, blocks, stream);
+  return sp.ph ? launch_sample2_t<float, 4, true>(sp, blocks, stream) : launch_sample2_t<float, 4>(sp, blocks, stream);
 }
 
 // Fused multi-draft tiles: when given, the verification launches multi_rows_kernel over
@@ -351,7 +355,7 @@ cudaError_t device_geometry(Geometry* out) {
       int sms = 0, ot = 0, os = 0, o2 = 0, o3 = 0, o4 = 0;
       if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
       if ((e = blocks_per_sm(rows_kernel<uint16_t, 8, M_STOCH, false>, kRowsSmem, &ot)) != cudaSuccess) return e;
-      if ((e = blocks_per_sm(sample2_kernel<uint16_t, 8, false, false>, kRowsSmem, &os)) != cudaSuccess) return e;
+      if ((e = blocks_per_sm(sample2_kernel<uint16_t, 8>, kRowsSmem, &os)) != cudaSuccess) return e;
       if ((e = blocks_per_sm(multi_rows_kernel<uint16_t, 8, 2, M_STOCH>, multi_smem<2>(), &o2)) != cudaSuccess) return e;
       if ((e = blocks_per_sm(multi_rows_kernel<uint16_t, 8, 3, M_STOCH>, multi_smem<3>(), &o3)) != cudaSuccess) return e;
       if ((e = blocks_per_sm(multi_rows_kernel<uint16_t, 8, 4, M_STOCH>, multi_smem<4>(), &o4)) != cudaSuccess) return e;
@@ -549,11 +553,13 @@ spec_status stochastic_impl(spec_batch g, spec_dtype dtype, const void* target_l
   sp.table_stride = L.table_stride;
   sp.tiles_done = reinterpret_cast<const unsigned*>(ws + L.cntA) + g.B;
   sp.ntiles = (unsigned)tiles;
-  // the aligned sampler takes phased rows only when every row sits at its base's offset
-  // (rows of a whole number of 16-byte blocks); single rows may be phased row by row
+  // rows of a whole number of 16-byte blocks keep their base's offset: the aligned sampler
+  // with that offset; any other layout: every row at its own offset (stages sized for the
+  // largest, VEC - 1)
   const bool uniform = ((long long)g.V * (long long)elem_bytes(dtype)) % 16 == 0;
-  const bool sampler_vec = path == P_VEC || (path == P_PHASED && uniform);
-  sp.ph = (path == P_PHASED && uniform) ? (int)(((uintptr_t)target_logits & 15u) / elem_bytes(dtype)) : 0;
+  const bool one_offset = path == P_VEC || (path == P_PHASED && uniform);
+  const int vec = bf16 ? 8 : 4;
+  sp.ph = one_offset ? (path == P_VEC ? 0 : (int)(((uintptr_t)target_logits & 15u) / elem_bytes(dtype))) : vec - 1;
   // One wave of blocks over the B * nst stages. The last kTailSeqs sequences (decided last
   // by the tile kernel) take short ranges of at least kTailStages stages on at most a
   // quarter of the wave, the others equal long ranges.
@@ -564,7 +570,8 @@ spec_status stochastic_impl(spec_batch g, spec_dtype dtype, const void* target_l
   sp.nb_head = (int)sg.nb_head;
   sp.seg_head = (int)sg.seg_head;
   sp.seg_tail = (int)sg.seg_tail;
-  if (launch_sample2(bf16, sampler_vec, sp, sg.nb_head + sg.nb_tail, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (launch_sample2(bf16, one_offset ? S_VEC : S_SHIFT, sp, sg.nb_head + sg.nb_tail, stream) != cudaSuccess)
+    return SPEC_ERR_CUDA;
   return SPEC_OK;
 }
 
@@ -1029,7 +1036,7 @@ spec_status spec_selftest_wait_timeout(uint32_t* device_status, void* workspace,
   sp.seg_tail = kTailStages;
   // an ordinary stream-ordered launch (no programmatic dependent launch): the sampler
   // starts only after the prologue has completed, so the record it polls is re-armed
-  auto kern = sample2_kernel<uint16_t, 8, false>;
+  auto kern = sample2_kernel<uint16_t, 8>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowsSmem) != cudaSuccess)
     return SPEC_ERR_CUDA;
   kern<<<1, kThreads, kRowsSmem, stream>>>(sp);
