@@ -527,6 +527,21 @@ __device__ __forceinline__ float min3(float a, float b, float c) {
   return d;
 }
 
+// max of the 8 bf16 values of a 16-byte vector, taken on the packed pairs (the maximum of
+// the exactly converted values; a NaN is ignored unless every value is NaN, as in vmax)
+__device__ __forceinline__ float vmax_bf16x8(const uint4& r) {
+  uint32_t a, b, m;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(a) : "r"(r.x), "r"(r.y));
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(b) : "r"(r.z), "r"(r.w));
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(a), "r"(b));
+  return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
+}
+// elements 2j and 2j + 1 of a 16-byte vector of bf16, as floats
+__device__ __forceinline__ float2 bf16_pair(const uint4& r, int j) {
+  const uint32_t w = j == 0 ? r.x : j == 1 ? r.y : j == 2 ? r.z : r.w;
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
 // N-element max / min as a shallow tree of 3-input instructions (N in {1, 4, 8, 16})
 template <int N>
 __device__ __forceinline__ float vmax(const float (&t)[N]) {
@@ -568,13 +583,18 @@ __device__ __forceinline__ float vmin(const float (&t)[N]) {
 
 constexpr float kLazy = 32.f;
 
+// TAcc::g0, where the thread's maximum m lies: -1 none; >= 0 a group of whole vectors, the
+// index of its first element (a multiple of the vector width) plus 1 when the group has a
+// second vector, kThreads vectors further on (the streams fold vectors v and v + kThreads
+// together); <= -2 the exact index i of m itself, stored as exact_idx(i) = -2 - i (an
+// element folded in alone). The lowest index inside a group is found once, at the end of
+// the tile, by the thread that holds the tile's maximum.
 struct TAcc {
   float m, mr, mth, nmc, lo, hi;
   float2 s;
-  int g0, g1;  // the group that holds m (resolved to the lowest index at the tile end; g0 < 0: none)
+  int g0;
 };
-// TAcc::g1 of an exact index: g0 is the index of m itself (an element folded in alone)
-constexpr int kExactIdx = INT_MIN;
+__host__ __device__ constexpr int exact_idx(int i) { return -2 - i; }
 struct DAcc {
   float mr, mth, nmc;
   float2 s, k;
@@ -584,7 +604,7 @@ struct DAcc {
 
 __device__ __forceinline__ void init(TAcc& a) {
   a.m = -INFINITY; a.mr = -INFINITY; a.mth = -INFINITY; a.nmc = 0.f; a.lo = INFINITY; a.hi = -INFINITY;
-  a.s = make_float2(0.f, 0.f); a.g0 = -1; a.g1 = -1;
+  a.s = make_float2(0.f, 0.f); a.g0 = -1;
 }
 __device__ __forceinline__ void init(DAcc& a) {
   a.mr = -INFINITY; a.mth = -INFINITY; a.nmc = 0.f; a.s = make_float2(0.f, 0.f); a.k = make_float2(0.f, 0.f);
@@ -642,25 +662,15 @@ __device__ __forceinline__ float2 exp_sum2(const float (&t)[VEC], float c, float
   }
 }
 
-// Exact max. A group only records where it starts, and the lowest index inside it is
-// found once, at the end of the tile, by the thread that holds the tile's maximum: a
-// contiguous group of 16-byte vectors (the first H elements from e0, the rest from e1)
-// by resolve_index; a strided group (H == 0, staged path: its VEC elements at
-// e0 + k * GS, GS the stride the tile's reduction is given; g1 records their count) by
-// resolve_strided.
+// Exact max. A group only records where it starts (TAcc::g0): the group's VEC elements are
+// one vector from e0 (H == VEC) or two, H from e0 and H from e1 = e0 + kThreads * H (H ==
+// VEC / 2); H == 0: no group is recorded (an element folded in alone, whose index the
+// caller keeps).
 template <int VEC, int H, bool IDX>
-__device__ __forceinline__ void track_max(TAcc& a, const float (&t)[VEC], float vm, int e0, int e1) {
-  static_assert(H == 0 || VEC > 1, "a contiguous group is at least one vector");
-  if (IDX) {
-    if (vm > a.m) {
-      if constexpr (H == 0) {
-        a.g0 = e0;
-        a.g1 = VEC;
-      } else {
-        a.g0 = e0;
-        a.g1 = (H == VEC) ? e0 + H : e1;
-      }
-    }
+__device__ __forceinline__ void track_max(TAcc& a, float vm, int e0) {
+  static_assert(H == 0 || H == VEC || 2 * H == VEC, "one or two vectors");
+  if (IDX && H > 0) {
+    if (vm > a.m) a.g0 = (H == VEC) ? e0 : (e0 | 1);
   }
   a.m = fmaxf(a.m, vm);
 }
@@ -701,12 +711,13 @@ __device__ __forceinline__ void lazy_ref2(float& mr, float& mth, float& nmc, flo
 }
 
 // target row with sum (bonus row of the stochastic call); lo tracks the minimum so a
-// -inf entry, which the sum alone cannot see, is still reported
-template <int VEC, int H = VEC>
-__device__ __forceinline__ void tsum_update(TAcc& a, const float (&t)[VEC], int e0, float c, int e1 = 0) {
+// -inf entry, which the sum alone cannot see, is still reported. IDX: record the group
+// holding the maximum (for its index).
+template <int VEC, int H = VEC, bool IDX = true>
+__device__ __forceinline__ void tsum_update(TAcc& a, const float (&t)[VEC], int e0, float c) {
   const float vm = vmax<VEC>(t);
   a.lo = fminf(a.lo, vmin<VEC>(t));
-  track_max<VEC, H, true>(a, t, vm, e0, e1);
+  track_max<VEC, H, IDX>(a, vm, e0);
   lazy_ref(a.mr, a.mth, a.nmc, a.s, nullptr, vm, c);
   float e[VEC];
   a.s = add2(a.s, exp_sum2<VEC>(t, c, a.nmc, e));
@@ -714,11 +725,11 @@ __device__ __forceinline__ void tsum_update(TAcc& a, const float (&t)[VEC], int 
 
 // argmax only (greedy and tree rows): no exponentials; hi propagates NaN
 template <int VEC, int H = VEC>
-__device__ __forceinline__ void argmax_update(TAcc& a, const float (&t)[VEC], int e0, int e1 = 0) {
+__device__ __forceinline__ void argmax_update(TAcc& a, const float (&t)[VEC], int e0) {
   const float vh = vmax_nan<VEC>(t);
   a.hi = max_nan(a.hi, vh);
   a.lo = fminf(a.lo, vmin<VEC>(t));
-  track_max<VEC, H, true>(a, t, vh, e0, e1);
+  track_max<VEC, H, true>(a, vh, e0);
 }
 
 // (target row, draft row) pair; a -inf or NaN in either makes the KL sum non-finite.
@@ -726,9 +737,9 @@ __device__ __forceinline__ void argmax_update(TAcc& a, const float (&t)[VEC], in
 // target scale c (for NKL at the target temperature) goes to s2, and k uses that scale.
 template <int VEC, bool IDX, int H = VEC, bool SEPT = false>
 __device__ __forceinline__ void pair_update(TAcc& a, DAcc& d, const float (&t)[VEC], const float (&z)[VEC], int e0,
-                                            float c, int e1 = 0, float cd = 0.f) {
+                                            float c, float cd = 0.f) {
   const float tm = vmax<VEC>(t), dm = vmax<VEC>(z);
-  track_max<VEC, H, IDX>(a, t, tm, e0, e1);
+  track_max<VEC, H, IDX>(a, tm, e0);
   lazy_ref(a.mr, a.mth, a.nmc, a.s, nullptr, tm, c);
   float et[VEC], ed[VEC];
   a.s = add2(a.s, exp_sum2<VEC>(t, c, a.nmc, et));
@@ -766,18 +777,22 @@ __device__ __forceinline__ void pair_update(TAcc& a, DAcc& d, const float (&t)[V
 // ---------------------------------------------------------------------------
 // block reduction of a tile into a Partial (valid in thread 0)
 
-// Lowest index of the value m inside the recorded group (g0: first VEC elements, g1:
-// the next VEC), re-read from the row (an L2 hit: the tile has just streamed it).
+// Lowest index of the value m inside the group g (TAcc::g0 >= 0: its first vector, and
+// the vector kThreads vectors on when bit 0 is set), re-read from the row (an L2 hit: the
+// tile has just streamed it).
 template <typename E, int VEC>
-__device__ __forceinline__ int resolve_index(const E* row, int g0, int g1, float m, const Ext* xr = nullptr,
+__device__ __forceinline__ int resolve_index(const E* row, int g, float m, const Ext* xr = nullptr,
                                              uint32_t* status = nullptr) {
-  if (g0 < 0) return INT_MAX;
+  if (g < 0) return INT_MAX;
+  const int g0 = g & ~1;
   float f[VEC];
   if (xr != nullptr && !in_ext(row + g0, 16, *xr, status)) return INT_MAX;
   IO<E, VEC>::unpack(ld_stream16(row + g0), f);
 #pragma unroll
   for (int k = 0; k < VEC; ++k)
     if (f[k] == m) return g0 + k;
+  if (!(g & 1)) return INT_MAX;
+  const int g1 = g0 + kThreads * VEC;
   if (xr != nullptr && !in_ext(row + g1, 16, *xr, status)) return INT_MAX;
   IO<E, VEC>::unpack(ld_stream16(row + g1), f);
 #pragma unroll
@@ -786,21 +801,11 @@ __device__ __forceinline__ int resolve_index(const E* row, int g0, int g1, float
   return INT_MAX;
 }
 
-// Lowest index of the value m among the g1 elements g0, g0 + GS, ... of a strided group
-// (staged path), re-read one by one from the row.
-template <typename E, int GS>
-__device__ __forceinline__ int resolve_strided(const E* row, int g0, int g1, float m) {
-  if (g0 < 0) return INT_MAX;
-  for (int k = 0; k < g1; ++k)
-    if (elem_at<E>(row, g0 + k * GS) == m) return g0 + k * GS;
-  return INT_MAX;
-}
-
-// row != nullptr: the target maximum's index is resolved from the recorded groups
-// (strided groups of stride GS when GS > 0); PRE: the caller has already resolved it into
-// ta.g0. SEPT: the draft sum s is at scale cd, s2 and k at c.
+// row != nullptr: the target maximum's index is resolved from the recorded groups; PRE:
+// the caller has already resolved it into ta.g0. SEPT: the draft sum s is at scale cd, s2
+// and k at c.
 // xr, status: the row's buffer for the bounds-checked build (null: unchecked).
-template <class SY, typename E = float, int VEC = 1, bool SEPT = false, int GS = 0, bool PRE = false>
+template <class SY, typename E = float, int VEC = 1, bool SEPT = false, bool PRE = false>
 __device__ __forceinline__ Partial reduce_tile(int kind, const TAcc& ta, const DAcc& da, float c,
                                                const E* row = nullptr, float cd = 0.f, const Ext* xr = nullptr,
                                                uint32_t* status = nullptr) {
@@ -822,17 +827,15 @@ __device__ __forceinline__ Partial reduce_tile(int kind, const TAcc& ta, const D
     TM = fmaxf(TM, s_m[0][w]);
     DM = fmaxf(DM, s_m[1][w]);
   }
-  static_assert(GS > 0 || VEC > 1, "groups are strided (GS) or whole vectors (VEC)");
+  static_assert(VEC > 1, "groups are whole vectors");
   int my_idx = INT_MAX;
   if (ta.m == TM) {
     if constexpr (PRE)
       my_idx = ta.g0 >= 0 ? ta.g0 : INT_MAX;
-    else if constexpr (GS > 0)
-      my_idx = row ? resolve_strided<E, GS>(row, ta.g0, ta.g1, TM) : INT_MAX;
-    else if (ta.g1 == kExactIdx)
-      my_idx = row ? ta.g0 : INT_MAX;
+    else if (ta.g0 <= -2)
+      my_idx = row ? exact_idx(ta.g0) : INT_MAX;  // exact_idx is its own inverse
     else
-      my_idx = row ? resolve_index<E, VEC>(row, ta.g0, ta.g1, TM, xr, status) : INT_MAX;
+      my_idx = row ? resolve_index<E, VEC>(row, ta.g0, TM, xr, status) : INT_MAX;
   }
   const int wi = warp_min_i(my_idx);
   float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f, v4 = 0.f;

@@ -414,77 +414,179 @@ __host__ __device__ constexpr int multi_smem() {
   return multi_stages<K>() * 2 * K * kThreads * 16;
 }
 
-// One stage of a fused tile on a draft position (K <= 3), thread-local: the K draft vectors
-// unpacked and their lazy references checked with one vote; every draft exponential
-// computed before the pairwise sums, so that one difference z_a - z_b feeds both K_ab and
-// K_ba (each pair sum chained from its accumulator and folded once per vector); then per
-// candidate its target vector -- stochastic: the maximum (no index: nothing reads the
-// argmax of a stochastic multi-draft row) and the sum, and the verification's KL sum
-// against the candidate's own target row; greedy: the argmax.
+// One stage of a fused tile on a draft position (K <= 3), thread-local. The lazy references
+// of the K draft rows (and, stochastic, of the K target rows) are checked with one vote;
+// one difference z_a - z_b feeds both K_ab and K_ba (each pair sum chained from its
+// accumulator and folded once per vector). Per candidate -- stochastic: the target maximum
+// (no index: nothing reads the argmax of a stochastic multi-draft row) and sum, and the
+// verification's KL sum against the candidate's own target row; greedy: the argmax.
+// bf16 keeps the 2K vectors packed and goes through them a pair of elements at a time
+// (every exponential used as soon as it is computed); fp32 unpacks the K draft vectors
+// together and computes all their exponentials before the pairwise sums.
 template <typename E, int VEC, int K, bool STOCH>
 __device__ __forceinline__ void multi_pair_stage(const uint4* sq, int e0, float c, float cq, TAcc (&ta)[K],
                                                  DAcc (&da)[K], float (&kk)[K][K]) {
   using io = IO<E, VEC>;
   static_assert(VEC % 2 == 0, "packed pairs of elements");
-  float fd[K][VEC], vm[K];
-  bool mv = false;
-#pragma unroll
-  for (int a = 0; a < K; ++a) {
-    io::unpack(sq[(K + a) * kThreads], fd[a]);
-    vm[a] = vmax<VEC>(fd[a]);
-    mv = mv || vm[a] > da[a].mth;
-  }
-  if (__any_sync(__activemask(), mv)) {
+  if constexpr (VEC == 8) {
+    // bf16: the 2K vectors stay packed until each pair of elements is used -- their maxima
+    // taken on the packed values -- so that a thread holds 2K words of raw data rather than
+    // 16K unpacked floats and the candidates' exponentials of a pair of elements are used
+    // as soon as they are computed
+    uint4 rd[K], rt[K];
+    float vmd[K], vmt[K];
+    bool mv = false;
 #pragma unroll
     for (int a = 0; a < K; ++a) {
-      if (vm[a] > da[a].mth) {
-        const float f = ex2((da[a].mr - vm[a]) * cq);
-        da[a].s = make_float2(da[a].s.x * f, da[a].s.y * f);
-        da[a].k = make_float2(da[a].k.x * f, da[a].k.y * f);
-#pragma unroll
-        for (int b = 0; b < K; ++b) kk[a][b] *= f;
-        da[a].mr = vm[a];
-        da[a].mth = vm[a] + kLazy / cq;
-        da[a].nmc = -vm[a] * cq;
+      rd[a] = sq[(K + a) * kThreads];
+      vmd[a] = vmax_bf16x8(rd[a]);
+      mv = mv || vmd[a] > da[a].mth;
+      rt[a] = sq[a * kThreads];
+      if constexpr (STOCH) {
+        vmt[a] = vmax_bf16x8(rt[a]);
+        ta[a].m = fmaxf(ta[a].m, vmt[a]);
+        mv = mv || vmt[a] > ta[a].mth;
       }
     }
-  }
-  float ed[K][VEC];
+    if (__any_sync(__activemask(), mv)) {
 #pragma unroll
-  for (int a = 0; a < K; ++a) da[a].s = add2(da[a].s, exp_sum2<VEC>(fd[a], cq, da[a].nmc, ed[a]));
+      for (int a = 0; a < K; ++a) {
+        if (vmd[a] > da[a].mth) {
+          const float f = ex2((da[a].mr - vmd[a]) * cq);
+          da[a].s = make_float2(da[a].s.x * f, da[a].s.y * f);
+          da[a].k = make_float2(da[a].k.x * f, da[a].k.y * f);
 #pragma unroll
-  for (int a = 0; a < K; ++a) {
-#pragma unroll
-    for (int b = a + 1; b < K; ++b) {
-      // K_ab += sum e_a (z_a - z_b); K_ba += sum e_b (z_b - z_a), kept negated in the chain
-      float2 pab = make_float2(kk[a][b], 0.f), nba = make_float2(-kk[b][a], 0.f);
-#pragma unroll
-      for (int j = 0; j < VEC / 2; ++j) {
-        const float2 d = sub2(make_float2(fd[a][2 * j], fd[a][2 * j + 1]), make_float2(fd[b][2 * j], fd[b][2 * j + 1]));
-        pab = fma2(make_float2(ed[a][2 * j], ed[a][2 * j + 1]), d, pab);
-        nba = fma2(make_float2(ed[b][2 * j], ed[b][2 * j + 1]), d, nba);
+          for (int b = 0; b < K; ++b) kk[a][b] *= f;
+          da[a].mr = vmd[a];
+          da[a].mth = vmd[a] + kLazy / cq;
+          da[a].nmc = -vmd[a] * cq;
+        }
+        if constexpr (STOCH) {
+          if (vmt[a] > ta[a].mth) {
+            const float f = ex2((ta[a].mr - vmt[a]) * c);
+            ta[a].s = make_float2(ta[a].s.x * f, ta[a].s.y * f);
+            ta[a].mr = vmt[a];
+            ta[a].mth = vmt[a] + kLazy / c;
+            ta[a].nmc = -vmt[a] * c;
+          }
+        }
       }
-      kk[a][b] = pab.x + pab.y;
-      kk[b][a] = -(nba.x + nba.y);
     }
-  }
+    // K_ab += sum e_a (z_a - z_b); K_ba += sum e_b (z_b - z_a), kept negated in its chain
+    float2 pk[K][K];
 #pragma unroll
-  for (int a = 0; a < K; ++a) {
-    float ft[VEC];
-    io::unpack(sq[a * kThreads], ft);
-    if constexpr (STOCH) {
-      const float tm = vmax<VEC>(ft);
-      ta[a].m = fmaxf(ta[a].m, tm);
-      lazy_ref(ta[a].mr, ta[a].mth, ta[a].nmc, ta[a].s, nullptr, tm, c);
-      float et[VEC];
-      ta[a].s = add2(ta[a].s, exp_sum2<VEC>(ft, c, ta[a].nmc, et));
+    for (int a = 0; a < K; ++a)
 #pragma unroll
-      for (int j = 0; j < VEC / 2; ++j)
-        da[a].k = fma2(make_float2(ed[a][2 * j], ed[a][2 * j + 1]),
-                       sub2(make_float2(fd[a][2 * j], fd[a][2 * j + 1]), make_float2(ft[2 * j], ft[2 * j + 1])),
-                       da[a].k);
-    } else {
-      argmax_update<VEC>(ta[a], ft, e0);
+      for (int b = a + 1; b < K; ++b) {
+        pk[a][b] = make_float2(kk[a][b], 0.f);
+        pk[b][a] = make_float2(-kk[b][a], 0.f);
+      }
+    const float2 cq2 = make_float2(cq, cq), c2 = make_float2(c, c);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float2 zd[K], ed[K];
+#pragma unroll
+      for (int a = 0; a < K; ++a) {
+        zd[a] = bf16_pair(rd[a], j);
+        const float2 x = fma2(zd[a], cq2, make_float2(da[a].nmc, da[a].nmc));
+        ed[a] = make_float2(ex2(x.x), ex2(x.y));
+        da[a].s = add2(da[a].s, ed[a]);
+      }
+#pragma unroll
+      for (int a = 0; a < K; ++a)
+#pragma unroll
+        for (int b = a + 1; b < K; ++b) {
+          const float2 d = sub2(zd[a], zd[b]);
+          pk[a][b] = fma2(ed[a], d, pk[a][b]);
+          pk[b][a] = fma2(ed[b], d, pk[b][a]);
+        }
+      if constexpr (STOCH) {
+#pragma unroll
+        for (int a = 0; a < K; ++a) {
+          const float2 zt = bf16_pair(rt[a], j);
+          const float2 x = fma2(zt, c2, make_float2(ta[a].nmc, ta[a].nmc));
+          ta[a].s = add2(ta[a].s, make_float2(ex2(x.x), ex2(x.y)));
+          da[a].k = fma2(ed[a], sub2(zd[a], zt), da[a].k);
+        }
+      }
+    }
+#pragma unroll
+    for (int a = 0; a < K; ++a)
+#pragma unroll
+      for (int b = a + 1; b < K; ++b) {
+        kk[a][b] = pk[a][b].x + pk[a][b].y;
+        kk[b][a] = -(pk[b][a].x + pk[b][a].y);
+      }
+    if constexpr (!STOCH) {
+#pragma unroll
+      for (int a = 0; a < K; ++a) {
+        float ft[VEC];
+        io::unpack(rt[a], ft);
+        argmax_update<VEC>(ta[a], ft, e0);
+      }
+    }
+  } else {
+    // fp32: the K draft vectors unpacked together
+    float fd[K][VEC], vm[K];
+    bool mv = false;
+#pragma unroll
+    for (int a = 0; a < K; ++a) {
+      io::unpack(sq[(K + a) * kThreads], fd[a]);
+      vm[a] = vmax<VEC>(fd[a]);
+      mv = mv || vm[a] > da[a].mth;
+    }
+    if (__any_sync(__activemask(), mv)) {
+#pragma unroll
+      for (int a = 0; a < K; ++a) {
+        if (vm[a] > da[a].mth) {
+          const float f = ex2((da[a].mr - vm[a]) * cq);
+          da[a].s = make_float2(da[a].s.x * f, da[a].s.y * f);
+          da[a].k = make_float2(da[a].k.x * f, da[a].k.y * f);
+#pragma unroll
+          for (int b = 0; b < K; ++b) kk[a][b] *= f;
+          da[a].mr = vm[a];
+          da[a].mth = vm[a] + kLazy / cq;
+          da[a].nmc = -vm[a] * cq;
+        }
+      }
+    }
+    float ed[K][VEC];
+#pragma unroll
+    for (int a = 0; a < K; ++a) da[a].s = add2(da[a].s, exp_sum2<VEC>(fd[a], cq, da[a].nmc, ed[a]));
+#pragma unroll
+    for (int a = 0; a < K; ++a) {
+#pragma unroll
+      for (int b = a + 1; b < K; ++b) {
+        // K_ab += sum e_a (z_a - z_b); K_ba += sum e_b (z_b - z_a), kept negated in the chain
+        float2 pab = make_float2(kk[a][b], 0.f), nba = make_float2(-kk[b][a], 0.f);
+#pragma unroll
+        for (int j = 0; j < VEC / 2; ++j) {
+          const float2 d = sub2(make_float2(fd[a][2 * j], fd[a][2 * j + 1]), make_float2(fd[b][2 * j], fd[b][2 * j + 1]));
+          pab = fma2(make_float2(ed[a][2 * j], ed[a][2 * j + 1]), d, pab);
+          nba = fma2(make_float2(ed[b][2 * j], ed[b][2 * j + 1]), d, nba);
+        }
+        kk[a][b] = pab.x + pab.y;
+        kk[b][a] = -(nba.x + nba.y);
+      }
+    }
+#pragma unroll
+    for (int a = 0; a < K; ++a) {
+      float ft[VEC];
+      io::unpack(sq[a * kThreads], ft);
+      if constexpr (STOCH) {
+        const float tm = vmax<VEC>(ft);
+        ta[a].m = fmaxf(ta[a].m, tm);
+        lazy_ref(ta[a].mr, ta[a].mth, ta[a].nmc, ta[a].s, nullptr, tm, c);
+        float et[VEC];
+        ta[a].s = add2(ta[a].s, exp_sum2<VEC>(ft, c, ta[a].nmc, et));
+#pragma unroll
+        for (int j = 0; j < VEC / 2; ++j)
+          da[a].k = fma2(make_float2(ed[a][2 * j], ed[a][2 * j + 1]),
+                         sub2(make_float2(fd[a][2 * j], fd[a][2 * j + 1]), make_float2(ft[2 * j], ft[2 * j + 1])),
+                         da[a].k);
+      } else {
+        argmax_update<VEC>(ta[a], ft, e0);
+      }
     }
   }
 }
@@ -580,12 +682,12 @@ __global__ void __launch_bounds__(kThreads, 2) multi_rows_kernel(const __grid_co
       io::unpack(sq[a * kThreads], ft);
       if (!pair || !STOCH) {
         if (STOCH)
-          tsum_update<VEC>(ta[a], ft, e0, c);  // the stochastic bonus row
+          tsum_update<VEC, VEC, false>(ta[a], ft, e0, c);  // the stochastic bonus row (no index)
         else
           argmax_update<VEC>(ta[a], ft, e0);   // greedy rows
       } else {
         const float vm = vmax<VEC>(ft);
-        track_max<VEC, VEC, true>(ta[a], ft, vm, e0, 0);
+        track_max<VEC, VEC, false>(ta[a], vm, e0);
         lazy_ref(ta[a].mr, ta[a].mth, ta[a].nmc, ta[a].s, nullptr, vm, c);
         float et[VEC];
         ta[a].s = add2(ta[a].s, exp_sum2<VEC>(ft, c, ta[a].nmc, et));

@@ -431,8 +431,12 @@ __device__ __forceinline__ void unpack2(const uint4& a, const uint4& b, float (&
 // Argmax rows (KIND == K_ARGMAX) also keep, in `best`, the raw vectors of the group that
 // holds the thread's maximum, so the tile end resolves its lowest index without
 // re-reading the row.
+// rot (0..7): vector v0 lies rot vectors past the start of its 128-byte line. Each stage's
+// 256-vector block is then assigned rotated by rot (thread t takes offset (t - rot) mod 256),
+// so that every warp but the first copies four whole lines instead of spreading its 32
+// vectors over five.
 template <typename E, int VEC, int MODE, int KIND>
-__device__ __forceinline__ void stream_tile(const E* trow, const E* drow, int v0, int v1, float c, float cd,
+__device__ __forceinline__ void stream_tile(const E* trow, const E* drow, int v0, int v1, int rot, float c, float cd,
                                             TAcc& ta, DAcc& da, unsigned char* smem, uint4 (&best)[2],
                                             const RowsParams& p) {
   constexpr bool IDX = is_stoch(MODE), SEPT = MODE == M_STOCH2;
@@ -441,7 +445,7 @@ __device__ __forceinline__ void stream_tile(const E* trow, const E* drow, int v0
   const int t = threadIdx.x;
   const uint32_t base = (uint32_t)__cvta_generic_to_shared(smem) + 16u * t;
   const int nst = (v1 - v0 + PER - 1) / PER;
-  const int vt = v0 + t;  // this thread's first vector in stage 0
+  const int vt = v0 + ((t - rot) & (kThreads - 1));  // this thread's first vector in stage 0
   const E* tp = trow + (size_t)vt * VEC;
   const E* dp = drow + (size_t)vt * VEC;
   auto issue = [&](int k) {
@@ -474,12 +478,12 @@ __device__ __forceinline__ void stream_tile(const E* trow, const E* drow, int v0
         float ft[2 * VEC], fd[2 * VEC];
         unpack2<E, VEC>(q[0], q[kThreads], ft);
         unpack2<E, VEC>(q[2 * kThreads], q[3 * kThreads], fd);
-        pair_update<2 * VEC, IDX, VEC, SEPT>(ta, da, ft, fd, va * VEC, c, vb * VEC, cd);
+        pair_update<2 * VEC, IDX, VEC, SEPT>(ta, da, ft, fd, va * VEC, c, cd);
       } else if (va < v1) {
         float ft[VEC], fd[VEC];
         IO<E, VEC>::unpack(q[0], ft);
         IO<E, VEC>::unpack(q[2 * kThreads], fd);
-        pair_update<VEC, IDX, VEC, SEPT>(ta, da, ft, fd, va * VEC, c, 0, cd);
+        pair_update<VEC, IDX, VEC, SEPT>(ta, da, ft, fd, va * VEC, c, cd);
       }
     } else {
 #pragma unroll
@@ -490,13 +494,13 @@ __device__ __forceinline__ void stream_tile(const E* trow, const E* drow, int v0
           const uint4 r0 = q[(2 * h) * kThreads], r1 = q[(2 * h + 1) * kThreads];
           unpack2<E, VEC>(r0, r1, ft);
           if constexpr (KIND == K_TSUM) {
-            tsum_update<2 * VEC, VEC>(ta, ft, pa * VEC, c, pb * VEC);
+            tsum_update<2 * VEC, VEC>(ta, ft, pa * VEC, c);
           } else {
             if (vmax_nan<2 * VEC>(ft) > ta.m) {
               best[0] = r0;
               best[1] = r1;
             }
-            argmax_update<2 * VEC, VEC>(ta, ft, pa * VEC, pb * VEC);
+            argmax_update<2 * VEC, VEC>(ta, ft, pa * VEC);
           }
         } else if (pa < v1) {
           float ft[VEC];
@@ -577,7 +581,7 @@ __device__ __forceinline__ void stream_tile_sh(const E* trv, const E* drv, int v
       const uint4 n0 = lane < 31 ? q[2 * kThreads + 1] : qx[0];
       const uint4 n1 = lane < 31 ? q[3 * kThreads + 1] : qx[1];
       unpack2<E, VEC>(shift_vec<E, M>(q[2 * kThreads], n0, sel), shift_vec<E, M>(q[3 * kThreads], n1, sel), fd);
-      pair_update<2 * VEC, IDX, VEC, SEPT>(ta, da, ft, fd, va * VEC, c, vb * VEC, cd);
+      pair_update<2 * VEC, IDX, VEC, SEPT>(ta, da, ft, fd, va * VEC, c, cd);
       continue;
     }
     // stochastic rows (and the NKL tile's last odd vector): one vector of each row at a time,
@@ -591,7 +595,7 @@ __device__ __forceinline__ void stream_tile_sh(const E* trv, const E* drv, int v
         IO<E, VEC>::unpack(q[h * kThreads], ft);
         const uint4 n = lane < 31 ? q[(2 + h) * kThreads + 1] : qx[h];
         IO<E, VEC>::unpack(shift_vec<E, M>(q[(2 + h) * kThreads], n, sel), fd);
-        pair_update<VEC, IDX, VEC, SEPT>(ta, da, ft, fd, v * VEC, c, 0, cd);
+        pair_update<VEC, IDX, VEC, SEPT>(ta, da, ft, fd, v * VEC, c, cd);
       }
     }
   }
@@ -688,8 +692,8 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
   static_assert(!SH || (PH && !ARGMAX), "shifted pairs are phased pair tiles");
   // PH: the row's offset in elements within the 16-byte grid; indices are counted from the
   // aligned base until the partial is written
-  int ph = 0;
   {
+    int ph = 0;
     uint4 best[2];
     // Rows at any element alignment (PH): the whole aligned 16-byte blocks of the chunk are
     // streamed as vectors of the aligned bases trv and drv (row element e is element
@@ -705,33 +709,37 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
     // v + dw + 1, from element sft on
     const int sft = (phd - ph + VEC) % VEC, dw = (phd - ph - sft) / VEC;
     const int vf0 = (e_begin + ph + VEC - 1) / VEC, vf1 = (e_end + ph) / VEC;
+    // vectors between the start of vf0's 128-byte line and vf0 (the streams' rotation)
+    const int rot = (int)((reinterpret_cast<uintptr_t>(trv + (size_t)vf0 * VEC) >> 4) & 7u);
     // The partial blocks at the chunk's ends, head [e_begin, hend) and tail [tbeg, e_end),
-    // fewer than VEC elements each: element j of the head is thread j's, element j of the
-    // tail thread VEC + j's; each copies the target block and the draft block holding its
-    // element beside the ring and folds the element in after the stream.
-    __shared__ uint4 s_edge[2 * VEC][2];  // [thread][target, draft]
-    // this thread's edge element, or -1 (recomputed after the stream, so that it is not held
-    // through it)
-    auto edge_elem = [&]() -> int {
-      if (threadIdx.x >= 2 * VEC) return -1;
-      const int side = threadIdx.x / VEC;
+    // fewer than VEC elements each: element j of the head is edge thread j's, element j of
+    // the tail edge thread VEC + j's -- the block's last 2·VEC threads, whose share of a
+    // tile's last stage is the smallest. Each copies the target block and the draft block
+    // holding its element beside the ring and folds the element in after the stream. What
+    // the fold needs -- the element's index from the aligned base and its draft position --
+    // goes to shared memory beside the blocks, so that nothing of it is held in registers
+    // through the stream.
+    __shared__ uint4 s_edge[2 * VEC][2];  // [edge thread][target, draft]
+    __shared__ int s_eidx[2 * VEC][2];    // [edge thread][e + ph or -1, (e + phd) % VEC]
+    const int et = (int)threadIdx.x - (kThreads - 2 * VEC);  // edge thread index, if >= 0
+    if (PH && et >= 0) {
+      const int side = et / VEC;
       const int hend = min(e_end, vf0 * VEC - ph), tbeg = max(hend, vf1 * VEC - ph);
-      const int e = (side == 0 ? e_begin : tbeg) + (int)(threadIdx.x % VEC);
-      return e < (side == 0 ? hend : e_end) ? e : -1;
-    };
-    if (PH) {
-      const int e = edge_elem();
+      int e = (side == 0 ? e_begin : tbeg) + et % VEC;
+      if (e >= (side == 0 ? hend : e_end)) e = -1;
+      s_eidx[et][0] = e >= 0 ? e + ph : -1;
+      s_eidx[et][1] = (e + phd) % VEC;
       if (e >= 0) {
         const size_t tb = (size_t)((e + ph) / VEC) * VEC, db = (size_t)((e + phd) / VEC) * VEC;
         if (in_ext(trv + tb, 16, p.x_target, p.status))
-          cp_async16((uint32_t)__cvta_generic_to_shared(&s_edge[threadIdx.x][0]), trv + tb);
+          cp_async16((uint32_t)__cvta_generic_to_shared(&s_edge[et][0]), trv + tb);
         if (kind == K_PAIR && in_ext(drv + db, 16, p.x_draft, p.status))
-          cp_async16((uint32_t)__cvta_generic_to_shared(&s_edge[threadIdx.x][1]), drv + db);
+          cp_async16((uint32_t)__cvta_generic_to_shared(&s_edge[et][1]), drv + db);
       }
     }
     // (stream_tile's last wait covers the edge copies too)
     if constexpr (ARGMAX) {
-      stream_tile<E, VEC, MODE, K_ARGMAX>(trv, drv, vf0, vf1, c, cd, ta, da, dsm, best, p);
+      stream_tile<E, VEC, MODE, K_ARGMAX>(trv, drv, vf0, vf1, rot, c, cd, ta, da, dsm, best, p);
       // the lowest index of the thread's maximum, from the raw vectors of its group
       if (ta.g0 >= 0) {
         float f[2 * VEC];
@@ -740,21 +748,23 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
 #pragma unroll
         for (int j = 2 * VEC - 2; j >= 0; --j)
           if (f[j] == ta.m) k = j;
-        ta.g0 = k < VEC ? ta.g0 + k : ta.g1 + (k - VEC);
+        const int g = ta.g0 & ~1;  // the group's first vector; its second is kThreads vectors on
+        ta.g0 = k < VEC ? g + k : g + kThreads * VEC + (k - VEC);
       }
     } else {
       if (kind == K_PAIR) {
         if (SH && sft != 0)
           stream_tile_shifted<E, VEC, MODE>(sft, trv, drv, vf0, vf1, dw, c, cd, ta, da, dsm, p);
         else
-          stream_tile<E, VEC, MODE, K_PAIR>(trv, drv, vf0, vf1, c, cd, ta, da, dsm, best, p);
+          stream_tile<E, VEC, MODE, K_PAIR>(trv, drv, vf0, vf1, rot, c, cd, ta, da, dsm, best, p);
       } else if constexpr (MODE != M_NKL) {
-        stream_tile<E, VEC, MODE, K_TSUM>(trv, drv, vf0, vf1, c, cd, ta, da, dsm, best, p);
+        stream_tile<E, VEC, MODE, K_TSUM>(trv, drv, vf0, vf1, rot, c, cd, ta, da, dsm, best, p);
       }
     }
-    const int e = PH ? edge_elem() : -1;
-    if (e >= 0) {
-      const float x = sh_elem<E>(reinterpret_cast<const E*>(&s_edge[threadIdx.x][0]), (e + ph) % VEC);
+    // (the thread's own shared-memory entries: no barrier needed)
+    const int ea = (PH && et >= 0) ? s_eidx[et][0] : -1;  // e + ph
+    if (ea >= 0) {
+      const float x = sh_elem<E>(reinterpret_cast<const E*>(&s_edge[et][0]), ea % VEC);
       if constexpr (ARGMAX) {
         ta.hi = max_nan(ta.hi, x);
         ta.lo = fminf(ta.lo, x);
@@ -762,30 +772,30 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
         // the sums; the maximum and its index are kept apart (the recorded group stays
         // the one that holds the thread's maximum over whole vectors)
         const float m0 = ta.m;
-        const int g0 = ta.g0, g1 = ta.g1;
+        const int g0 = ta.g0;
         const float xt[1] = {x};
         if (kind == K_PAIR) {
-          const float xd[1] = {sh_elem<E>(reinterpret_cast<const E*>(&s_edge[threadIdx.x][1]), (e + phd) % VEC)};
-          pair_update<1, false, 0, SEPT>(ta, da, xt, xd, 0, c, 0, cd);
+          const float xd[1] = {sh_elem<E>(reinterpret_cast<const E*>(&s_edge[et][1]), s_eidx[et][1])};
+          pair_update<1, false, 0, SEPT>(ta, da, xt, xd, 0, c, cd);
         } else {
           tsum_update<1, 0>(ta, xt, 0, c);
         }
         ta.m = m0;
         ta.g0 = g0;
-        ta.g1 = g1;
       }
       // an edge element holding the thread's maximum carries its exact index (a head
       // element precedes every whole vector of the chunk: it wins ties)
-      if (x > ta.m || (x == ta.m && ta.g0 >= 0 && e + ph < ta.g0)) {
+      if (x > ta.m || (x == ta.m && ta.g0 >= 0 && ea < ta.g0)) {
         ta.m = x;
-        ta.g0 = e + ph;
-        if constexpr (!ARGMAX) ta.g1 = kExactIdx;
+        ta.g0 = ARGMAX ? ea : exact_idx(ea);  // argmax rows hold resolved indices already
       }
     }
   }
 
-  Partial part = reduce_tile<BlockSync, E, VEC, SEPT, 0, ARGMAX>(kind, ta, da, c, trow - ph, cd, &p.x_target, p.status);
-  if (PH && part.tidx != INT_MAX) part.tidx -= ph;  // from the aligned base to the row
+  // the row's offset again (recomputed rather than held through the stream)
+  const int ph2 = PH ? (int)(((uintptr_t)trow & 15u) / sizeof(E)) : 0;
+  Partial part = reduce_tile<BlockSync, E, VEC, SEPT, ARGMAX>(kind, ta, da, c, trow - ph2, cd, &p.x_target, p.status);
+  if (PH && part.tidx != INT_MAX) part.tidx -= ph2;  // from the aligned base to the row
   if (threadIdx.x == 0) {
     float4* dst = reinterpret_cast<float4*>(p.part + tile);
     const bool okw = in_ext(dst, sizeof(Partial), p.x_ws, p.status) && in_ext(p.cnt + b, sizeof(unsigned), p.x_ws, p.status);
