@@ -287,10 +287,11 @@ cudaError_t launch_sample2(bool bf16, SamplePath path, const SampleParams& sp, l
 
 // Fused multi-draft tiles: when given, the verification launches multi_rows_kernel over
 // (group, row, chunk) tiles instead of rows_kernel over (row, chunk) tiles. A fused tile
-// reads 2K rows of a chunk of up to 131072 tokens, whole rows at the usual vocabulary
-// sizes (G=64, K=3, same box: 222.5 us, against 229.5 with 65536-token chunks and 242.1
-// with 32768; shorter chunks cost more per-tile fixed work).
-constexpr int kMultiChunk = 131072;
+// reads 2K rows of a chunk of up to 65536 tokens (G=64, K=3, V=128256, same box: 176.4 us
+// against 177.8 with whole rows and 177.3 with three chunks per row: the shorter tiles even
+// out the last wave; with the pair stage on packed data the per-tile fixed work weighs less
+// than it did at 229.5 against 222.5 us).
+constexpr int kMultiChunk = 65536;
 struct MultiTiles {
   int K = 0;
   PairParams pp;
