@@ -931,13 +931,54 @@ __device__ __forceinline__ float row_nkl(const RowStat& r, float invT, float inv
   return kl * inv_lnV;
 }
 
+// A row whose tiles streamed only the whole 16-byte blocks of each chunk (a row off the
+// 16-byte grid, or of a length that is not a whole number of blocks): the elements of the
+// partial blocks at every chunk's two ends, which no tile read, are folded into the row's
+// merge, each element as a partial of its own (its value as the maximum and reference,
+// sums of 1).
+template <typename E>
+struct RowEdges {
+  const E* t = nullptr;  // the target row; null: the row has no partial blocks
+  const E* d = nullptr;  // the draft row of a pair (draft statistics folded too), else null
+  int ph = 0;            // the target row's offset in elements within the 16-byte grid
+  int V = 0, ce = 0;     // vocabulary; chunk length (a multiple of the vector width)
+  bool sums = false;     // the sums (pair and sum rows) besides the maximum and its index
+  bool sept = false;     // separate draft temperature: ds2 (the draft at the target scale) too
+  const Ext* xt = nullptr;  // bounds-checked build: the buffers of t and d
+  const Ext* xd = nullptr;
+  uint32_t* status = nullptr;
+};
+
 // ds is merged at the draft scale cd, dk and ds2 at the target scale c. A group of W
 // lanes (aligned within the warp; every lane of the warp calls it) merges one row.
-template <int W = 32>
-__device__ __forceinline__ RowStat merge_row(const Partial* pp, int nchunks, float c, float cd) {
+template <int W = 32, typename E = float>
+__device__ __forceinline__ RowStat merge_row(const Partial* pp, int nchunks, float c, float cd,
+                                             const RowEdges<E>& edges = RowEdges<E>()) {
+  constexpr int VEC = 16 / (int)sizeof(E);
   const int lane = threadIdx.x & (W - 1);
   float tm = -INFINITY, ts = 0.f, dm = -INFINITY, ds = 0.f, dk = 0.f, ds2 = 0.f;
   int idx = INT_MAX, bad = 0;
+  // one element of a partial block: index e, target value xt, draft value xd
+  auto fold_elem = [&](int e, float xt, float xd) {
+    bad |= (!isfinite(xt) || (edges.d != nullptr && !isfinite(xd))) ? 1 : 0;
+    if (xt > tm || (xt == tm && e < idx)) idx = e;
+    const float M = fmaxf(tm, xt);
+    if (edges.sums) ts = rescale(ts, tm, M, c) + ex2((xt - M) * c);
+    tm = M;
+    if (edges.d != nullptr) {
+      const float D = fmaxf(dm, xd);
+      const float f0 = (dm == -INFINITY) ? 0.f : ex2((dm - D) * c);
+      const float g0 = (dm == -INFINITY) ? 0.f : ex2((dm - D) * cd);
+      const float f1 = ex2((xd - D) * c);
+      ds = ds * g0 + ex2((xd - D) * cd);
+      dk = dk * f0 + f1 * (xd - xt);
+      if (edges.sept) ds2 = ds2 * f0 + f1;
+      dm = D;
+    }
+  };
+  auto elem = [&](const E* row, const Ext* x, int e) -> float {
+    return (x == nullptr || in_ext(row + e, sizeof(E), *x, edges.status)) ? elem_at<E>(row, e) : 0.f;
+  };
   for (int ch = lane; ch < nchunks; ch += W) {
     const float4 lo = __ldcg(reinterpret_cast<const float4*>(pp + ch));
     const float4 hi = __ldcg(reinterpret_cast<const float4*>(pp + ch) + 1);
@@ -958,6 +999,32 @@ __device__ __forceinline__ RowStat merge_row(const Partial* pp, int nchunks, flo
     dk = dk * f0 + qdk * f1;
     ds2 = ds2 * f0 + qds2 * f1;
     dm = D;
+  }
+  if (edges.t != nullptr) {
+    // The partial blocks' elements, spread over the W lanes: chunk ch's head [e_begin, hend)
+    // and tail [tbeg, e_end) -- as the tile kernel leaves them out of its stream, fewer than
+    // VEC each -- take slots ch * NE ... ch * NE + NE - 1, and lane l folds slots l, l + W,
+    // ... (a few loads per lane, issued together), each element as a partial of its own; the
+    // lanes' states are then merged with the chunk partials' below.
+    constexpr int NE = 2 * (VEC - 1);
+    const int ph = edges.ph;
+#pragma unroll 4
+    for (int f = lane; f < nchunks * NE; f += W) {
+      const int ch = f / NE, k = f - ch * NE;
+      const int e_begin = ch * edges.ce, e_end = min(e_begin + edges.ce, edges.V);
+      const int vf0 = (e_begin + ph + VEC - 1) / VEC, vf1 = (e_end + ph) / VEC;
+      const int hend = min(e_end, vf0 * VEC - ph), tbeg = max(hend, vf1 * VEC - ph);
+      const int nh = hend - e_begin, nt = e_end - tbeg;
+      if (nh + nt > NE) {
+        // a chunk without a whole block (a tiny vocabulary): its first slot's lane folds it all
+        if (k == 0)
+          for (int e = e_begin; e < e_end; ++e)
+            fold_elem(e, elem(edges.t, edges.xt, e), edges.d ? elem(edges.d, edges.xd, e) : 0.f);
+        continue;
+      }
+      const int e = k < nh ? e_begin + k : (k - nh < nt ? tbeg + (k - nh) : -1);
+      if (e >= 0) fold_elem(e, elem(edges.t, edges.xt, e), edges.d ? elem(edges.d, edges.xd, e) : 0.f);
+    }
   }
   RowStat r;
   r.tm = warp_max<W>(tm);

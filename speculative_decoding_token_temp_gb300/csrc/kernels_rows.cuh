@@ -191,6 +191,30 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
       s_par[j] = p.parent[j];
     }
   }
+  // The partial 16-byte blocks at the chunks' ends of stochastic row ii (rows off the grid,
+  // or of a length that is not a whole number of blocks), which its tiles left out, for the
+  // merge.
+  auto edges_of = [&](int ii) {
+    constexpr int VEC = 16 / (int)sizeof(E);
+    if constexpr (!is_stoch(MODE)) return RowEdges<E>();  // the other modes' tiles fold them
+    const int r = row0 + ii;
+    const E* trow = target + ((MODE == M_NKL) ? (size_t)r + b : (size_t)r) * V;
+    const int ph = (int)(((uintptr_t)trow & 15u) / sizeof(E));
+    RowEdges<E> ed;
+    if (ph == 0 && p.V % VEC == 0) return ed;  // chunk lengths are whole vectors: none
+    const bool pair = (MODE == M_NKL) || (is_stoch(MODE) && ii < gb);
+    ed.t = trow;
+    ed.d = pair ? draft + ((MODE == M_NKL) ? (size_t)r : (size_t)(r - b)) * V : nullptr;
+    ed.ph = ph;
+    ed.V = p.V;
+    ed.ce = p.chunk_elems;
+    ed.sums = MODE != M_GREEDY && MODE != M_TREE;
+    ed.sept = MODE == M_STOCH2;
+    ed.xt = &p.x_target;
+    ed.xd = &p.x_draft;
+    ed.status = p.status;
+    return ed;
+  };
   if (p.nchunks <= 16) {
     // two rows per warp (one per half-warp): one round of partial reads for up to 2 NW rows
     const int half = lane >> 4;
@@ -198,14 +222,14 @@ __device__ __noinline__ void finalize(const RowsParams& p, int b, int gb, int ro
       const int ii = min(i + half, R - 1);
       const Partial* pr = p.part + (size_t)(row0 + ii) * p.nchunks;
       const bool okp = in_ext(pr, sizeof(Partial) * p.nchunks, p.x_ws, p.status);
-      const RowStat r = merge_row<16>(okp ? pr : p.part, okp ? p.nchunks : 0, c, p.cd);
+      const RowStat r = merge_row<16, E>(okp ? pr : p.part, okp ? p.nchunks : 0, c, p.cd, edges_of(ii));
       if ((lane & 15) == 0 && i + half < R) rs[i + half] = r;
     }
   } else {
     for (int i = warp; i < R; i += NW) {
       const Partial* pr = p.part + (size_t)(row0 + i) * p.nchunks;
       const bool okp = in_ext(pr, sizeof(Partial) * p.nchunks, p.x_ws, p.status);
-      const RowStat r = merge_row(okp ? pr : p.part, okp ? p.nchunks : 0, c, p.cd);
+      const RowStat r = merge_row<32, E>(okp ? pr : p.part, okp ? p.nchunks : 0, c, p.cd, edges_of(i));
       if (lane == 0) rs[i] = r;
     }
   }
@@ -697,10 +721,12 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
     uint4 best[2];
     // Rows at any element alignment (PH): the whole aligned 16-byte blocks of the chunk are
     // streamed as vectors of the aligned bases trv and drv (row element e is element
-    // e + ph of trv, e + phd of drv); the partial blocks at the chunk's ends, head
-    // [e_begin, hend) and tail [tbeg, e_end), are copied beside the ring by threads 0 and 1
-    // (the target's block, and the one or two draft blocks holding the same elements) and
-    // folded in element by element.
+    // e + ph of trv, e + phd of drv). The elements of the partial blocks at the chunk's
+    // ends: stochastic rows leave them to the row's merge in the finalisation (RowEdges),
+    // so that their tiles carry no code for them (measured: the headline batch one element
+    // off the grid, 192.1 -> 185.0 us); NKL, greedy and tree tiles fold them themselves
+    // (TE), which measured faster for them (NKL 150.7 against 155.6 us).
+    constexpr bool TE = PH && !is_stoch(MODE);
     if constexpr (PH) ph = (int)(((uintptr_t)trow & 15u) / sizeof(E));
     const int phd = (PH && kind == K_PAIR) ? (int)(((uintptr_t)drow & 15u) / sizeof(E)) : ph;
     const E* trv = trow - ph;
@@ -711,7 +737,7 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
     const int vf0 = (e_begin + ph + VEC - 1) / VEC, vf1 = (e_end + ph) / VEC;
     // vectors between the start of vf0's 128-byte line and vf0 (the streams' rotation)
     const int rot = (int)((reinterpret_cast<uintptr_t>(trv + (size_t)vf0 * VEC) >> 4) & 7u);
-    // The partial blocks at the chunk's ends, head [e_begin, hend) and tail [tbeg, e_end),
+    // TE: the partial blocks at the chunk's ends, head [e_begin, hend) and tail [tbeg, e_end),
     // fewer than VEC elements each: element j of the head is edge thread j's, element j of
     // the tail edge thread VEC + j's -- the block's last 2·VEC threads, whose share of a
     // tile's last stage is the smallest. Each copies the target block and the draft block
@@ -719,10 +745,10 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
     // the fold needs -- the element's index from the aligned base and its draft position --
     // goes to shared memory beside the blocks, so that nothing of it is held in registers
     // through the stream.
-    __shared__ uint4 s_edge[2 * VEC][2];  // [edge thread][target, draft]
-    __shared__ int s_eidx[2 * VEC][2];    // [edge thread][e + ph or -1, (e + phd) % VEC]
+    __shared__ uint4 s_edge[TE ? 2 * VEC : 1][2];  // [edge thread][target, draft]
+    __shared__ int s_eidx[TE ? 2 * VEC : 1][2];    // [edge thread][e + ph or -1, (e + phd) % VEC]
     const int et = (int)threadIdx.x - (kThreads - 2 * VEC);  // edge thread index, if >= 0
-    if (PH && et >= 0) {
+    if (TE && et >= 0) {
       const int side = et / VEC;
       const int hend = min(e_end, vf0 * VEC - ph), tbeg = max(hend, vf1 * VEC - ph);
       int e = (side == 0 ? e_begin : tbeg) + et % VEC;
@@ -737,7 +763,7 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
           cp_async16((uint32_t)__cvta_generic_to_shared(&s_edge[et][1]), drv + db);
       }
     }
-    // (stream_tile's last wait covers the edge copies too)
+    // (the stream's last wait covers the edge copies too)
     if constexpr (ARGMAX) {
       stream_tile<E, VEC, MODE, K_ARGMAX>(trv, drv, vf0, vf1, rot, c, cd, ta, da, dsm, best, p);
       // the lowest index of the thread's maximum, from the raw vectors of its group
@@ -762,7 +788,7 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
       }
     }
     // (the thread's own shared-memory entries: no barrier needed)
-    const int ea = (PH && et >= 0) ? s_eidx[et][0] : -1;  // e + ph
+    const int ea = (TE && et >= 0) ? s_eidx[et][0] : -1;  // e + ph
     if (ea >= 0) {
       const float x = sh_elem<E>(reinterpret_cast<const E*>(&s_edge[et][0]), ea % VEC);
       if constexpr (ARGMAX) {
@@ -774,12 +800,8 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
         const float m0 = ta.m;
         const int g0 = ta.g0;
         const float xt[1] = {x};
-        if (kind == K_PAIR) {
-          const float xd[1] = {sh_elem<E>(reinterpret_cast<const E*>(&s_edge[et][1]), s_eidx[et][1])};
-          pair_update<1, false, 0, SEPT>(ta, da, xt, xd, 0, c, cd);
-        } else {
-          tsum_update<1, 0>(ta, xt, 0, c);
-        }
+        const float xd[1] = {sh_elem<E>(reinterpret_cast<const E*>(&s_edge[et][1]), s_eidx[et][1])};
+        pair_update<1, false, 0, SEPT>(ta, da, xt, xd, 0, c, cd);  // NKL: pairs only
         ta.m = m0;
         ta.g0 = g0;
       }
@@ -795,7 +817,12 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
   // the row's offset again (recomputed rather than held through the stream)
   const int ph2 = PH ? (int)(((uintptr_t)trow & 15u) / sizeof(E)) : 0;
   Partial part = reduce_tile<BlockSync, E, VEC, SEPT, ARGMAX>(kind, ta, da, c, trow - ph2, cd, &p.x_target, p.status);
-  if (PH && part.tidx != INT_MAX) part.tidx -= ph2;  // from the aligned base to the row
+  if constexpr (PH) {
+    if (part.tidx != INT_MAX) part.tidx -= ph2;  // from the aligned base to the row
+    // stochastic rows: a chunk without a whole block streamed nothing; its statistics are
+    // empty, not non-finite (its elements are the merge's)
+    if (is_stoch(MODE) && (e_end + ph2) / VEC <= (e_begin + ph2 + VEC - 1) / VEC) part.bad = 0;
+  }
   if (threadIdx.x == 0) {
     float4* dst = reinterpret_cast<float4*>(p.part + tile);
     const bool okw = in_ext(dst, sizeof(Partial), p.x_ws, p.status) && in_ext(p.cnt + b, sizeof(unsigned), p.x_ws, p.status);
