@@ -480,7 +480,16 @@ def run_ours(args):
         modes["stochastic_draft_T0.4_B256_g8_V128256"] = {
             "us_per_call": t_x * 1e6, "GBps": ab["stochastic"] / t_x / 1e9,
             "frac_of_peak": ab["stochastic"] / t_x / 1e9 / hbm,
-            "note": "target T 0.6, drafts at T_d 0.4: the draft rows are summed at both temperatures"}
+            "note": "target T 0.6, drafts at T_d 0.4, with the NKL outputs: the draft rows are summed at "
+                    "both temperatures"}
+        xn_out = {}
+        xnfn = lambda: api.spec_verify_stochastic_ex(call.t, call.d, call.tok, w.T, call.ua, call.us,  # noqa: E731
+                                                     gamma=gam, out=xn_out, temperature_draft=0.4, want_nkl=False)
+        t_xn = time_mode(xnfn, 200, 10, dev)
+        modes["stochastic_draft_T0.4_no_nkl_B256_g8_V128256"] = {
+            "us_per_call": t_xn * 1e6, "GBps": ab["stochastic"] / t_xn / 1e9,
+            "frac_of_peak": ab["stochastic"] / t_xn / 1e9 / hbm,
+            "note": "the same without the NKL outputs: the draft rows at T_d only (single-scale tiles)"}
         a_out = {}
         afn = lambda: api.spec_verify_stochastic_ex(call.t, call.d, call.tok, w.T, call.ua, call.us,  # noqa: E731
                                                     gamma=gam, out=a_out, position=pos, min_block_len=3,

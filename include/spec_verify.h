@@ -216,7 +216,9 @@ typedef struct {
 typedef struct {
   /* stochastic: > 0 and finite = the temperature T_d the drafts were drawn at ([PD] 4.4:
    * draft 0.3-0.5, target 0.7-0.9). q = softmax(draft / T_d) for q(x), alpha and the
-   * residual; NKL still scales both rows by the target temperature ([CoD] 3.2).
+   * residual; NKL still scales both rows by the target temperature ([CoD] 3.2), so a call
+   * that asks for nkl or nkl_mask sums each draft row at both temperatures (one more
+   * exponential per draft logit), and one that asks for neither does not.
    * 0 = T_d equals the target temperature. */
   float temperature_draft;
   /* stochastic, NKL: device [B] or NULL. The 1-based position of each sequence's first

@@ -749,8 +749,10 @@ __device__ __forceinline__ void pair_update(TAcc& a, DAcc& d, const float (&t)[V
     d.s = add2(d.s, exp_sum2<VEC>(z, cd, d.nmc, eq));
     d.s2 = add2(d.s2, exp_sum2<VEC>(z, c, d.nmc2, ed));
   } else {
-    lazy_ref(d.mr, d.mth, d.nmc, d.s, &d.k, dm, c);
-    d.s = add2(d.s, exp_sum2<VEC>(z, c, d.nmc, ed));
+    // the draft at its own scale cd (cd == c unless the draft's temperature differs and
+    // the caller wants no NKL, which alone reads k at the target scale)
+    lazy_ref(d.mr, d.mth, d.nmc, d.s, &d.k, dm, cd);
+    d.s = add2(d.s, exp_sum2<VEC>(z, cd, d.nmc, ed));
   }
   if constexpr (VEC == 1) {
     d.k.x = fmaf(ed[0], z[0] - t[0], d.k.x);
@@ -848,7 +850,7 @@ __device__ __forceinline__ Partial reduce_tile(int kind, const TAcc& ta, const D
     v0 = warp_sum(rescale(ta.s.x + ta.s.y, ta.mr, TM, c));
     if (kind == K_TSUM) v1 = warp_min(ta.lo);
     if (kind == K_PAIR) {
-      const float fd = (da.mr == -INFINITY) ? 0.f : ex2((da.mr - DM) * (SEPT ? cd : c));
+      const float fd = (da.mr == -INFINITY) ? 0.f : ex2((da.mr - DM) * cd);
       v2 = warp_sum((da.s.x + da.s.y) * fd);
       if constexpr (SEPT) {
         const float ft = (da.mr == -INFINITY) ? 0.f : ex2((da.mr - DM) * c);

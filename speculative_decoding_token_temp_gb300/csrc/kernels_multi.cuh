@@ -733,7 +733,7 @@ __global__ void __launch_bounds__(kThreads, 2) multi_rows_kernel(const __grid_co
   const int kind = pair ? (STOCH ? K_PAIR : K_ARGMAX) : (STOCH ? K_TSUM : K_ARGMAX);
 #pragma unroll
   for (int a = 0; a < K; ++a) {
-    const Partial part = reduce_tile<BlockSync, E, VEC>(kind, ta[a], da[a], c, trow[a], 0.f, &p.x_target, p.status);
+    const Partial part = reduce_tile<BlockSync, E, VEC>(kind, ta[a], da[a], c, trow[a], cq, &p.x_target, p.status);
     const size_t row = ((size_t)g * K + a) * (gamma + 1) + r;
     float4* dst = reinterpret_cast<float4*>(p.part + row * nchunks + chunk);
     if (threadIdx.x == 0 && in_ext(dst, sizeof(Partial), p.x_ws, p.status)) {

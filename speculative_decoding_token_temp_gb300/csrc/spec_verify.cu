@@ -528,9 +528,13 @@ spec_status stochastic_impl(spec_batch g, spec_dtype dtype, const void* target_l
   rp.g_tok = greedy_tokens;
   // fused multi-draft tiles: (group, row, chunk), one per group row instead of per sequence row
   const long long tiles = mt ? (long long)(g.B / mt->K) * (g.gamma + 1) * L.nchunks : L.rows * L.nchunks;
-  const cudaError_t le = mt     ? launch_multi<M_STOCH>(bf16, *mt, rp, tiles, stream)
-                         : sept ? launch_rows<M_STOCH2>(bf16, path, rp, tiles, stream)
-                                : launch_rows<M_STOCH>(bf16, path, rp, tiles, stream);
+  // a draft temperature of its own needs the draft row at both scales only for the NKL
+  // outputs (both rows at the target's temperature); without them the single-scale tiles
+  // serve, the draft at its own scale cd
+  const bool two_scales = sept && (nkl != nullptr || nkl_mask != nullptr);
+  const cudaError_t le = mt           ? launch_multi<M_STOCH>(bf16, *mt, rp, tiles, stream)
+                         : two_scales ? launch_rows<M_STOCH2>(bf16, path, rp, tiles, stream)
+                                      : launch_rows<M_STOCH>(bf16, path, rp, tiles, stream);
   if (le != cudaSuccess) return SPEC_ERR_CUDA;
 
   SampleParams sp;

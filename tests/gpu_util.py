@@ -35,16 +35,18 @@ def _offsets(offset):
     return offset if isinstance(offset, tuple) else (offset, offset)
 
 
-def run_stochastic(w, dev, T=None, delta=0.15, offset=0, options=None):
+def run_stochastic(w, dev, T=None, delta=0.15, offset=0, options=None, want_nkl=True):
     """Call spec_verify_stochastic (spec_verify_stochastic_ex when `options` is given: a
     dict of its keywords, numpy arrays for position) on a workload; offset (an int, or a
-    (target, draft) pair) shifts the logit buffers by that many elements."""
+    (target, draft) pair) shifts the logit buffers by that many elements; want_nkl=False
+    asks for no NKL outputs."""
     T = w.T if T is None else T
     ot, od = _offsets(offset)
     t = put(w.target, dev, ot)
     d = put(w.draft, dev, od)
     cu = None if w.dense else torch.from_numpy(w.cu_draft).to(dev)
-    kw = dict(cu_draft=cu, gamma=w.gamma_max if not w.dense else int(w.gammas[0]) if w.B else 0, nkl_delta=delta)
+    kw = dict(cu_draft=cu, gamma=w.gamma_max if not w.dense else int(w.gammas[0]) if w.B else 0, nkl_delta=delta,
+              want_nkl=want_nkl)
     if options is None:
         res = api.spec_verify_stochastic(t, d, to_dev(w.tokens, dev), T, to_dev(w.u_accept, dev),
                                          to_dev(w.u_sample, dev), **kw)
@@ -90,6 +92,8 @@ def compare_stochastic(w, res, seqs, T=None, delta=0.15, check_greedy=True, T_dr
             for k in ("p_x", "q_x", "alpha"):
                 got = res[k][d0:d0 + g].astype(np.float64)
                 assert np.allclose(got, r[k], rtol=REL, atol=1e-30), (b, k, got, r[k])
+            if "nkl" not in res:
+                continue  # a call without the NKL outputs
             got = res["nkl"][d0:d0 + g].astype(np.float64)
             assert np.allclose(got, r["nkl"], rtol=REL, atol=NKL_ABS), (b, got, r["nkl"])
             m = res["nkl_mask"][d0:d0 + g]

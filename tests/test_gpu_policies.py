@@ -52,6 +52,20 @@ def test_separate_draft_temperature(dev, V, dtype, offset):
     compare_stochastic(w, res, range(w.B), T_draft=0.4)
 
 
+@pytest.mark.parametrize("V,dtype,offset", [(128256, synth.BF16, 0), (5000, synth.BF16, 1), (40000, synth.F32, 0),
+                                            (50257, synth.BF16, 0)])
+def test_separate_draft_temperature_without_nkl(dev, V, dtype, offset):
+    """Without the NKL outputs (the only ones that need the draft row at the target's
+    temperature as well) a call with its own draft temperature runs on the single-scale
+    tiles, the draft at T_d alone: decisions, p(x), q(x), alpha and the greedy outputs as the
+    oracle's, on aligned rows, rows shifted by one element, and a vocabulary off the grid."""
+    w = handmade(4, 5, V, dtype, T=0.8, seed=V + 7 + offset)
+    w.draft[:] = synth.storage(0.5 * O.widen(w.draft, w.dtype), dtype)
+    res = run_stochastic(w, dev, offset=offset, options={"temperature_draft": 0.4}, want_nkl=False)
+    assert res["device_status"][0] == 0 and "nkl" not in res
+    compare_stochastic(w, res, range(w.B), T_draft=0.4)
+
+
 def test_draft_temperature_equal_to_target_is_the_plain_call(dev):
     w = handmade(6, 4, 32000, synth.BF16, T=0.7, seed=81)
     a = run_stochastic(w, dev)
