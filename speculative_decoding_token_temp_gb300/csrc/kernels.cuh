@@ -392,19 +392,18 @@ __device__ __forceinline__ float elem_at<float>(const float* row, int x) {
 }
 
 // ---------------------------------------------------------------------------
-// staged path, for rows that do not start on a 16-byte boundary (an offset base pointer,
-// or a row length whose byte size is not a multiple of 16): each warp streams its own
-// runs of a row through a private ring of shared-memory slots, filled by bulk copies
-// (cp.async.bulk, completion counted in bytes on one mbarrier per slot) of the whole
-// aligned 16-byte blocks that cover a run; its lanes then read single elements at the
-// run's phase. The first and last block may reach up to 15 bytes before the run's first
+// Staged rows (the multi-draft pair pass over rows that do not start on a 16-byte
+// boundary: an offset base pointer, or a row length whose byte size is not a multiple of
+// 16): each warp streams its own runs of a row through a private ring of shared-memory
+// slots, filled by bulk copies (cp.async.bulk, completion counted in bytes on one mbarrier
+// per slot) of the whole aligned 16-byte blocks that cover a run; its lanes then read
+// single elements at the run's phase. The first and last block may reach up to 15 bytes before the run's first
 // element or after its last; each block holds at least one element of the run, so it
 // lies on the same mapped page, and the extra bytes are never used.
 
 constexpr int kStageRowBytes = 8192;                      // one row of a pair in one block stage (twice that for a single row)
 constexpr int kWarpRowBytes = kStageRowBytes / kWarps;    // a warp's run of a row of a pair in one stage
 constexpr int kWarpSlot = kWarpRowBytes + 16;             // with room for the phase
-constexpr int kWarpStage = 2 * kWarpSlot;                 // a warp's part of one stage (two rows, or one of twice the run)
 constexpr int kRingPollLimit = 1 << 20;                   // bounded wait for a slot's bytes (SPEC_DEV_TIMEOUT)
 
 // Elements of the 16-byte block holding p that precede p.
