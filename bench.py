@@ -429,7 +429,7 @@ def run_ours(args):
     __graft_entry__.build()
     cfg = synth.HEADLINE
     from speculative_decoding_token_temp_gb300 import sharding
-    w = cfg.make(seed=sharding.rank_seed(cfg.seed, rank), B=args.batch)
+    w = cfg.make(seed=sharding.rank_seed(cfg.seed, rank), B=args.batch, V=args.vocab)
     call = StochasticCall(w, dev, host_inputs=True, offset=args.offset)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
@@ -457,8 +457,8 @@ def run_ours(args):
     e2e_val = sum_over_ranks(rows_step * e2e_steps, world, dev) / e2e_el
 
     modes = {}
-    if rank == 0 and not args.no_modes:
-        # the standalone calls, same inputs
+    if rank == 0 and not args.no_modes and w.V == cfg.V:
+        # the standalone calls, same inputs (the workload's own vocabulary only)
         res = {}
         g_out = {}
         gfn = lambda: api.spec_verify_greedy(call.t, call.tok, gamma=8, out=g_out)  # noqa: E731
@@ -535,10 +535,10 @@ def run_ours(args):
             modes["stochastic_offset1_B256_g8_V128256"] = {
                 "us_per_call": t_s * 1e6, "GBps": ab["stochastic"] / t_s / 1e9,
                 "frac_of_peak": ab["stochastic"] / t_s / 1e9 / hbm, "greedy_us_per_call": t_sg * 1e6,
-                "note": "logits one element off the 16-byte grid (as for a vocabulary whose row is not a "
-                        "multiple of 16 bytes): the stochastic call's pairs through per-warp bulk-copy rings "
-                        "read back at the row's phase; the greedy call's rows as aligned vectors with the "
-                        "phase applied to the indices"}
+                "note": "logits one element off the 16-byte grid (both rows of a pair at one offset): the "
+                        "phased tiles stream the whole aligned blocks with the offset applied to the "
+                        "indices, the partial blocks at the chunks' ends folded by the row merge "
+                        "(stochastic) or the tiles' last threads (greedy)"}
             del ts, ds, s_out, sg_out
         del res
         tw = synth.TREE.make()
@@ -583,7 +583,7 @@ def run_ours(args):
             "rows_per_s": w5.total_target / t_5, "greedy_us_per_call": t_5g * 1e6,
             "greedy_frac_of_peak": algorithmic_bytes(w5)["greedy"] / t_5g / 1e9 / hbm,
             "note": "rows of 50257 bf16 (not a whole number of 16-byte blocks): the pair tiles shift the draft "
-                    "rows' vectors to the target rows' offset; the sampler takes the staged path"}
+                    "rows' vectors to the target rows' offset, and the sampler reads them the same way"}
         del c5, w5, g5_out
         if not args.skip_ragged:
             w4 = synth.RAGGED.make()
@@ -600,7 +600,7 @@ def run_ours(args):
     cpu = None
     if world == 1 and not args.no_cpu:
         one = cpu_baseline(w)
-        allc = cpu_baseline_all_cores(cfg, cfg.seed, w.B) if w.dense and w.B == cfg.B else None
+        allc = cpu_baseline_all_cores(cfg, cfg.seed, w.B) if w.dense and w.B == cfg.B and w.V == cfg.V else None
         if allc is not None:
             allc["single_thread"] = one
         cpu = allc if allc is not None else one
@@ -608,7 +608,7 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"B{w.B}_g8_V128256_bf16: stochastic verify + NKL(delta=0.15) + greedy, one call"
+        "config": {"workload": f"B{w.B}_g8_V{w.V}_bf16: stochastic verify + NKL(delta=0.15) + greedy, one call"
                                + (f" (logits {args.offset} element(s) off the 16-byte grid: phased path)"
                                   if args.offset else ""),
                    "B": w.B, "gamma": 8, "V": w.V, "T": w.T, "seed": cfg.seed, "rows_per_step": rows_step,
@@ -617,7 +617,7 @@ def run_ours(args):
                    "parallelism": f"{world} independent shard(s), no collective"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm,
-                     "traffic": profiled_traffic() if w.B == 256 and args.offset == 0 else None,
+                     "traffic": profiled_traffic() if w.B == 256 and w.V == cfg.V and args.offset == 0 else None,
                      "kernel": "spec_verify_stochastic call (prologue_kernel + rows_kernel + sample2_kernel)",
                      "algorithmic_bytes": ab["stochastic"], "peak_source": peak_kind,
                      "peak_datasheet": datasheet_gbs(), "frac_datasheet": achieved / datasheet_gbs(),
@@ -717,6 +717,9 @@ def main():
                     help="shift the timed call's logits by N elements (N not a multiple of 8: the phased path)")
     ap.add_argument("--batch", type=int, default=None,
                     help="sequences per step (default: the workload's 256); smaller slices serve profiling")
+    ap.add_argument("--vocab", type=int, default=None, metavar="V",
+                    help="vocabulary of the timed call (default: the workload's 128256); a secondary line, e.g. "
+                         "V=50257, whose rows are not whole 16-byte blocks (the shifted path), for profiling")
     ap.add_argument("--tree", action="store_true",
                     help="time only the tree call (B=32, 12 nodes, V=128256, bf16): back-to-back and with L2 flushed "
                          "before every call; a secondary line for profiling, not the headline metric")

@@ -317,12 +317,13 @@ class Config:
     seed: int = 0
     extra: dict = field(default_factory=dict)
 
-    def make(self, T: float | None = None, seed: int | None = None, B: int | None = None):
+    def make(self, T: float | None = None, seed: int | None = None, B: int | None = None, V: int | None = None):
         s = self.seed if seed is None else seed
         nb = self.B if B is None else B
+        nv = self.V if V is None else V
         if self.kind == "tree":
-            return make_tree(nb, self.V, self.dtype, s, name=self.name)
-        return make_stochastic(nb, self.V, self.dtype, self.T[0] if T is None else T, s,
+            return make_tree(nb, nv, self.dtype, s, name=self.name)
+        return make_stochastic(nb, nv, self.dtype, self.T[0] if T is None else T, s,
                                gamma=self.gamma, gamma_range=self.gamma_range,
                                agreement=self.agreement, name=self.name)
 
