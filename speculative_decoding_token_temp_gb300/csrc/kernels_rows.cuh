@@ -705,7 +705,8 @@ __global__ void __launch_bounds__(kThreads, 4) rows_kernel(const __grid_constant
   const E* drow = static_cast<const E*>(p.draft) + ((kind == K_PAIR) ? drow_i * V : 0);
   const int e_begin = chunk * p.chunk_elems;
   const int e_end = min(e_begin + p.chunk_elems, p.V);
-  const float c = p.c, cd = p.cd;
+  // the draft's scale: the NKL call's is the target's (so the compiler keeps one register)
+  const float c = p.c, cd = (MODE == M_NKL) ? p.c : p.cd;
 
   TAcc ta;
   DAcc da;
