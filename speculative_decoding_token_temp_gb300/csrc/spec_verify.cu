@@ -12,6 +12,8 @@
 #include "plan.h"
 #include "spec_verify.h"
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <atomic>
 #include <initializer_list>
 #include <mutex>
@@ -225,6 +227,16 @@ cudaError_t launch_rows_t(const RowsParams& rp, long long tiles, cudaStream_t st
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, rp);
 }
+
+// One NVTX range per entry point, over the host side of the call (argument checks and the
+// launches it enqueues), so that a timeline shows which calls issued which kernels. With no
+// tool attached a push or pop costs a function-pointer test.
+struct ApiRange {
+  explicit ApiRange(const char* name) { nvtxRangePushA(name); }
+  ~ApiRange() { nvtxRangePop(); }
+  ApiRange(const ApiRange&) = delete;
+  ApiRange& operator=(const ApiRange&) = delete;
+};
 
 // The tile kernel's layout of the rows: every row on the 16-byte grid (vector tiles); rows
 // off the grid with one offset within it for both rows of every pair (phased vector tiles:
@@ -773,6 +785,7 @@ spec_status spec_verify_stochastic_ex(spec_batch g, spec_dtype dtype, const void
                                       uint8_t* nkl_mask, float nkl_delta, int32_t* greedy_n,
                                       int32_t* greedy_tokens, const spec_options* options, uint32_t* device_status,
                                       void* workspace, size_t workspace_bytes, spec_stream_t stream) {
+  const ApiRange range("spec_verify_stochastic");
   return stochastic_impl(g, dtype, target_logits, draft_logits, draft_tokens, temperature, u_accept, u_sample,
                          n_accepted, out_tokens, p_x, q_x, alpha, nkl, nkl_mask, nkl_delta, greedy_n, greedy_tokens,
                          options, device_status, workspace, workspace_bytes, stream, ZeroRegion());
@@ -790,6 +803,7 @@ spec_status spec_verify_greedy_ex(spec_batch g, spec_dtype dtype, const void* ta
                                   const int32_t* draft_tokens, int32_t* n_accepted, int32_t* out_tokens,
                                   const spec_options* options, uint32_t* device_status, void* workspace,
                                   size_t workspace_bytes, spec_stream_t stream) {
+  const ApiRange range("spec_verify_greedy");
   return greedy_impl(g, dtype, target_logits, draft_tokens, n_accepted, out_tokens, options, device_status,
                      workspace, workspace_bytes, stream, ZeroRegion());
 }
@@ -798,6 +812,7 @@ spec_status spec_verify_tree(int32_t B, int32_t N, int32_t V, spec_dtype dtype, 
                              const int32_t* node_tokens, const int32_t* parent, int32_t* accept_len,
                              int32_t* path_nodes, int32_t* out_tokens, uint32_t* device_status, void* workspace,
                              size_t workspace_bytes, spec_stream_t stream_) {
+  const ApiRange range("spec_verify_tree");
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
   if (B < 0 || V < 1 || V > (1 << 26)) return SPEC_ERR_INVALID_ARG;
   const int D = spec_tree_depth(parent, N);
@@ -850,6 +865,7 @@ spec_status spec_nkl(spec_batch g, spec_dtype dtype, const void* target_logits, 
 spec_status spec_nkl_ex(spec_batch g, spec_dtype dtype, const void* target_logits, const void* draft_logits,
                         float temperature, float delta, float* nkl, uint8_t* nkl_mask, const spec_options* options,
                         uint32_t* device_status, void* workspace, size_t workspace_bytes, spec_stream_t stream_) {
+  const ApiRange range("spec_nkl");
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
   spec_status st = check_batch(g);
   if (st != SPEC_OK) return st;
@@ -898,6 +914,7 @@ spec_status spec_verify_multi(spec_multi_batch m, spec_dtype dtype, int32_t stoc
                               int32_t* best_n, int32_t* best_tokens, float* pair_nkl, uint8_t* consensus,
                               uint8_t* divergence, uint32_t* device_status, void* workspace,
                               size_t workspace_bytes, spec_stream_t stream_) {
+  const ApiRange range("spec_verify_multi");
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
   spec_status st = check_multi(m);
   if (st != SPEC_OK) return st;
@@ -985,6 +1002,7 @@ spec_status spec_verify_multi(spec_multi_batch m, spec_dtype dtype, int32_t stoc
 
 spec_status spec_accept_summary(const spec_accept_stats* stats, int64_t bucket_now, int32_t window, double* out,
                                 spec_stream_t stream_) {
+  const ApiRange range("spec_accept_summary");
   if (!stats || !out || window < 1 || window > SPEC_STATS_SLOTS || !aligned_to(8, {stats, out}))
     return SPEC_ERR_INVALID_ARG;
   cudaLaunchConfig_t cfg;
@@ -1109,6 +1127,7 @@ extern "C" spec_status spec_verify_stochastic_static(
     float temperature, const float* u_accept, const float* u_sample, int32_t* n_accepted, int32_t* out_tokens,
     float* p_x, float* q_x, float* alpha, float* nkl, uint8_t* nkl_mask, float nkl_delta, int32_t* greedy_n,
     int32_t* greedy_tokens, uint32_t* device_status, spec_stream_t stream) {
+  const ApiRange range("spec_verify_stochastic_static");
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
   if (check_batch(g) != SPEC_OK) return SPEC_ERR_INVALID_ARG;
   // Everything in the scratch that must start at zero (the per-sequence tickets) or in a
