@@ -22,7 +22,7 @@ def to_dev(a, dev):
 def put(a, dev, offset=0):
     """A device copy of `a` that starts `offset` elements into its buffer (offset > 0 puts
     the rows off the 16-byte grid: the phased path when every row is a whole number of
-    16-byte blocks and both buffers are shifted alike, else the staged path)."""
+    16-byte blocks and both buffers are shifted alike, else the shifted path)."""
     if offset == 0:
         return to_dev(a, dev)
     flat = to_dev(np.ascontiguousarray(a).reshape(-1), dev)
