@@ -31,16 +31,16 @@
  *     zeroes it when it wants a fresh reading. A sequence with a data error reports
  *     n = -1, -1 in its integer outputs and NaN in its real outputs. No kernel traps
  *     or asserts; every wait (the sampler polling a sequence's decision, a warp of the
- *     staged path waiting for its bulk copies) is bounded and reports SPEC_DEV_TIMEOUT
- *     if it runs out.
+ *     multi-draft pair pass over misaligned rows waiting for its bulk copies) is bounded
+ *     and reports SPEC_DEV_TIMEOUT if it runs out.
  *   - Logits are row-major [rows, V] with V contiguous, fp32 or bf16 (raw bf16 bit
  *     patterns). Rows whose byte size is a multiple of 16 and whose base pointers are
  *     16-byte aligned take the vectorised path. Any other layout takes the phased
- *     vector path (greedy and tree rows: each tile applies its row's offset within the
- *     16-byte grid) or the staged path (row pairs), with the same results: both read
- *     whole aligned 16-byte blocks, so they may read up to 15 bytes before a row's first
- *     or after its last element, always inside a 16-byte block that holds one of the
- *     row's elements (never used, never written).
+ *     vector path (each tile applies its row's offset within the 16-byte grid; row pairs
+ *     whose two rows sit at different offsets have the draft's vectors shifted to the
+ *     target's), with the same results: it reads whole aligned 16-byte blocks, so it may
+ *     read up to 15 bytes before a row's first or after its last element, always inside
+ *     a 16-byte block that holds one of the row's elements (never used, never written).
  *   - Every pointer is aligned to its element type: logits to 2 (bf16) or 4 (fp32)
  *     bytes, int32 and float arrays to 4, the statistics block and double outputs to 8.
  *     A misaligned pointer is SPEC_ERR_INVALID_ARG.

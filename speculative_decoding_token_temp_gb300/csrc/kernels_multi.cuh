@@ -235,10 +235,11 @@ __global__ void __launch_bounds__(kThreads, 2) pair_kernel(const __grid_constant
   pair_merge<K>(p, gi);
 }
 
-// Rows off the 16-byte grid: the same pairwise sums through per-warp bulk-copy rings (as
-// the tile kernel's staged path). Warp w takes the w-th contiguous run of every stage of
-// the K rows, one slot per row (each with its own phase); lane l reads the elements
-// l, l + 32, ... of a run and folds them in as strided groups.
+// Rows off the 16-byte grid: the same pairwise sums through per-warp bulk-copy rings of the
+// aligned blocks covering each run (the K rows may sit at K different offsets). Warp w
+// takes the w-th contiguous run of every stage of the K rows, one slot per row (each with
+// its own phase); lane l reads the elements l, l + 32, ... of a run and folds them in as
+// strided groups.
 template <int K>
 __host__ __device__ constexpr int pair_staged_smem() {
   return kCS * kWarps * K * kWarpSlot;
