@@ -407,7 +407,9 @@ __device__ __forceinline__ float dot_diff(const float (&e)[VEC], const float (&x
 // from the same draft exponentials it keeps the pairwise sums of the matrix.
 template <int K>
 __host__ __device__ constexpr int multi_stages() {
-  return 3;  // two blocks per SM: 3 x 24 KB (K = 3) or 3 x 32 KB (K = 4) each
+  // two blocks per SM: 4 x 24 KB (K = 3; G=64, gamma=8, V=128256: 175.0 against 177.1 us
+  // with 3 stages, same box), 3 x 32 KB (K = 4)
+  return K <= 3 ? 4 : 3;
 }
 
 template <int K>
