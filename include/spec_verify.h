@@ -234,7 +234,8 @@ typedef struct {
    * block_n [B] gets e, the end of the longest run of >= min_block_len consecutive
    * positions where the draft equals the target argmax (the earliest of equally long
    * runs), or 0 when there is none (-1 on a data error); block_tokens [total_draft] gets
-   * the draft tokens before e and the target argmax from e on. */
+   * the draft tokens before e and the target argmax from e on. Either may be NULL when it
+   * has no elements (B = 0, or total_draft = 0). */
   int32_t min_block_len;
   int32_t* block_n;
   int32_t* block_tokens;

@@ -441,8 +441,9 @@ RowPath row_path(spec_dtype dt, int V, const void* a, const void* b) {
 bool temperature_ok(float T) { return isfinite(T) && T > 0.f; }
 
 // Host checks of an options block for a call of the given kind (stochastic, greedy or
-// NKL); fields the call does not use are not looked at.
-spec_status check_options(const spec_options* o, spec_mode mode) {
+// NKL) on batch g; fields the call does not use are not looked at. An output array of
+// no elements (block_n when B = 0, block_tokens when no sequence has a draft) may be NULL.
+spec_status check_options(const spec_options* o, spec_mode mode, const spec_batch& g) {
   if (o == nullptr) return SPEC_OK;
   if (mode == SPEC_MODE_STOCHASTIC && !(o->temperature_draft == 0.f || temperature_ok(o->temperature_draft)))
     return SPEC_ERR_INVALID_ARG;
@@ -451,7 +452,8 @@ spec_status check_options(const spec_options* o, spec_mode mode) {
     return SPEC_ERR_INVALID_ARG;
   if (mode != SPEC_MODE_NKL) {
     if (o->min_block_len < 0) return SPEC_ERR_INVALID_ARG;
-    if (o->min_block_len > 0 && (!o->block_n || !o->block_tokens)) return SPEC_ERR_INVALID_ARG;
+    if (o->min_block_len > 0 && ((g.B > 0 && !o->block_n) || (g.total_draft > 0 && !o->block_tokens)))
+      return SPEC_ERR_INVALID_ARG;
   }
   if (!aligned_to(4, {o->position, o->block_n, o->block_tokens}) || !aligned_to(8, {o->stats}))
     return SPEC_ERR_INVALID_ARG;
@@ -487,7 +489,7 @@ spec_status stochastic_impl(spec_batch g, spec_dtype dtype, const void* target_l
   spec_status st = check_batch(g);
   if (st != SPEC_OK) return st;
   if (!temperature_ok(temperature)) return SPEC_ERR_INVALID_ARG;
-  st = check_options(options, SPEC_MODE_STOCHASTIC);
+  st = check_options(options, SPEC_MODE_STOCHASTIC, g);
   if (st != SPEC_OK) return st;
   if (g.B == 0) return SPEC_OK;
   if (!target_logits || !n_accepted || !out_tokens || !u_sample || !device_status) return SPEC_ERR_INVALID_ARG;
@@ -599,7 +601,7 @@ spec_status greedy_impl(spec_batch g, spec_dtype dtype, const void* target_logit
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
   spec_status st = check_batch(g);
   if (st != SPEC_OK) return st;
-  st = check_options(options, SPEC_MODE_GREEDY);
+  st = check_options(options, SPEC_MODE_GREEDY, g);
   if (st != SPEC_OK) return st;
   if (g.B == 0) return SPEC_OK;
   if (!target_logits || !n_accepted || !out_tokens || !device_status) return SPEC_ERR_INVALID_ARG;
@@ -870,7 +872,7 @@ spec_status spec_nkl_ex(spec_batch g, spec_dtype dtype, const void* target_logit
   spec_status st = check_batch(g);
   if (st != SPEC_OK) return st;
   if (!temperature_ok(temperature)) return SPEC_ERR_INVALID_ARG;
-  st = check_options(options, SPEC_MODE_NKL);
+  st = check_options(options, SPEC_MODE_NKL, g);
   if (st != SPEC_OK) return st;
   if (g.B == 0 || g.total_draft == 0) return SPEC_OK;
   if (!target_logits || !draft_logits || !nkl || !device_status) return SPEC_ERR_INVALID_ARG;

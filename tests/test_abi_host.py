@@ -162,6 +162,22 @@ def test_option_checks_without_launch(lib):
     o = _lib.SpecOptions()
     o.stats = 260                                          # 64-bit counters off their 8-byte grid
     assert greedy(o) == _lib.SPEC_ERR_INVALID_ARG
+    # block-accept outputs of no elements may be NULL: block_tokens when no sequence has a
+    # draft (the options pass; the missing workspace is the next check), both when B = 0
+    o = _lib.SpecOptions()
+    o.min_block_len = 3
+    o.block_n = 256
+    g0 = _g(4, 0, 1000)
+    assert lib.spec_verify_stochastic_ex(g0, _lib.SPEC_BF16, one, None, None, 0.6, None, one, one, one, None, None,
+                                         None, None, None, 0.15, None, None, ctypes.byref(o), one, None, 1 << 30,
+                                         None) == _lib.SPEC_ERR_WORKSPACE
+    assert lib.spec_verify_greedy_ex(g0, _lib.SPEC_BF16, one, None, one, one, ctypes.byref(o), one, None, 1 << 30,
+                                     None) == _lib.SPEC_ERR_WORKSPACE
+    o.block_n = None
+    assert lib.spec_verify_greedy_ex(g0, _lib.SPEC_BF16, one, None, one, one, ctypes.byref(o), one, None, 1 << 30,
+                                     None) == _lib.SPEC_ERR_INVALID_ARG   # B = 4 sequences: block_n needed
+    assert lib.spec_verify_greedy_ex(_g(0, 3, 1000), _lib.SPEC_BF16, one, None, one, one, ctypes.byref(o), one,
+                                     None, 1 << 30, None) == _lib.SPEC_OK
 
 
 def test_option_structs_match_the_header(tmp_path):

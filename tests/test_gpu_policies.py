@@ -134,6 +134,23 @@ def test_block_accept_ragged_and_errors(dev):
     compare_greedy(bad, r, [0, 2], min_block_len=3)
 
 
+@pytest.mark.parametrize("ragged", [False, True])
+def test_block_accept_without_drafts(dev, ragged):
+    """A batch in which no sequence has a draft: block_tokens has no elements (its pointer
+    is NULL), every block_n is 0, and the greedy and stochastic decisions are the bonus
+    tokens alone."""
+    if ragged:
+        w = synth.make_stochastic(5, 777, synth.BF16, 0.8, seed=88, gamma_range=(0, 0))
+    else:
+        w = handmade(6, 0, 4097, synth.F32, seed=88)
+    g = run_greedy(w, dev, options={"min_block_len": 3})
+    assert g["device_status"][0] == 0 and np.all(g["block_n"] == 0)
+    compare_greedy(w, g, range(w.B), min_block_len=3)
+    s = run_stochastic(w, dev, options={"min_block_len": 3})
+    assert s["device_status"][0] == 0 and np.all(s["block_n"] == 0)
+    compare_stochastic(w, s, range(w.B), min_block_len=3)
+
+
 # ---------------------------------------------------------------- acceptance statistics
 
 def test_acceptance_statistics_over_buckets(dev):
