@@ -4,9 +4,13 @@ The library is plain C ABI (include/spec_verify.h) with the CUDA runtime linked
 statically, so the Python layer loads it with ctypes and nothing else."""
 from __future__ import annotations
 
+import hashlib
 import os
+import platform
 import shutil
 import subprocess
+import sys
+import time
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
@@ -35,11 +39,39 @@ def _inputs():
     return files
 
 
+def _nvcc_version() -> str:
+    try:
+        out = subprocess.run([nvcc_path(), "--version"], capture_output=True, text=True, timeout=60).stdout
+    except (OSError, subprocess.SubprocessError):
+        return "unknown"
+    return out.strip().splitlines()[-1] if out.strip() else "unknown"
+
+
+def build_key(lib: str = LIB) -> str:
+    """What a library build depends on: the bytes of every input, the command line, the
+    machine architecture (a library built on another host does not load here) and the
+    compiler's version."""
+    h = hashlib.sha256()
+    for f in _inputs():
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    h.update(" ".join(_command(lib, False)[1:]).encode())
+    h.update(platform.machine().encode())
+    h.update(_nvcc_version().encode())
+    return h.hexdigest()
+
+
+def _stamp(lib: str) -> str:
+    return lib + ".stamp"
+
+
 def up_to_date(lib: str = LIB) -> bool:
-    if not os.path.exists(lib):
+    """The library exists and its stamp records the current build key."""
+    if not os.path.exists(lib) or not os.path.exists(_stamp(lib)):
         return False
-    t = os.path.getmtime(lib)
-    return all(os.path.getmtime(f) <= t for f in _inputs())
+    with open(_stamp(lib)) as f:
+        return f.read().split()[0:1] == [build_key(lib)]
 
 
 def _command(lib: str, ptxas_info: bool) -> list:
@@ -58,6 +90,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, 
     parallel); return the path of the ordinary library."""
     libs = [LIB] + ([LIB_BOUNDS] if bounds else [])
     todo = [lib for lib in libs if force or not up_to_date(lib)]
+    t0 = time.time()
     procs = []
     for lib in todo:
         cmd = _command(lib, ptxas_info)
@@ -73,8 +106,13 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, 
         if verbose or ptxas_info:
             print(out + err)
         os.replace(lib + ".tmp", lib)
+        with open(_stamp(lib), "w") as f:
+            f.write(f"{build_key(lib)} {platform.machine()} sm_103a\n")
     if failed:
         raise RuntimeError("\n".join(failed))
+    names = ", ".join(os.path.basename(x) for x in todo)
+    print(f"[build] {'compiled ' + names + f' for sm_103a on {platform.machine()} in {time.time() - t0:.0f} s' if todo else 'libraries up to date'}",
+          file=sys.stderr)
     return LIB
 
 
