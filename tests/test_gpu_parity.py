@@ -509,6 +509,34 @@ def test_draw_at_cdf_ends(dev, u, V, dtype):
         assert _draw_in_band(w, b, n, y, w.T), (b, n, y)
 
 
+def test_accept_at_u_equal_to_alpha(dev):
+    """Reading R4 on the device: a draft is accepted when u <= alpha, so u set to the call's
+    own alpha at a sequence's first rejected position turns it into an acceptance, and u one
+    float above alpha keeps the rejection. A property of the device's comparison: both runs
+    read the alpha the first call returned, no oracle value."""
+    w = handmade(24, 6, 5000, synth.BF16, T=0.8, seed=62)
+    first = run_stochastic(w, dev)
+    n0 = first["n_accepted"].astype(int)
+    alpha = first["alpha"]
+    rejected = [b for b in range(w.B) if n0[b] < 6 and alpha[6 * b + n0[b]] < 1.0]
+    assert len(rejected) >= 5
+    at = w.u_accept.copy()
+    above = w.u_accept.copy()
+    for b in rejected:
+        a = np.float32(alpha[6 * b + n0[b]])
+        at[6 * b + n0[b]] = a
+        above[6 * b + n0[b]] = np.nextafter(a, np.float32(np.inf), dtype=np.float32)
+    w.u_accept[:] = at
+    eq = run_stochastic(w, dev)
+    w.u_accept[:] = above
+    gt = run_stochastic(w, dev)
+    for b in rejected:
+        i = 6 * b + n0[b]
+        assert eq["alpha"][i] == alpha[i] and gt["alpha"][i] == alpha[i], b
+        assert int(eq["n_accepted"][b]) > n0[b], (b, n0[b], int(eq["n_accepted"][b]))
+        assert int(gt["n_accepted"][b]) == n0[b], (b, n0[b], int(gt["n_accepted"][b]))
+
+
 def test_back_to_back_calls_on_shared_buffers(dev):
     """Calls queued on one stream with no synchronisation between them, all on one
     workspace, each preceded by torch kernels that overwrite the input buffers the previous
