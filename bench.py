@@ -202,7 +202,7 @@ class StochasticCall:
     """Preallocated inputs/outputs for repeated spec_verify_stochastic calls (logits
     shifted by `offset` elements when offset > 0)."""
 
-    def __init__(self, w, dev, host_inputs=False, offset=0):
+    def __init__(self, w, dev, host_inputs=False, offset=0, temperature_draft=None):
         import ctypes
 
         import torch
@@ -234,6 +234,10 @@ class StochasticCall:
         self.dt = _lib.SPEC_BF16 if w.dtype == "bf16" else _lib.SPEC_F32
         self.host = None
         self.P = ctypes.c_void_p
+        self.opts = None
+        if temperature_draft is not None:  # spec_verify_stochastic_ex with the draft's own temperature
+            self.opts = _lib.SpecOptions()
+            self.opts.temperature_draft = float(temperature_draft)
         self.ins = [{"t": self.t, "d": self.d, "tok": self.tok, "ua": self.ua, "us": self.us}]
         if host_inputs:
             pin = lambda t: t.cpu().pin_memory()  # noqa: E731
@@ -259,14 +263,18 @@ class StochasticCall:
         return sum(v.numel() * v.element_size() for v in self.host_out.values())
 
     def __call__(self, stream_handle, k=0):
+        import ctypes
         P = self.P
         x = self.ins[k]
-        code = self.lib.spec_verify_stochastic(
-            self.g, self.dt, P(x["t"].data_ptr()), P(x["d"].data_ptr()), P(x["tok"].data_ptr()), self.w.T,
-            P(x["ua"].data_ptr()), P(x["us"].data_ptr()), P(self.n.data_ptr()), P(self.out.data_ptr()),
-            P(self.px.data_ptr()), P(self.qx.data_ptr()), P(self.al.data_ptr()), P(self.nkl.data_ptr()),
-            P(self.mask.data_ptr()), 0.15, P(self.gn.data_ptr()), P(self.gt.data_ptr()), P(self.status.data_ptr()),
-            P(self.ws.data_ptr()), self.ws.numel(), P(stream_handle))
+        args = (self.g, self.dt, P(x["t"].data_ptr()), P(x["d"].data_ptr()), P(x["tok"].data_ptr()), self.w.T,
+                P(x["ua"].data_ptr()), P(x["us"].data_ptr()), P(self.n.data_ptr()), P(self.out.data_ptr()),
+                P(self.px.data_ptr()), P(self.qx.data_ptr()), P(self.al.data_ptr()), P(self.nkl.data_ptr()),
+                P(self.mask.data_ptr()), 0.15, P(self.gn.data_ptr()), P(self.gt.data_ptr()))
+        tail = (P(self.status.data_ptr()), P(self.ws.data_ptr()), self.ws.numel(), P(stream_handle))
+        if self.opts is None:
+            code = self.lib.spec_verify_stochastic(*args, *tail)
+        else:
+            code = self.lib.spec_verify_stochastic_ex(*args, ctypes.byref(self.opts), *tail)
         if code != 0:
             raise RuntimeError(f"spec_verify_stochastic returned {code}")
 
@@ -475,7 +483,8 @@ def run_ours(args):
     cfg = synth.HEADLINE
     from speculative_decoding_token_temp_gb300 import sharding
     w = cfg.make(seed=sharding.rank_seed(cfg.seed, rank), B=args.batch, V=args.vocab)
-    call = StochasticCall(w, dev, host_inputs=True, offset=args.offset)
+    call = StochasticCall(w, dev, host_inputs=True, offset=args.offset, temperature_draft=args.temperature_draft)
+    secondary = args.offset != 0 or args.temperature_draft is not None
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
     step = lambda: call(sh)  # noqa: E731
@@ -504,7 +513,7 @@ def run_ours(args):
     e2e_val = sum_over_ranks(rows_step * e2e_steps, world, dev) / e2e_el
 
     modes = {}
-    if rank == 0 and not args.no_modes and w.V == cfg.V:
+    if rank == 0 and not args.no_modes and w.V == cfg.V and args.temperature_draft is None:
         # the standalone calls, same inputs (the workload's own vocabulary only)
         res = {}
         g_out = {}
@@ -657,14 +666,16 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"B{w.B}_g8_V{w.V}_bf16: stochastic verify + NKL(delta=0.15) + greedy, one call"
                                + (f" (logits {args.offset} element(s) off the 16-byte grid: phased path)"
-                                  if args.offset else ""),
+                                  if args.offset else "")
+                               + (f" (draft temperature {args.temperature_draft}: both draft scales)"
+                                  if args.temperature_draft is not None else ""),
                    "B": w.B, "gamma": 8, "V": w.V, "T": w.T, "seed": cfg.seed, "rows_per_step": rows_step,
                    "l2": f"inputs {(w.target.nbytes + w.draft.nbytes) / 1e6:.0f} MB per step, larger than the "
                          "129 MB L2; no flush",
                    "parallelism": f"{world} independent shard(s), no collective"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm,
-                     "traffic": profiled_traffic() if w.B == 256 and w.V == cfg.V and args.offset == 0 else None,
+                     "traffic": profiled_traffic() if w.B == 256 and w.V == cfg.V and not secondary else None,
                      "kernel": "spec_verify_stochastic call (prologue_kernel + rows_kernel + sample2_kernel)",
                      "algorithmic_bytes": ab["stochastic"], "peak_source": peak_kind,
                      "peak_datasheet": datasheet_gbs(), "frac_datasheet": achieved / datasheet_gbs(),
@@ -767,6 +778,10 @@ def main():
     ap.add_argument("--vocab", type=int, default=None, metavar="V",
                     help="vocabulary of the timed call (default: the workload's 128256); a secondary line, e.g. "
                          "V=50257, whose rows are not whole 16-byte blocks (the shifted path), for profiling")
+    ap.add_argument("--temperature-draft", type=float, default=None, metavar="T_D",
+                    help="time the call with the drafts at their own temperature T_D (spec_verify_stochastic_ex, "
+                         "NKL outputs kept: the tiles sum the draft row at both scales); a secondary line, for "
+                         "profiling")
     ap.add_argument("--tree", action="store_true",
                     help="time only the tree call (B=32, 12 nodes, V=128256, bf16): back-to-back and with L2 flushed "
                          "before every call; a secondary line for profiling, not the headline metric")
